@@ -1,0 +1,431 @@
+"""Pins for the CPU oracle: checks against facts that do not come from the
+oracle itself (closed forms, invariants, exact-rational brute force, a worked
+example done by hand).  Each check takes no arguments, calls the oracle through
+the `oracle` package, and raises AssertionError on a mismatch; test_oracle_pins
+runs them on the real oracle and test_oracle_mutants on deliberately broken
+copies of it (every planted mistake must trip at least one check).
+"""
+from __future__ import annotations
+
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ------------------------------------------------------------------ helpers
+def _case(rng, *, B=2, N=5, Hk=2, Hv=4, dk=4, dv=4, tree=False, alpha=None, beta=None,
+          unit_k=True, n_slots=None):
+    n_slots = B if n_slots is None else n_slots
+    q = rng.standard_normal((B, N, Hk, dk))
+    k = rng.standard_normal((B, N, Hk, dk))
+    if unit_k:
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, N, Hv, dv))
+    a = rng.uniform(0.3, 1.0, (B, N, Hv)) if alpha is None else np.full((B, N, Hv), alpha)
+    b = rng.uniform(0.0, 1.0, (B, N, Hv)) if beta is None else np.full((B, N, Hv), beta)
+    cache = rng.standard_normal((n_slots, Hv, dk, dv)) * 0.5
+    slot = rng.permutation(n_slots)[:B].astype(np.int32)
+    if tree:
+        parent = np.full((B, N), -1, np.int32)
+        for bb in range(B):
+            for i in range(1, N):
+                parent[bb, i] = rng.integers(0, i)
+    else:
+        parent = None
+    return dict(q=q, k=k, v=v, alpha=a, beta=b, cache=cache, slot=slot, parent=parent, B=B,
+                N=N, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+
+
+_DEFAULT = object()
+
+
+def _run(c, parent=_DEFAULT, cache=None, v=None, precision="f64"):
+    par = c["parent"] if parent is _DEFAULT else parent
+    st, snap, o = oracle.verify(c["q"], c["k"], c["v"] if v is None else v, c["alpha"],
+                                c["beta"], c["cache"] if cache is None else cache, c["slot"], par,
+                                B=c["B"], N=c["N"], Hk=c["Hk"], Hv=c["Hv"], dk=c["dk"],
+                                dv=c["dv"], precision=precision)
+    assert st == oracle.OK, st
+    return snap, o
+
+
+def _src_state(c, snap, b, n, h):
+    par = c["parent"]
+    p = (n - 1) if par is None else par[b, n]
+    return c["cache"][c["slot"][b], h] if p < 0 else snap[b, p, h]
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    scale = max(1.0, float(np.max(np.abs(b))) if b.size else 1.0)
+    err = float(np.max(np.abs(a - b))) if a.size else 0.0
+    assert err <= tol * scale, f"{what}: max abs err {err:.3e} > {tol:.1e} x {scale:.3g}"
+
+
+# --------------------------------------------------------------- the checks
+def check_golden_hand_example():
+    """Worked by hand in exact decimals (tests/golden/hand_d2_tree.json)."""
+    g = json.load(open(os.path.join(GOLDEN, "hand_d2_tree.json")))
+    I, E = g["inputs"], g["expected"]
+    N = len(I["parent"])
+    sh = lambda x: np.array(x, dtype=np.float64).reshape(1, N, 1, 2)  # noqa: E731
+    st, snap, o = oracle.verify(sh(I["q"]), sh(I["k"]), sh(I["v"]),
+                                np.array(I["alpha"]).reshape(1, N, 1),
+                                np.array(I["beta"]).reshape(1, N, 1),
+                                np.array(I["H0"]).reshape(1, 1, 2, 2), np.zeros(1, np.int32),
+                                np.array(I["parent"], np.int32).reshape(1, N), B=1, N=N, Hk=1,
+                                Hv=1, dk=2, dv=2)
+    assert st == oracle.OK
+    _close(snap[0, :, 0], np.array(E["H"]), 1e-14, "hand example H")
+    _close(o[0, :, 0], np.array(E["o"]), 1e-14, "hand example o")
+    st, depth = oracle.tree_depth(np.array(I["parent"], np.int32).reshape(1, N))
+    assert st == oracle.OK and depth[0].tolist() == E["depth"]
+
+
+def check_identity_gate():
+    """beta = 0, alpha = 1: the state never changes and o = S q."""
+    rng = np.random.default_rng(11)
+    for tree in (False, True):
+        c = _case(rng, alpha=1.0, beta=0.0, tree=tree)
+        snap, o = _run(c)
+        G = c["Hv"] // c["Hk"]
+        for b in range(c["B"]):
+            for n in range(c["N"]):
+                for h in range(c["Hv"]):
+                    H0 = c["cache"][c["slot"][b], h]
+                    assert np.array_equal(snap[b, n, h], H0), "state moved with beta=0, alpha=1"
+                    _close(o[b, n, h], H0.T @ c["q"][b, n, h // G], 1e-13, "o = S q")
+
+
+def check_delta_rule_closed_form():
+    """beta = 1 and |k| = 1: after the update S k = v exactly, for any alpha."""
+    rng = np.random.default_rng(12)
+    for tree in (False, True):
+        c = _case(rng, beta=1.0, tree=tree)
+        snap, _ = _run(c)
+        G = c["Hv"] // c["Hk"]
+        for b in range(c["B"]):
+            for n in range(c["N"]):
+                for h in range(c["Hv"]):
+                    Sk = snap[b, n, h].T @ c["k"][b, n, h // G]
+                    _close(Sk, c["v"][b, n, h], 1e-12, "S k = v")
+
+
+def check_zero_decay():
+    """alpha = 0: the old state is forgotten, S_n = beta v k^T, o = beta (k.q) v."""
+    rng = np.random.default_rng(13)
+    c = _case(rng, alpha=0.0)
+    snap, o = _run(c)
+    G = c["Hv"] // c["Hk"]
+    for b in range(c["B"]):
+        for n in range(c["N"]):
+            for h in range(c["Hv"]):
+                kk, qq, vv, be = (c["k"][b, n, h // G], c["q"][b, n, h // G], c["v"][b, n, h],
+                                  c["beta"][b, n, h])
+                _close(snap[b, n, h], be * np.outer(kk, vv), 1e-14, "rank-1 state")
+                _close(o[b, n, h], be * (kk @ qq) * vv, 1e-13, "o for alpha=0")
+
+
+def check_scalar_closed_form():
+    """d_k = d_v = 1: s_n = a_n s_{n-1} + b_n with a = alpha(1 - beta k^2),
+    b = beta v k (a first-order linear recurrence), whose solution is
+    s_N = (prod a) s_0 + sum_m (prod_{j>m} a_j) b_m."""
+    rng = np.random.default_rng(14)
+    c = _case(rng, B=1, N=7, Hk=1, Hv=1, dk=1, dv=1, unit_k=False)
+    snap, o = _run(c)
+    al, be = c["alpha"][0, :, 0], c["beta"][0, :, 0]
+    kk, vv, qq = c["k"][0, :, 0, 0], c["v"][0, :, 0, 0], c["q"][0, :, 0, 0]
+    a = al * (1 - be * kk * kk)
+    bterm = be * vv * kk
+    s0 = c["cache"][c["slot"][0], 0, 0, 0]
+    for n in range(c["N"]):
+        s = np.prod(a[: n + 1]) * s0 + sum(np.prod(a[m + 1: n + 1]) * bterm[m] for m in range(n + 1))
+        _close(snap[0, n, 0, 0, 0], s, 1e-13, f"scalar s_{n}")
+        _close(o[0, n, 0, 0], s * qq[n], 1e-13, f"scalar o_{n}")
+
+
+def check_linearity():
+    """For fixed k, q, alpha, beta the map (S_0, V) -> (S_n, o) is linear."""
+    rng = np.random.default_rng(15)
+    c = _case(rng, tree=True)
+    s_full, o_full = _run(c)
+    s_h0, o_h0 = _run(c, v=np.zeros_like(c["v"]))
+    s_v, o_v = _run(c, cache=np.zeros_like(c["cache"]))
+    _close(s_full, s_h0 + s_v, 1e-13, "superposition (state)")
+    _close(o_full, o_h0 + o_v, 1e-13, "superposition (o)")
+    s_c, o_c = _run(c, cache=2.5 * c["cache"], v=2.5 * c["v"])
+    _close(s_c, 2.5 * s_full, 1e-13, "homogeneity (state)")
+    _close(o_c, 2.5 * o_full, 1e-13, "homogeneity (o)")
+
+
+def check_column_independence():
+    """Permuting the d_v columns of S_0 and of v permutes every output the same way."""
+    rng = np.random.default_rng(16)
+    c = _case(rng, dv=6, tree=True)
+    perm = rng.permutation(c["dv"])
+    s1, o1 = _run(c)
+    s2, o2 = _run(c, cache=c["cache"][..., perm], v=c["v"][..., perm])
+    _close(s2, s1[..., perm], 1e-14, "column permutation (state)")
+    _close(o2, o1[..., perm], 1e-14, "column permutation (o)")
+
+
+def check_contraction():
+    """v = 0, alpha <= 1, 0 <= beta <= 2, |k| = 1: |S_n|_F never grows; at
+    alpha = 1, beta = 2 the step is a Householder reflection and keeps the norm."""
+    rng = np.random.default_rng(17)
+    for alpha, beta, equal in ((None, None, False), (1.0, 2.0, True)):
+        c = _case(rng, tree=True, alpha=alpha, beta=beta)
+        if alpha is None:
+            c["beta"] = rng.uniform(0.0, 2.0, c["beta"].shape)
+        snap, _ = _run(c, v=np.zeros_like(c["v"]))
+        for b in range(c["B"]):
+            for n in range(c["N"]):
+                for h in range(c["Hv"]):
+                    before = np.linalg.norm(_src_state(c, snap, b, n, h))
+                    after = np.linalg.norm(snap[b, n, h])
+                    assert after <= before * (1 + 1e-13), "norm grew"
+                    if equal:
+                        assert abs(after - before) <= 1e-12 * before, "reflection changed norm"
+
+
+def check_tree_matches_chain_and_paths():
+    """A single-path tree is the chain, bit for bit; every tree node equals the
+    chain run over its root-to-node ancestor path; a star tree starts every
+    non-root node from node 0's state."""
+    rng = np.random.default_rng(18)
+    c = _case(rng, N=7)
+    chain_s, chain_o = _run(c, parent=None)
+    line = np.tile(np.arange(-1, c["N"] - 1, dtype=np.int32), (c["B"], 1))
+    tree_s, tree_o = _run(c, parent=line)
+    assert np.array_equal(chain_s, tree_s) and np.array_equal(chain_o, tree_o)
+
+    c = _case(rng, N=8, tree=True)
+    ts, to = _run(c)
+    for b in range(c["B"]):
+        for n in range(c["N"]):
+            path = []
+            m = n
+            while m >= 0:
+                path.append(m)
+                m = c["parent"][b, m]
+            path = path[::-1]
+            sub = {key: c[key][b:b + 1, path] for key in ("q", "k", "v", "alpha", "beta")}
+            st, ss, so = oracle.verify(sub["q"], sub["k"], sub["v"], sub["alpha"], sub["beta"],
+                                       c["cache"], c["slot"][b:b + 1], None, B=1, N=len(path),
+                                       Hk=c["Hk"], Hv=c["Hv"], dk=c["dk"], dv=c["dv"])
+            assert st == oracle.OK
+            assert np.array_equal(ss[0, -1], ts[b, n]), f"tree node {n} != its ancestor chain"
+            assert np.array_equal(so[0, -1], to[b, n])
+
+    c = _case(rng, N=6, tree=True)
+    c["parent"][:, 1:] = 0
+    ss, so = _run(c)
+    for b in range(c["B"]):
+        for i in range(2, c["N"]):
+            sub = {key: c[key][b:b + 1, [0, i]] for key in ("q", "k", "v", "alpha", "beta")}
+            st, s2, o2 = oracle.verify(sub["q"], sub["k"], sub["v"], sub["alpha"], sub["beta"],
+                                       c["cache"], c["slot"][b:b + 1], None, B=1, N=2,
+                                       Hk=c["Hk"], Hv=c["Hv"], dk=c["dk"], dv=c["dv"])
+            assert np.array_equal(s2[0, 1], ss[b, i]) and np.array_equal(o2[0, 1], so[b, i])
+
+
+def _fraction_verify(c, b):
+    """Exact rational arithmetic, the recurrence in its literal matrix form
+    S_n = alpha S_src (I - beta k k^T) + beta v k^T, o_n = S_n q_n, S = H^T.
+    Value head h reads q/k head h // (Hv/Hk).  Returns per-node S and o."""
+    F = Fraction
+    dk, dv, G = c["dk"], c["dv"], c["Hv"] // c["Hk"]
+    out_S, out_o = {}, {}
+    for h in range(c["Hv"]):
+        H0 = c["cache"][c["slot"][b], h]
+        S0 = [[F(float(H0[i][j])) for i in range(dk)] for j in range(dv)]
+        states = []
+        for n in range(c["N"]):
+            p = (n - 1) if c["parent"] is None else int(c["parent"][b, n])
+            S = S0 if p < 0 else states[p]
+            k = [F(float(x)) for x in c["k"][b, n, h // G]]
+            q = [F(float(x)) for x in c["q"][b, n, h // G]]
+            v = [F(float(x)) for x in c["v"][b, n, h]]
+            a, be = F(float(c["alpha"][b, n, h])), F(float(c["beta"][b, n, h]))
+            P = [[(F(1) if i == m else F(0)) - be * k[i] * k[m] for m in range(dk)]
+                 for i in range(dk)]
+            SP = [[sum(S[j][i] * P[i][m] for i in range(dk)) for m in range(dk)]
+                  for j in range(dv)]
+            Sn = [[a * SP[j][m] + be * v[j] * k[m] for m in range(dk)] for j in range(dv)]
+            states.append(Sn)
+            out_S[(n, h)] = Sn
+            out_o[(n, h)] = [sum(Sn[j][m] * q[m] for m in range(dk)) for j in range(dv)]
+    return out_S, out_o
+
+
+def check_exact_rational_bruteforce():
+    """Tiny cases in exact rationals vs the float64 and long-double oracle."""
+    rng = np.random.default_rng(19)
+    for dk, dv, tree in ((2, 2, False), (3, 2, True), (2, 3, True)):
+        c = _case(rng, B=2, N=4, Hk=2, Hv=4, dk=dk, dv=dv, tree=tree, n_slots=3)
+        snap, o = _run(c)
+        snap_ld, o_ld = _run(c, precision="ld")
+        for b in range(c["B"]):
+            S_ex, o_ex = _fraction_verify(c, b)
+            for (n, h), S in S_ex.items():
+                H = np.array([[float(S[j][i]) for j in range(dv)] for i in range(dk)])
+                _close(snap[b, n, h], H, 1e-13, f"exact state b{b} n{n} h{h}")
+                _close(o[b, n, h], np.array([float(x) for x in o_ex[(n, h)]]), 1e-13,
+                       f"exact o b{b} n{n} h{h}")
+        _close(snap_ld, snap, 1e-14, "long double vs double")
+        _close(o_ld, o, 1e-14, "long double vs double (o)")
+
+
+def check_tree_depth_and_validation():
+    rng = np.random.default_rng(20)
+    N = 12
+    parent = np.full((3, N), -1, np.int32)
+    for b in range(3):
+        for i in range(1, N):
+            parent[b, i] = rng.integers(0, i)
+    st, depth = oracle.tree_depth(parent)
+    assert st == oracle.OK
+    for b in range(3):
+        for i in range(N):
+            d, m = 0, i
+            while m >= 0:
+                d, m = d + 1, parent[b, m]
+            assert depth[b, i] == d
+    for bad in ([0, 0, 1], [-1, 1, 0], [-1, 0, 3], [-1, -1, 0]):
+        st, _ = oracle.tree_depth(np.array([bad], np.int32))
+        assert st == oracle.ERR_BAD_TREE, bad
+    # a bad tree skips its sequence and reports the error; the good one still runs
+    c = _case(rng, B=2, N=4, tree=True)
+    c["parent"][1] = [-1, 0, 2, 1]
+    st, snap, o = oracle.verify(c["q"], c["k"], c["v"], c["alpha"], c["beta"], c["cache"],
+                                c["slot"], c["parent"], B=2, N=4, Hk=c["Hk"], Hv=c["Hv"],
+                                dk=c["dk"], dv=c["dv"])
+    assert st == oracle.ERR_BAD_TREE
+    assert not np.any(snap[1]) and np.any(snap[0])
+
+
+def check_commit():
+    """Commit copies snap[layer][b][accept[b]] into cache[layer][slot[b]] and
+    nothing else; bad accept / slot values are reported and skipped."""
+    rng = np.random.default_rng(21)
+    L, B, N, Hv, dk, dv, n_slots = 3, 2, 5, 2, 3, 4, 4
+    snap = rng.standard_normal((L, B, N, Hv, dk, dv))
+    cache = rng.standard_normal((L, n_slots, Hv, dk, dv))
+    before = cache.copy()
+    acc = np.array([4, 1], np.int32)
+    slot = np.array([3, 0], np.int32)
+    st = oracle.commit(snap, acc, cache, slot, B=B, N=N, Hv=Hv, dk=dk, dv=dv, n_layers=L,
+                       snap_layer_stride=B * N * Hv * dk * dv,
+                       cache_layer_stride=n_slots * Hv * dk * dv, n_slots=n_slots)
+    assert st == oracle.OK
+    for l in range(L):
+        for s in range(n_slots):
+            if s in slot:
+                b = int(np.nonzero(slot == s)[0][0])
+                assert np.array_equal(cache[l, s], snap[l, b, acc[b]])
+            else:
+                assert np.array_equal(cache[l, s], before[l, s])
+    for bad_acc, bad_slot, err in (([5, 1], [3, 0], oracle.ERR_ACCEPT_RANGE),
+                                   ([-1, 1], [3, 0], oracle.ERR_ACCEPT_RANGE),
+                                   ([0, 1], [4, 0], oracle.ERR_SLOT_RANGE)):
+        cache2 = before.copy()
+        st = oracle.commit(snap, np.array(bad_acc, np.int32), cache2,
+                           np.array(bad_slot, np.int32), B=B, N=N, Hv=Hv, dk=dk, dv=dv,
+                           n_layers=L, snap_layer_stride=B * N * Hv * dk * dv,
+                           cache_layer_stride=n_slots * Hv * dk * dv, n_slots=n_slots)
+        assert st == err
+        # the good sequence (b = 1) is still committed
+        assert np.array_equal(cache2[0, 0], snap[0, 1, 1])
+
+
+def chunked_reference(q, k, v, alpha, beta, state, chunk):
+    """Chunked (WY / UT-transform) evaluation of the same recurrence, float64,
+    one value head: q, k [T][dk], v [T][dv], alpha, beta [T], state H [dk][dv].
+
+    Inside a chunk with cumulative decay g_t = prod_{s<=t} alpha_s and
+    delta_t = beta_t (v_t - alpha_t H_{t-1}^T k_t), the rows of Delta solve
+    (I + A) Delta = diag(beta) (V - diag(g) K H) with
+    A[t][s] = beta_t (g_t / g_s) (k_t . k_s) for s < t; then
+    O = diag(g) Q H + (causal(g_t / g_s) * Q K^T) Delta and
+    H <- g_C H + K^T diag(g_C / g) Delta."""
+    T = q.shape[0]
+    H = state.copy()
+    O = np.zeros((T, v.shape[1]))
+    for t0 in range(0, T, chunk):
+        sl = slice(t0, min(T, t0 + chunk))
+        Q, K, V, a, b = q[sl], k[sl], v[sl], alpha[sl], beta[sl]
+        C = Q.shape[0]
+        g = np.cumprod(a)
+        ratio = g[:, None] / g[None, :]
+        A = np.tril(b[:, None] * ratio * (K @ K.T), -1)
+        X = b[:, None] * (V - g[:, None] * (K @ H))
+        Delta = np.linalg.solve(np.eye(C) + A, X)
+        O[sl] = g[:, None] * (Q @ H) + (np.tril(ratio) * (Q @ K.T)) @ Delta
+        H = g[-1] * H + K.T @ ((g[-1] / g)[:, None] * Delta)
+    return H, O
+
+
+def check_chunked_equals_step():
+    """The chunked form (C = 1, 4, 64) reaches the step recurrence's result."""
+    rng = np.random.default_rng(22)
+    Hk, Hv, dk, dv = 1, 2, 8, 6
+    for T in (1, 63, 64, 65, 200):
+        q = rng.standard_normal((T, Hk, dk))
+        k = rng.standard_normal((T, Hk, dk))
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+        v = rng.standard_normal((T, Hv, dv))
+        al = rng.uniform(0.85, 1.0, (T, Hv))
+        be = rng.uniform(0.0, 1.0, (T, Hv))
+        s0 = rng.standard_normal((Hv, dk, dv)) * 0.1
+        st, sT, o = oracle.prefill_step(q, k, v, al, be, s0, T=T, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+        assert st == oracle.OK
+        for C in (1, 4, 64):
+            for h in range(Hv):
+                Hc, Oc = chunked_reference(q[:, 0], k[:, 0], v[:, h], al[:, h], be[:, h], s0[h], C)
+                _close(Hc, sT[h], 1e-10, f"chunked state T={T} C={C}")
+                _close(Oc, o[:, h], 1e-10, f"chunked o T={T} C={C}")
+
+
+def check_rounds_equal_sequential():
+    """verify -> commit(accepted) -> verify the next block from the cache, for
+    several rounds, equals one token-by-token run over the accepted tokens
+    (speculation is lossless; the replayed prefix equals the persisted state)."""
+    rng = np.random.default_rng(23)
+    Hk, Hv, dk, dv, N = 2, 4, 4, 3, 5
+    cache = rng.standard_normal((2, Hv, dk, dv)) * 0.3
+    slot = np.array([1], np.int32)
+    start = cache[1].copy()
+    acc_q, acc_k, acc_v, acc_a, acc_b = [], [], [], [], []
+    for _ in range(4):
+        c = _case(rng, B=1, N=N, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+        st, snap, o = oracle.verify(c["q"], c["k"], c["v"], c["alpha"], c["beta"], cache, slot,
+                                    None, B=1, N=N, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+        assert st == oracle.OK
+        L = int(rng.integers(1, N + 1))
+        st = oracle.commit(snap, np.array([L - 1], np.int32), cache, slot, B=1, N=N, Hv=Hv,
+                           dk=dk, dv=dv, n_slots=2)
+        assert st == oracle.OK
+        for lst, key in ((acc_q, "q"), (acc_k, "k"), (acc_v, "v"), (acc_a, "alpha"),
+                         (acc_b, "beta")):
+            lst.append(c[key][0, :L])
+    cat = [np.concatenate(x) for x in (acc_q, acc_k, acc_v, acc_a, acc_b)]
+    T = cat[0].shape[0]
+    st, sT, _ = oracle.prefill_step(*cat, start, T=T, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+    assert st == oracle.OK
+    _close(cache[1], sT, 1e-13, "rounds of verify+commit vs sequential")
+
+
+ALL_CHECKS = [
+    check_golden_hand_example, check_identity_gate, check_delta_rule_closed_form,
+    check_zero_decay, check_scalar_closed_form, check_linearity, check_column_independence,
+    check_contraction, check_tree_matches_chain_and_paths, check_exact_rational_bruteforce,
+    check_tree_depth_and_validation, check_commit, check_chunked_equals_step,
+    check_rounds_equal_sequential,
+]
