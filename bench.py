@@ -1,0 +1,698 @@
+"""Benchmark of the GDN verification hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the hot path over one batch of synthetic input:
+
+  chain16      (default) one GDN layer, 1 sequence, a 16-position chain,
+               16 q/k heads / 48 value heads, d_k = d_v = 128, bf16 q/k/v,
+               fp32 state: gdn_verify_chain + gdn_commit_accepted
+  tree22       the same heads over a 22-node draft tree: gdn_verify_tree + commit
+  batched8x16  8 sequences x 16-position chains over 48 layers:
+               48 x gdn_verify_chain + one gdn_commit_accepted over the 48 layers
+  prefill8192  one 8192-token sequence, chunk 64: gdn_prefill_chunked
+
+Metric: node-heads/s (B x N x Hv per layer call, summed over the step; for the
+prefill, token-heads/s).  L2 (129 MB) is flushed by a 256 MiB write before
+every step and the flush is not timed: each step's kernels are bracketed by
+CUDA events on the launch stream, and the dominant kernel (the verify / the
+prefill) by its own pair, which gives the roofline figure.  Prints ONE JSON
+line on rank 0.  Under torchrun every rank runs its own replica (independent
+sequences, no collective on the data path): weak scaling.
+
+--impl reference times the CPU oracle (plain float64 C++, the reference for
+every parity test) on this host's cores, on a bounded sample of the same
+workload each step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+HEADS = synthetic.HEADS
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+METRIC = "GDN verify node-heads/s per layer at block 16 / tree 22; % of GB300 HBM roofline"
+
+
+# ------------------------------------------------------------------ workloads
+def verify_bytes(B, N, Hk, Hv, dk, dv, in_bytes=2, tree=False):
+    """Algorithmic HBM bytes of one verify call: every input read once, the
+    initial state read once, every output (o and all N snapshots) written once."""
+    state_in = B * Hv * dk * dv * 4
+    snap = B * N * Hv * dk * dv * 4
+    qk = 2 * B * N * Hk * dk * in_bytes
+    v = B * N * Hv * dv * in_bytes
+    gates = 2 * B * N * Hv * 4
+    o = B * N * Hv * dv * 4
+    extra = (B * N * 4 * 2) if tree else 0   # parent in, depth out
+    return state_in + snap + qk + v + gates + o + extra
+
+
+def commit_bytes(B, Hv, dk, dv, n_layers=1):
+    return 2 * B * Hv * dk * dv * 4 * n_layers
+
+
+def prefill_bytes(T, Hk, Hv, dk, dv, in_bytes=2):
+    return (2 * T * Hk * dk * in_bytes + T * Hv * dv * in_bytes + 2 * T * Hv * 4 +
+            T * Hv * dv * 4 + 2 * Hv * dk * dv * 4)
+
+
+def prefill_flops(T, Hk, Hv, dk, dv, C=64):
+    """Algorithmic flops of the chunked form per value head and chunk: Q K^T,
+    K K^T, the two C x C x d products (W or U and the masked P Delta) ... as
+    2 C^2 d each five times, plus the three C d^2 products with the state."""
+    n_chunks = -(-T // C)
+    return n_chunks * Hv * (5 * 2 * C * C * dk + 3 * 2 * C * dk * dv)
+
+
+WORKLOADS = {
+    "chain16": dict(B=1, N=16, tree=False, layers=1,
+                    desc="1 sequence x 16-position chain (last committed token + 15 drafts), "
+                         "16 q/k heads, 48 value heads, d_k=d_v=128, bf16 q/k/v, fp32 gates "
+                         "and state; verify + commit of a seeded accept length"),
+    "tree22": dict(B=1, N=22, tree=True, layers=1,
+                   desc="1 sequence x 22-node DDTree (parent uniform over earlier nodes, depth "
+                        "<= 16), same heads; verify + commit of a seeded node"),
+    "batched8x16": dict(B=8, N=16, tree=False, layers=48,
+                        desc="8 sequences x 16-position chains, same heads, 48 GDN layers with "
+                             "fresh inputs per layer; 48 verifies + one 48-layer commit"),
+    "prefill8192": dict(T=8192, layers=1,
+                        desc="1 sequence of 8192 tokens, 16 q/k heads, 48 value heads, "
+                             "d_k=d_v=128, bf16 q/k/v, chunk 64, WY/UT form on tensor cores"),
+}
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background; each line is stamped
+    on arrival so the samples inside the timed region can be picked out."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if self.gpu_id is not None:
+                cmd += ["-i", str(self.gpu_id)]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [s for ts, s in self.samples if t0 <= ts <= t1]
+        if not inside and self.samples:   # nearest sample to the window
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda x: abs(x[0] - mid))[1]]
+        sm, mx, reasons = [], [], set()
+        for s in inside:
+            try:
+                sm.append(float(s[0]))
+                mx.append(float(s[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(self.NAMES, s[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ---------------------------------------------------------------- roofline
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "verify": ["hybrid_gated_deltanet_delta_gb300/csrc/gdn_verify.cu",
+               "hybrid_gated_deltanet_delta_gb300/csrc/gdn_common.cuh"],
+    "prefill": ["hybrid_gated_deltanet_delta_gb300/csrc/gdn_prefill.cu",
+                "hybrid_gated_deltanet_delta_gb300/csrc/gdn_common.cuh"],
+}
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch recorded by an ncu capture in profiles/, if the
+    kernel's sources are unchanged since (source hash in the summary)."""
+    sha = source_sha(KERNEL_SOURCES[kernel])
+    pat = re.compile(r"bench-traffic: kernel=(\S+) workload=(\S+) source_sha=(\S+) "
+                     r"dram_bytes_per_launch=(\d+)")
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        for m in pat.finditer(open(os.path.join(pdir, name)).read()):
+            if m.group(1) == kernel and m.group(2) == workload and m.group(3) == sha:
+                return int(m.group(4))
+    return None
+
+
+# ------------------------------------------------------------------ oracle leg
+def oracle_step_sample(wl_name, heads_per_step):
+    """The oracle (CPU, float64) on `heads_per_step` value heads of the
+    workload's first sequence (one layer), plus the commit of that head:
+    returns (seconds, node-heads done)."""
+    import oracle
+
+    if wl_name == "prefill8192":
+        inp = synthetic.prefill8192()
+        t0 = time.perf_counter()
+        st, _, _ = oracle.prefill_step(inp["q_f64"], inp["k_f64"], inp["v_f64"], inp["alpha"],
+                                       inp["beta"], inp["state"], T=inp["T"], Hk=16, Hv=48,
+                                       dk=128, dv=128, heads=(0, heads_per_step))
+        assert st == oracle.OK
+        return time.perf_counter() - t0, inp["T"] * heads_per_step
+    raise NotImplementedError
+
+
+class OracleSampler:
+    """Bounded samples of a verify workload for the oracle: value heads
+    h0..h0+G-1 of one q/k head group of sequence 0 (contiguous arrays)."""
+
+    def __init__(self, wl_name):
+        self.wl = wl_name
+        if wl_name == "chain16":
+            inp = synthetic.chain16()
+        elif wl_name == "tree22":
+            inp = synthetic.tree22()
+        elif wl_name == "batched8x16":
+            inp = synthetic.batched8x16_layer(0)
+        else:
+            inp = None
+        self.inp = inp
+
+    def run(self, n_heads=1):
+        """Verify + commit for n_heads value heads of sequence 0; returns node-heads."""
+        import oracle
+
+        inp = self.inp
+        b = 0
+        N = inp["N"]
+        h_sel = np.arange(n_heads) % inp["Hv"]
+        G = inp["Hv"] // inp["Hk"]
+        hk_sel = h_sel // G
+        q = inp["q_f64"][b:b + 1][:, :, hk_sel]
+        k = inp["k_f64"][b:b + 1][:, :, hk_sel]
+        v = inp["v_f64"][b:b + 1][:, :, h_sel]
+        al = inp["alpha"][b:b + 1][:, :, h_sel]
+        be = inp["beta"][b:b + 1][:, :, h_sel]
+        cache = inp["cache"][inp["slot"][b]][h_sel][None]
+        parent = inp["parent"][b:b + 1] if inp["tree"] else None
+        st, snap, _ = oracle.verify(q, k, v, al, be, cache, np.zeros(1, np.int32), parent, B=1,
+                                    N=N, Hk=n_heads, Hv=n_heads, dk=inp["dk"], dv=inp["dv"])
+        assert st == oracle.OK
+        dst = np.zeros((1, n_heads, inp["dk"], inp["dv"]))
+        st = oracle.commit(snap, inp["accept"][b:b + 1], dst, None, B=1, N=N, Hv=n_heads,
+                           dk=inp["dk"], dv=inp["dv"])
+        assert st == oracle.OK
+        return N * n_heads
+
+
+def cpu_baseline(wl_name, budget_s=10.0):
+    """The oracle as it stands, single-threaded, repeated on samples of the
+    workload until about budget_s seconds of CPU work are done."""
+    if wl_name == "prefill8192":
+        done, spent, reps = 0, 0.0, 0
+        while spent < budget_s or reps == 0:
+            dt, n = oracle_step_sample(wl_name, 1)
+            spent += dt
+            done += n
+            reps += 1
+        return {"value": done / spent, "unit": "token-heads/s", "cores": 1, "kind": "oracle",
+                "sample": f"{reps} x (8192 tokens x 1 value head, step form, float64)"}
+    smp = OracleSampler(wl_name)
+    heads = 3
+    done, reps = 0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s or reps == 0:
+        done += smp.run(heads)
+        reps += 1
+    spent = time.perf_counter() - t0
+    return {"value": done / spent, "unit": "node-heads/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} x (verify + commit of {heads} value heads x {smp.inp['N']} "
+                      f"nodes of sequence 0, float64)"}
+
+
+# ----------------------------------------------------------------- ours: GPU
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _dev(a, torch):
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+class VerifyCase:
+    """Device buffers for one verify layer (inputs, cache, outputs)."""
+
+    def __init__(self, inp, torch, pinned=False):
+        self.inp = inp
+        self.B, self.N, self.Hv = inp["B"], inp["N"], inp["Hv"]
+        dk, dv = inp["dk"], inp["dv"]
+        self.names = ("q", "k", "v", "alpha", "beta", "accept")
+        self.dev = {n: _dev(inp[n], torch) for n in self.names}
+        self.cache = _dev(inp["cache"], torch)
+        self.slot = _dev(inp["slot"], torch)
+        self.parent = _dev(inp["parent"], torch) if inp["tree"] else None
+        self.snap = torch.empty((self.B, self.N, self.Hv, dk, dv), device="cuda")
+        self.o = torch.empty((self.B, self.N, self.Hv, dv), device="cuda")
+        self.host = None
+        if pinned:
+            self.host = {n: self.dev[n].cpu().pin_memory() for n in self.names}
+            self.o_host = torch.empty(self.o.shape, dtype=torch.float32).pin_memory()
+
+    def verify(self, gdn):
+        d = self.dev
+        args = (d["q"], d["k"], d["v"], d["alpha"], d["beta"], self.cache, self.snap, self.o)
+        if self.parent is not None:
+            gdn.gdn_verify_tree(*args, self.parent, slot=self.slot, n_slots=self.inp["n_slots"])
+        else:
+            gdn.gdn_verify_chain(*args, slot=self.slot, n_slots=self.inp["n_slots"])
+
+    def h2d(self):
+        for n in self.names:
+            self.dev[n].copy_(self.host[n], non_blocking=True)
+        return sum(self.host[n].numel() * self.host[n].element_size() for n in self.names)
+
+    def d2h(self):
+        self.o_host.copy_(self.o, non_blocking=True)
+        return self.o.numel() * 4
+
+
+def run_ours(args, wl_name, world, rank, local):
+    import torch
+
+    import hybrid_gated_deltanet_delta_gb300 as gdn
+
+    torch.cuda.set_device(local)
+    gdn.load()
+    wl = WORKLOADS[wl_name]
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    if wl_name == "prefill8192":
+        return run_prefill(args, gdn, torch, flush, world, rank, local)
+
+    Hk, Hv, dk, dv = HEADS["Hk"], HEADS["Hv"], HEADS["dk"], HEADS["dv"]
+    B, N, L = wl["B"], wl["N"], wl["layers"]
+    if wl_name == "batched8x16":
+        layers = []
+        for l in range(L):
+            inp = synthetic.batched8x16_layer(l)
+            if rank:
+                inp = dict(inp)  # replicas share shapes; the data is the same recipe
+            layers.append(VerifyCase(inp, torch, pinned=True))
+        # one cache for all layers: [layer][slot][Hv][dk][dv]; snapshots likewise
+        cache_all = torch.stack([c.cache for c in layers])
+        snap_all = torch.empty((L, B, N, Hv, dk, dv), device="cuda")
+        for l, c in enumerate(layers):
+            c.cache = cache_all[l]
+            c.snap = snap_all[l]
+        commit_layers = L
+    else:
+        inp = synthetic.chain16() if wl_name == "chain16" else synthetic.tree22()
+        layers = [VerifyCase(inp, torch, pinned=True)]
+        cache_all = layers[0].cache
+        snap_all = layers[0].snap
+        commit_layers = 1
+    accept = layers[0].dev["accept"]
+    slot = layers[0].slot
+
+    def commit():
+        gdn.gdn_commit_accepted(snap_all, accept, cache_all, B=B, N=N, Hv=Hv, dk=dk, dv=dv,
+                                n_layers=commit_layers, snap_layer_stride=B * N * Hv * dk * dv,
+                                cache_layer_stride=B * Hv * dk * dv, slot=slot, n_slots=B)
+
+    cache_init = cache_all.clone()
+
+    def step(ev=None):
+        """verify every layer, then commit; ev = (start, after_verify, end) events."""
+        if ev is not None:
+            ev[0].record(stream)
+        for c in layers:
+            c.verify(gdn)
+        if ev is not None:
+            ev[1].record(stream)
+        commit()
+        if ev is not None:
+            ev[2].record(stream)
+
+    launches_per_step = len(layers) + 1
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+
+    gpu_id = gpu_uuid(torch, local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.25)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    verify_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    total_ms = sum(step_ms)
+    total_ms = max_over_ranks(total_ms, world)
+
+    # end to end through the public API: host inputs -> device -> verify/commit -> host o
+    cache_all.copy_(cache_init)
+    e2e_steps = min(args.steps, 200)
+    e2e_s = 0.0
+    h2d = d2h = 0
+    for i in range(e2e_steps + 3):
+        flush.fill_(float(i))
+        torch.cuda.synchronize()
+        ta = time.perf_counter()
+        h2d = sum(c.h2d() for c in layers)
+        step()
+        d2h = sum(c.d2h() for c in layers)
+        torch.cuda.synchronize()
+        if i >= 3:
+            e2e_s += time.perf_counter() - ta
+    e2e_s = max_over_ranks(e2e_s, world)
+
+    node_heads = B * N * Hv * len(layers)
+    value = world * node_heads * args.steps / (total_ms / 1e3)
+    hbm, bf16, peak_kind = measured_peaks()
+    vbytes = verify_bytes(B, N, Hk, Hv, dk, dv, tree=wl.get("tree", False))
+    launch_ms = statistics.mean(verify_ms) / len(layers)
+    achieved = vbytes / (launch_ms / 1e3) / 1e9
+    clocks = sampler.summary(t0, t1)
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC,
+        "value": value,
+        "unit": "node-heads/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{wl_name}: {wl['desc']}",
+            "B": B, "N": N, "Hk": Hk, "Hv": Hv, "dk": dk, "dv": dv, "layers": len(layers),
+            "inputs": "bf16 q/k/v (L2-normalised q/k), fp32 alpha/beta/state/outputs",
+            "node_heads_per_step": node_heads,
+            "l2": "flushed by a 256 MiB write before every step; flush not timed",
+            "timing": "CUDA events around each step's kernels on the launch stream",
+            "parallelism": f"replicas x{world}, no collective",
+            "verify_ms_p50": statistics.median(verify_ms) / len(layers),
+            "step_ms_p10": float(np.percentile(step_ms, 10)),
+            "step_ms_p90": float(np.percentile(step_ms, 90)),
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "gdn_verify_tree" if wl.get("tree") else "gdn_verify_chain",
+            "achieved": achieved,
+            "peak": hbm,
+            "unit": "GB/s",
+            "frac": achieved / hbm,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
+            "measured" else "fallback 6.8 TB/s",
+            "algorithmic_bytes_per_launch": vbytes,
+            "traffic": profiled_traffic("verify", wl_name),
+        },
+        "e2e": {
+            "value": world * node_heads * e2e_steps / e2e_s,
+            "unit": "node-heads/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+
+
+def run_prefill(args, gdn, torch, flush, world, rank, local):
+    inp = synthetic.prefill8192()
+    T, Hk, Hv, dk, dv = inp["T"], inp["Hk"], inp["Hv"], inp["dk"], inp["dv"]
+    q, k, v = (_dev(inp[n], torch) for n in ("q", "k", "v"))
+    alpha, beta = _dev(inp["alpha"], torch), _dev(inp["beta"], torch)
+    state0 = _dev(inp["state"], torch)
+    state = state0.clone()
+    o = torch.empty((T, Hv, dv), device="cuda")
+    wbytes = gdn.gdn_prefill_workspace_bytes(T, Hk, Hv, dk, dv, 64)
+    ws = torch.empty(max(wbytes, 16), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        state.copy_(state0)
+        if ev is not None:
+            ev[0].record(stream)
+        gdn.gdn_prefill_chunked(q, k, v, alpha, beta, state, o, ws)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid(torch, local))
+    sampler.start()
+    time.sleep(0.25)
+    steps = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(steps):
+        flush.fill_(float(i))
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    ms = [e[0].elapsed_time(e[1]) for e in evs]
+    total_ms = max_over_ranks(sum(ms), world)
+    # end to end: host inputs (pinned) -> device -> prefill -> host o and state
+    hq, hk, hv, ha, hb = (x.cpu().pin_memory() for x in (q, k, v, alpha, beta))
+    hs0 = state0.cpu().pin_memory()
+    ho = torch.empty(o.shape).pin_memory()
+    hst = torch.empty(state.shape).pin_memory()
+    e2e_steps = min(steps, 20)
+    e2e_s = 0.0
+    for i in range(e2e_steps + 2):
+        flush.fill_(float(i))
+        torch.cuda.synchronize()
+        ta = time.perf_counter()
+        for d, h in ((q, hq), (k, hk), (v, hv), (alpha, ha), (beta, hb), (state, hs0)):
+            d.copy_(h, non_blocking=True)
+        gdn.gdn_prefill_chunked(q, k, v, alpha, beta, state, o, ws)
+        ho.copy_(o, non_blocking=True)
+        hst.copy_(state, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= 2:
+            e2e_s += time.perf_counter() - ta
+    e2e_s = max_over_ranks(e2e_s, world)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, ha, hb, hs0))
+    d2h = ho.numel() * 4 + hst.numel() * 4
+    hbm, bf16, kind = measured_peaks()
+    pbytes = prefill_bytes(T, Hk, Hv, dk, dv)
+    launch_ms = statistics.mean(ms)
+    achieved = pbytes / (launch_ms / 1e3) / 1e9
+    flops = prefill_flops(T, Hk, Hv, dk, dv)
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC,
+        "value": world * T * Hv * steps / (total_ms / 1e3),
+        "unit": "token-heads/s",
+        "n_gpus": world, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"prefill8192: {WORKLOADS['prefill8192']['desc']}",
+                   "T": T, "Hk": Hk, "Hv": Hv, "dk": dk, "dv": dv, "chunk": 64,
+                   "l2": "flushed by a 256 MiB write before every step; flush not timed",
+                   "timing": "CUDA events around each prefill call on the launch stream",
+                   "achieved_tflops": flops / (launch_ms / 1e3) / 1e12,
+                   "tensor_frac_of_measured_bf16": flops / (launch_ms / 1e3) / 1e12 / bf16},
+        "roofline": {"bound": "hbm", "kernel": "gdn_prefill_chunked", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_source": kind, "algorithmic_bytes_per_launch": pbytes,
+                     "traffic": profiled_traffic("prefill", "prefill8192")},
+        "e2e": {"value": world * T * Hv * e2e_steps / e2e_s, "unit": "token-heads/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": None,
+        "clocks": sampler.summary(t0, t1),
+    }
+
+
+def gpu_uuid(torch, local):
+    try:
+        u = torch.cuda.get_device_properties(local).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:  # noqa: BLE001
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[local]
+        return local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# -------------------------------------------------------------- reference arm
+def run_reference(args, wl_name, world, rank):
+    if rank != 0:
+        return None
+    if wl_name == "prefill8192":
+        for _ in range(args.warmup):
+            oracle_step_sample(wl_name, 1)
+        spent, done = 0.0, 0
+        for _ in range(args.steps):
+            dt, n = oracle_step_sample(wl_name, 1)
+            spent += dt
+            done += n
+        unit, sample = "token-heads/s", "8192 tokens x 1 value head per step (step form)"
+    else:
+        smp = OracleSampler(wl_name)
+        for _ in range(args.warmup):
+            smp.run(1)
+        done = 0
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            done += smp.run(1)
+        spent = time.perf_counter() - t0
+        unit = "node-heads/s"
+        sample = f"verify + commit of 1 value head x {smp.inp['N']} nodes per step"
+    value = done / spent
+    wl = WORKLOADS[wl_name]
+    return {
+        "metric": METRIC, "value": value, "unit": unit, "impl": "reference",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * spent / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl_name}: {wl['desc']}"},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="chain16", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing (for quick runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        out = run_reference(args, args.workload, world, rank)
+    else:
+        out = run_ours(args, args.workload, world, rank, local)
+        if out is not None:
+            out["cpu_baseline"] = (None if args.no_cpu_baseline or world > 1 else
+                                   cpu_baseline(args.workload))
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+"""GB300 gated delta-rule verification library: Python binding.
+
+A thin ctypes layer over libgdn.so (C ABI in include/gdn.h).  It only
+marshals arguments: torch tensors in, raw device pointers and sizes out, the
+current torch CUDA stream as the launch stream.  Every step of the path runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback, and the
+functions raise if the library is missing or a call fails.
+
+Entry points (same names as the C ABI):
+  gdn_verify_chain, gdn_verify_tree, gdn_commit_accepted,
+  gdn_prefill_chunked, gdn_prefill_workspace_bytes
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libgdn.so")
+
+GDN_OK = 0
+GDN_ERR_INVALID_ARG = -1
+GDN_ERR_UNSUPPORTED = -2
+GDN_ERR_MISALIGNED = -3
+GDN_ERR_CUDA = -4
+GDN_ERR_BAD_TREE = -5
+GDN_ERR_ACCEPT_RANGE = -6
+GDN_ERR_SLOT_RANGE = -7
+GDN_ERR_WORKSPACE = -8
+
+GDN_F32 = 0
+GDN_BF16 = 1
+
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+class VerifyArgs(ctypes.Structure):
+    """Mirror of gdn_verify_args."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("alpha", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+        ("state_cache", ctypes.c_void_p), ("slot", ctypes.c_void_p),
+        ("snapshots", ctypes.c_void_p), ("o", ctypes.c_void_p), ("status", ctypes.c_void_p),
+        ("cache_slot_stride", ctypes.c_int64), ("n_slots", ctypes.c_int32),
+        ("B", ctypes.c_int32), ("N", ctypes.c_int32), ("Hk", ctypes.c_int32),
+        ("Hv", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
+        ("in_dtype", ctypes.c_int32), ("tile_cols", ctypes.c_int32),
+        ("row_warps", ctypes.c_int32),
+    ]
+
+
+def load(path: str | None = None):
+    """Load libgdn.so (built by __graft_entry__.build()); raise if it is absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libgdn.so not found at {p}: build it first "
+                           "(python -m hybrid_gated_deltanet_delta_gb300.build)")
+    lib = ctypes.CDLL(p)
+    P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.gdn_verify_chain.argtypes = [ctypes.POINTER(VerifyArgs), P]
+    lib.gdn_verify_chain.restype = ctypes.c_int
+    lib.gdn_verify_tree.argtypes = [ctypes.POINTER(VerifyArgs), P, P, P]
+    lib.gdn_verify_tree.restype = ctypes.c_int
+    lib.gdn_commit_accepted.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32,
+                                        i32, P, P]
+    lib.gdn_commit_accepted.restype = ctypes.c_int
+    lib.gdn_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.gdn_prefill_workspace_bytes.restype = sz
+    lib.gdn_prefill_chunked.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, P, P,
+                                        P, sz, P]
+    lib.gdn_prefill_chunked.restype = ctypes.c_int
+    lib.gdn_status_string.argtypes = [ctypes.c_int]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_version.argtypes = []
+    lib.gdn_version.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().gdn_status_string(int(code)).decode()
+    except RuntimeError:
+        return f"status {code}"
+
+
+# ------------------------------------------------------------- marshalling
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code, where):
+    if code != GDN_OK:
+        raise GdnError(code, where)
+
+
+def _dtype_code(t):
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, *, slot=None, n_slots=None,
+                     status=None, cache_slot_stride=None, tile_cols=0, row_warps=0):
+    """Build a gdn_verify_args from tensors.  q, k [B,N,Hk,dk]; v [B,N,Hv,dv];
+    alpha, beta [B,N,Hv] fp32; state_cache [n_slots,Hv,dk,dv] fp32 (or any
+    buffer with `cache_slot_stride`); snapshots [B,N,Hv,dk,dv] fp32; o [B,N,Hv,dv] fp32."""
+    B, N, Hk, dk = q.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    for t in (q, k, v, alpha, beta, state_cache, snapshots, o):
+        _need(t.is_contiguous(), "all tensors must be contiguous")
+    _need(k.shape == q.shape and v.shape[:2] == (B, N), "q/k/v shapes disagree")
+    _need(q.dtype == k.dtype == v.dtype, "q, k and v must share a dtype")
+    if cache_slot_stride is None:
+        cache_slot_stride = Hv * dk * dv
+    if n_slots is None:
+        n_slots = state_cache.numel() // cache_slot_stride
+    return VerifyArgs(
+        q=q.data_ptr(), k=k.data_ptr(), v=v.data_ptr(), alpha=alpha.data_ptr(),
+        beta=beta.data_ptr(), state_cache=state_cache.data_ptr(),
+        slot=None if slot is None else slot.data_ptr(), snapshots=snapshots.data_ptr(),
+        o=o.data_ptr(), status=None if status is None else status.data_ptr(),
+        cache_slot_stride=cache_slot_stride, n_slots=n_slots, B=B, N=N, Hk=Hk, Hv=Hv, dk=dk,
+        dv=dv, in_dtype=_dtype_code(q), tile_cols=tile_cols, row_warps=row_warps)
+
+
+def gdn_verify_chain(q, k, v, alpha, beta, state_cache, snapshots, o, *, slot=None, n_slots=None,
+                     status=None, cache_slot_stride=None, tile_cols=0, row_warps=0, stream=None):
+    """Causal-chain verification; writes snapshots and o (see include/gdn.h)."""
+    a = make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, slot=slot,
+                         n_slots=n_slots, status=status, cache_slot_stride=cache_slot_stride,
+                         tile_cols=tile_cols, row_warps=row_warps)
+    _check(load().gdn_verify_chain(ctypes.byref(a), _stream(stream)), "gdn_verify_chain")
+
+
+def gdn_verify_tree(q, k, v, alpha, beta, state_cache, snapshots, o, parent, *, depth_out=None,
+                    slot=None, n_slots=None, status=None, cache_slot_stride=None, tile_cols=0,
+                    row_warps=0, stream=None):
+    """Tree verification; parent [B,N] int32 (see include/gdn.h)."""
+    _need(parent.is_contiguous() and tuple(parent.shape) == tuple(q.shape[:2]),
+          "parent must be a contiguous [B,N] int32 tensor")
+    a = make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, slot=slot,
+                         n_slots=n_slots, status=status, cache_slot_stride=cache_slot_stride,
+                         tile_cols=tile_cols, row_warps=row_warps)
+    _check(load().gdn_verify_tree(ctypes.byref(a), _ptr(parent), _ptr(depth_out),
+                                  _stream(stream)), "gdn_verify_tree")
+
+
+def gdn_commit_accepted(snapshots, accept_idx, state_cache, *, B, N, Hv, dk, dv, n_layers=1,
+                        snap_layer_stride=0, cache_slot_stride=None, cache_layer_stride=0,
+                        slot=None, n_slots=None, status=None, stream=None):
+    """state_cache[l][slot[b]][h] = snapshots[l][b][accept_idx[b]][h] for every layer."""
+    if cache_slot_stride is None:
+        cache_slot_stride = Hv * dk * dv
+    if n_slots is None:
+        n_slots = (state_cache.numel() - (n_layers - 1) * cache_layer_stride) // cache_slot_stride
+    _check(load().gdn_commit_accepted(_ptr(snapshots), snap_layer_stride, _ptr(accept_idx),
+                                      _ptr(state_cache), cache_slot_stride, cache_layer_stride,
+                                      _ptr(slot), n_slots, B, N, Hv, dk, dv, n_layers,
+                                      _ptr(status), _stream(stream)), "gdn_commit_accepted")
+
+
+def gdn_prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk=64) -> int:
+    return int(load().gdn_prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk))
+
+
+def gdn_prefill_chunked(q, k, v, alpha, beta, state, o, workspace=None, *, chunk=64,
+                        stream=None):
+    """Chunked prefill of one sequence: q, k [T,Hk,dk]; v [T,Hv,dv]; alpha, beta [T,Hv];
+    state [Hv,dk,dv] fp32 in/out; o [T,Hv,dv] fp32; workspace a uint8 device tensor of
+    gdn_prefill_workspace_bytes(...) bytes (or None when that is 0)."""
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().gdn_prefill_chunked(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha),
+                                      _ptr(beta), T, Hk, Hv, dk, dv, chunk, _ptr(state), _ptr(o),
+                                      _ptr(workspace), wbytes, _stream(stream)),
+           "gdn_prefill_chunked")

@@ -1,0 +1,144 @@
+// The C ABI (include/gdn.h): argument checks, tile choice and launches.
+// Nothing here allocates, synchronises or keeps state between calls.
+#include <stdint.h>
+
+#include "gdn_common.cuh"
+#include "gdn_launch.h"
+
+namespace {
+
+bool ok_ptr16(const void* p) { return p != nullptr && gdn::aligned16(p); }
+bool ok_ptr4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Default slab shape for the verify kernel: columns per block and row warps.
+// Small problems (few heads) want more, thinner blocks to fill 152 SMs; the
+// state of a lane stays at <= 64 registers.
+void auto_tile(int dk, int dv, int B, int Hv, int* wc, int* nw) {
+  (void)dv;
+  (void)B;
+  (void)Hv;
+  *wc = 16;
+  *nw = 1;
+  if (dk != 128) *nw = 1;
+}
+
+int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, bool tree,
+                  void* stream) {
+  if (a == nullptr) return GDN_ERR_INVALID_ARG;
+  if (a->B < 0 || a->N < 1 || a->Hk < 1 || a->Hv < 1 || a->Hv % a->Hk != 0)
+    return GDN_ERR_INVALID_ARG;
+  if (a->in_dtype != GDN_F32 && a->in_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (a->N > 64 || a->B > 65535 || a->Hv > 65535) return GDN_ERR_UNSUPPORTED;
+  if (a->dk != 16 && a->dk != 32 && a->dk != 64 && a->dk != 128) return GDN_ERR_UNSUPPORTED;
+  if (a->dv < 16 || a->dv > 1024 || a->dv % 16 != 0) return GDN_ERR_UNSUPPORTED;
+  if (a->B == 0) return GDN_OK;
+  if (a->n_slots < 1) return GDN_ERR_INVALID_ARG;
+  const int64_t head_set = (int64_t)a->Hv * a->dk * a->dv;
+  if (a->cache_slot_stride < head_set) return GDN_ERR_INVALID_ARG;
+  if (a->cache_slot_stride % 4 != 0) return GDN_ERR_MISALIGNED;
+  const void* need16[] = {a->q, a->k, a->v, a->state_cache, a->snapshots, a->o};
+  for (const void* p : need16) {
+    if (p == nullptr) return GDN_ERR_INVALID_ARG;
+    if (!gdn::aligned16(p)) return GDN_ERR_MISALIGNED;
+  }
+  if (a->alpha == nullptr || a->beta == nullptr) return GDN_ERR_INVALID_ARG;
+  if (tree && parent == nullptr) return GDN_ERR_INVALID_ARG;
+  const void* need4[] = {a->alpha, a->beta, a->slot, a->status, parent, depth_out};
+  for (const void* p : need4)
+    if (!ok_ptr4(p)) return GDN_ERR_MISALIGNED;
+
+  int wc = 0, nw = 0;
+  auto_tile(a->dk, a->dv, a->B, a->Hv, &wc, &nw);
+  if (a->tile_cols != 0) wc = a->tile_cols;
+  if (a->row_warps != 0) nw = a->row_warps;
+  if (!gdn::verify_tile_supported(a->dk, wc, nw) || a->dv % wc != 0) return GDN_ERR_UNSUPPORTED;
+  return gdn::launch_verify(a, tree ? parent : nullptr, tree ? depth_out : nullptr, wc, nw,
+                            static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_verify_chain(const gdn_verify_args* args, void* stream) {
+  return verify_common(args, nullptr, nullptr, false, stream);
+}
+
+int gdn_verify_tree(const gdn_verify_args* args, const int32_t* parent, int32_t* depth_out,
+                    void* stream) {
+  return verify_common(args, parent, depth_out, true, stream);
+}
+
+int gdn_commit_accepted(const float* snapshots, int64_t snap_layer_stride,
+                        const int32_t* accept_idx, float* state_cache, int64_t cache_slot_stride,
+                        int64_t cache_layer_stride, const int32_t* slot, int32_t n_slots,
+                        int32_t B, int32_t N, int32_t Hv, int32_t dk, int32_t dv,
+                        int32_t n_layers, int32_t* status, void* stream) {
+  if (B < 0 || n_layers < 0 || N < 1 || Hv < 1 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
+  if (snap_layer_stride < 0 || cache_slot_stride < 0 || cache_layer_stride < 0)
+    return GDN_ERR_INVALID_ARG;
+  if (B > 65535 || n_layers > 65535) return GDN_ERR_UNSUPPORTED;
+  if (B == 0 || n_layers == 0) return GDN_OK;
+  const int64_t head_set = (int64_t)Hv * dk * dv;
+  if (n_slots < 1 || cache_slot_stride < head_set) return GDN_ERR_INVALID_ARG;
+  if (head_set % 4 != 0 || snap_layer_stride % 4 != 0 || cache_slot_stride % 4 != 0 ||
+      cache_layer_stride % 4 != 0)
+    return GDN_ERR_MISALIGNED;
+  if (snapshots == nullptr || accept_idx == nullptr || state_cache == nullptr)
+    return GDN_ERR_INVALID_ARG;
+  if (!ok_ptr16(snapshots) || !ok_ptr16(state_cache)) return GDN_ERR_MISALIGNED;
+  if (!ok_ptr4(accept_idx) || !ok_ptr4(slot) || !ok_ptr4(status)) return GDN_ERR_MISALIGNED;
+  return gdn::launch_commit(snapshots, snap_layer_stride, accept_idx, state_cache,
+                            cache_slot_stride, cache_layer_stride, slot, n_slots, B, N, Hv, dk,
+                            dv, n_layers, status, static_cast<cudaStream_t>(stream));
+}
+
+size_t gdn_prefill_workspace_bytes(int32_t T, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+                                   int32_t chunk) {
+  if (T < 0 || Hk < 1 || Hv < 1 || dk < 1 || dv < 1 || chunk < 1) return 0;
+  return gdn::prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk);
+}
+
+int gdn_prefill_chunked(const void* q, const void* k, const void* v, int32_t in_dtype,
+                        const float* alpha, const float* beta, int32_t T, int32_t Hk, int32_t Hv,
+                        int32_t dk, int32_t dv, int32_t chunk, float* state, float* o,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0 || Hk < 1 || Hv < 1 || Hv % Hk != 0) return GDN_ERR_INVALID_ARG;
+  if (in_dtype != GDN_F32 && in_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (dk != 128 || dv != 128 || chunk != 64) return GDN_ERR_UNSUPPORTED;
+  if (Hv > 65535) return GDN_ERR_UNSUPPORTED;
+  if (state == nullptr) return GDN_ERR_INVALID_ARG;
+  if (!gdn::aligned16(state)) return GDN_ERR_MISALIGNED;
+  if (T == 0) return GDN_OK;
+  const void* need16[] = {q, k, v, o};
+  for (const void* p : need16) {
+    if (p == nullptr) return GDN_ERR_INVALID_ARG;
+    if (!gdn::aligned16(p)) return GDN_ERR_MISALIGNED;
+  }
+  if (alpha == nullptr || beta == nullptr) return GDN_ERR_INVALID_ARG;
+  if (!ok_ptr4(alpha) || !ok_ptr4(beta)) return GDN_ERR_MISALIGNED;
+  const size_t need = gdn::prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
+  if (need > 0 && !gdn::aligned16(workspace)) return GDN_ERR_MISALIGNED;
+  return gdn::launch_prefill(q, k, v, in_dtype == GDN_BF16, alpha, beta, T, Hk, Hv, dk, dv, chunk,
+                             state, o, workspace, static_cast<cudaStream_t>(stream));
+}
+
+const char* gdn_status_string(int status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_BAD_TREE: return "GDN_ERR_BAD_TREE";
+    case GDN_ERR_ACCEPT_RANGE: return "GDN_ERR_ACCEPT_RANGE";
+    case GDN_ERR_SLOT_RANGE: return "GDN_ERR_SLOT_RANGE";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+    default: return "GDN_ERR_UNKNOWN";
+  }
+}
+
+int gdn_version(void) { return GDN_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// Commit kernel: copy the accepted node's persisted state into the
+// recurrent-state cache, for every sequence and every layer in one launch
+// ("Photon 2.6", section "Handling recurrent state": the state at the accepted
+// boundary becomes the request's state; when the whole block is accepted it is
+// the last node's state).
+//
+// For one (layer, sequence) the source, snapshots[l][b][accept[b]][0..Hv), and
+// the destination, cache[l][slot[b]][0..Hv), are each one contiguous run of
+// Hv*dk*dv floats, so the kernel is a batched, bit-exact 16-byte-vector copy:
+// grid = (pieces of the run, B, n_layers); each thread issues all its loads
+// before its stores.  The snapshots are read with an evict-first hint since
+// nothing reads them again.
+#include "gdn_common.cuh"
+#include "gdn_launch.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+__global__ void __launch_bounds__(kThreads)
+commit_kernel(const float4* __restrict__ snap, int64_t snap_layer4, const int32_t* accept,
+              float4* __restrict__ cache, int64_t slot4, int64_t layer4, const int32_t* slot,
+              int n_slots, int N, int64_t run4, int32_t* status) {
+  const int b = blockIdx.y, l = blockIdx.z;
+  const int a = __ldg(accept + b);
+  const int s = slot != nullptr ? __ldg(slot + b) : b;
+  if (a < 0 || a >= N || s < 0 || s >= n_slots) {
+    if (blockIdx.x == 0 && l == 0 && threadIdx.x == 0)
+      report(status, (a < 0 || a >= N) ? GDN_ERR_ACCEPT_RANGE : GDN_ERR_SLOT_RANGE);
+    return;
+  }
+  const float4* src = snap + l * snap_layer4 + ((int64_t)b * N + a) * run4;
+  float4* dst = cache + l * layer4 + (int64_t)s * slot4;
+  const int64_t base = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x;
+  float4 t[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int64_t i = base + (int64_t)u * kThreads;
+    if (i < run4) t[u] = __ldcs(src + i);
+  }
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int64_t i = base + (int64_t)u * kThreads;
+    if (i < run4) dst[i] = t[u];
+  }
+}
+
+}  // namespace
+
+int launch_commit(const float* snap, int64_t snap_layer_stride, const int32_t* accept,
+                  float* cache, int64_t cache_slot_stride, int64_t cache_layer_stride,
+                  const int32_t* slot, int n_slots, int B, int N, int Hv, int dk, int dv,
+                  int n_layers, int32_t* status, cudaStream_t stream) {
+  const int64_t run4 = (int64_t)Hv * dk * dv / 4;
+  const int64_t per_block = (int64_t)kThreads * kUnroll;
+  const int64_t gx = (run4 + per_block - 1) / per_block;
+  if (gx > 0x7fffffff) return GDN_ERR_UNSUPPORTED;
+  const dim3 grid((unsigned)gx, B, n_layers);
+  commit_kernel<<<grid, kThreads, 0, stream>>>(
+      reinterpret_cast<const float4*>(snap), snap_layer_stride / 4, accept,
+      reinterpret_cast<float4*>(cache), cache_slot_stride / 4, cache_layer_stride / 4, slot,
+      n_slots, N, run4, status);
+  return launch_status();
+}
+
+}  // namespace gdn

@@ -1,0 +1,49 @@
+// Internal helpers shared by the library's translation units (not part of the
+// C ABI).  Device code here is plain CUDA C++ with a few inline-PTX memory
+// operations; nothing here is shared with the CPU oracle.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// First device-side error wins; the caller zeroes the word before the call.
+__device__ __forceinline__ void report(int32_t* status, int32_t code) {
+  if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, code);
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// 16-byte global load through the read-only (non-coherent) path: only for
+// data that no thread writes during the kernel.
+__device__ __forceinline__ float4 ld_nc_f4(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+__device__ __forceinline__ uint4 ld_nc_u4(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// 16-byte global load cached in L2 only: used to read back data this thread
+// wrote earlier in the same kernel (program order makes it visible).
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
+  return __ldcg(reinterpret_cast<const float4*>(p));
+}
+
+__device__ __forceinline__ void st_f4(float* p, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace gdn

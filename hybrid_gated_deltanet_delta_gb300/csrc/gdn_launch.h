@@ -1,0 +1,27 @@
+// Internal launchers (one per kernel family); the C ABI in gdn_api.cu checks
+// every argument before calling them.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+bool verify_tile_supported(int dk, int wc, int nw);
+int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, int wc,
+                  int nw, cudaStream_t stream);
+
+int launch_commit(const float* snap, int64_t snap_layer_stride, const int32_t* accept,
+                  float* cache, int64_t cache_slot_stride, int64_t cache_layer_stride,
+                  const int32_t* slot, int n_slots, int B, int N, int Hv, int dk, int dv,
+                  int n_layers, int32_t* status, cudaStream_t stream);
+
+size_t prefill_workspace_bytes(int T, int Hk, int Hv, int dk, int dv, int chunk);
+int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const float* alpha,
+                   const float* beta, int T, int Hk, int Hv, int dk, int dv, int chunk,
+                   float* state, float* o, void* workspace, cudaStream_t stream);
+
+}  // namespace gdn

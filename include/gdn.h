@@ -1,0 +1,185 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) gated delta-rule verification library.
+ *
+ * The library runs the Gated DeltaNet recurrence of a hybrid (linear +
+ * full attention) model over a speculative verification block and commits
+ * the accepted state:
+ *
+ *     S_n = alpha_n * S_src(n) * (I - beta_n k_n k_n^T) + beta_n v_n k_n^T
+ *     o_n = S_n q_n
+ *
+ * ("TokenSpeed hits 580 tok/s", section "Why Qwen3.5 is hard to serve fast":
+ * a fixed d x d state per head, updated per token and queried by q.)
+ * S_src(n) is the previous position for a causal chain ("Photon 2.6",
+ * section "Speculative verification in a megakernel") and the parent node
+ * for a best-first draft tree ("Qwen3.6 27B: From 20 t/s to 184 t/s",
+ * DFlash section, steps 3-4).  Every node's state is persisted so that a
+ * rejected suffix needs no work ("We got 207 tok/s with Qwen3.5-27B on an
+ * RTX 3090", list "Key wins", persist-write kernel), and the accepted node's
+ * state is committed into the recurrent-state cache ("Photon 2.6", section
+ * "Handling recurrent state").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - The state of one value head is stored TRANSPOSED: H[i][j] = S[j][i],
+ *    an fp32 row-major d_k x d_v matrix (i over d_k, j over d_v).
+ *  - Value head h reads q/k head h / (Hv / Hk) (contiguous groups).
+ *  - No scaling is applied to q; fold any 1/sqrt(d_k) into q beforehand.
+ *    q and k are used as given (callers L2-normalise them upstream).
+ *  - Every pointer argument is DEVICE memory of the current CUDA device,
+ *    allocated and owned by the caller, unless stated otherwise.  The library
+ *    allocates nothing, keeps no global state and never synchronises: work
+ *    is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and the call returns once it is launched.
+ *  - All pointers must be 16-byte aligned; element strides are in elements.
+ *  - Host-detected errors return a negative gdn_status before anything is
+ *    launched.  Errors that depend on device data (a malformed tree, an
+ *    out-of-range accept index or slot) are written to the optional device
+ *    word `status` (first error wins; the caller zeroes it) and the affected
+ *    sequence is skipped; kernels never trap and never wait on other blocks.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_VERSION 1
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = -1,   /* null pointer, negative or inconsistent size */
+  GDN_ERR_UNSUPPORTED = -2,   /* a size outside what the kernels implement */
+  GDN_ERR_MISALIGNED = -3,    /* pointer not 16-byte aligned, or stride not a multiple of 4 */
+  GDN_ERR_CUDA = -4,          /* the launch itself failed */
+  GDN_ERR_BAD_TREE = -5,      /* device: parent[0] != -1 or parent[n] outside [0, n) */
+  GDN_ERR_ACCEPT_RANGE = -6,  /* device: accept index outside [0, N) */
+  GDN_ERR_SLOT_RANGE = -7,    /* device: slot outside [0, n_slots) */
+  GDN_ERR_WORKSPACE = -8      /* workspace missing or smaller than required */
+} gdn_status;
+
+typedef enum gdn_dtype {
+  GDN_F32 = 0,
+  GDN_BF16 = 1
+} gdn_dtype;
+
+/*
+ * Arguments of one verify call (one GDN layer, B sequences, N nodes each).
+ *
+ *   q, k          [B][N][Hk][dk]  in_dtype (GDN_F32 or GDN_BF16)
+ *   v             [B][N][Hv][dv]  in_dtype
+ *   alpha, beta   [B][N][Hv]      fp32 gates (decay alpha, write strength beta)
+ *   state_cache   recurrent-state cache, READ ONLY here: the state of
+ *                 sequence b, head h starts at
+ *                 state_cache + slot[b]*cache_slot_stride + h*dk*dv
+ *   slot          [B] int32 cache slot per sequence; NULL means slot[b] = b
+ *   n_slots       number of valid slots (slot[b] is checked against it)
+ *   snapshots     [B][N][Hv][dk][dv] fp32 output: S_n of every node
+ *   o             [B][N][Hv][dv] fp32 output
+ *   status        optional device int32 error word (see above)
+ *   tile_cols, row_warps
+ *                 0 = automatic; otherwise the d_v columns owned by one
+ *                 thread block (8, 16 or 32) and the warps that split its
+ *                 d_k rows (1, 2 or 4).  A pure performance hint.
+ *
+ * Supported sizes: dk in {16, 32, 64, 128}; dv a multiple of 16, <= 1024;
+ * 1 <= N <= 64; Hv a multiple of Hk; B >= 0 (B = 0 launches nothing).
+ */
+typedef struct gdn_verify_args {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* alpha;
+  const float* beta;
+  const float* state_cache;
+  const int32_t* slot;
+  float* snapshots;
+  float* o;
+  int32_t* status;
+  int64_t cache_slot_stride;
+  int32_t n_slots;
+  int32_t B;
+  int32_t N;
+  int32_t Hk;
+  int32_t Hv;
+  int32_t dk;
+  int32_t dv;
+  int32_t in_dtype;
+  int32_t tile_cols;
+  int32_t row_warps;
+} gdn_verify_args;
+
+/*
+ * Causal-chain verification (DFlash block: the last committed token plus the
+ * drafts).  Node n starts from node n-1's state; node 0 from the cache.
+ * Writes every node's state to `snapshots` and its output to `o`.
+ */
+int gdn_verify_chain(const gdn_verify_args* args, void* stream);
+
+/*
+ * Tree verification (DDTree block).  parent [B][N] int32 with parent[b][0] = -1
+ * (the root, i.e. the last committed token, starts from the cache) and
+ * 0 <= parent[b][n] < n otherwise (nodes in topological order).  Node n starts
+ * from its parent's state.  depth_out [B][N] int32 (optional, may be NULL)
+ * receives each node's depth, root = 1.  A sequence whose parent array breaks
+ * the rule is skipped and GDN_ERR_BAD_TREE is written to args->status.
+ */
+int gdn_verify_tree(const gdn_verify_args* args, const int32_t* parent, int32_t* depth_out,
+                    void* stream);
+
+/*
+ * Commit the accepted node of every sequence, for n_layers layers at once:
+ *
+ *   state_cache[l][slot[b]][h] = snapshots[l][b][accept_idx[b]][h]
+ *
+ * Layer l of the snapshots starts at snapshots + l*snap_layer_stride and is
+ * laid out [B][N][Hv][dk][dv]; layer l of the cache starts at
+ * state_cache + l*cache_layer_stride, slot s at + s*cache_slot_stride, head h
+ * at + h*dk*dv.  For a chain with accept length L, accept_idx = L - 1.
+ * The copy is bit-exact.  An accept index outside [0, N) or a slot outside
+ * [0, n_slots) skips that sequence and is reported through `status`.
+ * snapshots and state_cache must not overlap.
+ */
+int gdn_commit_accepted(const float* snapshots, int64_t snap_layer_stride,
+                        const int32_t* accept_idx, float* state_cache, int64_t cache_slot_stride,
+                        int64_t cache_layer_stride, const int32_t* slot, int32_t n_slots,
+                        int32_t B, int32_t N, int32_t Hv, int32_t dk, int32_t dv,
+                        int32_t n_layers, int32_t* status, void* stream);
+
+/*
+ * Chunked prefill of one sequence of T tokens: the same recurrence, evaluated
+ * chunk by chunk in the WY / UT-transform form on tensor cores.
+ *
+ *   q, k   [T][Hk][dk]  in_dtype;  v [T][Hv][dv] in_dtype
+ *   alpha, beta [T][Hv] fp32
+ *   state  [Hv][dk][dv] fp32, in: the state before token 0, out: after token T-1
+ *   o      [T][Hv][dv] fp32 output
+ *   workspace  device scratch of at least gdn_prefill_workspace_bytes(...) bytes,
+ *              owned by the caller, contents need not be initialised
+ *
+ * Supported: dk = dv = 128, chunk = 64, T >= 0 (any T; the last chunk may be
+ * partial).  GDN_ERR_WORKSPACE if the workspace is NULL or too small.
+ */
+size_t gdn_prefill_workspace_bytes(int32_t T, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+                                   int32_t chunk);
+
+int gdn_prefill_chunked(const void* q, const void* k, const void* v, int32_t in_dtype,
+                        const float* alpha, const float* beta, int32_t T, int32_t Hk, int32_t Hv,
+                        int32_t dk, int32_t dv, int32_t chunk, float* state, float* o,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a gdn_status value (static string, never NULL). */
+const char* gdn_status_string(int status);
+
+/* GDN_VERSION of the loaded library. */
+int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

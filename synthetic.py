@@ -185,9 +185,16 @@ def tree22(seed=None, B=1):
 
 
 def batched8x16_layer(layer: int):
+    """Inputs of one of the 48 layers.  The slot of each sequence and its
+    accept index belong to the batch, not the layer, so they are drawn once
+    from the workload's base seed and shared by every layer."""
     base = workload_seed("batched8x16")
-    return make_verify_inputs(B=8, N=16, dtype="bf16", alpha_kind="near_one", state_sigma=0.05,
-                              seed=layer_seed(base, layer), **HEADS)
+    inp = make_verify_inputs(B=8, N=16, dtype="bf16", alpha_kind="near_one", state_sigma=0.05,
+                             seed=layer_seed(base, layer), **HEADS)
+    rng = np.random.default_rng(base)
+    inp["slot"] = rng.permutation(8).astype(np.int32)
+    inp["accept"] = (rng.integers(1, 17, size=8) - 1).astype(np.int32)
+    return inp
 
 
 BATCHED_LAYERS = 48

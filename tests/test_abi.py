@@ -1,0 +1,165 @@
+"""CPU-only checks of the C ABI: the library builds and loads, exports every
+function include/gdn.h declares, the struct layout matches, and host-side
+argument checks reject bad calls before anything is launched (these calls
+never reach the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import hybrid_gated_deltanet_delta_gb300 as gdn
+from hybrid_gated_deltanet_delta_gb300 import build as gdn_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gdn_build.build()
+    return gdn.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("gdn_verify_chain", "gdn_verify_tree", "gdn_commit_accepted",
+                 "gdn_prefill_chunked", "gdn_prefill_workspace_bytes", "gdn_status_string",
+                 "gdn_version"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} is declared in gdn.h but not exported"
+
+
+def test_struct_layout_matches_c(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text('#include "gdn.h"\n#include <stdio.h>\n#include <stddef.h>\n'
+                   'int main(void){printf("%zu %zu %zu %zu\\n", sizeof(gdn_verify_args),'
+                   ' offsetof(gdn_verify_args, cache_slot_stride),'
+                   ' offsetof(gdn_verify_args, n_slots), offsetof(gdn_verify_args, row_warps));'
+                   'return 0;}\n')
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.check_call(["gcc", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)])
+    size, off_stride, off_slots, off_rw = map(int, subprocess.check_output([str(exe)]).split())
+    A = gdn.VerifyArgs
+    assert ctypes.sizeof(A) == size
+    assert A.cache_slot_stride.offset == off_stride
+    assert A.n_slots.offset == off_slots and A.row_warps.offset == off_rw
+
+
+def test_version_and_status_strings(lib):
+    assert lib.gdn_version() == 1
+    assert gdn.status_string(gdn.GDN_ERR_BAD_TREE) == "GDN_ERR_BAD_TREE"
+    assert gdn.status_string(12345) == "GDN_ERR_UNKNOWN"
+
+
+def _args(**kw):
+    a = gdn.VerifyArgs()
+    base = dict(q=0x10000, k=0x20000, v=0x30000, alpha=0x40000, beta=0x50000,
+                state_cache=0x60000, snapshots=0x70000, o=0x80000, cache_slot_stride=48 * 128 * 128,
+                n_slots=1, B=1, N=16, Hk=16, Hv=48, dk=128, dv=128, in_dtype=gdn.GDN_BF16)
+    base.update(kw)
+    for key, val in base.items():
+        setattr(a, key, val)
+    return a
+
+
+@pytest.mark.parametrize("change, want", [
+    (dict(N=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(B=-1), gdn.GDN_ERR_INVALID_ARG),
+    (dict(Hv=47), gdn.GDN_ERR_INVALID_ARG),
+    (dict(in_dtype=7), gdn.GDN_ERR_INVALID_ARG),
+    (dict(N=65), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(dk=96), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(dv=40), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(q=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(snapshots=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(alpha=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(v=0x30008), gdn.GDN_ERR_MISALIGNED),
+    (dict(o=0x80004), gdn.GDN_ERR_MISALIGNED),
+    (dict(alpha=0x40002), gdn.GDN_ERR_MISALIGNED),
+    (dict(n_slots=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(cache_slot_stride=100), gdn.GDN_ERR_INVALID_ARG),
+    (dict(cache_slot_stride=48 * 128 * 128 + 2), gdn.GDN_ERR_MISALIGNED),
+    (dict(tile_cols=24), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(tile_cols=32, row_warps=1), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(dk=64, row_warps=4), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(B=0), gdn.GDN_OK),
+])
+def test_verify_host_checks(lib, change, want):
+    a = _args(**change)
+    assert lib.gdn_verify_chain(ctypes.byref(a), None) == want
+    assert lib.gdn_verify_tree(ctypes.byref(a), ctypes.c_void_p(0x90000), None, None) == want
+
+
+def test_verify_tree_needs_parent(lib):
+    assert lib.gdn_verify_tree(ctypes.byref(_args()), None, None, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_verify_chain(None, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def _commit(lib, **kw):
+    base = dict(snap=0x10000, sls=0, acc=0x20000, cache=0x30000, css=48 * 128 * 128, cls=0,
+                slot=None, n_slots=1, B=1, N=16, Hv=48, dk=128, dv=128, L=1, status=None)
+    base.update(kw)
+    b = base
+    return lib.gdn_commit_accepted(b["snap"], b["sls"], b["acc"], b["cache"], b["css"], b["cls"],
+                                   b["slot"], b["n_slots"], b["B"], b["N"], b["Hv"], b["dk"],
+                                   b["dv"], b["L"], b["status"], None)
+
+
+@pytest.mark.parametrize("change, want", [
+    (dict(B=0), gdn.GDN_OK),
+    (dict(L=0), gdn.GDN_OK),
+    (dict(N=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(snap=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(acc=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(cache=0x30004), gdn.GDN_ERR_MISALIGNED),
+    (dict(sls=6), gdn.GDN_ERR_MISALIGNED),
+    (dict(css=5), gdn.GDN_ERR_INVALID_ARG),
+    (dict(n_slots=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(dk=3, dv=3, Hv=1, css=16), gdn.GDN_ERR_MISALIGNED),
+    (dict(cls=-4), gdn.GDN_ERR_INVALID_ARG),
+])
+def test_commit_host_checks(lib, change, want):
+    assert _commit(lib, **change) == want
+
+
+def test_prefill_host_checks(lib):
+    f = lib.gdn_prefill_chunked
+    P = 0x100000
+    ok = dict(q=P, k=P, v=P, dt=gdn.GDN_BF16, a=P, b=P, T=128, Hk=16, Hv=48, dk=128, dv=128,
+              C=64, s=P, o=P, w=P, wb=1 << 40)
+
+    def call(**kw):
+        x = dict(ok)
+        x.update(kw)
+        return f(x["q"], x["k"], x["v"], x["dt"], x["a"], x["b"], x["T"], x["Hk"], x["Hv"],
+                 x["dk"], x["dv"], x["C"], x["s"], x["o"], x["w"], x["wb"], None)
+
+    assert call(T=-1) == gdn.GDN_ERR_INVALID_ARG
+    assert call(Hv=47) == gdn.GDN_ERR_INVALID_ARG
+    assert call(dk=64) == gdn.GDN_ERR_UNSUPPORTED
+    assert call(C=32) == gdn.GDN_ERR_UNSUPPORTED
+    assert call(s=0) == gdn.GDN_ERR_INVALID_ARG
+    assert call(o=P + 4) == gdn.GDN_ERR_MISALIGNED
+    assert call(T=0) == gdn.GDN_OK
+    need = lib.gdn_prefill_workspace_bytes(128, 16, 48, 128, 128, 64)
+    if need > 0:
+        assert call(w=0) == gdn.GDN_ERR_WORKSPACE
+        assert call(wb=need - 1) == gdn.GDN_ERR_WORKSPACE
+    assert lib.gdn_prefill_workspace_bytes(-1, 16, 48, 128, 128, 64) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        gdn.load(str(tmp_path / "missing.so"))

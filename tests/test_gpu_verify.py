@@ -1,0 +1,246 @@
+"""CUDA verify / commit path against the CPU oracle, element by element,
+on the same seeded inputs, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from gpu_helpers import (assert_close, canaries_ok, dev, guarded, torch, verify_on_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle(inp, tree=None):
+    st, snap, o = oracle.verify_inputs(inp, tree=tree)
+    assert st == oracle.OK
+    return snap, o
+
+
+def test_tiny_chain_verify_and_commit(gpu_lib):
+    """4-node chain, 2 heads, d = 16, fp32 everything; commit node 2."""
+    inp = synthetic.tiny_chain()
+    out = verify_on_gpu(gpu_lib, inp)
+    snap, o = _oracle(inp)
+    assert out["status"] == 0
+    assert_close(out["o"], o, "tiny o")
+    assert_close(out["snap"], snap, "tiny snapshots")
+    t = torch()
+    acc = t.tensor([synthetic.tiny_chain_accept()], dtype=t.int32, device="cuda")
+    st = t.zeros(1, dtype=t.int32, device="cuda")
+    cache = out["cache_t"]
+    gpu_lib.gdn_commit_accepted(out["snap_t"], acc, cache, B=1, N=4, Hv=2, dk=16, dv=16,
+                                slot=out["slot_t"], n_slots=1, status=st)
+    t.cuda.synchronize()
+    assert st.item() == 0
+    got = cache.cpu().numpy()[inp["slot"][0]]
+    assert np.array_equal(got, out["snap"][0, 2]), "commit is not a bit-exact copy"
+    assert_close(got, snap[0, 2], "committed state vs oracle")
+
+
+@pytest.mark.parametrize("tile", [(0, 0), (8, 1), (16, 1), (16, 2), (32, 2), (16, 4), (32, 4)])
+def test_chain16_full(gpu_lib, tile):
+    """Single-sequence chain of 16, 16 q/k heads, 48 value heads, d = 128, bf16
+    inputs; every output and every snapshot, in every tile shape."""
+    inp = synthetic.chain16()
+    out = verify_on_gpu(gpu_lib, inp, tile_cols=tile[0], row_warps=tile[1])
+    snap, o = _oracle(inp)
+    assert out["status"] == 0
+    assert_close(out["o"], o, "chain16 o")
+    assert_close(out["snap"], snap, "chain16 snapshots")
+
+
+def test_tree22_full(gpu_lib):
+    """DDTree of 22 nodes: per-node states from the parent, depths bit-exact,
+    commit of the accepted node."""
+    inp = synthetic.tree22()
+    out = verify_on_gpu(gpu_lib, inp)
+    snap, o = _oracle(inp)
+    assert out["status"] == 0
+    assert_close(out["o"], o, "tree22 o")
+    assert_close(out["snap"], snap, "tree22 snapshots")
+    st, depth = oracle.tree_depth(inp["parent"])
+    assert st == oracle.OK and np.array_equal(out["depth"], depth)
+    t = torch()
+    acc = dev(inp["accept"])
+    gpu_lib.gdn_commit_accepted(out["snap_t"], acc, out["cache_t"], B=1, N=22, Hv=48, dk=128,
+                                dv=128, slot=out["slot_t"], n_slots=inp["n_slots"])
+    t.cuda.synchronize()
+    got = out["cache_t"].cpu().numpy()[inp["slot"][0]]
+    assert np.array_equal(got, out["snap"][0, inp["accept"][0]])
+
+
+@pytest.mark.parametrize("tile", [(16, 1), (32, 4), (16, 2)])
+def test_single_path_tree_equals_chain(gpu_lib, tile):
+    inp = synthetic.chain16(seed=99)
+    a = verify_on_gpu(gpu_lib, inp, tree=False, tile_cols=tile[0], row_warps=tile[1])
+    b = verify_on_gpu(gpu_lib, inp, tree=True, tile_cols=tile[0], row_warps=tile[1])
+    assert np.array_equal(a["snap"], b["snap"]) and np.array_equal(a["o"], b["o"])
+    assert b["depth"][0].tolist() == list(range(1, 17))
+
+
+def test_batched_48_layers_as_benchmarked(gpu_lib):
+    """8 sequences x chain of 16 x 48 layers, each layer with its own inputs and
+    cache, then one commit over all 48 layers; layers 0, 23 and 47 are compared
+    with the oracle in full, the commit of every layer bit-exactly."""
+    t = torch()
+    L, B, N, Hv, d = synthetic.BATCHED_LAYERS, 8, 16, 48, 128
+    cache = t.empty((L, B, Hv, d, d), dtype=t.float32, device="cuda")
+    snaps = t.empty((L, B, N, Hv, d, d), dtype=t.float32, device="cuda")
+    outs = t.empty((L, B, N, Hv, d), dtype=t.float32, device="cuda")
+    acc = dev(synthetic.batched8x16_layer(0)["accept"])
+    slot = dev(synthetic.batched8x16_layer(0)["slot"])
+    inputs = {}
+    for l in range(L):
+        inp = synthetic.batched8x16_layer(l)
+        cache[l].copy_(dev(inp["cache"]))
+        if l in (0, 23, 47):
+            inputs[l] = inp
+        gpu_lib.gdn_verify_chain(dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha"]),
+                                 dev(inp["beta"]), cache[l], snaps[l], outs[l], slot=slot,
+                                 n_slots=B)
+    gpu_lib.gdn_commit_accepted(snaps, acc, cache, B=B, N=N, Hv=Hv, dk=d, dv=d, n_layers=L,
+                                snap_layer_stride=B * N * Hv * d * d,
+                                cache_layer_stride=B * Hv * d * d, slot=slot, n_slots=B)
+    t.cuda.synchronize()
+    for l, inp in inputs.items():
+        snap, o = _oracle(inp)
+        assert_close(outs[l].cpu().numpy(), o, f"layer {l} o")
+        assert_close(snaps[l].cpu().numpy(), snap, f"layer {l} snapshots")
+    acc_n, slot_n = acc.cpu().numpy(), slot.cpu().numpy()
+    for b in range(B):
+        got = cache[:, slot_n[b]]
+        want = snaps[:, b, acc_n[b]]
+        assert t.equal(got, want), f"commit of sequence {b}"
+
+
+@pytest.mark.parametrize("shape", [
+    dict(B=1, N=1, Hk=1, Hv=1, dk=128, dv=128),     # single node
+    dict(B=3, N=64, Hk=2, Hv=6, dk=128, dv=128),    # maximum block, several sequences
+    dict(B=2, N=5, Hk=1, Hv=3, dk=64, dv=48),       # dv not a multiple of 32
+    dict(B=2, N=7, Hk=4, Hv=4, dk=32, dv=16),
+    dict(B=1, N=3, Hk=1, Hv=2, dk=16, dv=32),
+])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("tree", [False, True])
+def test_edge_shapes(gpu_lib, shape, dtype, tree):
+    inp = synthetic.make_verify_inputs(dtype=dtype, alpha_kind="near_one", state_sigma=0.05,
+                                       seed=1234 + shape["N"], tree=tree, n_slots=shape["B"] + 2,
+                                       **shape)
+    out = verify_on_gpu(gpu_lib, inp)
+    snap, o = _oracle(inp)
+    assert out["status"] == 0
+    assert_close(out["o"], o, "o")
+    assert_close(out["snap"], snap, "snapshots")
+    if tree:
+        assert np.array_equal(out["depth"], oracle.tree_depth(inp["parent"])[1])
+
+
+def test_unit_decay_gates_f32(gpu_lib):
+    """alpha = exp(-softplus(z)) spans (0, 1), fp32 inputs, d = 128."""
+    inp = synthetic.make_verify_inputs(B=2, N=16, Hk=2, Hv=6, dk=128, dv=128, dtype="f32",
+                                       alpha_kind="unit", state_sigma=0.1, seed=77, tree=True)
+    out = verify_on_gpu(gpu_lib, inp)
+    snap, o = _oracle(inp)
+    assert_close(out["o"], o, "o")
+    assert_close(out["snap"], snap, "snapshots")
+
+
+def test_empty_batch_is_a_no_op(gpu_lib):
+    t = torch()
+    z = t.zeros((0, 4, 1, 16), dtype=t.float32, device="cuda")
+    zv = t.zeros((0, 4, 1, 16), dtype=t.float32, device="cuda")
+    ab = t.zeros((0, 4, 1), dtype=t.float32, device="cuda")
+    cache = t.zeros((1, 1, 16, 16), device="cuda")
+    snap = t.zeros((0, 4, 1, 16, 16), device="cuda")
+    o = t.zeros((0, 4, 1, 16), device="cuda")
+    gpu_lib.gdn_verify_chain(z, z, zv, ab, ab, cache, snap, o, n_slots=1)
+    gpu_lib.gdn_commit_accepted(snap, t.zeros(0, dtype=t.int32, device="cuda"), cache, B=0,
+                                N=4, Hv=1, dk=16, dv=16)
+    t.cuda.synchronize()
+
+
+def test_device_errors_skip_only_the_bad_sequence(gpu_lib):
+    """A malformed tree, a bad slot and a bad accept index are reported in the
+    status word; the other sequences are still computed correctly."""
+    t = torch()
+    inp = synthetic.make_verify_inputs(B=3, N=6, Hk=1, Hv=2, dk=32, dv=32, dtype="bf16",
+                                       alpha_kind="near_one", state_sigma=0.05, seed=5, tree=True)
+    good_snap, good_o = _oracle(inp)
+    bad = dict(inp)
+    bad["parent"] = inp["parent"].copy()
+    bad["parent"][1, 3] = 4          # forward reference
+    out = verify_on_gpu(gpu_lib, bad)
+    assert out["status"] == gpu_lib.GDN_ERR_BAD_TREE
+    for b in (0, 2):
+        assert_close(out["o"][b], good_o[b], f"sequence {b} o")
+    assert not np.any(out["snap"][1]), "the bad sequence must be skipped"
+
+    bad = dict(inp)
+    bad["slot"] = inp["slot"].copy()
+    bad["slot"][2] = 99
+    out = verify_on_gpu(gpu_lib, bad)
+    assert out["status"] == gpu_lib.GDN_ERR_SLOT_RANGE
+    assert_close(out["snap"][0], good_snap[0], "sequence 0 snapshots")
+
+    out = verify_on_gpu(gpu_lib, inp)
+    cache = out["cache_t"]
+    before = cache.clone()
+    st = t.zeros(1, dtype=t.int32, device="cuda")
+    acc = t.tensor([2, 6, 0], dtype=t.int32, device="cuda")   # 6 is out of range
+    gpu_lib.gdn_commit_accepted(out["snap_t"], acc, cache, B=3, N=6, Hv=2, dk=32, dv=32,
+                                slot=out["slot_t"], n_slots=inp["n_slots"], status=st)
+    t.cuda.synchronize()
+    assert st.item() == gpu_lib.GDN_ERR_ACCEPT_RANGE
+    s = inp["slot"]
+    assert t.equal(cache[s[1]], before[s[1]])
+    assert t.equal(cache[s[0]], out["snap_t"][0, 2]) and t.equal(cache[s[2]], out["snap_t"][2, 0])
+
+
+def test_rounds_of_verify_and_commit_match_one_sequential_run(gpu_lib):
+    """Several speculative rounds on the GPU (verify from the cache, commit the
+    accepted prefix) reach the state of one token-by-token run over the
+    accepted tokens (oracle), i.e. speculation does not change the state."""
+    t = torch()
+    rng = np.random.default_rng(8)
+    Hk, Hv, d, N = 2, 6, 128, 16
+    first = synthetic.make_verify_inputs(B=1, N=N, Hk=Hk, Hv=Hv, dk=d, dv=d, dtype="bf16",
+                                         alpha_kind="near_one", state_sigma=0.05, seed=300)
+    cache = dev(first["cache"])
+    start = first["cache"][first["slot"][0]].astype(np.float64)
+    slot = dev(first["slot"])
+    acc_parts = {key: [] for key in ("q_f64", "k_f64", "v_f64", "alpha", "beta")}
+    for r in range(5):
+        inp = first if r == 0 else synthetic.make_verify_inputs(
+            B=1, N=N, Hk=Hk, Hv=Hv, dk=d, dv=d, dtype="bf16", alpha_kind="near_one",
+            state_sigma=0.05, seed=300 + r)
+        snap = t.empty((1, N, Hv, d, d), device="cuda")
+        o = t.empty((1, N, Hv, d), device="cuda")
+        gpu_lib.gdn_verify_chain(dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha"]),
+                                 dev(inp["beta"]), cache, snap, o, slot=slot, n_slots=1)
+        L = int(rng.integers(1, N + 1))
+        gpu_lib.gdn_commit_accepted(snap, t.tensor([L - 1], dtype=t.int32, device="cuda"), cache,
+                                    B=1, N=N, Hv=Hv, dk=d, dv=d, slot=slot, n_slots=1)
+        for key in acc_parts:
+            acc_parts[key].append(inp[key][0, :L])
+    t.cuda.synchronize()
+    cat = {key: np.concatenate(v) for key, v in acc_parts.items()}
+    T = cat["alpha"].shape[0]
+    st, final, _ = oracle.prefill_step(cat["q_f64"], cat["k_f64"], cat["v_f64"], cat["alpha"],
+                                       cat["beta"], start, T=T, Hk=Hk, Hv=Hv, dk=d, dv=d)
+    assert st == oracle.OK
+    assert_close(cache.cpu().numpy()[0], final, "state after rounds")
+
+
+def test_outputs_have_guard_canaries_after_commit(gpu_lib):
+    """The commit writes exactly the accepted slots of the cache and nothing past it."""
+    t = torch()
+    inp = synthetic.chain16(seed=5)
+    out = verify_on_gpu(gpu_lib, inp)
+    n = 48 * 128 * 128
+    cache, back = guarded((1, 48, 128, 128))
+    cache.copy_(out["cache_t"])
+    gpu_lib.gdn_commit_accepted(out["snap_t"], dev(inp["accept"]), cache, B=1, N=16, Hv=48,
+                                dk=128, dv=128, slot=t.zeros(1, dtype=t.int32, device="cuda"),
+                                n_slots=1)
+    t.cuda.synchronize()
+    assert canaries_ok(back, n)
