@@ -308,14 +308,33 @@ def _dev(a, torch):
 
 
 class VerifyCase:
-    """Device buffers for one verify layer (inputs, cache, outputs)."""
+    """Device buffers for one verify layer (inputs, cache, outputs).  The
+    per-step inputs (q, k, v, alpha, beta, accept) live in one packed device
+    buffer so that the end-to-end leg moves them with a single copy from one
+    pinned host buffer."""
+
+    NAMES = ("q", "k", "v", "alpha", "beta", "accept")
 
     def __init__(self, inp, torch, pinned=False):
         self.inp = inp
         self.B, self.N, self.Hv = inp["B"], inp["N"], inp["Hv"]
         dk, dv = inp["dk"], inp["dv"]
-        self.names = ("q", "k", "v", "alpha", "beta", "accept")
-        self.dev = {n: _dev(inp[n], torch) for n in self.names}
+        arrays = {n: np.ascontiguousarray(inp[n]) for n in self.NAMES}
+        offs, total = {}, 0
+        for n in self.NAMES:
+            offs[n] = total
+            total += (arrays[n].nbytes + 255) // 256 * 256
+        host = np.zeros(total, np.uint8)
+        for n in self.NAMES:
+            host[offs[n]:offs[n] + arrays[n].nbytes] = arrays[n].view(np.uint8).ravel()
+        self.packed = torch.from_numpy(host).cuda()
+        tdt = {np.dtype(np.uint16): torch.bfloat16, np.dtype(np.float32): torch.float32,
+               np.dtype(np.int32): torch.int32}
+        self.dev = {}
+        for n in self.NAMES:
+            a = arrays[n]
+            seg = self.packed[offs[n]:offs[n] + a.nbytes]
+            self.dev[n] = seg.view(tdt[a.dtype]).view(*a.shape)
         self.cache = _dev(inp["cache"], torch)
         self.slot = _dev(inp["slot"], torch)
         self.parent = _dev(inp["parent"], torch) if inp["tree"] else None
@@ -323,7 +342,7 @@ class VerifyCase:
         self.o = torch.empty((self.B, self.N, self.Hv, dv), device="cuda")
         self.host = None
         if pinned:
-            self.host = {n: self.dev[n].cpu().pin_memory() for n in self.names}
+            self.host = self.packed.cpu().pin_memory()
             self.o_host = torch.empty(self.o.shape, dtype=torch.float32).pin_memory()
 
     def verify(self, gdn):
@@ -335,9 +354,8 @@ class VerifyCase:
             gdn.gdn_verify_chain(*args, slot=self.slot, n_slots=self.inp["n_slots"])
 
     def h2d(self):
-        for n in self.names:
-            self.dev[n].copy_(self.host[n], non_blocking=True)
-        return sum(self.host[n].numel() * self.host[n].element_size() for n in self.names)
+        self.packed.copy_(self.host, non_blocking=True)
+        return self.host.numel()
 
     def d2h(self):
         self.o_host.copy_(self.o, non_blocking=True)
@@ -362,7 +380,8 @@ def run_ours(args, wl_name, world, rank, local):
         return run_prefill(args, gdn, torch, flush, world, rank, local)
 
     Hk, Hv, dk, dv = HEADS["Hk"], HEADS["Hv"], HEADS["dk"], HEADS["dv"]
-    B, N, L = wl["B"], wl["N"], wl["layers"]
+    B, N = wl["B"], wl["N"]
+    L = args.layers if (args.layers and wl_name == "batched8x16") else wl["layers"]
     if wl_name == "batched8x16":
         layers = []
         for l in range(L):
@@ -450,7 +469,7 @@ def run_ours(args, wl_name, world, rank, local):
     e2e_s = max_over_ranks(e2e_s, world)
 
     node_heads = B * N * Hv * len(layers)
-    value = world * node_heads * args.steps / (total_ms / 1e3)
+    value = job_throughput(node_heads, args.steps, total_ms, world)
     hbm, bf16, peak_kind = measured_peaks()
     vbytes = verify_bytes(B, N, Hk, Hv, dk, dv, tree=wl.get("tree", False))
     launch_ms = statistics.mean(verify_ms) / len(layers)
@@ -621,13 +640,21 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The slowest rank's time (host-side control message, not data path)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([float(x)], device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_step_per_rank, steps, max_rank_ms, world):
+    """Whole-job units/s: every rank processed the same units; the job took
+    as long as its slowest rank."""
+    return world * units_per_step_per_rank * steps / (max_rank_ms / 1e3)
 
 
 # -------------------------------------------------------------- reference arm
@@ -675,6 +702,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="chain16", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=0,
+                    help="batched8x16 only: run this many of the 48 layers (profiling slices)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (for quick runs)")
     args = ap.parse_args()

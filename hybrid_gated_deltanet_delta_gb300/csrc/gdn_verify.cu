@@ -4,34 +4,43 @@
 // kernel instead of by a separate copy; "Photon 2.6", section "Handling
 // recurrent state": the working state stays in registers across the block).
 //
+// Recurrence
+// ----------
+// The state of one value head is H = S^T (d_k x d_v, fp32, row-major).  With
+// src(n) = n - 1 for a chain and the parent for a tree,
+//     u_n = H_src(n)^T k_n,   delta_n = beta_n (v_n - alpha_n u_n),
+//     H_n = alpha_n H_src(n) + k_n delta_n^T,   o_n = H_n^T q_n,
+// which is S_n = alpha_n S_src(n) (I - beta_n k_n k_n^T) + beta_n v_n k_n^T,
+// o_n = S_n q_n with the product distributed.  Column j of every H_n depends
+// only on column j of the cached state, so a head splits into independent
+// column slabs.
+//
 // Work decomposition
 // ------------------
-// The state of one value head is H = S^T, d_k x d_v fp32, row-major.  With
-//     u = S k  (u_j = sum_i H[i][j] k_i)
-//     delta = beta (v - alpha u)
-//     H' = alpha H + k delta^T
-//     o = S' q (o_j = sum_i H'[i][j] q_i)
-// (the update S(alpha I - alpha beta k k^T) + beta v k^T with the product
-// distributed), column j of H' depends only on column j of H.  One thread
-// block therefore owns a slab of WC columns of one (sequence, value head):
-// grid = (dv / WC, Hv, B), with no communication between blocks.
+// One warp (one thread block) owns a slab of WC columns of one (sequence,
+// value head): grid = (dv / WC, Hv, B).  lane = cg + CG*rl: cg picks 4 adjacent
+// columns (a 16-byte vector), rl one of RL = 32/CG row lanes, and each lane
+// keeps R = d_k/RL consecutive rows x 4 columns of the state in registers (as
+// float2 pairs for the paired fp32 FMA) for the whole block.  Column sums
+// reduce over the RL row lanes with warp shuffles.
 //
-// Inside a block, NW warps split the d_k rows.  In a warp, lane = cg + CG*rl:
-// cg picks a group of 4 adjacent columns (one 16-byte vector), rl one of RL
-// row lanes, and each lane keeps R consecutive rows x 4 columns of the state
-// in registers for the whole block.  Column sums (u and o) reduce over the RL
-// row lanes with warp shuffles and, when NW > 1, over warps through shared
-// memory (u: one barrier per node; o: partials kept per node and reduced once
-// at the end).  q, k, v and the gates of all N nodes are staged in shared
-// memory (fp32) before the node loop.
-//
-// Snapshots: every lane stores its R x 4 block with 16-byte vector stores;
-// a warp-wide store covers RL rows x (WC * 4) contiguous bytes.
-//
-// Tree: node n continues from the registers when parent[n] == n - 1 and
-// otherwise re-reads its parent's snapshot.  Each thread re-reads exactly the
-// elements it stored itself, so program order alone makes them visible (no
-// fence, no barrier); the re-read goes through L2.
+// The node loop is built so that snapshot stores never wait on a reduction:
+// the reduction that feeds node n+1 runs while node n updates and stores.
+// When src(n+1) = n,
+//     u_{n+1} = H_n^T k_{n+1} = alpha_n (H_src(n)^T k_{n+1}) + delta_n (k_n . k_{n+1}),
+// and both sums on the right come from the registers BEFORE node n's update.
+// When src(n) != n - 1 (a tree), H_src(n) comes from a pool of shared-memory
+// stash slots: a node whose state a later, non-adjacent child will need is
+// copied there when it is computed (slots are assigned by a greedy pass over
+// the tree in the prologue and freed after the last such child starts); only
+// if the pool runs out is the parent read back from the snapshot this thread
+// stored earlier (same thread, same addresses: program order makes it
+// visible).  u_n is then reduced when node n starts.  Shared-memory traffic
+// does not compete with the snapshot stores for the SM's global-memory pipe,
+// which is what bounds this kernel.
+// q, k, v, the gates and the parents are staged with cp.async while the
+// cached state loads.  Snapshots leave as 16-byte stores; a warp-wide store
+// covers RL rows x WC*4 contiguous bytes.
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
 
@@ -40,35 +49,48 @@ namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
 
-template <int DK, int WC, int NW>
+template <int DK, int WC>
 struct Shape {
-  static constexpr int CG = WC / 4;        // 16-byte column groups per row of the slab
-  static constexpr int RL = 32 / CG;       // row lanes per warp
-  static constexpr int ROWS_W = DK / NW;   // rows per warp
-  static constexpr int R = ROWS_W / RL;    // rows per lane
-  static_assert(WC % 4 == 0 && 32 % CG == 0, "slab width");
-  static_assert(R >= 1 && R * RL == ROWS_W && ROWS_W * NW == DK, "row split");
+  static constexpr int CG = WC / 4;   // 16-byte column groups per row of the slab
+  static constexpr int RL = 32 / CG;  // row lanes per warp
+  static constexpr int R = DK / RL;   // rows per lane
+  static_assert(WC % 4 == 0 && 32 % CG == 0 && RL >= 2, "slab width");
+  static_assert(R >= 1 && R * RL == DK, "row split");
 };
 
-// Shared-memory plan in floats; every array starts on a 16-byte boundary.
-__host__ __device__ constexpr int round4(int x) { return (x + 3) & ~3; }
+__host__ __device__ constexpr int round16(int x) { return (x + 15) & ~15; }
 
+// Shared-memory plan in bytes; every array starts on a 16-byte boundary.
+// Tree blocks add per-node tables and `pool` stash slots of dk x WC floats.
 struct SmemPlan {
-  int q, k, v, a, b, par, u, o, total;
+  int q, k, v, a, b, par, src, stash, last, pool, total;
 };
 
-__host__ __device__ inline SmemPlan smem_plan(int N, int DK, int WC, int NW) {
+__host__ __device__ inline SmemPlan smem_plan(int N, int DK, int WC, int esz, bool tree,
+                                              int pool) {
   SmemPlan s{};
   s.q = 0;
-  s.k = s.q + N * DK;
-  s.v = s.k + N * DK;
-  s.a = s.v + N * WC;
-  s.b = round4(s.a + N);
-  s.par = round4(s.b + N);
-  s.u = round4(s.par + N);
-  s.o = s.u + (NW > 1 ? 2 * NW * WC : 0);
-  s.total = s.o + (NW > 1 ? N * NW * WC : 0);
+  s.k = s.q + round16(N * DK * esz);
+  s.v = s.k + round16(N * DK * esz);
+  s.a = s.v + round16(N * WC * esz);
+  s.b = s.a + round16(N * 4);
+  s.par = s.b + round16(N * 4);
+  const int t = tree ? round16(N * 4) : 0;
+  s.src = s.par + t;
+  s.stash = s.src + t;
+  s.last = s.stash + t;
+  s.pool = s.last + t;
+  s.total = s.pool + (tree ? pool * DK * WC * 4 : 0);
   return s;
+}
+
+// Stash slots per tree block: as many as fit next to the staged inputs while
+// three blocks still share an SM (at least 1, at most 12).
+inline int tree_pool_slots(int N, int DK, int WC, int esz) {
+  const SmemPlan base = smem_plan(N, DK, WC, esz, true, 0);
+  const int budget = 74 * 1024 - base.total;
+  int slots = budget / (DK * WC * 4);
+  return slots < 1 ? 1 : (slots > 12 ? 12 : slots);
 }
 
 struct VerifyParams {
@@ -85,229 +107,322 @@ struct VerifyParams {
   const int32_t* parent;
   int32_t* depth_out;
   int64_t cache_slot_stride;
-  int n_slots, N, Hk, Hv, dv, bf16;
+  int n_slots, N, Hk, Hv, dv, bf16, pool;
 };
 
-// Stage n_rows rows of `width` elements (row r at src + r*row_stride elements)
-// into dst[r*width + c] as fp32.  16-byte loads; width is a multiple of 8 (bf16)
-// or 4 (fp32) and every row start is 16-byte aligned.
-__device__ __forceinline__ void stage_rows(float* dst, const void* src, int64_t row_stride,
-                                           int n_rows, int width, bool bf16, int tid,
-                                           int nthreads) {
-  if (bf16) {
-    const int per_row = width / 8;
-    const uint16_t* s = static_cast<const uint16_t*>(src);
-    for (int idx = tid; idx < n_rows * per_row; idx += nthreads) {
-      const int r = idx / per_row, c8 = idx - r * per_row;
-      const uint4 raw = ld_nc_u4(s + r * row_stride + c8 * 8);
-      float* d = dst + r * width + c8 * 8;
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        d[2 * e] = __uint_as_float(w[e] << 16);
-        d[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-      }
-    }
-  } else {
-    const int per_row = width / 4;
-    const float* s = static_cast<const float*>(src);
-    for (int idx = tid; idx < n_rows * per_row; idx += nthreads) {
-      const int r = idx / per_row, c4 = idx - r * per_row;
-      *reinterpret_cast<float4*>(dst + r * width + c4 * 4) = ld_nc_f4(s + r * row_stride + c4 * 4);
-    }
+// Start copying n_rows rows of row_bytes bytes (row r at src + r*src_stride)
+// to dst + r*row_bytes with 16-byte cp.async.
+__device__ __forceinline__ void stage_rows(char* dst, const char* src, int64_t src_stride,
+                                           int n_rows, int row_bytes, int lane) {
+  const int per_row = row_bytes / 16;
+  for (int idx = lane; idx < n_rows * per_row; idx += 32) {
+    const int r = idx / per_row, c = idx - r * per_row;
+    cp_async16(dst + r * row_bytes + c * 16, src + r * src_stride + c * 16);
   }
 }
 
+// x[0..R) = R consecutive values of a staged row (bf16 or fp32), as fp32.
 template <int R>
-__device__ __forceinline__ void load_rows(float (&x)[R], const float* s) {
-  if constexpr (R % 4 == 0) {
+__device__ __forceinline__ void load_rows(float (&x)[R], const char* row, int first, bool bf16) {
+  if (bf16) {
+    const uint16_t* s = reinterpret_cast<const uint16_t*>(row) + first;
+    if constexpr (R % 8 == 0) {
 #pragma unroll
-    for (int m = 0; m < R; m += 4) {
-      const float4 t = *reinterpret_cast<const float4*>(s + m);
-      x[m] = t.x; x[m + 1] = t.y; x[m + 2] = t.z; x[m + 3] = t.w;
-    }
-  } else if constexpr (R % 2 == 0) {
+      for (int m = 0; m < R; m += 8) {
+        const uint4 t = *reinterpret_cast<const uint4*>(s + m);
+        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-    for (int m = 0; m < R; m += 2) {
-      const float2 t = *reinterpret_cast<const float2*>(s + m);
-      x[m] = t.x; x[m + 1] = t.y;
+        for (int e = 0; e < 4; ++e) {
+          x[m + 2 * e] = __uint_as_float(w[e] << 16);
+          x[m + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int m = 0; m < R; ++m) x[m] = bf16_to_f32(s[m]);
     }
   } else {
+    const float* s = reinterpret_cast<const float*>(row) + first;
+    if constexpr (R % 4 == 0) {
 #pragma unroll
-    for (int m = 0; m < R; ++m) x[m] = s[m];
+      for (int m = 0; m < R; m += 4) {
+        const float4 t = *reinterpret_cast<const float4*>(s + m);
+        x[m] = t.x; x[m + 1] = t.y; x[m + 2] = t.z; x[m + 3] = t.w;
+      }
+    } else {
+#pragma unroll
+      for (int m = 0; m < R; ++m) x[m] = s[m];
+    }
   }
 }
 
-template <int DK, int WC, int NW, bool TREE>
-__global__ void __launch_bounds__(NW * 32) verify_kernel(const VerifyParams p) {
-  using S = Shape<DK, WC, NW>;
-  constexpr int R = S::R;
-  extern __shared__ __align__(16) float smem[];
-  const int N = p.N;
-  const SmemPlan plan = smem_plan(N, DK, WC, NW);
-  float* sq = smem + plan.q;
-  float* sk = smem + plan.k;
-  float* sv = smem + plan.v;
-  float* sa = smem + plan.a;
-  float* sb = smem + plan.b;
-  int* spar = reinterpret_cast<int*>(smem + plan.par);
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+template <int DK, int WC, bool TREE>
+__global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
+  using S = Shape<DK, WC>;
+  constexpr int R = S::R;
+  extern __shared__ __align__(16) char smem[];
+  const int N = p.N;
+  const bool bf16 = p.bf16 != 0;
+  const int esz = bf16 ? 2 : 4;
+  const SmemPlan pl = smem_plan(N, DK, WC, esz, TREE, p.pool);
+  char* sq = smem + pl.q;
+  char* sk = smem + pl.k;
+  char* sv = smem + pl.v;
+  float* sa = reinterpret_cast<float*>(smem + pl.a);
+  float* sb = reinterpret_cast<float*>(smem + pl.b);
+  int* spar = reinterpret_cast<int*>(smem + pl.par);
+  int* ssrc = reinterpret_cast<int*>(smem + pl.src);      // tree: -1 regs, >= 0 slot, -2 global
+  int* sstash = reinterpret_cast<int*>(smem + pl.stash);  // tree: slot receiving node n, or -1
+  int* slast = reinterpret_cast<int*>(smem + pl.last);    // tree: last non-adjacent child
+  float* pool = reinterpret_cast<float*>(smem + pl.pool);
+
+  const int lane = threadIdx.x;
   const int cg = lane % S::CG, rl = lane / S::CG;
   const int j0 = blockIdx.x * WC, h = blockIdx.y, b = blockIdx.z;
   const int hk = h / (p.Hv / p.Hk);
   const bool lead = blockIdx.x == 0 && blockIdx.y == 0;  // per-sequence reporting
   const int dv = p.dv;
+  const int row0 = rl * R;
+
+  // ---- stage q, k, v, gates, parents (independent of the slot: issued first)
+  {
+    const int64_t node0 = (int64_t)b * N;
+    const char* qb = static_cast<const char*>(p.q) + ((node0 * p.Hk + hk) * DK) * esz;
+    const char* kb = static_cast<const char*>(p.k) + ((node0 * p.Hk + hk) * DK) * esz;
+    const char* vb = static_cast<const char*>(p.v) + ((node0 * p.Hv + h) * dv + j0) * esz;
+    stage_rows(sk, kb, (int64_t)p.Hk * DK * esz, N, DK * esz, lane);
+    stage_rows(sq, qb, (int64_t)p.Hk * DK * esz, N, DK * esz, lane);
+    stage_rows(sv, vb, (int64_t)p.Hv * dv * esz, N, WC * esz, lane);
+    for (int n = lane; n < N; n += 32) {
+      cp_async4(sa + n, p.alpha + (node0 + n) * p.Hv + h);
+      cp_async4(sb + n, p.beta + (node0 + n) * p.Hv + h);
+      if constexpr (TREE) cp_async4(spar + n, p.parent + node0 + n);
+    }
+  }
 
   const int sl = p.slot != nullptr ? __ldg(p.slot + b) : b;
   if (sl < 0 || sl >= p.n_slots) {
-    if (lead && tid == 0) report(p.status, GDN_ERR_SLOT_RANGE);
+    cp_async_wait_all();
+    if (lead && lane == 0) report(p.status, GDN_ERR_SLOT_RANGE);
     return;
   }
 
-  // ---- initial state (issued first: the longest-latency load)
-  const int row0 = w * S::ROWS_W + rl * R;
-  float H[R][4];
+  // ---- the cached state -> registers
+  float2 H[R][2];
   {
     const float* c0 = p.cache + (int64_t)sl * p.cache_slot_stride + (int64_t)h * DK * dv +
                       (int64_t)row0 * dv + j0 + cg * 4;
 #pragma unroll
     for (int m = 0; m < R; ++m) {
       const float4 t = ld_nc_f4(c0 + (int64_t)m * dv);
-      H[m][0] = t.x; H[m][1] = t.y; H[m][2] = t.z; H[m][3] = t.w;
+      H[m][0] = make_float2(t.x, t.y);
+      H[m][1] = make_float2(t.z, t.w);
     }
   }
-
-  // ---- stage the block's inputs in shared memory
-  {
-    const int nt = NW * 32;
-    const int64_t node0 = (int64_t)b * N;
-    const size_t esz = p.bf16 ? 2 : 4;
-    const char* qb = static_cast<const char*>(p.q) + ((node0 * p.Hk + hk) * DK) * esz;
-    const char* kb = static_cast<const char*>(p.k) + ((node0 * p.Hk + hk) * DK) * esz;
-    const char* vb = static_cast<const char*>(p.v) + ((node0 * p.Hv + h) * dv + j0) * esz;
-    stage_rows(sq, qb, (int64_t)p.Hk * DK, N, DK, p.bf16, tid, nt);
-    stage_rows(sk, kb, (int64_t)p.Hk * DK, N, DK, p.bf16, tid, nt);
-    stage_rows(sv, vb, (int64_t)p.Hv * dv, N, WC, p.bf16, tid, nt);
-    for (int n = tid; n < N; n += nt) {
-      sa[n] = __ldg(p.alpha + (node0 + n) * p.Hv + h);
-      sb[n] = __ldg(p.beta + (node0 + n) * p.Hv + h);
-      if constexpr (TREE) spar[n] = __ldg(p.parent + node0 + n);
-    }
-  }
-  __syncthreads();
+  cp_async_wait_all();
+  __syncwarp();
 
   if constexpr (TREE) {
-    // every warp checks the whole parent array (N <= 64): parent[0] == -1,
-    // 0 <= parent[n] < n; the block leaves as a whole if it is malformed.
+    // parent[0] == -1, 0 <= parent[n] < n; the block leaves otherwise
     bool ok = true;
     for (int n = lane; n < N; n += 32) {
       const int pp = spar[n];
       ok = ok && (n == 0 ? pp == -1 : (pp >= 0 && pp < n));
     }
     if (!__all_sync(FULL, ok)) {
-      if (lead && tid == 0) report(p.status, GDN_ERR_BAD_TREE);
+      if (lead && lane == 0) report(p.status, GDN_ERR_BAD_TREE);
       return;
     }
+  }
+
+  if constexpr (TREE) {
+    // ---- stash plan (greedy over nodes in index order; runs while the
+    //      cached state is still on its way)
+    for (int n = lane; n < N; n += 32) slast[n] = -1;
+    __syncwarp();
+    for (int f = lane; f < N; f += 32) {
+      const int pf = spar[f];
+      if (f > 0 && pf != f - 1) atomicMax(slast + pf, f);
+    }
+    __syncwarp();
+    int par_r[2], last_r[2], stash_r[2] = {-1, -1};
+#pragma unroll
+    for (int s2 = 0; s2 < 2; ++s2) {
+      const int n = lane + 32 * s2;
+      par_r[s2] = n < N ? spar[n] : -1;
+      last_r[s2] = n < N ? slast[n] : -1;
+    }
+    unsigned free_mask = (p.pool >= 32) ? 0xffffffffu : ((1u << p.pool) - 1u);
+    for (int n = 0; n < N; ++n) {
+      const int hi = n >> 5, ln = n & 31;
+      const int pn = __shfl_sync(FULL, hi ? par_r[1] : par_r[0], ln);
+      const int lastn = __shfl_sync(FULL, hi ? last_r[1] : last_r[0], ln);
+      int src = -1;
+      if (n > 0 && pn != n - 1) {
+        const int sp = __shfl_sync(FULL, (pn >> 5) ? stash_r[1] : stash_r[0], pn & 31);
+        const int lastp = __shfl_sync(FULL, (pn >> 5) ? last_r[1] : last_r[0], pn & 31);
+        if (sp >= 0) {
+          src = sp;
+          if (n == lastp) free_mask |= 1u << sp;
+        } else {
+          src = -2;
+        }
+      }
+      int mine = -1;
+      if (lastn >= 0 && free_mask != 0u) {
+        mine = __ffs(free_mask) - 1;
+        free_mask &= free_mask - 1u;
+      }
+      if (lane == ln) {
+        if (hi) stash_r[1] = mine; else stash_r[0] = mine;
+      }
+      if (lane == 0) {
+        ssrc[n] = src;
+        sstash[n] = mine;
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---- u_0 = H0^T k_0
+  float kn[R];  // k of the current node
+  load_rows<R>(kn, sk, row0, bf16);
+  float u[4];
+  {
+    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+      a01 = __ffma2_rn(H[m][0], f2(kn[m]), a01);
+      a23 = __ffma2_rn(H[m][1], f2(kn[m]), a23);
+    }
+    u[0] = a01.x; u[1] = a01.y; u[2] = a23.x; u[3] = a23.y;
+#pragma unroll
+    for (int off = S::CG; off < 32; off <<= 1)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
   }
 
   const int64_t node_stride = (int64_t)p.Hv * DK * dv;
   float* snap_h = p.snap + ((int64_t)b * N * p.Hv + h) * DK * dv + (int64_t)row0 * dv + j0 + cg * 4;
   float* o_h = p.o + ((int64_t)b * N * p.Hv + h) * dv + j0 + cg * 4;
-  float* su = smem + plan.u;
-  float* so = smem + plan.o;
+  // a stash slot holds each lane's R x 4 block lane-major: row m of lane l at
+  // float offset (m*32 + l)*4, so every slot access is bank-conflict free
+  const int slot_floats = DK * WC;
 
   for (int n = 0; n < N; ++n) {
+    // (a) a tree node whose source is not node n-1 starts from its parent's
+    //     stashed (or, if the pool ran out, re-read) state; its u is reduced here
     if constexpr (TREE) {
-      const int src = spar[n];
-      if (n > 0 && src != n - 1) {  // uniform over the block
-        const float* from = snap_h + (int64_t)src * node_stride;
+      if (n > 0 && spar[n] != n - 1) {
+        const int src = ssrc[n];
+        if (src >= 0) {
+          const float* rs = pool + src * slot_floats + lane * 4;
+#pragma unroll
+          for (int m = 0; m < R; ++m) {
+            const float4 t = *reinterpret_cast<const float4*>(rs + m * 128);
+            H[m][0] = make_float2(t.x, t.y);
+            H[m][1] = make_float2(t.z, t.w);
+          }
+        } else {
+          const float* from = snap_h + (int64_t)spar[n] * node_stride;
+#pragma unroll
+          for (int m = 0; m < R; ++m) {
+            const float4 t = ld_cg_f4(from + (int64_t)m * dv);
+            H[m][0] = make_float2(t.x, t.y);
+            H[m][1] = make_float2(t.z, t.w);
+          }
+        }
+        float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int m = 0; m < R; ++m) {
-          const float4 t = ld_cg_f4(from + (int64_t)m * dv);
-          H[m][0] = t.x; H[m][1] = t.y; H[m][2] = t.z; H[m][3] = t.w;
+          a01 = __ffma2_rn(H[m][0], f2(kn[m]), a01);
+          a23 = __ffma2_rn(H[m][1], f2(kn[m]), a23);
         }
+        u[0] = a01.x; u[1] = a01.y; u[2] = a23.x; u[3] = a23.y;
+#pragma unroll
+        for (int off = S::CG; off < 32; off <<= 1)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
       }
     }
-    float kr[R], qr[R];
-    load_rows<R>(kr, sk + n * DK + row0);
-    load_rows<R>(qr, sq + n * DK + row0);
-    const float4 vv = *reinterpret_cast<const float4*>(sv + n * WC + cg * 4);
+
+    const bool has_next = n + 1 < N;
+    const bool next_chain = !TREE || (has_next && spar[n + 1] == n);
+    float knx[R];  // k of node n+1
+    if (has_next) {
+      load_rows<R>(knx, sk + (n + 1) * DK * esz, row0, bf16);
+    } else {
+#pragma unroll
+      for (int m = 0; m < R; ++m) knx[m] = 0.f;
+    }
+    float qr[R];
+    load_rows<R>(qr, sq + n * DK * esz, row0, bf16);
+    float vj[4];
+    load_rows<4>(vj, sv + n * WC * esz, cg * 4, bf16);
     const float al = sa[n], be = sb[n];
 
-    // u = S k over this lane's rows, then over the row lanes (and warps)
-    float u[4] = {0.f, 0.f, 0.f, 0.f};
+    // (c) partial sums for u_{n+1} when node n+1 continues from node n:
+    //     from the registers before node n's update
+    float2 w01 = make_float2(0.f, 0.f), w23 = make_float2(0.f, 0.f);
+    float kk = 0.f;
+    if (next_chain) {
 #pragma unroll
-    for (int m = 0; m < R; ++m)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) u[c] = fmaf(H[m][c], kr[m], u[c]);
-#pragma unroll
-    for (int off = S::CG; off < 32; off <<= 1)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
-    if constexpr (NW > 1) {
-      float* buf = su + (n & 1) * NW * WC;
-      if (rl == 0) st_f4(buf + w * WC + cg * 4, u[0], u[1], u[2], u[3]);
-      __syncthreads();
-      const float4 t0 = *reinterpret_cast<const float4*>(buf + cg * 4);
-      u[0] = t0.x; u[1] = t0.y; u[2] = t0.z; u[3] = t0.w;
-#pragma unroll
-      for (int ww = 1; ww < NW; ++ww) {
-        const float4 t = *reinterpret_cast<const float4*>(buf + ww * WC + cg * 4);
-        u[0] += t.x; u[1] += t.y; u[2] += t.z; u[3] += t.w;
+      for (int m = 0; m < R; ++m) {
+        w01 = __ffma2_rn(H[m][0], f2(knx[m]), w01);
+        w23 = __ffma2_rn(H[m][1], f2(knx[m]), w23);
+        kk = fmaf(kn[m], knx[m], kk);
       }
     }
 
-    // delta = beta (v - alpha u);  H' = alpha H + k delta^T;  o = S' q
-    const float vj[4] = {vv.x, vv.y, vv.z, vv.w};
-    float d[4], o[4];
+    // (d) delta_n, update, output partial
+    float d[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      d[c] = be * (vj[c] - al * u[c]);
-      o[c] = 0.f;
+    for (int c = 0; c < 4; ++c) d[c] = be * (vj[c] - al * u[c]);
+    const float2 d01 = make_float2(d[0], d[1]), d23 = make_float2(d[2], d[3]);
+    const float2 al2 = f2(al);
+    float2 o01 = make_float2(0.f, 0.f), o23 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+      H[m][0] = __ffma2_rn(f2(kn[m]), d01, __fmul2_rn(al2, H[m][0]));
+      H[m][1] = __ffma2_rn(f2(kn[m]), d23, __fmul2_rn(al2, H[m][1]));
+      o01 = __ffma2_rn(H[m][0], f2(qr[m]), o01);
+      o23 = __ffma2_rn(H[m][1], f2(qr[m]), o23);
     }
+    if constexpr (TREE) {
+      // a later, non-adjacent child continues from node n: stash H_n
+      const int st = sstash[n];
+      if (st >= 0) {
+        float* to = pool + st * slot_floats + lane * 4;
 #pragma unroll
-    for (int m = 0; m < R; ++m)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        H[m][c] = fmaf(kr[m], d[c], al * H[m][c]);
-        o[c] = fmaf(H[m][c], qr[m], o[c]);
+        for (int m = 0; m < R; ++m)
+          *reinterpret_cast<float4*>(to + m * 128) =
+              make_float4(H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
       }
+    }
+
+    // (e) one shuffle tree for the 4 + 1 + 4 column sums
+    float red[9] = {w01.x, w01.y, w23.x, w23.y, kk, o01.x, o01.y, o23.x, o23.y};
 #pragma unroll
     for (int off = S::CG; off < 32; off <<= 1)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) o[c] += __shfl_xor_sync(FULL, o[c], off);
-    if constexpr (NW == 1) {
-      if (rl == 0) st_f4(o_h + (int64_t)n * p.Hv * dv, o[0], o[1], o[2], o[3]);
-    } else {
-      if (rl == 0) st_f4(so + (n * NW + w) * WC + cg * 4, o[0], o[1], o[2], o[3]);
-    }
+      for (int i = 0; i < 9; ++i) red[i] += __shfl_xor_sync(FULL, red[i], off);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) u[c] = next_chain ? fmaf(al, red[c], d[c] * red[4]) : red[c];
 
-    // persist S_n
+    // (f) persist
+    if (rl == 0) st_f4(o_h + (int64_t)n * p.Hv * dv, red[5], red[6], red[7], red[8]);
     float* dst = snap_h + (int64_t)n * node_stride;
 #pragma unroll
-    for (int m = 0; m < R; ++m) st_f4(dst + (int64_t)m * dv, H[m][0], H[m][1], H[m][2], H[m][3]);
-  }
-
-  if constexpr (NW > 1) {
-    __syncthreads();
-    constexpr int C4 = WC / 4;
-    float* ob = p.o + ((int64_t)b * N * p.Hv + h) * dv + j0;
-    for (int idx = tid; idx < N * C4; idx += NW * 32) {
-      const int n = idx / C4, c4 = idx - n * C4;
-      float4 acc = *reinterpret_cast<const float4*>(so + (n * NW) * WC + c4 * 4);
+    for (int m = 0; m < R; ++m) st_f4(dst + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
 #pragma unroll
-      for (int ww = 1; ww < NW; ++ww) {
-        const float4 t = *reinterpret_cast<const float4*>(so + (n * NW + ww) * WC + c4 * 4);
-        acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
-      }
-      *reinterpret_cast<float4*>(ob + (int64_t)n * p.Hv * dv + c4 * 4) = acc;
-    }
+    for (int m = 0; m < R; ++m) kn[m] = knx[m];
   }
 
   if constexpr (TREE) {
-    // node depths (root = 1), written once per sequence, off the critical path
-    if (lead && w == 0 && p.depth_out != nullptr) {
+    // node depths (root = 1), written once per sequence
+    if (lead && p.depth_out != nullptr) {
       for (int n = lane; n < N; n += 32) {
         int dpt = 1;
         for (int m = n; m > 0; m = spar[m]) ++dpt;
@@ -317,37 +432,36 @@ __global__ void __launch_bounds__(NW * 32) verify_kernel(const VerifyParams p) {
   }
 }
 
-template <int DK, int WC, int NW, bool TREE>
+template <int DK, int WC, bool TREE>
 int launch(const VerifyParams& p, int B, cudaStream_t stream) {
-  const SmemPlan plan = smem_plan(p.N, DK, WC, NW);
-  const size_t smem = (size_t)plan.total * sizeof(float);
-  auto kern = verify_kernel<DK, WC, NW, TREE>;
+  VerifyParams q = p;
+  q.pool = TREE ? tree_pool_slots(p.N, DK, WC, p.bf16 ? 2 : 4) : 0;
+  const SmemPlan pl = smem_plan(p.N, DK, WC, p.bf16 ? 2 : 4, TREE, q.pool);
+  const size_t smem = (size_t)pl.total;
+  if (smem > 227 * 1024) return GDN_ERR_UNSUPPORTED;
+  auto kern = verify_kernel<DK, WC, TREE>;
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return GDN_ERR_CUDA;
   }
   const dim3 grid(p.dv / WC, p.Hv, B);
-  kern<<<grid, NW * 32, smem, stream>>>(p);
+  kern<<<grid, 32, smem, stream>>>(q);
   return launch_status();
 }
 
 template <bool TREE>
-int dispatch(const VerifyParams& p, int B, int dk, int wc, int nw, cudaStream_t s) {
-#define GDN_CASE(DK_, WC_, NW_) \
-  if (dk == DK_ && wc == WC_ && nw == NW_) return launch<DK_, WC_, NW_, TREE>(p, B, s);
-  GDN_CASE(128, 16, 1)
-  GDN_CASE(128, 8, 1)
-  GDN_CASE(128, 16, 2)
-  GDN_CASE(128, 32, 2)
-  GDN_CASE(128, 16, 4)
-  GDN_CASE(128, 32, 4)
-  GDN_CASE(64, 16, 1)
-  GDN_CASE(64, 8, 1)
-  GDN_CASE(32, 16, 1)
-  GDN_CASE(32, 8, 1)
-  GDN_CASE(16, 16, 1)
-  GDN_CASE(16, 8, 1)
+int dispatch(const VerifyParams& p, int B, int dk, int wc, cudaStream_t s) {
+#define GDN_CASE(DK_, WC_) \
+  if (dk == DK_ && wc == WC_) return launch<DK_, WC_, TREE>(p, B, s);
+  GDN_CASE(128, 16)
+  GDN_CASE(128, 8)
+  GDN_CASE(64, 16)
+  GDN_CASE(64, 8)
+  GDN_CASE(32, 16)
+  GDN_CASE(32, 8)
+  GDN_CASE(16, 16)
+  GDN_CASE(16, 8)
 #undef GDN_CASE
   return GDN_ERR_UNSUPPORTED;
 }
@@ -355,15 +469,12 @@ int dispatch(const VerifyParams& p, int B, int dk, int wc, int nw, cudaStream_t 
 }  // namespace
 
 bool verify_tile_supported(int dk, int wc, int nw) {
-  if (dk == 128) {
-    return (wc == 16 && nw == 1) || (wc == 8 && nw == 1) || (wc == 16 && nw == 2) ||
-           (wc == 32 && nw == 2) || (wc == 16 && nw == 4) || (wc == 32 && nw == 4);
-  }
-  return (dk == 64 || dk == 32 || dk == 16) && nw == 1 && (wc == 16 || wc == 8);
+  return (dk == 128 || dk == 64 || dk == 32 || dk == 16) && (wc == 16 || wc == 8) && nw == 1;
 }
 
 int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, int wc,
                   int nw, cudaStream_t stream) {
+  (void)nw;
   VerifyParams p{};
   p.q = a->q;
   p.k = a->k;
@@ -384,8 +495,8 @@ int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   p.Hv = a->Hv;
   p.dv = a->dv;
   p.bf16 = a->in_dtype == GDN_BF16;
-  if (parent != nullptr) return dispatch<true>(p, a->B, a->dk, wc, nw, stream);
-  return dispatch<false>(p, a->B, a->dk, wc, nw, stream);
+  if (parent != nullptr) return dispatch<true>(p, a->B, a->dk, wc, stream);
+  return dispatch<false>(p, a->B, a->dk, wc, stream);
 }
 
 }  // namespace gdn

@@ -83,8 +83,8 @@ typedef enum gdn_dtype {
  *   status        optional device int32 error word (see above)
  *   tile_cols, row_warps
  *                 0 = automatic; otherwise the d_v columns owned by one
- *                 thread block (8, 16 or 32) and the warps that split its
- *                 d_k rows (1, 2 or 4).  A pure performance hint.
+ *                 thread block (8 or 16) and the warps that split its d_k
+ *                 rows (1).  A pure performance hint.
  *
  * Supported sizes: dk in {16, 32, 64, 128}; dv a multiple of 16, <= 1024;
  * 1 <= N <= 64; Hv a multiple of Hk; B >= 0 (B = 0 launches nothing).

@@ -422,10 +422,58 @@ def check_rounds_equal_sequential():
     _close(cache[1], sT, 1e-13, "rounds of verify+commit vs sequential")
 
 
+def block_form_reference(H0, K, V, Q, alpha, beta, parent):
+    """The whole block at once (float64, one value head): with G(n) the sum of
+    log alpha over the root-to-n path and the deltas solved first from
+        delta_n = beta_n v_n - beta_n e^G(n) H0^T k_n
+                  - sum_{m strict ancestor of n} beta_n e^(G(n)-G(m)) (k_m . k_n) delta_m,
+    every state is H_n = e^G(n) H0 + sum_{m on the path} e^(G(n)-G(m)) k_m delta_m^T."""
+    N = K.shape[0]
+    G = np.zeros(N)
+    anc = [[] for _ in range(N)]
+    for n in range(N):
+        p = parent[n]
+        G[n] = np.log(alpha[n]) + (G[p] if p >= 0 else 0.0)
+        anc[n] = (anc[p] + [p]) if p >= 0 else []
+    X = K @ H0
+    KK = K @ K.T
+    D = np.zeros((N, V.shape[1]))
+    for n in range(N):
+        D[n] = beta[n] * V[n] - beta[n] * np.exp(G[n]) * X[n]
+        for m in anc[n]:
+            D[n] -= beta[n] * np.exp(G[n] - G[m]) * KK[n, m] * D[m]
+    S = np.array([np.exp(G[n]) * H0 + sum(np.exp(G[n] - G[m]) * np.outer(K[m], D[m])
+                                          for m in anc[n] + [n]) for n in range(N)])
+    return S, np.einsum("nij,ni->nj", S, Q)
+
+
+def check_block_form_equals_recurrence():
+    """All deltas first, then every state from the cached one: the same states
+    and outputs as the node-by-node recurrence, for chains and trees."""
+    rng = np.random.default_rng(24)
+    for tree in (False, True):
+        N, dk, dv = 12, 8, 6
+        parent = np.array([-1] + [int(rng.integers(0, i)) if tree else i - 1
+                                  for i in range(1, N)], np.int32)
+        K = rng.standard_normal((N, dk))
+        K /= np.linalg.norm(K, axis=1, keepdims=True)
+        Q, V = rng.standard_normal((N, dk)), rng.standard_normal((N, dv))
+        al, be = rng.uniform(0.5, 1.0, N), rng.uniform(0.0, 1.0, N)
+        H0 = rng.standard_normal((dk, dv))
+        S, O = block_form_reference(H0, K, V, Q, al, be, parent)
+        st, snap, o = oracle.verify(Q[None, :, None], K[None, :, None], V[None, :, None],
+                                    al[None, :, None], be[None, :, None], H0[None, None],
+                                    np.zeros(1, np.int32), parent[None] if tree else None, B=1,
+                                    N=N, Hk=1, Hv=1, dk=dk, dv=dv)
+        assert st == oracle.OK
+        _close(S, snap[0, :, 0], 1e-12, "block form states")
+        _close(O, o[0, :, 0], 1e-12, "block form outputs")
+
+
 ALL_CHECKS = [
     check_golden_hand_example, check_identity_gate, check_delta_rule_closed_form,
     check_zero_decay, check_scalar_closed_form, check_linearity, check_column_independence,
     check_contraction, check_tree_matches_chain_and_paths, check_exact_rational_bruteforce,
     check_tree_depth_and_validation, check_commit, check_chunked_equals_step,
-    check_rounds_equal_sequential,
+    check_rounds_equal_sequential, check_block_form_equals_recurrence,
 ]

@@ -37,7 +37,7 @@ def test_tiny_chain_verify_and_commit(gpu_lib):
     assert_close(got, snap[0, 2], "committed state vs oracle")
 
 
-@pytest.mark.parametrize("tile", [(0, 0), (8, 1), (16, 1), (16, 2), (32, 2), (16, 4), (32, 4)])
+@pytest.mark.parametrize("tile", [(0, 0), (16, 1), (8, 1)])
 def test_chain16_full(gpu_lib, tile):
     """Single-sequence chain of 16, 16 q/k heads, 48 value heads, d = 128, bf16
     inputs; every output and every snapshot, in every tile shape."""
@@ -49,11 +49,12 @@ def test_chain16_full(gpu_lib, tile):
     assert_close(out["snap"], snap, "chain16 snapshots")
 
 
-def test_tree22_full(gpu_lib):
+@pytest.mark.parametrize("tile", [(0, 0), (16, 1), (8, 1)])
+def test_tree22_full(gpu_lib, tile):
     """DDTree of 22 nodes: per-node states from the parent, depths bit-exact,
     commit of the accepted node."""
     inp = synthetic.tree22()
-    out = verify_on_gpu(gpu_lib, inp)
+    out = verify_on_gpu(gpu_lib, inp, tile_cols=tile[0], row_warps=tile[1])
     snap, o = _oracle(inp)
     assert out["status"] == 0
     assert_close(out["o"], o, "tree22 o")
@@ -69,7 +70,7 @@ def test_tree22_full(gpu_lib):
     assert np.array_equal(got, out["snap"][0, inp["accept"][0]])
 
 
-@pytest.mark.parametrize("tile", [(16, 1), (32, 4), (16, 2)])
+@pytest.mark.parametrize("tile", [(16, 1), (8, 1)])
 def test_single_path_tree_equals_chain(gpu_lib, tile):
     inp = synthetic.chain16(seed=99)
     a = verify_on_gpu(gpu_lib, inp, tree=False, tile_cols=tile[0], row_warps=tile[1])
