@@ -154,15 +154,19 @@ int gdn_commit_accepted(const float* snapshots, int64_t snap_layer_stride,
  * Chunked prefill of one sequence of T tokens: the same recurrence, evaluated
  * chunk by chunk in the WY / UT-transform form on tensor cores.
  *
- *   q, k   [T][Hk][dk]  in_dtype;  v [T][Hv][dv] in_dtype
+ *   q, k   [T][Hk][dk]  bf16 (in_dtype must be GDN_BF16);  v [T][Hv][dv] bf16
  *   alpha, beta [T][Hv] fp32
  *   state  [Hv][dk][dv] fp32, in: the state before token 0, out: after token T-1
  *   o      [T][Hv][dv] fp32 output
  *   workspace  device scratch of at least gdn_prefill_workspace_bytes(...) bytes,
  *              owned by the caller, contents need not be initialised
  *
- * Supported: dk = dv = 128, chunk = 64, T >= 0 (any T; the last chunk may be
- * partial).  GDN_ERR_WORKSPACE if the workspace is NULL or too small.
+ * Supported: dk = dv = 128, chunk = 64, bf16 inputs, T >= 0 (any T; the last
+ * chunk may be partial).  GDN_ERR_WORKSPACE if the workspace is NULL or too
+ * small.  Two kernels run on `stream`: a parallel pass over (chunk, q/k head)
+ * that fills the workspace, then the sequential pass over the chunks of each
+ * value head; the workspace may be reused once the call's work has finished
+ * on the stream.
  */
 size_t gdn_prefill_workspace_bytes(int32_t T, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
                                    int32_t chunk);
