@@ -27,6 +27,8 @@ GDN_ERR_BAD_TREE = -5
 GDN_ERR_ACCEPT_RANGE = -6
 GDN_ERR_SLOT_RANGE = -7
 GDN_ERR_WORKSPACE = -8
+GDN_ERR_SCRATCH_LIMIT = -9
+PREFILL_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 GDN_F32 = 0
 GDN_BF16 = 1
@@ -78,6 +80,9 @@ def load(path: str | None = None):
     lib.gdn_prefill_chunked.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, P, P,
                                         P, sz, P]
     lib.gdn_prefill_chunked.restype = ctypes.c_int
+    lib.gdn_prefill_chunked_noalloc.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32,
+                                                P, P, P]
+    lib.gdn_prefill_chunked_noalloc.restype = ctypes.c_int
     lib.gdn_status_string.argtypes = [ctypes.c_int]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_version.argtypes = []
@@ -203,3 +208,17 @@ def gdn_prefill_chunked(q, k, v, alpha, beta, state, o, workspace=None, *, chunk
                                       _ptr(beta), T, Hk, Hv, dk, dv, chunk, _ptr(state), _ptr(o),
                                       _ptr(workspace), wbytes, _stream(stream)),
            "gdn_prefill_chunked")
+
+
+def gdn_prefill_chunked_noalloc(q, k, v, alpha, beta, state, o, *, chunk=64, stream=None):
+    """gdn_prefill_chunked on the library's built-in device scratch, for callers
+    that cannot allocate device memory (no workspace argument).  Problems whose
+    workspace would exceed PREFILL_NOALLOC_SCRATCH_BYTES raise GdnError with
+    GDN_ERR_SCRATCH_LIMIT; calls that overlap on the GPU share the scratch and
+    must be serialised by the caller."""
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    _check(load().gdn_prefill_chunked_noalloc(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q),
+                                              _ptr(alpha), _ptr(beta), T, Hk, Hv, dk, dv, chunk,
+                                              _ptr(state), _ptr(o), _stream(stream)),
+           "gdn_prefill_chunked_noalloc")

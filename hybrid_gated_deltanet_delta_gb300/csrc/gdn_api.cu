@@ -124,6 +124,28 @@ int gdn_prefill_chunked(const void* q, const void* k, const void* v, int32_t in_
                              state, o, workspace, static_cast<cudaStream_t>(stream));
 }
 
+int gdn_prefill_chunked_noalloc(const void* q, const void* k, const void* v, int32_t in_dtype,
+                                const float* alpha, const float* beta, int32_t T, int32_t Hk,
+                                int32_t Hv, int32_t dk, int32_t dv, int32_t chunk, float* state,
+                                float* o, void* stream) {
+  if (T < 0 || Hk < 1 || Hv < 1 || Hv % Hk != 0) return GDN_ERR_INVALID_ARG;
+  if (in_dtype != GDN_F32 && in_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (dk != 128 || dv != 128 || chunk != 64 || in_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  if (Hv > 65535) return GDN_ERR_UNSUPPORTED;
+  if (state == nullptr) return GDN_ERR_INVALID_ARG;
+  if (!gdn::aligned16(state)) return GDN_ERR_MISALIGNED;
+  if (T == 0) return GDN_OK;
+  const void* need16[] = {q, k, v, o};
+  for (const void* p : need16) {
+    if (p == nullptr) return GDN_ERR_INVALID_ARG;
+    if (!gdn::aligned16(p)) return GDN_ERR_MISALIGNED;
+  }
+  if (alpha == nullptr || beta == nullptr) return GDN_ERR_INVALID_ARG;
+  if (!ok_ptr4(alpha) || !ok_ptr4(beta)) return GDN_ERR_MISALIGNED;
+  return gdn::launch_prefill_noalloc(q, k, v, true, alpha, beta, T, Hk, Hv, dk, dv, chunk, state,
+                                     o, static_cast<cudaStream_t>(stream));
+}
+
 const char* gdn_status_string(int status) {
   switch (status) {
     case GDN_OK: return "GDN_OK";
@@ -135,6 +157,7 @@ const char* gdn_status_string(int status) {
     case GDN_ERR_ACCEPT_RANGE: return "GDN_ERR_ACCEPT_RANGE";
     case GDN_ERR_SLOT_RANGE: return "GDN_ERR_SLOT_RANGE";
     case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+    case GDN_ERR_SCRATCH_LIMIT: return "GDN_ERR_SCRATCH_LIMIT";
     default: return "GDN_ERR_UNKNOWN";
   }
 }

@@ -24,4 +24,9 @@ int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const
                    const float* beta, int T, int Hk, int Hv, int dk, int dv, int chunk,
                    float* state, float* o, void* workspace, cudaStream_t stream);
 
+// gdn_prefill_chunked on the library's built-in scratch (no allocation).
+int launch_prefill_noalloc(const void* q, const void* k, const void* v, bool bf16,
+                           const float* alpha, const float* beta, int T, int Hk, int Hv, int dk,
+                           int dv, int chunk, float* state, float* o, cudaStream_t stream);
+
 }  // namespace gdn

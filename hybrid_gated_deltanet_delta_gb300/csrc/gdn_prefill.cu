@@ -30,6 +30,8 @@
 // them costs ~1% of the output RMS at this size.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
 
@@ -540,6 +542,52 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// Built-in scratch for gdn_prefill_chunked_noalloc: a file-scope device array,
+// so that callers who cannot allocate device memory still get the chunked
+// prefill.  Every GPU that loads the library holds it until the process exits.
+// Host code must not hand the symbol itself to a kernel (on the host it names
+// a stand-in, not device memory): its device address is looked up once per
+// device with cudaGetSymbolAddress and cached.
+static __device__ __align__(256) char g_prefill_scratch[GDN_PREFILL_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 256;
+
+// Device address of g_prefill_scratch on the current device (set up on the
+// first call for that device).  Returns GDN_OK or GDN_ERR_CUDA.
+int scratch_on_current_device(void** ptr) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess || p == nullptr)
+      return GDN_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return GDN_OK;
+}
+
+}  // namespace
+
+int launch_prefill_noalloc(const void* q, const void* k, const void* v, bool bf16,
+                           const float* alpha, const float* beta, int T, int Hk, int Hv, int dk,
+                           int dv, int chunk, float* state, float* o, cudaStream_t stream) {
+  if (!bf16 || dk != DK || dv != DV || chunk != C) return GDN_ERR_UNSUPPORTED;
+  const size_t need = prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk);
+  if (need > (size_t)GDN_PREFILL_NOALLOC_SCRATCH_BYTES) return GDN_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  const int st = scratch_on_current_device(&scratch);
+  if (st != GDN_OK) return st;
+  return launch_prefill(q, k, v, bf16, alpha, beta, T, Hk, Hv, dk, dv, chunk, state, o, scratch,
+                        stream);
+}
 
 size_t prefill_workspace_bytes(int T, int Hk, int Hv, int dk, int dv, int chunk) {
   (void)Hk;

@@ -59,7 +59,8 @@ typedef enum gdn_status {
   GDN_ERR_BAD_TREE = -5,      /* device: parent[0] != -1 or parent[n] outside [0, n) */
   GDN_ERR_ACCEPT_RANGE = -6,  /* device: accept index outside [0, N) */
   GDN_ERR_SLOT_RANGE = -7,    /* device: slot outside [0, n_slots) */
-  GDN_ERR_WORKSPACE = -8      /* workspace missing or smaller than required */
+  GDN_ERR_WORKSPACE = -8,     /* workspace missing or smaller than required */
+  GDN_ERR_SCRATCH_LIMIT = -9  /* problem too large for the built-in scratch of the _noalloc call */
 } gdn_status;
 
 typedef enum gdn_dtype {
@@ -175,6 +176,38 @@ int gdn_prefill_chunked(const void* q, const void* k, const void* v, int32_t in_
                         const float* alpha, const float* beta, int32_t T, int32_t Hk, int32_t Hv,
                         int32_t dk, int32_t dv, int32_t chunk, float* state, float* o,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gdn_prefill_chunked without a workspace argument, for callers that cannot
+ * allocate device memory themselves: for example a plugin whose host engine
+ * owns every device allocation and offers it no allocator, or a code path
+ * where the implicit synchronisation of cudaMalloc is not acceptable and no
+ * buffer was reserved up front.  (The source pages have no counterpart to this
+ * call; it is an addition of this library.)
+ *
+ * The call computes exactly what gdn_prefill_chunked computes, with the same
+ * arguments minus `workspace`/`workspace_bytes`; the scratch it needs lives in
+ * a device array built into the library of GDN_PREFILL_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) per GPU that loads the library, held until the process exits.
+ * Limit: ceil(T/64) * Hv * 33280 bytes must fit, i.e. ceil(T/64) * Hv <= 504
+ * (T <= 640 tokens at 48 value heads); larger problems return
+ * GDN_ERR_SCRATCH_LIMIT without launching anything.  The library allocates
+ * nothing here: no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * The first call on a device looks up the device address of the scratch
+ * array (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  All calls share the one array, which keeps
+ * the previous call's contents (nothing in it needs clearing: the first kernel
+ * of a call writes every byte the second kernel reads).  Calls that overlap on
+ * the GPU -- on different streams, or from different host threads -- race on
+ * the shared scratch and must be serialised by the caller.
+ */
+#define GDN_PREFILL_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+int gdn_prefill_chunked_noalloc(const void* q, const void* k, const void* v, int32_t in_dtype,
+                                const float* alpha, const float* beta, int32_t T, int32_t Hk,
+                                int32_t Hv, int32_t dk, int32_t dv, int32_t chunk, float* state,
+                                float* o, void* stream);
 
 /* Human-readable name of a gdn_status value (static string, never NULL). */
 const char* gdn_status_string(int status);
