@@ -58,18 +58,97 @@ __device__ __forceinline__ uint32_t ld32(const char* p) {
 }
 
 // ------------------------------------------------------------------- prep
+constexpr int PREP_THREADS = 256;
+constexpr int TS = 65;  // fp32 row stride of the 64 x 64 work matrices (bank spread)
 constexpr int PREP_K = 0;
 constexpr int PREP_Q = PREP_K + C * KS;
 constexpr int PREP_KK = PREP_Q + C * KS;
 constexpr int PREP_QK = PREP_KK + C * C * 4;
 constexpr int PREP_A = PREP_QK + C * C * 4;
-constexpr int PREP_T = PREP_A + C * 65 * 4;
-constexpr int PREP_LG = PREP_T + C * 65 * 4;
+// T and the product scratch reuse the K / Q staging area, dead once K K^T and
+// Q K^T are formed
+constexpr int PREP_T = PREP_K;
+constexpr int PREP_S = PREP_T + C * TS * 4;
+static_assert(PREP_S + C * TS * 4 <= PREP_KK, "T and S must fit in the K/Q staging area");
+constexpr int PREP_GATE = PREP_A + C * TS * 4;  // [2 buffers][alpha 64, beta 64]
+constexpr int PREP_LG = PREP_GATE + 2 * 2 * C * 4;
 constexpr int PREP_G = PREP_LG + C * 4;
 constexpr int PREP_B = PREP_G + C * 4;
 constexpr int PREP_SMEM = PREP_B + C * 4;
 
-__global__ void __launch_bounds__(128)
+// C = sign * X Y for M x N outputs over K terms (all three row stride TS);
+// `nthreads` threads starting at `tid` = 0 share the 2 x 2 output tiles.
+__device__ __forceinline__ void mm_tiles(float* Cm, const float* X, const float* Y, int M, int N,
+                                         int K, float sign, int tid, int nthreads) {
+  const int tn = N / 2;
+  for (int tile = tid; tile < (M / 2) * tn; tile += nthreads) {
+    const int r = 2 * (tile / tn), c = 2 * (tile % tn);
+    float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+    for (int k = 0; k < K; ++k) {
+      const float x0 = X[r * TS + k], x1 = X[(r + 1) * TS + k];
+      const float y0 = Y[k * TS + c], y1 = Y[k * TS + c + 1];
+      a00 = fmaf(x0, y0, a00); a01 = fmaf(x0, y1, a01);
+      a10 = fmaf(x1, y0, a10); a11 = fmaf(x1, y1, a11);
+    }
+    Cm[r * TS + c] = sign * a00;
+    Cm[r * TS + c + 1] = sign * a01;
+    Cm[(r + 1) * TS + c] = sign * a10;
+    Cm[(r + 1) * TS + c + 1] = sign * a11;
+  }
+}
+
+// T = (I + A)^-1 for a strictly lower-triangular 64 x 64 A (row stride TS) by
+// recursive doubling of the block inverse
+//     [[L11, 0], [L21, L22]]^-1 = [[L11^-1, 0], [-L22^-1 L21 L11^-1, L22^-1]]:
+// the four 16 x 16 diagonal blocks by forward substitution held in registers
+// (one column per lane), then the 16 -> 32 and 32 -> 64 merges as two products
+// each.  S is 64 x 64 scratch.
+__device__ void invert_unit_lower(const float* A, float* T, float* S, int tid) {
+  const int w = tid >> 5, lane = tid & 31;
+  if (w < 2) {
+    const int b0 = 16 * (2 * w + (lane >> 4)), j = lane & 15;
+    float tc[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      float acc = 0.f;
+#pragma unroll
+      for (int r = 0; r < t; ++r) acc = fmaf(A[(b0 + t) * TS + b0 + r], tc[r], acc);
+      tc[t] = t < j ? 0.f : (t == j ? 1.f : -acc);
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) T[(b0 + t) * TS + b0 + j] = tc[t];
+  }
+  // blocks above the diagonal are zero
+  for (int idx = tid; idx < C * C; idx += PREP_THREADS) {
+    const int t = idx >> 6, s = idx & 63;
+    if ((s >> 4) > (t >> 4)) T[t * TS + s] = 0.f;
+  }
+  __syncthreads();
+  // 16 -> 32: T[b+16.., b..] = -T[b+16.., b+16..] (A[b+16.., b..] T[b.., b..]), b = 0, 32
+  {
+    const int half = tid >> 7, ht = tid & 127, b = 32 * half;
+    mm_tiles(S + (b + 16) * TS + b, A + (b + 16) * TS + b, T + b * TS + b, 16, 16, 16, 1.f, ht,
+             128);
+    __syncthreads();
+    mm_tiles(T + (b + 16) * TS + b, T + (b + 16) * TS + b + 16, S + (b + 16) * TS + b, 16, 16,
+             16, -1.f, ht, 128);
+    __syncthreads();
+  }
+  // 32 -> 64: T[32.., 0..] = -T[32.., 32..] (A[32.., 0..] T[0.., 0..])
+  mm_tiles(S + 32 * TS, A + 32 * TS, T, 32, 32, 32, 1.f, tid, PREP_THREADS);
+  __syncthreads();
+  mm_tiles(T + 32 * TS, T + 32 * TS + 32, S + 32 * TS, 32, 32, 32, -1.f, tid, PREP_THREADS);
+  __syncthreads();
+}
+
+__device__ __forceinline__ void cp_async4_zfill(void* smem, const void* gmem, bool valid) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  const int n = valid ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(s), "l"(gmem), "r"(n)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(PREP_THREADS)
 prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
             const float* __restrict__ alpha, const float* __restrict__ beta, int T, int Hk,
             int Hv, char* __restrict__ ws) {
@@ -80,6 +159,8 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
   float* sqk = reinterpret_cast<float*>(smem + PREP_QK);
   float* sa = reinterpret_cast<float*>(smem + PREP_A);
   float* st = reinterpret_cast<float*>(smem + PREP_T);
+  float* ss = reinterpret_cast<float*>(smem + PREP_S);
+  float* sgate = reinterpret_cast<float*>(smem + PREP_GATE);
   float* slg = reinterpret_cast<float*>(smem + PREP_LG);
   float* sg = reinterpret_cast<float*>(smem + PREP_G);
   float* sb = reinterpret_cast<float*>(smem + PREP_B);
@@ -89,67 +170,76 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g8 = lane >> 2, t4 = lane & 3;
 
+  // gates of value head hk*G + j into gate buffer j & 1 (rows past the end read as 0)
+  auto stage_gates = [&](int j) {
+    float* dst = sgate + (j & 1) * 2 * C;
+    const int h = hk * G + j;
+    if (tid < 2 * C) {
+      const int t = tid & 63;
+      const bool valid = t < nv;
+      const float* src = (tid < C ? alpha : beta) + (size_t)(t0 + (valid ? t : 0)) * Hv + h;
+      cp_async4_zfill(dst + tid, src, valid);
+    }
+  };
+
   // K and Q rows of the chunk (rows past the end of the sequence read as zero)
-  for (int idx = tid; idx < C * 16; idx += 128) {
+  for (int idx = tid; idx < C * 16; idx += PREP_THREADS) {
     const int r = idx >> 4, ch = idx & 15;
     const bool valid = r < nv;
     const size_t src = ((size_t)(t0 + (valid ? r : 0)) * Hk + hk) * DK + ch * 8;
     cp_async16_zfill(sk + r * KS + ch * 16, k + src, valid);
     cp_async16_zfill(sq + r * KS + ch * 16, q + src, valid);
   }
+  stage_gates(0);
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
 
-  // K K^T and Q K^T (64 x 64, fp32 accumulate of exact bf16 products)
+  // K K^T (warps 0-3) and Q K^T (warps 4-7): 16 rows each, 64 columns
   {
-    float ckk[8][4], cqk[8][4];
+    float acc[8][4];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) ckk[nt][e] = cqk[nt][e] = 0.f;
-    const char* ka0 = sk + (16 * w + g8) * KS;
-    const char* qa0 = sq + (16 * w + g8) * KS;
+      for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+    const int mt = w & 3;
+    const char* a0 = (w < 4 ? sk : sq) + (16 * mt + g8) * KS;
 #pragma unroll
     for (int kc = 0; kc < DK / 16; ++kc) {
       const int off = (kc * 16 + t4 * 2) * 2;
-      const uint32_t ak[4] = {ld32(ka0 + off), ld32(ka0 + 8 * KS + off), ld32(ka0 + off + 16),
-                              ld32(ka0 + 8 * KS + off + 16)};
-      const uint32_t aq[4] = {ld32(qa0 + off), ld32(qa0 + 8 * KS + off), ld32(qa0 + off + 16),
-                              ld32(qa0 + 8 * KS + off + 16)};
+      const uint32_t a[4] = {ld32(a0 + off), ld32(a0 + 8 * KS + off), ld32(a0 + off + 16),
+                             ld32(a0 + 8 * KS + off + 16)};
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const char* rb = sk + (nt * 8 + g8) * KS + off;
-        const uint32_t b0 = ld32(rb), b1 = ld32(rb + 16);
-        mma_bf16_16816(ckk[nt], ak, b0, b1);
-        mma_bf16_16816(cqk[nt], aq, b0, b1);
+        mma_bf16_16816(acc[nt], a, ld32(rb), ld32(rb + 16));
       }
     }
-    const int r0 = 16 * w + g8;
+    float* dst = w < 4 ? skk : sqk;
+    const int r0 = 16 * mt + g8;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const int c0 = nt * 8 + t4 * 2;
-      skk[r0 * C + c0] = ckk[nt][0];
-      skk[r0 * C + c0 + 1] = ckk[nt][1];
-      skk[(r0 + 8) * C + c0] = ckk[nt][2];
-      skk[(r0 + 8) * C + c0 + 1] = ckk[nt][3];
-      sqk[r0 * C + c0] = cqk[nt][0];
-      sqk[r0 * C + c0 + 1] = cqk[nt][1];
-      sqk[(r0 + 8) * C + c0] = cqk[nt][2];
-      sqk[(r0 + 8) * C + c0 + 1] = cqk[nt][3];
+      dst[r0 * C + c0] = acc[nt][0];
+      dst[r0 * C + c0 + 1] = acc[nt][1];
+      dst[(r0 + 8) * C + c0] = acc[nt][2];
+      dst[(r0 + 8) * C + c0 + 1] = acc[nt][3];
     }
   }
   __syncthreads();
 
   for (int j = 0; j < G; ++j) {
     const int h = hk * G + j;
-    // gates and the log-space cumulative decay G_t = sum_{s<=t} log alpha_s
+    if (j + 1 < G) {
+      stage_gates(j + 1);
+      cp_async_commit();
+    }
+    // log-space cumulative decay G_t = sum_{s<=t} log alpha_s (gates of head j landed)
     if (tid < C) {
       const int t = tid;
-      const bool valid = t < nv;
-      const float a = valid ? alpha[(size_t)(t0 + t) * Hv + h] : 1.f;
-      const float b = valid ? beta[(size_t)(t0 + t) * Hv + h] : 0.f;
-      float lg = valid ? logf(fmaxf(a, 1e-30f)) : 0.f;
+      const float* gate = sgate + (j & 1) * 2 * C;
+      const float a = gate[t], b = gate[C + t];
+      float lg = t < nv ? __logf(fmaxf(a, 1e-30f)) : 0.f;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const float y = __shfl_up_sync(0xffffffffu, lg, off);
@@ -162,44 +252,27 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
     if (tid < C) sg[tid] = slg[tid] + (tid >= 32 ? slg[31] : 0.f);
     __syncthreads();
     // A (strictly lower)
-    for (int idx = tid; idx < C * C; idx += 128) {
+    for (int idx = tid; idx < C * C; idx += PREP_THREADS) {
       const int t = idx >> 6, s = idx & 63;
-      sa[t * 65 + s] = s < t ? sb[t] * expf(sg[t] - sg[s]) * skk[t * C + s] : 0.f;
+      sa[t * TS + s] = s < t ? sb[t] * __expf(sg[t] - sg[s]) * skk[t * C + s] : 0.f;
     }
     __syncthreads();
-    // T = (I + A)^-1, one column per thread, rows in order
-    if (tid < C) {
-      const int s = tid;
-      for (int r = 0; r <= s; ++r) st[r * 65 + s] = r == s ? 1.f : 0.f;
-      for (int t = s + 1; t < C; ++t) {
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        int r = s;
-        for (; r + 3 < t; r += 4) {
-          a0 = fmaf(sa[t * 65 + r], st[r * 65 + s], a0);
-          a1 = fmaf(sa[t * 65 + r + 1], st[(r + 1) * 65 + s], a1);
-          a2 = fmaf(sa[t * 65 + r + 2], st[(r + 2) * 65 + s], a2);
-          a3 = fmaf(sa[t * 65 + r + 3], st[(r + 3) * 65 + s], a3);
-        }
-        for (; r < t; ++r) a0 = fmaf(sa[t * 65 + r], st[r * 65 + s], a0);
-        st[t * 65 + s] = -((a0 + a1) + (a2 + a3));
-      }
-    }
-    __syncthreads();
+    invert_unit_lower(sa, st, ss, tid);
     // T and P as bf16 hi/lo pairs, g and beta
     char* wsb = ws + ((size_t)c * Hv + h) * WS_STRIDE;
-    for (int idx = tid; idx < C * 8; idx += 128) {
+    for (int idx = tid; idx < C * 8; idx += PREP_THREADS) {
       const int t = idx >> 3, e8 = (idx & 7) * 8;
       uint32_t th[4], tl[4], ph[4], pl[4];
 #pragma unroll
       for (int qd = 0; qd < 4; ++qd) {
         const int s = e8 + 2 * qd;
         uint32_t h0, l0, h1, l1;
-        split_bf16(st[t * 65 + s], h0, l0);
-        split_bf16(st[t * 65 + s + 1], h1, l1);
+        split_bf16(st[t * TS + s], h0, l0);
+        split_bf16(st[t * TS + s + 1], h1, l1);
         th[qd] = h0 | (h1 << 16);
         tl[qd] = l0 | (l1 << 16);
-        const float p0 = s <= t ? expf(sg[t] - sg[s]) * sqk[t * C + s] : 0.f;
-        const float p1 = s + 1 <= t ? expf(sg[t] - sg[s + 1]) * sqk[t * C + s + 1] : 0.f;
+        const float p0 = s <= t ? __expf(sg[t] - sg[s]) * sqk[t * C + s] : 0.f;
+        const float p1 = s + 1 <= t ? __expf(sg[t] - sg[s + 1]) * sqk[t * C + s + 1] : 0.f;
         split_bf16(p0, h0, l0);
         split_bf16(p1, h1, l1);
         ph[qd] = h0 | (h1 << 16);
@@ -212,16 +285,20 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
       *reinterpret_cast<uint4*>(wsb + WS_P_LO + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
     }
     if (tid < C) {
-      reinterpret_cast<float*>(wsb + WS_G)[tid] = expf(sg[tid]);
+      reinterpret_cast<float*>(wsb + WS_G)[tid] = __expf(sg[tid]);
       reinterpret_cast<float*>(wsb + WS_B)[tid] = sb[tid];
     }
+    // the next head's gates have landed and every thread is done with this head
+    cp_async_wait<0>();
     __syncthreads();
   }
 }
 
 // ------------------------------------------------------------------- scan
-constexpr int NTMAX = 6;         // 8-column tiles per state slab (<= 48 columns)
-constexpr int VS = NTMAX * 16;   // staged V slab row (bytes)
+constexpr int SCAN_THREADS = 256;  // 8 warps
+constexpr int NTMAX = 6;           // 8-column tiles per state slab (<= 48 columns)
+constexpr int NTW = 3;             // tiles per warp in the chunk x slab products
+constexpr int VS = NTMAX * 16;     // staged V slab row (bytes)
 
 // one staging buffer
 constexpr int BUF_K = 0;
@@ -253,7 +330,22 @@ __device__ __forceinline__ void st16(char* base, int idx, uint32_t v) {
   reinterpret_cast<uint16_t*>(base)[idx] = static_cast<uint16_t>(v);
 }
 
-__global__ void __launch_bounds__(128, 1)
+// A fragment (16 x 16 bf16, row-major, row stride `stride` bytes) at (m0, k0)
+__device__ __forceinline__ void load_a(uint32_t (&a)[4], const char* base, int stride, int m0,
+                                       int k0, int lane) {
+  const int q = lane >> 3, r = lane & 7;
+  ldmatrix_x4(a, base + (m0 + (q & 1) * 8 + r) * stride + (k0 + (q >> 1) * 8) * 2);
+}
+
+// B fragments of one 8-column tile for the hi and lo halves (stored [n][k],
+// row stride `stride` bytes): b[0], b[1] = hi; b[2], b[3] = lo.
+__device__ __forceinline__ void load_b_pair(uint32_t (&b)[4], const char* hi, const char* lo,
+                                            int stride, int n0, int k0, int lane) {
+  const int q = lane >> 3, r = lane & 7;
+  ldmatrix_x4(b, (q < 2 ? hi : lo) + (n0 + r) * stride + (k0 + (q & 1) * 8) * 2);
+}
+
+__global__ void __launch_bounds__(SCAN_THREADS, 1)
 scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
             const uint16_t* __restrict__ v, float* __restrict__ state, float* __restrict__ o,
             const char* __restrict__ ws, int T, int Hk, int Hv) {
@@ -263,6 +355,7 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
   const int n_chunks = (T + C - 1) / C;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g8 = lane >> 2, t4 = lane & 3;
+  const int mt = w & 3, nt0 = (w >> 2) * NTW;  // this warp's chunk rows and column tiles
   char* hth = smem + SCAN_HTH;
   char* htl = smem + SCAN_HTL;
   char* xth = smem + SCAN_XTH;
@@ -272,68 +365,92 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
   char* pth = smem + SCAN_PTH;
   char* ptl = smem + SCAN_PTL;
 
+  // Staging: every thread copies the same (row, 16-byte column) pieces of
+  // every chunk, so its offsets are computed once; a chunk only adds its base.
+  //   K, Q: 64 rows x 16 pieces -> 4 per thread; V slab: 64 rows x NT pieces
+  //   -> up to 2 per thread; T/P hi/lo: 4 x 64 rows x 8 -> 8 per thread; g, beta: 32.
+  constexpr int KQ_PER = C * 16 / SCAN_THREADS;
+  constexpr int WSP_PER = 4 * C * 8 / SCAN_THREADS;
+  int kq_row[KQ_PER], kq_dst[KQ_PER], kq_src[KQ_PER];
+#pragma unroll
+  for (int u = 0; u < KQ_PER; ++u) {
+    const int idx = tid + u * SCAN_THREADS, r = idx >> 4, ch = idx & 15;
+    kq_row[u] = r;
+    kq_dst[u] = r * KS + ch * 16;
+    kq_src[u] = (r * Hk + hk) * DK + ch * 8;  // elements, relative to the chunk's first row
+  }
+  int v_row[2], v_dst[2], v_src[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int idx = tid + u * SCAN_THREADS;
+    const int r = idx < C * NT ? idx / NT : C, ch = idx < C * NT ? idx - (idx / NT) * NT : 0;
+    v_row[u] = r;
+    v_dst[u] = r * VS + ch * 16;
+    v_src[u] = (r * Hv + h) * DV + j0 + ch * 8;
+  }
+  int w_dst[WSP_PER], w_src[WSP_PER];
+#pragma unroll
+  for (int u = 0; u < WSP_PER; ++u) {
+    const int idx = tid + u * SCAN_THREADS, m = idx >> 9, r = (idx >> 3) & 63, ch = idx & 7;
+    w_dst[u] = BUF_TH + m * C * XS + r * XS + ch * 16;
+    w_src[u] = m * 8192 + r * 128 + ch * 16;
+  }
   auto stage = [&](int c, int buf) {
     char* B = smem + buf * BUF_SIZE;
     const int t0 = c * C, nv = min(C, T - t0);
-    for (int idx = tid; idx < C * 16; idx += 128) {
-      const int r = idx >> 4, ch = idx & 15;
-      const bool valid = r < nv;
-      const size_t src = ((size_t)(t0 + (valid ? r : 0)) * Hk + hk) * DK + ch * 8;
-      cp_async16_zfill(B + BUF_K + r * KS + ch * 16, k + src, valid);
-      cp_async16_zfill(B + BUF_Q + r * KS + ch * 16, q + src, valid);
+    const uint16_t* kb = k + (size_t)t0 * Hk * DK;
+    const uint16_t* qb = q + (size_t)t0 * Hk * DK;
+    const uint16_t* vbase = v + (size_t)t0 * Hv * DV;
+#pragma unroll
+    for (int u = 0; u < KQ_PER; ++u) {
+      const bool valid = kq_row[u] < nv;
+      const int src = valid ? kq_src[u] : 0;
+      cp_async16_zfill(B + BUF_K + kq_dst[u], kb + src, valid);
+      cp_async16_zfill(B + BUF_Q + kq_dst[u], qb + src, valid);
     }
-    for (int idx = tid; idx < C * NT; idx += 128) {
-      const int r = idx / NT, ch = idx - r * NT;
-      const bool valid = r < nv;
-      const size_t src = ((size_t)(t0 + (valid ? r : 0)) * Hv + h) * DV + j0 + ch * 8;
-      cp_async16_zfill(B + BUF_V + r * VS + ch * 16, v + src, valid);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (v_row[u] < C) {
+        const bool valid = v_row[u] < nv;
+        cp_async16_zfill(B + BUF_V + v_dst[u], vbase + (valid ? v_src[u] : 0), valid);
+      }
     }
     const char* wsb = ws + ((size_t)c * Hv + h) * WS_STRIDE;
-    for (int idx = tid; idx < 4 * C * 8; idx += 128) {
-      const int m = idx >> 9, r = (idx >> 3) & 63, ch = idx & 7;
-      cp_async16(B + BUF_TH + m * C * XS + r * XS + ch * 16, wsb + m * 8192 + r * 128 + ch * 16);
-    }
-    for (int idx = tid; idx < 32; idx += 128)
-      cp_async16(B + BUF_G + idx * 16, wsb + WS_G + idx * 16);
+#pragma unroll
+    for (int u = 0; u < WSP_PER; ++u) cp_async16(B + w_dst[u], wsb + w_src[u]);
+    if (tid < 32) cp_async16(B + BUF_G + tid * 16, wsb + WS_G + tid * 16);
     cp_async_commit();
   };
 
-  // ---- the state slab -> fp32 fragments (rows 32w + 16mi + g8 (+8), cols nt*8 + 2t4)
-  float Hf[2][NTMAX][4];
+  // ---- this warp's 16 state rows (16w + g8 (+8)), all slab columns (nt*8 + 2t4)
+  float Hf[NTMAX][4];
   float* sth = state + (size_t)h * DK * DV + j0;
+  const int ia = 16 * w + g8;
 #pragma unroll
-  for (int mi = 0; mi < 2; ++mi) {
-    const int ia = 32 * w + 16 * mi + g8;
-#pragma unroll
-    for (int nt = 0; nt < NTMAX; ++nt) {
-      if (nt < NT) {
-        const int jj = nt * 8 + t4 * 2;
-        const float2 x = *reinterpret_cast<const float2*>(sth + (size_t)ia * DV + jj);
-        const float2 y = *reinterpret_cast<const float2*>(sth + (size_t)(ia + 8) * DV + jj);
-        Hf[mi][nt][0] = x.x; Hf[mi][nt][1] = x.y; Hf[mi][nt][2] = y.x; Hf[mi][nt][3] = y.y;
-      } else {
-        Hf[mi][nt][0] = Hf[mi][nt][1] = Hf[mi][nt][2] = Hf[mi][nt][3] = 0.f;
-      }
+  for (int nt = 0; nt < NTMAX; ++nt) {
+    if (nt < NT) {
+      const int jj = nt * 8 + t4 * 2;
+      const float2 x = *reinterpret_cast<const float2*>(sth + (size_t)ia * DV + jj);
+      const float2 y = *reinterpret_cast<const float2*>(sth + (size_t)(ia + 8) * DV + jj);
+      Hf[nt][0] = x.x; Hf[nt][1] = x.y; Hf[nt][2] = y.x; Hf[nt][3] = y.y;
+    } else {
+      Hf[nt][0] = Hf[nt][1] = Hf[nt][2] = Hf[nt][3] = 0.f;
     }
   }
   // H^T as bf16 hi/lo: element (j, i) at j*KS/2 + i
   auto write_ht = [&]() {
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi) {
-      const int ia = 32 * w + 16 * mi + g8;
+    for (int nt = 0; nt < NTMAX; ++nt) {
+      if (nt < NT) {
+        const int jj = nt * 8 + t4 * 2;
+        const int idx[4] = {jj * (KS / 2) + ia, (jj + 1) * (KS / 2) + ia, jj * (KS / 2) + ia + 8,
+                            (jj + 1) * (KS / 2) + ia + 8};
 #pragma unroll
-      for (int nt = 0; nt < NTMAX; ++nt) {
-        if (nt < NT) {
-          const int jj = nt * 8 + t4 * 2;
+        for (int e = 0; e < 4; ++e) {
           uint32_t hi, lo;
-          split_bf16(Hf[mi][nt][0], hi, lo);
-          st16(hth, jj * (KS / 2) + ia, hi); st16(htl, jj * (KS / 2) + ia, lo);
-          split_bf16(Hf[mi][nt][1], hi, lo);
-          st16(hth, (jj + 1) * (KS / 2) + ia, hi); st16(htl, (jj + 1) * (KS / 2) + ia, lo);
-          split_bf16(Hf[mi][nt][2], hi, lo);
-          st16(hth, jj * (KS / 2) + ia + 8, hi); st16(htl, jj * (KS / 2) + ia + 8, lo);
-          split_bf16(Hf[mi][nt][3], hi, lo);
-          st16(hth, (jj + 1) * (KS / 2) + ia + 8, hi); st16(htl, (jj + 1) * (KS / 2) + ia + 8, lo);
+          split_bf16(Hf[nt][e], hi, lo);
+          st16(hth, idx[e], hi);
+          st16(htl, idx[e], lo);
         }
       }
     }
@@ -341,7 +458,7 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
   write_ht();
   stage(0, 0);
 
-  const int ta = 16 * w + g8, tb = ta + 8;  // this thread's chunk rows in C x slab tiles
+  const int ta = 16 * mt + g8, tb = ta + 8;  // this thread's chunk rows
   for (int c = 0; c < n_chunks; ++c) {
     const int buf = c & 1;
     const int nv = min(C, T - c * C);
@@ -356,33 +473,26 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
     const float* bg = reinterpret_cast<const float*>(B + BUF_G);
     const float* bb = reinterpret_cast<const float*>(B + BUF_B);
 
-    // ---- K H and Q H for rows ta, tb
-    float kh[NTMAX][4], qh[NTMAX][4];
+    // ---- K H and Q H: rows of m-tile mt, column tiles nt0 .. nt0+2
+    float kh[NTW][4], qh[NTW][4];
 #pragma unroll
-    for (int nt = 0; nt < NTMAX; ++nt)
+    for (int i = 0; i < NTW; ++i)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) kh[nt][e] = qh[nt][e] = 0.f;
-    {
-      const char* ka = B + BUF_K + ta * KS;
-      const char* qa = B + BUF_Q + ta * KS;
+      for (int e = 0; e < 4; ++e) kh[i][e] = qh[i][e] = 0.f;
 #pragma unroll
-      for (int kc = 0; kc < DK / 16; ++kc) {
-        const int off = (kc * 16 + t4 * 2) * 2;
-        const uint32_t ak[4] = {ld32(ka + off), ld32(ka + 8 * KS + off), ld32(ka + off + 16),
-                                ld32(ka + 8 * KS + off + 16)};
-        const uint32_t aq[4] = {ld32(qa + off), ld32(qa + 8 * KS + off), ld32(qa + off + 16),
-                                ld32(qa + 8 * KS + off + 16)};
+    for (int kc = 0; kc < DK / 16; ++kc) {
+      uint32_t ak[4], aq[4];
+      load_a(ak, B + BUF_K, KS, 16 * mt, kc * 16, lane);
+      load_a(aq, B + BUF_Q, KS, 16 * mt, kc * 16, lane);
 #pragma unroll
-        for (int nt = 0; nt < NTMAX; ++nt) {
-          if (nt < NT) {
-            const int rb = (nt * 8 + g8) * KS + off;
-            const uint32_t bh0 = ld32(hth + rb), bh1 = ld32(hth + rb + 16);
-            const uint32_t bl0 = ld32(htl + rb), bl1 = ld32(htl + rb + 16);
-            mma_bf16_16816(kh[nt], ak, bh0, bh1);
-            mma_bf16_16816(kh[nt], ak, bl0, bl1);
-            mma_bf16_16816(qh[nt], aq, bh0, bh1);
-            mma_bf16_16816(qh[nt], aq, bl0, bl1);
-          }
+      for (int i = 0; i < NTW; ++i) {
+        if (nt0 + i < NT) {
+          uint32_t b[4];
+          load_b_pair(b, hth, htl, KS, (nt0 + i) * 8, kc * 16, lane);
+          mma_bf16_16816(kh[i], ak, b[0], b[1]);
+          mma_bf16_16816(kh[i], ak, b[2], b[3]);
+          mma_bf16_16816(qh[i], aq, b[0], b[1]);
+          mma_bf16_16816(qh[i], aq, b[2], b[3]);
         }
       }
     }
@@ -392,45 +502,46 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
       const char* va = B + BUF_V + ta * VS;
       const char* vb = B + BUF_V + tb * VS;
 #pragma unroll
-      for (int nt = 0; nt < NTMAX; ++nt) {
-        if (nt < NT) {
-          const int jj = nt * 8 + t4 * 2;
+      for (int i = 0; i < NTW; ++i) {
+        if (nt0 + i < NT) {
+          const int jj = (nt0 + i) * 8 + t4 * 2;
           const uint32_t pa = ld32(va + jj * 2), pb = ld32(vb + jj * 2);
-          const float x0 = ba * (__uint_as_float(pa << 16) - ga * kh[nt][0]);
-          const float x1 = ba * (__uint_as_float(pa & 0xffff0000u) - ga * kh[nt][1]);
-          const float x2 = bbv * (__uint_as_float(pb << 16) - gb * kh[nt][2]);
-          const float x3 = bbv * (__uint_as_float(pb & 0xffff0000u) - gb * kh[nt][3]);
-          uint32_t hi, lo;
-          split_bf16(x0, hi, lo); st16(xth, jj * (XS / 2) + ta, hi); st16(xtl, jj * (XS / 2) + ta, lo);
-          split_bf16(x1, hi, lo); st16(xth, (jj + 1) * (XS / 2) + ta, hi); st16(xtl, (jj + 1) * (XS / 2) + ta, lo);
-          split_bf16(x2, hi, lo); st16(xth, jj * (XS / 2) + tb, hi); st16(xtl, jj * (XS / 2) + tb, lo);
-          split_bf16(x3, hi, lo); st16(xth, (jj + 1) * (XS / 2) + tb, hi); st16(xtl, (jj + 1) * (XS / 2) + tb, lo);
+          const float x[4] = {ba * (__uint_as_float(pa << 16) - ga * kh[i][0]),
+                              ba * (__uint_as_float(pa & 0xffff0000u) - ga * kh[i][1]),
+                              bbv * (__uint_as_float(pb << 16) - gb * kh[i][2]),
+                              bbv * (__uint_as_float(pb & 0xffff0000u) - gb * kh[i][3])};
+          const int idx[4] = {jj * (XS / 2) + ta, (jj + 1) * (XS / 2) + ta, jj * (XS / 2) + tb,
+                              (jj + 1) * (XS / 2) + tb};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint32_t hi, lo;
+            split_bf16(x[e], hi, lo);
+            st16(xth, idx[e], hi);
+            st16(xtl, idx[e], lo);
+          }
         }
       }
     }
     __syncthreads();
 
-    // ---- Delta = T X (T lower triangular: k-blocks 0..w)
-    float dl[NTMAX][4];
+    // ---- Delta = T X (T lower triangular: k-blocks 0..mt)
+    float dl[NTW][4];
 #pragma unroll
-    for (int nt = 0; nt < NTMAX; ++nt)
+    for (int i = 0; i < NTW; ++i)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) dl[nt][e] = 0.f;
-    for (int kc = 0; kc <= w; ++kc) {
-      const int off = (kc * 16 + t4 * 2) * 2;
-      const char* th = B + BUF_TH + ta * XS + off;
-      const char* tl = B + BUF_TL + ta * XS + off;
-      const uint32_t ah[4] = {ld32(th), ld32(th + 8 * XS), ld32(th + 16), ld32(th + 8 * XS + 16)};
-      const uint32_t al[4] = {ld32(tl), ld32(tl + 8 * XS), ld32(tl + 16), ld32(tl + 8 * XS + 16)};
+      for (int e = 0; e < 4; ++e) dl[i][e] = 0.f;
+    for (int kc = 0; kc <= mt; ++kc) {
+      uint32_t ah[4], al[4];
+      load_a(ah, B + BUF_TH, XS, 16 * mt, kc * 16, lane);
+      load_a(al, B + BUF_TL, XS, 16 * mt, kc * 16, lane);
 #pragma unroll
-      for (int nt = 0; nt < NTMAX; ++nt) {
-        if (nt < NT) {
-          const int rb = (nt * 8 + g8) * XS + off;
-          const uint32_t bh0 = ld32(xth + rb), bh1 = ld32(xth + rb + 16);
-          const uint32_t bl0 = ld32(xtl + rb), bl1 = ld32(xtl + rb + 16);
-          mma_bf16_16816(dl[nt], ah, bh0, bh1);
-          mma_bf16_16816(dl[nt], ah, bl0, bl1);
-          mma_bf16_16816(dl[nt], al, bh0, bh1);
+      for (int i = 0; i < NTW; ++i) {
+        if (nt0 + i < NT) {
+          uint32_t b[4];
+          load_b_pair(b, xth, xtl, XS, (nt0 + i) * 8, kc * 16, lane);
+          mma_bf16_16816(dl[i], ah, b[0], b[1]);
+          mma_bf16_16816(dl[i], ah, b[2], b[3]);
+          mma_bf16_16816(dl[i], al, b[0], b[1]);
         }
       }
     }
@@ -438,18 +549,20 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
     {
       const float ra = gC / bg[ta], rbv = gC / bg[tb];
 #pragma unroll
-      for (int nt = 0; nt < NTMAX; ++nt) {
-        if (nt < NT) {
-          const int jj = nt * 8 + t4 * 2;
+      for (int i = 0; i < NTW; ++i) {
+        if (nt0 + i < NT) {
+          const int jj = (nt0 + i) * 8 + t4 * 2;
           const int idx[4] = {jj * (XS / 2) + ta, (jj + 1) * (XS / 2) + ta, jj * (XS / 2) + tb,
                               (jj + 1) * (XS / 2) + tb};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint32_t hi, lo;
-            split_bf16(dl[nt][e], hi, lo);
-            st16(dth, idx[e], hi); st16(dtl, idx[e], lo);
-            split_bf16((e < 2 ? ra : rbv) * dl[nt][e], hi, lo);
-            st16(pth, idx[e], hi); st16(ptl, idx[e], lo);
+            split_bf16(dl[i][e], hi, lo);
+            st16(dth, idx[e], hi);
+            st16(dtl, idx[e], lo);
+            split_bf16((e < 2 ? ra : rbv) * dl[i][e], hi, lo);
+            st16(pth, idx[e], hi);
+            st16(ptl, idx[e], lo);
           }
         }
       }
@@ -460,65 +573,56 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
     {
       const float ga = bg[ta], gb = bg[tb];
 #pragma unroll
-      for (int nt = 0; nt < NTMAX; ++nt) {
-        qh[nt][0] *= ga; qh[nt][1] *= ga; qh[nt][2] *= gb; qh[nt][3] *= gb;
+      for (int i = 0; i < NTW; ++i) {
+        qh[i][0] *= ga; qh[i][1] *= ga; qh[i][2] *= gb; qh[i][3] *= gb;
       }
-      for (int kc = 0; kc <= w; ++kc) {
-        const int off = (kc * 16 + t4 * 2) * 2;
-        const char* ph = B + BUF_PH + ta * XS + off;
-        const char* pl = B + BUF_PL + ta * XS + off;
-        const uint32_t ah[4] = {ld32(ph), ld32(ph + 8 * XS), ld32(ph + 16), ld32(ph + 8 * XS + 16)};
-        const uint32_t al[4] = {ld32(pl), ld32(pl + 8 * XS), ld32(pl + 16), ld32(pl + 8 * XS + 16)};
+      for (int kc = 0; kc <= mt; ++kc) {
+        uint32_t ah[4], al[4];
+        load_a(ah, B + BUF_PH, XS, 16 * mt, kc * 16, lane);
+        load_a(al, B + BUF_PL, XS, 16 * mt, kc * 16, lane);
 #pragma unroll
-        for (int nt = 0; nt < NTMAX; ++nt) {
-          if (nt < NT) {
-            const int rb = (nt * 8 + g8) * XS + off;
-            const uint32_t bh0 = ld32(dth + rb), bh1 = ld32(dth + rb + 16);
-            const uint32_t bl0 = ld32(dtl + rb), bl1 = ld32(dtl + rb + 16);
-            mma_bf16_16816(qh[nt], ah, bh0, bh1);
-            mma_bf16_16816(qh[nt], ah, bl0, bl1);
-            mma_bf16_16816(qh[nt], al, bh0, bh1);
+        for (int i = 0; i < NTW; ++i) {
+          if (nt0 + i < NT) {
+            uint32_t b[4];
+            load_b_pair(b, dth, dtl, XS, (nt0 + i) * 8, kc * 16, lane);
+            mma_bf16_16816(qh[i], ah, b[0], b[1]);
+            mma_bf16_16816(qh[i], ah, b[2], b[3]);
+            mma_bf16_16816(qh[i], al, b[0], b[1]);
           }
         }
       }
       float* oa = o + ((size_t)(c * C + ta) * Hv + h) * DV + j0;
       float* ob = o + ((size_t)(c * C + tb) * Hv + h) * DV + j0;
 #pragma unroll
-      for (int nt = 0; nt < NTMAX; ++nt) {
-        if (nt < NT) {
-          const int jj = nt * 8 + t4 * 2;
-          if (ta < nv) *reinterpret_cast<float2*>(oa + jj) = make_float2(qh[nt][0], qh[nt][1]);
-          if (tb < nv) *reinterpret_cast<float2*>(ob + jj) = make_float2(qh[nt][2], qh[nt][3]);
+      for (int i = 0; i < NTW; ++i) {
+        if (nt0 + i < NT) {
+          const int jj = (nt0 + i) * 8 + t4 * 2;
+          if (ta < nv) *reinterpret_cast<float2*>(oa + jj) = make_float2(qh[i][0], qh[i][1]);
+          if (tb < nv) *reinterpret_cast<float2*>(ob + jj) = make_float2(qh[i][2], qh[i][3]);
         }
       }
     }
 
     // ---- H <- g_C H + K^T D'  (A = K^T tiles through ldmatrix.trans)
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
+    for (int nt = 0; nt < NTMAX; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < NTMAX; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) Hf[mi][nt][e] *= gC;
+      for (int e = 0; e < 4; ++e) Hf[nt][e] *= gC;
     {
       const int q4 = lane >> 3, r8 = lane & 7;
 #pragma unroll
       for (int kc = 0; kc < C / 16; ++kc) {
-        const int off = (kc * 16 + t4 * 2) * 2;
+        const int row = kc * 16 + ((q4 & 2) ? 8 : 0) + r8;
+        const int col = 16 * w + ((q4 & 1) ? 8 : 0);
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, B + BUF_K + row * KS + col * 2);
 #pragma unroll
-        for (int mi = 0; mi < 2; ++mi) {
-          const int i0 = 32 * w + 16 * mi;
-          const int row = kc * 16 + ((q4 & 2) ? 8 : 0) + r8;
-          const int col = i0 + ((q4 & 1) ? 8 : 0);
-          uint32_t a[4];
-          ldmatrix_x4_trans(a, B + BUF_K + row * KS + col * 2);
-#pragma unroll
-          for (int nt = 0; nt < NTMAX; ++nt) {
-            if (nt < NT) {
-              const int rb = (nt * 8 + g8) * XS + off;
-              mma_bf16_16816(Hf[mi][nt], a, ld32(pth + rb), ld32(pth + rb + 16));
-              mma_bf16_16816(Hf[mi][nt], a, ld32(ptl + rb), ld32(ptl + rb + 16));
-            }
+        for (int nt = 0; nt < NTMAX; ++nt) {
+          if (nt < NT) {
+            uint32_t b[4];
+            load_b_pair(b, pth, ptl, XS, nt * 8, kc * 16, lane);
+            mma_bf16_16816(Hf[nt], a, b[0], b[1]);
+            mma_bf16_16816(Hf[nt], a, b[2], b[3]);
           }
         }
       }
@@ -528,15 +632,11 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
   }
 
 #pragma unroll
-  for (int mi = 0; mi < 2; ++mi) {
-    const int ia = 32 * w + 16 * mi + g8;
-#pragma unroll
-    for (int nt = 0; nt < NTMAX; ++nt) {
-      if (nt < NT) {
-        const int jj = nt * 8 + t4 * 2;
-        *reinterpret_cast<float2*>(sth + (size_t)ia * DV + jj) = make_float2(Hf[mi][nt][0], Hf[mi][nt][1]);
-        *reinterpret_cast<float2*>(sth + (size_t)(ia + 8) * DV + jj) = make_float2(Hf[mi][nt][2], Hf[mi][nt][3]);
-      }
+  for (int nt = 0; nt < NTMAX; ++nt) {
+    if (nt < NT) {
+      const int jj = nt * 8 + t4 * 2;
+      *reinterpret_cast<float2*>(sth + (size_t)ia * DV + jj) = make_float2(Hf[nt][0], Hf[nt][1]);
+      *reinterpret_cast<float2*>(sth + (size_t)(ia + 8) * DV + jj) = make_float2(Hf[nt][2], Hf[nt][3]);
     }
   }
 }
@@ -606,12 +706,12 @@ int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const
       cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SCAN_SMEM) != cudaSuccess)
     return GDN_ERR_CUDA;
-  prep_kernel<<<dim3(n_chunks, Hk), 128, PREP_SMEM, stream>>>(
+  prep_kernel<<<dim3(n_chunks, Hk), PREP_THREADS, PREP_SMEM, stream>>>(
       static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), alpha, beta, T, Hk, Hv,
       static_cast<char*>(workspace));
   int st = launch_status();
   if (st != GDN_OK) return st;
-  scan_kernel<<<dim3(3, Hv), 128, SCAN_SMEM, stream>>>(
+  scan_kernel<<<dim3(3, Hv), SCAN_THREADS, SCAN_SMEM, stream>>>(
       static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
       static_cast<const uint16_t*>(v), state, o, static_cast<const char*>(workspace), T, Hk, Hv);
   return launch_status();
