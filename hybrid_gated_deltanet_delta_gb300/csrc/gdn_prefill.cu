@@ -44,7 +44,11 @@ constexpr int DV = 128;       // value width
 constexpr int KS = DK * 2 + 16;  // staged bf16 row of K / Q, padded (bytes)
 constexpr int XS = C * 2 + 16;   // staged bf16 row of length C, padded (bytes)
 
-// workspace block of one (chunk, value head)
+// workspace block of one (chunk, value head): T and P as bf16 hi/lo, 64 x 64
+// each in 128-byte rows whose 16-byte chunks are XOR-swizzled by row (chunk ch
+// of row t at chunk ch ^ (t & 7)), then g and beta.  The scan copies the block
+// into shared memory as is; the swizzle keeps its fragment loads free of bank
+// conflicts.
 constexpr int WS_T_HI = 0;
 constexpr int WS_T_LO = 8192;
 constexpr int WS_P_HI = 16384;
@@ -278,7 +282,8 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
         ph[qd] = h0 | (h1 << 16);
         pl[qd] = l0 | (l1 << 16);
       }
-      const int off = (t * C + e8) * 2;
+      // 128-byte rows, 16-byte chunk ch of row t stored at chunk ch ^ (t & 7)
+      const int off = t * 128 + (((e8 >> 3) ^ (t & 7)) << 4);
       *reinterpret_cast<uint4*>(wsb + WS_T_HI + off) = make_uint4(th[0], th[1], th[2], th[3]);
       *reinterpret_cast<uint4*>(wsb + WS_T_LO + off) = make_uint4(tl[0], tl[1], tl[2], tl[3]);
       *reinterpret_cast<uint4*>(wsb + WS_P_HI + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
@@ -300,17 +305,20 @@ constexpr int NTMAX = 6;           // 8-column tiles per state slab (<= 48 colum
 constexpr int NTW = 3;             // tiles per warp in the chunk x slab products
 constexpr int VS = NTMAX * 16;     // staged V slab row (bytes)
 
-// one staging buffer
+// one staging buffer: K and Q rows (padded), the V slab, then the chunk's
+// workspace block copied as is (T hi/lo, P hi/lo in swizzled 128-byte rows, g, beta)
 constexpr int BUF_K = 0;
 constexpr int BUF_Q = BUF_K + C * KS;
 constexpr int BUF_V = BUF_Q + C * KS;
-constexpr int BUF_TH = BUF_V + C * VS;
-constexpr int BUF_TL = BUF_TH + C * XS;
-constexpr int BUF_PH = BUF_TL + C * XS;
-constexpr int BUF_PL = BUF_PH + C * XS;
-constexpr int BUF_G = BUF_PL + C * XS;
-constexpr int BUF_B = BUF_G + C * 4;
-constexpr int BUF_SIZE = BUF_B + C * 4;
+constexpr int BUF_W = BUF_V + C * VS;
+constexpr int BUF_TH = BUF_W + WS_T_HI;
+constexpr int BUF_TL = BUF_W + WS_T_LO;
+constexpr int BUF_PH = BUF_W + WS_P_HI;
+constexpr int BUF_PL = BUF_W + WS_P_LO;
+constexpr int BUF_G = BUF_W + WS_G;
+constexpr int BUF_B = BUF_W + WS_B;
+constexpr int BUF_SIZE = BUF_W + WS_STRIDE;
+static_assert(BUF_W % 16 == 0 && BUF_SIZE % 16 == 0, "bulk copy destinations are 16-byte aligned");
 
 constexpr int SCAN_HTH = 2 * BUF_SIZE;          // H^T hi: [48][KS]
 constexpr int SCAN_HTL = SCAN_HTH + 48 * KS;
@@ -320,7 +328,11 @@ constexpr int SCAN_DTH = SCAN_XTL + 48 * XS;    // Delta^T
 constexpr int SCAN_DTL = SCAN_DTH + 48 * XS;
 constexpr int SCAN_PTH = SCAN_DTL + 48 * XS;    // D'^T
 constexpr int SCAN_PTL = SCAN_PTH + 48 * XS;
-constexpr int SCAN_SMEM = SCAN_PTL + 48 * XS;
+constexpr int SCAN_BAR = SCAN_PTL + 48 * XS;    // two mbarriers, one per buffer
+constexpr int SCAN_SMEM = SCAN_BAR + 16;
+
+// polls of an mbarrier before a block gives up on its staged chunk
+constexpr long long kWaitPolls = 1ll << 22;
 
 // the three column slabs of a 128-wide state: 48 + 40 + 40 columns
 __device__ __forceinline__ int slab_j0(int s) { return s == 0 ? 0 : (s == 1 ? 48 : 88); }
@@ -335,6 +347,15 @@ __device__ __forceinline__ void load_a(uint32_t (&a)[4], const char* base, int s
                                        int k0, int lane) {
   const int q = lane >> 3, r = lane & 7;
   ldmatrix_x4(a, base + (m0 + (q & 1) * 8 + r) * stride + (k0 + (q >> 1) * 8) * 2);
+}
+
+// A fragment (16 x 16) of a 64 x 64 bf16 matrix in swizzled 128-byte rows
+// (16-byte chunk ch of row r stored at chunk ch ^ (r & 7)) at (m0, k0)
+__device__ __forceinline__ void load_a_swz(uint32_t (&a)[4], const char* base, int m0, int k0,
+                                           int lane) {
+  const int q = lane >> 3, r = lane & 7;
+  const int row = m0 + (q & 1) * 8 + r, ch = (k0 >> 3) + (q >> 1);
+  ldmatrix_x4(a, base + row * 128 + ((ch ^ (row & 7)) << 4));
 }
 
 // B fragments of one 8-column tile for the hi and lo halves (stored [n][k],
@@ -365,12 +386,20 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
   char* pth = smem + SCAN_PTH;
   char* ptl = smem + SCAN_PTL;
 
-  // Staging: every thread copies the same (row, 16-byte column) pieces of
-  // every chunk, so its offsets are computed once; a chunk only adds its base.
-  //   K, Q: 64 rows x 16 pieces -> 4 per thread; V slab: 64 rows x NT pieces
-  //   -> up to 2 per thread; T/P hi/lo: 4 x 64 rows x 8 -> 8 per thread; g, beta: 32.
+  // Staging of one chunk: the chunk's workspace block (33 KB, contiguous) by a
+  // single bulk (TMA) copy completing on the buffer's mbarrier; the K, Q and V
+  // slab rows by 16-byte cp.async spread over all threads, whose (row, piece)
+  // assignment is the same for every chunk, so the offsets are computed once.
+  // Rows past the end of the sequence read as zero.  The buffer being filled
+  // was last read before the previous iteration's closing barrier.
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + SCAN_BAR);
+  if (tid == 0) {
+    mbar_init(&mbar[0], 1);
+    mbar_init(&mbar[1], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
   constexpr int KQ_PER = C * 16 / SCAN_THREADS;
-  constexpr int WSP_PER = 4 * C * 8 / SCAN_THREADS;
   int kq_row[KQ_PER], kq_dst[KQ_PER], kq_src[KQ_PER];
 #pragma unroll
   for (int u = 0; u < KQ_PER; ++u) {
@@ -388,16 +417,14 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
     v_dst[u] = r * VS + ch * 16;
     v_src[u] = (r * Hv + h) * DV + j0 + ch * 8;
   }
-  int w_dst[WSP_PER], w_src[WSP_PER];
-#pragma unroll
-  for (int u = 0; u < WSP_PER; ++u) {
-    const int idx = tid + u * SCAN_THREADS, m = idx >> 9, r = (idx >> 3) & 63, ch = idx & 7;
-    w_dst[u] = BUF_TH + m * C * XS + r * XS + ch * 16;
-    w_src[u] = m * 8192 + r * 128 + ch * 16;
-  }
   auto stage = [&](int c, int buf) {
     char* B = smem + buf * BUF_SIZE;
     const int t0 = c * C, nv = min(C, T - t0);
+    if (tid == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&mbar[buf], (unsigned)WS_STRIDE);
+      bulk_g2s(B + BUF_W, ws + ((size_t)c * Hv + h) * WS_STRIDE, WS_STRIDE, &mbar[buf]);
+    }
     const uint16_t* kb = k + (size_t)t0 * Hk * DK;
     const uint16_t* qb = q + (size_t)t0 * Hk * DK;
     const uint16_t* vbase = v + (size_t)t0 * Hv * DV;
@@ -415,10 +442,6 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
         cp_async16_zfill(B + BUF_V + v_dst[u], vbase + (valid ? v_src[u] : 0), valid);
       }
     }
-    const char* wsb = ws + ((size_t)c * Hv + h) * WS_STRIDE;
-#pragma unroll
-    for (int u = 0; u < WSP_PER; ++u) cp_async16(B + w_dst[u], wsb + w_src[u]);
-    if (tid < 32) cp_async16(B + BUF_G + tid * 16, wsb + WS_G + tid * 16);
     cp_async_commit();
   };
 
@@ -468,7 +491,15 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
     } else {
       cp_async_wait<0>();
     }
-    __syncthreads();
+    // chunk c is the (c/2)-th use of its buffer: wait for that phase
+    if (!__syncthreads_and(mbar_wait_bounded(&mbar[buf], (c >> 1) & 1, kWaitPolls))) {
+      // a staged chunk never arrived: give the copies in flight a last bounded
+      // chance to land, mark this block's state slab as failed (NaN), stop
+      mbar_wait_bounded(&mbar[buf ^ 1], ((c + 1) >> 1) & 1, kWaitPolls);
+      for (int idx = tid; idx < DK * 8 * NT; idx += SCAN_THREADS)
+        sth[(size_t)(idx / (8 * NT)) * DV + idx % (8 * NT)] = __int_as_float(0x7fc00000);
+      return;
+    }
     const char* B = smem + buf * BUF_SIZE;
     const float* bg = reinterpret_cast<const float*>(B + BUF_G);
     const float* bb = reinterpret_cast<const float*>(B + BUF_B);
@@ -532,8 +563,8 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
       for (int e = 0; e < 4; ++e) dl[i][e] = 0.f;
     for (int kc = 0; kc <= mt; ++kc) {
       uint32_t ah[4], al[4];
-      load_a(ah, B + BUF_TH, XS, 16 * mt, kc * 16, lane);
-      load_a(al, B + BUF_TL, XS, 16 * mt, kc * 16, lane);
+      load_a_swz(ah, B + BUF_TH, 16 * mt, kc * 16, lane);
+      load_a_swz(al, B + BUF_TL, 16 * mt, kc * 16, lane);
 #pragma unroll
       for (int i = 0; i < NTW; ++i) {
         if (nt0 + i < NT) {
@@ -578,8 +609,8 @@ scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
       }
       for (int kc = 0; kc <= mt; ++kc) {
         uint32_t ah[4], al[4];
-        load_a(ah, B + BUF_PH, XS, 16 * mt, kc * 16, lane);
-        load_a(al, B + BUF_PL, XS, 16 * mt, kc * 16, lane);
+        load_a_swz(ah, B + BUF_PH, 16 * mt, kc * 16, lane);
+        load_a_swz(al, B + BUF_PL, 16 * mt, kc * 16, lane);
 #pragma unroll
         for (int i = 0; i < NTW; ++i) {
           if (nt0 + i < NT) {
