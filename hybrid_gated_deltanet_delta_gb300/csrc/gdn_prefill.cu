@@ -28,12 +28,15 @@
 // as hi*hi + hi*lo + lo*hi (or hi + lo against an exact bf16 K / Q), which
 // keeps ~16 significant bits per operand; a single bf16 rounding of any of
 // them costs ~1% of the output RMS at this size.
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 
 #include <mutex>
 
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 namespace {
@@ -42,17 +45,14 @@ constexpr int C = 64;         // chunk length
 constexpr int DK = 128;       // key / query width
 constexpr int DV = 128;       // value width
 constexpr int KS = DK * 2 + 16;  // staged bf16 row of K / Q, padded (bytes)
-constexpr int XS = C * 2 + 16;   // staged bf16 row of length C, padded (bytes)
 
-// workspace block of one (chunk, value head): T and P as bf16 hi/lo, 64 x 64
-// each in 128-byte rows whose 16-byte chunks are XOR-swizzled by row (chunk ch
-// of row t at chunk ch ^ (t & 7)), then g and beta.  The scan copies the block
-// into shared memory as is; the swizzle keeps its fragment loads free of bank
-// conflicts.
-constexpr int WS_T_HI = 0;
-constexpr int WS_T_LO = 8192;
-constexpr int WS_P_HI = 16384;
-constexpr int WS_P_LO = 24576;
+// workspace block of one (chunk, value head): A = [T; P T] (128 x 64) as bf16
+// hi then lo, in 128-byte rows whose 16-byte chunks are XOR-swizzled by row
+// (chunk ch of row r at chunk ch ^ (r & 7): the tensor cores' 128-byte
+// swizzle), then g and beta.  The scan copies the block into shared memory as
+// is and hands A to the tensor cores without further staging.
+constexpr int WS_AH = 0;      // rows 0-63: T, rows 64-127: P T
+constexpr int WS_AL = 16384;
 constexpr int WS_G = 32768;
 constexpr int WS_B = 33024;
 constexpr int WS_STRIDE = 33280;
@@ -98,6 +98,26 @@ __device__ __forceinline__ void mm_tiles(float* Cm, const float* X, const float*
     Cm[r * TS + c + 1] = sign * a01;
     Cm[(r + 1) * TS + c] = sign * a10;
     Cm[(r + 1) * TS + c + 1] = sign * a11;
+  }
+}
+
+// R = X Y for lower-triangular 64 x 64 X and Y (row stride TS): only the
+// terms k in [s, t] of R[t][s] are nonzero.  All PREP_THREADS threads share
+// the 2 x 2 output tiles; tiles above the diagonal are written as zero.
+__device__ __forceinline__ void mm_lower(float* R, const float* X, const float* Y, int tid) {
+  for (int tile = tid; tile < (C / 2) * (C / 2); tile += PREP_THREADS) {
+    const int r = 2 * (tile >> 5), c = 2 * (tile & 31);
+    float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+    for (int k = c; k <= r + 1; ++k) {
+      const float x0 = X[r * TS + k], x1 = X[(r + 1) * TS + k];
+      const float y0 = Y[k * TS + c], y1 = Y[k * TS + c + 1];
+      a00 = fmaf(x0, y0, a00); a01 = fmaf(x0, y1, a01);
+      a10 = fmaf(x1, y0, a10); a11 = fmaf(x1, y1, a11);
+    }
+    R[r * TS + c] = a00;
+    R[r * TS + c + 1] = a01;
+    R[(r + 1) * TS + c] = a10;
+    R[(r + 1) * TS + c + 1] = a11;
   }
 }
 
@@ -262,32 +282,32 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
     }
     __syncthreads();
     invert_unit_lower(sa, st, ss, tid);
-    // T and P as bf16 hi/lo pairs, g and beta
+    // P (lower triangular with the diagonal) into S, then P T into the A buffer
+    for (int idx = tid; idx < C * C; idx += PREP_THREADS) {
+      const int t = idx >> 6, s = idx & 63;
+      ss[t * TS + s] = s <= t ? __expf(sg[t] - sg[s]) * sqk[t * C + s] : 0.f;
+    }
+    __syncthreads();
+    mm_lower(sa, ss, st, tid);
+    __syncthreads();
+    // A = [T; P T] as bf16 hi/lo pairs, g and beta
     char* wsb = ws + ((size_t)c * Hv + h) * WS_STRIDE;
-    for (int idx = tid; idx < C * 8; idx += PREP_THREADS) {
-      const int t = idx >> 3, e8 = (idx & 7) * 8;
-      uint32_t th[4], tl[4], ph[4], pl[4];
+    for (int idx = tid; idx < 2 * C * 8; idx += PREP_THREADS) {
+      const int r = idx >> 3, e8 = (idx & 7) * 8;
+      const float* src = r < C ? st + r * TS : sa + (r - C) * TS;
+      uint32_t hv[4], lv[4];
 #pragma unroll
       for (int qd = 0; qd < 4; ++qd) {
-        const int s = e8 + 2 * qd;
         uint32_t h0, l0, h1, l1;
-        split_bf16(st[t * TS + s], h0, l0);
-        split_bf16(st[t * TS + s + 1], h1, l1);
-        th[qd] = h0 | (h1 << 16);
-        tl[qd] = l0 | (l1 << 16);
-        const float p0 = s <= t ? __expf(sg[t] - sg[s]) * sqk[t * C + s] : 0.f;
-        const float p1 = s + 1 <= t ? __expf(sg[t] - sg[s + 1]) * sqk[t * C + s + 1] : 0.f;
-        split_bf16(p0, h0, l0);
-        split_bf16(p1, h1, l1);
-        ph[qd] = h0 | (h1 << 16);
-        pl[qd] = l0 | (l1 << 16);
+        split_bf16(src[e8 + 2 * qd], h0, l0);
+        split_bf16(src[e8 + 2 * qd + 1], h1, l1);
+        hv[qd] = h0 | (h1 << 16);
+        lv[qd] = l0 | (l1 << 16);
       }
-      // 128-byte rows, 16-byte chunk ch of row t stored at chunk ch ^ (t & 7)
-      const int off = t * 128 + (((e8 >> 3) ^ (t & 7)) << 4);
-      *reinterpret_cast<uint4*>(wsb + WS_T_HI + off) = make_uint4(th[0], th[1], th[2], th[3]);
-      *reinterpret_cast<uint4*>(wsb + WS_T_LO + off) = make_uint4(tl[0], tl[1], tl[2], tl[3]);
-      *reinterpret_cast<uint4*>(wsb + WS_P_HI + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-      *reinterpret_cast<uint4*>(wsb + WS_P_LO + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+      // 128-byte rows, 16-byte chunk ch of row r stored at chunk ch ^ (r & 7)
+      const int off = r * 128 + (((e8 >> 3) ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(wsb + WS_AH + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      *reinterpret_cast<uint4*>(wsb + WS_AL + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
     }
     if (tid < C) {
       reinterpret_cast<float*>(wsb + WS_G)[tid] = __expf(sg[tid]);
@@ -300,376 +320,313 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
 }
 
 // ------------------------------------------------------------------- scan
-constexpr int SCAN_THREADS = 256;  // 8 warps
-constexpr int NTMAX = 6;           // 8-column tiles per state slab (<= 48 columns)
-constexpr int NTW = 3;             // tiles per warp in the chunk x slab products
-constexpr int VS = NTMAX * 16;     // staged V slab row (bytes)
+// One CTA of 8 warps per (value head, column slab of the state), sequential
+// over the chunks.  Every product is a tcgen05 MMA with M = 128 and the slab
+// width n as N, accumulating in TMEM:
+//
+//   D1 = [K; Q] H            rows 0-63: K H,      rows 64-127: Q H
+//   D2 = [T; P T] X          rows 0-63: Delta,    rows 64-127: P Delta
+//   D3 = K^T D'              rows = the d_k rows of the state update
+//
+// TMEM lane i is row i of each product.  Warp w reads lanes 32*(w%4) .. +31
+// and the columns of its half of the slab (w / 4), so each thread owns one
+// row and n/2 columns of D1, D2 and D3 and of the fp32 state.  The "chunk"
+// warps (lanes 0-63) turn K H into X and Delta into D' and carry the
+// recurrence; the "output" warps (lanes 64-127) keep Q H and finish
+// O = g Q H + P Delta while the next MMA runs, joining only for the state
+// update.  The B operands (H, X, D' as bf16 hi/lo pairs) are written by their
+// owners straight into the 128-byte-swizzle layout.  Thread 0 issues the MMAs
+// and, one chunk ahead, the TMA loads of K and Q and the bulk copy of the
+// chunk's workspace block, all completing on one mbarrier per buffer.
+constexpr int SCAN_THREADS = 256;
+constexpr int NMAX = 48;                     // widest column slab
+constexpr int NH = NMAX / 2;                 // columns per thread
+constexpr int TMEM_COLS = 256;               // D1 at column 0, D2 at 64, D3 at 128
+// one staging buffer: K and Q in two d_k halves of 128 rows x 128 bytes (K
+// rows 0-63, Q rows 64-127), then the workspace block as copied
+constexpr int SB_KQ = 0;
+constexpr int SB_KQ_HALF = 16384;
+constexpr int SB_W = 32768;
+constexpr int SB_SIZE = 66560;               // SB_W + WS_STRIDE, rounded up to 1 KB
+constexpr unsigned SB_TX = 4 * 8192 + WS_STRIDE;  // bytes landing per staged chunk
+static_assert(SB_W + WS_STRIDE <= SB_SIZE && SB_SIZE % 1024 == 0, "staging buffer layout");
+constexpr int SCAN_HB = 2 * SB_SIZE;         // H: [128 d_k rows][128 B], hi then lo
+constexpr int SCAN_XB = SCAN_HB + 2 * 16384;  // X: [64 chunk rows][128 B], hi then lo
+constexpr int SCAN_DB = SCAN_XB + 2 * 8192;   // D'
+constexpr int SCAN_BAR = SCAN_DB + 2 * 8192;  // mbarriers: staging [2], MMA; TMEM address
+constexpr int SCAN_SMEM = SCAN_BAR + 64 + 1024;  // + room to align the base to 1 KB
 
-// one staging buffer: K and Q rows (padded), the V slab, then the chunk's
-// workspace block copied as is (T hi/lo, P hi/lo in swizzled 128-byte rows, g, beta)
-constexpr int BUF_K = 0;
-constexpr int BUF_Q = BUF_K + C * KS;
-constexpr int BUF_V = BUF_Q + C * KS;
-constexpr int BUF_W = BUF_V + C * VS;
-constexpr int BUF_TH = BUF_W + WS_T_HI;
-constexpr int BUF_TL = BUF_W + WS_T_LO;
-constexpr int BUF_PH = BUF_W + WS_P_HI;
-constexpr int BUF_PL = BUF_W + WS_P_LO;
-constexpr int BUF_G = BUF_W + WS_G;
-constexpr int BUF_B = BUF_W + WS_B;
-constexpr int BUF_SIZE = BUF_W + WS_STRIDE;
-static_assert(BUF_W % 16 == 0 && BUF_SIZE % 16 == 0, "bulk copy destinations are 16-byte aligned");
-
-constexpr int SCAN_HTH = 2 * BUF_SIZE;          // H^T hi: [48][KS]
-constexpr int SCAN_HTL = SCAN_HTH + 48 * KS;
-constexpr int SCAN_XTH = SCAN_HTL + 48 * KS;    // X^T hi: [48][XS]
-constexpr int SCAN_XTL = SCAN_XTH + 48 * XS;
-constexpr int SCAN_DTH = SCAN_XTL + 48 * XS;    // Delta^T
-constexpr int SCAN_DTL = SCAN_DTH + 48 * XS;
-constexpr int SCAN_PTH = SCAN_DTL + 48 * XS;    // D'^T
-constexpr int SCAN_PTL = SCAN_PTH + 48 * XS;
-constexpr int SCAN_BAR = SCAN_PTL + 48 * XS;    // two mbarriers, one per buffer
-constexpr int SCAN_SMEM = SCAN_BAR + 16;
-
-// polls of an mbarrier before a block gives up on its staged chunk
+// polls of an mbarrier before a block gives up
 constexpr long long kWaitPolls = 1ll << 22;
 
-// the three column slabs of a 128-wide state: 48 + 40 + 40 columns
-__device__ __forceinline__ int slab_j0(int s) { return s == 0 ? 0 : (s == 1 ? 48 : 88); }
-__device__ __forceinline__ int slab_nt(int s) { return s == 0 ? 6 : 5; }
+// the three column slabs of a 128-wide state: 48 + 48 + 32 columns
+__device__ __forceinline__ int slab_width(int s) { return s == 2 ? 32 : 48; }
 
-__device__ __forceinline__ void st16(char* base, int idx, uint32_t v) {
-  reinterpret_cast<uint16_t*>(base)[idx] = static_cast<uint16_t>(v);
+// nh (16 or 24) fp32 columns of TMEM lane (warp quarter base + lane) starting
+// at `taddr`; columns past nh read as zero.
+__device__ __forceinline__ void tmem_cols(uint32_t taddr, int nh, float (&x)[NH]) {
+  uint32_t r0[8], r1[8], r2[8];
+  tc::tmem_ld8(taddr, r0);
+  tc::tmem_ld8(taddr + 8, r1);
+  if (nh > 16) tc::tmem_ld8(taddr + 16, r2);
+  tc::tmem_wait_ld(r0);
+  tc::tmem_wait_ld(r1);
+  if (nh > 16) {
+    tc::tmem_wait_ld(r2);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r2[e] = 0u;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    x[e] = __uint_as_float(r0[e]);
+    x[8 + e] = __uint_as_float(r1[e]);
+    x[16 + e] = __uint_as_float(r2[e]);
+  }
 }
 
-// A fragment (16 x 16 bf16, row-major, row stride `stride` bytes) at (m0, k0)
-__device__ __forceinline__ void load_a(uint32_t (&a)[4], const char* base, int stride, int m0,
-                                       int k0, int lane) {
-  const int q = lane >> 3, r = lane & 7;
-  ldmatrix_x4(a, base + (m0 + (q & 1) * 8 + r) * stride + (k0 + (q >> 1) * 8) * 2);
+// Columns [c0, c0 + nh) of row `row` of a bf16 hi/lo operand pair in the
+// 128-byte-swizzle layout (c0 and nh multiples of 8).
+__device__ __forceinline__ void put_split(char* hi, char* lo, int row, int c0,
+                                          const float (&x)[NH], int nh) {
+#pragma unroll
+  for (int cc = 0; cc < NH / 8; ++cc) {
+    if (cc * 8 < nh) {
+      uint32_t hv[4], lv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) tc::split_bf16x2(x[cc * 8 + 2 * e], x[cc * 8 + 2 * e + 1], hv[e], lv[e]);
+      const int off = row * 128 + ((((c0 >> 3) + cc) ^ (row & 7)) << 4);
+      *reinterpret_cast<uint4*>(hi + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      *reinterpret_cast<uint4*>(lo + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+    }
+  }
 }
 
-// A fragment (16 x 16) of a 64 x 64 bf16 matrix in swizzled 128-byte rows
-// (16-byte chunk ch of row r stored at chunk ch ^ (r & 7)) at (m0, k0)
-__device__ __forceinline__ void load_a_swz(uint32_t (&a)[4], const char* base, int m0, int k0,
-                                           int lane) {
-  const int q = lane >> 3, r = lane & 7;
-  const int row = m0 + (q & 1) * 8 + r, ch = (k0 >> 3) + (q >> 1);
-  ldmatrix_x4(a, base + row * 128 + ((ch ^ (row & 7)) << 4));
+// Barrier over the whole CTA that also orders tcgen05 operations and generic
+// shared-memory writes (made visible to the tensor cores) across it; returns
+// the AND of `ok` over the CTA.
+__device__ __forceinline__ bool tc_barrier(bool ok) {
+  fence_proxy_async_smem();
+  tc::fence_before_sync();
+  const bool all = __syncthreads_and(ok) != 0;
+  tc::fence_after_sync();
+  return all;
 }
 
-// B fragments of one 8-column tile for the hi and lo halves (stored [n][k],
-// row stride `stride` bytes): b[0], b[1] = hi; b[2], b[3] = lo.
-__device__ __forceinline__ void load_b_pair(uint32_t (&b)[4], const char* hi, const char* lo,
-                                            int stride, int n0, int k0, int lane) {
-  const int q = lane >> 3, r = lane & 7;
-  ldmatrix_x4(b, (q < 2 ? hi : lo) + (n0 + r) * stride + (k0 + (q & 1) * 8) * 2);
+// The same over the chunk warps only (warps 0, 1, 4, 5; barrier 1).
+__device__ __forceinline__ void chunk_barrier() {
+  fence_proxy_async_smem();
+  tc::fence_before_sync();
+  tc::named_barrier(1, SCAN_THREADS / 2);
+  tc::fence_after_sync();
 }
 
 __global__ void __launch_bounds__(SCAN_THREADS, 1)
-scan_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
             const uint16_t* __restrict__ v, float* __restrict__ state, float* __restrict__ o,
             const char* __restrict__ ws, int T, int Hk, int Hv) {
-  extern __shared__ __align__(16) char smem[];
+  extern __shared__ __align__(1024) char smem_raw[];
+  char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int sl = blockIdx.x, h = blockIdx.y, hk = h / (Hv / Hk);
-  const int j0 = slab_j0(sl), NT = slab_nt(sl);
+  const int j0 = 48 * sl, n = slab_width(sl), nh = n / 2;
   const int n_chunks = (T + C - 1) / C;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int g8 = lane >> 2, t4 = lane & 3;
-  const int mt = w & 3, nt0 = (w >> 2) * NTW;  // this warp's chunk rows and column tiles
-  char* hth = smem + SCAN_HTH;
-  char* htl = smem + SCAN_HTL;
-  char* xth = smem + SCAN_XTH;
-  char* xtl = smem + SCAN_XTL;
-  char* dth = smem + SCAN_DTH;
-  char* dtl = smem + SCAN_DTL;
-  char* pth = smem + SCAN_PTH;
-  char* ptl = smem + SCAN_PTL;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int qd = w & 3, c0 = (w >> 2) * nh;  // lane quarter; first slab column of this thread
+  const int r = 32 * qd + lane;              // TMEM lane: row of D1 / D2 / D3
+  const bool chunk_warp = qd < 2;            // rows 0-63: K H, Delta
+  const int row = r & (C - 1);               // chunk row (D1 / D2)
+  char* hb_hi = smem + SCAN_HB;
+  char* hb_lo = hb_hi + 16384;
+  char* xb_hi = smem + SCAN_XB;
+  char* xb_lo = xb_hi + 8192;
+  char* db_hi = smem + SCAN_DB;
+  char* db_lo = db_hi + 8192;
+  // mbarriers: [0], [1] staging buffers; [2], [3], [4] completion of the
+  // chunk's first, second and third MMA group (one phase per chunk each)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SCAN_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + SCAN_BAR + 40);
 
-  // Staging of one chunk: the chunk's workspace block (33 KB, contiguous) by a
-  // single bulk (TMA) copy completing on the buffer's mbarrier; the K, Q and V
-  // slab rows by 16-byte cp.async spread over all threads, whose (row, piece)
-  // assignment is the same for every chunk, so the offsets are computed once.
-  // Rows past the end of the sequence read as zero.  The buffer being filled
-  // was last read before the previous iteration's closing barrier.
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + SCAN_BAR);
   if (tid == 0) {
-    mbar_init(&mbar[0], 1);
-    mbar_init(&mbar[1], 1);
+    for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
     mbar_init_fence();
   }
-  __syncthreads();
-  constexpr int KQ_PER = C * 16 / SCAN_THREADS;
-  int kq_row[KQ_PER], kq_dst[KQ_PER], kq_src[KQ_PER];
-#pragma unroll
-  for (int u = 0; u < KQ_PER; ++u) {
-    const int idx = tid + u * SCAN_THREADS, r = idx >> 4, ch = idx & 15;
-    kq_row[u] = r;
-    kq_dst[u] = r * KS + ch * 16;
-    kq_src[u] = (r * Hk + hk) * DK + ch * 8;  // elements, relative to the chunk's first row
+  if (w == 0) {
+    tc::tmem_alloc(tslot, TMEM_COLS);
+    tc::tmem_relinquish();
   }
-  int v_row[2], v_dst[2], v_src[2];
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int idx = tid + u * SCAN_THREADS;
-    const int r = idx < C * NT ? idx / NT : C, ch = idx < C * NT ? idx - (idx / NT) * NT : 0;
-    v_row[u] = r;
-    v_dst[u] = r * VS + ch * 16;
-    v_src[u] = (r * Hv + h) * DV + j0 + ch * 8;
-  }
+  tc_barrier(true);
+  const uint32_t tmem = *tslot;
+  const uint32_t t_mine = tmem + ((uint32_t)(32 * qd) << 16) + c0;
+
+  // Staging of chunk c into buffer buf (thread 0): K and Q as four TMA tiles
+  // of 64 rows x 64 columns in the 128-byte swizzle (rows past the end of the
+  // sequence arrive as zero), and the workspace block by one bulk copy.
   auto stage = [&](int c, int buf) {
-    char* B = smem + buf * BUF_SIZE;
-    const int t0 = c * C, nv = min(C, T - t0);
-    if (tid == 0) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&mbar[buf], (unsigned)WS_STRIDE);
-      bulk_g2s(B + BUF_W, ws + ((size_t)c * Hv + h) * WS_STRIDE, WS_STRIDE, &mbar[buf]);
-    }
-    const uint16_t* kb = k + (size_t)t0 * Hk * DK;
-    const uint16_t* qb = q + (size_t)t0 * Hk * DK;
-    const uint16_t* vbase = v + (size_t)t0 * Hv * DV;
-#pragma unroll
-    for (int u = 0; u < KQ_PER; ++u) {
-      const bool valid = kq_row[u] < nv;
-      const int src = valid ? kq_src[u] : 0;
-      cp_async16_zfill(B + BUF_K + kq_dst[u], kb + src, valid);
-      cp_async16_zfill(B + BUF_Q + kq_dst[u], qb + src, valid);
-    }
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      if (v_row[u] < C) {
-        const bool valid = v_row[u] < nv;
-        cp_async16_zfill(B + BUF_V + v_dst[u], vbase + (valid ? v_src[u] : 0), valid);
-      }
-    }
-    cp_async_commit();
+    char* B = smem + buf * SB_SIZE;
+    const int t0 = c * C;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&bar[buf], SB_TX);
+    tc::tma_load_2d(B + SB_KQ, &tm_k, hk * DK, t0, &bar[buf]);
+    tc::tma_load_2d(B + SB_KQ + SB_KQ_HALF, &tm_k, hk * DK + 64, t0, &bar[buf]);
+    tc::tma_load_2d(B + SB_KQ + C * 128, &tm_q, hk * DK, t0, &bar[buf]);
+    tc::tma_load_2d(B + SB_KQ + SB_KQ_HALF + C * 128, &tm_q, hk * DK + 64, t0, &bar[buf]);
+    bulk_g2s(B + SB_W, ws + ((size_t)c * Hv + h) * WS_STRIDE, WS_STRIDE, &bar[buf]);
   };
 
-  // ---- this warp's 16 state rows (16w + g8 (+8)), all slab columns (nt*8 + 2t4)
-  float Hf[NTMAX][4];
-  float* sth = state + (size_t)h * DK * DV + j0;
-  const int ia = 16 * w + g8;
+  // this thread's part of the state: d_k row r, slab columns c0 .. c0+nh-1
+  float Hr[NH];
+  float* srow = state + ((size_t)h * DK + r) * DV + j0 + c0;
 #pragma unroll
-  for (int nt = 0; nt < NTMAX; ++nt) {
-    if (nt < NT) {
-      const int jj = nt * 8 + t4 * 2;
-      const float2 x = *reinterpret_cast<const float2*>(sth + (size_t)ia * DV + jj);
-      const float2 y = *reinterpret_cast<const float2*>(sth + (size_t)(ia + 8) * DV + jj);
-      Hf[nt][0] = x.x; Hf[nt][1] = x.y; Hf[nt][2] = y.x; Hf[nt][3] = y.y;
-    } else {
-      Hf[nt][0] = Hf[nt][1] = Hf[nt][2] = Hf[nt][3] = 0.f;
-    }
+  for (int e = 0; e < NH; e += 4) {
+    const float4 x = e < nh ? *reinterpret_cast<const float4*>(srow + e)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    Hr[e] = x.x; Hr[e + 1] = x.y; Hr[e + 2] = x.z; Hr[e + 3] = x.w;
   }
-  // H^T as bf16 hi/lo: element (j, i) at j*KS/2 + i
-  auto write_ht = [&]() {
-#pragma unroll
-    for (int nt = 0; nt < NTMAX; ++nt) {
-      if (nt < NT) {
-        const int jj = nt * 8 + t4 * 2;
-        const int idx[4] = {jj * (KS / 2) + ia, (jj + 1) * (KS / 2) + ia, jj * (KS / 2) + ia + 8,
-                            (jj + 1) * (KS / 2) + ia + 8};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint32_t hi, lo;
-          split_bf16(Hf[nt][e], hi, lo);
-          st16(hth, idx[e], hi);
-          st16(htl, idx[e], lo);
-        }
-      }
-    }
-  };
-  write_ht();
-  stage(0, 0);
+  put_split(hb_hi, hb_lo, r, c0, Hr, nh);
+  if (tid == 0) stage(0, 0);
+  int inflight = 0;  // chunk whose staging is in flight, or -1
 
-  const int ta = 16 * mt + g8, tb = ta + 8;  // this thread's chunk rows
+  const uint32_t id_ab = tc::idesc_bf16_f32(128, n, false, true);  // A K-major, B MN-major
+  const uint32_t id_kt = tc::idesc_bf16_f32(128, n, true, true);   // A = K^T (MN-major)
+  const uint32_t s_hb = smem_addr(hb_hi), s_xb = smem_addr(xb_hi), s_db = smem_addr(db_hi);
+  bool ok = true;
   for (int c = 0; c < n_chunks; ++c) {
-    const int buf = c & 1;
-    const int nv = min(C, T - c * C);
+    const int buf = c & 1, t0 = c * C, nv = min(C, T - t0);
+    const unsigned par = c & 1;
+    char* B = smem + buf * SB_SIZE;
+    // V row of the chunk warps (read from global; consumed after the first MMA)
+    uint4 vr[NH / 8];
+    if (chunk_warp) {
+      const uint4* vsrc = reinterpret_cast<const uint4*>(
+          v + ((size_t)(t0 + (row < nv ? row : 0)) * Hv + h) * DV + j0 + c0);
+#pragma unroll
+      for (int e = 0; e < NH / 8; ++e)
+        vr[e] = (e * 8 < nh && row < nv) ? __ldg(vsrc + e) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    ok = tc_barrier(ok && mbar_wait_bounded(&bar[buf], (c >> 1) & 1, kWaitPolls));
+    if (!ok) break;
+    inflight = -1;
     if (c + 1 < n_chunks) {
-      stage(c + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+      if (tid == 0) stage(c + 1, buf ^ 1);
+      inflight = c + 1;
     }
-    // chunk c is the (c/2)-th use of its buffer: wait for that phase
-    if (!__syncthreads_and(mbar_wait_bounded(&mbar[buf], (c >> 1) & 1, kWaitPolls))) {
-      // a staged chunk never arrived: give the copies in flight a last bounded
-      // chance to land, mark this block's state slab as failed (NaN), stop
-      mbar_wait_bounded(&mbar[buf ^ 1], ((c + 1) >> 1) & 1, kWaitPolls);
-      for (int idx = tid; idx < DK * 8 * NT; idx += SCAN_THREADS)
-        sth[(size_t)(idx / (8 * NT)) * DV + idx % (8 * NT)] = __int_as_float(0x7fc00000);
-      return;
-    }
-    const char* B = smem + buf * BUF_SIZE;
-    const float* bg = reinterpret_cast<const float*>(B + BUF_G);
-    const float* bb = reinterpret_cast<const float*>(B + BUF_B);
+    const uint32_t s_kq = smem_addr(B + SB_KQ);
+    const uint32_t s_ah = smem_addr(B + SB_W + WS_AH), s_al = smem_addr(B + SB_W + WS_AL);
+    const float* bg = reinterpret_cast<const float*>(B + SB_W + WS_G);
+    const float* bb = reinterpret_cast<const float*>(B + SB_W + WS_B);
 
-    // ---- K H and Q H: rows of m-tile mt, column tiles nt0 .. nt0+2
-    float kh[NTW][4], qh[NTW][4];
+    // ---- D1 = [K; Q] (H_hi + H_lo)
+    if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < NTW; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) kh[i][e] = qh[i][e] = 0.f;
-#pragma unroll
-    for (int kc = 0; kc < DK / 16; ++kc) {
-      uint32_t ak[4], aq[4];
-      load_a(ak, B + BUF_K, KS, 16 * mt, kc * 16, lane);
-      load_a(aq, B + BUF_Q, KS, 16 * mt, kc * 16, lane);
-#pragma unroll
-      for (int i = 0; i < NTW; ++i) {
-        if (nt0 + i < NT) {
-          uint32_t b[4];
-          load_b_pair(b, hth, htl, KS, (nt0 + i) * 8, kc * 16, lane);
-          mma_bf16_16816(kh[i], ak, b[0], b[1]);
-          mma_bf16_16816(kh[i], ak, b[2], b[3]);
-          mma_bf16_16816(qh[i], aq, b[0], b[1]);
-          mma_bf16_16816(qh[i], aq, b[2], b[3]);
-        }
+      for (int s = 0; s < DK / 16; ++s) {
+        const uint64_t a = tc::sdesc_sw128(s_kq + (s >> 2) * SB_KQ_HALF + (s & 3) * 32, 16, 1024);
+        tc::mma_bf16(tmem, a, tc::sdesc_sw128(s_hb + s * 2048, 16384, 1024), id_ab, s > 0);
+        tc::mma_bf16(tmem, a, tc::sdesc_sw128(s_hb + 16384 + s * 2048, 16384, 1024), id_ab, 1);
       }
+      tc::mma_commit(&bar[2]);
     }
-    // ---- X = beta (V - g K H), stored transposed as bf16 hi/lo
+    const float g_r = bg[row], b_r = bb[row], gC = bg[C - 1];
+    ok = mbar_wait_bounded(&bar[2], par, kWaitPolls) && ok;
+    tc::fence_after_sync();
+    float qh[NH];
     {
-      const float ga = bg[ta], gb = bg[tb], ba = bb[ta], bbv = bb[tb];
-      const char* va = B + BUF_V + ta * VS;
-      const char* vb = B + BUF_V + tb * VS;
+      float x[NH];
+      tmem_cols(t_mine, nh, x);
+      if (chunk_warp) {
+        // X = beta (V - g K H)
 #pragma unroll
-      for (int i = 0; i < NTW; ++i) {
-        if (nt0 + i < NT) {
-          const int jj = (nt0 + i) * 8 + t4 * 2;
-          const uint32_t pa = ld32(va + jj * 2), pb = ld32(vb + jj * 2);
-          const float x[4] = {ba * (__uint_as_float(pa << 16) - ga * kh[i][0]),
-                              ba * (__uint_as_float(pa & 0xffff0000u) - ga * kh[i][1]),
-                              bbv * (__uint_as_float(pb << 16) - gb * kh[i][2]),
-                              bbv * (__uint_as_float(pb & 0xffff0000u) - gb * kh[i][3])};
-          const int idx[4] = {jj * (XS / 2) + ta, (jj + 1) * (XS / 2) + ta, jj * (XS / 2) + tb,
-                              (jj + 1) * (XS / 2) + tb};
+        for (int e = 0; e < NH / 8; ++e) {
+          const uint32_t p[4] = {vr[e].x, vr[e].y, vr[e].z, vr[e].w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint32_t hi, lo;
-            split_bf16(x[e], hi, lo);
-            st16(xth, idx[e], hi);
-            st16(xtl, idx[e], lo);
+          for (int u = 0; u < 4; ++u) {
+            const int j = e * 8 + 2 * u;
+            x[j] = b_r * (__uint_as_float(p[u] << 16) - g_r * x[j]);
+            x[j + 1] = b_r * (__uint_as_float(p[u] & 0xffff0000u) - g_r * x[j + 1]);
           }
         }
-      }
-    }
-    __syncthreads();
-
-    // ---- Delta = T X (T lower triangular: k-blocks 0..mt)
-    float dl[NTW][4];
+        put_split(xb_hi, xb_lo, row, c0, x, nh);
+        chunk_barrier();
+        // ---- D2 = [T; P T] X  (hi*hi + hi*lo + lo*hi)
+        if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < NTW; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) dl[i][e] = 0.f;
-    for (int kc = 0; kc <= mt; ++kc) {
-      uint32_t ah[4], al[4];
-      load_a_swz(ah, B + BUF_TH, 16 * mt, kc * 16, lane);
-      load_a_swz(al, B + BUF_TL, 16 * mt, kc * 16, lane);
-#pragma unroll
-      for (int i = 0; i < NTW; ++i) {
-        if (nt0 + i < NT) {
-          uint32_t b[4];
-          load_b_pair(b, xth, xtl, XS, (nt0 + i) * 8, kc * 16, lane);
-          mma_bf16_16816(dl[i], ah, b[0], b[1]);
-          mma_bf16_16816(dl[i], ah, b[2], b[3]);
-          mma_bf16_16816(dl[i], al, b[0], b[1]);
-        }
-      }
-    }
-    const float gC = bg[C - 1];
-    {
-      const float ra = gC / bg[ta], rbv = gC / bg[tb];
-#pragma unroll
-      for (int i = 0; i < NTW; ++i) {
-        if (nt0 + i < NT) {
-          const int jj = (nt0 + i) * 8 + t4 * 2;
-          const int idx[4] = {jj * (XS / 2) + ta, (jj + 1) * (XS / 2) + ta, jj * (XS / 2) + tb,
-                              (jj + 1) * (XS / 2) + tb};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint32_t hi, lo;
-            split_bf16(dl[i][e], hi, lo);
-            st16(dth, idx[e], hi);
-            st16(dtl, idx[e], lo);
-            split_bf16((e < 2 ? ra : rbv) * dl[i][e], hi, lo);
-            st16(pth, idx[e], hi);
-            st16(ptl, idx[e], lo);
+          for (int s = 0; s < C / 16; ++s) {
+            const uint64_t ah = tc::sdesc_sw128(s_ah + s * 32, 16, 1024);
+            const uint64_t al = tc::sdesc_sw128(s_al + s * 32, 16, 1024);
+            const uint64_t xh = tc::sdesc_sw128(s_xb + s * 2048, 8192, 1024);
+            const uint64_t xl = tc::sdesc_sw128(s_xb + 8192 + s * 2048, 8192, 1024);
+            tc::mma_bf16(tmem + 64, ah, xh, id_ab, s > 0);
+            tc::mma_bf16(tmem + 64, ah, xl, id_ab, 1);
+            tc::mma_bf16(tmem + 64, al, xh, id_ab, 1);
           }
+          tc::mma_commit(&bar[3]);
         }
+      } else {
+#pragma unroll
+        for (int e = 0; e < NH; ++e) qh[e] = g_r * x[e];
       }
     }
-    __syncthreads();
-
-    // ---- O = g Q H + P Delta (P lower triangular incl. the diagonal)
+    ok = mbar_wait_bounded(&bar[3], par, kWaitPolls) && ok;
+    tc::fence_after_sync();
     {
-      const float ga = bg[ta], gb = bg[tb];
+      float x[NH];
+      tmem_cols(t_mine + 64, nh, x);
+      if (chunk_warp) {
+        // D' = (g_C / g) Delta
+        const float rg = gC / g_r;
 #pragma unroll
-      for (int i = 0; i < NTW; ++i) {
-        qh[i][0] *= ga; qh[i][1] *= ga; qh[i][2] *= gb; qh[i][3] *= gb;
-      }
-      for (int kc = 0; kc <= mt; ++kc) {
-        uint32_t ah[4], al[4];
-        load_a_swz(ah, B + BUF_PH, 16 * mt, kc * 16, lane);
-        load_a_swz(al, B + BUF_PL, 16 * mt, kc * 16, lane);
+        for (int e = 0; e < NH; ++e) x[e] *= rg;
+        put_split(db_hi, db_lo, row, c0, x, nh);
+        chunk_barrier();
+        // ---- D3 = K^T (D'_hi + D'_lo)
+        if (tid == 0) {
 #pragma unroll
-        for (int i = 0; i < NTW; ++i) {
-          if (nt0 + i < NT) {
-            uint32_t b[4];
-            load_b_pair(b, dth, dtl, XS, (nt0 + i) * 8, kc * 16, lane);
-            mma_bf16_16816(qh[i], ah, b[0], b[1]);
-            mma_bf16_16816(qh[i], ah, b[2], b[3]);
-            mma_bf16_16816(qh[i], al, b[0], b[1]);
+          for (int s = 0; s < C / 16; ++s) {
+            const uint64_t a = tc::sdesc_sw128(s_kq + s * 2048, SB_KQ_HALF, 1024);
+            tc::mma_bf16(tmem + 128, a, tc::sdesc_sw128(s_db + s * 2048, 8192, 1024), id_kt,
+                         s > 0);
+            tc::mma_bf16(tmem + 128, a, tc::sdesc_sw128(s_db + 8192 + s * 2048, 8192, 1024),
+                         id_kt, 1);
           }
+          tc::mma_commit(&bar[4]);
         }
-      }
-      float* oa = o + ((size_t)(c * C + ta) * Hv + h) * DV + j0;
-      float* ob = o + ((size_t)(c * C + tb) * Hv + h) * DV + j0;
+      } else if (row < nv) {
+        // O = g Q H + P Delta
+        float* orow = o + ((size_t)(t0 + row) * Hv + h) * DV + j0 + c0;
 #pragma unroll
-      for (int i = 0; i < NTW; ++i) {
-        if (nt0 + i < NT) {
-          const int jj = (nt0 + i) * 8 + t4 * 2;
-          if (ta < nv) *reinterpret_cast<float2*>(oa + jj) = make_float2(qh[i][0], qh[i][1]);
-          if (tb < nv) *reinterpret_cast<float2*>(ob + jj) = make_float2(qh[i][2], qh[i][3]);
-        }
+        for (int e = 0; e < NH; e += 4)
+          if (e < nh)
+            *reinterpret_cast<float4*>(orow + e) =
+                make_float4(qh[e] + x[e], qh[e + 1] + x[e + 1], qh[e + 2] + x[e + 2],
+                            qh[e + 3] + x[e + 3]);
       }
     }
-
-    // ---- H <- g_C H + K^T D'  (A = K^T tiles through ldmatrix.trans)
-#pragma unroll
-    for (int nt = 0; nt < NTMAX; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) Hf[nt][e] *= gC;
+    // ---- H <- g_C H + D3
+    ok = mbar_wait_bounded(&bar[4], par, kWaitPolls) && ok;
+    tc::fence_after_sync();
     {
-      const int q4 = lane >> 3, r8 = lane & 7;
+      float x[NH];
+      tmem_cols(t_mine + 128, nh, x);
 #pragma unroll
-      for (int kc = 0; kc < C / 16; ++kc) {
-        const int row = kc * 16 + ((q4 & 2) ? 8 : 0) + r8;
-        const int col = 16 * w + ((q4 & 1) ? 8 : 0);
-        uint32_t a[4];
-        ldmatrix_x4_trans(a, B + BUF_K + row * KS + col * 2);
-#pragma unroll
-        for (int nt = 0; nt < NTMAX; ++nt) {
-          if (nt < NT) {
-            uint32_t b[4];
-            load_b_pair(b, pth, ptl, XS, nt * 8, kc * 16, lane);
-            mma_bf16_16816(Hf[nt], a, b[0], b[1]);
-            mma_bf16_16816(Hf[nt], a, b[2], b[3]);
-          }
-        }
-      }
+      for (int e = 0; e < NH; ++e) Hr[e] = fmaf(gC, Hr[e], x[e]);
+      put_split(hb_hi, hb_lo, r, c0, Hr, nh);
     }
-    write_ht();
-    __syncthreads();
   }
 
+  ok = tc_barrier(ok);
+  if (!ok) {
+    // a staged chunk or an MMA never completed: give the staging still in
+    // flight a last bounded chance to land, then mark the slab as failed
+    if (tid == 0 && inflight >= 0)
+      mbar_wait_bounded(&bar[inflight & 1], (inflight >> 1) & 1, kWaitPolls);
 #pragma unroll
-  for (int nt = 0; nt < NTMAX; ++nt) {
-    if (nt < NT) {
-      const int jj = nt * 8 + t4 * 2;
-      *reinterpret_cast<float2*>(sth + (size_t)ia * DV + jj) = make_float2(Hf[nt][0], Hf[nt][1]);
-      *reinterpret_cast<float2*>(sth + (size_t)(ia + 8) * DV + jj) = make_float2(Hf[nt][2], Hf[nt][3]);
-    }
+    for (int e = 0; e < NH; ++e) Hr[e] = __int_as_float(0x7fc00000);
   }
+#pragma unroll
+  for (int e = 0; e < NH; e += 4)
+    if (e < nh)
+      *reinterpret_cast<float4*>(srow + e) = make_float4(Hr[e], Hr[e + 1], Hr[e + 2], Hr[e + 3]);
+  tc_barrier(true);
+  if (w == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
 }  // namespace
@@ -727,11 +684,50 @@ size_t prefill_workspace_bytes(int T, int Hk, int Hv, int dk, int dv, int chunk)
   return n_chunks * (size_t)Hv * WS_STRIDE;
 }
 
+namespace {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); null if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult res;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &res) != cudaSuccess ||
+        res != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// K or Q ([T][Hk][128] bf16) as a 2-D tensor of T rows and Hk*128 columns,
+// read in 64 x 64 tiles with the 128-byte swizzle; rows past T read as zero.
+int kq_tensor_map(CUtensorMap* m, const void* base, int T, int Hk) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return GDN_ERR_CUDA;
+  const cuuint64_t dims[2] = {(cuuint64_t)Hk * DK, (cuuint64_t)T};
+  const cuuint64_t strides[1] = {(cuuint64_t)Hk * DK * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                         strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
 int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const float* alpha,
                    const float* beta, int T, int Hk, int Hv, int dk, int dv, int chunk,
                    float* state, float* o, void* workspace, cudaStream_t stream) {
   if (!bf16 || dk != DK || dv != DV || chunk != C) return GDN_ERR_UNSUPPORTED;
   const int n_chunks = (T + C - 1) / C;
+  CUtensorMap tm_k, tm_q;
+  int st = kq_tensor_map(&tm_k, k, T, Hk);
+  if (st == GDN_OK) st = kq_tensor_map(&tm_q, q, T, Hk);
+  if (st != GDN_OK) return st;
   if (cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            PREP_SMEM) != cudaSuccess ||
       cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -740,11 +736,11 @@ int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const
   prep_kernel<<<dim3(n_chunks, Hk), PREP_THREADS, PREP_SMEM, stream>>>(
       static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), alpha, beta, T, Hk, Hv,
       static_cast<char*>(workspace));
-  int st = launch_status();
+  st = launch_status();
   if (st != GDN_OK) return st;
   scan_kernel<<<dim3(3, Hv), SCAN_THREADS, SCAN_SMEM, stream>>>(
-      static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
-      static_cast<const uint16_t*>(v), state, o, static_cast<const char*>(workspace), T, Hk, Hv);
+      tm_k, tm_q, static_cast<const uint16_t*>(v), state, o, static_cast<const char*>(workspace),
+      T, Hk, Hv);
   return launch_status();
 }
 
