@@ -341,7 +341,7 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
 constexpr int SCAN_THREADS = 256;
 constexpr int NMAX = 48;                     // widest column slab
 constexpr int NH = NMAX / 2;                 // columns per thread
-constexpr int TMEM_COLS = 256;               // D1 at column 0, D2 at 64, D3 at 128
+constexpr int TMEM_COLS = 512;               // D1 at column 0, D2 at 128, D3 at 256
 // one staging buffer: K and Q in two d_k halves of 128 rows x 128 bytes (K
 // rows 0-63, Q rows 64-127), then the workspace block as copied
 constexpr int SB_KQ = 0;
@@ -350,8 +350,10 @@ constexpr int SB_W = 32768;
 constexpr int SB_SIZE = 66560;               // SB_W + WS_STRIDE, rounded up to 1 KB
 constexpr unsigned SB_TX = 4 * 8192 + WS_STRIDE;  // bytes landing per staged chunk
 static_assert(SB_W + WS_STRIDE <= SB_SIZE && SB_SIZE % 1024 == 0, "staging buffer layout");
-constexpr int SCAN_HB = 2 * SB_SIZE;         // H: [128 d_k rows][128 B], hi then lo
-constexpr int SCAN_XB = SCAN_HB + 2 * 16384;  // X: [64 chunk rows][128 B], hi then lo
+// B operands [hi | lo] side by side (2n columns, MN-major): columns 0-63 in
+// the first block of 128-byte rows, 64-127 in the second
+constexpr int SCAN_HB = 2 * SB_SIZE;         // H: 2 blocks of [128 d_k rows][128 B]
+constexpr int SCAN_XB = SCAN_HB + 2 * 16384;  // X: 2 blocks of [64 chunk rows][128 B]
 constexpr int SCAN_DB = SCAN_XB + 2 * 8192;   // D'
 constexpr int SCAN_BAR = SCAN_DB + 2 * 8192;  // mbarriers: staging [2], MMA; TMEM address
 constexpr int SCAN_SMEM = SCAN_BAR + 64 + 1024;  // + room to align the base to 1 KB
@@ -385,19 +387,34 @@ __device__ __forceinline__ void tmem_cols(uint32_t taddr, int nh, float (&x)[NH]
   }
 }
 
-// Columns [c0, c0 + nh) of row `row` of a bf16 hi/lo operand pair in the
-// 128-byte-swizzle layout (c0 and nh multiples of 8).
-__device__ __forceinline__ void put_split(char* hi, char* lo, int row, int c0,
+// An accumulator of the [hi | lo] products: columns c .. c+nh-1 (at `taddr`)
+// plus columns n+c .. n+c+nh-1.
+__device__ __forceinline__ void tmem_cols_sum(uint32_t taddr, int n, int nh, float (&x)[NH]) {
+  float y[NH];
+  tmem_cols(taddr, nh, x);
+  tmem_cols(taddr + n, nh, y);
+#pragma unroll
+  for (int e = 0; e < NH; ++e) x[e] += y[e];
+}
+
+// Row `row`, columns c0 .. c0+nh-1 of an fp32 matrix as bf16 hi (columns c0..)
+// and lo (columns n+c0..) of a [hi | lo] operand: MN-major, 128-byte swizzle,
+// 64 columns per block of rows, blocks `blk` bytes apart (c0, n, nh multiples
+// of 8).
+__device__ __forceinline__ void put_split(char* base, int blk, int row, int c0, int n,
                                           const float (&x)[NH], int nh) {
 #pragma unroll
   for (int cc = 0; cc < NH / 8; ++cc) {
     if (cc * 8 < nh) {
       uint32_t hv[4], lv[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) tc::split_bf16x2(x[cc * 8 + 2 * e], x[cc * 8 + 2 * e + 1], hv[e], lv[e]);
-      const int off = row * 128 + ((((c0 >> 3) + cc) ^ (row & 7)) << 4);
-      *reinterpret_cast<uint4*>(hi + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-      *reinterpret_cast<uint4*>(lo + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+      for (int e = 0; e < 4; ++e)
+        tc::split_bf16x2(x[cc * 8 + 2 * e], x[cc * 8 + 2 * e + 1], hv[e], lv[e]);
+      const int ch = c0 + cc * 8, cl = n + ch;
+      const int oh = (ch >> 6) * blk + row * 128 + ((((ch & 63) >> 3) ^ (row & 7)) << 4);
+      const int ol = (cl >> 6) * blk + row * 128 + ((((cl & 63) >> 3) ^ (row & 7)) << 4);
+      *reinterpret_cast<uint4*>(base + oh) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      *reinterpret_cast<uint4*>(base + ol) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
     }
   }
 }
@@ -435,12 +452,9 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
   const int r = 32 * qd + lane;              // TMEM lane: row of D1 / D2 / D3
   const bool chunk_warp = qd < 2;            // rows 0-63: K H, Delta
   const int row = r & (C - 1);               // chunk row (D1 / D2)
-  char* hb_hi = smem + SCAN_HB;
-  char* hb_lo = hb_hi + 16384;
-  char* xb_hi = smem + SCAN_XB;
-  char* xb_lo = xb_hi + 8192;
-  char* db_hi = smem + SCAN_DB;
-  char* db_lo = db_hi + 8192;
+  char* hb = smem + SCAN_HB;
+  char* xb = smem + SCAN_XB;
+  char* db = smem + SCAN_DB;
   // mbarriers: [0], [1] staging buffers; [2], [3], [4] completion of the
   // chunk's first, second and third MMA group (one phase per chunk each)
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SCAN_BAR);
@@ -482,13 +496,15 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
                             : make_float4(0.f, 0.f, 0.f, 0.f);
     Hr[e] = x.x; Hr[e + 1] = x.y; Hr[e + 2] = x.z; Hr[e + 3] = x.w;
   }
-  put_split(hb_hi, hb_lo, r, c0, Hr, nh);
+  put_split(hb, 16384, r, c0, n, Hr, nh);
   if (tid == 0) stage(0, 0);
   int inflight = 0;  // chunk whose staging is in flight, or -1
 
-  const uint32_t id_ab = tc::idesc_bf16_f32(128, n, false, true);  // A K-major, B MN-major
-  const uint32_t id_kt = tc::idesc_bf16_f32(128, n, true, true);   // A = K^T (MN-major)
-  const uint32_t s_hb = smem_addr(hb_hi), s_xb = smem_addr(xb_hi), s_db = smem_addr(db_hi);
+  // A K-major or MN-major (K^T); B MN-major with 2n ([hi | lo]) or n (hi) columns
+  const uint32_t id_cat = tc::idesc_bf16_f32(128, 2 * n, false, true);
+  const uint32_t id_hi = tc::idesc_bf16_f32(128, n, false, true);
+  const uint32_t id_kt = tc::idesc_bf16_f32(128, 2 * n, true, true);
+  const uint32_t s_hb = smem_addr(hb), s_xb = smem_addr(xb), s_db = smem_addr(db);
   bool ok = true;
   for (int c = 0; c < n_chunks; ++c) {
     const int buf = c & 1, t0 = c * C, nv = min(C, T - t0);
@@ -505,25 +521,24 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     }
     ok = tc_barrier(ok && mbar_wait_bounded(&bar[buf], (c >> 1) & 1, kWaitPolls));
     if (!ok) break;
-    inflight = -1;
-    if (c + 1 < n_chunks) {
-      if (tid == 0) stage(c + 1, buf ^ 1);
-      inflight = c + 1;
-    }
     const uint32_t s_kq = smem_addr(B + SB_KQ);
     const uint32_t s_ah = smem_addr(B + SB_W + WS_AH), s_al = smem_addr(B + SB_W + WS_AL);
     const float* bg = reinterpret_cast<const float*>(B + SB_W + WS_G);
     const float* bb = reinterpret_cast<const float*>(B + SB_W + WS_B);
 
-    // ---- D1 = [K; Q] (H_hi + H_lo)
+    // ---- D1 = [K; Q] [H_hi | H_lo]; then the next chunk's staging
     if (tid == 0) {
 #pragma unroll
       for (int s = 0; s < DK / 16; ++s) {
         const uint64_t a = tc::sdesc_sw128(s_kq + (s >> 2) * SB_KQ_HALF + (s & 3) * 32, 16, 1024);
-        tc::mma_bf16(tmem, a, tc::sdesc_sw128(s_hb + s * 2048, 16384, 1024), id_ab, s > 0);
-        tc::mma_bf16(tmem, a, tc::sdesc_sw128(s_hb + 16384 + s * 2048, 16384, 1024), id_ab, 1);
+        tc::mma_bf16(tmem, a, tc::sdesc_sw128(s_hb + s * 2048, 16384, 1024), id_cat, s > 0);
       }
       tc::mma_commit(&bar[2]);
+    }
+    inflight = -1;
+    if (c + 1 < n_chunks) {
+      if (tid == 0) stage(c + 1, buf ^ 1);
+      inflight = c + 1;
     }
     const float g_r = bg[row], b_r = bb[row], gC = bg[C - 1];
     ok = mbar_wait_bounded(&bar[2], par, kWaitPolls) && ok;
@@ -531,7 +546,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     float qh[NH];
     {
       float x[NH];
-      tmem_cols(t_mine, nh, x);
+      tmem_cols_sum(t_mine, n, nh, x);
       if (chunk_warp) {
         // X = beta (V - g K H)
 #pragma unroll
@@ -544,19 +559,15 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
             x[j + 1] = b_r * (__uint_as_float(p[u] & 0xffff0000u) - g_r * x[j + 1]);
           }
         }
-        put_split(xb_hi, xb_lo, row, c0, x, nh);
+        put_split(xb, 8192, row, c0, n, x, nh);
         chunk_barrier();
-        // ---- D2 = [T; P T] X  (hi*hi + hi*lo + lo*hi)
+        // ---- D2 = A_hi [X_hi | X_lo] + A_lo X_hi,  A = [T; P T]
         if (tid == 0) {
 #pragma unroll
           for (int s = 0; s < C / 16; ++s) {
-            const uint64_t ah = tc::sdesc_sw128(s_ah + s * 32, 16, 1024);
-            const uint64_t al = tc::sdesc_sw128(s_al + s * 32, 16, 1024);
-            const uint64_t xh = tc::sdesc_sw128(s_xb + s * 2048, 8192, 1024);
-            const uint64_t xl = tc::sdesc_sw128(s_xb + 8192 + s * 2048, 8192, 1024);
-            tc::mma_bf16(tmem + 64, ah, xh, id_ab, s > 0);
-            tc::mma_bf16(tmem + 64, ah, xl, id_ab, 1);
-            tc::mma_bf16(tmem + 64, al, xh, id_ab, 1);
+            const uint64_t xd = tc::sdesc_sw128(s_xb + s * 2048, 8192, 1024);
+            tc::mma_bf16(tmem + 128, tc::sdesc_sw128(s_ah + s * 32, 16, 1024), xd, id_cat, s > 0);
+            tc::mma_bf16(tmem + 128, tc::sdesc_sw128(s_al + s * 32, 16, 1024), xd, id_hi, 1);
           }
           tc::mma_commit(&bar[3]);
         }
@@ -569,24 +580,20 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     tc::fence_after_sync();
     {
       float x[NH];
-      tmem_cols(t_mine + 64, nh, x);
+      tmem_cols_sum(t_mine + 128, n, nh, x);
       if (chunk_warp) {
         // D' = (g_C / g) Delta
         const float rg = gC / g_r;
 #pragma unroll
         for (int e = 0; e < NH; ++e) x[e] *= rg;
-        put_split(db_hi, db_lo, row, c0, x, nh);
+        put_split(db, 8192, row, c0, n, x, nh);
         chunk_barrier();
-        // ---- D3 = K^T (D'_hi + D'_lo)
+        // ---- D3 = K^T [D'_hi | D'_lo]
         if (tid == 0) {
 #pragma unroll
-          for (int s = 0; s < C / 16; ++s) {
-            const uint64_t a = tc::sdesc_sw128(s_kq + s * 2048, SB_KQ_HALF, 1024);
-            tc::mma_bf16(tmem + 128, a, tc::sdesc_sw128(s_db + s * 2048, 8192, 1024), id_kt,
-                         s > 0);
-            tc::mma_bf16(tmem + 128, a, tc::sdesc_sw128(s_db + 8192 + s * 2048, 8192, 1024),
-                         id_kt, 1);
-          }
+          for (int s = 0; s < C / 16; ++s)
+            tc::mma_bf16(tmem + 256, tc::sdesc_sw128(s_kq + s * 2048, SB_KQ_HALF, 1024),
+                         tc::sdesc_sw128(s_db + s * 2048, 8192, 1024), id_kt, s > 0);
           tc::mma_commit(&bar[4]);
         }
       } else if (row < nv) {
@@ -605,10 +612,10 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     tc::fence_after_sync();
     {
       float x[NH];
-      tmem_cols(t_mine + 128, nh, x);
+      tmem_cols_sum(t_mine + 256, n, nh, x);
 #pragma unroll
       for (int e = 0; e < NH; ++e) Hr[e] = fmaf(gC, Hr[e], x[e]);
-      put_split(hb_hi, hb_lo, r, c0, Hr, nh);
+      put_split(hb, 16384, r, c0, n, Hr, nh);
     }
   }
 
