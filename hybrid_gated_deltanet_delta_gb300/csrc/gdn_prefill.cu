@@ -49,8 +49,9 @@ constexpr int KS = DK * 2 + 16;  // staged bf16 row of K / Q, padded (bytes)
 // workspace block of one (chunk, value head): A = [T; P T] (128 x 64) as bf16
 // hi then lo, in 128-byte rows whose 16-byte chunks are XOR-swizzled by row
 // (chunk ch of row r at chunk ch ^ (r & 7): the tensor cores' 128-byte
-// swizzle), then g and beta.  The scan copies the block into shared memory as
-// is and hands A to the tensor cores without further staging.
+// swizzle), then the log decay G_t = sum_{s<=t} log alpha_s (g_t = exp G_t) and
+// beta.  The scan copies the block into shared memory as is and hands A to the
+// tensor cores without further staging.
 constexpr int WS_AH = 0;      // rows 0-63: T, rows 64-127: P T
 constexpr int WS_AL = 16384;
 constexpr int WS_G = 32768;
@@ -310,7 +311,7 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
       *reinterpret_cast<uint4*>(wsb + WS_AL + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
     }
     if (tid < C) {
-      reinterpret_cast<float*>(wsb + WS_G)[tid] = __expf(sg[tid]);
+      reinterpret_cast<float*>(wsb + WS_G)[tid] = sg[tid];
       reinterpret_cast<float*>(wsb + WS_B)[tid] = sb[tid];
     }
     // the next head's gates have landed and every thread is done with this head
@@ -335,27 +336,29 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
 // recurrence; the "output" warps (lanes 64-127) keep Q H and finish
 // O = g Q H + P Delta while the next MMA runs, joining only for the state
 // update.  The B operands (H, X, D' as bf16 hi/lo pairs) are written by their
-// owners straight into the 128-byte-swizzle layout.  Thread 0 issues the MMAs
-// and, one chunk ahead, the TMA loads of K and Q and the bulk copy of the
-// chunk's workspace block, all completing on one mbarrier per buffer.
+// owners straight into the 128-byte-swizzle layout.  Thread 0 issues the MMAs;
+// thread 64 issues, one chunk ahead, the TMA loads of K, Q and the V slab and
+// the bulk copy of the chunk's workspace block (all completing on one mbarrier
+// per buffer), and the TMA store of each chunk's output tile.
 constexpr int SCAN_THREADS = 256;
 constexpr int NMAX = 48;                     // widest column slab
 constexpr int NH = NMAX / 2;                 // columns per thread
 constexpr int TMEM_COLS = 512;               // D1 at column 0, D2 at 128, D3 at 256
 // one staging buffer: K and Q in two d_k halves of 128 rows x 128 bytes (K
-// rows 0-63, Q rows 64-127), then the workspace block as copied
+// rows 0-63, Q rows 64-127), the workspace block as copied, the V slab [64][n]
 constexpr int SB_KQ = 0;
 constexpr int SB_KQ_HALF = 16384;
 constexpr int SB_W = 32768;
-constexpr int SB_SIZE = 66560;               // SB_W + WS_STRIDE, rounded up to 1 KB
-constexpr unsigned SB_TX = 4 * 8192 + WS_STRIDE;  // bytes landing per staged chunk
-static_assert(SB_W + WS_STRIDE <= SB_SIZE && SB_SIZE % 1024 == 0, "staging buffer layout");
+constexpr int SB_V = 66560;                  // SB_W + WS_STRIDE, rounded up to 1 KB
+constexpr int SB_SIZE = SB_V + C * NMAX * 2;
+static_assert(SB_W + WS_STRIDE <= SB_V && SB_SIZE % 1024 == 0, "staging buffer layout");
 // B operands [hi | lo] side by side (2n columns, MN-major): columns 0-63 in
 // the first block of 128-byte rows, 64-127 in the second
 constexpr int SCAN_HB = 2 * SB_SIZE;         // H: 2 blocks of [128 d_k rows][128 B]
 constexpr int SCAN_XB = SCAN_HB + 2 * 16384;  // X: 2 blocks of [64 chunk rows][128 B]
 constexpr int SCAN_DB = SCAN_XB + 2 * 8192;   // D'
-constexpr int SCAN_BAR = SCAN_DB + 2 * 8192;  // mbarriers: staging [2], MMA; TMEM address
+constexpr int SCAN_O = SCAN_DB + 2 * 8192;    // O tile [64][n] fp32, stored by TMA
+constexpr int SCAN_BAR = SCAN_O + C * NMAX * 4;  // mbarriers; TMEM address
 constexpr int SCAN_SMEM = SCAN_BAR + 64 + 1024;  // + room to align the base to 1 KB
 
 // polls of an mbarrier before a block gives up
@@ -440,8 +443,9 @@ __device__ __forceinline__ void chunk_barrier() {
 
 __global__ void __launch_bounds__(SCAN_THREADS, 1)
 scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-            const uint16_t* __restrict__ v, float* __restrict__ state, float* __restrict__ o,
-            const char* __restrict__ ws, int T, int Hk, int Hv) {
+            const __grid_constant__ CUtensorMap tm_v48, const __grid_constant__ CUtensorMap tm_v32,
+            const __grid_constant__ CUtensorMap tm_o48, const __grid_constant__ CUtensorMap tm_o32,
+            float* __restrict__ state, const char* __restrict__ ws, int T, int Hk, int Hv) {
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int sl = blockIdx.x, h = blockIdx.y, hk = h / (Hv / Hk);
@@ -452,9 +456,15 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
   const int r = 32 * qd + lane;              // TMEM lane: row of D1 / D2 / D3
   const bool chunk_warp = qd < 2;            // rows 0-63: K H, Delta
   const int row = r & (C - 1);               // chunk row (D1 / D2)
+  constexpr int kIssuer = 0;                 // issues the MMAs (a chunk warp)
+  constexpr int kCopier = 64;                // issues staging and output copies (an output warp)
+  const CUtensorMap* tm_v = n == 48 ? &tm_v48 : &tm_v32;
+  const CUtensorMap* tm_o = n == 48 ? &tm_o48 : &tm_o32;
+  const unsigned stage_bytes = 4 * 8192 + WS_STRIDE + C * n * 2;
   char* hb = smem + SCAN_HB;
   char* xb = smem + SCAN_XB;
   char* db = smem + SCAN_DB;
+  float* otile = reinterpret_cast<float*>(smem + SCAN_O);
   // mbarriers: [0], [1] staging buffers; [2], [3], [4] completion of the
   // chunk's first, second and third MMA group (one phase per chunk each)
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SCAN_BAR);
@@ -472,18 +482,20 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
   const uint32_t tmem = *tslot;
   const uint32_t t_mine = tmem + ((uint32_t)(32 * qd) << 16) + c0;
 
-  // Staging of chunk c into buffer buf (thread 0): K and Q as four TMA tiles
-  // of 64 rows x 64 columns in the 128-byte swizzle (rows past the end of the
-  // sequence arrive as zero), and the workspace block by one bulk copy.
+  // Staging of chunk c into buffer buf (thread kCopier): K and Q as four TMA
+  // tiles of 64 rows x 64 columns in the 128-byte swizzle, the V slab as one
+  // tile (rows past the end of the sequence arrive as zero), the workspace
+  // block by one bulk copy, all completing on bar[buf].
   auto stage = [&](int c, int buf) {
     char* B = smem + buf * SB_SIZE;
     const int t0 = c * C;
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&bar[buf], SB_TX);
+    mbar_arrive_expect_tx(&bar[buf], stage_bytes);
     tc::tma_load_2d(B + SB_KQ, &tm_k, hk * DK, t0, &bar[buf]);
     tc::tma_load_2d(B + SB_KQ + SB_KQ_HALF, &tm_k, hk * DK + 64, t0, &bar[buf]);
     tc::tma_load_2d(B + SB_KQ + C * 128, &tm_q, hk * DK, t0, &bar[buf]);
     tc::tma_load_2d(B + SB_KQ + SB_KQ_HALF + C * 128, &tm_q, hk * DK + 64, t0, &bar[buf]);
+    tc::tma_load_2d(B + SB_V, tm_v, h * DV + j0, t0, &bar[buf]);
     bulk_g2s(B + SB_W, ws + ((size_t)c * Hv + h) * WS_STRIDE, WS_STRIDE, &bar[buf]);
   };
 
@@ -497,7 +509,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     Hr[e] = x.x; Hr[e + 1] = x.y; Hr[e + 2] = x.z; Hr[e + 3] = x.w;
   }
   put_split(hb, 16384, r, c0, n, Hr, nh);
-  if (tid == 0) stage(0, 0);
+  if (tid == kCopier) stage(0, 0);
   int inflight = 0;  // chunk whose staging is in flight, or -1
 
   // A K-major or MN-major (K^T); B MN-major with 2n ([hi | lo]) or n (hi) columns
@@ -507,27 +519,18 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
   const uint32_t s_hb = smem_addr(hb), s_xb = smem_addr(xb), s_db = smem_addr(db);
   bool ok = true;
   for (int c = 0; c < n_chunks; ++c) {
-    const int buf = c & 1, t0 = c * C, nv = min(C, T - t0);
+    const int buf = c & 1, t0 = c * C;
     const unsigned par = c & 1;
     char* B = smem + buf * SB_SIZE;
-    // V row of the chunk warps (read from global; consumed after the first MMA)
-    uint4 vr[NH / 8];
-    if (chunk_warp) {
-      const uint4* vsrc = reinterpret_cast<const uint4*>(
-          v + ((size_t)(t0 + (row < nv ? row : 0)) * Hv + h) * DV + j0 + c0);
-#pragma unroll
-      for (int e = 0; e < NH / 8; ++e)
-        vr[e] = (e * 8 < nh && row < nv) ? __ldg(vsrc + e) : make_uint4(0u, 0u, 0u, 0u);
-    }
     ok = tc_barrier(ok && mbar_wait_bounded(&bar[buf], (c >> 1) & 1, kWaitPolls));
     if (!ok) break;
     const uint32_t s_kq = smem_addr(B + SB_KQ);
     const uint32_t s_ah = smem_addr(B + SB_W + WS_AH), s_al = smem_addr(B + SB_W + WS_AL);
-    const float* bg = reinterpret_cast<const float*>(B + SB_W + WS_G);
+    const float* bG = reinterpret_cast<const float*>(B + SB_W + WS_G);
     const float* bb = reinterpret_cast<const float*>(B + SB_W + WS_B);
 
-    // ---- D1 = [K; Q] [H_hi | H_lo]; then the next chunk's staging
-    if (tid == 0) {
+    // ---- D1 = [K; Q] [H_hi | H_lo]
+    if (tid == kIssuer) {
 #pragma unroll
       for (int s = 0; s < DK / 16; ++s) {
         const uint64_t a = tc::sdesc_sw128(s_kq + (s >> 2) * SB_KQ_HALF + (s & 3) * 32, 16, 1024);
@@ -535,12 +538,20 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
       }
       tc::mma_commit(&bar[2]);
     }
+    // the next chunk's staging (its buffer was last read by the previous chunk)
     inflight = -1;
     if (c + 1 < n_chunks) {
-      if (tid == 0) stage(c + 1, buf ^ 1);
+      if (tid == kCopier) stage(c + 1, buf ^ 1);
       inflight = c + 1;
     }
-    const float g_r = bg[row], b_r = bb[row], gC = bg[C - 1];
+    const float G_r = bG[row], GC = bG[C - 1];
+    const float g_r = __expf(G_r), b_r = bb[row], gC = __expf(GC);
+    uint4 vr[NH / 8];
+    if (chunk_warp) {
+      const uint4* vsrc = reinterpret_cast<const uint4*>(B + SB_V + (row * n + c0) * 2);
+#pragma unroll
+      for (int e = 0; e < NH / 8; ++e) vr[e] = e * 8 < nh ? vsrc[e] : make_uint4(0u, 0u, 0u, 0u);
+    }
     ok = mbar_wait_bounded(&bar[2], par, kWaitPolls) && ok;
     tc::fence_after_sync();
     float qh[NH];
@@ -562,7 +573,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
         put_split(xb, 8192, row, c0, n, x, nh);
         chunk_barrier();
         // ---- D2 = A_hi [X_hi | X_lo] + A_lo X_hi,  A = [T; P T]
-        if (tid == 0) {
+        if (tid == kIssuer) {
 #pragma unroll
           for (int s = 0; s < C / 16; ++s) {
             const uint64_t xd = tc::sdesc_sw128(s_xb + s * 2048, 8192, 1024);
@@ -583,28 +594,34 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
       tmem_cols_sum(t_mine + 128, n, nh, x);
       if (chunk_warp) {
         // D' = (g_C / g) Delta
-        const float rg = gC / g_r;
+        const float rg = __expf(GC - G_r);
 #pragma unroll
         for (int e = 0; e < NH; ++e) x[e] *= rg;
         put_split(db, 8192, row, c0, n, x, nh);
         chunk_barrier();
         // ---- D3 = K^T [D'_hi | D'_lo]
-        if (tid == 0) {
+        if (tid == kIssuer) {
 #pragma unroll
           for (int s = 0; s < C / 16; ++s)
             tc::mma_bf16(tmem + 256, tc::sdesc_sw128(s_kq + s * 2048, SB_KQ_HALF, 1024),
                          tc::sdesc_sw128(s_db + s * 2048, 8192, 1024), id_kt, s > 0);
           tc::mma_commit(&bar[4]);
         }
-      } else if (row < nv) {
-        // O = g Q H + P Delta
-        float* orow = o + ((size_t)(t0 + row) * Hv + h) * DV + j0 + c0;
+      } else {
+        // O = g Q H + P Delta into the output tile, stored by one TMA copy
+        float* orow = otile + row * n + c0;
 #pragma unroll
         for (int e = 0; e < NH; e += 4)
           if (e < nh)
             *reinterpret_cast<float4*>(orow + e) =
                 make_float4(qh[e] + x[e], qh[e + 1] + x[e + 1], qh[e + 2] + x[e + 2],
                             qh[e + 3] + x[e + 3]);
+        fence_proxy_async_smem();
+        tc::named_barrier(2, SCAN_THREADS / 2);
+        if (tid == kCopier) {
+          tc::tma_store_2d(tm_o, h * DV + j0, t0, otile);
+          tc::bulk_commit();
+        }
       }
     }
     // ---- H <- g_C H + D3
@@ -617,16 +634,21 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
       for (int e = 0; e < NH; ++e) Hr[e] = fmaf(gC, Hr[e], x[e]);
       put_split(hb, 16384, r, c0, n, Hr, nh);
     }
+    // the output tile is rewritten next chunk: its store must have read it
+    if (tid == kCopier) tc::bulk_wait_read_all();
   }
 
   ok = tc_barrier(ok);
-  if (!ok) {
+  if (tid == kCopier) {
     // a staged chunk or an MMA never completed: give the staging still in
-    // flight a last bounded chance to land, then mark the slab as failed
-    if (tid == 0 && inflight >= 0)
+    // flight a last bounded chance to land; the output stores complete here
+    if (!ok && inflight >= 0)
       mbar_wait_bounded(&bar[inflight & 1], (inflight >> 1) & 1, kWaitPolls);
+    tc::bulk_wait_all();
+  }
+  if (!ok) {
 #pragma unroll
-    for (int e = 0; e < NH; ++e) Hr[e] = __int_as_float(0x7fc00000);
+    for (int e = 0; e < NH; ++e) Hr[e] = __int_as_float(0x7fc00000);  // the slab failed
   }
 #pragma unroll
   for (int e = 0; e < NH; e += 4)
@@ -708,19 +730,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// K or Q ([T][Hk][128] bf16) as a 2-D tensor of T rows and Hk*128 columns,
-// read in 64 x 64 tiles with the 128-byte swizzle; rows past T read as zero.
-int kq_tensor_map(CUtensorMap* m, const void* base, int T, int Hk) {
+// A [T][heads][128] tensor (bf16 or fp32) as a 2-D tensor of T rows and
+// heads*128 columns, moved in tiles of `box_cols` x 64 rows (rows past T read
+// as zero and are not written).
+int rows_tensor_map(CUtensorMap* m, const void* base, CUtensorMapDataType type, int elem_bytes,
+                    int T, int heads, int box_cols, CUtensorMapSwizzle swizzle) {
   const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return GDN_ERR_CUDA;
-  const cuuint64_t dims[2] = {(cuuint64_t)Hk * DK, (cuuint64_t)T};
-  const cuuint64_t strides[1] = {(cuuint64_t)Hk * DK * 2};
-  const cuuint32_t box[2] = {64, 64};
+  const cuuint64_t dims[2] = {(cuuint64_t)heads * DK, (cuuint64_t)T};
+  const cuuint64_t strides[1] = {(cuuint64_t)heads * DK * elem_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, 64};
   const cuuint32_t elem[2] = {1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                         strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = enc(m, type, 2, const_cast<void*>(base), dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -731,9 +754,17 @@ int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const
                    float* state, float* o, void* workspace, cudaStream_t stream) {
   if (!bf16 || dk != DK || dv != DV || chunk != C) return GDN_ERR_UNSUPPORTED;
   const int n_chunks = (T + C - 1) / C;
-  CUtensorMap tm_k, tm_q;
-  int st = kq_tensor_map(&tm_k, k, T, Hk);
-  if (st == GDN_OK) st = kq_tensor_map(&tm_q, q, T, Hk);
+  // K and Q in 64 x 64 tiles, 128-byte swizzle; V and O in 64-row tiles of
+  // one column slab (48 or 32 wide), unswizzled
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUtensorMap tm_k, tm_q, tm_v48, tm_v32, tm_o48, tm_o32;
+  int st = rows_tensor_map(&tm_k, k, bf, 2, T, Hk, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st == GDN_OK) st = rows_tensor_map(&tm_q, q, bf, 2, T, Hk, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st == GDN_OK) st = rows_tensor_map(&tm_v48, v, bf, 2, T, Hv, 48, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st == GDN_OK) st = rows_tensor_map(&tm_v32, v, bf, 2, T, Hv, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st == GDN_OK) st = rows_tensor_map(&tm_o48, o, f32, 4, T, Hv, 48, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st == GDN_OK) st = rows_tensor_map(&tm_o32, o, f32, 4, T, Hv, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != GDN_OK) return st;
   if (cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            PREP_SMEM) != cudaSuccess ||
@@ -746,8 +777,8 @@ int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const
   st = launch_status();
   if (st != GDN_OK) return st;
   scan_kernel<<<dim3(3, Hv), SCAN_THREADS, SCAN_SMEM, stream>>>(
-      tm_k, tm_q, static_cast<const uint16_t*>(v), state, o, static_cast<const char*>(workspace),
-      T, Hk, Hv);
+      tm_k, tm_q, tm_v48, tm_v32, tm_o48, tm_o32, state, static_cast<const char*>(workspace), T,
+      Hk, Hv);
   return launch_status();
 }
 
