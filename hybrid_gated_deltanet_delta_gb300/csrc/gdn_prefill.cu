@@ -63,108 +63,36 @@ __device__ __forceinline__ uint32_t ld32(const char* p) {
 }
 
 // ------------------------------------------------------------------- prep
+// One CTA per (chunk, q/k head), 8 warps.  K K^T and Q K^T are formed once on
+// tensor cores and stay in the warps' accumulator fragments; the value heads
+// of the q/k head are then handled three at a time:
+//   1. gates: warp j scans log alpha of head j (two rows per lane) into the
+//      log decay G, and writes G and beta to the workspace;
+//   2. A = beta_t e^{G_t - G_s} K K^T (s < t) and P = e^{G_t - G_s} Q K^T
+//      (s <= t) straight from the accumulators into shared memory (fp32);
+//   3. T = (I + A)^-1 by blocks of 16: the diagonal blocks by forward
+//      substitution, then N = D A below the diagonal and T block row by block
+//      row; P T block by block (the block products on tensor cores with the
+//      fp32 operands split into bf16 hi/lo pairs);
+//   4. [T; P T] as bf16 hi/lo pairs into the workspace block, 16 bytes a store.
 constexpr int PREP_THREADS = 256;
-constexpr int TS = 65;  // fp32 row stride of the 64 x 64 work matrices (bank spread)
+constexpr int HG = 3;    // value heads per pass
+constexpr int AS = 68;   // fp32 row stride of A and P (16-byte rows, spread banks)
+// shared memory: the K / Q staging (dead once K K^T and Q K^T are formed) is
+// reused by A and P of the pass's heads
 constexpr int PREP_K = 0;
 constexpr int PREP_Q = PREP_K + C * KS;
-constexpr int PREP_KK = PREP_Q + C * KS;
-constexpr int PREP_QK = PREP_KK + C * C * 4;
-constexpr int PREP_A = PREP_QK + C * C * 4;
-// T and the product scratch reuse the K / Q staging area, dead once K K^T and
-// Q K^T are formed
-constexpr int PREP_T = PREP_K;
-constexpr int PREP_S = PREP_T + C * TS * 4;
-static_assert(PREP_S + C * TS * 4 <= PREP_KK, "T and S must fit in the K/Q staging area");
-constexpr int PREP_GATE = PREP_A + C * TS * 4;  // [2 buffers][alpha 64, beta 64]
-constexpr int PREP_LG = PREP_GATE + 2 * 2 * C * 4;
-constexpr int PREP_G = PREP_LG + C * 4;
-constexpr int PREP_B = PREP_G + C * 4;
-constexpr int PREP_SMEM = PREP_B + C * 4;
-
-// C = sign * X Y for M x N outputs over K terms (all three row stride TS);
-// `nthreads` threads starting at `tid` = 0 share the 2 x 2 output tiles.
-__device__ __forceinline__ void mm_tiles(float* Cm, const float* X, const float* Y, int M, int N,
-                                         int K, float sign, int tid, int nthreads) {
-  const int tn = N / 2;
-  for (int tile = tid; tile < (M / 2) * tn; tile += nthreads) {
-    const int r = 2 * (tile / tn), c = 2 * (tile % tn);
-    float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-    for (int k = 0; k < K; ++k) {
-      const float x0 = X[r * TS + k], x1 = X[(r + 1) * TS + k];
-      const float y0 = Y[k * TS + c], y1 = Y[k * TS + c + 1];
-      a00 = fmaf(x0, y0, a00); a01 = fmaf(x0, y1, a01);
-      a10 = fmaf(x1, y0, a10); a11 = fmaf(x1, y1, a11);
-    }
-    Cm[r * TS + c] = sign * a00;
-    Cm[r * TS + c + 1] = sign * a01;
-    Cm[(r + 1) * TS + c] = sign * a10;
-    Cm[(r + 1) * TS + c + 1] = sign * a11;
-  }
-}
-
-// R = X Y for lower-triangular 64 x 64 X and Y (row stride TS): only the
-// terms k in [s, t] of R[t][s] are nonzero.  All PREP_THREADS threads share
-// the 2 x 2 output tiles; tiles above the diagonal are written as zero.
-__device__ __forceinline__ void mm_lower(float* R, const float* X, const float* Y, int tid) {
-  for (int tile = tid; tile < (C / 2) * (C / 2); tile += PREP_THREADS) {
-    const int r = 2 * (tile >> 5), c = 2 * (tile & 31);
-    float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-    for (int k = c; k <= r + 1; ++k) {
-      const float x0 = X[r * TS + k], x1 = X[(r + 1) * TS + k];
-      const float y0 = Y[k * TS + c], y1 = Y[k * TS + c + 1];
-      a00 = fmaf(x0, y0, a00); a01 = fmaf(x0, y1, a01);
-      a10 = fmaf(x1, y0, a10); a11 = fmaf(x1, y1, a11);
-    }
-    R[r * TS + c] = a00;
-    R[r * TS + c + 1] = a01;
-    R[(r + 1) * TS + c] = a10;
-    R[(r + 1) * TS + c + 1] = a11;
-  }
-}
-
-// T = (I + A)^-1 for a strictly lower-triangular 64 x 64 A (row stride TS) by
-// recursive doubling of the block inverse
-//     [[L11, 0], [L21, L22]]^-1 = [[L11^-1, 0], [-L22^-1 L21 L11^-1, L22^-1]]:
-// the four 16 x 16 diagonal blocks by forward substitution held in registers
-// (one column per lane), then the 16 -> 32 and 32 -> 64 merges as two products
-// each.  S is 64 x 64 scratch.
-__device__ void invert_unit_lower(const float* A, float* T, float* S, int tid) {
-  const int w = tid >> 5, lane = tid & 31;
-  if (w < 2) {
-    const int b0 = 16 * (2 * w + (lane >> 4)), j = lane & 15;
-    float tc[16];
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      float acc = 0.f;
-#pragma unroll
-      for (int r = 0; r < t; ++r) acc = fmaf(A[(b0 + t) * TS + b0 + r], tc[r], acc);
-      tc[t] = t < j ? 0.f : (t == j ? 1.f : -acc);
-    }
-#pragma unroll
-    for (int t = 0; t < 16; ++t) T[(b0 + t) * TS + b0 + j] = tc[t];
-  }
-  // blocks above the diagonal are zero
-  for (int idx = tid; idx < C * C; idx += PREP_THREADS) {
-    const int t = idx >> 6, s = idx & 63;
-    if ((s >> 4) > (t >> 4)) T[t * TS + s] = 0.f;
-  }
-  __syncthreads();
-  // 16 -> 32: T[b+16.., b..] = -T[b+16.., b+16..] (A[b+16.., b..] T[b.., b..]), b = 0, 32
-  {
-    const int half = tid >> 7, ht = tid & 127, b = 32 * half;
-    mm_tiles(S + (b + 16) * TS + b, A + (b + 16) * TS + b, T + b * TS + b, 16, 16, 16, 1.f, ht,
-             128);
-    __syncthreads();
-    mm_tiles(T + (b + 16) * TS + b, T + (b + 16) * TS + b + 16, S + (b + 16) * TS + b, 16, 16,
-             16, -1.f, ht, 128);
-    __syncthreads();
-  }
-  // 32 -> 64: T[32.., 0..] = -T[32.., 32..] (A[32.., 0..] T[0.., 0..])
-  mm_tiles(S + 32 * TS, A + 32 * TS, T, 32, 32, 32, 1.f, tid, PREP_THREADS);
-  __syncthreads();
-  mm_tiles(T + 32 * TS, T + 32 * TS + 32, S + 32 * TS, 32, 32, 32, -1.f, tid, PREP_THREADS);
-  __syncthreads();
-}
+constexpr int PREP_AP = 0;                          // [head][A, P][64][AS] fp32
+constexpr int PREP_AP_SIZE = HG * 2 * C * AS * 4;
+static_assert(2 * C * KS <= PREP_AP_SIZE, "K and Q staging fits in the A / P area");
+constexpr int PREP_GATE = PREP_AP_SIZE;              // [head][alpha 64, beta 64]
+constexpr int PREP_G = PREP_GATE + HG * 2 * C * 4;   // [head][64] log decay
+constexpr int PREP_B = PREP_G + HG * C * 4;          // [head][64] beta
+constexpr int PREP_SMEM = PREP_B + HG * C * 4;
+// with more than HG value heads per q/k head the accumulator fragments are
+// parked in shared memory between passes (one float4 row per thread and tile)
+constexpr int PREP_ACC = PREP_SMEM;
+constexpr int PREP_SMEM_MULTIPASS = PREP_ACC + PREP_THREADS * 32 * 4;
 
 __device__ __forceinline__ void cp_async4_zfill(void* smem, const void* gmem, bool valid) {
   const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
@@ -173,37 +101,80 @@ __device__ __forceinline__ void cp_async4_zfill(void* smem, const void* gmem, bo
                : "memory");
 }
 
-__global__ void __launch_bounds__(PREP_THREADS)
+// Fragments of 16 x 16 fp32 blocks (row stride AS) for mma m16n8k16, as bf16
+// hi/lo pairs: the A operand X (row-major) and the B operand Y (columns
+// 8*nh .. 8*nh+7).
+__device__ __forceinline__ void frag_a(const float* X, int g8, int t4, uint32_t (&hi)[4],
+                                       uint32_t (&lo)[4]) {
+  const float2 x0 = *reinterpret_cast<const float2*>(X + g8 * AS + 2 * t4);
+  const float2 x1 = *reinterpret_cast<const float2*>(X + (g8 + 8) * AS + 2 * t4);
+  const float2 x2 = *reinterpret_cast<const float2*>(X + g8 * AS + 2 * t4 + 8);
+  const float2 x3 = *reinterpret_cast<const float2*>(X + (g8 + 8) * AS + 2 * t4 + 8);
+  tc::split_bf16x2(x0.x, x0.y, hi[0], lo[0]);
+  tc::split_bf16x2(x1.x, x1.y, hi[1], lo[1]);
+  tc::split_bf16x2(x2.x, x2.y, hi[2], lo[2]);
+  tc::split_bf16x2(x3.x, x3.y, hi[3], lo[3]);
+}
+
+__device__ __forceinline__ void frag_b(const float* Y, int nh, int g8, int t4, uint32_t (&hi)[2],
+                                       uint32_t (&lo)[2]) {
+  const int n = 8 * nh + g8;
+  tc::split_bf16x2(Y[(2 * t4) * AS + n], Y[(2 * t4 + 1) * AS + n], hi[0], lo[0]);
+  tc::split_bf16x2(Y[(2 * t4 + 8) * AS + n], Y[(2 * t4 + 9) * AS + n], hi[1], lo[1]);
+}
+
+// acc (16 x 16 as two 16 x 8 accumulator tiles) += X Y, with the three
+// products hi*hi + hi*lo + lo*hi of the bf16 pairs.
+__device__ __forceinline__ void block_mma(float (&acc)[2][4], const float* X, const float* Y,
+                                          int g8, int t4) {
+  uint32_t ah[4], al[4];
+  frag_a(X, g8, t4, ah, al);
+#pragma unroll
+  for (int nh = 0; nh < 2; ++nh) {
+    uint32_t bh[2], bl[2];
+    frag_b(Y, nh, g8, t4, bh, bl);
+    mma_bf16_16816(acc[nh], ah, bh[0], bh[1]);
+    mma_bf16_16816(acc[nh], ah, bl[0], bl[1]);
+    mma_bf16_16816(acc[nh], al, bh[0], bh[1]);
+  }
+}
+
+// sign * acc into the 16 x 16 fp32 block at Z (row stride AS).
+__device__ __forceinline__ void put_block(float* Z, const float (&acc)[2][4], float sign, int g8,
+                                          int t4) {
+#pragma unroll
+  for (int nh = 0; nh < 2; ++nh) {
+    const int col = 8 * nh + 2 * t4;
+    *reinterpret_cast<float2*>(Z + g8 * AS + col) = make_float2(sign * acc[nh][0], sign * acc[nh][1]);
+    *reinterpret_cast<float2*>(Z + (g8 + 8) * AS + col) =
+        make_float2(sign * acc[nh][2], sign * acc[nh][3]);
+  }
+}
+
+__global__ void __launch_bounds__(PREP_THREADS, 2)
 prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
             const float* __restrict__ alpha, const float* __restrict__ beta, int T, int Hk,
             int Hv, char* __restrict__ ws) {
   extern __shared__ __align__(16) char smem[];
   char* sk = smem + PREP_K;
   char* sq = smem + PREP_Q;
-  float* skk = reinterpret_cast<float*>(smem + PREP_KK);
-  float* sqk = reinterpret_cast<float*>(smem + PREP_QK);
-  float* sa = reinterpret_cast<float*>(smem + PREP_A);
-  float* st = reinterpret_cast<float*>(smem + PREP_T);
-  float* ss = reinterpret_cast<float*>(smem + PREP_S);
+  float* sap = reinterpret_cast<float*>(smem + PREP_AP);
   float* sgate = reinterpret_cast<float*>(smem + PREP_GATE);
-  float* slg = reinterpret_cast<float*>(smem + PREP_LG);
-  float* sg = reinterpret_cast<float*>(smem + PREP_G);
-  float* sb = reinterpret_cast<float*>(smem + PREP_B);
+  float* sG = reinterpret_cast<float*>(smem + PREP_G);
+  float* sB = reinterpret_cast<float*>(smem + PREP_B);
 
   const int c = blockIdx.x, hk = blockIdx.y, G = Hv / Hk;
   const int t0 = c * C, nv = min(C, T - t0);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g8 = lane >> 2, t4 = lane & 3;
 
-  // gates of value head hk*G + j into gate buffer j & 1 (rows past the end read as 0)
-  auto stage_gates = [&](int j) {
-    float* dst = sgate + (j & 1) * 2 * C;
-    const int h = hk * G + j;
-    if (tid < 2 * C) {
-      const int t = tid & 63;
+  // gates of the pass's value heads (rows past the end read as zero)
+  auto stage_gates = [&](int h0, int ng) {
+    for (int idx = tid; idx < ng * 2 * C; idx += PREP_THREADS) {
+      const int j = idx / (2 * C), e = idx - j * 2 * C, t = e & (C - 1);
       const bool valid = t < nv;
-      const float* src = (tid < C ? alpha : beta) + (size_t)(t0 + (valid ? t : 0)) * Hv + h;
-      cp_async4_zfill(dst + tid, src, valid);
+      const float* src = (e < C ? alpha : beta) + (size_t)(t0 + (valid ? t : 0)) * Hv + h0 + j;
+      cp_async4_zfill(sgate + idx, src, valid);
     }
   };
 
@@ -215,20 +186,21 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
     cp_async16_zfill(sk + r * KS + ch * 16, k + src, valid);
     cp_async16_zfill(sq + r * KS + ch * 16, q + src, valid);
   }
-  stage_gates(0);
+  stage_gates(hk * G, min(HG, G));
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
 
-  // K K^T (warps 0-3) and Q K^T (warps 4-7): 16 rows each, 64 columns
+  // K K^T (warps 0-3) and Q K^T (warps 4-7): rows 16*mt + g8 (+8), all 64 columns
+  const int mt = w & 3;
+  const bool is_kk = w < 4;
+  float acc[8][4];
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
   {
-    float acc[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-    const int mt = w & 3;
-    const char* a0 = (w < 4 ? sk : sq) + (16 * mt + g8) * KS;
+    const char* a0 = (is_kk ? sk : sq) + (16 * mt + g8) * KS;
 #pragma unroll
     for (int kc = 0; kc < DK / 16; ++kc) {
       const int off = (kc * 16 + t4 * 2) * 2;
@@ -240,83 +212,184 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
         mma_bf16_16816(acc[nt], a, ld32(rb), ld32(rb + 16));
       }
     }
-    float* dst = w < 4 ? skk : sqk;
-    const int r0 = 16 * mt + g8;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const int c0 = nt * 8 + t4 * 2;
-      dst[r0 * C + c0] = acc[nt][0];
-      dst[r0 * C + c0 + 1] = acc[nt][1];
-      dst[(r0 + 8) * C + c0] = acc[nt][2];
-      dst[(r0 + 8) * C + c0 + 1] = acc[nt][3];
-    }
   }
-  __syncthreads();
 
-  for (int j = 0; j < G; ++j) {
-    const int h = hk * G + j;
-    if (j + 1 < G) {
-      stage_gates(j + 1);
-      cp_async_commit();
-    }
-    // log-space cumulative decay G_t = sum_{s<=t} log alpha_s (gates of head j landed)
-    if (tid < C) {
-      const int t = tid;
-      const float* gate = sgate + (j & 1) * 2 * C;
-      const float a = gate[t], b = gate[C + t];
-      float lg = t < nv ? __logf(fmaxf(a, 1e-30f)) : 0.f;
+  // Steps 1-3 for value heads h0 .. h0+ng-1 from the accumulators `a`.
+  auto pass = [&](int h0, int ng, const float (&a)[8][4]) {
+    __syncthreads();  // gates landed; K / Q (or the previous A / P) no longer read
+    // ---- 1. log decay of head j by warp j: lane l holds rows 2l, 2l+1
+    if (w < ng) {
+      const float* ga = sgate + w * 2 * C;
+      const int ta = 2 * lane, tb = ta + 1;
+      const float la = ta < nv ? __logf(fmaxf(ga[ta], 1e-30f)) : 0.f;
+      const float lb = tb < nv ? __logf(fmaxf(ga[tb], 1e-30f)) : 0.f;
+      float sum = la + lb;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, lg, off);
-        if (lane >= off) lg += y;
+        const float y = __shfl_up_sync(0xffffffffu, sum, off);
+        if (lane >= off) sum += y;
       }
-      slg[t] = lg;
-      sb[t] = b;
+      const float Ga = sum - lb, Gb = sum;
+      sG[w * C + ta] = Ga;
+      sG[w * C + tb] = Gb;
+      sB[w * C + ta] = ga[C + ta];
+      sB[w * C + tb] = ga[C + tb];
+      char* wsb = ws + ((size_t)c * Hv + h0 + w) * WS_STRIDE;
+      *reinterpret_cast<float2*>(wsb + WS_G + ta * 4) = make_float2(Ga, Gb);
+      *reinterpret_cast<float2*>(wsb + WS_B + ta * 4) = make_float2(ga[C + ta], ga[C + tb]);
     }
     __syncthreads();
-    if (tid < C) sg[tid] = slg[tid] + (tid >= 32 ? slg[31] : 0.f);
-    __syncthreads();
-    // A (strictly lower)
-    for (int idx = tid; idx < C * C; idx += PREP_THREADS) {
-      const int t = idx >> 6, s = idx & 63;
-      sa[t * TS + s] = s < t ? sb[t] * __expf(sg[t] - sg[s]) * skk[t * C + s] : 0.f;
-    }
-    __syncthreads();
-    invert_unit_lower(sa, st, ss, tid);
-    // P (lower triangular with the diagonal) into S, then P T into the A buffer
-    for (int idx = tid; idx < C * C; idx += PREP_THREADS) {
-      const int t = idx >> 6, s = idx & 63;
-      ss[t * TS + s] = s <= t ? __expf(sg[t] - sg[s]) * sqk[t * C + s] : 0.f;
-    }
-    __syncthreads();
-    mm_lower(sa, ss, st, tid);
-    __syncthreads();
-    // A = [T; P T] as bf16 hi/lo pairs, g and beta
-    char* wsb = ws + ((size_t)c * Hv + h) * WS_STRIDE;
-    for (int idx = tid; idx < 2 * C * 8; idx += PREP_THREADS) {
-      const int r = idx >> 3, e8 = (idx & 7) * 8;
-      const float* src = r < C ? st + r * TS : sa + (r - C) * TS;
-      uint32_t hv[4], lv[4];
+    // ---- 2. A (warps 0-3) and P (warps 4-7) of each head from the accumulators
+    for (int j = 0; j < ng; ++j) {
+      float* dst = sap + (j * 2 + (is_kk ? 0 : 1)) * C * AS;
+      const float* Gj = sG + j * C;
 #pragma unroll
-      for (int qd = 0; qd < 4; ++qd) {
-        uint32_t h0, l0, h1, l1;
-        split_bf16(src[e8 + 2 * qd], h0, l0);
-        split_bf16(src[e8 + 2 * qd + 1], h1, l1);
-        hv[qd] = h0 | (h1 << 16);
-        lv[qd] = l0 | (l1 << 16);
+      for (int half = 0; half < 2; ++half) {
+        const int t = 16 * mt + g8 + 8 * half;
+        const float Gt = Gj[t], bt = is_kk ? sB[j * C + t] : 1.f;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const int s = nt * 8 + 2 * t4;
+          const bool m0 = is_kk ? s < t : s <= t, m1 = is_kk ? s + 1 < t : s + 1 <= t;
+          const float v0 = m0 ? bt * __expf(Gt - Gj[s]) * a[nt][2 * half] : 0.f;
+          const float v1 = m1 ? bt * __expf(Gt - Gj[s + 1]) * a[nt][2 * half + 1] : 0.f;
+          *reinterpret_cast<float2*>(dst + t * AS + s) = make_float2(v0, v1);
+        }
       }
-      // 128-byte rows, 16-byte chunk ch of row r stored at chunk ch ^ (r & 7)
+    }
+    __syncthreads();
+    // ---- 3. T = (I + A)^-1 in 16 x 16 blocks, in place of A:
+    //   D_b = (I + A_bb)^-1 (forward substitution, one column per thread),
+    //   N_ik = D_i A_ik (i > k), then block row by block row
+    //   T_ij = -sum_{k=j}^{i-1} N_ik T_kj  (T_jj = D_j),
+    // and P T in place of P: (P T)_ij = sum_{k=j}^{i} P_ik T_kj.
+    {
+      const bool solver = tid < ng * C;
+      const int j = tid >> 6, b = (tid >> 4) & 3, cl = tid & 15;
+      float* Ab = sap + (j * 2) * C * AS + (16 * b) * AS + 16 * b;
+      float x[16];
+      if (solver) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+          for (int r = 0; r < t; ++r) {
+            if (r & 1) acc1 = fmaf(Ab[t * AS + r], x[r], acc1);
+            else acc0 = fmaf(Ab[t * AS + r], x[r], acc0);
+          }
+          x[t] = t == cl ? 1.f : (t < cl ? 0.f : -(acc0 + acc1));
+        }
+      }
+      __syncthreads();  // every solver has read its diagonal block
+      if (solver) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) Ab[t * AS + cl] = x[t];
+      }
+    }
+    __syncthreads();
+    // N_ik = D_i A_ik over the 6 blocks below the diagonal of each head
+    for (int task = w; task < ng * 6; task += PREP_THREADS / 32) {
+      const int j = task / 6, p = task - j * 6;
+      const int i = p < 1 ? 1 : (p < 3 ? 2 : 3), k = p - (i * (i - 1)) / 2;
+      float* Am = sap + (j * 2) * C * AS;
+      float acc[2][4] = {};
+      block_mma(acc, Am + 16 * i * AS + 16 * i, Am + 16 * i * AS + 16 * k, g8, t4);
+      put_block(Am + 16 * i * AS + 16 * k, acc, 1.f, g8, t4);  // only this task reads A_ik
+    }
+    __syncthreads();
+    // block rows 1, 2, 3 of T
+    for (int i = 1; i < 4; ++i) {
+      float res[2][2][4];
+      int dst[2] = {-1, -1};
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int task = w + u * (PREP_THREADS / 32);
+        if (task < ng * i) {
+          const int j = task / i, jb = task - j * i;
+          float* Am = sap + (j * 2) * C * AS;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) res[u][h][e] = 0.f;
+          for (int k = jb; k < i; ++k)
+            block_mma(res[u], Am + 16 * i * AS + 16 * k, Am + 16 * k * AS + 16 * jb, g8, t4);
+          dst[u] = (j * 2) * C * AS + 16 * i * AS + 16 * jb;
+        }
+      }
+      __syncthreads();  // the row's N blocks are read
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        if (dst[u] >= 0) put_block(sap + dst[u], res[u], -1.f, g8, t4);
+      __syncthreads();
+    }
+    // P T over the 10 blocks on and below the diagonal of each head
+    {
+      float res[4][2][4];
+      int dst[4] = {-1, -1, -1, -1};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int task = w + u * (PREP_THREADS / 32);
+        if (task < ng * 10) {
+          const int j = task / 10, p = task - j * 10;
+          const int i = p < 1 ? 0 : (p < 3 ? 1 : (p < 6 ? 2 : 3)), jb = p - (i * (i + 1)) / 2;
+          const float* Tm = sap + (j * 2) * C * AS;
+          float* Pm = sap + (j * 2 + 1) * C * AS;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) res[u][h][e] = 0.f;
+          for (int k = jb; k <= i; ++k)
+            block_mma(res[u], Pm + 16 * i * AS + 16 * k, Tm + 16 * k * AS + 16 * jb, g8, t4);
+          dst[u] = (j * 2 + 1) * C * AS + 16 * i * AS + 16 * jb;
+        }
+      }
+      __syncthreads();  // P is read
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (dst[u] >= 0) put_block(sap + dst[u], res[u], 1.f, g8, t4);
+      __syncthreads();
+    }
+    // ---- 4. [T; P T] as bf16 hi/lo into the workspace: 16 bytes per row chunk
+    for (int idx = tid; idx < ng * 2 * C * 8; idx += PREP_THREADS) {
+      const int j = idx / (2 * C * 8), rem = idx - j * 2 * C * 8;
+      const int r = rem >> 3, e8 = (rem & 7) * 8;  // row of [T; P T], first column
+      const float* src = sap + (j * 2 + (r >= C)) * C * AS + (r & (C - 1)) * AS + e8;
+      const float4 x0 = *reinterpret_cast<const float4*>(src);
+      const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+      uint32_t hv[4], lv[4];
+      tc::split_bf16x2(x0.x, x0.y, hv[0], lv[0]);
+      tc::split_bf16x2(x0.z, x0.w, hv[1], lv[1]);
+      tc::split_bf16x2(x1.x, x1.y, hv[2], lv[2]);
+      tc::split_bf16x2(x1.z, x1.w, hv[3], lv[3]);
+      char* wsb = ws + ((size_t)c * Hv + h0 + j) * WS_STRIDE;
       const int off = r * 128 + (((e8 >> 3) ^ (r & 7)) << 4);
       *reinterpret_cast<uint4*>(wsb + WS_AH + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
       *reinterpret_cast<uint4*>(wsb + WS_AL + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
     }
-    if (tid < C) {
-      reinterpret_cast<float*>(wsb + WS_G)[tid] = sg[tid];
-      reinterpret_cast<float*>(wsb + WS_B)[tid] = sb[tid];
-    }
-    // the next head's gates have landed and every thread is done with this head
-    cp_async_wait<0>();
+  };
+
+  if (G > HG) {
+    // park the accumulators for the later passes
+    float4* park = reinterpret_cast<float4*>(smem + PREP_ACC) + tid;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+      park[nt * PREP_THREADS] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+  }
+  pass(hk * G, min(HG, G), acc);
+  for (int h0 = hk * G + HG; h0 < (hk + 1) * G; h0 += HG) {
+    // the previous pass is done with the gate buffer once every thread is here
     __syncthreads();
+    stage_gates(h0, min(HG, (hk + 1) * G - h0));
+    cp_async_commit();
+    cp_async_wait<0>();
+    float a2[8][4];
+    const float4* park = reinterpret_cast<const float4*>(smem + PREP_ACC) + tid;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const float4 x = park[nt * PREP_THREADS];
+      a2[nt][0] = x.x; a2[nt][1] = x.y; a2[nt][2] = x.z; a2[nt][3] = x.w;
+    }
+    pass(h0, min(HG, (hk + 1) * G - h0), a2);
   }
 }
 
@@ -766,12 +839,13 @@ int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const
   if (st == GDN_OK) st = rows_tensor_map(&tm_o48, o, f32, 4, T, Hv, 48, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st == GDN_OK) st = rows_tensor_map(&tm_o32, o, f32, 4, T, Hv, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != GDN_OK) return st;
+  const int prep_smem = Hv / Hk > HG ? PREP_SMEM_MULTIPASS : PREP_SMEM;
   if (cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           PREP_SMEM) != cudaSuccess ||
+                           PREP_SMEM_MULTIPASS) != cudaSuccess ||
       cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SCAN_SMEM) != cudaSuccess)
     return GDN_ERR_CUDA;
-  prep_kernel<<<dim3(n_chunks, Hk), PREP_THREADS, PREP_SMEM, stream>>>(
+  prep_kernel<<<dim3(n_chunks, Hk), PREP_THREADS, prep_smem, stream>>>(
       static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), alpha, beta, T, Hk, Hv,
       static_cast<char*>(workspace));
   st = launch_status();

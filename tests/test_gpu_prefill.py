@@ -48,6 +48,20 @@ def test_prefill_ragged_lengths(gpu_lib, T, heads):
     assert_close(H, Hr, f"prefill state T={T}")
 
 
+@pytest.mark.parametrize("heads", [(1, 4), (2, 16)])
+def test_prefill_many_value_heads_per_qk_head(gpu_lib, heads):
+    """More than three value heads share a q/k head: the preparation runs in
+    several passes over the value heads (4 = 3 + 1, 8 = 3 + 3 + 2)."""
+    Hk, Hv = heads
+    inp = synthetic.make_prefill_inputs(T=130, Hk=Hk, Hv=Hv, dk=128, dv=128, dtype="bf16",
+                                        alpha_kind="near_one", state_sigma=0.05,
+                                        seed=4500 + Hv)
+    H, O = run_prefill(gpu_lib, inp)
+    Hr, Or = oracle_prefill(inp)
+    assert_close(O, Or, f"prefill o heads={heads}")
+    assert_close(H, Hr, f"prefill state heads={heads}")
+
+
 def test_prefill_wide_decay(gpu_lib):
     """alpha = exp(-softplus(z)) over (0, 1): decays within a chunk reach ~1e-20."""
     inp = synthetic.make_prefill_inputs(T=256, Hk=2, Hv=6, dk=128, dv=128, dtype="bf16",
