@@ -185,7 +185,8 @@ KERNEL_SOURCES = {
     "verify": ["hybrid_gated_deltanet_delta_gb300/csrc/gdn_verify.cu",
                "hybrid_gated_deltanet_delta_gb300/csrc/gdn_common.cuh"],
     "prefill": ["hybrid_gated_deltanet_delta_gb300/csrc/gdn_prefill.cu",
-                "hybrid_gated_deltanet_delta_gb300/csrc/gdn_common.cuh"],
+                "hybrid_gated_deltanet_delta_gb300/csrc/gdn_common.cuh",
+                "hybrid_gated_deltanet_delta_gb300/csrc/gdn_tc.cuh"],
 }
 
 
