@@ -76,11 +76,15 @@ def prefill_bytes(T, Hk, Hv, dk, dv, in_bytes=2):
 
 
 def prefill_flops(T, Hk, Hv, dk, dv, C=64):
-    """Algorithmic flops of the chunked form per value head and chunk: Q K^T,
-    K K^T, the two C x C x d products (W or U and the masked P Delta) ... as
-    2 C^2 d each five times, plus the three C d^2 products with the state."""
+    """Algorithmic flops of the chunked (WY/UT) form, one multiply-add = 2:
+    per chunk and q/k head K K^T and Q K^T (C x C x d_k each); per chunk and
+    value head K H, Q H and K^T D' (C x d_k x d_v each) and T X, P Delta
+    (C x C x d_v each).  The inverse (C^3/3) and the elementwise work are left
+    out; the bf16 hi/lo splits are not counted."""
     n_chunks = -(-T // C)
-    return n_chunks * Hv * (5 * 2 * C * C * dk + 3 * 2 * C * dk * dv)
+    per_khead = 2 * (2 * C * C * dk)
+    per_vhead = 3 * (2 * C * dk * dv) + 2 * (2 * C * C * dv)
+    return n_chunks * (Hk * per_khead + Hv * per_vhead)
 
 
 WORKLOADS = {
@@ -593,8 +597,9 @@ def run_prefill(args, gdn, torch, flush, world, rank, local):
     hbm, bf16, kind = measured_peaks()
     pbytes = prefill_bytes(T, Hk, Hv, dk, dv)
     launch_ms = statistics.mean(ms)
-    achieved = pbytes / (launch_ms / 1e3) / 1e9
+    gbs = pbytes / (launch_ms / 1e3) / 1e9
     flops = prefill_flops(T, Hk, Hv, dk, dv)
+    tflops = flops / (launch_ms / 1e3) / 1e12
     if rank != 0:
         return None
     return {
@@ -608,16 +613,17 @@ def run_prefill(args, gdn, torch, flush, world, rank, local):
         "config": {"workload": f"prefill8192: {WORKLOADS['prefill8192']['desc']}",
                    "T": T, "Hk": Hk, "Hv": Hv, "dk": dk, "dv": dv, "chunk": 64,
                    "l2": "flushed by a 256 MiB write before every step; flush not timed",
-                   "timing": "CUDA events around each prefill call on the launch stream",
-                   "achieved_tflops": flops / (launch_ms / 1e3) / 1e12,
-                   "tensor_frac_of_measured_bf16": flops / (launch_ms / 1e3) / 1e12 / bf16},
-        "roofline": {"bound": "hbm", "kernel": "gdn_prefill_chunked", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": kind, "algorithmic_bytes_per_launch": pbytes,
+                   "timing": "CUDA events around each prefill call (prep + scan kernels) "
+                             "on the launch stream",
+                   "hbm_achieved_gbs": gbs, "hbm_frac_of_measured": gbs / hbm,
+                   "algorithmic_bytes_per_call": pbytes},
+        "roofline": {"bound": "tensor", "kernel": "gdn_prefill_chunked (prep + scan)",
+                     "achieved": tflops, "peak": bf16, "unit": "TFLOP/s", "frac": tflops / bf16,
+                     "peak_source": kind, "algorithmic_flops_per_launch": flops,
                      "traffic": profiled_traffic("prefill", "prefill8192")},
         "e2e": {"value": world * T * Hv * e2e_steps / e2e_s, "unit": "token-heads/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": None,
+        "gpu_launches": 2 * steps,   # prep + scan per call
         "clocks": sampler.summary(t0, t1),
     }
 
