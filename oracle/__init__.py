@@ -48,6 +48,9 @@ def bind(lib):
     lib.oracle_commit_f64.restype = ctypes.c_int
     lib.oracle_commit_f64.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32,
                                       i32, i32]
+    lib.oracle_replay_f64.restype = ctypes.c_int
+    lib.oracle_replay_f64.argtypes = [P, P, P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32,
+                                      i32]
     lib.oracle_prefill_step_f64.restype = ctypes.c_int
     lib.oracle_prefill_step_f64.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                             i32, P, P]
@@ -125,6 +128,26 @@ def commit(snap, accept, cache, slot, *, B, N, Hv, dk, dv, n_layers=1,
     return lib.oracle_commit_f64(_ptr(snap), snap_layer_stride, _ptr(acc), _ptr(cache),
                                  cache_slot_stride, cache_layer_stride, _ptr(slot_a), n_slots,
                                  B, N, Hv, dk, dv, n_layers)
+
+
+def replay(k, v, alpha, beta, cache, slot, parent, accept, *, B, N, Hk, Hv, dk, dv,
+           cache_slot_stride=None, n_slots=None):
+    """Replay commit in place on `cache` (float64 array): the recurrence over
+    each sequence's accepted path from its cached state.  parent=None -> chain
+    (accept = accept length - 1).  Returns the status."""
+    lib = _load()
+    assert cache.dtype == np.float64 and cache.flags.c_contiguous
+    if cache_slot_stride is None:
+        cache_slot_stride = Hv * dk * dv
+    if n_slots is None:
+        n_slots = cache.size // cache_slot_stride
+    arrs = [_c(k, np.float64), _c(v, np.float64), _c(alpha, np.float64), _c(beta, np.float64)]
+    slot_a = None if slot is None else _c(slot, np.int32)
+    par_a = None if parent is None else _c(parent, np.int32)
+    acc = _c(accept, np.int32)
+    return lib.oracle_replay_f64(*[_ptr(a) for a in arrs], _ptr(cache), cache_slot_stride,
+                                 _ptr(slot_a), n_slots, _ptr(par_a), _ptr(acc), B, N, Hk, Hv,
+                                 dk, dv)
 
 
 def prefill_step(q, k, v, alpha, beta, state, *, T, Hk, Hv, dk, dv, heads=None):

@@ -111,9 +111,70 @@ int verify(const R* q, const R* k, const R* v, const R* alpha, const R* beta, co
   return status;
 }
 
+// Checkpoint-and-replay commit ("Photon 2.6", section "Handling recurrent
+// state": keep the state from before the block and re-run the accepted tokens
+// instead of persisting every node): for every sequence, the recurrence over
+// the accepted path (chain: nodes 0 .. accept; tree: the ancestors of accept,
+// root first), starting from the cached state, replaces the cached state.
+template <typename R>
+int replay(const R* k, const R* v, const R* alpha, const R* beta, R* cache,
+           int64_t cache_slot_stride, const int32_t* slot, int32_t n_slots, const int32_t* parent,
+           const int32_t* accept, int32_t B, int32_t N, int32_t Hk, int32_t Hv, int32_t dk,
+           int32_t dv) {
+  if (B < 0 || N <= 0 || Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || Hv % Hk != 0)
+    return ERR_INVALID_ARG;
+  const int G = Hv / Hk;
+  const int64_t hs = (int64_t)dk * dv;
+  std::vector<R> u(dv), o(dv), H(hs);
+  std::vector<int32_t> depth(N), path;
+  int status = OK;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* par = parent ? parent + (int64_t)b * N : nullptr;
+    if (par) {
+      int st = tree_depth(par, N, depth.data());
+      if (st != OK) { status = st; continue; }
+    }
+    const int acc = accept[b];
+    if (acc < 0 || acc >= N) { status = ERR_ACCEPT_RANGE; continue; }
+    int sl = slot ? slot[b] : b;
+    if (sl < 0 || sl >= n_slots) { status = ERR_SLOT_RANGE; continue; }
+    // the accepted path, root first
+    path.clear();
+    if (par) {
+      for (int m = acc; m >= 0; m = par[m]) path.insert(path.begin(), m);
+    } else {
+      for (int m = 0; m <= acc; ++m) path.push_back(m);
+    }
+    for (int h = 0; h < Hv; ++h) {
+      const int hk = h / G;
+      R* S = cache + (int64_t)sl * cache_slot_stride + (int64_t)h * hs;
+      std::memcpy(H.data(), S, sizeof(R) * hs);
+      for (int n : path) {
+        const int64_t node = (int64_t)b * N + n;
+        const R* kn = k + (node * Hk + hk) * dk;
+        // the output is not needed here: k stands in for q
+        gdn_step<R>(H.data(), kn, v + (node * Hv + h) * dv, kn, alpha[node * Hv + h],
+                    beta[node * Hv + h], dk, dv, o.data(), u);
+      }
+      std::memcpy(S, H.data(), sizeof(R) * hs);
+    }
+  }
+  return status;
+}
+
 }  // namespace
 
 extern "C" {
+
+// Replay commit, in place on `cache` (same layouts as oracle_verify_f64);
+// accept [B] is the accepted node index (chain: accept length - 1).
+int oracle_replay_f64(const double* k, const double* v, const double* alpha, const double* beta,
+                      double* cache, int64_t cache_slot_stride, const int32_t* slot,
+                      int32_t n_slots, const int32_t* parent, const int32_t* accept, int32_t B,
+                      int32_t N, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv) {
+  return replay<double>(k, v, alpha, beta, cache, cache_slot_stride, slot, n_slots, parent,
+                        accept, B, N, Hk, Hv, dk, dv);
+}
 
 // Verify one block.  parent == nullptr means a chain (node n continues from
 // node n-1, node 0 from the cache).  Layouts:

@@ -422,6 +422,73 @@ def check_rounds_equal_sequential():
     _close(cache[1], sT, 1e-13, "rounds of verify+commit vs sequential")
 
 
+def check_replay_equals_persist():
+    """Checkpoint-and-replay commit: re-running each sequence's accepted path
+    (a chain prefix, or a tree node's ancestors from the root) from the cached
+    state gives the state the verify block persisted for that node; rounds of
+    verify -> replay commit equal one token-by-token run over the accepted
+    tokens; a bad accept index, slot or parent array leaves the cache alone."""
+    rng = np.random.default_rng(31)
+    for tree in (False, True):
+        c = _case(rng, B=3, N=6, Hk=2, Hv=4, dk=4, dv=3, tree=tree, n_slots=4)
+        snap, _ = _run(c)
+        acc = rng.integers(0, c["N"], c["B"]).astype(np.int32)
+        cache = np.ascontiguousarray(c["cache"], dtype=np.float64).copy()
+        st = oracle.replay(c["k"], c["v"], c["alpha"], c["beta"], cache, c["slot"], c["parent"],
+                           acc, B=c["B"], N=c["N"], Hk=c["Hk"], Hv=c["Hv"], dk=c["dk"],
+                           dv=c["dv"])
+        assert st == oracle.OK, st
+        for b in range(c["B"]):
+            _close(cache[c["slot"][b]], snap[b, acc[b]], 1e-13,
+                   f"replay of node {acc[b]} ({'tree' if tree else 'chain'}) vs persisted")
+        untouched = sorted(set(range(4)) - set(int(x) for x in c["slot"]))
+        for s_ in untouched:
+            _close(cache[s_], c["cache"][s_], 0.0, "slot not in the batch is untouched")
+    # rounds with the replay commit
+    Hk, Hv, dk, dv, N = 2, 4, 4, 3, 5
+    cache = rng.standard_normal((2, Hv, dk, dv)) * 0.3
+    slot = np.array([1], np.int32)
+    start = cache[1].copy()
+    acc_l = {key: [] for key in ("q", "k", "v", "alpha", "beta")}
+    for _ in range(4):
+        c = _case(rng, B=1, N=N, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+        L = int(rng.integers(1, N + 1))
+        st = oracle.replay(c["k"], c["v"], c["alpha"], c["beta"], cache, slot, None,
+                           np.array([L - 1], np.int32), B=1, N=N, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+        assert st == oracle.OK
+        for key in acc_l:
+            acc_l[key].append(c[key][0, :L])
+    cat = [np.concatenate(acc_l[key]) for key in ("q", "k", "v", "alpha", "beta")]
+    st, sT, _ = oracle.prefill_step(*cat, start, T=cat[0].shape[0], Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+    assert st == oracle.OK
+    _close(cache[1], sT, 1e-13, "rounds of verify+replay vs sequential")
+    # errors: the offending sequence is skipped, the other one still commits
+    c = _case(rng, B=2, N=4, Hk=1, Hv=2, dk=2, dv=2, tree=True)
+    cases = (  # (accept, slot, parent, status, bad sequence)
+        (np.array([4, 1], np.int32), c["slot"], c["parent"], oracle.ERR_ACCEPT_RANGE, 0),
+        (np.array([2, 3], np.int32), np.array([0, 5], np.int32), c["parent"],
+         oracle.ERR_SLOT_RANGE, 1),
+        (np.array([2, 3], np.int32), c["slot"], None, oracle.ERR_BAD_TREE, 1),
+    )
+    for acc, slot, par, code, bad_b in cases:
+        if par is None:
+            par = c["parent"].copy()
+            par[1, 2] = 3
+        cache = np.ascontiguousarray(c["cache"], dtype=np.float64).copy()
+        st = oracle.replay(c["k"], c["v"], c["alpha"], c["beta"], cache, slot, par, acc, B=2,
+                           N=4, Hk=1, Hv=2, dk=2, dv=2, n_slots=2)
+        assert st == code, (st, code)
+        good_b = 1 - bad_b
+        _, snap, _ = oracle.verify(c["q"], c["k"], c["v"], c["alpha"], c["beta"], c["cache"],
+                                   slot, c["parent"], B=2, N=4, Hk=1, Hv=2, dk=2, dv=2,
+                                   n_slots=2)
+        _close(cache[int(slot[good_b])], snap[good_b, acc[good_b]], 1e-13,
+               "the valid sequence still commits")
+        if 0 <= int(slot[bad_b]) < 2:
+            _close(cache[int(slot[bad_b])], c["cache"][int(slot[bad_b])], 0.0,
+                   "a skipped sequence keeps its cached state")
+
+
 def block_form_reference(H0, K, V, Q, alpha, beta, parent):
     """The whole block at once (float64, one value head): with G(n) the sum of
     log alpha over the root-to-n path and the deltas solved first from
@@ -476,4 +543,5 @@ ALL_CHECKS = [
     check_contraction, check_tree_matches_chain_and_paths, check_exact_rational_bruteforce,
     check_tree_depth_and_validation, check_commit, check_chunked_equals_step,
     check_rounds_equal_sequential, check_block_form_equals_recurrence,
+    check_replay_equals_persist,
 ]

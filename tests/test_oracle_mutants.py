@@ -31,6 +31,10 @@ MUTANTS = {
     "depth_off_by_one": ("depth[n] = depth[p] + 1;", "depth[n] = depth[p] + (p > 0);"),
     "prefill_drops_decay": ("alpha[(int64_t)t * Hv + h],\n",
                             "1.0 + 0 * alpha[(int64_t)t * Hv + h],\n"),
+    "replay_drops_root": ("for (int m = acc; m >= 0; m = par[m]) path.insert",
+                          "for (int m = acc; m > 0; m = par[m]) path.insert"),
+    "replay_chain_short": ("for (int m = 0; m <= acc; ++m) path.push_back(m);",
+                           "for (int m = 0; m < acc; ++m) path.push_back(m);"),
 }
 
 
