@@ -53,11 +53,12 @@ METRIC = "GDN verify node-heads/s per layer at block 16 / tree 22; % of GB300 HB
 
 
 # ------------------------------------------------------------------ workloads
-def verify_bytes(B, N, Hk, Hv, dk, dv, in_bytes=2, tree=False):
+def verify_bytes(B, N, Hk, Hv, dk, dv, in_bytes=2, tree=False, persist=True):
     """Algorithmic HBM bytes of one verify call: every input read once, the
-    initial state read once, every output (o and all N snapshots) written once."""
+    initial state read once, every output (o and, when persisted, all N
+    snapshots) written once."""
     state_in = B * Hv * dk * dv * 4
-    snap = B * N * Hv * dk * dv * 4
+    snap = B * N * Hv * dk * dv * 4 if persist else 0
     qk = 2 * B * N * Hk * dk * in_bytes
     v = B * N * Hv * dv * in_bytes
     gates = 2 * B * N * Hv * 4
@@ -98,6 +99,13 @@ WORKLOADS = {
     "batched8x16": dict(B=8, N=16, tree=False, layers=48,
                         desc="8 sequences x 16-position chains, same heads, 48 GDN layers with "
                              "fresh inputs per layer; 48 verifies + one 48-layer commit"),
+    "chain16_replay": dict(B=1, N=16, tree=False, layers=1, replay=True,
+                           desc="chain16 committed by checkpoint and replay: verify without "
+                                "snapshots, then the accepted prefix re-run from the cached "
+                                "state into the cache"),
+    "batched8x16_replay": dict(B=8, N=16, tree=False, layers=48, replay=True,
+                               desc="batched8x16 committed by checkpoint and replay: 48 verifies "
+                                    "without snapshots, 48 replays of the accepted prefixes"),
     "prefill8192": dict(T=8192, layers=1,
                         desc="1 sequence of 8192 tokens, 16 q/k heads, 48 value heads, "
                              "d_k=d_v=128, bf16 q/k/v, chunk 64, WY/UT form on tensor cores"),
@@ -236,18 +244,19 @@ class OracleSampler:
 
     def __init__(self, wl_name):
         self.wl = wl_name
-        if wl_name == "chain16":
+        if wl_name.startswith("chain16"):
             inp = synthetic.chain16()
         elif wl_name == "tree22":
             inp = synthetic.tree22()
-        elif wl_name == "batched8x16":
+        elif wl_name.startswith("batched8x16"):
             inp = synthetic.batched8x16_layer(0)
         else:
             inp = None
         self.inp = inp
 
     def run(self, n_heads=1):
-        """Verify + commit for n_heads value heads of sequence 0; returns node-heads."""
+        """Verify + commit (copy, or replay for the *_replay workloads) for n_heads
+        value heads of sequence 0; returns node-heads."""
         import oracle
 
         inp = self.inp
@@ -266,9 +275,15 @@ class OracleSampler:
         st, snap, _ = oracle.verify(q, k, v, al, be, cache, np.zeros(1, np.int32), parent, B=1,
                                     N=N, Hk=n_heads, Hv=n_heads, dk=inp["dk"], dv=inp["dv"])
         assert st == oracle.OK
-        dst = np.zeros((1, n_heads, inp["dk"], inp["dv"]))
-        st = oracle.commit(snap, inp["accept"][b:b + 1], dst, None, B=1, N=N, Hv=n_heads,
-                           dk=inp["dk"], dv=inp["dv"])
+        if self.wl.endswith("_replay"):
+            dst = np.ascontiguousarray(cache, dtype=np.float64).copy()
+            st = oracle.replay(k, v, al, be, dst, np.zeros(1, np.int32), parent,
+                               inp["accept"][b:b + 1], B=1, N=N, Hk=n_heads, Hv=n_heads,
+                               dk=inp["dk"], dv=inp["dv"])
+        else:
+            dst = np.zeros((1, n_heads, inp["dk"], inp["dv"]))
+            st = oracle.commit(snap, inp["accept"][b:b + 1], dst, None, B=1, N=N, Hv=n_heads,
+                               dk=inp["dk"], dv=inp["dv"])
         assert st == oracle.OK
         return N * n_heads
 
@@ -320,7 +335,7 @@ class VerifyCase:
 
     NAMES = ("q", "k", "v", "alpha", "beta", "accept")
 
-    def __init__(self, inp, torch, pinned=False):
+    def __init__(self, inp, torch, pinned=False, persist=True):
         self.inp = inp
         self.B, self.N, self.Hv = inp["B"], inp["N"], inp["Hv"]
         dk, dv = inp["dk"], inp["dv"]
@@ -343,7 +358,8 @@ class VerifyCase:
         self.cache = _dev(inp["cache"], torch)
         self.slot = _dev(inp["slot"], torch)
         self.parent = _dev(inp["parent"], torch) if inp["tree"] else None
-        self.snap = torch.empty((self.B, self.N, self.Hv, dk, dv), device="cuda")
+        self.snap = (torch.empty((self.B, self.N, self.Hv, dk, dv), device="cuda") if persist
+                     else None)
         self.o = torch.empty((self.B, self.N, self.Hv, dv), device="cuda")
         self.host = None
         if pinned:
@@ -357,6 +373,12 @@ class VerifyCase:
             gdn.gdn_verify_tree(*args, self.parent, slot=self.slot, n_slots=self.inp["n_slots"])
         else:
             gdn.gdn_verify_chain(*args, slot=self.slot, n_slots=self.inp["n_slots"])
+
+    def replay(self, gdn):
+        d = self.dev
+        gdn.gdn_replay_accepted(d["k"], d["v"], d["alpha"], d["beta"], self.cache, d["accept"],
+                                parent=self.parent, slot=self.slot,
+                                n_slots=self.inp["n_slots"])
 
     def h2d(self):
         self.packed.copy_(self.host, non_blocking=True)
@@ -386,24 +408,27 @@ def run_ours(args, wl_name, world, rank, local):
 
     Hk, Hv, dk, dv = HEADS["Hk"], HEADS["Hv"], HEADS["dk"], HEADS["dv"]
     B, N = wl["B"], wl["N"]
-    L = args.layers if (args.layers and wl_name == "batched8x16") else wl["layers"]
-    if wl_name == "batched8x16":
+    replay = wl.get("replay", False)
+    batched = wl_name.startswith("batched8x16")
+    L = args.layers if (args.layers and batched) else wl["layers"]
+    if batched:
         layers = []
         for l in range(L):
             inp = synthetic.batched8x16_layer(l)
             if rank:
                 inp = dict(inp)  # replicas share shapes; the data is the same recipe
-            layers.append(VerifyCase(inp, torch, pinned=True))
+            layers.append(VerifyCase(inp, torch, pinned=True, persist=not replay))
         # one cache for all layers: [layer][slot][Hv][dk][dv]; snapshots likewise
         cache_all = torch.stack([c.cache for c in layers])
-        snap_all = torch.empty((L, B, N, Hv, dk, dv), device="cuda")
+        snap_all = None if replay else torch.empty((L, B, N, Hv, dk, dv), device="cuda")
         for l, c in enumerate(layers):
             c.cache = cache_all[l]
-            c.snap = snap_all[l]
+            if not replay:
+                c.snap = snap_all[l]
         commit_layers = L
     else:
-        inp = synthetic.chain16() if wl_name == "chain16" else synthetic.tree22()
-        layers = [VerifyCase(inp, torch, pinned=True)]
+        inp = synthetic.tree22() if wl.get("tree") else synthetic.chain16()
+        layers = [VerifyCase(inp, torch, pinned=True, persist=not replay)]
         cache_all = layers[0].cache
         snap_all = layers[0].snap
         commit_layers = 1
@@ -411,6 +436,11 @@ def run_ours(args, wl_name, world, rank, local):
     slot = layers[0].slot
 
     def commit():
+        if replay:
+            # checkpoint and replay: the accepted prefix of every layer again
+            for c in layers:
+                c.replay(gdn)
+            return
         gdn.gdn_commit_accepted(snap_all, accept, cache_all, B=B, N=N, Hv=Hv, dk=dk, dv=dv,
                                 n_layers=commit_layers, snap_layer_stride=B * N * Hv * dk * dv,
                                 cache_layer_stride=B * Hv * dk * dv, slot=slot, n_slots=B)
@@ -429,7 +459,7 @@ def run_ours(args, wl_name, world, rank, local):
         if ev is not None:
             ev[2].record(stream)
 
-    launches_per_step = len(layers) + 1
+    launches_per_step = len(layers) * 2 if replay else len(layers) + 1
     for _ in range(args.warmup):
         flush.fill_(1.0)
         step()
@@ -476,7 +506,7 @@ def run_ours(args, wl_name, world, rank, local):
     node_heads = B * N * Hv * len(layers)
     value = job_throughput(node_heads, args.steps, total_ms, world)
     hbm, bf16, peak_kind = measured_peaks()
-    vbytes = verify_bytes(B, N, Hk, Hv, dk, dv, tree=wl.get("tree", False))
+    vbytes = verify_bytes(B, N, Hk, Hv, dk, dv, tree=wl.get("tree", False), persist=not replay)
     launch_ms = statistics.mean(verify_ms) / len(layers)
     achieved = vbytes / (launch_ms / 1e3) / 1e9
     clocks = sampler.summary(t0, t1)
@@ -509,7 +539,8 @@ def run_ours(args, wl_name, world, rank, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "gdn_verify_tree" if wl.get("tree") else "gdn_verify_chain",
+            "kernel": ("gdn_verify_tree" if wl.get("tree") else "gdn_verify_chain") +
+                      (" (no snapshots)" if replay else ""),
             "achieved": achieved,
             "peak": hbm,
             "unit": "GB/s",

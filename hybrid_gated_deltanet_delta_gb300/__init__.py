@@ -7,8 +7,8 @@ in the library's CUDA kernels; there is no CPU or PyTorch fallback, and the
 functions raise if the library is missing or a call fails.
 
 Entry points (same names as the C ABI):
-  gdn_verify_chain, gdn_verify_tree, gdn_commit_accepted,
-  gdn_prefill_chunked, gdn_prefill_workspace_bytes
+  gdn_verify_chain, gdn_verify_tree, gdn_commit_accepted, gdn_replay_accepted,
+  gdn_prefill_chunked, gdn_prefill_workspace_bytes, gdn_prefill_chunked_noalloc
 """
 from __future__ import annotations
 
@@ -75,6 +75,8 @@ def load(path: str | None = None):
     lib.gdn_commit_accepted.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32,
                                         i32, P, P]
     lib.gdn_commit_accepted.restype = ctypes.c_int
+    lib.gdn_replay_accepted.argtypes = [ctypes.POINTER(VerifyArgs), P, P, P]
+    lib.gdn_replay_accepted.restype = ctypes.c_int
     lib.gdn_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.gdn_prefill_workspace_bytes.restype = sz
     lib.gdn_prefill_chunked.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, P, P,
@@ -136,24 +138,29 @@ def make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, *, slot=No
                      status=None, cache_slot_stride=None, tile_cols=0, row_warps=0):
     """Build a gdn_verify_args from tensors.  q, k [B,N,Hk,dk]; v [B,N,Hv,dv];
     alpha, beta [B,N,Hv] fp32; state_cache [n_slots,Hv,dk,dv] fp32 (or any
-    buffer with `cache_slot_stride`); snapshots [B,N,Hv,dk,dv] fp32; o [B,N,Hv,dv] fp32."""
-    B, N, Hk, dk = q.shape
+    buffer with `cache_slot_stride`); snapshots [B,N,Hv,dk,dv] fp32 or None
+    (a chain committed by replay); o [B,N,Hv,dv] fp32.  q and o may be None for
+    gdn_replay_accepted."""
+    B, N, Hk, dk = k.shape
     Hv, dv = v.shape[2], v.shape[3]
     for t in (q, k, v, alpha, beta, state_cache, snapshots, o):
-        _need(t.is_contiguous(), "all tensors must be contiguous")
-    _need(k.shape == q.shape and v.shape[:2] == (B, N), "q/k/v shapes disagree")
-    _need(q.dtype == k.dtype == v.dtype, "q, k and v must share a dtype")
+        _need(t is None or t.is_contiguous(), "all tensors must be contiguous")
+    _need((q is None or q.shape == k.shape) and v.shape[:2] == (B, N), "q/k/v shapes disagree")
+    _need((q is None or q.dtype == k.dtype) and k.dtype == v.dtype,
+          "q, k and v must share a dtype")
     if cache_slot_stride is None:
         cache_slot_stride = Hv * dk * dv
     if n_slots is None:
         n_slots = state_cache.numel() // cache_slot_stride
+    def ptr(t):
+        return None if t is None else t.data_ptr()
+
     return VerifyArgs(
-        q=q.data_ptr(), k=k.data_ptr(), v=v.data_ptr(), alpha=alpha.data_ptr(),
-        beta=beta.data_ptr(), state_cache=state_cache.data_ptr(),
-        slot=None if slot is None else slot.data_ptr(), snapshots=snapshots.data_ptr(),
-        o=o.data_ptr(), status=None if status is None else status.data_ptr(),
+        q=ptr(q), k=k.data_ptr(), v=v.data_ptr(), alpha=alpha.data_ptr(),
+        beta=beta.data_ptr(), state_cache=state_cache.data_ptr(), slot=ptr(slot),
+        snapshots=ptr(snapshots), o=ptr(o), status=ptr(status),
         cache_slot_stride=cache_slot_stride, n_slots=n_slots, B=B, N=N, Hk=Hk, Hv=Hv, dk=dk,
-        dv=dv, in_dtype=_dtype_code(q), tile_cols=tile_cols, row_warps=row_warps)
+        dv=dv, in_dtype=_dtype_code(k), tile_cols=tile_cols, row_warps=row_warps)
 
 
 def gdn_verify_chain(q, k, v, alpha, beta, state_cache, snapshots, o, *, slot=None, n_slots=None,
@@ -190,6 +197,24 @@ def gdn_commit_accepted(snapshots, accept_idx, state_cache, *, B, N, Hv, dk, dv,
                                       _ptr(state_cache), cache_slot_stride, cache_layer_stride,
                                       _ptr(slot), n_slots, B, N, Hv, dk, dv, n_layers,
                                       _ptr(status), _stream(stream)), "gdn_commit_accepted")
+
+
+def gdn_replay_accepted(k, v, alpha, beta, state_cache, accept_idx, *, parent=None, slot=None,
+                        n_slots=None, status=None, cache_slot_stride=None, tile_cols=0,
+                        row_warps=0, stream=None):
+    """Checkpoint-and-replay commit: state_cache[slot[b]] <- the state of node
+    accept_idx[b], recomputed over the accepted path from the cached state
+    (chain when parent is None; parent [B,N] int32 for a tree)."""
+    if parent is not None:
+        _need(parent.is_contiguous() and tuple(parent.shape) == tuple(k.shape[:2]),
+              "parent must be a contiguous [B,N] int32 tensor")
+    _need(accept_idx.is_contiguous() and accept_idx.numel() == k.shape[0],
+          "accept_idx must be a contiguous [B] int32 tensor")
+    a = make_verify_args(None, k, v, alpha, beta, state_cache, None, None, slot=slot,
+                         n_slots=n_slots, status=status, cache_slot_stride=cache_slot_stride,
+                         tile_cols=tile_cols, row_warps=row_warps)
+    _check(load().gdn_replay_accepted(ctypes.byref(a), _ptr(parent), _ptr(accept_idx),
+                                      _stream(stream)), "gdn_replay_accepted")
 
 
 def gdn_prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk=64) -> int:

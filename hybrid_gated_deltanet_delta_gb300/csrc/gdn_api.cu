@@ -36,11 +36,15 @@ int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   const int64_t head_set = (int64_t)a->Hv * a->dk * a->dv;
   if (a->cache_slot_stride < head_set) return GDN_ERR_INVALID_ARG;
   if (a->cache_slot_stride % 4 != 0) return GDN_ERR_MISALIGNED;
-  const void* need16[] = {a->q, a->k, a->v, a->state_cache, a->snapshots, a->o};
+  const void* need16[] = {a->q, a->k, a->v, a->state_cache, a->o};
   for (const void* p : need16) {
     if (p == nullptr) return GDN_ERR_INVALID_ARG;
     if (!gdn::aligned16(p)) return GDN_ERR_MISALIGNED;
   }
+  // a chain may skip persistence (commit by replay); a tree re-reads persisted
+  // states when its stash pool runs out, so it needs them
+  if (a->snapshots == nullptr && tree) return GDN_ERR_INVALID_ARG;
+  if (a->snapshots != nullptr && !gdn::aligned16(a->snapshots)) return GDN_ERR_MISALIGNED;
   if (a->alpha == nullptr || a->beta == nullptr) return GDN_ERR_INVALID_ARG;
   if (tree && parent == nullptr) return GDN_ERR_INVALID_ARG;
   const void* need4[] = {a->alpha, a->beta, a->slot, a->status, parent, depth_out};
@@ -56,9 +60,45 @@ int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
                             static_cast<cudaStream_t>(stream));
 }
 
+int replay_common(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept,
+                  void* stream) {
+  if (a == nullptr) return GDN_ERR_INVALID_ARG;
+  if (a->B < 0 || a->N < 1 || a->Hk < 1 || a->Hv < 1 || a->Hv % a->Hk != 0)
+    return GDN_ERR_INVALID_ARG;
+  if (a->in_dtype != GDN_F32 && a->in_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (a->N > 64 || a->B > 65535 || a->Hv > 65535) return GDN_ERR_UNSUPPORTED;
+  if (a->dk != 16 && a->dk != 32 && a->dk != 64 && a->dk != 128) return GDN_ERR_UNSUPPORTED;
+  if (a->dv < 16 || a->dv > 1024 || a->dv % 16 != 0) return GDN_ERR_UNSUPPORTED;
+  if (a->B == 0) return GDN_OK;
+  if (a->n_slots < 1) return GDN_ERR_INVALID_ARG;
+  const int64_t head_set = (int64_t)a->Hv * a->dk * a->dv;
+  if (a->cache_slot_stride < head_set) return GDN_ERR_INVALID_ARG;
+  if (a->cache_slot_stride % 4 != 0) return GDN_ERR_MISALIGNED;
+  const void* need16[] = {a->k, a->v, a->state_cache};
+  for (const void* p : need16) {
+    if (p == nullptr) return GDN_ERR_INVALID_ARG;
+    if (!gdn::aligned16(p)) return GDN_ERR_MISALIGNED;
+  }
+  if (a->alpha == nullptr || a->beta == nullptr || accept == nullptr) return GDN_ERR_INVALID_ARG;
+  const void* need4[] = {a->alpha, a->beta, a->slot, a->status, parent, accept};
+  for (const void* p : need4)
+    if (!ok_ptr4(p)) return GDN_ERR_MISALIGNED;
+  int wc = 0, nw = 0;
+  auto_tile(a->dk, a->dv, a->B, a->Hv, &wc, &nw);
+  if (a->tile_cols != 0) wc = a->tile_cols;
+  if (a->row_warps != 0) nw = a->row_warps;
+  if (!gdn::verify_tile_supported(a->dk, wc, nw) || a->dv % wc != 0) return GDN_ERR_UNSUPPORTED;
+  return gdn::launch_replay(a, parent, accept, wc, static_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 extern "C" {
+
+int gdn_replay_accepted(const gdn_verify_args* args, const int32_t* parent,
+                        const int32_t* accept_idx, void* stream) {
+  return replay_common(args, parent, accept_idx, stream);
+}
 
 int gdn_verify_chain(const gdn_verify_args* args, void* stream) {
   return verify_common(args, nullptr, nullptr, false, stream);

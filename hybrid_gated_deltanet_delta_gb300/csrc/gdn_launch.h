@@ -14,6 +14,10 @@ bool verify_tile_supported(int dk, int wc, int nw);
 int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, int wc,
                   int nw, cudaStream_t stream);
 
+// Replay of the accepted path from the cached state, written back in place.
+int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept, int wc,
+                  cudaStream_t stream);
+
 int launch_commit(const float* snap, int64_t snap_layer_stride, const int32_t* accept,
                   float* cache, int64_t cache_slot_stride, int64_t cache_layer_stride,
                   const int32_t* slot, int n_slots, int B, int N, int Hv, int dk, int dv,

@@ -305,7 +305,9 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
   }
 
   const int64_t node_stride = (int64_t)p.Hv * DK * dv;
-  float* snap_h = p.snap + ((int64_t)b * N * p.Hv + h) * DK * dv + (int64_t)row0 * dv + j0 + cg * 4;
+  float* snap_h = p.snap == nullptr ? nullptr
+                                    : p.snap + ((int64_t)b * N * p.Hv + h) * DK * dv +
+                                          (int64_t)row0 * dv + j0 + cg * 4;
   float* o_h = p.o + ((int64_t)b * N * p.Hv + h) * dv + j0 + cg * 4;
   // a stash slot holds each lane's R x 4 block lane-major: row m of lane l at
   // float offset (m*32 + l)*4, so every slot access is bank-conflict free
@@ -411,11 +413,14 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) u[c] = next_chain ? fmaf(al, red[c], d[c] * red[4]) : red[c];
 
-    // (f) persist
+    // (f) persist (a chain verified for a replay commit keeps no snapshots)
     if (rl == 0) st_f4(o_h + (int64_t)n * p.Hv * dv, red[5], red[6], red[7], red[8]);
-    float* dst = snap_h + (int64_t)n * node_stride;
+    if (p.snap != nullptr) {
+      float* dst = snap_h + (int64_t)n * node_stride;
 #pragma unroll
-    for (int m = 0; m < R; ++m) st_f4(dst + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
+      for (int m = 0; m < R; ++m)
+        st_f4(dst + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
+    }
 #pragma unroll
     for (int m = 0; m < R; ++m) kn[m] = knx[m];
   }
@@ -430,6 +435,209 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
       }
     }
   }
+}
+
+// ---------------------------------------------------------------- replay
+// Checkpoint-and-replay commit: the recurrence again over the accepted path
+// (chain: nodes 0 .. acc; tree: the ancestors of acc from the root), from the
+// cached state, written back into the same cache slot.  Same slab
+// decomposition as verify; along a path every node continues from the
+// previous one, so u always comes from the look-ahead
+//     u_{i+1} = alpha_i (H_{i-1}^T k_{i+1}) + delta_i (k_i . k_{i+1}),
+// which also makes a chain replay repeat the verify kernel's arithmetic.
+struct ReplayParams {
+  const void* k;
+  const void* v;
+  const float* alpha;
+  const float* beta;
+  float* cache;
+  const int32_t* slot;
+  const int32_t* parent;
+  const int32_t* accept;
+  int32_t* status;
+  int64_t cache_slot_stride;
+  int n_slots, N, Hk, Hv, dv, bf16;
+};
+
+struct ReplayPlan {
+  int path, par, k, v, a, b, total;
+};
+
+__host__ __device__ inline ReplayPlan replay_plan(int N, int DK, int WC, int esz) {
+  ReplayPlan s{};
+  s.path = 0;
+  s.par = s.path + round16(N * 4);
+  s.k = s.par + round16(N * 4);
+  s.v = s.k + round16(N * DK * esz);
+  s.a = s.v + round16(N * WC * esz);
+  s.b = s.a + round16(N * 4);
+  s.total = s.b + round16(N * 4);
+  return s;
+}
+
+template <int DK, int WC>
+__global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
+  using S = Shape<DK, WC>;
+  constexpr int R = S::R;
+  extern __shared__ __align__(16) char smem[];
+  const int N = p.N;
+  const bool bf16 = p.bf16 != 0;
+  const int esz = bf16 ? 2 : 4;
+  const ReplayPlan pl = replay_plan(N, DK, WC, esz);
+  int* spath = reinterpret_cast<int*>(smem + pl.path);
+  int* spar = reinterpret_cast<int*>(smem + pl.par);
+  char* sk = smem + pl.k;
+  char* sv = smem + pl.v;
+  float* sa = reinterpret_cast<float*>(smem + pl.a);
+  float* sb = reinterpret_cast<float*>(smem + pl.b);
+
+  const int lane = threadIdx.x;
+  const int cg = lane % S::CG, rl = lane / S::CG;
+  const int j0 = blockIdx.x * WC, h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / (p.Hv / p.Hk);
+  const bool lead = blockIdx.x == 0 && blockIdx.y == 0;
+  const int dv = p.dv;
+  const int row0 = rl * R;
+  const int64_t node0 = (int64_t)b * N;
+
+  const int acc = __ldg(p.accept + b);
+  const int sl = p.slot != nullptr ? __ldg(p.slot + b) : b;
+  if (acc < 0 || acc >= N) {
+    if (lead && lane == 0) report(p.status, GDN_ERR_ACCEPT_RANGE);
+    return;
+  }
+  if (sl < 0 || sl >= p.n_slots) {
+    if (lead && lane == 0) report(p.status, GDN_ERR_SLOT_RANGE);
+    return;
+  }
+
+  // ---- the accepted path, root first
+  int L = acc + 1;
+  if (p.parent == nullptr) {
+    for (int n = lane; n < L; n += 32) spath[n] = n;
+  } else {
+    bool ok = true;
+    for (int n = lane; n < N; n += 32) {
+      const int pp = __ldg(p.parent + node0 + n);
+      spar[n] = pp;
+      ok = ok && (n == 0 ? pp == -1 : (pp >= 0 && pp < n));
+    }
+    if (!__all_sync(FULL, ok)) {
+      if (lead && lane == 0) report(p.status, GDN_ERR_BAD_TREE);
+      return;
+    }
+    __syncwarp();
+    int len = 0;
+    if (lane == 0) {
+      for (int m = acc; m >= 0; m = spar[m]) ++len;
+      int i = len;
+      for (int m = acc; m >= 0; m = spar[m]) spath[--i] = m;
+    }
+    L = __shfl_sync(FULL, len, 0);
+  }
+  __syncwarp();
+
+  // ---- stage k, v, gates of the path nodes
+  {
+    const char* kb = static_cast<const char*>(p.k) + ((node0 * p.Hk + hk) * DK) * esz;
+    const char* vb = static_cast<const char*>(p.v) + ((node0 * p.Hv + h) * dv + j0) * esz;
+    const int64_t kstride = (int64_t)p.Hk * DK * esz, vstride = (int64_t)p.Hv * dv * esz;
+    const int kper = DK * esz / 16, vper = WC * esz / 16;
+    for (int idx = lane; idx < L * kper; idx += 32) {
+      const int r = idx / kper, c = idx - r * kper;
+      cp_async16(sk + r * DK * esz + c * 16, kb + spath[r] * kstride + c * 16);
+    }
+    for (int idx = lane; idx < L * vper; idx += 32) {
+      const int r = idx / vper, c = idx - r * vper;
+      cp_async16(sv + r * WC * esz + c * 16, vb + spath[r] * vstride + c * 16);
+    }
+    for (int r = lane; r < L; r += 32) {
+      cp_async4(sa + r, p.alpha + (node0 + spath[r]) * p.Hv + h);
+      cp_async4(sb + r, p.beta + (node0 + spath[r]) * p.Hv + h);
+    }
+  }
+
+  // ---- the cached state -> registers
+  float* c0 = p.cache + (int64_t)sl * p.cache_slot_stride + (int64_t)h * DK * dv +
+              (int64_t)row0 * dv + j0 + cg * 4;
+  float2 H[R][2];
+#pragma unroll
+  for (int m = 0; m < R; ++m) {
+    const float4 t = *reinterpret_cast<const float4*>(c0 + (int64_t)m * dv);
+    H[m][0] = make_float2(t.x, t.y);
+    H[m][1] = make_float2(t.z, t.w);
+  }
+  cp_async_wait_all();
+  __syncwarp();
+
+  float kn[R];
+  load_rows<R>(kn, sk, row0, bf16);
+  float u[4];
+  {
+    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+      a01 = __ffma2_rn(H[m][0], f2(kn[m]), a01);
+      a23 = __ffma2_rn(H[m][1], f2(kn[m]), a23);
+    }
+    u[0] = a01.x; u[1] = a01.y; u[2] = a23.x; u[3] = a23.y;
+#pragma unroll
+    for (int off = S::CG; off < 32; off <<= 1)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
+  }
+  for (int i = 0; i < L; ++i) {
+    float knx[R];
+    if (i + 1 < L) {
+      load_rows<R>(knx, sk + (i + 1) * DK * esz, row0, bf16);
+    } else {
+#pragma unroll
+      for (int m = 0; m < R; ++m) knx[m] = 0.f;
+    }
+    float vj[4];
+    load_rows<4>(vj, sv + i * WC * esz, cg * 4, bf16);
+    const float al = sa[i], be = sb[i];
+    float2 w01 = make_float2(0.f, 0.f), w23 = make_float2(0.f, 0.f);
+    float kk = 0.f;
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+      w01 = __ffma2_rn(H[m][0], f2(knx[m]), w01);
+      w23 = __ffma2_rn(H[m][1], f2(knx[m]), w23);
+      kk = fmaf(kn[m], knx[m], kk);
+    }
+    float d[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) d[c] = be * (vj[c] - al * u[c]);
+    const float2 d01 = make_float2(d[0], d[1]), d23 = make_float2(d[2], d[3]);
+    const float2 al2 = f2(al);
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+      H[m][0] = __ffma2_rn(f2(kn[m]), d01, __fmul2_rn(al2, H[m][0]));
+      H[m][1] = __ffma2_rn(f2(kn[m]), d23, __fmul2_rn(al2, H[m][1]));
+    }
+    float red[5] = {w01.x, w01.y, w23.x, w23.y, kk};
+#pragma unroll
+    for (int off = S::CG; off < 32; off <<= 1)
+#pragma unroll
+      for (int e = 0; e < 5; ++e) red[e] += __shfl_xor_sync(FULL, red[e], off);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) u[c] = fmaf(al, red[c], d[c] * red[4]);
+#pragma unroll
+    for (int m = 0; m < R; ++m) kn[m] = knx[m];
+  }
+
+  // ---- back into the cache slot (this warp is the only reader and writer)
+#pragma unroll
+  for (int m = 0; m < R; ++m)
+    st_f4(c0 + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
+}
+
+template <int DK, int WC>
+int launch_replay_t(const ReplayParams& p, int B, cudaStream_t stream) {
+  const ReplayPlan pl = replay_plan(p.N, DK, WC, p.bf16 ? 2 : 4);
+  const dim3 grid(p.dv / WC, p.Hv, B);
+  replay_kernel<DK, WC><<<grid, 32, pl.total, stream>>>(p);
+  return launch_status();
 }
 
 template <int DK, int WC, bool TREE>
@@ -497,6 +705,39 @@ int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   p.bf16 = a->in_dtype == GDN_BF16;
   if (parent != nullptr) return dispatch<true>(p, a->B, a->dk, wc, stream);
   return dispatch<false>(p, a->B, a->dk, wc, stream);
+}
+
+int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept, int wc,
+                  cudaStream_t stream) {
+  ReplayParams p{};
+  p.k = a->k;
+  p.v = a->v;
+  p.alpha = a->alpha;
+  p.beta = a->beta;
+  p.cache = const_cast<float*>(a->state_cache);
+  p.slot = a->slot;
+  p.parent = parent;
+  p.accept = accept;
+  p.status = a->status;
+  p.cache_slot_stride = a->cache_slot_stride;
+  p.n_slots = a->n_slots;
+  p.N = a->N;
+  p.Hk = a->Hk;
+  p.Hv = a->Hv;
+  p.dv = a->dv;
+  p.bf16 = a->in_dtype == GDN_BF16;
+#define GDN_CASE(DK_, WC_) \
+  if (a->dk == DK_ && wc == WC_) return launch_replay_t<DK_, WC_>(p, a->B, stream);
+  GDN_CASE(128, 16)
+  GDN_CASE(128, 8)
+  GDN_CASE(64, 16)
+  GDN_CASE(64, 8)
+  GDN_CASE(32, 16)
+  GDN_CASE(32, 8)
+  GDN_CASE(16, 16)
+  GDN_CASE(16, 8)
+#undef GDN_CASE
+  return GDN_ERR_UNSUPPORTED;
 }
 
 }  // namespace gdn

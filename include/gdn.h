@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define GDN_VERSION 1
+#define GDN_VERSION 2
 
 typedef enum gdn_status {
   GDN_OK = 0,
@@ -79,7 +79,9 @@ typedef enum gdn_dtype {
  *                 state_cache + slot[b]*cache_slot_stride + h*dk*dv
  *   slot          [B] int32 cache slot per sequence; NULL means slot[b] = b
  *   n_slots       number of valid slots (slot[b] is checked against it)
- *   snapshots     [B][N][Hv][dk][dv] fp32 output: S_n of every node
+ *   snapshots     [B][N][Hv][dk][dv] fp32 output: S_n of every node.  May be
+ *                 NULL for a chain: nothing is persisted and the accepted
+ *                 state is committed by replay (gdn_replay_accepted)
  *   o             [B][N][Hv][dv] fp32 output
  *   status        optional device int32 error word (see above)
  *   tile_cols, row_warps
@@ -117,7 +119,8 @@ typedef struct gdn_verify_args {
 /*
  * Causal-chain verification (DFlash block: the last committed token plus the
  * drafts).  Node n starts from node n-1's state; node 0 from the cache.
- * Writes every node's state to `snapshots` and its output to `o`.
+ * Writes every node's state to `snapshots` (when not NULL) and its output to
+ * `o`.
  */
 int gdn_verify_chain(const gdn_verify_args* args, void* stream);
 
@@ -150,6 +153,29 @@ int gdn_commit_accepted(const float* snapshots, int64_t snap_layer_stride,
                         int64_t cache_layer_stride, const int32_t* slot, int32_t n_slots,
                         int32_t B, int32_t N, int32_t Hv, int32_t dk, int32_t dv,
                         int32_t n_layers, int32_t* status, void* stream);
+
+/*
+ * Checkpoint-and-replay commit ("Photon 2.6", section "Handling recurrent
+ * state": keep the state from before the block and re-run the accepted
+ * tokens instead of persisting every node).  For every sequence b the
+ * recurrence is run again over the accepted path, starting from the cached
+ * state, and the result replaces the cached state in place:
+ *
+ *   state_cache[slot[b]][h] <- S_{accept_idx[b]} of the block
+ *
+ * The path is nodes 0 .. accept_idx[b] for a chain (parent == NULL; accept
+ * length L = accept_idx + 1) and the ancestors of accept_idx[b] from the root
+ * for a tree (parent [B][N] as in gdn_verify_tree).  Uses k, v, alpha, beta,
+ * state_cache, slot, n_slots, status and the sizes of `args` (args->q,
+ * snapshots and o are not used and may be NULL); here state_cache is read and
+ * written.  The state equals snapshots[b][accept_idx[b]] of a verify call on
+ * the same inputs up to floating-point rounding.  An accept index outside
+ * [0, N), a slot outside [0, n_slots) or a bad parent array skips that
+ * sequence and is reported through args->status.  Two sequences must not
+ * share a slot.
+ */
+int gdn_replay_accepted(const gdn_verify_args* args, const int32_t* parent,
+                        const int32_t* accept_idx, void* stream);
 
 /*
  * Chunked prefill of one sequence of T tokens: the same recurrence, evaluated

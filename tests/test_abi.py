@@ -30,8 +30,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("gdn_verify_chain", "gdn_verify_tree", "gdn_commit_accepted",
-                 "gdn_prefill_chunked", "gdn_prefill_workspace_bytes", "gdn_status_string",
-                 "gdn_version"):
+                 "gdn_replay_accepted", "gdn_prefill_chunked", "gdn_prefill_workspace_bytes",
+                 "gdn_status_string", "gdn_version"):
         assert want in names
 
 
@@ -58,7 +58,7 @@ def test_struct_layout_matches_c(tmp_path):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.gdn_version() == 1
+    assert lib.gdn_version() == 2
     assert gdn.status_string(gdn.GDN_ERR_BAD_TREE) == "GDN_ERR_BAD_TREE"
     assert gdn.status_string(12345) == "GDN_ERR_UNKNOWN"
 
@@ -83,7 +83,6 @@ def _args(**kw):
     (dict(dk=96), gdn.GDN_ERR_UNSUPPORTED),
     (dict(dv=40), gdn.GDN_ERR_UNSUPPORTED),
     (dict(q=0), gdn.GDN_ERR_INVALID_ARG),
-    (dict(snapshots=0), gdn.GDN_ERR_INVALID_ARG),
     (dict(alpha=0), gdn.GDN_ERR_INVALID_ARG),
     (dict(v=0x30008), gdn.GDN_ERR_MISALIGNED),
     (dict(o=0x80004), gdn.GDN_ERR_MISALIGNED),
@@ -105,6 +104,42 @@ def test_verify_host_checks(lib, change, want):
 def test_verify_tree_needs_parent(lib):
     assert lib.gdn_verify_tree(ctypes.byref(_args()), None, None, None) == gdn.GDN_ERR_INVALID_ARG
     assert lib.gdn_verify_chain(None, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_verify_tree_needs_snapshots(lib):
+    """A chain may skip persistence (commit by replay); a tree may not.  Only
+    the tree call is made: the chain call would pass the checks and launch."""
+    a = _args(snapshots=0)
+    assert lib.gdn_verify_tree(ctypes.byref(a), ctypes.c_void_p(0x90000), None, None) == \
+        gdn.GDN_ERR_INVALID_ARG
+    a = _args(snapshots=0x70004, q=0)
+    assert lib.gdn_verify_chain(ctypes.byref(a), None) == gdn.GDN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("change, acc, want", [
+    (dict(N=0), 0xA0000, gdn.GDN_ERR_INVALID_ARG),
+    (dict(B=-1), 0xA0000, gdn.GDN_ERR_INVALID_ARG),
+    (dict(Hv=47), 0xA0000, gdn.GDN_ERR_INVALID_ARG),
+    (dict(N=65), 0xA0000, gdn.GDN_ERR_UNSUPPORTED),
+    (dict(dk=96), 0xA0000, gdn.GDN_ERR_UNSUPPORTED),
+    (dict(k=0), 0xA0000, gdn.GDN_ERR_INVALID_ARG),
+    (dict(state_cache=0), 0xA0000, gdn.GDN_ERR_INVALID_ARG),
+    (dict(beta=0), 0xA0000, gdn.GDN_ERR_INVALID_ARG),
+    (dict(), 0, gdn.GDN_ERR_INVALID_ARG),
+    (dict(), 0xA0002, gdn.GDN_ERR_MISALIGNED),
+    (dict(v=0x30008), 0xA0000, gdn.GDN_ERR_MISALIGNED),
+    (dict(n_slots=0), 0xA0000, gdn.GDN_ERR_INVALID_ARG),
+    (dict(cache_slot_stride=100), 0xA0000, gdn.GDN_ERR_INVALID_ARG),
+    (dict(tile_cols=24), 0xA0000, gdn.GDN_ERR_UNSUPPORTED),
+    (dict(B=0), 0xA0000, gdn.GDN_OK),
+])
+def test_replay_host_checks(lib, change, acc, want):
+    """gdn_replay_accepted needs no q, snapshots or o; everything else is
+    checked as for verify (these calls never launch)."""
+    a = _args(q=0, snapshots=0, o=0, **change)
+    assert lib.gdn_replay_accepted(ctypes.byref(a), None, ctypes.c_void_p(acc), None) == want
+    assert lib.gdn_replay_accepted(ctypes.byref(a), ctypes.c_void_p(0x90000),
+                                   ctypes.c_void_p(acc), None) == want
 
 
 def _commit(lib, **kw):
