@@ -106,6 +106,14 @@ WORKLOADS = {
     "batched8x16_replay": dict(B=8, N=16, tree=False, layers=48, replay=True,
                                desc="batched8x16 committed by checkpoint and replay: 48 verifies "
                                     "without snapshots, 48 replays of the accepted prefixes"),
+    "chain16_index": dict(B=1, N=16, tree=False, layers=1, index=True,
+                          desc="chain16 committed through the index table: verify reads its "
+                               "state from the previous block's snapshot region and writes "
+                               "its own snapshots there; commit sets slot[b] = b*N + accept"),
+    "batched8x16_index": dict(B=8, N=16, tree=False, layers=48, index=True,
+                              desc="batched8x16 committed through the index table: 48 verifies "
+                                   "on per-layer snapshot regions, one slot table for all "
+                                   "layers"),
     "prefill8192": dict(T=8192, layers=1,
                         desc="1 sequence of 8192 tokens, 16 q/k heads, 48 value heads, "
                              "d_k=d_v=128, bf16 q/k/v, chunk 64, WY/UT form on tensor cores"),
@@ -434,8 +442,24 @@ def run_ours(args, wl_name, world, rank, local):
         commit_layers = 1
     accept = layers[0].dev["accept"]
     slot = layers[0].slot
+    index = wl.get("index", False)
+    if index:
+        # the first verify of every layer reads the cache; afterwards each
+        # layer's snapshot region is its cache, addressed through one slot table
+        for c in layers:
+            c.verify(gdn)
+        slot_idx = torch.empty(B, dtype=torch.int32, device="cuda")
+        gdn.gdn_commit_index(accept, slot_idx, N=N)
+        for c in layers:
+            c.cache = c.snap.view(B * N, Hv, dk, dv)
+            c.slot = slot_idx
+            c.inp = dict(c.inp, n_slots=B * N)
+        torch.cuda.synchronize()
 
     def commit():
+        if index:
+            gdn.gdn_commit_index(accept, slot_idx, N=N)
+            return
         if replay:
             # checkpoint and replay: the accepted prefix of every layer again
             for c in layers:
@@ -445,7 +469,7 @@ def run_ours(args, wl_name, world, rank, local):
                                 n_layers=commit_layers, snap_layer_stride=B * N * Hv * dk * dv,
                                 cache_layer_stride=B * Hv * dk * dv, slot=slot, n_slots=B)
 
-    cache_init = cache_all.clone()
+    cache_init = None if index else cache_all.clone()
 
     def step(ev=None):
         """verify every layer, then commit; ev = (start, after_verify, end) events."""
@@ -487,7 +511,8 @@ def run_ours(args, wl_name, world, rank, local):
     total_ms = max_over_ranks(total_ms, world)
 
     # end to end through the public API: host inputs -> device -> verify/commit -> host o
-    cache_all.copy_(cache_init)
+    if cache_init is not None:
+        cache_all.copy_(cache_init)
     e2e_steps = min(args.steps, 200)
     e2e_s = 0.0
     h2d = d2h = 0
@@ -540,7 +565,8 @@ def run_ours(args, wl_name, world, rank, local):
         "roofline": {
             "bound": "hbm",
             "kernel": ("gdn_verify_tree" if wl.get("tree") else "gdn_verify_chain") +
-                      (" (no snapshots)" if replay else ""),
+                      (" (no snapshots)" if replay else
+                       " (state and snapshots in the slot region)" if index else ""),
             "achieved": achieved,
             "peak": hbm,
             "unit": "GB/s",

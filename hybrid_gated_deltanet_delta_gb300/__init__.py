@@ -7,7 +7,8 @@ in the library's CUDA kernels; there is no CPU or PyTorch fallback, and the
 functions raise if the library is missing or a call fails.
 
 Entry points (same names as the C ABI):
-  gdn_verify_chain, gdn_verify_tree, gdn_commit_accepted, gdn_replay_accepted,
+  gdn_verify_chain, gdn_verify_tree, gdn_commit_accepted, gdn_commit_index,
+  gdn_replay_accepted,
   gdn_prefill_chunked, gdn_prefill_workspace_bytes, gdn_prefill_chunked_noalloc
 """
 from __future__ import annotations
@@ -75,6 +76,8 @@ def load(path: str | None = None):
     lib.gdn_commit_accepted.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32,
                                         i32, P, P]
     lib.gdn_commit_accepted.restype = ctypes.c_int
+    lib.gdn_commit_index.argtypes = [P, i32, i32, i32, P, P, P]
+    lib.gdn_commit_index.restype = ctypes.c_int
     lib.gdn_replay_accepted.argtypes = [ctypes.POINTER(VerifyArgs), P, P, P]
     lib.gdn_replay_accepted.restype = ctypes.c_int
     lib.gdn_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
@@ -197,6 +200,16 @@ def gdn_commit_accepted(snapshots, accept_idx, state_cache, *, B, N, Hv, dk, dv,
                                       _ptr(state_cache), cache_slot_stride, cache_layer_stride,
                                       _ptr(slot), n_slots, B, N, Hv, dk, dv, n_layers,
                                       _ptr(status), _stream(stream)), "gdn_commit_accepted")
+
+
+def gdn_commit_index(accept_idx, slot, *, N, base_slot=0, status=None, stream=None):
+    """Index-table commit: slot[b] = base_slot + b*N + accept_idx[b] (int32
+    device tensors of B entries), so that the next verify reads its state from
+    this block's snapshots buffer."""
+    _need(accept_idx.is_contiguous() and slot.is_contiguous() and
+          accept_idx.numel() == slot.numel(), "accept_idx and slot must be [B] int32")
+    _check(load().gdn_commit_index(_ptr(accept_idx), accept_idx.numel(), N, base_slot, _ptr(slot),
+                                   _ptr(status), _stream(stream)), "gdn_commit_index")
 
 
 def gdn_replay_accepted(k, v, alpha, beta, state_cache, accept_idx, *, parent=None, slot=None,

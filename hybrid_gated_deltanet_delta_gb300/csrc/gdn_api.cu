@@ -133,6 +133,17 @@ int gdn_commit_accepted(const float* snapshots, int64_t snap_layer_stride,
                             dv, n_layers, status, static_cast<cudaStream_t>(stream));
 }
 
+int gdn_commit_index(const int32_t* accept_idx, int32_t B, int32_t N, int32_t base_slot,
+                     int32_t* slot, int32_t* status, void* stream) {
+  if (B < 0 || N < 1 || base_slot < 0) return GDN_ERR_INVALID_ARG;
+  if ((int64_t)base_slot + (int64_t)B * N > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+  if (B == 0) return GDN_OK;
+  if (accept_idx == nullptr || slot == nullptr) return GDN_ERR_INVALID_ARG;
+  if (!ok_ptr4(accept_idx) || !ok_ptr4(slot) || !ok_ptr4(status)) return GDN_ERR_MISALIGNED;
+  return gdn::launch_commit_index(accept_idx, B, N, base_slot, slot, status,
+                                  static_cast<cudaStream_t>(stream));
+}
+
 size_t gdn_prefill_workspace_bytes(int32_t T, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
                                    int32_t chunk) {
   if (T < 0 || Hk < 1 || Hv < 1 || dk < 1 || dv < 1 || chunk < 1) return 0;

@@ -47,7 +47,31 @@ commit_kernel(const float4* __restrict__ snap, int64_t snap_layer4, const int32_
   }
 }
 
+// Index-table commit: point each sequence's slot at its accepted node in the
+// block's snapshot region ("TokenSpeed hits 580 tok/s", section "How they
+// actually got there": move pointers, not data).  One thread per sequence.
+__global__ void commit_index_kernel(const int32_t* accept, int B, int N, int base_slot,
+                                    int32_t* slot, int32_t* status) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int a = __ldg(accept + b);
+  if (a < 0 || a >= N) {
+    report(status, GDN_ERR_ACCEPT_RANGE);
+    return;
+  }
+  slot[b] = base_slot + b * N + a;
+}
+
 }  // namespace
+
+int launch_commit_index(const int32_t* accept, int B, int N, int base_slot, int32_t* slot,
+                        int32_t* status, cudaStream_t stream) {
+  const int threads = 128;
+  commit_index_kernel<<<(B + threads - 1) / threads, threads, 0, stream>>>(accept, B, N,
+                                                                           base_slot, slot,
+                                                                           status);
+  return launch_status();
+}
 
 int launch_commit(const float* snap, int64_t snap_layer_stride, const int32_t* accept,
                   float* cache, int64_t cache_slot_stride, int64_t cache_layer_stride,

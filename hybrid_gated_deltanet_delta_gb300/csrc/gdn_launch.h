@@ -23,6 +23,10 @@ int launch_commit(const float* snap, int64_t snap_layer_stride, const int32_t* a
                   const int32_t* slot, int n_slots, int B, int N, int Hv, int dk, int dv,
                   int n_layers, int32_t* status, cudaStream_t stream);
 
+// slot[b] = base_slot + b*N + accept[b] (accept checked).
+int launch_commit_index(const int32_t* accept, int B, int N, int base_slot, int32_t* slot,
+                        int32_t* status, cudaStream_t stream);
+
 size_t prefill_workspace_bytes(int T, int Hk, int Hv, int dk, int dv, int chunk);
 int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const float* alpha,
                    const float* beta, int T, int Hk, int Hv, int dk, int dv, int chunk,

@@ -209,14 +209,15 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
     return;
   }
 
-  // ---- the cached state -> registers
+  // ---- the cached state -> registers (an L2 load: with an index-table
+  //      commit the cache is this block's snapshot region, written below)
   float2 H[R][2];
   {
     const float* c0 = p.cache + (int64_t)sl * p.cache_slot_stride + (int64_t)h * DK * dv +
                       (int64_t)row0 * dv + j0 + cg * 4;
 #pragma unroll
     for (int m = 0; m < R; ++m) {
-      const float4 t = ld_nc_f4(c0 + (int64_t)m * dv);
+      const float4 t = ld_cg_f4(c0 + (int64_t)m * dv);
       H[m][0] = make_float2(t.x, t.y);
       H[m][1] = make_float2(t.z, t.w);
     }

@@ -76,7 +76,10 @@ typedef enum gdn_dtype {
  *   alpha, beta   [B][N][Hv]      fp32 gates (decay alpha, write strength beta)
  *   state_cache   recurrent-state cache, READ ONLY here: the state of
  *                 sequence b, head h starts at
- *                 state_cache + slot[b]*cache_slot_stride + h*dk*dv
+ *                 state_cache + slot[b]*cache_slot_stride + h*dk*dv.
+ *                 It may be the snapshots buffer itself (index-table
+ *                 commit, gdn_commit_index): each sequence's state is read
+ *                 before any of its nodes is written
  *   slot          [B] int32 cache slot per sequence; NULL means slot[b] = b
  *   n_slots       number of valid slots (slot[b] is checked against it)
  *   snapshots     [B][N][Hv][dk][dv] fp32 output: S_n of every node.  May be
@@ -153,6 +156,24 @@ int gdn_commit_accepted(const float* snapshots, int64_t snap_layer_stride,
                         int64_t cache_layer_stride, const int32_t* slot, int32_t n_slots,
                         int32_t B, int32_t N, int32_t Hv, int32_t dk, int32_t dv,
                         int32_t n_layers, int32_t* status, void* stream);
+
+/*
+ * Index-table commit ("TokenSpeed hits 580 tok/s", section "How they actually
+ * got there": move pointers, not data -- the persisted states form a draft
+ * region and a small index table says which one is current).  No state is
+ * copied: the slot table is pointed at the accepted node's snapshot,
+ *
+ *   slot[b] = base_slot + b*N + accept_idx[b]
+ *
+ * so that a verify call given the snapshots buffer [B][N][Hv][dk][dv] of this
+ * block as its state_cache (cache_slot_stride = Hv*dk*dv, n_slots >=
+ * base_slot + B*N) starts every sequence from its accepted node; base_slot
+ * places the block's region inside a larger slot space.  That verify may
+ * write its own snapshots into the same buffer.  An accept index outside
+ * [0, N) leaves slot[b] unchanged and is reported through `status`.
+ */
+int gdn_commit_index(const int32_t* accept_idx, int32_t B, int32_t N, int32_t base_slot,
+                     int32_t* slot, int32_t* status, void* stream);
 
 /*
  * Checkpoint-and-replay commit ("Photon 2.6", section "Handling recurrent

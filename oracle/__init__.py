@@ -48,6 +48,8 @@ def bind(lib):
     lib.oracle_commit_f64.restype = ctypes.c_int
     lib.oracle_commit_f64.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32,
                                       i32, i32]
+    lib.oracle_commit_index.restype = ctypes.c_int
+    lib.oracle_commit_index.argtypes = [P, i32, i32, i32, P]
     lib.oracle_replay_f64.restype = ctypes.c_int
     lib.oracle_replay_f64.argtypes = [P, P, P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32,
                                       i32]
@@ -128,6 +130,14 @@ def commit(snap, accept, cache, slot, *, B, N, Hv, dk, dv, n_layers=1,
     return lib.oracle_commit_f64(_ptr(snap), snap_layer_stride, _ptr(acc), _ptr(cache),
                                  cache_slot_stride, cache_layer_stride, _ptr(slot_a), n_slots,
                                  B, N, Hv, dk, dv, n_layers)
+
+
+def commit_index(accept, slot, *, N, base=0):
+    """Index-table commit in place on `slot` (int32 array of B entries)."""
+    lib = _load()
+    assert slot.dtype == np.int32 and slot.flags.c_contiguous
+    acc = _c(accept, np.int32)
+    return lib.oracle_commit_index(_ptr(acc), len(acc), N, base, _ptr(slot))
 
 
 def replay(k, v, alpha, beta, cache, slot, parent, accept, *, B, N, Hk, Hv, dk, dv,

@@ -166,6 +166,22 @@ int replay(const R* k, const R* v, const R* alpha, const R* beta, R* cache,
 
 extern "C" {
 
+// Index-table commit ("TokenSpeed hits 580 tok/s", section "How they actually
+// got there": move pointers, not data): the accepted node's persisted state is
+// made current by pointing the sequence's slot at it in the block's snapshot
+// region, slot[b] = base + b*N + accept[b].  A bad accept index leaves the
+// slot as it was.
+int oracle_commit_index(const int32_t* accept, int32_t B, int32_t N, int32_t base,
+                        int32_t* slot) {
+  if (B < 0 || N <= 0 || base < 0) return ERR_INVALID_ARG;
+  int status = OK;
+  for (int b = 0; b < B; ++b) {
+    if (accept[b] < 0 || accept[b] >= N) { status = ERR_ACCEPT_RANGE; continue; }
+    slot[b] = base + b * N + accept[b];
+  }
+  return status;
+}
+
 // Replay commit, in place on `cache` (same layouts as oracle_verify_f64);
 // accept [B] is the accepted node index (chain: accept length - 1).
 int oracle_replay_f64(const double* k, const double* v, const double* alpha, const double* beta,

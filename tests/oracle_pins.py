@@ -489,6 +489,44 @@ def check_replay_equals_persist():
                    "a skipped sequence keeps its cached state")
 
 
+def check_index_commit_equals_copy():
+    """Index-table commit: a block that starts from the previous block's
+    snapshot region through the slot table computes exactly what it computes
+    after the accepted states were copied into the cache; a bad accept index
+    leaves its slot alone."""
+    rng = np.random.default_rng(37)
+    B, N, Hk, Hv, dk, dv = 3, 5, 2, 4, 4, 3
+    for tree in (False, True):
+        c1 = _case(rng, B=B, N=N, Hk=Hk, Hv=Hv, dk=dk, dv=dv, tree=tree)
+        snap1, _ = _run(c1)
+        acc = rng.integers(0, N, B).astype(np.int32)
+        # (a) copy commit into the cache, then block 2 from the cache
+        cache = np.ascontiguousarray(c1["cache"], dtype=np.float64).copy()
+        assert oracle.commit(snap1, acc, cache, c1["slot"], B=B, N=N, Hv=Hv, dk=dk,
+                             dv=dv) == oracle.OK
+        c2 = _case(rng, B=B, N=N, Hk=Hk, Hv=Hv, dk=dk, dv=dv, tree=tree)
+        st, snap_a, o_a = oracle.verify(c2["q"], c2["k"], c2["v"], c2["alpha"], c2["beta"],
+                                        cache, c1["slot"], c2["parent"], B=B, N=N, Hk=Hk,
+                                        Hv=Hv, dk=dk, dv=dv)
+        assert st == oracle.OK
+        # (b) index commit, then block 2 from block 1's snapshot region
+        base = 7
+        slot = np.full(B, -1, np.int32)
+        assert oracle.commit_index(acc, slot, N=N, base=base) == oracle.OK
+        assert [int(x) for x in slot] == [base + b * N + int(acc[b]) for b in range(B)]
+        region = np.zeros((base + B * N, Hv, dk, dv))
+        region[base:] = snap1.reshape(B * N, Hv, dk, dv)
+        st, snap_b, o_b = oracle.verify(c2["q"], c2["k"], c2["v"], c2["alpha"], c2["beta"],
+                                        region, slot, c2["parent"], B=B, N=N, Hk=Hk, Hv=Hv,
+                                        dk=dk, dv=dv)
+        assert st == oracle.OK
+        assert np.array_equal(snap_a, snap_b) and np.array_equal(o_a, o_b), \
+            "index-table commit differs from copy commit"
+    slot = np.array([3, 4], np.int32)
+    assert oracle.commit_index(np.array([1, 5], np.int32), slot, N=5) == oracle.ERR_ACCEPT_RANGE
+    assert [int(x) for x in slot] == [1, 4], "a bad accept index must leave its slot alone"
+
+
 def block_form_reference(H0, K, V, Q, alpha, beta, parent):
     """The whole block at once (float64, one value head): with G(n) the sum of
     log alpha over the root-to-n path and the deltas solved first from
@@ -543,5 +581,5 @@ ALL_CHECKS = [
     check_contraction, check_tree_matches_chain_and_paths, check_exact_rational_bruteforce,
     check_tree_depth_and_validation, check_commit, check_chunked_equals_step,
     check_rounds_equal_sequential, check_block_form_equals_recurrence,
-    check_replay_equals_persist,
+    check_replay_equals_persist, check_index_commit_equals_copy,
 ]

@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("gdn_verify_chain", "gdn_verify_tree", "gdn_commit_accepted",
-                 "gdn_replay_accepted", "gdn_prefill_chunked", "gdn_prefill_workspace_bytes",
+                 "gdn_commit_index", "gdn_replay_accepted", "gdn_prefill_chunked", "gdn_prefill_workspace_bytes",
                  "gdn_status_string", "gdn_version"):
         assert want in names
 
@@ -140,6 +140,24 @@ def test_replay_host_checks(lib, change, acc, want):
     assert lib.gdn_replay_accepted(ctypes.byref(a), None, ctypes.c_void_p(acc), None) == want
     assert lib.gdn_replay_accepted(ctypes.byref(a), ctypes.c_void_p(0x90000),
                                    ctypes.c_void_p(acc), None) == want
+
+
+@pytest.mark.parametrize("args, want", [
+    ((0xA0000, -1, 16, 0, 0xB0000, None), gdn.GDN_ERR_INVALID_ARG),
+    ((0xA0000, 4, 0, 0, 0xB0000, None), gdn.GDN_ERR_INVALID_ARG),
+    ((0xA0000, 4, 16, -2, 0xB0000, None), gdn.GDN_ERR_INVALID_ARG),
+    ((0xA0000, 1 << 27, 64, 0, 0xB0000, None), gdn.GDN_ERR_UNSUPPORTED),
+    ((None, 4, 16, 0, 0xB0000, None), gdn.GDN_ERR_INVALID_ARG),
+    ((0xA0000, 4, 16, 0, None, None), gdn.GDN_ERR_INVALID_ARG),
+    ((0xA0002, 4, 16, 0, 0xB0000, None), gdn.GDN_ERR_MISALIGNED),
+    ((0xA0000, 4, 16, 0, 0xB0001, None), gdn.GDN_ERR_MISALIGNED),
+    ((0xA0000, 0, 16, 0, None, None), gdn.GDN_OK),
+])
+def test_commit_index_host_checks(lib, args, want):
+    acc, B, N, base, slot, status = args
+    P = ctypes.c_void_p
+    lib.gdn_commit_index.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P, P]
+    assert lib.gdn_commit_index(acc, B, N, base, slot, status, None) == want
 
 
 def _commit(lib, **kw):

@@ -33,6 +33,8 @@ MUTANTS = {
                             "1.0 + 0 * alpha[(int64_t)t * Hv + h],\n"),
     "replay_drops_root": ("for (int m = acc; m >= 0; m = par[m]) path.insert",
                           "for (int m = acc; m > 0; m = par[m]) path.insert"),
+    "index_commit_wrong_stride": ("slot[b] = base + b * N + accept[b];",
+                                  "slot[b] = base + b * (N - 1) + accept[b];"),
     "replay_chain_short": ("for (int m = 0; m <= acc; ++m) path.push_back(m);",
                            "for (int m = 0; m < acc; ++m) path.push_back(m);"),
 }
