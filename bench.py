@@ -53,12 +53,12 @@ METRIC = "GDN verify node-heads/s per layer at block 16 / tree 22; % of GB300 HB
 
 
 # ------------------------------------------------------------------ workloads
-def verify_bytes(B, N, Hk, Hv, dk, dv, in_bytes=2, tree=False, persist=True):
+def verify_bytes(B, N, Hk, Hv, dk, dv, in_bytes=2, tree=False, persist=True, snap_bytes=4):
     """Algorithmic HBM bytes of one verify call: every input read once, the
     initial state read once, every output (o and, when persisted, all N
     snapshots) written once."""
     state_in = B * Hv * dk * dv * 4
-    snap = B * N * Hv * dk * dv * 4 if persist else 0
+    snap = B * N * Hv * dk * dv * snap_bytes if persist else 0
     qk = 2 * B * N * Hk * dk * in_bytes
     v = B * N * Hv * dv * in_bytes
     gates = 2 * B * N * Hv * 4
@@ -114,6 +114,12 @@ WORKLOADS = {
                               desc="batched8x16 committed through the index table: 48 verifies "
                                    "on per-layer snapshot regions, one slot table for all "
                                    "layers"),
+    "chain16_f16": dict(B=1, N=16, tree=False, layers=1, snap16=True,
+                        desc="chain16 persisting binary16 snapshots (gdn_verify_chain_f16) "
+                             "and committing by widening (gdn_commit_accepted_f16)"),
+    "batched8x16_f16": dict(B=8, N=16, tree=False, layers=48, snap16=True,
+                            desc="batched8x16 persisting binary16 snapshots, 48-layer "
+                                 "widening commit"),
     "prefill8192": dict(T=8192, layers=1,
                         desc="1 sequence of 8192 tokens, 16 q/k heads, 48 value heads, "
                              "d_k=d_v=128, bf16 q/k/v, chunk 64, WY/UT form on tensor cores"),
@@ -343,8 +349,9 @@ class VerifyCase:
 
     NAMES = ("q", "k", "v", "alpha", "beta", "accept")
 
-    def __init__(self, inp, torch, pinned=False, persist=True):
+    def __init__(self, inp, torch, pinned=False, persist=True, snap16=False):
         self.inp = inp
+        self.snap16 = snap16
         self.B, self.N, self.Hv = inp["B"], inp["N"], inp["Hv"]
         dk, dv = inp["dk"], inp["dv"]
         arrays = {n: np.ascontiguousarray(inp[n]) for n in self.NAMES}
@@ -366,8 +373,9 @@ class VerifyCase:
         self.cache = _dev(inp["cache"], torch)
         self.slot = _dev(inp["slot"], torch)
         self.parent = _dev(inp["parent"], torch) if inp["tree"] else None
-        self.snap = (torch.empty((self.B, self.N, self.Hv, dk, dv), device="cuda") if persist
-                     else None)
+        self.snap = (torch.empty((self.B, self.N, self.Hv, dk, dv), device="cuda",
+                                 dtype=torch.float16 if snap16 else torch.float32)
+                     if persist else None)
         self.o = torch.empty((self.B, self.N, self.Hv, dv), device="cuda")
         self.host = None
         if pinned:
@@ -377,7 +385,9 @@ class VerifyCase:
     def verify(self, gdn):
         d = self.dev
         args = (d["q"], d["k"], d["v"], d["alpha"], d["beta"], self.cache, self.snap, self.o)
-        if self.parent is not None:
+        if self.snap16:
+            gdn.gdn_verify_chain_f16(*args, slot=self.slot, n_slots=self.inp["n_slots"])
+        elif self.parent is not None:
             gdn.gdn_verify_tree(*args, self.parent, slot=self.slot, n_slots=self.inp["n_slots"])
         else:
             gdn.gdn_verify_chain(*args, slot=self.slot, n_slots=self.inp["n_slots"])
@@ -425,10 +435,13 @@ def run_ours(args, wl_name, world, rank, local):
             inp = synthetic.batched8x16_layer(l)
             if rank:
                 inp = dict(inp)  # replicas share shapes; the data is the same recipe
-            layers.append(VerifyCase(inp, torch, pinned=True, persist=not replay))
+            layers.append(VerifyCase(inp, torch, pinned=True, persist=not replay,
+                                     snap16=wl.get("snap16", False)))
         # one cache for all layers: [layer][slot][Hv][dk][dv]; snapshots likewise
         cache_all = torch.stack([c.cache for c in layers])
-        snap_all = None if replay else torch.empty((L, B, N, Hv, dk, dv), device="cuda")
+        snap_all = None if replay else torch.empty(
+            (L, B, N, Hv, dk, dv), device="cuda",
+            dtype=torch.float16 if wl.get("snap16") else torch.float32)
         for l, c in enumerate(layers):
             c.cache = cache_all[l]
             if not replay:
@@ -436,7 +449,8 @@ def run_ours(args, wl_name, world, rank, local):
         commit_layers = L
     else:
         inp = synthetic.tree22() if wl.get("tree") else synthetic.chain16()
-        layers = [VerifyCase(inp, torch, pinned=True, persist=not replay)]
+        layers = [VerifyCase(inp, torch, pinned=True, persist=not replay,
+                             snap16=wl.get("snap16", False))]
         cache_all = layers[0].cache
         snap_all = layers[0].snap
         commit_layers = 1
@@ -531,7 +545,8 @@ def run_ours(args, wl_name, world, rank, local):
     node_heads = B * N * Hv * len(layers)
     value = job_throughput(node_heads, args.steps, total_ms, world)
     hbm, bf16, peak_kind = measured_peaks()
-    vbytes = verify_bytes(B, N, Hk, Hv, dk, dv, tree=wl.get("tree", False), persist=not replay)
+    vbytes = verify_bytes(B, N, Hk, Hv, dk, dv, tree=wl.get("tree", False), persist=not replay,
+                          snap_bytes=2 if wl.get("snap16") else 4)
     launch_ms = statistics.mean(verify_ms) / len(layers)
     achieved = vbytes / (launch_ms / 1e3) / 1e9
     clocks = sampler.summary(t0, t1)
@@ -566,6 +581,7 @@ def run_ours(args, wl_name, world, rank, local):
             "bound": "hbm",
             "kernel": ("gdn_verify_tree" if wl.get("tree") else "gdn_verify_chain") +
                       (" (no snapshots)" if replay else
+                       " (binary16 snapshots)" if wl.get("snap16") else
                        " (state and snapshots in the slot region)" if index else ""),
             "achieved": achieved,
             "peak": hbm,

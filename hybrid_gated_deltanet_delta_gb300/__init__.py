@@ -7,7 +7,8 @@ in the library's CUDA kernels; there is no CPU or PyTorch fallback, and the
 functions raise if the library is missing or a call fails.
 
 Entry points (same names as the C ABI):
-  gdn_verify_chain, gdn_verify_tree, gdn_commit_accepted, gdn_commit_index,
+  gdn_verify_chain, gdn_verify_chain_f16, gdn_verify_tree, gdn_commit_accepted,
+  gdn_commit_accepted_f16, gdn_commit_index,
   gdn_replay_accepted,
   gdn_prefill_chunked, gdn_prefill_workspace_bytes, gdn_prefill_chunked_noalloc
 """
@@ -76,6 +77,11 @@ def load(path: str | None = None):
     lib.gdn_commit_accepted.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32,
                                         i32, P, P]
     lib.gdn_commit_accepted.restype = ctypes.c_int
+    lib.gdn_verify_chain_f16.argtypes = [ctypes.POINTER(VerifyArgs), P, P]
+    lib.gdn_verify_chain_f16.restype = ctypes.c_int
+    lib.gdn_commit_accepted_f16.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32,
+                                            i32, i32, P, P]
+    lib.gdn_commit_accepted_f16.restype = ctypes.c_int
     lib.gdn_commit_index.argtypes = [P, i32, i32, i32, P, P, P]
     lib.gdn_commit_index.restype = ctypes.c_int
     lib.gdn_replay_accepted.argtypes = [ctypes.POINTER(VerifyArgs), P, P, P]
@@ -175,6 +181,22 @@ def gdn_verify_chain(q, k, v, alpha, beta, state_cache, snapshots, o, *, slot=No
     _check(load().gdn_verify_chain(ctypes.byref(a), _stream(stream)), "gdn_verify_chain")
 
 
+def gdn_verify_chain_f16(q, k, v, alpha, beta, state_cache, snapshots_f16, o, *, slot=None,
+                         n_slots=None, status=None, cache_slot_stride=None, tile_cols=0,
+                         row_warps=0, stream=None):
+    """Chain verification persisting every node's state as float16 (RNE) in
+    snapshots_f16 [B,N,Hv,dk,dv]; outputs unchanged (see include/gdn.h)."""
+    import torch
+
+    _need(snapshots_f16.dtype == torch.float16 and snapshots_f16.is_contiguous(),
+          "snapshots_f16 must be a contiguous float16 tensor")
+    a = make_verify_args(q, k, v, alpha, beta, state_cache, None, o, slot=slot,
+                         n_slots=n_slots, status=status, cache_slot_stride=cache_slot_stride,
+                         tile_cols=tile_cols, row_warps=row_warps)
+    _check(load().gdn_verify_chain_f16(ctypes.byref(a), _ptr(snapshots_f16), _stream(stream)),
+           "gdn_verify_chain_f16")
+
+
 def gdn_verify_tree(q, k, v, alpha, beta, state_cache, snapshots, o, parent, *, depth_out=None,
                     slot=None, n_slots=None, status=None, cache_slot_stride=None, tile_cols=0,
                     row_warps=0, stream=None):
@@ -191,15 +213,27 @@ def gdn_verify_tree(q, k, v, alpha, beta, state_cache, snapshots, o, parent, *, 
 def gdn_commit_accepted(snapshots, accept_idx, state_cache, *, B, N, Hv, dk, dv, n_layers=1,
                         snap_layer_stride=0, cache_slot_stride=None, cache_layer_stride=0,
                         slot=None, n_slots=None, status=None, stream=None):
-    """state_cache[l][slot[b]][h] = snapshots[l][b][accept_idx[b]][h] for every layer."""
+    """state_cache[l][slot[b]][h] = snapshots[l][b][accept_idx[b]][h] for every layer
+    (fp32 snapshots; float16 ones go through gdn_commit_accepted_f16)."""
     if cache_slot_stride is None:
         cache_slot_stride = Hv * dk * dv
     if n_slots is None:
         n_slots = (state_cache.numel() - (n_layers - 1) * cache_layer_stride) // cache_slot_stride
-    _check(load().gdn_commit_accepted(_ptr(snapshots), snap_layer_stride, _ptr(accept_idx),
-                                      _ptr(state_cache), cache_slot_stride, cache_layer_stride,
-                                      _ptr(slot), n_slots, B, N, Hv, dk, dv, n_layers,
-                                      _ptr(status), _stream(stream)), "gdn_commit_accepted")
+    fn = load().gdn_commit_accepted
+    name = "gdn_commit_accepted"
+    if snapshots.dtype != state_cache.dtype:
+        fn, name = load().gdn_commit_accepted_f16, "gdn_commit_accepted_f16"
+    _check(fn(_ptr(snapshots), snap_layer_stride, _ptr(accept_idx), _ptr(state_cache),
+              cache_slot_stride, cache_layer_stride, _ptr(slot), n_slots, B, N, Hv, dk, dv,
+              n_layers, _ptr(status), _stream(stream)), name)
+
+
+def gdn_commit_accepted_f16(snapshots_f16, accept_idx, state_cache, **kw):
+    """gdn_commit_accepted from float16 snapshots, widened into the fp32 cache."""
+    import torch
+
+    _need(snapshots_f16.dtype == torch.float16, "snapshots_f16 must be float16")
+    gdn_commit_accepted(snapshots_f16, accept_idx, state_cache, **kw)
 
 
 def gdn_commit_index(accept_idx, slot, *, N, base_slot=0, status=None, stream=None):

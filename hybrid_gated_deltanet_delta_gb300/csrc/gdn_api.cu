@@ -23,7 +23,7 @@ void auto_tile(int dk, int dv, int B, int Hv, int* wc, int* nw) {
 }
 
 int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, bool tree,
-                  void* stream) {
+                  void* stream, void* snap16 = nullptr) {
   if (a == nullptr) return GDN_ERR_INVALID_ARG;
   if (a->B < 0 || a->N < 1 || a->Hk < 1 || a->Hv < 1 || a->Hv % a->Hk != 0)
     return GDN_ERR_INVALID_ARG;
@@ -44,7 +44,9 @@ int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   // a chain may skip persistence (commit by replay); a tree re-reads persisted
   // states when its stash pool runs out, so it needs them
   if (a->snapshots == nullptr && tree) return GDN_ERR_INVALID_ARG;
-  if (a->snapshots != nullptr && !gdn::aligned16(a->snapshots)) return GDN_ERR_MISALIGNED;
+  if (snap16 == nullptr && a->snapshots != nullptr && !gdn::aligned16(a->snapshots))
+    return GDN_ERR_MISALIGNED;
+  if (snap16 != nullptr && !gdn::aligned16(snap16)) return GDN_ERR_MISALIGNED;
   if (a->alpha == nullptr || a->beta == nullptr) return GDN_ERR_INVALID_ARG;
   if (tree && parent == nullptr) return GDN_ERR_INVALID_ARG;
   const void* need4[] = {a->alpha, a->beta, a->slot, a->status, parent, depth_out};
@@ -57,7 +59,31 @@ int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   if (a->row_warps != 0) nw = a->row_warps;
   if (!gdn::verify_tile_supported(a->dk, wc, nw) || a->dv % wc != 0) return GDN_ERR_UNSUPPORTED;
   return gdn::launch_verify(a, tree ? parent : nullptr, tree ? depth_out : nullptr, wc, nw,
-                            static_cast<cudaStream_t>(stream));
+                            static_cast<cudaStream_t>(stream), snap16);
+}
+
+int commit_common(const void* snapshots, bool src16, int64_t snap_layer_stride,
+                  const int32_t* accept_idx, float* state_cache, int64_t cache_slot_stride,
+                  int64_t cache_layer_stride, const int32_t* slot, int32_t n_slots, int32_t B,
+                  int32_t N, int32_t Hv, int32_t dk, int32_t dv, int32_t n_layers,
+                  int32_t* status, void* stream) {
+  if (B < 0 || n_layers < 0 || N < 1 || Hv < 1 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
+  if (snap_layer_stride < 0 || cache_slot_stride < 0 || cache_layer_stride < 0)
+    return GDN_ERR_INVALID_ARG;
+  if (B > 65535 || n_layers > 65535) return GDN_ERR_UNSUPPORTED;
+  if (B == 0 || n_layers == 0) return GDN_OK;
+  const int64_t head_set = (int64_t)Hv * dk * dv;
+  if (n_slots < 1 || cache_slot_stride < head_set) return GDN_ERR_INVALID_ARG;
+  if (head_set % 4 != 0 || snap_layer_stride % 4 != 0 || cache_slot_stride % 4 != 0 ||
+      cache_layer_stride % 4 != 0)
+    return GDN_ERR_MISALIGNED;
+  if (snapshots == nullptr || accept_idx == nullptr || state_cache == nullptr)
+    return GDN_ERR_INVALID_ARG;
+  if (!ok_ptr16(snapshots) || !ok_ptr16(state_cache)) return GDN_ERR_MISALIGNED;
+  if (!ok_ptr4(accept_idx) || !ok_ptr4(slot) || !ok_ptr4(status)) return GDN_ERR_MISALIGNED;
+  return gdn::launch_commit(snapshots, src16, snap_layer_stride, accept_idx, state_cache,
+                            cache_slot_stride, cache_layer_stride, slot, n_slots, B, N, Hv, dk,
+                            dv, n_layers, status, static_cast<cudaStream_t>(stream));
 }
 
 int replay_common(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept,
@@ -109,28 +135,30 @@ int gdn_verify_tree(const gdn_verify_args* args, const int32_t* parent, int32_t*
   return verify_common(args, parent, depth_out, true, stream);
 }
 
+int gdn_verify_chain_f16(const gdn_verify_args* args, void* snapshots_f16, void* stream) {
+  if (snapshots_f16 == nullptr) return GDN_ERR_INVALID_ARG;
+  return verify_common(args, nullptr, nullptr, false, stream, snapshots_f16);
+}
+
 int gdn_commit_accepted(const float* snapshots, int64_t snap_layer_stride,
                         const int32_t* accept_idx, float* state_cache, int64_t cache_slot_stride,
                         int64_t cache_layer_stride, const int32_t* slot, int32_t n_slots,
                         int32_t B, int32_t N, int32_t Hv, int32_t dk, int32_t dv,
                         int32_t n_layers, int32_t* status, void* stream) {
-  if (B < 0 || n_layers < 0 || N < 1 || Hv < 1 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
-  if (snap_layer_stride < 0 || cache_slot_stride < 0 || cache_layer_stride < 0)
-    return GDN_ERR_INVALID_ARG;
-  if (B > 65535 || n_layers > 65535) return GDN_ERR_UNSUPPORTED;
-  if (B == 0 || n_layers == 0) return GDN_OK;
-  const int64_t head_set = (int64_t)Hv * dk * dv;
-  if (n_slots < 1 || cache_slot_stride < head_set) return GDN_ERR_INVALID_ARG;
-  if (head_set % 4 != 0 || snap_layer_stride % 4 != 0 || cache_slot_stride % 4 != 0 ||
-      cache_layer_stride % 4 != 0)
-    return GDN_ERR_MISALIGNED;
-  if (snapshots == nullptr || accept_idx == nullptr || state_cache == nullptr)
-    return GDN_ERR_INVALID_ARG;
-  if (!ok_ptr16(snapshots) || !ok_ptr16(state_cache)) return GDN_ERR_MISALIGNED;
-  if (!ok_ptr4(accept_idx) || !ok_ptr4(slot) || !ok_ptr4(status)) return GDN_ERR_MISALIGNED;
-  return gdn::launch_commit(snapshots, snap_layer_stride, accept_idx, state_cache,
-                            cache_slot_stride, cache_layer_stride, slot, n_slots, B, N, Hv, dk,
-                            dv, n_layers, status, static_cast<cudaStream_t>(stream));
+  return commit_common(snapshots, false, snap_layer_stride, accept_idx, state_cache,
+                       cache_slot_stride, cache_layer_stride, slot, n_slots, B, N, Hv, dk, dv,
+                       n_layers, status, stream);
+}
+
+int gdn_commit_accepted_f16(const void* snapshots_f16, int64_t snap_layer_stride,
+                            const int32_t* accept_idx, float* state_cache,
+                            int64_t cache_slot_stride, int64_t cache_layer_stride,
+                            const int32_t* slot, int32_t n_slots, int32_t B, int32_t N,
+                            int32_t Hv, int32_t dk, int32_t dv, int32_t n_layers,
+                            int32_t* status, void* stream) {
+  return commit_common(snapshots_f16, true, snap_layer_stride, accept_idx, state_cache,
+                       cache_slot_stride, cache_layer_stride, slot, n_slots, B, N, Hv, dk, dv,
+                       n_layers, status, stream);
 }
 
 int gdn_commit_index(const int32_t* accept_idx, int32_t B, int32_t N, int32_t base_slot,

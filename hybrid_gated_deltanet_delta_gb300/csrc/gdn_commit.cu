@@ -10,6 +10,8 @@
 // grid = (pieces of the run, B, n_layers); each thread issues all its loads
 // before its stores.  The snapshots are read with an evict-first hint since
 // nothing reads them again.
+#include <cuda_fp16.h>
+
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
 
@@ -19,8 +21,23 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
+// Four consecutive snapshot elements as fp32: a float4, or four binary16
+// values (8 bytes) widened exactly.
+template <bool SRC16>
+__device__ __forceinline__ float4 load4(const void* base, int64_t i) {
+  if constexpr (SRC16) {
+    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(base) + i);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  } else {
+    return __ldcs(reinterpret_cast<const float4*>(base) + i);
+  }
+}
+
+template <bool SRC16>
 __global__ void __launch_bounds__(kThreads)
-commit_kernel(const float4* __restrict__ snap, int64_t snap_layer4, const int32_t* accept,
+commit_kernel(const void* __restrict__ snap, int64_t snap_layer4, const int32_t* accept,
               float4* __restrict__ cache, int64_t slot4, int64_t layer4, const int32_t* slot,
               int n_slots, int N, int64_t run4, int32_t* status) {
   const int b = blockIdx.y, l = blockIdx.z;
@@ -31,14 +48,14 @@ commit_kernel(const float4* __restrict__ snap, int64_t snap_layer4, const int32_
       report(status, (a < 0 || a >= N) ? GDN_ERR_ACCEPT_RANGE : GDN_ERR_SLOT_RANGE);
     return;
   }
-  const float4* src = snap + l * snap_layer4 + ((int64_t)b * N + a) * run4;
+  const int64_t src = l * snap_layer4 + ((int64_t)b * N + a) * run4;  // in groups of 4
   float4* dst = cache + l * layer4 + (int64_t)s * slot4;
   const int64_t base = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x;
   float4 t[kUnroll];
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
     const int64_t i = base + (int64_t)u * kThreads;
-    if (i < run4) t[u] = __ldcs(src + i);
+    if (i < run4) t[u] = load4<SRC16>(snap, src + i);
   }
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
@@ -73,7 +90,7 @@ int launch_commit_index(const int32_t* accept, int B, int N, int base_slot, int3
   return launch_status();
 }
 
-int launch_commit(const float* snap, int64_t snap_layer_stride, const int32_t* accept,
+int launch_commit(const void* snap, bool src16, int64_t snap_layer_stride, const int32_t* accept,
                   float* cache, int64_t cache_slot_stride, int64_t cache_layer_stride,
                   const int32_t* slot, int n_slots, int B, int N, int Hv, int dk, int dv,
                   int n_layers, int32_t* status, cudaStream_t stream) {
@@ -82,10 +99,14 @@ int launch_commit(const float* snap, int64_t snap_layer_stride, const int32_t* a
   const int64_t gx = (run4 + per_block - 1) / per_block;
   if (gx > 0x7fffffff) return GDN_ERR_UNSUPPORTED;
   const dim3 grid((unsigned)gx, B, n_layers);
-  commit_kernel<<<grid, kThreads, 0, stream>>>(
-      reinterpret_cast<const float4*>(snap), snap_layer_stride / 4, accept,
-      reinterpret_cast<float4*>(cache), cache_slot_stride / 4, cache_layer_stride / 4, slot,
-      n_slots, N, run4, status);
+  if (src16)
+    commit_kernel<true><<<grid, kThreads, 0, stream>>>(
+        snap, snap_layer_stride / 4, accept, reinterpret_cast<float4*>(cache),
+        cache_slot_stride / 4, cache_layer_stride / 4, slot, n_slots, N, run4, status);
+  else
+    commit_kernel<false><<<grid, kThreads, 0, stream>>>(
+        snap, snap_layer_stride / 4, accept, reinterpret_cast<float4*>(cache),
+        cache_slot_stride / 4, cache_layer_stride / 4, slot, n_slots, N, run4, status);
   return launch_status();
 }
 

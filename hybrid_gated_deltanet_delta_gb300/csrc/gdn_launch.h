@@ -11,14 +11,16 @@
 namespace gdn {
 
 bool verify_tile_supported(int dk, int wc, int nw);
+// snap16 != NULL: chain with binary16 snapshots there (a->snapshots unused).
 int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, int wc,
-                  int nw, cudaStream_t stream);
+                  int nw, cudaStream_t stream, void* snap16 = nullptr);
 
 // Replay of the accepted path from the cached state, written back in place.
 int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept, int wc,
                   cudaStream_t stream);
 
-int launch_commit(const float* snap, int64_t snap_layer_stride, const int32_t* accept,
+// src16: the snapshots are binary16 (widened exactly into the fp32 cache).
+int launch_commit(const void* snap, bool src16, int64_t snap_layer_stride, const int32_t* accept,
                   float* cache, int64_t cache_slot_stride, int64_t cache_layer_stride,
                   const int32_t* slot, int n_slots, int B, int N, int Hv, int dk, int dv,
                   int n_layers, int32_t* status, cudaStream_t stream);

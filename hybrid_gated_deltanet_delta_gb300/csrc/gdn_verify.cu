@@ -41,6 +41,8 @@
 // q, k, v, the gates and the parents are staged with cp.async while the
 // cached state loads.  Snapshots leave as 16-byte stores; a warp-wide store
 // covers RL rows x WC*4 contiguous bytes.
+#include <cuda_fp16.h>
+
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
 
@@ -102,6 +104,7 @@ struct VerifyParams {
   const float* cache;
   const int32_t* slot;
   float* snap;
+  __half* snap16;  // binary16 snapshots instead of snap (chain only)
   float* o;
   int32_t* status;
   const int32_t* parent;
@@ -158,7 +161,7 @@ __device__ __forceinline__ void load_rows(float (&x)[R], const char* row, int fi
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
-template <int DK, int WC, bool TREE>
+template <int DK, int WC, bool TREE, bool SNAP16>
 __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
   using S = Shape<DK, WC>;
   constexpr int R = S::R;
@@ -306,9 +309,9 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
   }
 
   const int64_t node_stride = (int64_t)p.Hv * DK * dv;
-  float* snap_h = p.snap == nullptr ? nullptr
-                                    : p.snap + ((int64_t)b * N * p.Hv + h) * DK * dv +
-                                          (int64_t)row0 * dv + j0 + cg * 4;
+  const int64_t lane_off = ((int64_t)b * N * p.Hv + h) * DK * dv + (int64_t)row0 * dv + j0 + cg * 4;
+  float* snap_h = p.snap == nullptr ? nullptr : p.snap + lane_off;
+  __half* snap16_h = SNAP16 ? p.snap16 + lane_off : nullptr;
   float* o_h = p.o + ((int64_t)b * N * p.Hv + h) * dv + j0 + cg * 4;
   // a stash slot holds each lane's R x 4 block lane-major: row m of lane l at
   // float offset (m*32 + l)*4, so every slot access is bank-conflict free
@@ -416,7 +419,18 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
 
     // (f) persist (a chain verified for a replay commit keeps no snapshots)
     if (rl == 0) st_f4(o_h + (int64_t)n * p.Hv * dv, red[5], red[6], red[7], red[8]);
-    if (p.snap != nullptr) {
+    if constexpr (SNAP16) {
+      // binary16, round to nearest even: 8 bytes per lane and row
+      __half* dst = snap16_h + (int64_t)n * node_stride;
+#pragma unroll
+      for (int m = 0; m < R; ++m) {
+        const __half2 lo = __floats2half2_rn(H[m][0].x, H[m][0].y);
+        const __half2 hi = __floats2half2_rn(H[m][1].x, H[m][1].y);
+        *reinterpret_cast<uint2*>(dst + (int64_t)m * dv) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                       *reinterpret_cast<const uint32_t*>(&hi));
+      }
+    } else if (p.snap != nullptr) {
       float* dst = snap_h + (int64_t)n * node_stride;
 #pragma unroll
       for (int m = 0; m < R; ++m)
@@ -641,14 +655,14 @@ int launch_replay_t(const ReplayParams& p, int B, cudaStream_t stream) {
   return launch_status();
 }
 
-template <int DK, int WC, bool TREE>
+template <int DK, int WC, bool TREE, bool SNAP16>
 int launch(const VerifyParams& p, int B, cudaStream_t stream) {
   VerifyParams q = p;
   q.pool = TREE ? tree_pool_slots(p.N, DK, WC, p.bf16 ? 2 : 4) : 0;
   const SmemPlan pl = smem_plan(p.N, DK, WC, p.bf16 ? 2 : 4, TREE, q.pool);
   const size_t smem = (size_t)pl.total;
   if (smem > 227 * 1024) return GDN_ERR_UNSUPPORTED;
-  auto kern = verify_kernel<DK, WC, TREE>;
+  auto kern = verify_kernel<DK, WC, TREE, SNAP16>;
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -659,10 +673,10 @@ int launch(const VerifyParams& p, int B, cudaStream_t stream) {
   return launch_status();
 }
 
-template <bool TREE>
+template <bool TREE, bool SNAP16>
 int dispatch(const VerifyParams& p, int B, int dk, int wc, cudaStream_t s) {
 #define GDN_CASE(DK_, WC_) \
-  if (dk == DK_ && wc == WC_) return launch<DK_, WC_, TREE>(p, B, s);
+  if (dk == DK_ && wc == WC_) return launch<DK_, WC_, TREE, SNAP16>(p, B, s);
   GDN_CASE(128, 16)
   GDN_CASE(128, 8)
   GDN_CASE(64, 16)
@@ -682,7 +696,7 @@ bool verify_tile_supported(int dk, int wc, int nw) {
 }
 
 int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, int wc,
-                  int nw, cudaStream_t stream) {
+                  int nw, cudaStream_t stream, void* snap16) {
   (void)nw;
   VerifyParams p{};
   p.q = a->q;
@@ -704,8 +718,10 @@ int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   p.Hv = a->Hv;
   p.dv = a->dv;
   p.bf16 = a->in_dtype == GDN_BF16;
-  if (parent != nullptr) return dispatch<true>(p, a->B, a->dk, wc, stream);
-  return dispatch<false>(p, a->B, a->dk, wc, stream);
+  p.snap16 = static_cast<__half*>(snap16);
+  if (parent != nullptr) return dispatch<true, false>(p, a->B, a->dk, wc, stream);
+  if (snap16 != nullptr) return dispatch<false, true>(p, a->B, a->dk, wc, stream);
+  return dispatch<false, false>(p, a->B, a->dk, wc, stream);
 }
 
 int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept, int wc,

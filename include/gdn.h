@@ -158,6 +158,31 @@ int gdn_commit_accepted(const float* snapshots, int64_t snap_layer_stride,
                         int32_t n_layers, int32_t* status, void* stream);
 
 /*
+ * Chain verification with 16-bit persisted states ("We got 207 tok/s with
+ * Qwen3.5-27B on an RTX 3090", list "Key wins": an f16 intermediate cache at
+ * half the bandwidth).  The same as gdn_verify_chain, except that every
+ * node's state is written to `snapshots_f16` [B][N][Hv][dk][dv] as IEEE
+ * binary16, rounded to nearest even from the fp32 state the recurrence keeps
+ * (args->snapshots is not used).  The recurrence itself and the outputs o
+ * are unchanged; only the persisted copies are rounded.  Chains only (a tree
+ * re-reads persisted parents, which would then continue from rounded states).
+ */
+int gdn_verify_chain_f16(const gdn_verify_args* args, void* snapshots_f16, void* stream);
+
+/*
+ * gdn_commit_accepted for binary16 snapshots: the accepted node's state is
+ * widened exactly to fp32 into the cache (so the committed state carries one
+ * binary16 rounding per block).  Strides are in elements; same checks and
+ * status reporting as gdn_commit_accepted.
+ */
+int gdn_commit_accepted_f16(const void* snapshots_f16, int64_t snap_layer_stride,
+                            const int32_t* accept_idx, float* state_cache,
+                            int64_t cache_slot_stride, int64_t cache_layer_stride,
+                            const int32_t* slot, int32_t n_slots, int32_t B, int32_t N,
+                            int32_t Hv, int32_t dk, int32_t dv, int32_t n_layers,
+                            int32_t* status, void* stream);
+
+/*
  * Index-table commit ("TokenSpeed hits 580 tok/s", section "How they actually
  * got there": move pointers, not data -- the persisted states form a draft
  * region and a small index table says which one is current).  No state is

@@ -160,6 +160,24 @@ def test_commit_index_host_checks(lib, args, want):
     assert lib.gdn_commit_index(acc, B, N, base, slot, status, None) == want
 
 
+def test_f16_entry_points_host_checks(lib):
+    """The binary16 variants check their own pointers (calls that never launch)."""
+    a = _args()
+    assert lib.gdn_verify_chain_f16(ctypes.byref(a), None, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_verify_chain_f16(ctypes.byref(a), ctypes.c_void_p(0x70008), None) == \
+        gdn.GDN_ERR_MISALIGNED
+    a = _args(q=0)
+    assert lib.gdn_verify_chain_f16(ctypes.byref(a), ctypes.c_void_p(0x70000), None) == \
+        gdn.GDN_ERR_INVALID_ARG
+    f = lib.gdn_commit_accepted_f16
+    assert f(None, 0, 0x20000, 0x30000, 48 * 128 * 128, 0, None, 1, 1, 16, 48, 128, 128, 1,
+             None, None) == gdn.GDN_ERR_INVALID_ARG
+    assert f(0x10008, 0, 0x20000, 0x30000, 48 * 128 * 128, 0, None, 1, 1, 16, 48, 128, 128, 1,
+             None, None) == gdn.GDN_ERR_MISALIGNED
+    assert f(0x10000, 0, 0x20000, 0x30000, 48 * 128 * 128, 0, None, 1, 0, 16, 48, 128, 128, 1,
+             None, None) == gdn.GDN_OK
+
+
 def _commit(lib, **kw):
     base = dict(snap=0x10000, sls=0, acc=0x20000, cache=0x30000, css=48 * 128 * 128, cls=0,
                 slot=None, n_slots=1, B=1, N=16, Hv=48, dk=128, dv=128, L=1, status=None)
