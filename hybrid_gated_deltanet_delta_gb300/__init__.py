@@ -8,7 +8,7 @@ functions raise if the library is missing or a call fails.
 
 Entry points (same names as the C ABI):
   gdn_verify_chain, gdn_verify_chain_f16, gdn_verify_tree, gdn_commit_accepted,
-  gdn_commit_accepted_f16, gdn_commit_index,
+  gdn_commit_accepted_f16, gdn_commit_index, gdn_conv_commit,
   gdn_replay_accepted,
   gdn_prefill_chunked, gdn_prefill_workspace_bytes, gdn_prefill_chunked_noalloc
 """
@@ -82,6 +82,8 @@ def load(path: str | None = None):
     lib.gdn_commit_accepted_f16.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32,
                                             i32, i32, P, P]
     lib.gdn_commit_accepted_f16.restype = ctypes.c_int
+    lib.gdn_conv_commit.argtypes = [P, i32, P, i64, P, i32, P, P, i32, i32, i32, i32, P, P]
+    lib.gdn_conv_commit.restype = ctypes.c_int
     lib.gdn_commit_index.argtypes = [P, i32, i32, i32, P, P, P]
     lib.gdn_commit_index.restype = ctypes.c_int
     lib.gdn_replay_accepted.argtypes = [ctypes.POINTER(VerifyArgs), P, P, P]
@@ -234,6 +236,24 @@ def gdn_commit_accepted_f16(snapshots_f16, accept_idx, state_cache, **kw):
 
     _need(snapshots_f16.dtype == torch.float16, "snapshots_f16 must be float16")
     gdn_commit_accepted(snapshots_f16, accept_idx, state_cache, **kw)
+
+
+def gdn_conv_commit(x, conv_state, accept_idx, *, parent=None, slot=None, n_slots=None,
+                    state_slot_stride=None, status=None, stream=None):
+    """Convolution-history commit in place: x [B,N,C] raw inputs of the block
+    (bfloat16 or float32), conv_state [n_slots,C,W] of the same dtype; the
+    history becomes the last W elements of [history, x of the accepted path]."""
+    B, N, C = x.shape
+    W = conv_state.shape[-1]
+    _need(x.is_contiguous() and conv_state.is_contiguous(), "tensors must be contiguous")
+    _need(x.dtype == conv_state.dtype, "x and conv_state must share a dtype")
+    if state_slot_stride is None:
+        state_slot_stride = C * W
+    if n_slots is None:
+        n_slots = conv_state.numel() // state_slot_stride
+    _check(load().gdn_conv_commit(_ptr(x), _dtype_code(x), _ptr(conv_state), state_slot_stride,
+                                  _ptr(slot), n_slots, _ptr(parent), _ptr(accept_idx), B, N, C,
+                                  W, _ptr(status), _stream(stream)), "gdn_conv_commit")
 
 
 def gdn_commit_index(accept_idx, slot, *, N, base_slot=0, status=None, stream=None):

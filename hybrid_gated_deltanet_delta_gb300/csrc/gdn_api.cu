@@ -161,6 +161,26 @@ int gdn_commit_accepted_f16(const void* snapshots_f16, int64_t snap_layer_stride
                        n_layers, status, stream);
 }
 
+int gdn_conv_commit(const void* x, int32_t in_dtype, void* conv_state,
+                    int64_t state_slot_stride, const int32_t* slot, int32_t n_slots,
+                    const int32_t* parent, const int32_t* accept_idx, int32_t B, int32_t N,
+                    int32_t C, int32_t W, int32_t* status, void* stream) {
+  if (in_dtype != GDN_F32 && in_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (B < 0 || N < 1 || C < 1 || W < 1 || n_slots < 1) return GDN_ERR_INVALID_ARG;
+  if (W > 8 || B > 65535) return GDN_ERR_UNSUPPORTED;
+  if (state_slot_stride < (int64_t)C * W) return GDN_ERR_INVALID_ARG;
+  if (B == 0) return GDN_OK;
+  if (x == nullptr || conv_state == nullptr || accept_idx == nullptr) return GDN_ERR_INVALID_ARG;
+  const uintptr_t esz = in_dtype == GDN_BF16 ? 2 : 4;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(conv_state)) % esz != 0)
+    return GDN_ERR_MISALIGNED;
+  if (!ok_ptr4(accept_idx) || !ok_ptr4(slot) || !ok_ptr4(parent) || !ok_ptr4(status))
+    return GDN_ERR_MISALIGNED;
+  return gdn::launch_conv_commit(x, in_dtype == GDN_BF16, conv_state, state_slot_stride, slot,
+                                 n_slots, parent, accept_idx, B, N, C, W, status,
+                                 static_cast<cudaStream_t>(stream));
+}
+
 int gdn_commit_index(const int32_t* accept_idx, int32_t B, int32_t N, int32_t base_slot,
                      int32_t* slot, int32_t* status, void* stream) {
   if (B < 0 || N < 1 || base_slot < 0) return GDN_ERR_INVALID_ARG;

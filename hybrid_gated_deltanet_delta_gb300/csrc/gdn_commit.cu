@@ -79,7 +79,95 @@ __global__ void commit_index_kernel(const int32_t* accept, int B, int N, int bas
   slot[b] = base_slot + b * N + a;
 }
 
+// Convolution-history commit ("Photon 2.6", section "Handling recurrent
+// state": the convolution history is committed to the same boundary as the
+// state).  Block (channel range, sequence b), one thread per channel: the new
+// window is the last W elements of [old history, x of the accepted path],
+// written in place after all old values are read.  Every thread checks the
+// sequence and loads its old window first; a chain's path tail is
+// acc-P+1 .. acc, a tree's is collected by thread 0 walking the parents.  E is
+// the element type moved bit for bit.
+constexpr int kMaxConvW = 8;
+
+template <typename E>
+__global__ void __launch_bounds__(256)
+conv_commit_kernel(const E* __restrict__ x, E* __restrict__ state, int64_t slot_stride,
+                   const int32_t* slot, int n_slots, const int32_t* parent,
+                   const int32_t* accept, int N, int C, int W, int32_t* status) {
+  __shared__ int s_tail[kMaxConvW];
+  __shared__ int s_count;
+  const int b = blockIdx.y;
+  const int64_t node0 = (int64_t)b * N;
+  const int a = __ldg(accept + b);
+  const int sl = slot != nullptr ? __ldg(slot + b) : b;
+  const bool ok = a >= 0 && a < N && sl >= 0 && sl < n_slots;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const bool mine = ok && c < C;
+  E* h = state + (int64_t)(ok ? sl : 0) * slot_stride + (int64_t)c * W;
+  E old[kMaxConvW];
+#pragma unroll
+  for (int w = 0; w < kMaxConvW; ++w)
+    if (mine && w < W) old[w] = h[w];
+  if (!ok) {
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+      report(status, (a < 0 || a >= N) ? GDN_ERR_ACCEPT_RANGE : GDN_ERR_SLOT_RANGE);
+    return;
+  }
+  int P;  // min(path length, W); the path tail, oldest first, in s_tail (tree)
+  if (parent == nullptr) {
+    P = min(a + 1, W);
+  } else {
+    if (threadIdx.x == 0) {
+      int count = 0;
+      bool valid = true;
+      for (int n = 0; n < N && valid; ++n) {
+        const int pp = __ldg(parent + node0 + n);
+        valid = n == 0 ? pp == -1 : (pp >= 0 && pp < n);
+      }
+      if (valid) {
+        int rev[kMaxConvW];
+        for (int m = a; m >= 0 && count < W; m = __ldg(parent + node0 + m)) rev[count++] = m;
+        for (int i = 0; i < count; ++i) s_tail[i] = rev[count - 1 - i];
+      } else if (blockIdx.x == 0) {
+        report(status, GDN_ERR_BAD_TREE);
+      }
+      s_count = valid ? count : -1;
+    }
+    __syncthreads();
+    P = s_count;
+    if (P < 0) return;
+  }
+  if (!mine) return;
+  const int keep = W - P;  // old entries that stay: the newest `keep`
+#pragma unroll
+  for (int w = 0; w < kMaxConvW; ++w) {
+    if (w < keep) {
+      h[w] = old[w + P];
+    } else if (w < W) {
+      const int i = w - keep;  // 0 .. P-1: the path tail, oldest first
+      const int node = parent == nullptr ? a - P + 1 + i : s_tail[i];
+      h[w] = x[(node0 + node) * C + c];
+    }
+  }
+}
+
 }  // namespace
+
+int launch_conv_commit(const void* x, bool bf16, void* state, int64_t slot_stride,
+                       const int32_t* slot, int n_slots, const int32_t* parent,
+                       const int32_t* accept, int B, int N, int C, int W, int32_t* status,
+                       cudaStream_t stream) {
+  const dim3 grid((unsigned)((C + 255) / 256), B);
+  if (bf16)
+    conv_commit_kernel<uint16_t><<<grid, 256, 0, stream>>>(
+        static_cast<const uint16_t*>(x), static_cast<uint16_t*>(state), slot_stride, slot,
+        n_slots, parent, accept, N, C, W, status);
+  else
+    conv_commit_kernel<uint32_t><<<grid, 256, 0, stream>>>(
+        static_cast<const uint32_t*>(x), static_cast<uint32_t*>(state), slot_stride, slot,
+        n_slots, parent, accept, N, C, W, status);
+  return launch_status();
+}
 
 int launch_commit_index(const int32_t* accept, int B, int N, int base_slot, int32_t* slot,
                         int32_t* status, cudaStream_t stream) {

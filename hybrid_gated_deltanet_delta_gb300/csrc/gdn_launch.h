@@ -29,6 +29,12 @@ int launch_commit(const void* snap, bool src16, int64_t snap_layer_stride, const
 int launch_commit_index(const int32_t* accept, int B, int N, int base_slot, int32_t* slot,
                         int32_t* status, cudaStream_t stream);
 
+// Convolution history: the last W elements of [history, x of the accepted path].
+int launch_conv_commit(const void* x, bool bf16, void* state, int64_t slot_stride,
+                       const int32_t* slot, int n_slots, const int32_t* parent,
+                       const int32_t* accept, int B, int N, int C, int W, int32_t* status,
+                       cudaStream_t stream);
+
 size_t prefill_workspace_bytes(int T, int Hk, int Hv, int dk, int dv, int chunk);
 int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const float* alpha,
                    const float* beta, int T, int Hk, int Hv, int dk, int dv, int chunk,

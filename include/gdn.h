@@ -183,6 +183,28 @@ int gdn_commit_accepted_f16(const void* snapshots_f16, int64_t snap_layer_stride
                             int32_t* status, void* stream);
 
 /*
+ * Convolution-history commit ("Photon 2.6", section "Handling recurrent
+ * state": the convolution history is committed to the same boundary as the
+ * recurrent state).  A short causal convolution before the recurrence keeps,
+ * per cache slot and channel, the last W raw inputs (oldest first):
+ *
+ *   conv_state  slot s, channel c at conv_state + s*state_slot_stride + c*W,
+ *               W consecutive elements (in_dtype)
+ *   x           [B][N][C] raw inputs of the block's nodes (in_dtype)
+ *
+ * For every sequence b the history is advanced in place over the accepted
+ * path (chain: nodes 0 .. accept_idx[b], parent == NULL; tree: the ancestors
+ * of accept_idx[b] from the root, parent [B][N] as in gdn_verify_tree): the
+ * new history is the last W elements of [old history, x of the path nodes].
+ * The copy is bit-exact.  1 <= W <= 8.  A bad accept index, slot or parent
+ * array skips that sequence and is reported through `status`.
+ */
+int gdn_conv_commit(const void* x, int32_t in_dtype, void* conv_state,
+                    int64_t state_slot_stride, const int32_t* slot, int32_t n_slots,
+                    const int32_t* parent, const int32_t* accept_idx, int32_t B, int32_t N,
+                    int32_t C, int32_t W, int32_t* status, void* stream);
+
+/*
  * Index-table commit ("TokenSpeed hits 580 tok/s", section "How they actually
  * got there": move pointers, not data -- the persisted states form a draft
  * region and a small index table says which one is current).  No state is

@@ -48,6 +48,8 @@ def bind(lib):
     lib.oracle_commit_f64.restype = ctypes.c_int
     lib.oracle_commit_f64.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32,
                                       i32, i32]
+    lib.oracle_conv_commit_f64.restype = ctypes.c_int
+    lib.oracle_conv_commit_f64.argtypes = [P, P, i64, P, i32, P, P, i32, i32, i32, i32]
     lib.oracle_commit_index.restype = ctypes.c_int
     lib.oracle_commit_index.argtypes = [P, i32, i32, i32, P]
     lib.oracle_replay_f64.restype = ctypes.c_int
@@ -130,6 +132,22 @@ def commit(snap, accept, cache, slot, *, B, N, Hv, dk, dv, n_layers=1,
     return lib.oracle_commit_f64(_ptr(snap), snap_layer_stride, _ptr(acc), _ptr(cache),
                                  cache_slot_stride, cache_layer_stride, _ptr(slot_a), n_slots,
                                  B, N, Hv, dk, dv, n_layers)
+
+
+def conv_commit(x, state, slot, parent, accept, *, n_slots=None):
+    """Convolution-history commit in place on `state` [n_slots, C, W] (float64);
+    x [B, N, C].  parent=None -> chain.  Returns the status."""
+    lib = _load()
+    assert state.dtype == np.float64 and state.flags.c_contiguous
+    x = _c(x, np.float64)
+    B, N, C = x.shape
+    W = state.shape[-1]
+    if n_slots is None:
+        n_slots = state.shape[0]
+    slot_a = None if slot is None else _c(slot, np.int32)
+    par_a = None if parent is None else _c(parent, np.int32)
+    return lib.oracle_conv_commit_f64(_ptr(x), _ptr(state), C * W, _ptr(slot_a), n_slots,
+                                      _ptr(par_a), _ptr(_c(accept, np.int32)), B, N, C, W)
 
 
 def commit_index(accept, slot, *, N, base=0):

@@ -166,6 +166,46 @@ int replay(const R* k, const R* v, const R* alpha, const R* beta, R* cache,
 
 extern "C" {
 
+// Convolution-history commit ("Photon 2.6", section "Handling recurrent
+// state": the convolution history is committed to the same boundary as the
+// state).  Per cache slot and channel the history holds the last W raw inputs,
+// oldest first (state + slot*stride + c*W); for every sequence the new history
+// is the last W elements of the old history followed by the channel's inputs
+// x[b][n][c] at the nodes of the accepted path (chain: 0 .. accept; tree: the
+// ancestors of accept from the root).
+int oracle_conv_commit_f64(const double* x, double* state, int64_t slot_stride,
+                           const int32_t* slot, int32_t n_slots, const int32_t* parent,
+                           const int32_t* accept, int32_t B, int32_t N, int32_t C, int32_t W) {
+  if (B < 0 || N <= 0 || C <= 0 || W <= 0) return ERR_INVALID_ARG;
+  std::vector<int32_t> depth(N), path;
+  std::vector<double> seq;
+  int status = OK;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* par = parent ? parent + (int64_t)b * N : nullptr;
+    if (par) {
+      int st = tree_depth(par, N, depth.data());
+      if (st != OK) { status = st; continue; }
+    }
+    const int acc = accept[b];
+    if (acc < 0 || acc >= N) { status = ERR_ACCEPT_RANGE; continue; }
+    const int sl = slot ? slot[b] : b;
+    if (sl < 0 || sl >= n_slots) { status = ERR_SLOT_RANGE; continue; }
+    path.clear();
+    if (par) {
+      for (int m = acc; m >= 0; m = par[m]) path.insert(path.begin(), m);
+    } else {
+      for (int m = 0; m <= acc; ++m) path.push_back(m);
+    }
+    for (int c = 0; c < C; ++c) {
+      double* h = state + (int64_t)sl * slot_stride + (int64_t)c * W;
+      seq.assign(h, h + W);
+      for (int n : path) seq.push_back(x[((int64_t)b * N + n) * C + c]);
+      for (int w = 0; w < W; ++w) h[w] = seq[seq.size() - W + w];
+    }
+  }
+  return status;
+}
+
 // Index-table commit ("TokenSpeed hits 580 tok/s", section "How they actually
 // got there": move pointers, not data): the accepted node's persisted state is
 // made current by pointing the sequence's slot at it in the block's snapshot

@@ -527,6 +527,57 @@ def check_index_commit_equals_copy():
     assert [int(x) for x in slot] == [1, 4], "a bad accept index must leave its slot alone"
 
 
+def check_conv_history_commit():
+    """Convolution history: after rounds of chain blocks each committed at
+    its accepted boundary, every channel holds the last W inputs of the whole
+    accepted token stream (the first history included); a tree commit equals
+    the chain commit over the accepted node's ancestor path; a short path
+    keeps the newest part of the old history; bad sequences are skipped."""
+    rng = np.random.default_rng(41)
+    C, W, N = 5, 4, 6
+    hist0 = rng.standard_normal((2, C, W))
+    state = hist0.copy()
+    slot = np.array([1], np.int32)
+    stream = [hist0[1].T]                          # [W][C], oldest first
+    for _ in range(5):
+        x = rng.standard_normal((1, N, C))
+        L = int(rng.integers(1, N + 1))
+        assert oracle.conv_commit(x, state, slot, None, np.array([L - 1], np.int32)) == oracle.OK
+        stream.append(x[0, :L])
+    tokens = np.concatenate(stream)                # [T][C]
+    assert np.array_equal(state[1], tokens[-W:].T), "history is not the last W inputs"
+    assert np.array_equal(state[0], hist0[0]), "another slot changed"
+    # tree == chain over the ancestor path
+    par = np.array([[-1, 0, 0, 1, 3, 2, 4]], np.int32)
+    x = rng.standard_normal((1, 7, C))
+    for acc in range(7):
+        t_state = hist0.copy()
+        assert oracle.conv_commit(x, t_state, slot, par, np.array([acc], np.int32)) == oracle.OK
+        path = []
+        m = acc
+        while m >= 0:
+            path.insert(0, m)
+            m = par[0, m]
+        c_state = hist0.copy()
+        xc = x[:, path]
+        assert oracle.conv_commit(xc, c_state, slot, None,
+                                  np.array([len(path) - 1], np.int32)) == oracle.OK
+        assert np.array_equal(t_state, c_state), f"tree node {acc} != chain over its path"
+    # a path shorter than W keeps the newest W - L old entries
+    s2 = hist0.copy()
+    assert oracle.conv_commit(x, s2, slot, None, np.array([1], np.int32)) == oracle.OK
+    assert np.array_equal(s2[1][:, :W - 2], hist0[1][:, 2:])
+    assert np.array_equal(s2[1][:, W - 2:], x[0, :2].T)
+    # errors
+    s3 = hist0.copy()
+    xb = rng.standard_normal((2, N, C))
+    st = oracle.conv_commit(xb, s3, np.array([0, 1], np.int32), None,
+                            np.array([2, N], np.int32))
+    assert st == oracle.ERR_ACCEPT_RANGE
+    assert np.array_equal(s3[1], hist0[1]), "a skipped sequence keeps its history"
+    assert np.array_equal(s3[0][:, W - 3:], xb[0, :3].T)
+
+
 def block_form_reference(H0, K, V, Q, alpha, beta, parent):
     """The whole block at once (float64, one value head): with G(n) the sum of
     log alpha over the root-to-n path and the deltas solved first from
@@ -581,5 +632,5 @@ ALL_CHECKS = [
     check_contraction, check_tree_matches_chain_and_paths, check_exact_rational_bruteforce,
     check_tree_depth_and_validation, check_commit, check_chunked_equals_step,
     check_rounds_equal_sequential, check_block_form_equals_recurrence,
-    check_replay_equals_persist, check_index_commit_equals_copy,
+    check_replay_equals_persist, check_index_commit_equals_copy, check_conv_history_commit,
 ]

@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("gdn_verify_chain", "gdn_verify_tree", "gdn_commit_accepted",
-                 "gdn_commit_index", "gdn_replay_accepted", "gdn_prefill_chunked", "gdn_prefill_workspace_bytes",
+                 "gdn_commit_index", "gdn_conv_commit", "gdn_replay_accepted", "gdn_prefill_chunked", "gdn_prefill_workspace_bytes",
                  "gdn_status_string", "gdn_version"):
         assert want in names
 
@@ -176,6 +176,29 @@ def test_f16_entry_points_host_checks(lib):
              None, None) == gdn.GDN_ERR_MISALIGNED
     assert f(0x10000, 0, 0x20000, 0x30000, 48 * 128 * 128, 0, None, 1, 0, 16, 48, 128, 128, 1,
              None, None) == gdn.GDN_OK
+
+
+@pytest.mark.parametrize("change, want", [
+    (dict(dtype=5), gdn.GDN_ERR_INVALID_ARG),
+    (dict(B=-1), gdn.GDN_ERR_INVALID_ARG),
+    (dict(N=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(W=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(W=9), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(stride=10), gdn.GDN_ERR_INVALID_ARG),
+    (dict(x=None), gdn.GDN_ERR_INVALID_ARG),
+    (dict(acc=None), gdn.GDN_ERR_INVALID_ARG),
+    (dict(x=0x10001), gdn.GDN_ERR_MISALIGNED),
+    (dict(dtype=0, state=0x30002), gdn.GDN_ERR_MISALIGNED),
+    (dict(acc=0x20002), gdn.GDN_ERR_MISALIGNED),
+    (dict(B=0), gdn.GDN_OK),
+])
+def test_conv_commit_host_checks(lib, change, want):
+    b = dict(x=0x10000, dtype=gdn.GDN_BF16, state=0x30000, stride=10240 * 3, slot=None,
+             n_slots=1, parent=None, acc=0x20000, B=1, N=16, C=10240, W=3, status=None)
+    b.update(change)
+    assert lib.gdn_conv_commit(b["x"], b["dtype"], b["state"], b["stride"], b["slot"],
+                               b["n_slots"], b["parent"], b["acc"], b["B"], b["N"], b["C"],
+                               b["W"], b["status"], None) == want
 
 
 def _commit(lib, **kw):

@@ -33,6 +33,14 @@ MUTANTS = {
                             "1.0 + 0 * alpha[(int64_t)t * Hv + h],\n"),
     "replay_drops_root": ("for (int m = acc; m >= 0; m = par[m]) path.insert",
                           "for (int m = acc; m > 0; m = par[m]) path.insert"),
+    "conv_keeps_oldest": ("for (int w = 0; w < W; ++w) h[w] = seq[seq.size() - W + w];",
+                          "for (int w = 0; w < W; ++w) h[w] = seq[w];"),
+    "conv_ignores_parent": ("for (int m = acc; m >= 0; m = par[m]) path.insert(path.begin(), m);\n"
+                            "    } else {\n      for (int m = 0; m <= acc; ++m) path.push_back(m);\n"
+                            "    }\n    for (int c = 0; c < C; ++c) {",
+                            "for (int m = 0; m <= acc; ++m) path.push_back(m);\n"
+                            "    } else {\n      for (int m = 0; m <= acc; ++m) path.push_back(m);\n"
+                            "    }\n    for (int c = 0; c < C; ++c) {"),
     "index_commit_wrong_stride": ("slot[b] = base + b * N + accept[b];",
                                   "slot[b] = base + b * (N - 1) + accept[b];"),
     "replay_chain_short": ("for (int m = 0; m <= acc; ++m) path.push_back(m);",
