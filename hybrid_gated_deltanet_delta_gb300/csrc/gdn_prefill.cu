@@ -413,9 +413,9 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
 // thread 64 issues, one chunk ahead, the TMA loads of K, Q and the V slab and
 // the bulk copy of the chunk's workspace block (all completing on one mbarrier
 // per buffer), and the TMA store of each chunk's output tile.
-constexpr int SCAN_THREADS = 256;
+constexpr int SCAN_THREADS = 384;          // 12 warps: 4 lane quarters x 3 column groups
 constexpr int NMAX = 48;                     // widest column slab
-constexpr int NH = NMAX / 2;                 // columns per thread
+constexpr int NH = 16;                       // columns per thread
 constexpr int TMEM_COLS = 512;               // D1 at column 0, D2 at 128, D3 at 256
 // one staging buffer: K and Q in two d_k halves of 128 rows x 128 bytes (K
 // rows 0-63, Q rows 64-127), the workspace block as copied, the V slab [64][n]
@@ -440,26 +440,19 @@ constexpr long long kWaitPolls = 1ll << 22;
 // the three column slabs of a 128-wide state: 48 + 48 + 32 columns
 __device__ __forceinline__ int slab_width(int s) { return s == 2 ? 32 : 48; }
 
-// nh (16 or 24) fp32 columns of TMEM lane (warp quarter base + lane) starting
-// at `taddr`; columns past nh read as zero.
+// NH = 16 fp32 columns of TMEM lane (warp quarter base + lane) starting at
+// `taddr`.
 __device__ __forceinline__ void tmem_cols(uint32_t taddr, int nh, float (&x)[NH]) {
-  uint32_t r0[8], r1[8], r2[8];
+  (void)nh;
+  uint32_t r0[8], r1[8];
   tc::tmem_ld8(taddr, r0);
   tc::tmem_ld8(taddr + 8, r1);
-  if (nh > 16) tc::tmem_ld8(taddr + 16, r2);
   tc::tmem_wait_ld(r0);
   tc::tmem_wait_ld(r1);
-  if (nh > 16) {
-    tc::tmem_wait_ld(r2);
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) r2[e] = 0u;
-  }
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     x[e] = __uint_as_float(r0[e]);
     x[8 + e] = __uint_as_float(r1[e]);
-    x[16 + e] = __uint_as_float(r2[e]);
   }
 }
 
@@ -506,7 +499,7 @@ __device__ __forceinline__ bool tc_barrier(bool ok) {
   return all;
 }
 
-// The same over the chunk warps only (warps 0, 1, 4, 5; barrier 1).
+// The same over the chunk warps only (lane quarters 0 and 1; barrier 1).
 __device__ __forceinline__ void chunk_barrier() {
   fence_proxy_async_smem();
   tc::fence_before_sync();
@@ -522,10 +515,12 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int sl = blockIdx.x, h = blockIdx.y, hk = h / (Hv / Hk);
-  const int j0 = 48 * sl, n = slab_width(sl), nh = n / 2;
+  const int j0 = 48 * sl, n = slab_width(sl);
   const int n_chunks = (T + C - 1) / C;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const int qd = w & 3, c0 = (w >> 2) * nh;  // lane quarter; first slab column of this thread
+  const int qd = w & 3, c0 = (w >> 2) * NH;  // lane quarter; first slab column of this thread
+  const bool active = c0 < n;                // a 32-wide slab leaves the third group idle
+  const int nh = active ? NH : 0;            // columns this thread owns
   const int r = 32 * qd + lane;              // TMEM lane: row of D1 / D2 / D3
   const bool chunk_warp = qd < 2;            // rows 0-63: K H, Delta
   const int row = r & (C - 1);               // chunk row (D1 / D2)
@@ -630,7 +625,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     float qh[NH];
     {
       float x[NH];
-      tmem_cols_sum(t_mine, n, nh, x);
+      if (active) tmem_cols_sum(t_mine, n, nh, x);
       if (chunk_warp) {
         // X = beta (V - g K H)
 #pragma unroll
@@ -664,7 +659,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     tc::fence_after_sync();
     {
       float x[NH];
-      tmem_cols_sum(t_mine + 128, n, nh, x);
+      if (active) tmem_cols_sum(t_mine + 128, n, nh, x);
       if (chunk_warp) {
         // D' = (g_C / g) Delta
         const float rg = __expf(GC - G_r);
@@ -702,7 +697,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     tc::fence_after_sync();
     {
       float x[NH];
-      tmem_cols_sum(t_mine + 256, n, nh, x);
+      if (active) tmem_cols_sum(t_mine + 256, n, nh, x);
 #pragma unroll
       for (int e = 0; e < NH; ++e) Hr[e] = fmaf(gC, Hr[e], x[e]);
       put_split(hb, 16384, r, c0, n, Hr, nh);
