@@ -88,7 +88,10 @@ static_assert(2 * C * KS <= PREP_AP_SIZE, "K and Q staging fits in the A / P are
 constexpr int PREP_GATE = PREP_AP_SIZE;              // [head][alpha 64, beta 64]
 constexpr int PREP_G = PREP_GATE + HG * 2 * C * 4;   // [head][64] log decay
 constexpr int PREP_B = PREP_G + HG * C * 4;          // [head][64] beta
-constexpr int PREP_SMEM = PREP_B + HG * C * 4;
+constexpr int PREP_E = PREP_B + HG * C * 4;          // [head][64] exp(G_t - G_ref)
+constexpr int PREP_F = PREP_E + HG * C * 4;          // [head][64] exp(G_ref - G_s)
+constexpr int PREP_SEP = PREP_F + HG * C * 4;        // [head] the split above is safe
+constexpr int PREP_SMEM = PREP_SEP + 16;
 // with more than HG value heads per q/k head the accumulator fragments are
 // parked in shared memory between passes (one float4 row per thread and tile)
 constexpr int PREP_ACC = PREP_SMEM;
@@ -162,6 +165,9 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
   float* sgate = reinterpret_cast<float*>(smem + PREP_GATE);
   float* sG = reinterpret_cast<float*>(smem + PREP_G);
   float* sB = reinterpret_cast<float*>(smem + PREP_B);
+  float* sE = reinterpret_cast<float*>(smem + PREP_E);
+  float* sF = reinterpret_cast<float*>(smem + PREP_F);
+  int* ssep = reinterpret_cast<int*>(smem + PREP_SEP);
 
   const int c = blockIdx.x, hk = blockIdx.y, G = Hv / Hk;
   const int t0 = c * C, nv = min(C, T - t0);
@@ -237,22 +243,48 @@ prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
       char* wsb = ws + ((size_t)c * Hv + h0 + w) * WS_STRIDE;
       *reinterpret_cast<float2*>(wsb + WS_G + ta * 4) = make_float2(Ga, Gb);
       *reinterpret_cast<float2*>(wsb + WS_B + ta * 4) = make_float2(ga[C + ta], ga[C + tb]);
+      // e^{G_t - G_s} = E_t F_s with E_t = e^{G_t - G_ref}, F_s = e^{G_ref - G_s}
+      // around the middle row; used when no factor can overflow (the decay
+      // across the chunk stays within e^{+-80}), else A and P take e^{G_t - G_s}
+      const float Gref = __shfl_sync(0xffffffffu, Gb, 15);
+      float span = fmaxf(fabsf(Ga - Gref), fabsf(Gb - Gref));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        span = fmaxf(span, __shfl_xor_sync(0xffffffffu, span, off));
+      sE[w * C + ta] = __expf(Ga - Gref);
+      sE[w * C + tb] = __expf(Gb - Gref);
+      sF[w * C + ta] = __expf(Gref - Ga);
+      sF[w * C + tb] = __expf(Gref - Gb);
+      if (lane == 0) ssep[w] = span <= 80.f;
     }
     __syncthreads();
     // ---- 2. A (warps 0-3) and P (warps 4-7) of each head from the accumulators
+    //      (column tiles wholly above this warp's 16 rows are zero)
     for (int j = 0; j < ng; ++j) {
       float* dst = sap + (j * 2 + (is_kk ? 0 : 1)) * C * AS;
       const float* Gj = sG + j * C;
+      const float* Ej = sE + j * C;
+      const float* Fj = sF + j * C;
+      const bool sep = ssep[j] != 0;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int t = 16 * mt + g8 + 8 * half;
-        const float Gt = Gj[t], bt = is_kk ? sB[j * C + t] : 1.f;
+        const float Gt = Gj[t], bt = is_kk ? sB[j * C + t] : 1.f, bE = bt * Ej[t];
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
           const int s = nt * 8 + 2 * t4;
-          const bool m0 = is_kk ? s < t : s <= t, m1 = is_kk ? s + 1 < t : s + 1 <= t;
-          const float v0 = m0 ? bt * __expf(Gt - Gj[s]) * a[nt][2 * half] : 0.f;
-          const float v1 = m1 ? bt * __expf(Gt - Gj[s + 1]) * a[nt][2 * half + 1] : 0.f;
+          float v0 = 0.f, v1 = 0.f;
+          if (nt * 8 <= 16 * mt + 15) {
+            const bool m0 = is_kk ? s < t : s <= t, m1 = is_kk ? s + 1 < t : s + 1 <= t;
+            if (sep) {
+              const float2 f = *reinterpret_cast<const float2*>(Fj + s);
+              v0 = m0 ? bE * f.x * a[nt][2 * half] : 0.f;
+              v1 = m1 ? bE * f.y * a[nt][2 * half + 1] : 0.f;
+            } else {
+              v0 = m0 ? bt * __expf(Gt - Gj[s]) * a[nt][2 * half] : 0.f;
+              v1 = m1 ? bt * __expf(Gt - Gj[s + 1]) * a[nt][2 * half + 1] : 0.f;
+            }
+          }
           *reinterpret_cast<float2*>(dst + t * AS + s) = make_float2(v0, v1);
         }
       }

@@ -48,6 +48,19 @@ def test_prefill_ragged_lengths(gpu_lib, T, heads):
     assert_close(H, Hr, f"prefill state T={T}")
 
 
+def test_prefill_extreme_decay(gpu_lib):
+    """Gates near zero on part of the sequence: the log decay spans hundreds
+    across a chunk, beyond what a product of two exponentials can hold in
+    fp32, so the preparation takes each decay ratio from its own exponential."""
+    inp = synthetic.make_prefill_inputs(T=192, Hk=1, Hv=3, dk=128, dv=128, dtype="bf16",
+                                        alpha_kind="unit", state_sigma=0.1, seed=4343)
+    inp["alpha"][64:128] = np.float32(1e-3)       # chunk 1: log decay spans ~440
+    H, O = run_prefill(gpu_lib, inp)
+    Hr, Or = oracle_prefill(inp)
+    assert_close(O, Or, "o")
+    assert_close(H, Hr, "state")
+
+
 @pytest.mark.parametrize("heads", [(1, 4), (2, 16)])
 def test_prefill_many_value_heads_per_qk_head(gpu_lib, heads):
     """More than three value heads share a q/k head: the preparation runs in
