@@ -77,6 +77,12 @@ def load(path: str | None = None):
     lib.gdn_commit_accepted.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32, i32,
                                         i32, P, P]
     lib.gdn_commit_accepted.restype = ctypes.c_int
+    lib.gdn_verify_chain_prep.argtypes = [ctypes.POINTER(VerifyArgs), P]
+    lib.gdn_verify_chain_prep.restype = ctypes.c_int
+    lib.gdn_verify_tree_prep.argtypes = [ctypes.POINTER(VerifyArgs), P, P, P]
+    lib.gdn_verify_tree_prep.restype = ctypes.c_int
+    lib.gdn_replay_accepted_prep.argtypes = [ctypes.POINTER(VerifyArgs), P, P, P]
+    lib.gdn_replay_accepted_prep.restype = ctypes.c_int
     lib.gdn_verify_chain_f16.argtypes = [ctypes.POINTER(VerifyArgs), P, P]
     lib.gdn_verify_chain_f16.restype = ctypes.c_int
     lib.gdn_commit_accepted_f16.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32,
@@ -175,12 +181,17 @@ def make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, *, slot=No
 
 
 def gdn_verify_chain(q, k, v, alpha, beta, state_cache, snapshots, o, *, slot=None, n_slots=None,
-                     status=None, cache_slot_stride=None, tile_cols=0, row_warps=0, stream=None):
-    """Causal-chain verification; writes snapshots and o (see include/gdn.h)."""
+                     status=None, cache_slot_stride=None, tile_cols=0, row_warps=0, stream=None,
+                     prep=False):
+    """Causal-chain verification; writes snapshots and o (see include/gdn.h).
+    prep=True: q, k are raw projections and alpha, beta gate pre-activations
+    (gdn_verify_chain_prep)."""
     a = make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, slot=slot,
                          n_slots=n_slots, status=status, cache_slot_stride=cache_slot_stride,
                          tile_cols=tile_cols, row_warps=row_warps)
-    _check(load().gdn_verify_chain(ctypes.byref(a), _stream(stream)), "gdn_verify_chain")
+    fn = load().gdn_verify_chain_prep if prep else load().gdn_verify_chain
+    _check(fn(ctypes.byref(a), _stream(stream)),
+           "gdn_verify_chain_prep" if prep else "gdn_verify_chain")
 
 
 def gdn_verify_chain_f16(q, k, v, alpha, beta, state_cache, snapshots_f16, o, *, slot=None,
@@ -201,15 +212,17 @@ def gdn_verify_chain_f16(q, k, v, alpha, beta, state_cache, snapshots_f16, o, *,
 
 def gdn_verify_tree(q, k, v, alpha, beta, state_cache, snapshots, o, parent, *, depth_out=None,
                     slot=None, n_slots=None, status=None, cache_slot_stride=None, tile_cols=0,
-                    row_warps=0, stream=None):
-    """Tree verification; parent [B,N] int32 (see include/gdn.h)."""
+                    row_warps=0, stream=None, prep=False):
+    """Tree verification; parent [B,N] int32 (see include/gdn.h).  prep=True:
+    raw projections and gate pre-activations (gdn_verify_tree_prep)."""
     _need(parent.is_contiguous() and tuple(parent.shape) == tuple(q.shape[:2]),
           "parent must be a contiguous [B,N] int32 tensor")
     a = make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, slot=slot,
                          n_slots=n_slots, status=status, cache_slot_stride=cache_slot_stride,
                          tile_cols=tile_cols, row_warps=row_warps)
-    _check(load().gdn_verify_tree(ctypes.byref(a), _ptr(parent), _ptr(depth_out),
-                                  _stream(stream)), "gdn_verify_tree")
+    fn = load().gdn_verify_tree_prep if prep else load().gdn_verify_tree
+    _check(fn(ctypes.byref(a), _ptr(parent), _ptr(depth_out), _stream(stream)),
+           "gdn_verify_tree_prep" if prep else "gdn_verify_tree")
 
 
 def gdn_commit_accepted(snapshots, accept_idx, state_cache, *, B, N, Hv, dk, dv, n_layers=1,
@@ -268,7 +281,7 @@ def gdn_commit_index(accept_idx, slot, *, N, base_slot=0, status=None, stream=No
 
 def gdn_replay_accepted(k, v, alpha, beta, state_cache, accept_idx, *, parent=None, slot=None,
                         n_slots=None, status=None, cache_slot_stride=None, tile_cols=0,
-                        row_warps=0, stream=None):
+                        row_warps=0, stream=None, prep=False):
     """Checkpoint-and-replay commit: state_cache[slot[b]] <- the state of node
     accept_idx[b], recomputed over the accepted path from the cached state
     (chain when parent is None; parent [B,N] int32 for a tree)."""
@@ -280,8 +293,9 @@ def gdn_replay_accepted(k, v, alpha, beta, state_cache, accept_idx, *, parent=No
     a = make_verify_args(None, k, v, alpha, beta, state_cache, None, None, slot=slot,
                          n_slots=n_slots, status=status, cache_slot_stride=cache_slot_stride,
                          tile_cols=tile_cols, row_warps=row_warps)
-    _check(load().gdn_replay_accepted(ctypes.byref(a), _ptr(parent), _ptr(accept_idx),
-                                      _stream(stream)), "gdn_replay_accepted")
+    fn = load().gdn_replay_accepted_prep if prep else load().gdn_replay_accepted
+    _check(fn(ctypes.byref(a), _ptr(parent), _ptr(accept_idx), _stream(stream)),
+           "gdn_replay_accepted_prep" if prep else "gdn_replay_accepted")
 
 
 def gdn_prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk=64) -> int:

@@ -23,7 +23,7 @@ void auto_tile(int dk, int dv, int B, int Hv, int* wc, int* nw) {
 }
 
 int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, bool tree,
-                  void* stream, void* snap16 = nullptr) {
+                  void* stream, void* snap16 = nullptr, bool prep = false) {
   if (a == nullptr) return GDN_ERR_INVALID_ARG;
   if (a->B < 0 || a->N < 1 || a->Hk < 1 || a->Hv < 1 || a->Hv % a->Hk != 0)
     return GDN_ERR_INVALID_ARG;
@@ -59,7 +59,7 @@ int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   if (a->row_warps != 0) nw = a->row_warps;
   if (!gdn::verify_tile_supported(a->dk, wc, nw) || a->dv % wc != 0) return GDN_ERR_UNSUPPORTED;
   return gdn::launch_verify(a, tree ? parent : nullptr, tree ? depth_out : nullptr, wc, nw,
-                            static_cast<cudaStream_t>(stream), snap16);
+                            static_cast<cudaStream_t>(stream), snap16, prep);
 }
 
 int commit_common(const void* snapshots, bool src16, int64_t snap_layer_stride,
@@ -87,7 +87,7 @@ int commit_common(const void* snapshots, bool src16, int64_t snap_layer_stride,
 }
 
 int replay_common(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept,
-                  void* stream) {
+                  void* stream, bool prep = false) {
   if (a == nullptr) return GDN_ERR_INVALID_ARG;
   if (a->B < 0 || a->N < 1 || a->Hk < 1 || a->Hv < 1 || a->Hv % a->Hk != 0)
     return GDN_ERR_INVALID_ARG;
@@ -114,7 +114,7 @@ int replay_common(const gdn_verify_args* a, const int32_t* parent, const int32_t
   if (a->tile_cols != 0) wc = a->tile_cols;
   if (a->row_warps != 0) nw = a->row_warps;
   if (!gdn::verify_tile_supported(a->dk, wc, nw) || a->dv % wc != 0) return GDN_ERR_UNSUPPORTED;
-  return gdn::launch_replay(a, parent, accept, wc, static_cast<cudaStream_t>(stream));
+  return gdn::launch_replay(a, parent, accept, wc, static_cast<cudaStream_t>(stream), prep);
 }
 
 }  // namespace
@@ -124,6 +124,20 @@ extern "C" {
 int gdn_replay_accepted(const gdn_verify_args* args, const int32_t* parent,
                         const int32_t* accept_idx, void* stream) {
   return replay_common(args, parent, accept_idx, stream);
+}
+
+int gdn_verify_chain_prep(const gdn_verify_args* args, void* stream) {
+  return verify_common(args, nullptr, nullptr, false, stream, nullptr, true);
+}
+
+int gdn_verify_tree_prep(const gdn_verify_args* args, const int32_t* parent, int32_t* depth_out,
+                         void* stream) {
+  return verify_common(args, parent, depth_out, true, stream, nullptr, true);
+}
+
+int gdn_replay_accepted_prep(const gdn_verify_args* args, const int32_t* parent,
+                             const int32_t* accept_idx, void* stream) {
+  return replay_common(args, parent, accept_idx, stream, true);
 }
 
 int gdn_verify_chain(const gdn_verify_args* args, void* stream) {

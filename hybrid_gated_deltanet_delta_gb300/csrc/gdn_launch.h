@@ -12,12 +12,14 @@ namespace gdn {
 
 bool verify_tile_supported(int dk, int wc, int nw);
 // snap16 != NULL: chain with binary16 snapshots there (a->snapshots unused).
+// prep: q, k are raw projections (L2-normalised here) and alpha, beta hold the
+// gate pre-activations (alpha = exp(-softplus(a)), beta = sigmoid(b) here).
 int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, int wc,
-                  int nw, cudaStream_t stream, void* snap16 = nullptr);
+                  int nw, cudaStream_t stream, void* snap16 = nullptr, bool prep = false);
 
 // Replay of the accepted path from the cached state, written back in place.
 int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept, int wc,
-                  cudaStream_t stream);
+                  cudaStream_t stream, bool prep = false);
 
 // src16: the snapshots are binary16 (widened exactly into the fp32 cache).
 int launch_commit(const void* snap, bool src16, int64_t snap_layer_stride, const int32_t* accept,

@@ -65,7 +65,7 @@ __host__ __device__ constexpr int round16(int x) { return (x + 15) & ~15; }
 // Shared-memory plan in bytes; every array starts on a 16-byte boundary.
 // Tree blocks add per-node tables and `pool` stash slots of dk x WC floats.
 struct SmemPlan {
-  int q, k, v, a, b, par, src, stash, last, pool, total;
+  int q, k, v, a, b, par, src, stash, last, pool, inv, total;
 };
 
 __host__ __device__ inline SmemPlan smem_plan(int N, int DK, int WC, int esz, bool tree,
@@ -82,7 +82,8 @@ __host__ __device__ inline SmemPlan smem_plan(int N, int DK, int WC, int esz, bo
   s.stash = s.src + t;
   s.last = s.stash + t;
   s.pool = s.last + t;
-  s.total = s.pool + (tree ? pool * DK * WC * 4 : 0);
+  s.inv = s.pool + (tree ? pool * DK * WC * 4 : 0);  // 1/|q_n|, 1/|k_n| (input preparation)
+  s.total = s.inv + 2 * round16(N * 4);
   return s;
 }
 
@@ -161,7 +162,47 @@ __device__ __forceinline__ void load_rows(float (&x)[R], const char* row, int fi
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
-template <int DK, int WC, bool TREE, bool SNAP16>
+// Input preparation from raw projections: 1/|x| of `rows` staged rows of DK
+// elements (bf16 or fp32) into inv[] (0 for a zero row, which then stays
+// zero), one row per lane; and the gates alpha = exp(-softplus(a)) =
+// 1/(1 + e^a), beta = sigmoid(b) = 1/(1 + e^-b) in place.
+template <int DK>
+__device__ __forceinline__ void prep_rows(const char* rows_base, int rows, bool bf16, float* inv,
+                                          int lane) {
+  for (int r = lane; r < rows; r += 32) {
+    float ss = 0.f;
+    if (bf16) {
+      const uint4* s = reinterpret_cast<const uint4*>(rows_base + (size_t)r * DK * 2);
+#pragma unroll 4
+      for (int c = 0; c < DK / 8; ++c) {
+        const uint4 t = s[c];
+        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+          ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+        }
+      }
+    } else {
+      const float4* s = reinterpret_cast<const float4*>(rows_base + (size_t)r * DK * 4);
+#pragma unroll 4
+      for (int c = 0; c < DK / 4; ++c) {
+        const float4 t = s[c];
+        ss = fmaf(t.x, t.x, fmaf(t.y, t.y, fmaf(t.z, t.z, fmaf(t.w, t.w, ss))));
+      }
+    }
+    inv[r] = ss > 0.f ? rsqrtf(ss) : 0.f;
+  }
+}
+
+__device__ __forceinline__ void prep_gates(float* a, float* b, int n_rows, int lane) {
+  for (int r = lane; r < n_rows; r += 32) {
+    a[r] = 1.f / (1.f + __expf(a[r]));
+    b[r] = 1.f / (1.f + __expf(-b[r]));
+  }
+}
+
+template <int DK, int WC, bool TREE, bool SNAP16, bool PREP>
 __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
   using S = Shape<DK, WC>;
   constexpr int R = S::R;
@@ -180,6 +221,8 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
   int* sstash = reinterpret_cast<int*>(smem + pl.stash);  // tree: slot receiving node n, or -1
   int* slast = reinterpret_cast<int*>(smem + pl.last);    // tree: last non-adjacent child
   float* pool = reinterpret_cast<float*>(smem + pl.pool);
+  float* sinvq = reinterpret_cast<float*>(smem + pl.inv);
+  float* sinvk = sinvq + round16(N * 4) / 4;
 
   const int lane = threadIdx.x;
   const int cg = lane % S::CG, rl = lane / S::CG;
@@ -227,6 +270,14 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
   }
   cp_async_wait_all();
   __syncwarp();
+
+  if constexpr (PREP) {
+    // raw projections: norms of q and k, gates from their pre-activations
+    prep_rows<DK>(sq, N, bf16, sinvq, lane);
+    prep_rows<DK>(sk, N, bf16, sinvk, lane);
+    prep_gates(sa, sb, N, lane);
+    __syncwarp();
+  }
 
   if constexpr (TREE) {
     // parent[0] == -1, 0 <= parent[n] < n; the block leaves otherwise
@@ -306,6 +357,10 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
     for (int off = S::CG; off < 32; off <<= 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
+    if constexpr (PREP) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) u[c] *= sinvk[0];
+    }
   }
 
   const int64_t node_stride = (int64_t)p.Hv * DK * dv;
@@ -351,6 +406,10 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
         for (int off = S::CG; off < 32; off <<= 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
+        if constexpr (PREP) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) u[c] *= sinvk[n];
+        }
       }
     }
 
@@ -368,6 +427,10 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
     float vj[4];
     load_rows<4>(vj, sv + n * WC * esz, cg * 4, bf16);
     const float al = sa[n], be = sb[n];
+    // 1/|k_n|, 1/|k_{n+1}|, 1/|q_n| when the inputs are raw projections
+    const float ik = PREP ? sinvk[n] : 1.f;
+    const float ikx = PREP && has_next ? sinvk[n + 1] : 1.f;
+    const float iq = PREP ? sinvq[n] : 1.f;
 
     // (c) partial sums for u_{n+1} when node n+1 continues from node n:
     //     from the registers before node n's update
@@ -386,7 +449,7 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
     float d[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) d[c] = be * (vj[c] - al * u[c]);
-    const float2 d01 = make_float2(d[0], d[1]), d23 = make_float2(d[2], d[3]);
+    const float2 d01 = make_float2(d[0] * ik, d[1] * ik), d23 = make_float2(d[2] * ik, d[3] * ik);
     const float2 al2 = f2(al);
     float2 o01 = make_float2(0.f, 0.f), o23 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -415,10 +478,12 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
 #pragma unroll
       for (int i = 0; i < 9; ++i) red[i] += __shfl_xor_sync(FULL, red[i], off);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) u[c] = next_chain ? fmaf(al, red[c], d[c] * red[4]) : red[c];
+    for (int c = 0; c < 4; ++c)
+      u[c] = next_chain ? fmaf(al, red[c] * ikx, d[c] * (red[4] * (ik * ikx))) : red[c];
 
     // (f) persist (a chain verified for a replay commit keeps no snapshots)
-    if (rl == 0) st_f4(o_h + (int64_t)n * p.Hv * dv, red[5], red[6], red[7], red[8]);
+    if (rl == 0)
+      st_f4(o_h + (int64_t)n * p.Hv * dv, red[5] * iq, red[6] * iq, red[7] * iq, red[8] * iq);
     if constexpr (SNAP16) {
       // binary16, round to nearest even: 8 bytes per lane and row
       __half* dst = snap16_h + (int64_t)n * node_stride;
@@ -475,7 +540,7 @@ struct ReplayParams {
 };
 
 struct ReplayPlan {
-  int path, par, k, v, a, b, total;
+  int path, par, k, v, a, b, inv, total;
 };
 
 __host__ __device__ inline ReplayPlan replay_plan(int N, int DK, int WC, int esz) {
@@ -486,11 +551,12 @@ __host__ __device__ inline ReplayPlan replay_plan(int N, int DK, int WC, int esz
   s.v = s.k + round16(N * DK * esz);
   s.a = s.v + round16(N * WC * esz);
   s.b = s.a + round16(N * 4);
-  s.total = s.b + round16(N * 4);
+  s.inv = s.b + round16(N * 4);  // 1/|k| of the path nodes (input preparation)
+  s.total = s.inv + round16(N * 4);
   return s;
 }
 
-template <int DK, int WC>
+template <int DK, int WC, bool PREP>
 __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
   using S = Shape<DK, WC>;
   constexpr int R = S::R;
@@ -505,6 +571,7 @@ __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
   char* sv = smem + pl.v;
   float* sa = reinterpret_cast<float*>(smem + pl.a);
   float* sb = reinterpret_cast<float*>(smem + pl.b);
+  float* sinvk = reinterpret_cast<float*>(smem + pl.inv);
 
   const int lane = threadIdx.x;
   const int cg = lane % S::CG, rl = lane / S::CG;
@@ -584,6 +651,11 @@ __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
   }
   cp_async_wait_all();
   __syncwarp();
+  if constexpr (PREP) {
+    prep_rows<DK>(sk, L, bf16, sinvk, lane);
+    prep_gates(sa, sb, L, lane);
+    __syncwarp();
+  }
 
   float kn[R];
   load_rows<R>(kn, sk, row0, bf16);
@@ -600,6 +672,10 @@ __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
     for (int off = S::CG; off < 32; off <<= 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
+    if constexpr (PREP) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) u[c] *= sinvk[0];
+    }
   }
   for (int i = 0; i < L; ++i) {
     float knx[R];
@@ -612,6 +688,8 @@ __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
     float vj[4];
     load_rows<4>(vj, sv + i * WC * esz, cg * 4, bf16);
     const float al = sa[i], be = sb[i];
+    const float ik = PREP ? sinvk[i] : 1.f;
+    const float ikx = PREP && i + 1 < L ? sinvk[i + 1] : 1.f;
     float2 w01 = make_float2(0.f, 0.f), w23 = make_float2(0.f, 0.f);
     float kk = 0.f;
 #pragma unroll
@@ -623,7 +701,7 @@ __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
     float d[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) d[c] = be * (vj[c] - al * u[c]);
-    const float2 d01 = make_float2(d[0], d[1]), d23 = make_float2(d[2], d[3]);
+    const float2 d01 = make_float2(d[0] * ik, d[1] * ik), d23 = make_float2(d[2] * ik, d[3] * ik);
     const float2 al2 = f2(al);
 #pragma unroll
     for (int m = 0; m < R; ++m) {
@@ -636,7 +714,7 @@ __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
 #pragma unroll
       for (int e = 0; e < 5; ++e) red[e] += __shfl_xor_sync(FULL, red[e], off);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) u[c] = fmaf(al, red[c], d[c] * red[4]);
+    for (int c = 0; c < 4; ++c) u[c] = fmaf(al, red[c] * ikx, d[c] * (red[4] * (ik * ikx)));
 #pragma unroll
     for (int m = 0; m < R; ++m) kn[m] = knx[m];
   }
@@ -648,21 +726,24 @@ __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
 }
 
 template <int DK, int WC>
-int launch_replay_t(const ReplayParams& p, int B, cudaStream_t stream) {
+int launch_replay_t(const ReplayParams& p, int B, bool prep, cudaStream_t stream) {
   const ReplayPlan pl = replay_plan(p.N, DK, WC, p.bf16 ? 2 : 4);
   const dim3 grid(p.dv / WC, p.Hv, B);
-  replay_kernel<DK, WC><<<grid, 32, pl.total, stream>>>(p);
+  if (prep)
+    replay_kernel<DK, WC, true><<<grid, 32, pl.total, stream>>>(p);
+  else
+    replay_kernel<DK, WC, false><<<grid, 32, pl.total, stream>>>(p);
   return launch_status();
 }
 
-template <int DK, int WC, bool TREE, bool SNAP16>
+template <int DK, int WC, bool TREE, bool SNAP16, bool PREP>
 int launch(const VerifyParams& p, int B, cudaStream_t stream) {
   VerifyParams q = p;
   q.pool = TREE ? tree_pool_slots(p.N, DK, WC, p.bf16 ? 2 : 4) : 0;
   const SmemPlan pl = smem_plan(p.N, DK, WC, p.bf16 ? 2 : 4, TREE, q.pool);
   const size_t smem = (size_t)pl.total;
   if (smem > 227 * 1024) return GDN_ERR_UNSUPPORTED;
-  auto kern = verify_kernel<DK, WC, TREE, SNAP16>;
+  auto kern = verify_kernel<DK, WC, TREE, SNAP16, PREP>;
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -673,10 +754,10 @@ int launch(const VerifyParams& p, int B, cudaStream_t stream) {
   return launch_status();
 }
 
-template <bool TREE, bool SNAP16>
+template <bool TREE, bool SNAP16, bool PREP>
 int dispatch(const VerifyParams& p, int B, int dk, int wc, cudaStream_t s) {
 #define GDN_CASE(DK_, WC_) \
-  if (dk == DK_ && wc == WC_) return launch<DK_, WC_, TREE, SNAP16>(p, B, s);
+  if (dk == DK_ && wc == WC_) return launch<DK_, WC_, TREE, SNAP16, PREP>(p, B, s);
   GDN_CASE(128, 16)
   GDN_CASE(128, 8)
   GDN_CASE(64, 16)
@@ -696,7 +777,7 @@ bool verify_tile_supported(int dk, int wc, int nw) {
 }
 
 int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, int wc,
-                  int nw, cudaStream_t stream, void* snap16) {
+                  int nw, cudaStream_t stream, void* snap16, bool prep) {
   (void)nw;
   VerifyParams p{};
   p.q = a->q;
@@ -719,13 +800,19 @@ int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   p.dv = a->dv;
   p.bf16 = a->in_dtype == GDN_BF16;
   p.snap16 = static_cast<__half*>(snap16);
-  if (parent != nullptr) return dispatch<true, false>(p, a->B, a->dk, wc, stream);
-  if (snap16 != nullptr) return dispatch<false, true>(p, a->B, a->dk, wc, stream);
-  return dispatch<false, false>(p, a->B, a->dk, wc, stream);
+  if (parent != nullptr)
+    return prep ? dispatch<true, false, true>(p, a->B, a->dk, wc, stream)
+                : dispatch<true, false, false>(p, a->B, a->dk, wc, stream);
+  if (snap16 != nullptr) {
+    if (prep) return GDN_ERR_UNSUPPORTED;
+    return dispatch<false, true, false>(p, a->B, a->dk, wc, stream);
+  }
+  return prep ? dispatch<false, false, true>(p, a->B, a->dk, wc, stream)
+              : dispatch<false, false, false>(p, a->B, a->dk, wc, stream);
 }
 
 int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept, int wc,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, bool prep) {
   ReplayParams p{};
   p.k = a->k;
   p.v = a->v;
@@ -744,7 +831,7 @@ int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t
   p.dv = a->dv;
   p.bf16 = a->in_dtype == GDN_BF16;
 #define GDN_CASE(DK_, WC_) \
-  if (a->dk == DK_ && wc == WC_) return launch_replay_t<DK_, WC_>(p, a->B, stream);
+  if (a->dk == DK_ && wc == WC_) return launch_replay_t<DK_, WC_>(p, a->B, prep, stream);
   GDN_CASE(128, 16)
   GDN_CASE(128, 8)
   GDN_CASE(64, 16)

@@ -158,6 +158,25 @@ int gdn_commit_accepted(const float* snapshots, int64_t snap_layer_stride,
                         int32_t n_layers, int32_t* status, void* stream);
 
 /*
+ * Verification and replay from raw projections (input preparation fused into
+ * the recurrence kernel).  The same calls as gdn_verify_chain,
+ * gdn_verify_tree and gdn_replay_accepted, except that
+ *   q, k          are the raw projections: each (node, q/k head) vector is
+ *                 L2-normalised in the kernel (a zero vector stays zero);
+ *   alpha, beta   hold the gate pre-activations a, b: the kernel uses
+ *                 alpha = exp(-softplus(a)) = 1 / (1 + e^a) and
+ *                 beta = sigmoid(b) = 1 / (1 + e^-b).
+ * These are the maps the block's inputs are defined by (q and k L2-normalised
+ * per head, alpha from exp(-softplus), beta from sigmoid).  Results equal the
+ * plain calls on the prepared inputs up to floating-point rounding.
+ */
+int gdn_verify_chain_prep(const gdn_verify_args* args, void* stream);
+int gdn_verify_tree_prep(const gdn_verify_args* args, const int32_t* parent, int32_t* depth_out,
+                         void* stream);
+int gdn_replay_accepted_prep(const gdn_verify_args* args, const int32_t* parent,
+                             const int32_t* accept_idx, void* stream);
+
+/*
  * Chain verification with 16-bit persisted states ("We got 207 tok/s with
  * Qwen3.5-27B on an RTX 3090", list "Key wins": an f16 intermediate cache at
  * half the bandwidth).  The same as gdn_verify_chain, except that every

@@ -48,6 +48,8 @@ def bind(lib):
     lib.oracle_commit_f64.restype = ctypes.c_int
     lib.oracle_commit_f64.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32,
                                       i32, i32]
+    lib.oracle_prepare_inputs_f64.restype = ctypes.c_int
+    lib.oracle_prepare_inputs_f64.argtypes = [P, P, i64, i32, P, P, i64]
     lib.oracle_conv_commit_f64.restype = ctypes.c_int
     lib.oracle_conv_commit_f64.argtypes = [P, P, i64, P, i32, P, P, i32, i32, i32, i32]
     lib.oracle_commit_index.restype = ctypes.c_int
@@ -132,6 +134,22 @@ def commit(snap, accept, cache, slot, *, B, N, Hv, dk, dv, n_layers=1,
     return lib.oracle_commit_f64(_ptr(snap), snap_layer_stride, _ptr(acc), _ptr(cache),
                                  cache_slot_stride, cache_layer_stride, _ptr(slot_a), n_slots,
                                  B, N, Hv, dk, dv, n_layers)
+
+
+def prepare_inputs(q, k, a, b):
+    """Raw projections -> verify inputs (float64 copies): q, k L2-normalised
+    over their last axis, alpha = exp(-softplus(a)), beta = sigmoid(b)."""
+    lib = _load()
+    q = np.array(q, dtype=np.float64, order="C")
+    k = np.array(k, dtype=np.float64, order="C")
+    al = np.array(a, dtype=np.float64, order="C")
+    be = np.array(b, dtype=np.float64, order="C")
+    assert q.shape == k.shape and al.shape == be.shape
+    d = q.shape[-1]
+    st = lib.oracle_prepare_inputs_f64(_ptr(q), _ptr(k), q.size // d, d, _ptr(al), _ptr(be),
+                                       al.size)
+    assert st == OK
+    return q, k, al, be
 
 
 def conv_commit(x, state, slot, parent, accept, *, n_slots=None):

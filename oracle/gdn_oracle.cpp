@@ -22,6 +22,7 @@
 // equation term by term, in index order.  Arithmetic is in R = double (or
 // long double for tiny brute-force cases).  parity pinned by tests/test_oracle_pins.py.
 
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <vector>
@@ -204,6 +205,33 @@ int oracle_conv_commit_f64(const double* x, double* state, int64_t slot_stride,
     }
   }
   return status;
+}
+
+// Input preparation of a verify block from raw projections (the maps the
+// block's inputs are defined by): q and k L2-normalised per (node, q/k head)
+// (a zero vector stays zero), alpha = exp(-softplus(a)), beta = sigmoid(b),
+// with softplus(a) = log(1 + e^a) and sigmoid(b) = 1 / (1 + e^-b).
+// q, k [rows][d] in place; a, b -> alpha, beta [n] in place.
+int oracle_prepare_inputs_f64(double* q, double* k, int64_t rows, int32_t d, double* ab_alpha,
+                              double* ab_beta, int64_t n) {
+  if (rows < 0 || d <= 0 || n < 0) return ERR_INVALID_ARG;
+  for (int64_t r = 0; r < rows; ++r) {
+    for (double* x : {q + r * d, k + r * d}) {
+      double ss = 0;
+      for (int i = 0; i < d; ++i) ss += x[i] * x[i];
+      if (ss > 0) {
+        const double inv = 1.0 / std::sqrt(ss);
+        for (int i = 0; i < d; ++i) x[i] *= inv;
+      }
+    }
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    const double a = ab_alpha[i], b = ab_beta[i];
+    const double softplus = a > 0 ? a + std::log1p(std::exp(-a)) : std::log1p(std::exp(a));
+    ab_alpha[i] = std::exp(-softplus);
+    ab_beta[i] = 1.0 / (1.0 + std::exp(-b));
+  }
+  return OK;
 }
 
 // Index-table commit ("TokenSpeed hits 580 tok/s", section "How they actually

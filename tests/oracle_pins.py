@@ -578,6 +578,35 @@ def check_conv_history_commit():
     assert np.array_equal(s3[0][:, W - 3:], xb[0, :3].T)
 
 
+def check_input_preparation():
+    """Raw projections -> inputs: unit-norm q and k in the same direction (a
+    zero vector stays zero); alpha = exp(-softplus(a)) equals 1/(1+e^a) (the
+    closed form of the composition) and lies in (0, 1), falling with a;
+    beta = sigmoid(b) with beta(b) + beta(-b) = 1 and beta(0) = 1/2."""
+    rng = np.random.default_rng(43)
+    q = rng.standard_normal((3, 5, 2, 8)) * 3.0
+    k = rng.standard_normal((3, 5, 2, 8)) * 0.1
+    k[1, 2, 0] = 0.0
+    a = rng.standard_normal((3, 5, 4)) * 4.0
+    b = rng.standard_normal((3, 5, 4)) * 4.0
+    qn, kn, al, be = oracle.prepare_inputs(q, k, a, b)
+    for x, xn in ((q, qn), (k, kn)):
+        norms = np.linalg.norm(xn, axis=-1)
+        zero = np.linalg.norm(x, axis=-1) == 0
+        _close(norms[~zero], np.ones(int((~zero).sum())), 1e-14, "unit norm")
+        assert np.all(xn[zero] == 0), "a zero vector must stay zero"
+        cos = np.sum(xn * x, axis=-1)[~zero] / np.linalg.norm(x, axis=-1)[~zero]
+        _close(cos, np.ones_like(cos), 1e-14, "same direction")
+    _close(al, 1.0 / (1.0 + np.exp(a)), 1e-14, "alpha closed form")
+    assert np.all((al > 0) & (al < 1))
+    order = np.argsort(a.ravel())
+    assert np.all(np.diff(al.ravel()[order]) <= 0), "alpha must fall as a rises"
+    _, _, _, be_neg = oracle.prepare_inputs(q, k, a, -b)
+    _close(be + be_neg, np.ones_like(be), 1e-14, "sigmoid symmetry")
+    _, _, _, half = oracle.prepare_inputs(q, k, a, np.zeros_like(b))
+    _close(half, np.full_like(half, 0.5), 0.0, "sigmoid(0)")
+
+
 def block_form_reference(H0, K, V, Q, alpha, beta, parent):
     """The whole block at once (float64, one value head): with G(n) the sum of
     log alpha over the root-to-n path and the deltas solved first from
@@ -633,4 +662,5 @@ ALL_CHECKS = [
     check_tree_depth_and_validation, check_commit, check_chunked_equals_step,
     check_rounds_equal_sequential, check_block_form_equals_recurrence,
     check_replay_equals_persist, check_index_commit_equals_copy, check_conv_history_commit,
+    check_input_preparation,
 ]

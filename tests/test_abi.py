@@ -201,6 +201,24 @@ def test_conv_commit_host_checks(lib, change, want):
                                b["W"], b["status"], None) == want
 
 
+@pytest.mark.parametrize("change, want", [
+    (dict(N=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(dk=96), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(q=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(v=0x30008), gdn.GDN_ERR_MISALIGNED),
+    (dict(B=0), gdn.GDN_OK),
+])
+def test_prep_entry_points_host_checks(lib, change, want):
+    """The raw-projection variants run the same checks (calls that never launch)."""
+    a = _args(**change)
+    assert lib.gdn_verify_chain_prep(ctypes.byref(a), None) == want
+    assert lib.gdn_verify_tree_prep(ctypes.byref(a), ctypes.c_void_p(0x90000), None, None) == want
+    r = _args(snapshots=0, o=0, **change)
+    if "q" not in change:
+        assert lib.gdn_replay_accepted_prep(ctypes.byref(r), None, ctypes.c_void_p(0xA0000),
+                                            None) == want
+
+
 def _commit(lib, **kw):
     base = dict(snap=0x10000, sls=0, acc=0x20000, cache=0x30000, css=48 * 128 * 128, cls=0,
                 slot=None, n_slots=1, B=1, N=16, Hv=48, dk=128, dv=128, L=1, status=None)

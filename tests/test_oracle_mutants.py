@@ -41,6 +41,8 @@ MUTANTS = {
                             "for (int m = 0; m <= acc; ++m) path.push_back(m);\n"
                             "    } else {\n      for (int m = 0; m <= acc; ++m) path.push_back(m);\n"
                             "    }\n    for (int c = 0; c < C; ++c) {"),
+    "prep_gate_sign": ("ab_alpha[i] = std::exp(-softplus);", "ab_alpha[i] = std::exp(softplus - 2 * a);"),
+    "prep_skips_norm": ("for (int i = 0; i < d; ++i) x[i] *= inv;", "for (int i = 0; i < d; ++i) x[i] *= 1.0;"),
     "index_commit_wrong_stride": ("slot[b] = base + b * N + accept[b];",
                                   "slot[b] = base + b * (N - 1) + accept[b];"),
     "replay_chain_short": ("for (int m = 0; m <= acc; ++m) path.push_back(m);",
