@@ -14,20 +14,25 @@
 // oracle in the test suite.)  The prefill splits the work in two launches:
 //
 //   prep  (grid: chunk x q/k head, fully parallel): K K^T and Q K^T on tensor
-//         cores, the log-space cumulative decay, A, T = (I + A)^-1 by forward
-//         substitution, P; T and P are written to the caller's workspace as
-//         bf16 hi/lo pairs, with g and beta.
+//         cores (mma.sync), the log-space cumulative decay G, A and P, the
+//         inverse T = (I + A)^-1 by 16 x 16 blocks and P T; [T; P T] goes to
+//         the caller's workspace as bf16 hi/lo pairs in the tensor cores'
+//         128-byte swizzle, with G and beta.
 //   scan  (grid: value head x 3 column slabs of the state, sequential over
-//         chunks): per chunk K H and Q H, X, Delta = T X, O = g Q H + P Delta,
-//         H <- g_C H + K^T D'.  The state stays in fp32 mma accumulator
-//         fragments for the whole sequence; the next chunk's inputs are staged
-//         with cp.async while the current one is processed.
+//         chunks): per chunk three tcgen05 MMA groups with M = 128 into
+//         tensor memory, [K; Q] H, [T; P T] X and K^T D', with the
+//         elementwise steps between them (X, D', O = g Q H + P Delta,
+//         H <- g_C H + K^T D').  The fp32 state stays in registers for the
+//         whole sequence; the next chunk's K, Q, V and workspace block are
+//         staged by TMA while the current one is processed, and each chunk's
+//         output tile leaves by one TMA store.
 //
 // Precision: every tensor-core operand that is not exactly a bf16 input (the
-// state, X, Delta, D', T, P) is carried as a bf16 pair hi + lo and multiplied
-// as hi*hi + hi*lo + lo*hi (or hi + lo against an exact bf16 K / Q), which
-// keeps ~16 significant bits per operand; a single bf16 rounding of any of
-// them costs ~1% of the output RMS at this size.
+// state, X, D', T, P T and the fp32 operands of the prep's block products) is
+// carried as a bf16 pair hi + lo and multiplied as hi*hi + hi*lo + lo*hi (or
+// hi + lo against an exact bf16 K / Q), which keeps ~16 significant bits per
+// operand; a single bf16 rounding of any of them costs ~1% of the output RMS
+// at this size.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>

@@ -41,6 +41,12 @@
 // q, k, v, the gates and the parents are staged with cp.async while the
 // cached state loads.  Snapshots leave as 16-byte stores; a warp-wide store
 // covers RL rows x WC*4 contiguous bytes.
+//
+// Variants (template flags): SNAP16 persists binary16 snapshots (chains);
+// PREP takes raw q/k projections and gate pre-activations (the per-node
+// inverse norms scale the reduced sums and delta instead of every element);
+// a chain may persist nothing at all and commit by replay, for which
+// replay_kernel below re-runs the accepted path from the cached state.
 #include <cuda_fp16.h>
 
 #include "gdn_common.cuh"
