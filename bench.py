@@ -13,10 +13,13 @@ A step is one pass of the hot path over one batch of synthetic input:
   prefill8192  one 8192-token sequence, chunk 64: gdn_prefill_chunked
 
 Metric: node-heads/s (B x N x Hv per layer call, summed over the step; for the
-prefill, token-heads/s).  L2 (129 MB) is flushed by a 256 MiB write before
-every step and the flush is not timed: each step's kernels are bracketed by
-CUDA events on the launch stream, and the dominant kernel (the verify / the
-prefill) by its own pair, which gives the roofline figure.  Prints ONE JSON
+prefill, token-heads/s).  No step finds its data in L2 (129 MB): the batched
+and prefill steps are preceded by a 256 MiB write that is not timed; a
+single-sequence step (less than L2) instead rotates, back to back and
+unflushed, over enough independent copies of the workload to exceed twice L2.
+Each step's kernels are bracketed by CUDA events on the launch stream, and the
+dominant kernel (the verify / the prefill) by its own pair, which gives the
+roofline figure.  Prints ONE JSON
 line on rank 0.  Under torchrun every rank runs its own replica (independent
 sequences, no collective on the data path): weak scaling.
 
@@ -46,6 +49,17 @@ import synthetic  # noqa: E402
 
 HEADS = synthetic.HEADS
 FLUSH_BYTES = 256 << 20
+L2_BYTES = 129 * 10**6
+
+
+def hold_device(torch, host_s_per_step, steps):
+    """Queue a spin on the device long enough for the host to enqueue all the
+    timed steps behind it, so that the steps then run back to back: without
+    it a step shorter than its own Python launch cost would be timed with
+    the host's launch latency in it.  The spin precedes the first step's
+    start event and is not timed."""
+    seconds = min(0.5, 0.002 + 2.0 * host_s_per_step * steps)
+    torch.cuda._sleep(int(seconds * 2.2e9))
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -398,6 +412,39 @@ class VerifyCase:
                                 parent=self.parent, slot=self.slot,
                                 n_slots=self.inp["n_slots"])
 
+    def bind(self, gdn, stream):
+        """Marshal this layer's verify and replay once for the timed loop: the
+        same C-ABI entry points the binding's functions call, with the
+        argument struct built up front, so that a launch costs one ctypes call
+        instead of the binding's per-call checks (which would otherwise leave
+        the device waiting on the host between short steps)."""
+        import ctypes
+
+        lib = gdn.load()
+        d = self.dev
+        s = ctypes.c_void_p(stream.cuda_stream)
+
+        def ptr(t):
+            return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+        n_slots = self.inp["n_slots"]
+        self._va = gdn.make_verify_args(d["q"], d["k"], d["v"], d["alpha"], d["beta"], self.cache,
+                                        None if self.snap16 else self.snap, self.o,
+                                        slot=self.slot, n_slots=n_slots)
+        va = ctypes.byref(self._va)
+        if self.snap16:
+            snap = ptr(self.snap)
+            self.verify_c = lambda: lib.gdn_verify_chain_f16(va, snap, s)
+        elif self.parent is not None:
+            par = ptr(self.parent)
+            self.verify_c = lambda: lib.gdn_verify_tree(va, par, None, s)
+        else:
+            self.verify_c = lambda: lib.gdn_verify_chain(va, s)
+        self._ra = gdn.make_verify_args(None, d["k"], d["v"], d["alpha"], d["beta"], self.cache,
+                                        None, None, slot=self.slot, n_slots=n_slots)
+        ra, par, acc = ctypes.byref(self._ra), ptr(self.parent), ptr(d["accept"])
+        self.replay_c = lambda: lib.gdn_replay_accepted(ra, par, acc, s)
+
     def h2d(self):
         self.packed.copy_(self.host, non_blocking=True)
         return self.host.numel()
@@ -427,116 +474,205 @@ def run_ours(args, wl_name, world, rank, local):
     Hk, Hv, dk, dv = HEADS["Hk"], HEADS["Hv"], HEADS["dk"], HEADS["dv"]
     B, N = wl["B"], wl["N"]
     replay = wl.get("replay", False)
+    index = wl.get("index", False)
+    snap16 = wl.get("snap16", False)
     batched = wl_name.startswith("batched8x16")
     L = args.layers if (args.layers and batched) else wl["layers"]
+    vbytes = verify_bytes(B, N, Hk, Hv, dk, dv, tree=wl.get("tree", False), persist=not replay,
+                          snap_bytes=2 if snap16 else 4)
     if batched:
-        layers = []
-        for l in range(L):
-            inp = synthetic.batched8x16_layer(l)
-            if rank:
-                inp = dict(inp)  # replicas share shapes; the data is the same recipe
-            layers.append(VerifyCase(inp, torch, pinned=True, persist=not replay,
-                                     snap16=wl.get("snap16", False)))
-        # one cache for all layers: [layer][slot][Hv][dk][dv]; snapshots likewise
-        cache_all = torch.stack([c.cache for c in layers])
-        snap_all = None if replay else torch.empty(
-            (L, B, N, Hv, dk, dv), device="cuda",
-            dtype=torch.float16 if wl.get("snap16") else torch.float32)
-        for l, c in enumerate(layers):
-            c.cache = cache_all[l]
-            if not replay:
-                c.snap = snap_all[l]
-        commit_layers = L
+        # every step moves far more than L2; the flush before it is not timed
+        n_sets, flush_each = 1, True
     else:
-        inp = synthetic.tree22() if wl.get("tree") else synthetic.chain16()
-        layers = [VerifyCase(inp, torch, pinned=True, persist=not replay,
-                             snap16=wl.get("snap16", False))]
-        cache_all = layers[0].cache
-        snap_all = layers[0].snap
-        commit_layers = 1
-    accept = layers[0].dev["accept"]
-    slot = layers[0].slot
-    index = wl.get("index", False)
-    if index:
-        # the first verify of every layer reads the cache; afterwards each
-        # layer's snapshot region is its cache, addressed through one slot table
-        for c in layers:
-            c.verify(gdn)
-        slot_idx = torch.empty(B, dtype=torch.int32, device="cuda")
-        gdn.gdn_commit_index(accept, slot_idx, N=N)
-        for c in layers:
-            c.cache = c.snap.view(B * N, Hv, dk, dv)
-            c.slot = slot_idx
-            c.inp = dict(c.inp, n_slots=B * N)
-        torch.cuda.synchronize()
+        # a single-sequence step touches less than L2: the steps rotate over
+        # independent copies of the workload, together more than twice L2,
+        # back to back with no flush in between
+        step_bytes = vbytes + commit_bytes(B, Hv, dk, dv)
+        n_sets, flush_each = min(64, max(2, -(-2 * L2_BYTES // step_bytes))), False
 
-    def commit():
+    def make_set():
+        """Buffers of one copy of the workload and its step (verify, commit)."""
+        ws = argparse.Namespace()
+        if batched:
+            ws.layers = [VerifyCase(synthetic.batched8x16_layer(l), torch, pinned=True,
+                                    persist=not replay, snap16=snap16) for l in range(L)]
+            # one cache for all layers: [layer][slot][Hv][dk][dv]; snapshots likewise
+            ws.cache_all = torch.stack([c.cache for c in ws.layers])
+            ws.snap_all = None if replay else torch.empty(
+                (L, B, N, Hv, dk, dv), device="cuda",
+                dtype=torch.float16 if snap16 else torch.float32)
+            for l, c in enumerate(ws.layers):
+                c.cache = ws.cache_all[l]
+                if not replay:
+                    c.snap = ws.snap_all[l]
+        else:
+            inp = synthetic.tree22() if wl.get("tree") else synthetic.chain16()
+            ws.layers = [VerifyCase(inp, torch, pinned=True, persist=not replay, snap16=snap16)]
+            ws.cache_all = ws.layers[0].cache
+            ws.snap_all = ws.layers[0].snap
+        ws.accept = ws.layers[0].dev["accept"]
+        ws.slot = ws.layers[0].slot
         if index:
-            gdn.gdn_commit_index(accept, slot_idx, N=N)
+            # the first verify of every layer reads the cache; afterwards each
+            # layer's snapshot region is its cache, addressed through one slot table
+            for c in ws.layers:
+                c.verify(gdn)
+            ws.slot_idx = torch.empty(B, dtype=torch.int32, device="cuda")
+            gdn.gdn_commit_index(ws.accept, ws.slot_idx, N=N)
+            for c in ws.layers:
+                c.cache = c.snap.view(B * N, Hv, dk, dv)
+                c.slot = ws.slot_idx
+                c.inp = dict(c.inp, n_slots=B * N)
+            torch.cuda.synchronize()
+        ws.cache_init = None if index else ws.cache_all.clone()
+        return ws
+
+    def commit(ws):
+        if index:
+            gdn.gdn_commit_index(ws.accept, ws.slot_idx, N=N)
             return
         if replay:
             # checkpoint and replay: the accepted prefix of every layer again
-            for c in layers:
+            for c in ws.layers:
                 c.replay(gdn)
             return
-        gdn.gdn_commit_accepted(snap_all, accept, cache_all, B=B, N=N, Hv=Hv, dk=dk, dv=dv,
-                                n_layers=commit_layers, snap_layer_stride=B * N * Hv * dk * dv,
-                                cache_layer_stride=B * Hv * dk * dv, slot=slot, n_slots=B)
+        gdn.gdn_commit_accepted(ws.snap_all, ws.accept, ws.cache_all, B=B, N=N, Hv=Hv, dk=dk,
+                                dv=dv, n_layers=len(ws.layers),
+                                snap_layer_stride=B * N * Hv * dk * dv,
+                                cache_layer_stride=B * Hv * dk * dv, slot=ws.slot, n_slots=B)
 
-    cache_init = None if index else cache_all.clone()
-
-    def step(ev=None):
-        """verify every layer, then commit; ev = (start, after_verify, end) events."""
+    def step(ws, ev=None):
+        """verify every layer, then commit, through the binding's functions;
+        ev = (start, after_verify, end) events."""
         if ev is not None:
             ev[0].record(stream)
-        for c in layers:
+        for c in ws.layers:
             c.verify(gdn)
         if ev is not None:
             ev[1].record(stream)
-        commit()
+        commit(ws)
         if ev is not None:
             ev[2].record(stream)
 
+    def bind_set(ws):
+        """The set's step as pre-marshalled C-ABI calls (see VerifyCase.bind)."""
+        import ctypes
+
+        lib = gdn.load()
+        s = ctypes.c_void_p(stream.cuda_stream)
+        for c in ws.layers:
+            c.bind(gdn, stream)
+        if index:
+            acc, sl = ctypes.c_void_p(ws.accept.data_ptr()), ctypes.c_void_p(ws.slot_idx.data_ptr())
+            ws.commit_c = [lambda: lib.gdn_commit_index(acc, B, N, 0, sl, None, s)]
+        elif replay:
+            ws.commit_c = [c.replay_c for c in ws.layers]
+        else:
+            fn = lib.gdn_commit_accepted_f16 if snap16 else lib.gdn_commit_accepted
+            cargs = (ctypes.c_void_p(ws.snap_all.data_ptr()), B * N * Hv * dk * dv,
+                     ctypes.c_void_p(ws.accept.data_ptr()),
+                     ctypes.c_void_p(ws.cache_all.data_ptr()), Hv * dk * dv, B * Hv * dk * dv,
+                     ctypes.c_void_p(ws.slot.data_ptr()), B, B, N, Hv, dk, dv,
+                     len(ws.layers), None, s)
+            ws.commit_c = [lambda: fn(*cargs)]
+        ws.verify_c = [c.verify_c for c in ws.layers]
+
+    def step_c(ws, ev=None):
+        """step() through the pre-marshalled calls; any non-zero status raises."""
+        if ev is not None:
+            ev[0].record(stream)
+        for f in ws.verify_c:
+            if f():
+                raise RuntimeError("verify launch failed")
+        if ev is not None:
+            ev[1].record(stream)
+        for f in ws.commit_c:
+            if f():
+                raise RuntimeError("commit launch failed")
+        if ev is not None:
+            ev[2].record(stream)
+
+    sets = [make_set() for _ in range(n_sets)]
+    for ws in sets:
+        bind_set(ws)
+    layers = sets[0].layers
     launches_per_step = len(layers) * 2 if replay else len(layers) + 1
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        step()
+    n_warm = max(args.warmup, n_sets)
+    for i in range(n_warm):  # the binding's own functions, then the bound calls
+        step(sets[i % n_sets])
+    th = time.perf_counter()
+    for i in range(n_warm):
+        if flush_each:
+            flush.fill_(1.0)
+        step_c(sets[i % n_sets])
+    host_s = (time.perf_counter() - th) / n_warm
     torch.cuda.synchronize()
 
     gpu_id = gpu_uuid(torch, local)
     sampler = ClockSampler(gpu_id)
     sampler.start()
     time.sleep(0.25)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier(world)
+    if not flush_each:
+        flush.fill_(0.0)  # the first timed step starts from an L2 without its data
     torch.cuda.synchronize()
     t0 = time.time()
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        step(evs[i])
-    torch.cuda.synchronize()
+    hold_device(torch, host_s, args.steps)
+    if flush_each:
+        # the flush between steps is excluded: one event pair per step phase
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            step_c(sets[i % n_sets], evs[i])
+        torch.cuda.synchronize()
+        step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+        verify_ms = [e[0].elapsed_time(e[1]) / len(layers) for e in evs]
+        total_ms = sum(step_ms)
+    else:
+        # back-to-back steps between one event pair, as a serving loop issues them
+        e_run = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e_run[0].record(stream)
+        for i in range(args.steps):
+            step_c(sets[i % n_sets])
+        e_run[1].record(stream)
+        torch.cuda.synchronize()
+        total_ms = e_run[0].elapsed_time(e_run[1])
+        step_ms = None
+        # the dominant kernel on its own: verify launches back to back over the
+        # same rotating copies (every launch again misses L2), one event pair
+        k_roof = min(args.steps, 1000)
+        hold_device(torch, host_s, k_roof)
+        e_roof = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e_roof[0].record(stream)
+        for i in range(k_roof):
+            for f in sets[i % n_sets].verify_c:
+                if f():
+                    raise RuntimeError("verify launch failed")
+        e_roof[1].record(stream)
+        torch.cuda.synchronize()
+        verify_ms = [e_roof[0].elapsed_time(e_roof[1]) / (k_roof * len(layers))]
     barrier(world)
     t1 = time.time()
     time.sleep(0.25)
     sampler.stop()
-    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
-    verify_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    total_ms = sum(step_ms)
     total_ms = max_over_ranks(total_ms, world)
 
     # end to end through the public API: host inputs -> device -> verify/commit -> host o
-    if cache_init is not None:
-        cache_all.copy_(cache_init)
+    for ws in sets:
+        if ws.cache_init is not None:
+            ws.cache_all.copy_(ws.cache_init)
     e2e_steps = min(args.steps, 200)
     e2e_s = 0.0
     h2d = d2h = 0
     for i in range(e2e_steps + 3):
+        ws = sets[i % n_sets]
         flush.fill_(float(i))
         torch.cuda.synchronize()
         ta = time.perf_counter()
-        h2d = sum(c.h2d() for c in layers)
-        step()
-        d2h = sum(c.d2h() for c in layers)
+        h2d = sum(c.h2d() for c in ws.layers)
+        step(ws)
+        d2h = sum(c.d2h() for c in ws.layers)
         torch.cuda.synchronize()
         if i >= 3:
             e2e_s += time.perf_counter() - ta
@@ -545,9 +681,7 @@ def run_ours(args, wl_name, world, rank, local):
     node_heads = B * N * Hv * len(layers)
     value = job_throughput(node_heads, args.steps, total_ms, world)
     hbm, bf16, peak_kind = measured_peaks()
-    vbytes = verify_bytes(B, N, Hk, Hv, dk, dv, tree=wl.get("tree", False), persist=not replay,
-                          snap_bytes=2 if wl.get("snap16") else 4)
-    launch_ms = statistics.mean(verify_ms) / len(layers)
+    launch_ms = statistics.mean(verify_ms)
     achieved = vbytes / (launch_ms / 1e3) / 1e9
     clocks = sampler.summary(t0, t1)
     if rank != 0:
@@ -570,12 +704,21 @@ def run_ours(args, wl_name, world, rank, local):
             "B": B, "N": N, "Hk": Hk, "Hv": Hv, "dk": dk, "dv": dv, "layers": len(layers),
             "inputs": "bf16 q/k/v (L2-normalised q/k), fp32 alpha/beta/state/outputs",
             "node_heads_per_step": node_heads,
-            "l2": "flushed by a 256 MiB write before every step; flush not timed",
-            "timing": "CUDA events around each step's kernels on the launch stream",
+            "l2": ("flushed by a 256 MiB write before every step; flush not timed"
+                   if flush_each else
+                   f"inputs larger than L2: the steps rotate, back to back and unflushed, over "
+                   f"{n_sets} independent copies of the workload ({n_sets} x "
+                   f"{(vbytes + commit_bytes(B, Hv, dk, dv)) / 1e6:.1f} MB > 2 x 129 MB)"),
+            "timing": ("CUDA events on the launch stream around each step's verify and "
+                       "commit phases" if flush_each else
+                       "CUDA events on the launch stream around the K back-to-back steps; the "
+                       "verify kernel alone from a second back-to-back run of verify launches"),
+            "launch": "programmatic dependent launch (each kernel waits on its predecessor "
+                      "before any global-memory access)",
             "parallelism": f"replicas x{world}, no collective",
-            "verify_ms_p50": statistics.median(verify_ms) / len(layers),
-            "step_ms_p10": float(np.percentile(step_ms, 10)),
-            "step_ms_p90": float(np.percentile(step_ms, 90)),
+            "verify_ms_per_launch": launch_ms,
+            **({"step_ms_p10": float(np.percentile(step_ms, 10)),
+                "step_ms_p90": float(np.percentile(step_ms, 90))} if step_ms else {}),
         },
         "roofline": {
             "bound": "hbm",
@@ -623,9 +766,11 @@ def run_prefill(args, gdn, torch, flush, world, rank, local):
         if ev is not None:
             ev[1].record(stream)
 
+    th = time.perf_counter()
     for _ in range(args.warmup):
         flush.fill_(1.0)
         step()
+    host_s = (time.perf_counter() - th) / max(1, args.warmup)
     torch.cuda.synchronize()
     sampler = ClockSampler(gpu_uuid(torch, local))
     sampler.start()
@@ -635,6 +780,7 @@ def run_prefill(args, gdn, torch, flush, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
+    hold_device(torch, host_s, steps)
     for i in range(steps):
         flush.fill_(float(i))
         step(evs[i])

@@ -10,16 +10,22 @@ namespace {
 bool ok_ptr16(const void* p) { return p != nullptr && gdn::aligned16(p); }
 bool ok_ptr4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-// Default slab shape for the verify kernel: columns per block and row warps.
-// Small problems (few heads) want more, thinner blocks to fill 152 SMs; the
-// state of a lane stays at <= 64 registers.
-void auto_tile(int dk, int dv, int B, int Hv, int* wc, int* nw) {
-  (void)dv;
-  (void)B;
-  (void)Hv;
+// Block count up to which the verify slab is split over two row warps
+// (4 blocks per SM on 152 SMs).
+constexpr int64_t kTwoWarpBlocks = 608;
+
+// Default slab shape for the verify and replay kernels: 16 columns per block,
+// and, for chains, two warps splitting the d_k rows when there are too few
+// blocks to give every SM sub-partition a warp of its own (one warp walking
+// the nodes alone is latency-bound); with many blocks, one warp per block.
+// A tree keeps one warp: its stash traffic and per-branch reductions gain
+// nothing from the split.  A replay takes the chain's shape, so that a chain
+// committed by replay repeats the verify arithmetic bit for bit.
+void auto_tile(int dk, int dv, int B, int Hv, bool tree, int* wc, int* nw) {
   *wc = 16;
   *nw = 1;
-  if (dk != 128) *nw = 1;
+  const int64_t blocks = (int64_t)(dv / 16) * Hv * B;
+  if (!tree && (dk == 128 || dk == 64) && blocks <= kTwoWarpBlocks) *nw = 2;
 }
 
 int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, bool tree,
@@ -54,9 +60,10 @@ int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
     if (!ok_ptr4(p)) return GDN_ERR_MISALIGNED;
 
   int wc = 0, nw = 0;
-  auto_tile(a->dk, a->dv, a->B, a->Hv, &wc, &nw);
+  auto_tile(a->dk, a->dv, a->B, a->Hv, tree, &wc, &nw);
   if (a->tile_cols != 0) wc = a->tile_cols;
   if (a->row_warps != 0) nw = a->row_warps;
+  else if (!gdn::verify_tile_supported(a->dk, wc, nw)) nw = 1;  // automatic, for a forced width
   if (!gdn::verify_tile_supported(a->dk, wc, nw) || a->dv % wc != 0) return GDN_ERR_UNSUPPORTED;
   return gdn::launch_verify(a, tree ? parent : nullptr, tree ? depth_out : nullptr, wc, nw,
                             static_cast<cudaStream_t>(stream), snap16, prep);
@@ -110,11 +117,12 @@ int replay_common(const gdn_verify_args* a, const int32_t* parent, const int32_t
   for (const void* p : need4)
     if (!ok_ptr4(p)) return GDN_ERR_MISALIGNED;
   int wc = 0, nw = 0;
-  auto_tile(a->dk, a->dv, a->B, a->Hv, &wc, &nw);
+  auto_tile(a->dk, a->dv, a->B, a->Hv, false, &wc, &nw);
   if (a->tile_cols != 0) wc = a->tile_cols;
   if (a->row_warps != 0) nw = a->row_warps;
+  else if (!gdn::verify_tile_supported(a->dk, wc, nw)) nw = 1;  // automatic, for a forced width
   if (!gdn::verify_tile_supported(a->dk, wc, nw) || a->dv % wc != 0) return GDN_ERR_UNSUPPORTED;
-  return gdn::launch_replay(a, parent, accept, wc, static_cast<cudaStream_t>(stream), prep);
+  return gdn::launch_replay(a, parent, accept, wc, nw, static_cast<cudaStream_t>(stream), prep);
 }
 
 }  // namespace

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kThreads)
 commit_kernel(const void* __restrict__ snap, int64_t snap_layer4, const int32_t* accept,
               float4* __restrict__ cache, int64_t slot4, int64_t layer4, const int32_t* slot,
               int n_slots, int N, int64_t run4, int32_t* status) {
+  pdl_enter();
   const int b = blockIdx.y, l = blockIdx.z;
   const int a = __ldg(accept + b);
   const int s = slot != nullptr ? __ldg(slot + b) : b;
@@ -69,6 +70,7 @@ commit_kernel(const void* __restrict__ snap, int64_t snap_layer4, const int32_t*
 // actually got there": move pointers, not data).  One thread per sequence.
 __global__ void commit_index_kernel(const int32_t* accept, int B, int N, int base_slot,
                                     int32_t* slot, int32_t* status) {
+  pdl_enter();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int a = __ldg(accept + b);
@@ -94,6 +96,7 @@ __global__ void __launch_bounds__(256)
 conv_commit_kernel(const E* __restrict__ x, E* __restrict__ state, int64_t slot_stride,
                    const int32_t* slot, int n_slots, const int32_t* parent,
                    const int32_t* accept, int N, int C, int W, int32_t* status) {
+  pdl_enter();
   __shared__ int s_tail[kMaxConvW];
   __shared__ int s_count;
   const int b = blockIdx.y;
@@ -159,23 +162,19 @@ int launch_conv_commit(const void* x, bool bf16, void* state, int64_t slot_strid
                        cudaStream_t stream) {
   const dim3 grid((unsigned)((C + 255) / 256), B);
   if (bf16)
-    conv_commit_kernel<uint16_t><<<grid, 256, 0, stream>>>(
-        static_cast<const uint16_t*>(x), static_cast<uint16_t*>(state), slot_stride, slot,
-        n_slots, parent, accept, N, C, W, status);
-  else
-    conv_commit_kernel<uint32_t><<<grid, 256, 0, stream>>>(
-        static_cast<const uint32_t*>(x), static_cast<uint32_t*>(state), slot_stride, slot,
-        n_slots, parent, accept, N, C, W, status);
-  return launch_status();
+    return launch_pdl(conv_commit_kernel<uint16_t>, grid, dim3(256), 0, stream,
+                      static_cast<const uint16_t*>(x), static_cast<uint16_t*>(state),
+                      slot_stride, slot, n_slots, parent, accept, N, C, W, status);
+  return launch_pdl(conv_commit_kernel<uint32_t>, grid, dim3(256), 0, stream,
+                    static_cast<const uint32_t*>(x), static_cast<uint32_t*>(state), slot_stride,
+                    slot, n_slots, parent, accept, N, C, W, status);
 }
 
 int launch_commit_index(const int32_t* accept, int B, int N, int base_slot, int32_t* slot,
                         int32_t* status, cudaStream_t stream) {
   const int threads = 128;
-  commit_index_kernel<<<(B + threads - 1) / threads, threads, 0, stream>>>(accept, B, N,
-                                                                           base_slot, slot,
-                                                                           status);
-  return launch_status();
+  return launch_pdl(commit_index_kernel, dim3((B + threads - 1) / threads), dim3(threads), 0,
+                    stream, accept, B, N, base_slot, slot, status);
 }
 
 int launch_commit(const void* snap, bool src16, int64_t snap_layer_stride, const int32_t* accept,
@@ -188,14 +187,14 @@ int launch_commit(const void* snap, bool src16, int64_t snap_layer_stride, const
   if (gx > 0x7fffffff) return GDN_ERR_UNSUPPORTED;
   const dim3 grid((unsigned)gx, B, n_layers);
   if (src16)
-    commit_kernel<true><<<grid, kThreads, 0, stream>>>(
-        snap, snap_layer_stride / 4, accept, reinterpret_cast<float4*>(cache),
-        cache_slot_stride / 4, cache_layer_stride / 4, slot, n_slots, N, run4, status);
-  else
-    commit_kernel<false><<<grid, kThreads, 0, stream>>>(
-        snap, snap_layer_stride / 4, accept, reinterpret_cast<float4*>(cache),
-        cache_slot_stride / 4, cache_layer_stride / 4, slot, n_slots, N, run4, status);
-  return launch_status();
+    return launch_pdl(commit_kernel<true>, grid, dim3(kThreads), 0, stream, snap,
+                      snap_layer_stride / 4, accept, reinterpret_cast<float4*>(cache),
+                      cache_slot_stride / 4, cache_layer_stride / 4, slot, n_slots, N, run4,
+                      status);
+  return launch_pdl(commit_kernel<false>, grid, dim3(kThreads), 0, stream, snap,
+                    snap_layer_stride / 4, accept, reinterpret_cast<float4*>(cache),
+                    cache_slot_stride / 4, cache_layer_stride / 4, slot, n_slots, N, run4,
+                    status);
 }
 
 }  // namespace gdn

@@ -62,4 +62,41 @@ inline int launch_status() {
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialisation allowed (launch_pdl), so that the
+// next kernel on the stream is set up while this one runs.  Each kernel
+// starts with pdl_enter(): it waits until the previous kernel has completed
+// and its memory operations are visible, before any global-memory access of
+// its own, so stream order holds for every read and write; then it lets the
+// next kernel begin launching.  The next kernel's blocks thus wait, resident,
+// for this one to finish, and at most one kernel ahead is waiting (a trigger
+// before the wait would let a whole queue of launches pile up on the SMs,
+// which measured slower).  After an operation that is not such a kernel (a
+// copy, an event, a kernel launched without the attribute) the wait returns
+// at once.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GDN_ERR_CUDA;
+  }
+  return launch_status();
+}
+
 }  // namespace gdn

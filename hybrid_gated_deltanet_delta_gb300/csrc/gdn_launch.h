@@ -19,7 +19,7 @@ int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
 
 // Replay of the accepted path from the cached state, written back in place.
 int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept, int wc,
-                  cudaStream_t stream, bool prep = false);
+                  int nw, cudaStream_t stream, bool prep = false);
 
 // src16: the snapshots are binary16 (widened exactly into the fp32 cache).
 int launch_commit(const void* snap, bool src16, int64_t snap_layer_stride, const int32_t* accept,

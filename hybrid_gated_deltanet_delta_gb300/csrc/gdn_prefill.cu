@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
 prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
             const float* __restrict__ alpha, const float* __restrict__ beta, int T, int Hk,
             int Hv, char* __restrict__ ws) {
+  pdl_enter();
   extern __shared__ __align__(16) char smem[];
   char* sk = smem + PREP_K;
   char* sq = smem + PREP_Q;
@@ -549,6 +550,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
             const __grid_constant__ CUtensorMap tm_v48, const __grid_constant__ CUtensorMap tm_v32,
             const __grid_constant__ CUtensorMap tm_o48, const __grid_constant__ CUtensorMap tm_o32,
             float* __restrict__ state, const char* __restrict__ ws, int T, int Hk, int Hv) {
+  pdl_enter();
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int sl = blockIdx.x, h = blockIdx.y, hk = h / (Hv / Hk);
@@ -877,15 +879,13 @@ int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const
       cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SCAN_SMEM) != cudaSuccess)
     return GDN_ERR_CUDA;
-  prep_kernel<<<dim3(n_chunks, Hk), PREP_THREADS, prep_smem, stream>>>(
-      static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), alpha, beta, T, Hk, Hv,
-      static_cast<char*>(workspace));
-  st = launch_status();
+  st = launch_pdl(prep_kernel, dim3(n_chunks, Hk), dim3(PREP_THREADS), prep_smem, stream,
+                  static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), alpha, beta,
+                  T, Hk, Hv, static_cast<char*>(workspace));
   if (st != GDN_OK) return st;
-  scan_kernel<<<dim3(3, Hv), SCAN_THREADS, SCAN_SMEM, stream>>>(
-      tm_k, tm_q, tm_v48, tm_v32, tm_o48, tm_o32, state, static_cast<const char*>(workspace), T,
-      Hk, Hv);
-  return launch_status();
+  return launch_pdl(scan_kernel, dim3(3, Hv), dim3(SCAN_THREADS), SCAN_SMEM, stream, tm_k, tm_q,
+                    tm_v48, tm_v32, tm_o48, tm_o32, state, static_cast<const char*>(workspace),
+                    T, Hk, Hv);
 }
 
 }  // namespace gdn

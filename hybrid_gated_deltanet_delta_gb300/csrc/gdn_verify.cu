@@ -57,25 +57,75 @@ namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
 
-template <int DK, int WC>
+template <int DK, int WC, int NW = 1>
 struct Shape {
-  static constexpr int CG = WC / 4;   // 16-byte column groups per row of the slab
-  static constexpr int RL = 32 / CG;  // row lanes per warp
-  static constexpr int R = DK / RL;   // rows per lane
+  static constexpr int CG = WC / 4;        // 16-byte column groups per row of the slab
+  static constexpr int RL = 32 / CG;       // row lanes per warp
+  static constexpr int R = DK / (RL * NW); // rows per lane (NW warps split the rows)
   static_assert(WC % 4 == 0 && 32 % CG == 0 && RL >= 2, "slab width");
-  static_assert(R >= 1 && R * RL == DK, "row split");
+  static_assert(R >= 1 && R * RL * NW == DK, "row split");
 };
+
+// Exchange slots for the cross-warp column sums: [2 buffers][NW][CG][XS]
+constexpr int XS = 12;
+
+__host__ __device__ constexpr int xchg_bytes(int nw, int WC) {
+  return nw > 1 ? 2 * nw * (WC / 4) * XS * 4 : 0;
+}
+
+// Barrier over the NW warps of a block.
+template <int NW>
+__device__ __forceinline__ void block_sync() {
+  if constexpr (NW == 1) __syncwarp();
+  else __syncthreads();
+}
+
+template <int NW>
+__device__ __forceinline__ bool block_all(bool x) {
+  if constexpr (NW == 1) return __all_sync(0xffffffffu, x);
+  else return __syncthreads_and(x) != 0;
+}
+
+// x[e] <- the sum of x[e] over the NW row warps of the block, added in warp
+// order so that every warp gets the same bits.  Each warp's value must already
+// be its full warp sum (all row lanes agree).  Exchanges alternate between two
+// buffers, so one barrier per exchange suffices: a warp can only refill a
+// buffer after the barrier of the next exchange, which every warp reaches
+// after reading that buffer.
+template <int NW, int CG, int NV>
+__device__ __forceinline__ void warps_sum(float (&x)[NV], float* sx, int& xc, int wi, int cg,
+                                          int rl) {
+  if constexpr (NW > 1) {
+    static_assert(NV <= XS, "exchange slot");
+    float* buf = sx + (xc & 1) * (NW * CG * XS);
+    ++xc;
+    if (rl == 0) {
+#pragma unroll
+      for (int e = 0; e < NV; ++e) buf[(wi * CG + cg) * XS + e] = x[e];
+    }
+    __syncthreads();
+    float acc[NV];
+#pragma unroll
+    for (int e = 0; e < NV; ++e) acc[e] = buf[cg * XS + e];
+#pragma unroll
+    for (int w = 1; w < NW; ++w)
+#pragma unroll
+      for (int e = 0; e < NV; ++e) acc[e] += buf[(w * CG + cg) * XS + e];
+#pragma unroll
+    for (int e = 0; e < NV; ++e) x[e] = acc[e];
+  }
+}
 
 __host__ __device__ constexpr int round16(int x) { return (x + 15) & ~15; }
 
 // Shared-memory plan in bytes; every array starts on a 16-byte boundary.
 // Tree blocks add per-node tables and `pool` stash slots of dk x WC floats.
 struct SmemPlan {
-  int q, k, v, a, b, par, src, stash, last, pool, inv, total;
+  int q, k, v, a, b, par, src, stash, last, pool, inv, x, total;
 };
 
 __host__ __device__ inline SmemPlan smem_plan(int N, int DK, int WC, int esz, bool tree,
-                                              int pool) {
+                                              int pool, int nw = 1) {
   SmemPlan s{};
   s.q = 0;
   s.k = s.q + round16(N * DK * esz);
@@ -89,14 +139,15 @@ __host__ __device__ inline SmemPlan smem_plan(int N, int DK, int WC, int esz, bo
   s.last = s.stash + t;
   s.pool = s.last + t;
   s.inv = s.pool + (tree ? pool * DK * WC * 4 : 0);  // 1/|q_n|, 1/|k_n| (input preparation)
-  s.total = s.inv + 2 * round16(N * 4);
+  s.x = s.inv + 2 * round16(N * 4);                   // cross-warp sums (NW > 1)
+  s.total = s.x + xchg_bytes(nw, WC);
   return s;
 }
 
 // Stash slots per tree block: as many as fit next to the staged inputs while
 // three blocks still share an SM (at least 1, at most 12).
-inline int tree_pool_slots(int N, int DK, int WC, int esz) {
-  const SmemPlan base = smem_plan(N, DK, WC, esz, true, 0);
+inline int tree_pool_slots(int N, int DK, int WC, int esz, int nw) {
+  const SmemPlan base = smem_plan(N, DK, WC, esz, true, 0, nw);
   const int budget = 74 * 1024 - base.total;
   int slots = budget / (DK * WC * 4);
   return slots < 1 ? 1 : (slots > 12 ? 12 : slots);
@@ -121,11 +172,11 @@ struct VerifyParams {
 };
 
 // Start copying n_rows rows of row_bytes bytes (row r at src + r*src_stride)
-// to dst + r*row_bytes with 16-byte cp.async.
+// to dst + r*row_bytes with 16-byte cp.async, thread t of nt.
 __device__ __forceinline__ void stage_rows(char* dst, const char* src, int64_t src_stride,
-                                           int n_rows, int row_bytes, int lane) {
+                                           int n_rows, int row_bytes, int t, int nt) {
   const int per_row = row_bytes / 16;
-  for (int idx = lane; idx < n_rows * per_row; idx += 32) {
+  for (int idx = t; idx < n_rows * per_row; idx += nt) {
     const int r = idx / per_row, c = idx - r * per_row;
     cp_async16(dst + r * row_bytes + c * 16, src + r * src_stride + c * 16);
   }
@@ -170,12 +221,12 @@ __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
 // Input preparation from raw projections: 1/|x| of `rows` staged rows of DK
 // elements (bf16 or fp32) into inv[] (0 for a zero row, which then stays
-// zero), one row per lane; and the gates alpha = exp(-softplus(a)) =
+// zero), one row per thread; and the gates alpha = exp(-softplus(a)) =
 // 1/(1 + e^a), beta = sigmoid(b) = 1/(1 + e^-b) in place.
 template <int DK>
 __device__ __forceinline__ void prep_rows(const char* rows_base, int rows, bool bf16, float* inv,
-                                          int lane) {
-  for (int r = lane; r < rows; r += 32) {
+                                          int t, int nt) {
+  for (int r = t; r < rows; r += nt) {
     float ss = 0.f;
     if (bf16) {
       const uint4* s = reinterpret_cast<const uint4*>(rows_base + (size_t)r * DK * 2);
@@ -201,22 +252,24 @@ __device__ __forceinline__ void prep_rows(const char* rows_base, int rows, bool 
   }
 }
 
-__device__ __forceinline__ void prep_gates(float* a, float* b, int n_rows, int lane) {
-  for (int r = lane; r < n_rows; r += 32) {
+__device__ __forceinline__ void prep_gates(float* a, float* b, int n_rows, int t, int nt) {
+  for (int r = t; r < n_rows; r += nt) {
     a[r] = 1.f / (1.f + __expf(a[r]));
     b[r] = 1.f / (1.f + __expf(-b[r]));
   }
 }
 
-template <int DK, int WC, bool TREE, bool SNAP16, bool PREP>
-__global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
-  using S = Shape<DK, WC>;
+template <int DK, int WC, int NW, bool TREE, bool SNAP16, bool PREP>
+__global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
+  pdl_enter();
+  using S = Shape<DK, WC, NW>;
   constexpr int R = S::R;
+  constexpr int NT = 32 * NW;
   extern __shared__ __align__(16) char smem[];
   const int N = p.N;
   const bool bf16 = p.bf16 != 0;
   const int esz = bf16 ? 2 : 4;
-  const SmemPlan pl = smem_plan(N, DK, WC, esz, TREE, p.pool);
+  const SmemPlan pl = smem_plan(N, DK, WC, esz, TREE, p.pool, NW);
   char* sq = smem + pl.q;
   char* sk = smem + pl.k;
   char* sv = smem + pl.v;
@@ -229,14 +282,16 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
   float* pool = reinterpret_cast<float*>(smem + pl.pool);
   float* sinvq = reinterpret_cast<float*>(smem + pl.inv);
   float* sinvk = sinvq + round16(N * 4) / 4;
+  float* sx = reinterpret_cast<float*>(smem + pl.x);
+  int xc = 0;  // cross-warp exchanges so far
 
-  const int lane = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
   const int cg = lane % S::CG, rl = lane / S::CG;
   const int j0 = blockIdx.x * WC, h = blockIdx.y, b = blockIdx.z;
   const int hk = h / (p.Hv / p.Hk);
   const bool lead = blockIdx.x == 0 && blockIdx.y == 0;  // per-sequence reporting
   const int dv = p.dv;
-  const int row0 = rl * R;
+  const int row0 = wi * (DK / NW) + rl * R;
 
   // ---- stage q, k, v, gates, parents (independent of the slot: issued first)
   {
@@ -244,10 +299,10 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
     const char* qb = static_cast<const char*>(p.q) + ((node0 * p.Hk + hk) * DK) * esz;
     const char* kb = static_cast<const char*>(p.k) + ((node0 * p.Hk + hk) * DK) * esz;
     const char* vb = static_cast<const char*>(p.v) + ((node0 * p.Hv + h) * dv + j0) * esz;
-    stage_rows(sk, kb, (int64_t)p.Hk * DK * esz, N, DK * esz, lane);
-    stage_rows(sq, qb, (int64_t)p.Hk * DK * esz, N, DK * esz, lane);
-    stage_rows(sv, vb, (int64_t)p.Hv * dv * esz, N, WC * esz, lane);
-    for (int n = lane; n < N; n += 32) {
+    stage_rows(sk, kb, (int64_t)p.Hk * DK * esz, N, DK * esz, tid, NT);
+    stage_rows(sq, qb, (int64_t)p.Hk * DK * esz, N, DK * esz, tid, NT);
+    stage_rows(sv, vb, (int64_t)p.Hv * dv * esz, N, WC * esz, tid, NT);
+    for (int n = tid; n < N; n += NT) {
       cp_async4(sa + n, p.alpha + (node0 + n) * p.Hv + h);
       cp_async4(sb + n, p.beta + (node0 + n) * p.Hv + h);
       if constexpr (TREE) cp_async4(spar + n, p.parent + node0 + n);
@@ -257,7 +312,7 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
   const int sl = p.slot != nullptr ? __ldg(p.slot + b) : b;
   if (sl < 0 || sl >= p.n_slots) {
     cp_async_wait_all();
-    if (lead && lane == 0) report(p.status, GDN_ERR_SLOT_RANGE);
+    if (lead && tid == 0) report(p.status, GDN_ERR_SLOT_RANGE);
     return;
   }
 
@@ -275,32 +330,31 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
     }
   }
   cp_async_wait_all();
-  __syncwarp();
+  block_sync<NW>();
 
   if constexpr (PREP) {
     // raw projections: norms of q and k, gates from their pre-activations
-    prep_rows<DK>(sq, N, bf16, sinvq, lane);
-    prep_rows<DK>(sk, N, bf16, sinvk, lane);
-    prep_gates(sa, sb, N, lane);
-    __syncwarp();
+    prep_rows<DK>(sq, N, bf16, sinvq, tid, NT);
+    prep_rows<DK>(sk, N, bf16, sinvk, tid, NT);
+    prep_gates(sa, sb, N, tid, NT);
+    block_sync<NW>();
   }
 
   if constexpr (TREE) {
     // parent[0] == -1, 0 <= parent[n] < n; the block leaves otherwise
     bool ok = true;
-    for (int n = lane; n < N; n += 32) {
+    for (int n = tid; n < N; n += NT) {
       const int pp = spar[n];
       ok = ok && (n == 0 ? pp == -1 : (pp >= 0 && pp < n));
     }
-    if (!__all_sync(FULL, ok)) {
-      if (lead && lane == 0) report(p.status, GDN_ERR_BAD_TREE);
+    if (!block_all<NW>(ok)) {
+      if (lead && tid == 0) report(p.status, GDN_ERR_BAD_TREE);
       return;
     }
   }
 
-  if constexpr (TREE) {
-    // ---- stash plan (greedy over nodes in index order; runs while the
-    //      cached state is still on its way)
+  if (TREE && wi == 0) {
+    // ---- stash plan (greedy over nodes in index order), by the first warp
     for (int n = lane; n < N; n += 32) slast[n] = -1;
     __syncwarp();
     for (int f = lane; f < N; f += 32) {
@@ -344,8 +398,8 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
         sstash[n] = mine;
       }
     }
-    __syncwarp();
   }
+  if constexpr (TREE) block_sync<NW>();
 
   // ---- u_0 = H0^T k_0
   float kn[R];  // k of the current node
@@ -363,6 +417,7 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
     for (int off = S::CG; off < 32; off <<= 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
+    warps_sum<NW, S::CG>(u, sx, xc, wi, cg, rl);
     if constexpr (PREP) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) u[c] *= sinvk[0];
@@ -374,9 +429,11 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
   float* snap_h = p.snap == nullptr ? nullptr : p.snap + lane_off;
   __half* snap16_h = SNAP16 ? p.snap16 + lane_off : nullptr;
   float* o_h = p.o + ((int64_t)b * N * p.Hv + h) * dv + j0 + cg * 4;
-  // a stash slot holds each lane's R x 4 block lane-major: row m of lane l at
-  // float offset (m*32 + l)*4, so every slot access is bank-conflict free
+  // a stash slot holds each warp's rows, each lane's R x 4 block lane-major:
+  // row m of lane l at float offset (m*32 + l)*4 of the warp's part, so every
+  // slot access is bank-conflict free
   const int slot_floats = DK * WC;
+  const int slot_part = wi * (DK / NW) * WC + lane * 4;
 
   for (int n = 0; n < N; ++n) {
     // (a) a tree node whose source is not node n-1 starts from its parent's
@@ -385,7 +442,7 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
       if (n > 0 && spar[n] != n - 1) {
         const int src = ssrc[n];
         if (src >= 0) {
-          const float* rs = pool + src * slot_floats + lane * 4;
+          const float* rs = pool + src * slot_floats + slot_part;
 #pragma unroll
           for (int m = 0; m < R; ++m) {
             const float4 t = *reinterpret_cast<const float4*>(rs + m * 128);
@@ -412,6 +469,7 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
         for (int off = S::CG; off < 32; off <<= 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
+        warps_sum<NW, S::CG>(u, sx, xc, wi, cg, rl);
         if constexpr (PREP) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) u[c] *= sinvk[n];
@@ -469,7 +527,7 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
       // a later, non-adjacent child continues from node n: stash H_n
       const int st = sstash[n];
       if (st >= 0) {
-        float* to = pool + st * slot_floats + lane * 4;
+        float* to = pool + st * slot_floats + slot_part;
 #pragma unroll
         for (int m = 0; m < R; ++m)
           *reinterpret_cast<float4*>(to + m * 128) =
@@ -483,12 +541,13 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
     for (int off = S::CG; off < 32; off <<= 1)
 #pragma unroll
       for (int i = 0; i < 9; ++i) red[i] += __shfl_xor_sync(FULL, red[i], off);
+    warps_sum<NW, S::CG>(red, sx, xc, wi, cg, rl);
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       u[c] = next_chain ? fmaf(al, red[c] * ikx, d[c] * (red[4] * (ik * ikx))) : red[c];
 
     // (f) persist (a chain verified for a replay commit keeps no snapshots)
-    if (rl == 0)
+    if (rl == 0 && wi == 0)
       st_f4(o_h + (int64_t)n * p.Hv * dv, red[5] * iq, red[6] * iq, red[7] * iq, red[8] * iq);
     if constexpr (SNAP16) {
       // binary16, round to nearest even: 8 bytes per lane and row
@@ -513,7 +572,7 @@ __global__ void __launch_bounds__(32) verify_kernel(const VerifyParams p) {
 
   if constexpr (TREE) {
     // node depths (root = 1), written once per sequence
-    if (lead && p.depth_out != nullptr) {
+    if (lead && wi == 0 && p.depth_out != nullptr) {
       for (int n = lane; n < N; n += 32) {
         int dpt = 1;
         for (int m = n; m > 0; m = spar[m]) ++dpt;
@@ -546,10 +605,10 @@ struct ReplayParams {
 };
 
 struct ReplayPlan {
-  int path, par, k, v, a, b, inv, total;
+  int path, par, k, v, a, b, inv, len, x, total;
 };
 
-__host__ __device__ inline ReplayPlan replay_plan(int N, int DK, int WC, int esz) {
+__host__ __device__ inline ReplayPlan replay_plan(int N, int DK, int WC, int esz, int nw = 1) {
   ReplayPlan s{};
   s.path = 0;
   s.par = s.path + round16(N * 4);
@@ -558,19 +617,23 @@ __host__ __device__ inline ReplayPlan replay_plan(int N, int DK, int WC, int esz
   s.a = s.v + round16(N * WC * esz);
   s.b = s.a + round16(N * 4);
   s.inv = s.b + round16(N * 4);  // 1/|k| of the path nodes (input preparation)
-  s.total = s.inv + round16(N * 4);
+  s.len = s.inv + round16(N * 4);  // path length
+  s.x = s.len + 16;               // cross-warp sums (NW > 1)
+  s.total = s.x + xchg_bytes(nw, WC);
   return s;
 }
 
-template <int DK, int WC, bool PREP>
-__global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
-  using S = Shape<DK, WC>;
+template <int DK, int WC, int NW, bool PREP>
+__global__ void __launch_bounds__(32 * NW) replay_kernel(const ReplayParams p) {
+  pdl_enter();
+  using S = Shape<DK, WC, NW>;
   constexpr int R = S::R;
+  constexpr int NT = 32 * NW;
   extern __shared__ __align__(16) char smem[];
   const int N = p.N;
   const bool bf16 = p.bf16 != 0;
   const int esz = bf16 ? 2 : 4;
-  const ReplayPlan pl = replay_plan(N, DK, WC, esz);
+  const ReplayPlan pl = replay_plan(N, DK, WC, esz, NW);
   int* spath = reinterpret_cast<int*>(smem + pl.path);
   int* spar = reinterpret_cast<int*>(smem + pl.par);
   char* sk = smem + pl.k;
@@ -578,52 +641,57 @@ __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
   float* sa = reinterpret_cast<float*>(smem + pl.a);
   float* sb = reinterpret_cast<float*>(smem + pl.b);
   float* sinvk = reinterpret_cast<float*>(smem + pl.inv);
+  int* slen = reinterpret_cast<int*>(smem + pl.len);
+  float* sx = reinterpret_cast<float*>(smem + pl.x);
+  int xc = 0;  // cross-warp exchanges so far
 
-  const int lane = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
   const int cg = lane % S::CG, rl = lane / S::CG;
   const int j0 = blockIdx.x * WC, h = blockIdx.y, b = blockIdx.z;
   const int hk = h / (p.Hv / p.Hk);
   const bool lead = blockIdx.x == 0 && blockIdx.y == 0;
   const int dv = p.dv;
-  const int row0 = rl * R;
+  const int row0 = wi * (DK / NW) + rl * R;
   const int64_t node0 = (int64_t)b * N;
 
   const int acc = __ldg(p.accept + b);
   const int sl = p.slot != nullptr ? __ldg(p.slot + b) : b;
   if (acc < 0 || acc >= N) {
-    if (lead && lane == 0) report(p.status, GDN_ERR_ACCEPT_RANGE);
+    if (lead && tid == 0) report(p.status, GDN_ERR_ACCEPT_RANGE);
     return;
   }
   if (sl < 0 || sl >= p.n_slots) {
-    if (lead && lane == 0) report(p.status, GDN_ERR_SLOT_RANGE);
+    if (lead && tid == 0) report(p.status, GDN_ERR_SLOT_RANGE);
     return;
   }
 
   // ---- the accepted path, root first
   int L = acc + 1;
   if (p.parent == nullptr) {
-    for (int n = lane; n < L; n += 32) spath[n] = n;
+    for (int n = tid; n < L; n += NT) spath[n] = n;
   } else {
     bool ok = true;
-    for (int n = lane; n < N; n += 32) {
+    for (int n = tid; n < N; n += NT) {
       const int pp = __ldg(p.parent + node0 + n);
       spar[n] = pp;
       ok = ok && (n == 0 ? pp == -1 : (pp >= 0 && pp < n));
     }
-    if (!__all_sync(FULL, ok)) {
-      if (lead && lane == 0) report(p.status, GDN_ERR_BAD_TREE);
+    if (!block_all<NW>(ok)) {
+      if (lead && tid == 0) report(p.status, GDN_ERR_BAD_TREE);
       return;
     }
-    __syncwarp();
-    int len = 0;
-    if (lane == 0) {
+    block_sync<NW>();
+    if (tid == 0) {
+      int len = 0;
       for (int m = acc; m >= 0; m = spar[m]) ++len;
       int i = len;
       for (int m = acc; m >= 0; m = spar[m]) spath[--i] = m;
+      *slen = len;
     }
-    L = __shfl_sync(FULL, len, 0);
+    block_sync<NW>();
+    L = *slen;
   }
-  __syncwarp();
+  block_sync<NW>();
 
   // ---- stage k, v, gates of the path nodes
   {
@@ -631,15 +699,15 @@ __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
     const char* vb = static_cast<const char*>(p.v) + ((node0 * p.Hv + h) * dv + j0) * esz;
     const int64_t kstride = (int64_t)p.Hk * DK * esz, vstride = (int64_t)p.Hv * dv * esz;
     const int kper = DK * esz / 16, vper = WC * esz / 16;
-    for (int idx = lane; idx < L * kper; idx += 32) {
+    for (int idx = tid; idx < L * kper; idx += NT) {
       const int r = idx / kper, c = idx - r * kper;
       cp_async16(sk + r * DK * esz + c * 16, kb + spath[r] * kstride + c * 16);
     }
-    for (int idx = lane; idx < L * vper; idx += 32) {
+    for (int idx = tid; idx < L * vper; idx += NT) {
       const int r = idx / vper, c = idx - r * vper;
       cp_async16(sv + r * WC * esz + c * 16, vb + spath[r] * vstride + c * 16);
     }
-    for (int r = lane; r < L; r += 32) {
+    for (int r = tid; r < L; r += NT) {
       cp_async4(sa + r, p.alpha + (node0 + spath[r]) * p.Hv + h);
       cp_async4(sb + r, p.beta + (node0 + spath[r]) * p.Hv + h);
     }
@@ -656,11 +724,11 @@ __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
     H[m][1] = make_float2(t.z, t.w);
   }
   cp_async_wait_all();
-  __syncwarp();
+  block_sync<NW>();
   if constexpr (PREP) {
-    prep_rows<DK>(sk, L, bf16, sinvk, lane);
-    prep_gates(sa, sb, L, lane);
-    __syncwarp();
+    prep_rows<DK>(sk, L, bf16, sinvk, tid, NT);
+    prep_gates(sa, sb, L, tid, NT);
+    block_sync<NW>();
   }
 
   float kn[R];
@@ -678,6 +746,7 @@ __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
     for (int off = S::CG; off < 32; off <<= 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
+    warps_sum<NW, S::CG>(u, sx, xc, wi, cg, rl);
     if constexpr (PREP) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) u[c] *= sinvk[0];
@@ -719,59 +788,60 @@ __global__ void __launch_bounds__(32) replay_kernel(const ReplayParams p) {
     for (int off = S::CG; off < 32; off <<= 1)
 #pragma unroll
       for (int e = 0; e < 5; ++e) red[e] += __shfl_xor_sync(FULL, red[e], off);
+    warps_sum<NW, S::CG>(red, sx, xc, wi, cg, rl);
 #pragma unroll
     for (int c = 0; c < 4; ++c) u[c] = fmaf(al, red[c] * ikx, d[c] * (red[4] * (ik * ikx)));
 #pragma unroll
     for (int m = 0; m < R; ++m) kn[m] = knx[m];
   }
 
-  // ---- back into the cache slot (this warp is the only reader and writer)
+  // ---- back into the cache slot (each thread is the only reader and writer
+  //      of its rows)
 #pragma unroll
   for (int m = 0; m < R; ++m)
     st_f4(c0 + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
 }
 
-template <int DK, int WC>
+template <int DK, int WC, int NW>
 int launch_replay_t(const ReplayParams& p, int B, bool prep, cudaStream_t stream) {
-  const ReplayPlan pl = replay_plan(p.N, DK, WC, p.bf16 ? 2 : 4);
+  const ReplayPlan pl = replay_plan(p.N, DK, WC, p.bf16 ? 2 : 4, NW);
   const dim3 grid(p.dv / WC, p.Hv, B);
   if (prep)
-    replay_kernel<DK, WC, true><<<grid, 32, pl.total, stream>>>(p);
-  else
-    replay_kernel<DK, WC, false><<<grid, 32, pl.total, stream>>>(p);
-  return launch_status();
+    return launch_pdl(replay_kernel<DK, WC, NW, true>, grid, dim3(32 * NW), pl.total, stream, p);
+  return launch_pdl(replay_kernel<DK, WC, NW, false>, grid, dim3(32 * NW), pl.total, stream, p);
 }
 
-template <int DK, int WC, bool TREE, bool SNAP16, bool PREP>
+template <int DK, int WC, int NW, bool TREE, bool SNAP16, bool PREP>
 int launch(const VerifyParams& p, int B, cudaStream_t stream) {
   VerifyParams q = p;
-  q.pool = TREE ? tree_pool_slots(p.N, DK, WC, p.bf16 ? 2 : 4) : 0;
-  const SmemPlan pl = smem_plan(p.N, DK, WC, p.bf16 ? 2 : 4, TREE, q.pool);
+  q.pool = TREE ? tree_pool_slots(p.N, DK, WC, p.bf16 ? 2 : 4, NW) : 0;
+  const SmemPlan pl = smem_plan(p.N, DK, WC, p.bf16 ? 2 : 4, TREE, q.pool, NW);
   const size_t smem = (size_t)pl.total;
   if (smem > 227 * 1024) return GDN_ERR_UNSUPPORTED;
-  auto kern = verify_kernel<DK, WC, TREE, SNAP16, PREP>;
+  auto kern = verify_kernel<DK, WC, NW, TREE, SNAP16, PREP>;
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return GDN_ERR_CUDA;
   }
   const dim3 grid(p.dv / WC, p.Hv, B);
-  kern<<<grid, 32, smem, stream>>>(q);
-  return launch_status();
+  return launch_pdl(kern, grid, dim3(32 * NW), smem, stream, q);
 }
 
 template <bool TREE, bool SNAP16, bool PREP>
-int dispatch(const VerifyParams& p, int B, int dk, int wc, cudaStream_t s) {
-#define GDN_CASE(DK_, WC_) \
-  if (dk == DK_ && wc == WC_) return launch<DK_, WC_, TREE, SNAP16, PREP>(p, B, s);
-  GDN_CASE(128, 16)
-  GDN_CASE(128, 8)
-  GDN_CASE(64, 16)
-  GDN_CASE(64, 8)
-  GDN_CASE(32, 16)
-  GDN_CASE(32, 8)
-  GDN_CASE(16, 16)
-  GDN_CASE(16, 8)
+int dispatch(const VerifyParams& p, int B, int dk, int wc, int nw, cudaStream_t s) {
+#define GDN_CASE(DK_, WC_, NW_) \
+  if (dk == DK_ && wc == WC_ && nw == NW_) return launch<DK_, WC_, NW_, TREE, SNAP16, PREP>(p, B, s);
+  GDN_CASE(128, 16, 1)
+  GDN_CASE(128, 16, 2)
+  GDN_CASE(128, 8, 1)
+  GDN_CASE(64, 16, 1)
+  GDN_CASE(64, 16, 2)
+  GDN_CASE(64, 8, 1)
+  GDN_CASE(32, 16, 1)
+  GDN_CASE(32, 8, 1)
+  GDN_CASE(16, 16, 1)
+  GDN_CASE(16, 8, 1)
 #undef GDN_CASE
   return GDN_ERR_UNSUPPORTED;
 }
@@ -779,12 +849,13 @@ int dispatch(const VerifyParams& p, int B, int dk, int wc, cudaStream_t s) {
 }  // namespace
 
 bool verify_tile_supported(int dk, int wc, int nw) {
-  return (dk == 128 || dk == 64 || dk == 32 || dk == 16) && (wc == 16 || wc == 8) && nw == 1;
+  if (!(dk == 128 || dk == 64 || dk == 32 || dk == 16) || !(wc == 16 || wc == 8)) return false;
+  // two row warps: 16-column slabs of d_k = 64 or 128
+  return nw == 1 || (nw == 2 && wc == 16 && (dk == 128 || dk == 64));
 }
 
 int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, int wc,
                   int nw, cudaStream_t stream, void* snap16, bool prep) {
-  (void)nw;
   VerifyParams p{};
   p.q = a->q;
   p.k = a->k;
@@ -807,18 +878,18 @@ int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   p.bf16 = a->in_dtype == GDN_BF16;
   p.snap16 = static_cast<__half*>(snap16);
   if (parent != nullptr)
-    return prep ? dispatch<true, false, true>(p, a->B, a->dk, wc, stream)
-                : dispatch<true, false, false>(p, a->B, a->dk, wc, stream);
+    return prep ? dispatch<true, false, true>(p, a->B, a->dk, wc, nw, stream)
+                : dispatch<true, false, false>(p, a->B, a->dk, wc, nw, stream);
   if (snap16 != nullptr) {
     if (prep) return GDN_ERR_UNSUPPORTED;
-    return dispatch<false, true, false>(p, a->B, a->dk, wc, stream);
+    return dispatch<false, true, false>(p, a->B, a->dk, wc, nw, stream);
   }
-  return prep ? dispatch<false, false, true>(p, a->B, a->dk, wc, stream)
-              : dispatch<false, false, false>(p, a->B, a->dk, wc, stream);
+  return prep ? dispatch<false, false, true>(p, a->B, a->dk, wc, nw, stream)
+              : dispatch<false, false, false>(p, a->B, a->dk, wc, nw, stream);
 }
 
 int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept, int wc,
-                  cudaStream_t stream, bool prep) {
+                  int nw, cudaStream_t stream, bool prep) {
   ReplayParams p{};
   p.k = a->k;
   p.v = a->v;
@@ -836,16 +907,19 @@ int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t
   p.Hv = a->Hv;
   p.dv = a->dv;
   p.bf16 = a->in_dtype == GDN_BF16;
-#define GDN_CASE(DK_, WC_) \
-  if (a->dk == DK_ && wc == WC_) return launch_replay_t<DK_, WC_>(p, a->B, prep, stream);
-  GDN_CASE(128, 16)
-  GDN_CASE(128, 8)
-  GDN_CASE(64, 16)
-  GDN_CASE(64, 8)
-  GDN_CASE(32, 16)
-  GDN_CASE(32, 8)
-  GDN_CASE(16, 16)
-  GDN_CASE(16, 8)
+#define GDN_CASE(DK_, WC_, NW_) \
+  if (a->dk == DK_ && wc == WC_ && nw == NW_) \
+    return launch_replay_t<DK_, WC_, NW_>(p, a->B, prep, stream);
+  GDN_CASE(128, 16, 1)
+  GDN_CASE(128, 16, 2)
+  GDN_CASE(128, 8, 1)
+  GDN_CASE(64, 16, 1)
+  GDN_CASE(64, 16, 2)
+  GDN_CASE(64, 8, 1)
+  GDN_CASE(32, 16, 1)
+  GDN_CASE(32, 8, 1)
+  GDN_CASE(16, 16, 1)
+  GDN_CASE(16, 8, 1)
 #undef GDN_CASE
   return GDN_ERR_UNSUPPORTED;
 }

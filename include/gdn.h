@@ -90,7 +90,11 @@ typedef enum gdn_dtype {
  *   tile_cols, row_warps
  *                 0 = automatic; otherwise the d_v columns owned by one
  *                 thread block (8 or 16) and the warps that split its d_k
- *                 rows (1).  A pure performance hint.
+ *                 rows (1, or 2 for 16 columns with d_k = 64 or 128).  A
+ *                 performance hint: results are identical up to the order
+ *                 in which the column sums are added, and a replay commit
+ *                 repeats a chain verify bit for bit only with the same
+ *                 tile.  GDN_ERR_UNSUPPORTED for any other combination.
  *
  * Supported sizes: dk in {16, 32, 64, 128}; dv a multiple of 16, <= 1024;
  * 1 <= N <= 64; Hv a multiple of Hk; B >= 0 (B = 0 launches nothing).

@@ -93,6 +93,8 @@ def _args(**kw):
     (dict(tile_cols=24), gdn.GDN_ERR_UNSUPPORTED),
     (dict(tile_cols=32, row_warps=1), gdn.GDN_ERR_UNSUPPORTED),
     (dict(dk=64, row_warps=4), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(dk=32, row_warps=2), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(tile_cols=8, row_warps=2), gdn.GDN_ERR_UNSUPPORTED),
     (dict(B=0), gdn.GDN_OK),
 ])
 def test_verify_host_checks(lib, change, want):

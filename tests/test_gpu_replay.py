@@ -20,14 +20,15 @@ def _oracle_replay(inp, accept, tree):
     return st, cache
 
 
-def _gpu_replay(gdn, inp, accept, tree, cache_t=None, tile_cols=0, status=None):
+def _gpu_replay(gdn, inp, accept, tree, cache_t=None, tile_cols=0, row_warps=0, status=None):
     t = torch()
     cache_t = dev(inp["cache"]) if cache_t is None else cache_t
     st = t.zeros(1, dtype=t.int32, device="cuda") if status is None else status
     gdn.gdn_replay_accepted(dev(inp["k"]), dev(inp["v"]), dev(inp["alpha"]), dev(inp["beta"]),
                             cache_t, dev(np.asarray(accept, np.int32)),
                             parent=dev(inp["parent"]) if tree else None, slot=dev(inp["slot"]),
-                            n_slots=inp["n_slots"], status=st, tile_cols=tile_cols)
+                            n_slots=inp["n_slots"], status=st, tile_cols=tile_cols,
+                            row_warps=row_warps)
     t.cuda.synchronize()
     return int(st.item()), cache_t
 
@@ -54,15 +55,16 @@ def test_chain_verify_without_snapshots(gpu_lib, tile):
     assert np.array_equal(o.cpu().numpy(), out["o"])
 
 
-@pytest.mark.parametrize("tile", [0, 8])
+@pytest.mark.parametrize("tile", [(0, 0), (16, 1), (16, 2), (8, 1)])
 def test_chain_replay_matches_persisted_state_bitwise(gpu_lib, tile):
-    """Along a chain the replay repeats the verify kernel's arithmetic: the
-    committed state is bit for bit the persisted snapshot of the accepted node,
-    and within tolerance of the oracle's replay."""
+    """Along a chain the replay repeats the verify kernel's arithmetic: with the
+    same tile, the committed state is bit for bit the persisted snapshot of the
+    accepted node, and within tolerance of the oracle's replay."""
     inp = _inputs(False)
-    out = verify_on_gpu(gpu_lib, inp, tile_cols=tile)
+    out = verify_on_gpu(gpu_lib, inp, tile_cols=tile[0], row_warps=tile[1])
     accept = inp["accept"]
-    st, cache_t = _gpu_replay(gpu_lib, inp, accept, False, tile_cols=tile)
+    st, cache_t = _gpu_replay(gpu_lib, inp, accept, False, tile_cols=tile[0],
+                              row_warps=tile[1])
     assert st == 0
     cache = cache_t.cpu().numpy()
     ost, ocache = _oracle_replay(inp, accept, False)
@@ -75,17 +77,17 @@ def test_chain_replay_matches_persisted_state_bitwise(gpu_lib, tile):
         assert np.array_equal(cache[sl], inp["cache"][sl]), "a slot outside the batch changed"
 
 
-@pytest.mark.parametrize("tile", [0, 8])
+@pytest.mark.parametrize("tile", [(0, 0), (16, 1), (16, 2), (8, 1)])
 def test_tree_replay_matches_oracle(gpu_lib, tile):
     """Tree: the ancestors of the accepted node from the root, from the cache."""
     inp = _inputs(True, seed=7200)
     accept = inp["accept"]
-    st, cache_t = _gpu_replay(gpu_lib, inp, accept, True, tile_cols=tile)
+    st, cache_t = _gpu_replay(gpu_lib, inp, accept, True, tile_cols=tile[0], row_warps=tile[1])
     assert st == 0
     cache = cache_t.cpu().numpy()
     ost, ocache = _oracle_replay(inp, accept, True)
     assert ost == oracle.OK
-    out = verify_on_gpu(gpu_lib, inp, tile_cols=tile)
+    out = verify_on_gpu(gpu_lib, inp, tile_cols=tile[0], row_warps=tile[1])
     for b in range(inp["B"]):
         sl = inp["slot"][b]
         assert_close(cache[sl], ocache[sl], f"tree replay, sequence {b}")

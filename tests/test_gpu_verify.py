@@ -37,7 +37,7 @@ def test_tiny_chain_verify_and_commit(gpu_lib):
     assert_close(got, snap[0, 2], "committed state vs oracle")
 
 
-@pytest.mark.parametrize("tile", [(0, 0), (16, 1), (8, 1)])
+@pytest.mark.parametrize("tile", [(0, 0), (16, 1), (16, 2), (8, 1)])
 def test_chain16_full(gpu_lib, tile):
     """Single-sequence chain of 16, 16 q/k heads, 48 value heads, d = 128, bf16
     inputs; every output and every snapshot, in every tile shape."""
@@ -49,7 +49,7 @@ def test_chain16_full(gpu_lib, tile):
     assert_close(out["snap"], snap, "chain16 snapshots")
 
 
-@pytest.mark.parametrize("tile", [(0, 0), (16, 1), (8, 1)])
+@pytest.mark.parametrize("tile", [(0, 0), (16, 1), (16, 2), (8, 1)])
 def test_tree22_full(gpu_lib, tile):
     """DDTree of 22 nodes: per-node states from the parent, depths bit-exact,
     commit of the accepted node."""
@@ -70,7 +70,7 @@ def test_tree22_full(gpu_lib, tile):
     assert np.array_equal(got, out["snap"][0, inp["accept"][0]])
 
 
-@pytest.mark.parametrize("tile", [(16, 1), (8, 1)])
+@pytest.mark.parametrize("tile", [(16, 1), (16, 2), (8, 1)])
 def test_single_path_tree_equals_chain(gpu_lib, tile):
     inp = synthetic.chain16(seed=99)
     a = verify_on_gpu(gpu_lib, inp, tree=False, tile_cols=tile[0], row_warps=tile[1])
@@ -160,11 +160,13 @@ def test_empty_batch_is_a_no_op(gpu_lib):
     t.cuda.synchronize()
 
 
-def test_device_errors_skip_only_the_bad_sequence(gpu_lib):
+@pytest.mark.parametrize("dk", [32, 64])
+def test_device_errors_skip_only_the_bad_sequence(gpu_lib, dk):
     """A malformed tree, a bad slot and a bad accept index are reported in the
-    status word; the other sequences are still computed correctly."""
+    status word; the other sequences are still computed correctly (d_k = 64
+    runs on two row warps per block)."""
     t = torch()
-    inp = synthetic.make_verify_inputs(B=3, N=6, Hk=1, Hv=2, dk=32, dv=32, dtype="bf16",
+    inp = synthetic.make_verify_inputs(B=3, N=6, Hk=1, Hv=2, dk=dk, dv=32, dtype="bf16",
                                        alpha_kind="near_one", state_sigma=0.05, seed=5, tree=True)
     good_snap, good_o = _oracle(inp)
     bad = dict(inp)
@@ -188,7 +190,7 @@ def test_device_errors_skip_only_the_bad_sequence(gpu_lib):
     before = cache.clone()
     st = t.zeros(1, dtype=t.int32, device="cuda")
     acc = t.tensor([2, 6, 0], dtype=t.int32, device="cuda")   # 6 is out of range
-    gpu_lib.gdn_commit_accepted(out["snap_t"], acc, cache, B=3, N=6, Hv=2, dk=32, dv=32,
+    gpu_lib.gdn_commit_accepted(out["snap_t"], acc, cache, B=3, N=6, Hv=2, dk=dk, dv=32,
                                 slot=out["slot_t"], n_slots=inp["n_slots"], status=st)
     t.cuda.synchronize()
     assert st.item() == gpu_lib.GDN_ERR_ACCEPT_RANGE
