@@ -17,30 +17,25 @@
 //
 // Work decomposition
 // ------------------
-// One warp (one thread block) owns a slab of WC columns of one (sequence,
-// value head): grid = (dv / WC, Hv, B).  lane = cg + CG*rl: cg picks 4 adjacent
+// A thread block owns a slab of WC columns of one (sequence, value head):
+// grid = (dv / WC, Hv, B).  In a warp, lane = cg + CG*rl: cg picks 4 adjacent
 // columns (a 16-byte vector), rl one of RL = 32/CG row lanes, and each lane
-// keeps R = d_k/RL consecutive rows x 4 columns of the state in registers (as
-// float2 pairs for the paired fp32 FMA) for the whole block.  Column sums
-// reduce over the RL row lanes with warp shuffles.
+// keeps R consecutive rows x 4 columns of the state in registers (as float2
+// pairs for the paired fp32 FMA).  Column sums reduce over the row lanes with
+// warp shuffles.
 //
-// The node loop is built so that snapshot stores never wait on a reduction:
-// the reduction that feeds node n+1 runs while node n updates and stores.
-// When src(n+1) = n,
-//     u_{n+1} = H_n^T k_{n+1} = alpha_n (H_src(n)^T k_{n+1}) + delta_n (k_n . k_{n+1}),
+// Chain (verify_kernel): the slab's d_k rows are split over NW row warps (one,
+// or two when there are too few blocks to give every SM sub-partition a warp);
+// the warps add their column sums through shared memory.  The node loop is
+// built so that snapshot stores never wait on a reduction: the reduction that
+// feeds node n+1 runs while node n updates and stores, since
+//     u_{n+1} = H_n^T k_{n+1} = alpha_n (H_{n-1}^T k_{n+1}) + delta_n (k_n . k_{n+1}),
 // and both sums on the right come from the registers BEFORE node n's update.
-// When src(n) != n - 1 (a tree), H_src(n) comes from a pool of shared-memory
-// stash slots: a node whose state a later, non-adjacent child will need is
-// copied there when it is computed (slots are assigned by a greedy pass over
-// the tree in the prologue and freed after the last such child starts); only
-// if the pool runs out is the parent read back from the snapshot this thread
-// stored earlier (same thread, same addresses: program order makes it
-// visible).  u_n is then reduced when node n starts.  Shared-memory traffic
-// does not compete with the snapshot stores for the SM's global-memory pipe,
-// which is what bounds this kernel.
-// q, k, v, the gates and the parents are staged with cp.async while the
-// cached state loads.  Snapshots leave as 16-byte stores; a warp-wide store
-// covers RL rows x WC*4 contiguous bytes.
+// Tree (tree_kernel, below): the block's warps take the nodes of each depth
+// level in turn.
+// q, k, v and the gates are staged with cp.async while the cached state
+// loads.  Snapshots leave as 16-byte stores; a warp-wide store covers RL rows
+// x WC*4 contiguous bytes.
 //
 // Variants (template flags): SNAP16 persists binary16 snapshots (chains);
 // PREP takes raw q/k projections and gate pre-activations (the per-node
@@ -118,39 +113,23 @@ __device__ __forceinline__ void warps_sum(float (&x)[NV], float* sx, int& xc, in
 
 __host__ __device__ constexpr int round16(int x) { return (x + 15) & ~15; }
 
-// Shared-memory plan in bytes; every array starts on a 16-byte boundary.
-// Tree blocks add per-node tables and `pool` stash slots of dk x WC floats.
+// Shared-memory plan of a chain block in bytes; every array starts on a
+// 16-byte boundary.
 struct SmemPlan {
-  int q, k, v, a, b, par, src, stash, last, pool, inv, x, total;
+  int q, k, v, a, b, inv, x, total;
 };
 
-__host__ __device__ inline SmemPlan smem_plan(int N, int DK, int WC, int esz, bool tree,
-                                              int pool, int nw = 1) {
+__host__ __device__ inline SmemPlan smem_plan(int N, int DK, int WC, int esz, int nw = 1) {
   SmemPlan s{};
   s.q = 0;
   s.k = s.q + round16(N * DK * esz);
   s.v = s.k + round16(N * DK * esz);
   s.a = s.v + round16(N * WC * esz);
   s.b = s.a + round16(N * 4);
-  s.par = s.b + round16(N * 4);
-  const int t = tree ? round16(N * 4) : 0;
-  s.src = s.par + t;
-  s.stash = s.src + t;
-  s.last = s.stash + t;
-  s.pool = s.last + t;
-  s.inv = s.pool + (tree ? pool * DK * WC * 4 : 0);  // 1/|q_n|, 1/|k_n| (input preparation)
-  s.x = s.inv + 2 * round16(N * 4);                   // cross-warp sums (NW > 1)
+  s.inv = s.b + round16(N * 4);       // 1/|q_n|, 1/|k_n| (input preparation)
+  s.x = s.inv + 2 * round16(N * 4);   // cross-warp sums (NW > 1)
   s.total = s.x + xchg_bytes(nw, WC);
   return s;
-}
-
-// Stash slots per tree block: as many as fit next to the staged inputs while
-// three blocks still share an SM (at least 1, at most 12).
-inline int tree_pool_slots(int N, int DK, int WC, int esz, int nw) {
-  const SmemPlan base = smem_plan(N, DK, WC, esz, true, 0, nw);
-  const int budget = 74 * 1024 - base.total;
-  int slots = budget / (DK * WC * 4);
-  return slots < 1 ? 1 : (slots > 12 ? 12 : slots);
 }
 
 struct VerifyParams {
@@ -168,7 +147,7 @@ struct VerifyParams {
   const int32_t* parent;
   int32_t* depth_out;
   int64_t cache_slot_stride;
-  int n_slots, N, Hk, Hv, dv, bf16, pool;
+  int n_slots, N, Hk, Hv, dv, bf16;
 };
 
 // Start copying n_rows rows of row_bytes bytes (row r at src + r*src_stride)
@@ -259,7 +238,7 @@ __device__ __forceinline__ void prep_gates(float* a, float* b, int n_rows, int t
   }
 }
 
-template <int DK, int WC, int NW, bool TREE, bool SNAP16, bool PREP>
+template <int DK, int WC, int NW, bool SNAP16, bool PREP>
 __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
   pdl_enter();
   using S = Shape<DK, WC, NW>;
@@ -269,17 +248,12 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
   const int N = p.N;
   const bool bf16 = p.bf16 != 0;
   const int esz = bf16 ? 2 : 4;
-  const SmemPlan pl = smem_plan(N, DK, WC, esz, TREE, p.pool, NW);
+  const SmemPlan pl = smem_plan(N, DK, WC, esz, NW);
   char* sq = smem + pl.q;
   char* sk = smem + pl.k;
   char* sv = smem + pl.v;
   float* sa = reinterpret_cast<float*>(smem + pl.a);
   float* sb = reinterpret_cast<float*>(smem + pl.b);
-  int* spar = reinterpret_cast<int*>(smem + pl.par);
-  int* ssrc = reinterpret_cast<int*>(smem + pl.src);      // tree: -1 regs, >= 0 slot, -2 global
-  int* sstash = reinterpret_cast<int*>(smem + pl.stash);  // tree: slot receiving node n, or -1
-  int* slast = reinterpret_cast<int*>(smem + pl.last);    // tree: last non-adjacent child
-  float* pool = reinterpret_cast<float*>(smem + pl.pool);
   float* sinvq = reinterpret_cast<float*>(smem + pl.inv);
   float* sinvk = sinvq + round16(N * 4) / 4;
   float* sx = reinterpret_cast<float*>(smem + pl.x);
@@ -293,7 +267,7 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
   const int dv = p.dv;
   const int row0 = wi * (DK / NW) + rl * R;
 
-  // ---- stage q, k, v, gates, parents (independent of the slot: issued first)
+  // ---- stage q, k, v, gates (independent of the slot: issued first)
   {
     const int64_t node0 = (int64_t)b * N;
     const char* qb = static_cast<const char*>(p.q) + ((node0 * p.Hk + hk) * DK) * esz;
@@ -305,7 +279,6 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
     for (int n = tid; n < N; n += NT) {
       cp_async4(sa + n, p.alpha + (node0 + n) * p.Hv + h);
       cp_async4(sb + n, p.beta + (node0 + n) * p.Hv + h);
-      if constexpr (TREE) cp_async4(spar + n, p.parent + node0 + n);
     }
   }
 
@@ -340,67 +313,6 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
     block_sync<NW>();
   }
 
-  if constexpr (TREE) {
-    // parent[0] == -1, 0 <= parent[n] < n; the block leaves otherwise
-    bool ok = true;
-    for (int n = tid; n < N; n += NT) {
-      const int pp = spar[n];
-      ok = ok && (n == 0 ? pp == -1 : (pp >= 0 && pp < n));
-    }
-    if (!block_all<NW>(ok)) {
-      if (lead && tid == 0) report(p.status, GDN_ERR_BAD_TREE);
-      return;
-    }
-  }
-
-  if (TREE && wi == 0) {
-    // ---- stash plan (greedy over nodes in index order), by the first warp
-    for (int n = lane; n < N; n += 32) slast[n] = -1;
-    __syncwarp();
-    for (int f = lane; f < N; f += 32) {
-      const int pf = spar[f];
-      if (f > 0 && pf != f - 1) atomicMax(slast + pf, f);
-    }
-    __syncwarp();
-    int par_r[2], last_r[2], stash_r[2] = {-1, -1};
-#pragma unroll
-    for (int s2 = 0; s2 < 2; ++s2) {
-      const int n = lane + 32 * s2;
-      par_r[s2] = n < N ? spar[n] : -1;
-      last_r[s2] = n < N ? slast[n] : -1;
-    }
-    unsigned free_mask = (p.pool >= 32) ? 0xffffffffu : ((1u << p.pool) - 1u);
-    for (int n = 0; n < N; ++n) {
-      const int hi = n >> 5, ln = n & 31;
-      const int pn = __shfl_sync(FULL, hi ? par_r[1] : par_r[0], ln);
-      const int lastn = __shfl_sync(FULL, hi ? last_r[1] : last_r[0], ln);
-      int src = -1;
-      if (n > 0 && pn != n - 1) {
-        const int sp = __shfl_sync(FULL, (pn >> 5) ? stash_r[1] : stash_r[0], pn & 31);
-        const int lastp = __shfl_sync(FULL, (pn >> 5) ? last_r[1] : last_r[0], pn & 31);
-        if (sp >= 0) {
-          src = sp;
-          if (n == lastp) free_mask |= 1u << sp;
-        } else {
-          src = -2;
-        }
-      }
-      int mine = -1;
-      if (lastn >= 0 && free_mask != 0u) {
-        mine = __ffs(free_mask) - 1;
-        free_mask &= free_mask - 1u;
-      }
-      if (lane == ln) {
-        if (hi) stash_r[1] = mine; else stash_r[0] = mine;
-      }
-      if (lane == 0) {
-        ssrc[n] = src;
-        sstash[n] = mine;
-      }
-    }
-  }
-  if constexpr (TREE) block_sync<NW>();
-
   // ---- u_0 = H0^T k_0
   float kn[R];  // k of the current node
   load_rows<R>(kn, sk, row0, bf16);
@@ -429,56 +341,9 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
   float* snap_h = p.snap == nullptr ? nullptr : p.snap + lane_off;
   __half* snap16_h = SNAP16 ? p.snap16 + lane_off : nullptr;
   float* o_h = p.o + ((int64_t)b * N * p.Hv + h) * dv + j0 + cg * 4;
-  // a stash slot holds each warp's rows, each lane's R x 4 block lane-major:
-  // row m of lane l at float offset (m*32 + l)*4 of the warp's part, so every
-  // slot access is bank-conflict free
-  const int slot_floats = DK * WC;
-  const int slot_part = wi * (DK / NW) * WC + lane * 4;
 
   for (int n = 0; n < N; ++n) {
-    // (a) a tree node whose source is not node n-1 starts from its parent's
-    //     stashed (or, if the pool ran out, re-read) state; its u is reduced here
-    if constexpr (TREE) {
-      if (n > 0 && spar[n] != n - 1) {
-        const int src = ssrc[n];
-        if (src >= 0) {
-          const float* rs = pool + src * slot_floats + slot_part;
-#pragma unroll
-          for (int m = 0; m < R; ++m) {
-            const float4 t = *reinterpret_cast<const float4*>(rs + m * 128);
-            H[m][0] = make_float2(t.x, t.y);
-            H[m][1] = make_float2(t.z, t.w);
-          }
-        } else {
-          const float* from = snap_h + (int64_t)spar[n] * node_stride;
-#pragma unroll
-          for (int m = 0; m < R; ++m) {
-            const float4 t = ld_cg_f4(from + (int64_t)m * dv);
-            H[m][0] = make_float2(t.x, t.y);
-            H[m][1] = make_float2(t.z, t.w);
-          }
-        }
-        float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int m = 0; m < R; ++m) {
-          a01 = __ffma2_rn(H[m][0], f2(kn[m]), a01);
-          a23 = __ffma2_rn(H[m][1], f2(kn[m]), a23);
-        }
-        u[0] = a01.x; u[1] = a01.y; u[2] = a23.x; u[3] = a23.y;
-#pragma unroll
-        for (int off = S::CG; off < 32; off <<= 1)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
-        warps_sum<NW, S::CG>(u, sx, xc, wi, cg, rl);
-        if constexpr (PREP) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) u[c] *= sinvk[n];
-        }
-      }
-    }
-
     const bool has_next = n + 1 < N;
-    const bool next_chain = !TREE || (has_next && spar[n + 1] == n);
     float knx[R];  // k of node n+1
     if (has_next) {
       load_rows<R>(knx, sk + (n + 1) * DK * esz, row0, bf16);
@@ -496,17 +361,14 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
     const float ikx = PREP && has_next ? sinvk[n + 1] : 1.f;
     const float iq = PREP ? sinvq[n] : 1.f;
 
-    // (c) partial sums for u_{n+1} when node n+1 continues from node n:
-    //     from the registers before node n's update
+    // (c) partial sums for u_{n+1}: from the registers before node n's update
     float2 w01 = make_float2(0.f, 0.f), w23 = make_float2(0.f, 0.f);
     float kk = 0.f;
-    if (next_chain) {
 #pragma unroll
-      for (int m = 0; m < R; ++m) {
-        w01 = __ffma2_rn(H[m][0], f2(knx[m]), w01);
-        w23 = __ffma2_rn(H[m][1], f2(knx[m]), w23);
-        kk = fmaf(kn[m], knx[m], kk);
-      }
+    for (int m = 0; m < R; ++m) {
+      w01 = __ffma2_rn(H[m][0], f2(knx[m]), w01);
+      w23 = __ffma2_rn(H[m][1], f2(knx[m]), w23);
+      kk = fmaf(kn[m], knx[m], kk);
     }
 
     // (d) delta_n, update, output partial
@@ -523,17 +385,6 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
       o01 = __ffma2_rn(H[m][0], f2(qr[m]), o01);
       o23 = __ffma2_rn(H[m][1], f2(qr[m]), o23);
     }
-    if constexpr (TREE) {
-      // a later, non-adjacent child continues from node n: stash H_n
-      const int st = sstash[n];
-      if (st >= 0) {
-        float* to = pool + st * slot_floats + slot_part;
-#pragma unroll
-        for (int m = 0; m < R; ++m)
-          *reinterpret_cast<float4*>(to + m * 128) =
-              make_float4(H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
-      }
-    }
 
     // (e) one shuffle tree for the 4 + 1 + 4 column sums
     float red[9] = {w01.x, w01.y, w23.x, w23.y, kk, o01.x, o01.y, o23.x, o23.y};
@@ -543,8 +394,7 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
       for (int i = 0; i < 9; ++i) red[i] += __shfl_xor_sync(FULL, red[i], off);
     warps_sum<NW, S::CG>(red, sx, xc, wi, cg, rl);
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      u[c] = next_chain ? fmaf(al, red[c] * ikx, d[c] * (red[4] * (ik * ikx))) : red[c];
+    for (int c = 0; c < 4; ++c) u[c] = fmaf(al, red[c] * ikx, d[c] * (red[4] * (ik * ikx)));
 
     // (f) persist (a chain verified for a replay commit keeps no snapshots)
     if (rl == 0 && wi == 0)
@@ -569,17 +419,217 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
 #pragma unroll
     for (int m = 0; m < R; ++m) kn[m] = knx[m];
   }
+}
 
-  if constexpr (TREE) {
-    // node depths (root = 1), written once per sequence
-    if (lead && wi == 0 && p.depth_out != nullptr) {
-      for (int n = lane; n < N; n += 32) {
-        int dpt = 1;
-        for (int m = n; m > 0; m = spar[m]) ++dpt;
-        p.depth_out[(int64_t)b * N + n] = dpt;
-      }
+// ------------------------------------------------------------------ tree
+// Tree verification, level by level.  Nodes of equal depth depend on nodes of
+// smaller depth only, so the TW warps of a block (one column slab of one
+// (sequence, value head)) take the nodes of each depth level in turn, all
+// rows of the slab per warp (the verify lane layout with one row warp).  A
+// node starts from its parent's state: still in the registers of the warp
+// that computed it when that warp takes the child, otherwise read back from
+// the parent's snapshot, which a warp of this block stored one level earlier
+// (the barrier between levels makes it visible; it is read through L2).  Each
+// node reduces u = H^T k before its update and o = H'^T q after it.
+struct TreePlan {
+  int q, k, v, a, b, par, dep, ord, lev, inv, total;
+};
+
+__host__ __device__ inline TreePlan tree_plan(int N, int DK, int WC, int esz) {
+  TreePlan s{};
+  s.q = 0;
+  s.k = s.q + round16(N * DK * esz);
+  s.v = s.k + round16(N * DK * esz);
+  s.a = s.v + round16(N * WC * esz);
+  s.b = s.a + round16(N * 4);
+  s.par = s.b + round16(N * 4);
+  s.dep = s.par + round16(N * 4);        // depth of each node (root = 1)
+  s.ord = s.dep + round16(N * 4);        // nodes by depth, then index
+  s.lev = s.ord + round16(N * 4);        // lev[L] = first position of depth L
+  s.inv = s.lev + round16((N + 2) * 4);  // 1/|q_n|, 1/|k_n| (input preparation)
+  s.total = s.inv + 2 * round16(N * 4);
+  return s;
+}
+
+template <int DK, int WC, int TW, bool PREP>
+__global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
+  pdl_enter();
+  using S = Shape<DK, WC, 1>;
+  constexpr int R = S::R;
+  constexpr int NT = 32 * TW;
+  extern __shared__ __align__(16) char smem[];
+  const int N = p.N;
+  const bool bf16 = p.bf16 != 0;
+  const int esz = bf16 ? 2 : 4;
+  const TreePlan pl = tree_plan(N, DK, WC, esz);
+  char* sq = smem + pl.q;
+  char* sk = smem + pl.k;
+  char* sv = smem + pl.v;
+  float* sa = reinterpret_cast<float*>(smem + pl.a);
+  float* sb = reinterpret_cast<float*>(smem + pl.b);
+  int* spar = reinterpret_cast<int*>(smem + pl.par);
+  int* sdep = reinterpret_cast<int*>(smem + pl.dep);
+  int* sord = reinterpret_cast<int*>(smem + pl.ord);
+  int* slev = reinterpret_cast<int*>(smem + pl.lev);
+  float* sinvq = reinterpret_cast<float*>(smem + pl.inv);
+  float* sinvk = sinvq + round16(N * 4) / 4;
+
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int cg = lane % S::CG, rl = lane / S::CG;
+  const int j0 = blockIdx.x * WC, h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / (p.Hv / p.Hk);
+  const bool lead = blockIdx.x == 0 && blockIdx.y == 0;  // per-sequence reporting
+  const int dv = p.dv;
+  const int row0 = rl * R;
+  const int64_t node0 = (int64_t)b * N;
+
+  // ---- stage q, k, v, gates, parents
+  {
+    const char* qb = static_cast<const char*>(p.q) + ((node0 * p.Hk + hk) * DK) * esz;
+    const char* kb = static_cast<const char*>(p.k) + ((node0 * p.Hk + hk) * DK) * esz;
+    const char* vb = static_cast<const char*>(p.v) + ((node0 * p.Hv + h) * dv + j0) * esz;
+    stage_rows(sk, kb, (int64_t)p.Hk * DK * esz, N, DK * esz, tid, NT);
+    stage_rows(sq, qb, (int64_t)p.Hk * DK * esz, N, DK * esz, tid, NT);
+    stage_rows(sv, vb, (int64_t)p.Hv * dv * esz, N, WC * esz, tid, NT);
+    for (int n = tid; n < N; n += NT) {
+      cp_async4(sa + n, p.alpha + (node0 + n) * p.Hv + h);
+      cp_async4(sb + n, p.beta + (node0 + n) * p.Hv + h);
+      cp_async4(spar + n, p.parent + node0 + n);
     }
   }
+  const int sl = p.slot != nullptr ? __ldg(p.slot + b) : b;
+  if (sl < 0 || sl >= p.n_slots) {
+    cp_async_wait_all();
+    if (lead && tid == 0) report(p.status, GDN_ERR_SLOT_RANGE);
+    return;
+  }
+  const float* cache_h = p.cache + (int64_t)sl * p.cache_slot_stride + (int64_t)h * DK * dv +
+                         (int64_t)row0 * dv + j0 + cg * 4;
+  // the root's warp starts the cached state on its way
+  float2 H[R][2];
+  if (w == 0) {
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+      const float4 t = ld_cg_f4(cache_h + (int64_t)m * dv);
+      H[m][0] = make_float2(t.x, t.y);
+      H[m][1] = make_float2(t.z, t.w);
+    }
+  }
+  int held = w == 0 ? -1 : -2;  // node whose state this warp holds (-1: the cache)
+  cp_async_wait_all();
+  __syncthreads();
+
+  if constexpr (PREP) {
+    prep_rows<DK>(sq, N, bf16, sinvq, tid, NT);
+    prep_rows<DK>(sk, N, bf16, sinvk, tid, NT);
+    prep_gates(sa, sb, N, tid, NT);
+  }
+  // parent[0] == -1, 0 <= parent[n] < n; the block leaves otherwise
+  {
+    bool ok = true;
+    for (int n = tid; n < N; n += NT) {
+      const int pp = spar[n];
+      ok = ok && (n == 0 ? pp == -1 : (pp >= 0 && pp < n));
+    }
+    if (!block_all<TW>(ok)) {
+      if (lead && tid == 0) report(p.status, GDN_ERR_BAD_TREE);
+      return;
+    }
+  }
+  // depths, then the order of the walk: by depth, then by index
+  for (int n = tid; n < N; n += NT) {
+    int d = 1;
+    for (int m = n; m > 0; m = spar[m]) ++d;
+    sdep[n] = d;
+  }
+  __syncthreads();
+  for (int n = tid; n < N; n += NT) {
+    const int dn = sdep[n];
+    int pos = 0;
+    for (int m = 0; m < N; ++m) {
+      const int dm = sdep[m];
+      pos += (dm < dn || (dm == dn && m < n)) ? 1 : 0;
+    }
+    sord[pos] = n;
+  }
+  for (int L = tid; L < N + 2; L += NT) {
+    int c = 0;
+    for (int m = 0; m < N; ++m) c += sdep[m] < L ? 1 : 0;
+    slev[L] = c;
+  }
+  __syncthreads();
+
+  const int64_t node_stride = (int64_t)p.Hv * DK * dv;
+  float* snap_h = p.snap + ((int64_t)b * N * p.Hv + h) * DK * dv + (int64_t)row0 * dv + j0 + cg * 4;
+  float* o_h = p.o + ((int64_t)b * N * p.Hv + h) * dv + j0 + cg * 4;
+
+  for (int L = 1; L <= N && slev[L] < N; ++L) {
+    for (int i = slev[L] + w; i < slev[L + 1]; i += TW) {
+      const int n = sord[i], par = spar[n];
+      if (par != held) {
+        const float* from = par < 0 ? cache_h : snap_h + (int64_t)par * node_stride;
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+          const float4 t = ld_cg_f4(from + (int64_t)m * dv);
+          H[m][0] = make_float2(t.x, t.y);
+          H[m][1] = make_float2(t.z, t.w);
+        }
+      }
+      float kn[R], qr[R], vj[4];
+      load_rows<R>(kn, sk + n * DK * esz, row0, bf16);
+      load_rows<R>(qr, sq + n * DK * esz, row0, bf16);
+      load_rows<4>(vj, sv + n * WC * esz, cg * 4, bf16);
+      const float al = sa[n], be = sb[n];
+      const float ik = PREP ? sinvk[n] : 1.f;
+      const float iq = PREP ? sinvq[n] : 1.f;
+
+      // u_n = H_par^T k_n
+      float u[4];
+      {
+        float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+          a01 = __ffma2_rn(H[m][0], f2(kn[m]), a01);
+          a23 = __ffma2_rn(H[m][1], f2(kn[m]), a23);
+        }
+        u[0] = a01.x; u[1] = a01.y; u[2] = a23.x; u[3] = a23.y;
+#pragma unroll
+        for (int off = S::CG; off < 32; off <<= 1)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
+      }
+      // delta_n, update, o_n
+      float d[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) d[c] = be * (vj[c] - al * (u[c] * ik));
+      const float2 d01 = make_float2(d[0] * ik, d[1] * ik), d23 = make_float2(d[2] * ik, d[3] * ik);
+      const float2 al2 = f2(al);
+      float2 o01 = make_float2(0.f, 0.f), o23 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < R; ++m) {
+        H[m][0] = __ffma2_rn(f2(kn[m]), d01, __fmul2_rn(al2, H[m][0]));
+        H[m][1] = __ffma2_rn(f2(kn[m]), d23, __fmul2_rn(al2, H[m][1]));
+        o01 = __ffma2_rn(H[m][0], f2(qr[m]), o01);
+        o23 = __ffma2_rn(H[m][1], f2(qr[m]), o23);
+      }
+      float* dst = snap_h + (int64_t)n * node_stride;
+#pragma unroll
+      for (int m = 0; m < R; ++m)
+        st_f4(dst + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
+      float o[4] = {o01.x, o01.y, o23.x, o23.y};
+#pragma unroll
+      for (int off = S::CG; off < 32; off <<= 1)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[c] += __shfl_xor_sync(FULL, o[c], off);
+      if (rl == 0) st_f4(o_h + (int64_t)n * p.Hv * dv, o[0] * iq, o[1] * iq, o[2] * iq, o[3] * iq);
+      held = n;
+    }
+    __syncthreads();  // this level's snapshots are visible to the next level
+  }
+
+  // node depths (root = 1), written once per sequence
+  if (lead && p.depth_out != nullptr)
+    for (int n = tid; n < N; n += NT) p.depth_out[(int64_t)b * N + n] = sdep[n];
 }
 
 // ---------------------------------------------------------------- replay
@@ -811,27 +861,60 @@ int launch_replay_t(const ReplayParams& p, int B, bool prep, cudaStream_t stream
   return launch_pdl(replay_kernel<DK, WC, NW, false>, grid, dim3(32 * NW), pl.total, stream, p);
 }
 
-template <int DK, int WC, int NW, bool TREE, bool SNAP16, bool PREP>
+template <int DK, int WC, int NW, bool SNAP16, bool PREP>
 int launch(const VerifyParams& p, int B, cudaStream_t stream) {
-  VerifyParams q = p;
-  q.pool = TREE ? tree_pool_slots(p.N, DK, WC, p.bf16 ? 2 : 4, NW) : 0;
-  const SmemPlan pl = smem_plan(p.N, DK, WC, p.bf16 ? 2 : 4, TREE, q.pool, NW);
+  const SmemPlan pl = smem_plan(p.N, DK, WC, p.bf16 ? 2 : 4, NW);
   const size_t smem = (size_t)pl.total;
   if (smem > 227 * 1024) return GDN_ERR_UNSUPPORTED;
-  auto kern = verify_kernel<DK, WC, NW, TREE, SNAP16, PREP>;
+  auto kern = verify_kernel<DK, WC, NW, SNAP16, PREP>;
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return GDN_ERR_CUDA;
   }
   const dim3 grid(p.dv / WC, p.Hv, B);
-  return launch_pdl(kern, grid, dim3(32 * NW), smem, stream, q);
+  return launch_pdl(kern, grid, dim3(32 * NW), smem, stream, p);
 }
 
-template <bool TREE, bool SNAP16, bool PREP>
+// Warps per tree block: each takes whole nodes of a depth level (measured on
+// a 22-node draft tree: 4 warps 20.7 us, 8 warps 33.5 us per launch).
+constexpr int kTreeWarps = 4;
+
+template <int DK, int WC, int TW, bool PREP>
+int launch_tree(const VerifyParams& p, int B, cudaStream_t stream) {
+  const TreePlan pl = tree_plan(p.N, DK, WC, p.bf16 ? 2 : 4);
+  const size_t smem = (size_t)pl.total;
+  if (smem > 227 * 1024) return GDN_ERR_UNSUPPORTED;
+  auto kern = tree_kernel<DK, WC, TW, PREP>;
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return GDN_ERR_CUDA;
+  }
+  const dim3 grid(p.dv / WC, p.Hv, B);
+  return launch_pdl(kern, grid, dim3(32 * TW), smem, stream, p);
+}
+
+template <bool PREP>
+int dispatch_tree(const VerifyParams& p, int B, int dk, int wc, cudaStream_t s) {
+#define GDN_CASE(DK_, WC_) \
+  if (dk == DK_ && wc == WC_) return launch_tree<DK_, WC_, kTreeWarps, PREP>(p, B, s);
+  GDN_CASE(128, 16)
+  GDN_CASE(128, 8)
+  GDN_CASE(64, 16)
+  GDN_CASE(64, 8)
+  GDN_CASE(32, 16)
+  GDN_CASE(32, 8)
+  GDN_CASE(16, 16)
+  GDN_CASE(16, 8)
+#undef GDN_CASE
+  return GDN_ERR_UNSUPPORTED;
+}
+
+template <bool SNAP16, bool PREP>
 int dispatch(const VerifyParams& p, int B, int dk, int wc, int nw, cudaStream_t s) {
 #define GDN_CASE(DK_, WC_, NW_) \
-  if (dk == DK_ && wc == WC_ && nw == NW_) return launch<DK_, WC_, NW_, TREE, SNAP16, PREP>(p, B, s);
+  if (dk == DK_ && wc == WC_ && nw == NW_) return launch<DK_, WC_, NW_, SNAP16, PREP>(p, B, s);
   GDN_CASE(128, 16, 1)
   GDN_CASE(128, 16, 2)
   GDN_CASE(128, 8, 1)
@@ -877,15 +960,15 @@ int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   p.dv = a->dv;
   p.bf16 = a->in_dtype == GDN_BF16;
   p.snap16 = static_cast<__half*>(snap16);
-  if (parent != nullptr)
-    return prep ? dispatch<true, false, true>(p, a->B, a->dk, wc, nw, stream)
-                : dispatch<true, false, false>(p, a->B, a->dk, wc, nw, stream);
+  if (parent != nullptr)  // row warps do not apply: a tree block's warps take whole nodes
+    return prep ? dispatch_tree<true>(p, a->B, a->dk, wc, stream)
+                : dispatch_tree<false>(p, a->B, a->dk, wc, stream);
   if (snap16 != nullptr) {
     if (prep) return GDN_ERR_UNSUPPORTED;
-    return dispatch<false, true, false>(p, a->B, a->dk, wc, nw, stream);
+    return dispatch<true, false>(p, a->B, a->dk, wc, nw, stream);
   }
-  return prep ? dispatch<false, false, true>(p, a->B, a->dk, wc, nw, stream)
-              : dispatch<false, false, false>(p, a->B, a->dk, wc, nw, stream);
+  return prep ? dispatch<false, true>(p, a->B, a->dk, wc, nw, stream)
+              : dispatch<false, false>(p, a->B, a->dk, wc, nw, stream);
 }
 
 int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept, int wc,

@@ -95,6 +95,8 @@ typedef enum gdn_dtype {
  *                 in which the column sums are added, and a replay commit
  *                 repeats a chain verify bit for bit only with the same
  *                 tile.  GDN_ERR_UNSUPPORTED for any other combination.
+ *                 A tree verify takes tile_cols only: its block's warps
+ *                 take whole nodes of a depth level, never rows.
  *
  * Supported sizes: dk in {16, 32, 64, 128}; dv a multiple of 16, <= 1024;
  * 1 <= N <= 64; Hv a multiple of Hk; B >= 0 (B = 0 launches nothing).

@@ -71,11 +71,18 @@ def test_tree22_full(gpu_lib, tile):
 
 
 @pytest.mark.parametrize("tile", [(16, 1), (16, 2), (8, 1)])
-def test_single_path_tree_equals_chain(gpu_lib, tile):
+def test_single_path_tree_matches_chain(gpu_lib, tile):
+    """A tree that is one path is the chain.  The tree kernel reduces u = H^T k
+    at every node while the chain kernel takes u from the previous node's
+    look-ahead, so the two agree to rounding, and each matches the oracle."""
     inp = synthetic.chain16(seed=99)
     a = verify_on_gpu(gpu_lib, inp, tree=False, tile_cols=tile[0], row_warps=tile[1])
     b = verify_on_gpu(gpu_lib, inp, tree=True, tile_cols=tile[0], row_warps=tile[1])
-    assert np.array_equal(a["snap"], b["snap"]) and np.array_equal(a["o"], b["o"])
+    snap, o = _oracle(inp)
+    for out, kind in ((a, "chain"), (b, "single-path tree")):
+        assert_close(out["snap"], snap, f"{kind} snapshots")
+        assert_close(out["o"], o, f"{kind} o")
+    assert_close(b["snap"], a["snap"], "tree vs chain snapshots")
     assert b["depth"][0].tolist() == list(range(1, 17))
 
 
