@@ -254,3 +254,39 @@ def test_outputs_have_guard_canaries_after_commit(gpu_lib):
                                 n_slots=1)
     t.cuda.synchronize()
     assert canaries_ok(back, n)
+
+
+@pytest.mark.parametrize("shape", ["star", "path", "broom", "two_paths"])
+def test_tree_kernel_level_shapes(gpu_lib, shape):
+    """The tree kernel walks depth levels with four warps: a star (one level of
+    63 nodes), a path (64 levels of one node: every node on the same warp), a
+    broom (a path then a fan) and two interleaved paths (siblings alternate,
+    so parents are read back from snapshots written by another warp); three
+    sequences with different trees, all against the oracle, depths exact."""
+    B, N = 3, 64
+    inp = synthetic.make_verify_inputs(B=B, N=N, Hk=2, Hv=4, dk=128, dv=32, dtype="bf16",
+                                       alpha_kind="near_one", state_sigma=0.05,
+                                       seed=9100 + len(shape), tree=True, n_slots=B + 1,
+                                       depth_cap=64)
+    par = np.empty((B, N), np.int32)
+    for b in range(B):
+        n = np.arange(N)
+        if shape == "star":
+            p = np.where(n == 0, -1, 0)
+        elif shape == "path":
+            p = n - 1
+        elif shape == "broom":
+            p = np.where(n < 20 + b, n - 1, 19 + b)
+            p[0] = -1
+        else:
+            p = np.where(n <= 2, n - 1, n - 2)
+            p[0], p[1], p[2] = -1, 0, 0
+        par[b] = p
+    inp = dict(inp, parent=par)
+    out = verify_on_gpu(gpu_lib, inp)
+    snap, o = _oracle(inp)
+    assert out["status"] == 0
+    assert_close(out["o"], o, f"{shape} o")
+    assert_close(out["snap"], snap, f"{shape} snapshots")
+    st, depth = oracle.tree_depth(par)
+    assert st == oracle.OK and np.array_equal(out["depth"], depth)
