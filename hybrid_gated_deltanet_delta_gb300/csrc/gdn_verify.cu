@@ -150,6 +150,50 @@ struct VerifyParams {
   int n_slots, N, Hk, Hv, dv, bf16;
 };
 
+__device__ __forceinline__ void prefetch_l2(const void* a) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a));
+}
+
+// Before the programmatic wait (which orders this kernel after the previous
+// one on the stream): hint L2 with the lines the block is about to read, so
+// that their DRAM latency overlaps the previous kernel's tail.  The slot table
+// and the inputs may still be being written by that kernel: a stale or
+// out-of-range slot only wastes (or skips) the hint, a prefetch never changes
+// memory, and every load that feeds a result is issued after the wait (L2 is
+// the point of coherence, and the hint bypasses L1).  Thread t of nt; the
+// state rows are those of thread t's own layout (row0, R rows, 16-byte column
+// group col), hinted once per 64-byte row segment.
+template <int DK, int R>
+__device__ __forceinline__ void prefetch_block(const VerifyParams& p, int b, int h, int hk, int j0,
+                                               bool state, int row0, int col, int t, int nt) {
+  const int N = p.N, dv = p.dv, esz = p.bf16 ? 2 : 4;
+  if (state) {
+    const int s0 = p.slot != nullptr ? __ldcg(p.slot + b) : b;
+    if (s0 >= 0 && s0 < p.n_slots) {
+      const float* c0 = p.cache + (int64_t)s0 * p.cache_slot_stride + (int64_t)h * DK * dv +
+                        (int64_t)row0 * dv + col;
+#pragma unroll
+      for (int m = 0; m < R; ++m) prefetch_l2(c0 + (int64_t)m * dv);
+    }
+  }
+  // q and k rows of the block's q/k head (128-byte lines), v segments
+  const int per = (DK * esz + 127) / 128;
+  const int qk_lines = N * per;
+  const int64_t node0 = (int64_t)b * N;
+  for (int i = t; i < 2 * qk_lines + N; i += nt) {
+    if (i < 2 * qk_lines) {
+      const int which = i / qk_lines, r = i - which * qk_lines;
+      const int n = r / per, part = r - n * per;
+      const char* base = static_cast<const char*>(which ? p.q : p.k);
+      prefetch_l2(base + ((node0 + n) * p.Hk + hk) * DK * esz + part * 128);
+    } else {
+      const int n = i - 2 * qk_lines;
+      prefetch_l2(static_cast<const char*>(p.v) + ((node0 + n) * p.Hv + h) * dv * esz +
+                  (int64_t)j0 * esz);
+    }
+  }
+}
+
 // Start copying n_rows rows of row_bytes bytes (row r at src + r*src_stride)
 // to dst + r*row_bytes with 16-byte cp.async, thread t of nt.
 __device__ __forceinline__ void stage_rows(char* dst, const char* src, int64_t src_stride,
@@ -240,10 +284,16 @@ __device__ __forceinline__ void prep_gates(float* a, float* b, int n_rows, int t
 
 template <int DK, int WC, int NW, bool SNAP16, bool PREP>
 __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
-  pdl_enter();
   using S = Shape<DK, WC, NW>;
   constexpr int R = S::R;
   constexpr int NT = 32 * NW;
+  {
+    const int t = threadIdx.x, ln = t & 31;
+    prefetch_block<DK, R>(p, blockIdx.z, blockIdx.y, blockIdx.y / (p.Hv / p.Hk),
+                          blockIdx.x * WC, ln % S::CG == 0,
+                          (t >> 5) * (DK / NW) + (ln / S::CG) * R, blockIdx.x * WC, t, NT);
+  }
+  pdl_enter();
   extern __shared__ __align__(16) char smem[];
   const int N = p.N;
   const bool bf16 = p.bf16 != 0;
@@ -453,10 +503,16 @@ __host__ __device__ inline TreePlan tree_plan(int N, int DK, int WC, int esz) {
 
 template <int DK, int WC, int TW, bool PREP>
 __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
-  pdl_enter();
   using S = Shape<DK, WC, 1>;
   constexpr int R = S::R;
   constexpr int NT = 32 * TW;
+  {
+    const int t = threadIdx.x, ln = t & 31;
+    prefetch_block<DK, R>(p, blockIdx.z, blockIdx.y, blockIdx.y / (p.Hv / p.Hk),
+                          blockIdx.x * WC, t < 32 && ln % S::CG == 0, (ln / S::CG) * R,
+                          blockIdx.x * WC, t, NT);
+  }
+  pdl_enter();
   extern __shared__ __align__(16) char smem[];
   const int N = p.N;
   const bool bf16 = p.bf16 != 0;
