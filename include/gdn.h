@@ -31,6 +31,14 @@
  *    allocates nothing, keeps no global state and never synchronises: work
  *    is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  *    stream) and the call returns once it is launched.
+ *  - Kernels are launched with programmatic dependent launch allowed: each
+ *    kernel starts by waiting until the kernel before it on the stream has
+ *    completed and its memory is visible, then lets the next kernel begin
+ *    launching.  Stream order is kept for every read and write.  Before that
+ *    wait a kernel only issues L2 prefetch hints for lines it will read
+ *    (which never change memory).  A kernel of the caller's that follows one
+ *    of ours with the same launch attribute must itself wait before reading
+ *    our outputs (griddepcontrol.wait), as programmatic launch requires.
  *  - All pointers must be 16-byte aligned; element strides are in elements.
  *  - Host-detected errors return a negative gdn_status before anything is
  *    launched.  Errors that depend on device data (a malformed tree, an
