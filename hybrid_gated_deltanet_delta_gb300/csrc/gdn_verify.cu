@@ -481,8 +481,13 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
 // the parent's snapshot, which a warp of this block stored one level earlier
 // (the barrier between levels makes it visible; it is read through L2).  Each
 // node reduces u = H^T k before its update and o = H'^T q after it.
+// Tree state stash: the states of the first kTreeSlots nodes of a level stay
+// in shared memory for the next level (two level buffers), so most children
+// read their parent from shared memory instead of L2.
+constexpr int kTreeSlots = 3;
+
 struct TreePlan {
-  int q, k, v, a, b, par, dep, ord, lev, inv, total;
+  int q, k, v, a, b, par, dep, ord, lev, pos, inv, stash, total;
 };
 
 __host__ __device__ inline TreePlan tree_plan(int N, int DK, int WC, int esz) {
@@ -496,8 +501,10 @@ __host__ __device__ inline TreePlan tree_plan(int N, int DK, int WC, int esz) {
   s.dep = s.par + round16(N * 4);        // depth of each node (root = 1)
   s.ord = s.dep + round16(N * 4);        // nodes by depth, then index
   s.lev = s.ord + round16(N * 4);        // lev[L] = first position of depth L
-  s.inv = s.lev + round16((N + 2) * 4);  // 1/|q_n|, 1/|k_n| (input preparation)
-  s.total = s.inv + 2 * round16(N * 4);
+  s.pos = s.lev + round16((N + 2) * 4);  // position of each node within its level
+  s.inv = s.pos + round16(N * 4);        // 1/|q_n|, 1/|k_n| (input preparation)
+  s.stash = s.inv + 2 * round16(N * 4);  // [2 levels][kTreeSlots][DK * WC] fp32
+  s.total = s.stash + 2 * kTreeSlots * DK * WC * 4;
   return s;
 }
 
@@ -527,8 +534,10 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
   int* sdep = reinterpret_cast<int*>(smem + pl.dep);
   int* sord = reinterpret_cast<int*>(smem + pl.ord);
   int* slev = reinterpret_cast<int*>(smem + pl.lev);
+  int* spos = reinterpret_cast<int*>(smem + pl.pos);
   float* sinvq = reinterpret_cast<float*>(smem + pl.inv);
   float* sinvk = sinvq + round16(N * 4) / 4;
+  float* stash = reinterpret_cast<float*>(smem + pl.stash);
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int cg = lane % S::CG, rl = lane / S::CG;
@@ -614,6 +623,14 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
     slev[L] = c;
   }
   __syncthreads();
+  for (int i = tid; i < N; i += NT) {
+    const int n = sord[i];
+    spos[n] = i - slev[sdep[n]];
+  }
+  __syncthreads();
+  // a stash slot holds each lane's R x 4 block lane-major: row m of lane l at
+  // float offset (m*32 + l)*4, so every slot access is bank-conflict free
+  constexpr int kSlot = DK * WC;
 
   const int64_t node_stride = (int64_t)p.Hv * DK * dv;
   float* snap_h = p.snap + ((int64_t)b * N * p.Hv + h) * DK * dv + (int64_t)row0 * dv + j0 + cg * 4;
@@ -623,12 +640,23 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
     for (int i = slev[L] + w; i < slev[L + 1]; i += TW) {
       const int n = sord[i], par = spar[n];
       if (par != held) {
-        const float* from = par < 0 ? cache_h : snap_h + (int64_t)par * node_stride;
+        const int ppos = par < 0 ? kTreeSlots : spos[par];
+        if (ppos < kTreeSlots) {
+          const float* rs = stash + (((L - 1) & 1) * kTreeSlots + ppos) * kSlot + lane * 4;
 #pragma unroll
-        for (int m = 0; m < R; ++m) {
-          const float4 t = ld_cg_f4(from + (int64_t)m * dv);
-          H[m][0] = make_float2(t.x, t.y);
-          H[m][1] = make_float2(t.z, t.w);
+          for (int m = 0; m < R; ++m) {
+            const float4 t = *reinterpret_cast<const float4*>(rs + m * 128);
+            H[m][0] = make_float2(t.x, t.y);
+            H[m][1] = make_float2(t.z, t.w);
+          }
+        } else {
+          const float* from = par < 0 ? cache_h : snap_h + (int64_t)par * node_stride;
+#pragma unroll
+          for (int m = 0; m < R; ++m) {
+            const float4 t = ld_cg_f4(from + (int64_t)m * dv);
+            H[m][0] = make_float2(t.x, t.y);
+            H[m][1] = make_float2(t.z, t.w);
+          }
         }
       }
       float kn[R], qr[R], vj[4];
@@ -672,6 +700,14 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
 #pragma unroll
       for (int m = 0; m < R; ++m)
         st_f4(dst + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
+      const int mypos = i - slev[L];
+      if (mypos < kTreeSlots) {
+        float* to = stash + ((L & 1) * kTreeSlots + mypos) * kSlot + lane * 4;
+#pragma unroll
+        for (int m = 0; m < R; ++m)
+          *reinterpret_cast<float4*>(to + m * 128) =
+              make_float4(H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
+      }
       float o[4] = {o01.x, o01.y, o23.x, o23.y};
 #pragma unroll
       for (int off = S::CG; off < 32; off <<= 1)
