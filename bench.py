@@ -4,24 +4,36 @@
 
 A step is one pass of the hot path over one batch of synthetic input:
 
-  chain16      (default) one GDN layer, 1 sequence, a 16-position chain,
-               16 q/k heads / 48 value heads, d_k = d_v = 128, bf16 q/k/v,
-               fp32 state: gdn_verify_chain + gdn_commit_accepted
+  chain16      one GDN layer, 1 sequence, a 16-position chain, 16 q/k heads /
+               48 value heads, d_k = d_v = 128, bf16 q/k/v, fp32 state:
+               gdn_verify_chain + gdn_commit_accepted
   tree22       the same heads over a 22-node draft tree: gdn_verify_tree + commit
   batched8x16  8 sequences x 16-position chains over 48 layers:
                48 x gdn_verify_chain + one gdn_commit_accepted over the 48 layers
   prefill8192  one 8192-token sequence, chunk 64: gdn_prefill_chunked
+  (and variants: *_replay, *_index, *_f16; see WORKLOADS)
 
-Metric: node-heads/s (B x N x Hv per layer call, summed over the step; for the
-prefill, token-heads/s).  No step finds its data in L2 (129 MB): the batched
-and prefill steps are preceded by a 256 MiB write that is not timed; a
-single-sequence step (less than L2) instead rotates, back to back and
+With no --workload the run prints ONE JSON line: the headline is chain16
+(the metric is quoted "at block 16"), and the other workloads the metric and
+its measurement plan name -- tree22 ("tree 22"), batched8x16 and
+prefill8192 -- are measured in the same run and nested under "workloads",
+each with its step time and percentiles, its own roofline and its end-to-end
+figure.  --workload NAME measures that one workload alone (for profiling).
+
+Metric: node-heads/s (B x N x Hv per layer call, summed over the step; for
+the prefill, token-heads/s).  No step finds its data in L2 (129 MB): the
+batched and prefill steps are preceded by a 256 MiB write that is not timed;
+a single-sequence step (less than L2) instead rotates, back to back and
 unflushed, over enough independent copies of the workload to exceed twice L2.
-Each step's kernels are bracketed by CUDA events on the launch stream, and the
-dominant kernel (the verify / the prefill) by its own pair, which gives the
-roofline figure.  Prints ONE JSON
-line on rank 0.  Under torchrun every rank runs its own replica (independent
-sequences, no collective on the data path): weak scaling.
+The K timed steps are bracketed by CUDA events on the launch stream; further
+blocks of back-to-back steps (and of the dominant kernel alone) give the
+percentiles and the roofline figure.  Under torchrun every rank runs its own
+replica (independent sequences, no collective on the data path): weak scaling.
+
+The end-to-end figure goes through the package's public API (bound calls,
+one ctypes call per launch): every step copies its inputs from pinned host
+memory to the device and its outputs back, all enqueued on the stream, timed
+on the host clock around the whole run.
 
 --impl reference times the CPU oracle (plain float64 C++, the reference for
 every parity test) on this host's cores, on a bounded sample of the same
@@ -30,6 +42,7 @@ workload each step.
 from __future__ import annotations
 
 import argparse
+import concurrent.futures as cf
 import hashlib
 import json
 import os
@@ -50,6 +63,18 @@ import synthetic  # noqa: E402
 HEADS = synthetic.HEADS
 FLUSH_BYTES = 256 << 20
 L2_BYTES = 129 * 10**6
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+# bars the kernels are held to: fraction of the measured HBM copy bandwidth
+# (verify, commit) and of the measured dense bf16 tensor throughput (prefill)
+TARGETS = {"hbm": 0.70, "tensor": 0.50}
+# blocks of back-to-back launches behind the percentiles and the roofline figure
+STAT_BLOCKS = 9
+KERNEL_BLOCK = 100
+
+METRIC = "GDN verify node-heads/s per layer at block 16 / tree 22; % of GB300 HBM roofline"
+HEADLINE = "chain16"
+NESTED = ("tree22", "batched8x16", "prefill8192")
 
 
 def hold_device(torch, host_s_per_step, steps):
@@ -60,10 +85,6 @@ def hold_device(torch, host_s_per_step, steps):
     start event and is not timed."""
     seconds = min(0.5, 0.002 + 2.0 * host_s_per_step * steps)
     torch.cuda._sleep(int(seconds * 2.2e9))
-FALLBACK_HBM_GBS = 6800.0
-FALLBACK_BF16_TFLOPS = 1900.0
-
-METRIC = "GDN verify node-heads/s per layer at block 16 / tree 22; % of GB300 HBM roofline"
 
 
 # ------------------------------------------------------------------ workloads
@@ -138,6 +159,30 @@ WORKLOADS = {
                         desc="1 sequence of 8192 tokens, 16 q/k heads, 48 value heads, "
                              "d_k=d_v=128, bf16 q/k/v, chunk 64, WY/UT form on tensor cores"),
 }
+
+
+def stats_ms(values, how):
+    """Summary of per-step (or per-launch) times in ms."""
+    v = [float(x) for x in values]
+    return {"mean": statistics.mean(v), "p10": float(np.percentile(v, 10)),
+            "p50": float(np.percentile(v, 50)), "p90": float(np.percentile(v, 90)),
+            "samples": len(v), "how": how}
+
+
+def roofline_entry(bound, kernel, work_per_launch, launch_ms, peak, peak_kind, traffic,
+                   work_key):
+    """achieved = algorithmic work per launch / launch time, against the
+    measured peak, with the bar the kernel is held to."""
+    unit = "GB/s" if bound == "hbm" else "TFLOP/s"
+    scale = 1e9 if bound == "hbm" else 1e12
+    achieved = work_per_launch / (launch_ms / 1e3) / scale
+    frac = achieved / peak
+    return {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": frac, "target": TARGETS[bound], "target_met": frac >= TARGETS[bound],
+            "peak_source": (f"{peak_kind} (MEASURED_PEAKS.json "
+                            f"{'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})"
+                            if peak_kind == "measured" else f"fallback {peak} {unit}"),
+            work_key: work_per_launch, "launch_ms": launch_ms, "traffic": traffic}
 
 
 # --------------------------------------------------------------------- clocks
@@ -249,48 +294,67 @@ def profiled_traffic(kernel, workload):
 
 
 # ------------------------------------------------------------------ oracle leg
-def oracle_step_sample(wl_name, heads_per_step):
-    """The oracle (CPU, float64) on `heads_per_step` value heads of the
-    workload's first sequence (one layer), plus the commit of that head:
-    returns (seconds, node-heads done)."""
-    import oracle
-
-    if wl_name == "prefill8192":
-        inp = synthetic.prefill8192()
-        t0 = time.perf_counter()
-        st, _, _ = oracle.prefill_step(inp["q_f64"], inp["k_f64"], inp["v_f64"], inp["alpha"],
-                                       inp["beta"], inp["state"], T=inp["T"], Hk=16, Hv=48,
-                                       dk=128, dv=128, heads=(0, heads_per_step))
-        assert st == oracle.OK
-        return time.perf_counter() - t0, inp["T"] * heads_per_step
-    raise NotImplementedError
+def host_cpu():
+    """(logical cores, CPU model) of this host."""
+    cores = os.cpu_count() or 1
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu model")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return cores, model or "unknown"
 
 
 class OracleSampler:
-    """Bounded samples of a verify workload for the oracle: value heads
-    h0..h0+G-1 of one q/k head group of sequence 0 (contiguous arrays)."""
+    """Bounded samples of a workload for the oracle.  A verify sample is value
+    heads h .. h+n-1 (wrapping) of sequence 0 of one layer, verified and then
+    committed (copy, or replay for the *_replay workloads); a prefill sample
+    is one value head over all 8192 tokens in the step form."""
 
     def __init__(self, wl_name):
         self.wl = wl_name
-        if wl_name.startswith("chain16"):
-            inp = synthetic.chain16()
-        elif wl_name == "tree22":
-            inp = synthetic.tree22()
-        elif wl_name.startswith("batched8x16"):
-            inp = synthetic.batched8x16_layer(0)
+        self.prefill = wl_name == "prefill8192"
+        if self.prefill:
+            self.inp = synthetic.prefill8192()
+        elif wl_name.startswith("chain16"):
+            self.inp = synthetic.chain16()
+        elif wl_name.startswith("tree22"):
+            self.inp = synthetic.tree22()
         else:
-            inp = None
-        self.inp = inp
+            self.inp = synthetic.batched8x16_layer(0)
 
-    def run(self, n_heads=1):
-        """Verify + commit (copy, or replay for the *_replay workloads) for n_heads
-        value heads of sequence 0; returns node-heads."""
+    @property
+    def unit(self):
+        return "token-heads/s" if self.prefill else "node-heads/s"
+
+    def run(self, h0=0, n_heads=1):
+        """One sample; returns the node-heads (token-heads) it covered."""
         import oracle
 
         inp = self.inp
+        if self.prefill:
+            h = h0 % inp["Hv"]
+            st, _, _ = oracle.prefill_step(inp["q_f64"], inp["k_f64"], inp["v_f64"],
+                                           inp["alpha"], inp["beta"], inp["state"], T=inp["T"],
+                                           Hk=inp["Hk"], Hv=inp["Hv"], dk=inp["dk"],
+                                           dv=inp["dv"], heads=(h, 1))
+            assert st == oracle.OK
+            return inp["T"]
         b = 0
         N = inp["N"]
-        h_sel = np.arange(n_heads) % inp["Hv"]
+        h_sel = (h0 + np.arange(n_heads)) % inp["Hv"]
         G = inp["Hv"] // inp["Hk"]
         hk_sel = h_sel // G
         q = inp["q_f64"][b:b + 1][:, :, hk_sel]
@@ -315,30 +379,46 @@ class OracleSampler:
         assert st == oracle.OK
         return N * n_heads
 
+    def describe(self, n_heads):
+        if self.prefill:
+            return "8192 tokens x 1 value head (step form, float64)"
+        return (f"verify + commit of {n_heads} value head(s) x {self.inp['N']} nodes of "
+                f"sequence 0, float64")
 
-def cpu_baseline(wl_name, budget_s=10.0):
-    """The oracle as it stands, single-threaded, repeated on samples of the
-    workload until about budget_s seconds of CPU work are done."""
-    if wl_name == "prefill8192":
-        done, spent, reps = 0, 0.0, 0
-        while spent < budget_s or reps == 0:
-            dt, n = oracle_step_sample(wl_name, 1)
-            spent += dt
-            done += n
-            reps += 1
-        return {"value": done / spent, "unit": "token-heads/s", "cores": 1, "kind": "oracle",
-                "sample": f"{reps} x (8192 tokens x 1 value head, step form, float64)"}
+    def timed(self, budget_s, threads, n_heads=3):
+        """Samples on `threads` host threads (each its own value heads; the
+        oracle's C calls release the interpreter lock) until about budget_s
+        seconds have passed; returns (units per second, samples)."""
+        done, reps = 0, 0
+        t0 = time.perf_counter()
+        if threads == 1:
+            while time.perf_counter() - t0 < budget_s or reps == 0:
+                done += self.run(reps * n_heads, n_heads)
+                reps += 1
+        else:
+            with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+                while time.perf_counter() - t0 < budget_s or reps == 0:
+                    futs = [ex.submit(self.run, (reps + i) * n_heads, n_heads)
+                            for i in range(threads)]
+                    done += sum(f.result() for f in futs)
+                    reps += threads
+        spent = time.perf_counter() - t0
+        return done / spent, reps
+
+
+def cpu_baseline(wl_name, budget_s=8.0):
+    """The oracle as it stands on this host: all cores (a thread pool over
+    independent value heads, the reported value) and one thread beside it."""
     smp = OracleSampler(wl_name)
-    heads = 3
-    done, reps = 0, 0
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < budget_s or reps == 0:
-        done += smp.run(heads)
-        reps += 1
-    spent = time.perf_counter() - t0
-    return {"value": done / spent, "unit": "node-heads/s", "cores": 1, "kind": "oracle",
-            "sample": f"{reps} x (verify + commit of {heads} value heads x {smp.inp['N']} "
-                      f"nodes of sequence 0, float64)"}
+    cores, model = host_cpu()
+    n_heads = 1 if smp.prefill else 3
+    multi, reps_m = smp.timed(budget_s, cores, n_heads)
+    single, reps_s = smp.timed(budget_s, 1, n_heads)
+    return {"value": multi, "unit": smp.unit, "cores": cores, "kind": "oracle",
+            "sample": f"{reps_m} samples on {cores} threads, each {smp.describe(n_heads)}",
+            "cpu_model": model, "host_cores": cores,
+            "single_thread": {"value": single, "cores": 1,
+                              "sample": f"{reps_s} samples, each {smp.describe(n_heads)}"}}
 
 
 # ----------------------------------------------------------------- ours: GPU
@@ -397,6 +477,7 @@ class VerifyCase:
             self.o_host = torch.empty(self.o.shape, dtype=torch.float32).pin_memory()
 
     def verify(self, gdn):
+        """The binding's plain (checked) call."""
         d = self.dev
         args = (d["q"], d["k"], d["v"], d["alpha"], d["beta"], self.cache, self.snap, self.o)
         if self.snap16:
@@ -407,43 +488,30 @@ class VerifyCase:
             gdn.gdn_verify_chain(*args, slot=self.slot, n_slots=self.inp["n_slots"])
 
     def replay(self, gdn):
+        """The binding's plain (checked) replay commit."""
         d = self.dev
         gdn.gdn_replay_accepted(d["k"], d["v"], d["alpha"], d["beta"], self.cache, d["accept"],
                                 parent=self.parent, slot=self.slot,
                                 n_slots=self.inp["n_slots"])
 
     def bind(self, gdn, stream):
-        """Marshal this layer's verify and replay once for the timed loop: the
-        same C-ABI entry points the binding's functions call, with the
-        argument struct built up front, so that a launch costs one ctypes call
-        instead of the binding's per-call checks (which would otherwise leave
-        the device waiting on the host between short steps)."""
-        import ctypes
-
-        lib = gdn.load()
+        """This layer's verify and replay as bound calls (the package's public
+        serving API: arguments marshalled once, one ctypes call per launch)."""
         d = self.dev
-        s = ctypes.c_void_p(stream.cuda_stream)
-
-        def ptr(t):
-            return None if t is None else ctypes.c_void_p(t.data_ptr())
-
         n_slots = self.inp["n_slots"]
-        self._va = gdn.make_verify_args(d["q"], d["k"], d["v"], d["alpha"], d["beta"], self.cache,
-                                        None if self.snap16 else self.snap, self.o,
-                                        slot=self.slot, n_slots=n_slots)
-        va = ctypes.byref(self._va)
+        common = (d["q"], d["k"], d["v"], d["alpha"], d["beta"], self.cache)
         if self.snap16:
-            snap = ptr(self.snap)
-            self.verify_c = lambda: lib.gdn_verify_chain_f16(va, snap, s)
+            self.verify_c = gdn.bind_verify_chain(*common, None, self.o, snapshots_f16=self.snap,
+                                                  slot=self.slot, n_slots=n_slots, stream=stream)
         elif self.parent is not None:
-            par = ptr(self.parent)
-            self.verify_c = lambda: lib.gdn_verify_tree(va, par, None, s)
+            self.verify_c = gdn.bind_verify_tree(*common, self.snap, self.o, self.parent,
+                                                 slot=self.slot, n_slots=n_slots, stream=stream)
         else:
-            self.verify_c = lambda: lib.gdn_verify_chain(va, s)
-        self._ra = gdn.make_verify_args(None, d["k"], d["v"], d["alpha"], d["beta"], self.cache,
-                                        None, None, slot=self.slot, n_slots=n_slots)
-        ra, par, acc = ctypes.byref(self._ra), ptr(self.parent), ptr(d["accept"])
-        self.replay_c = lambda: lib.gdn_replay_accepted(ra, par, acc, s)
+            self.verify_c = gdn.bind_verify_chain(*common, self.snap, self.o, slot=self.slot,
+                                                  n_slots=n_slots, stream=stream)
+        self.replay_c = gdn.bind_replay_accepted(d["k"], d["v"], d["alpha"], d["beta"],
+                                                 self.cache, d["accept"], parent=self.parent,
+                                                 slot=self.slot, n_slots=n_slots, stream=stream)
 
     def h2d(self):
         self.packed.copy_(self.host, non_blocking=True)
@@ -454,31 +522,48 @@ class VerifyCase:
         return self.o.numel() * 4
 
 
-def run_ours(args, wl_name, world, rank, local):
-    import torch
+class Context:
+    """What every measurement shares: the library, the stream, the L2 flush
+    buffer, the clock sampler and the rank layout."""
 
-    import hybrid_gated_deltanet_delta_gb300 as gdn
+    def __init__(self, args, world, rank, local):
+        import torch
 
-    torch.cuda.set_device(local)
-    gdn.load()
+        import hybrid_gated_deltanet_delta_gb300 as gdn
+
+        self.args, self.world, self.rank, self.local = args, world, rank, local
+        self.torch, self.gdn = torch, gdn
+        torch.cuda.set_device(local)
+        gdn.load()
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        self.stream = torch.cuda.current_stream()
+        self.flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.sampler = ClockSampler(gpu_uuid(torch, local))
+        self.sampler.start()
+        self.peaks = measured_peaks()
+
+    def close(self):
+        self.sampler.stop()
+
+    def events(self, n):
+        return [self.torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def measure_verify(ctx, wl_name):
+    torch, gdn, args, stream, flush = ctx.torch, ctx.gdn, ctx.args, ctx.stream, ctx.flush
+    world = ctx.world
     wl = WORKLOADS[wl_name]
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-
-    if wl_name == "prefill8192":
-        return run_prefill(args, gdn, torch, flush, world, rank, local)
-
     Hk, Hv, dk, dv = HEADS["Hk"], HEADS["Hv"], HEADS["dk"], HEADS["dv"]
     B, N = wl["B"], wl["N"]
     replay = wl.get("replay", False)
     index = wl.get("index", False)
     snap16 = wl.get("snap16", False)
+    tree = wl.get("tree", False)
     batched = wl_name.startswith("batched8x16")
     L = args.layers if (args.layers and batched) else wl["layers"]
-    vbytes = verify_bytes(B, N, Hk, Hv, dk, dv, tree=wl.get("tree", False), persist=not replay,
+    vbytes = verify_bytes(B, N, Hk, Hv, dk, dv, tree=tree, persist=not replay,
                           snap_bytes=2 if snap16 else 4)
     if batched:
         # every step moves far more than L2; the flush before it is not timed
@@ -506,7 +591,7 @@ def run_ours(args, wl_name, world, rank, local):
                 if not replay:
                     c.snap = ws.snap_all[l]
         else:
-            inp = synthetic.tree22() if wl.get("tree") else synthetic.chain16()
+            inp = synthetic.tree22() if tree else synthetic.chain16()
             ws.layers = [VerifyCase(inp, torch, pinned=True, persist=not replay, snap16=snap16)]
             ws.cache_all = ws.layers[0].cache
             ws.snap_all = ws.layers[0].snap
@@ -528,67 +613,44 @@ def run_ours(args, wl_name, world, rank, local):
         return ws
 
     def commit(ws):
+        """The binding's plain (checked) commit of a set."""
         if index:
             gdn.gdn_commit_index(ws.accept, ws.slot_idx, N=N)
-            return
-        if replay:
-            # checkpoint and replay: the accepted prefix of every layer again
+        elif replay:
             for c in ws.layers:
                 c.replay(gdn)
-            return
-        gdn.gdn_commit_accepted(ws.snap_all, ws.accept, ws.cache_all, B=B, N=N, Hv=Hv, dk=dk,
-                                dv=dv, n_layers=len(ws.layers),
-                                snap_layer_stride=B * N * Hv * dk * dv,
-                                cache_layer_stride=B * Hv * dk * dv, slot=ws.slot, n_slots=B)
-
-    def step(ws, ev=None):
-        """verify every layer, then commit, through the binding's functions;
-        ev = (start, after_verify, end) events."""
-        if ev is not None:
-            ev[0].record(stream)
-        for c in ws.layers:
-            c.verify(gdn)
-        if ev is not None:
-            ev[1].record(stream)
-        commit(ws)
-        if ev is not None:
-            ev[2].record(stream)
+        else:
+            gdn.gdn_commit_accepted(ws.snap_all, ws.accept, ws.cache_all, B=B, N=N, Hv=Hv, dk=dk,
+                                    dv=dv, n_layers=len(ws.layers),
+                                    snap_layer_stride=B * N * Hv * dk * dv,
+                                    cache_layer_stride=B * Hv * dk * dv, slot=ws.slot, n_slots=B)
 
     def bind_set(ws):
-        """The set's step as pre-marshalled C-ABI calls (see VerifyCase.bind)."""
-        import ctypes
-
-        lib = gdn.load()
-        s = ctypes.c_void_p(stream.cuda_stream)
+        """The set's step as bound calls."""
         for c in ws.layers:
             c.bind(gdn, stream)
         if index:
-            acc, sl = ctypes.c_void_p(ws.accept.data_ptr()), ctypes.c_void_p(ws.slot_idx.data_ptr())
-            ws.commit_c = [lambda: lib.gdn_commit_index(acc, B, N, 0, sl, None, s)]
+            ws.commit_c = [lambda: gdn.gdn_commit_index(ws.accept, ws.slot_idx, N=N,
+                                                        stream=stream)]
         elif replay:
             ws.commit_c = [c.replay_c for c in ws.layers]
         else:
-            fn = lib.gdn_commit_accepted_f16 if snap16 else lib.gdn_commit_accepted
-            cargs = (ctypes.c_void_p(ws.snap_all.data_ptr()), B * N * Hv * dk * dv,
-                     ctypes.c_void_p(ws.accept.data_ptr()),
-                     ctypes.c_void_p(ws.cache_all.data_ptr()), Hv * dk * dv, B * Hv * dk * dv,
-                     ctypes.c_void_p(ws.slot.data_ptr()), B, B, N, Hv, dk, dv,
-                     len(ws.layers), None, s)
-            ws.commit_c = [lambda: fn(*cargs)]
+            ws.commit_c = [gdn.bind_commit_accepted(
+                ws.snap_all, ws.accept, ws.cache_all, B=B, N=N, Hv=Hv, dk=dk, dv=dv,
+                n_layers=len(ws.layers), snap_layer_stride=B * N * Hv * dk * dv,
+                cache_layer_stride=B * Hv * dk * dv, slot=ws.slot, n_slots=B, stream=stream)]
         ws.verify_c = [c.verify_c for c in ws.layers]
 
     def step_c(ws, ev=None):
-        """step() through the pre-marshalled calls; any non-zero status raises."""
+        """One step through the bound calls; ev = (start, after verify, end)."""
         if ev is not None:
             ev[0].record(stream)
         for f in ws.verify_c:
-            if f():
-                raise RuntimeError("verify launch failed")
+            f()
         if ev is not None:
             ev[1].record(stream)
         for f in ws.commit_c:
-            if f():
-                raise RuntimeError("commit launch failed")
+            f()
         if ev is not None:
             ev[2].record(stream)
 
@@ -597,9 +659,12 @@ def run_ours(args, wl_name, world, rank, local):
         bind_set(ws)
     layers = sets[0].layers
     launches_per_step = len(layers) * 2 if replay else len(layers) + 1
+    # warm-up: the binding's checked calls once per set, then the bound calls
+    for ws in sets:
+        for c in ws.layers:
+            c.verify(gdn)
+        commit(ws)
     n_warm = max(args.warmup, n_sets)
-    for i in range(n_warm):  # the binding's own functions, then the bound calls
-        step(sets[i % n_sets])
     th = time.perf_counter()
     for i in range(n_warm):
         if flush_each:
@@ -608,97 +673,112 @@ def run_ours(args, wl_name, world, rank, local):
     host_s = (time.perf_counter() - th) / n_warm
     torch.cuda.synchronize()
 
-    gpu_id = gpu_uuid(torch, local)
-    sampler = ClockSampler(gpu_id)
-    sampler.start()
-    time.sleep(0.25)
     barrier(world)
     if not flush_each:
         flush.fill_(0.0)  # the first timed step starts from an L2 without its data
     torch.cuda.synchronize()
     t0 = time.time()
-    hold_device(torch, host_s, args.steps)
+    K = args.steps
     if flush_each:
-        # the flush between steps is excluded: one event pair per step phase
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
-               for _ in range(args.steps)]
-        for i in range(args.steps):
+        # the timed K steps, one event pair per step phase; the flush between
+        # steps is excluded
+        hold_device(torch, host_s, K)
+        evs = [ctx.events(3) for _ in range(K)]
+        for i in range(K):
             flush.fill_(float(i))
             step_c(sets[i % n_sets], evs[i])
         torch.cuda.synchronize()
-        step_ms = [e[0].elapsed_time(e[2]) for e in evs]
-        verify_ms = [e[0].elapsed_time(e[1]) / len(layers) for e in evs]
-        total_ms = sum(step_ms)
+        step_list = [e[0].elapsed_time(e[2]) for e in evs]
+        kernel_list = [e[0].elapsed_time(e[1]) / len(layers) for e in evs]
+        total_ms = sum(step_list)
+        step_stats = stats_ms(step_list, "one event pair per step (flush before each step "
+                                         "not timed)")
+        kernel_stats = stats_ms(kernel_list, "verify phase of each timed step / layers")
     else:
-        # back-to-back steps between one event pair, as a serving loop issues them
-        e_run = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        # the timed K steps back to back between one event pair, as a serving
+        # loop issues them
+        hold_device(torch, host_s, K)
+        e_run = ctx.events(2)
         e_run[0].record(stream)
-        for i in range(args.steps):
+        for i in range(K):
             step_c(sets[i % n_sets])
         e_run[1].record(stream)
         torch.cuda.synchronize()
         total_ms = e_run[0].elapsed_time(e_run[1])
-        step_ms = None
-        # the dominant kernel on its own: verify launches back to back over the
-        # same rotating copies (every launch again misses L2), one event pair
-        k_roof = min(args.steps, 1000)
-        hold_device(torch, host_s, k_roof)
-        e_roof = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        e_roof[0].record(stream)
-        for i in range(k_roof):
-            for f in sets[i % n_sets].verify_c:
-                if f():
-                    raise RuntimeError("verify launch failed")
-        e_roof[1].record(stream)
-        torch.cuda.synchronize()
-        verify_ms = [e_roof[0].elapsed_time(e_roof[1]) / (k_roof * len(layers))]
+        # percentiles: further blocks of back-to-back steps, one event pair per
+        # block (an event between two steps would break the programmatic
+        # overlap, so per-step pairs are not used here)
+        kb = max(20, K)
+        per_step = []
+        for r in range(STAT_BLOCKS):
+            hold_device(torch, host_s, kb)
+            e = ctx.events(2)
+            e[0].record(stream)
+            for i in range(kb):
+                step_c(sets[(r * kb + i) % n_sets])
+            e[1].record(stream)
+            torch.cuda.synchronize()
+            per_step.append(e[0].elapsed_time(e[1]) / kb)
+        step_stats = stats_ms(per_step, f"{STAT_BLOCKS} blocks of {kb} back-to-back steps, "
+                                        "one event pair per block; per-step mean of each block")
+        # the dominant kernel on its own: verify launches back to back over
+        # the same rotating copies (every launch again misses L2)
+        per_launch = []
+        for r in range(STAT_BLOCKS):
+            hold_device(torch, host_s / 2, KERNEL_BLOCK)
+            e = ctx.events(2)
+            e[0].record(stream)
+            for i in range(KERNEL_BLOCK):
+                for f in sets[(r * KERNEL_BLOCK + i) % n_sets].verify_c:
+                    f()
+            e[1].record(stream)
+            torch.cuda.synchronize()
+            per_launch.append(e[0].elapsed_time(e[1]) / (KERNEL_BLOCK * len(layers)))
+        kernel_stats = stats_ms(per_launch, f"{STAT_BLOCKS} blocks of {KERNEL_BLOCK} "
+                                            "back-to-back verify launches over the rotating "
+                                            "copies, one event pair per block")
     barrier(world)
     t1 = time.time()
-    time.sleep(0.25)
-    sampler.stop()
     total_ms = max_over_ranks(total_ms, world)
 
-    # end to end through the public API: host inputs -> device -> verify/commit -> host o
+    # end to end through the bound calls: every step copies its inputs from
+    # pinned host memory and its outputs back; the whole run is enqueued
+    # asynchronously and timed on the host clock around it
     for ws in sets:
         if ws.cache_init is not None:
             ws.cache_all.copy_(ws.cache_init)
-    e2e_steps = min(args.steps, 200)
-    e2e_s = 0.0
+    e2e_steps = max(K, 50 if batched else 400)
     h2d = d2h = 0
-    for i in range(e2e_steps + 3):
+    for i in range(3):   # warm the copy paths
         ws = sets[i % n_sets]
-        flush.fill_(float(i))
-        torch.cuda.synchronize()
-        ta = time.perf_counter()
+        for c in ws.layers:
+            c.h2d()
+        step_c(ws)
+        for c in ws.layers:
+            c.d2h()
+    torch.cuda.synchronize()
+    barrier(world)
+    ta = time.perf_counter()
+    for i in range(e2e_steps):
+        ws = sets[i % n_sets]
         h2d = sum(c.h2d() for c in ws.layers)
-        step(ws)
+        step_c(ws)
         d2h = sum(c.d2h() for c in ws.layers)
-        torch.cuda.synchronize()
-        if i >= 3:
-            e2e_s += time.perf_counter() - ta
-    e2e_s = max_over_ranks(e2e_s, world)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - ta, world)
 
     node_heads = B * N * Hv * len(layers)
-    value = job_throughput(node_heads, args.steps, total_ms, world)
-    hbm, bf16, peak_kind = measured_peaks()
-    launch_ms = statistics.mean(verify_ms)
-    achieved = vbytes / (launch_ms / 1e3) / 1e9
-    clocks = sampler.summary(t0, t1)
-    if rank != 0:
-        return None
-    return {
+    hbm, _, peak_kind = ctx.peaks
+    kname = ("gdn_verify_tree" if tree else "gdn_verify_chain") + \
+        (" (no snapshots)" if replay else " (binary16 snapshots)" if snap16 else
+         " (state and snapshots in the slot region)" if index else "")
+    out = {
         "metric": METRIC,
-        "value": value,
+        "value": job_throughput(node_heads, K, total_ms, world),
         "unit": "node-heads/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": total_ms / args.steps,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f32",
-        "data": "synthetic",
+        "steps": K,
+        "ms_per_step": total_ms / K,
+        "step_ms": step_stats,
         "config": {
             "workload": f"{wl_name}: {wl['desc']}",
             "B": B, "N": N, "Hk": Hk, "Hv": Hv, "dk": dk, "dv": dv, "layers": len(layers),
@@ -711,42 +791,33 @@ def run_ours(args, wl_name, world, rank, local):
                    f"{(vbytes + commit_bytes(B, Hv, dk, dv)) / 1e6:.1f} MB > 2 x 129 MB)"),
             "timing": ("CUDA events on the launch stream around each step's verify and "
                        "commit phases" if flush_each else
-                       "CUDA events on the launch stream around the K back-to-back steps; the "
-                       "verify kernel alone from a second back-to-back run of verify launches"),
+                       "CUDA events on the launch stream around the K back-to-back steps"),
             "launch": "programmatic dependent launch (each kernel waits on its predecessor "
-                      "before any global-memory access)",
+                      "before any global-memory access); bound calls, one ctypes call per "
+                      "launch",
             "parallelism": f"replicas x{world}, no collective",
-            "verify_ms_per_launch": launch_ms,
-            **({"step_ms_p10": float(np.percentile(step_ms, 10)),
-                "step_ms_p90": float(np.percentile(step_ms, 90))} if step_ms else {}),
         },
-        "roofline": {
-            "bound": "hbm",
-            "kernel": ("gdn_verify_tree" if wl.get("tree") else "gdn_verify_chain") +
-                      (" (no snapshots)" if replay else
-                       " (binary16 snapshots)" if wl.get("snap16") else
-                       " (state and snapshots in the slot region)" if index else ""),
-            "achieved": achieved,
-            "peak": hbm,
-            "unit": "GB/s",
-            "frac": achieved / hbm,
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
-            "measured" else "fallback 6.8 TB/s",
-            "algorithmic_bytes_per_launch": vbytes,
-            "traffic": profiled_traffic("verify", wl_name),
-        },
-        "e2e": {
-            "value": world * node_heads * e2e_steps / e2e_s,
-            "unit": "node-heads/s",
-            "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h,
-        },
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
+        "kernel_ms": kernel_stats,
+        "roofline": roofline_entry("hbm", kname, vbytes, kernel_stats["p50"], hbm, peak_kind,
+                                   profiled_traffic("verify", wl_name),
+                                   "algorithmic_bytes_per_launch"),
+        "e2e": {"value": world * node_heads * e2e_steps / e2e_s, "unit": "node-heads/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "how": "bound calls; per step the packed inputs copied from pinned host memory "
+                       "and the outputs o copied back, all enqueued on the stream, host clock "
+                       "around the run"},
+        "gpu_launches": launches_per_step * K,
+        "clocks": ctx.sampler.summary(t0, t1),
     }
+    del sets
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
 
 
-def run_prefill(args, gdn, torch, flush, world, rank, local):
+def measure_prefill(ctx, wl_name="prefill8192"):
+    torch, gdn, args, stream, flush = ctx.torch, ctx.gdn, ctx.args, ctx.stream, ctx.flush
+    world = ctx.world
     inp = synthetic.prefill8192()
     T, Hk, Hv, dk, dv = inp["T"], inp["Hk"], inp["Hv"], inp["dk"], inp["dv"]
     q, k, v = (_dev(inp[n], torch) for n in ("q", "k", "v"))
@@ -754,97 +825,135 @@ def run_prefill(args, gdn, torch, flush, world, rank, local):
     state0 = _dev(inp["state"], torch)
     state = state0.clone()
     o = torch.empty((T, Hv, dv), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     wbytes = gdn.gdn_prefill_workspace_bytes(T, Hk, Hv, dk, dv, 64)
     ws = torch.empty(max(wbytes, 16), dtype=torch.uint8, device="cuda")
-    stream = torch.cuda.current_stream()
+    call = gdn.bind_prefill_chunked(q, k, v, alpha, beta, state, o, ws, status=status,
+                                    stream=stream)
 
     def step(ev=None):
         state.copy_(state0)
         if ev is not None:
             ev[0].record(stream)
-        gdn.gdn_prefill_chunked(q, k, v, alpha, beta, state, o, ws)
+        call()
         if ev is not None:
             ev[1].record(stream)
 
+    gdn.gdn_prefill_chunked(q, k, v, alpha, beta, state, o, ws)   # the checked call once
     th = time.perf_counter()
     for _ in range(args.warmup):
         flush.fill_(1.0)
         step()
     host_s = (time.perf_counter() - th) / max(1, args.warmup)
     torch.cuda.synchronize()
-    sampler = ClockSampler(gpu_uuid(torch, local))
-    sampler.start()
-    time.sleep(0.25)
-    steps = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    K = args.steps
+    # the K timed calls, then more for the percentiles, each with its own
+    # event pair and the flush before it untimed
+    n_stat = max(K, 30)
+    evs = [ctx.events(2) for _ in range(K + n_stat)]
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
-    hold_device(torch, host_s, steps)
-    for i in range(steps):
+    hold_device(torch, host_s, K + n_stat)
+    for i in range(K + n_stat):
         flush.fill_(float(i))
         step(evs[i])
     torch.cuda.synchronize()
     barrier(world)
     t1 = time.time()
-    time.sleep(0.25)
-    sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"prefill status {gdn.status_string(int(status.item()))}")
     ms = [e[0].elapsed_time(e[1]) for e in evs]
-    total_ms = max_over_ranks(sum(ms), world)
-    # end to end: host inputs (pinned) -> device -> prefill -> host o and state
+    total_ms = max_over_ranks(sum(ms[:K]), world)
+    call_stats = stats_ms(ms, "one event pair per call (prep + scan kernels), 256 MiB flush "
+                              "before each call not timed")
+    # end to end: host inputs (pinned) -> device -> prefill -> host o and state,
+    # enqueued on the stream for every step, host clock around the run
     hq, hk, hv, ha, hb = (x.cpu().pin_memory() for x in (q, k, v, alpha, beta))
     hs0 = state0.cpu().pin_memory()
     ho = torch.empty(o.shape).pin_memory()
     hst = torch.empty(state.shape).pin_memory()
-    e2e_steps = min(steps, 20)
-    e2e_s = 0.0
-    for i in range(e2e_steps + 2):
-        flush.fill_(float(i))
-        torch.cuda.synchronize()
-        ta = time.perf_counter()
-        for d, h in ((q, hq), (k, hk), (v, hv), (alpha, ha), (beta, hb), (state, hs0)):
+    pairs = ((q, hq), (k, hk), (v, hv), (alpha, ha), (beta, hb), (state, hs0))
+
+    def e2e_step():
+        for d, h in pairs:
             d.copy_(h, non_blocking=True)
-        gdn.gdn_prefill_chunked(q, k, v, alpha, beta, state, o, ws)
+        call()
         ho.copy_(o, non_blocking=True)
         hst.copy_(state, non_blocking=True)
-        torch.cuda.synchronize()
-        if i >= 2:
-            e2e_s += time.perf_counter() - ta
-    e2e_s = max_over_ranks(e2e_s, world)
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, ha, hb, hs0))
+
+    e2e_steps = max(min(K, 40), 10)
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    ta = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - ta, world)
+    h2d = sum(h.numel() * h.element_size() for _, h in pairs)
     d2h = ho.numel() * 4 + hst.numel() * 4
-    hbm, bf16, kind = measured_peaks()
+    hbm, bf16, kind = ctx.peaks
     pbytes = prefill_bytes(T, Hk, Hv, dk, dv)
-    launch_ms = statistics.mean(ms)
-    gbs = pbytes / (launch_ms / 1e3) / 1e9
     flops = prefill_flops(T, Hk, Hv, dk, dv)
-    tflops = flops / (launch_ms / 1e3) / 1e12
-    if rank != 0:
-        return None
-    return {
+    launch_ms = call_stats["p50"]
+    gbs = pbytes / (launch_ms / 1e3) / 1e9
+    out = {
         "metric": METRIC,
-        "value": world * T * Hv * steps / (total_ms / 1e3),
+        "value": world * T * Hv * K / (total_ms / 1e3),
         "unit": "token-heads/s",
-        "n_gpus": world, "steps": steps, "warmup": args.warmup,
-        "ms_per_step": total_ms / steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"prefill8192: {WORKLOADS['prefill8192']['desc']}",
+        "steps": K,
+        "ms_per_step": total_ms / K,
+        "step_ms": call_stats,
+        "config": {"workload": f"{wl_name}: {WORKLOADS[wl_name]['desc']}",
                    "T": T, "Hk": Hk, "Hv": Hv, "dk": dk, "dv": dv, "chunk": 64,
-                   "l2": "flushed by a 256 MiB write before every step; flush not timed",
+                   "l2": "flushed by a 256 MiB write before every call; flush not timed",
                    "timing": "CUDA events around each prefill call (prep + scan kernels) "
                              "on the launch stream",
                    "hbm_achieved_gbs": gbs, "hbm_frac_of_measured": gbs / hbm,
-                   "algorithmic_bytes_per_call": pbytes},
-        "roofline": {"bound": "tensor", "kernel": "gdn_prefill_chunked (prep + scan)",
-                     "achieved": tflops, "peak": bf16, "unit": "TFLOP/s", "frac": tflops / bf16,
-                     "peak_source": kind, "algorithmic_flops_per_launch": flops,
-                     "traffic": profiled_traffic("prefill", "prefill8192")},
+                   "algorithmic_bytes_per_call": pbytes,
+                   "workspace_bytes": wbytes},
+        "kernel_ms": call_stats,
+        "roofline": roofline_entry("tensor", "gdn_prefill_chunked (prep + scan)", flops,
+                                   launch_ms, bf16, kind, profiled_traffic("prefill", wl_name),
+                                   "algorithmic_flops_per_launch"),
         "e2e": {"value": world * T * Hv * e2e_steps / e2e_s, "unit": "token-heads/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * steps,   # prep + scan per call
-        "clocks": sampler.summary(t0, t1),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "how": "bound call; per step q, k, v, gates and the initial state copied from "
+                       "pinned host memory, o and the final state copied back, all enqueued "
+                       "on the stream, host clock around the run"},
+        "gpu_launches": 2 * K,   # prep + scan per call
+        "clocks": ctx.sampler.summary(t0, t1),
     }
+    del ws, o, q, k, v
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure(ctx, wl_name):
+    if wl_name == "prefill8192":
+        return measure_prefill(ctx, wl_name)
+    return measure_verify(ctx, wl_name)
+
+
+def run_ours(args, world, rank, local):
+    ctx = Context(args, world, rank, local)
+    try:
+        name = args.workload or HEADLINE
+        out = measure(ctx, name)
+        if args.workload is None and not args.no_nested:
+            out["workloads"] = {n: measure(ctx, n) for n in NESTED}
+    finally:
+        ctx.close()
+    if rank != 0:
+        return None
+    line = {"metric": METRIC, "value": out["value"], "unit": out["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": out["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic"}
+    line.update({k: v for k, v in out.items() if k not in line})
+    return line
 
 
 def gpu_uuid(torch, local):
@@ -885,29 +994,27 @@ def job_throughput(units_per_step_per_rank, steps, max_rank_ms, world):
 
 # -------------------------------------------------------------- reference arm
 def run_reference(args, wl_name, world, rank):
+    """The oracle as it stands on this host's cores, each step one bounded
+    sample of the workload per host thread."""
     if rank != 0:
         return None
-    if wl_name == "prefill8192":
-        for _ in range(args.warmup):
-            oracle_step_sample(wl_name, 1)
-        spent, done = 0.0, 0
-        for _ in range(args.steps):
-            dt, n = oracle_step_sample(wl_name, 1)
-            spent += dt
-            done += n
-        unit, sample = "token-heads/s", "8192 tokens x 1 value head per step (step form)"
-    else:
-        smp = OracleSampler(wl_name)
-        for _ in range(args.warmup):
-            smp.run(1)
+    smp = OracleSampler(wl_name)
+    cores, model = host_cpu()
+    n_heads = 1
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        def one_step(i):
+            return sum(f.result() for f in [ex.submit(smp.run, (i * cores + j) * n_heads, n_heads)
+                                            for j in range(cores)])
+        for i in range(args.warmup):
+            one_step(i)
         done = 0
         t0 = time.perf_counter()
-        for _ in range(args.steps):
-            done += smp.run(1)
+        for i in range(args.steps):
+            done += one_step(args.warmup + i)
         spent = time.perf_counter() - t0
-        unit = "node-heads/s"
-        sample = f"verify + commit of 1 value head x {smp.inp['N']} nodes per step"
     value = done / spent
+    unit = smp.unit
+    sample = f"{cores} samples per step on {cores} threads, each {smp.describe(n_heads)}"
     wl = WORKLOADS[wl_name]
     return {
         "metric": METRIC, "value": value, "unit": unit, "impl": "reference",
@@ -915,8 +1022,8 @@ def run_reference(args, wl_name, world, rank):
         "ms_per_step": 1e3 * spent / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{wl_name}: {wl['desc']}"},
-        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                         "sample": sample, "cpu_model": model},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -924,14 +1031,18 @@ def run_reference(args, wl_name, world, rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="chain16", choices=sorted(WORKLOADS))
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=None, choices=sorted(WORKLOADS),
+                    help="measure this workload alone (default: chain16 headline with the "
+                         "other workloads nested)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=0,
                     help="batched8x16 only: run this many of the 48 layers (profiling slices)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (for quick runs)")
+    ap.add_argument("--no-nested", action="store_true",
+                    help="headline workload only, without the nested workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -939,12 +1050,15 @@ def main():
     if args.gpus != world and world > 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
     if args.impl == "reference":
-        out = run_reference(args, args.workload, world, rank)
+        out = run_reference(args, args.workload or HEADLINE, world, rank)
     else:
-        out = run_ours(args, args.workload, world, rank, local)
-        if out is not None:
-            out["cpu_baseline"] = (None if args.no_cpu_baseline or world > 1 else
-                                   cpu_baseline(args.workload))
+        out = run_ours(args, world, rank, local)
+        if out is not None and world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(args.workload or HEADLINE)
+            for name, sub in out.get("workloads", {}).items():
+                sub["cpu_baseline"] = cpu_baseline(name, budget_s=3.0)
+        elif out is not None:
+            out["cpu_baseline"] = None
     if out is not None:
         print(json.dumps(out), flush=True)
 

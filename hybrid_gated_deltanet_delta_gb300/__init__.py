@@ -11,6 +11,10 @@ Entry points (same names as the C ABI):
   gdn_commit_accepted_f16, gdn_commit_index, gdn_conv_commit,
   gdn_replay_accepted,
   gdn_prefill_chunked, gdn_prefill_workspace_bytes, gdn_prefill_chunked_noalloc
+and, for serving loops that issue the same call every step, bound calls
+(bind_verify_chain, bind_verify_tree, bind_commit_accepted,
+bind_replay_accepted, bind_prefill_chunked): the arguments are marshalled once
+and each call is one ctypes call.
 """
 from __future__ import annotations
 
@@ -30,6 +34,7 @@ GDN_ERR_ACCEPT_RANGE = -6
 GDN_ERR_SLOT_RANGE = -7
 GDN_ERR_WORKSPACE = -8
 GDN_ERR_SCRATCH_LIMIT = -9
+GDN_ERR_TIMEOUT = -10
 PREFILL_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 GDN_F32 = 0
@@ -55,7 +60,7 @@ class VerifyArgs(ctypes.Structure):
         ("B", ctypes.c_int32), ("N", ctypes.c_int32), ("Hk", ctypes.c_int32),
         ("Hv", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
         ("in_dtype", ctypes.c_int32), ("tile_cols", ctypes.c_int32),
-        ("row_warps", ctypes.c_int32),
+        ("row_warps", ctypes.c_int32), ("max_depth", ctypes.c_int32),
     ]
 
 
@@ -97,10 +102,10 @@ def load(path: str | None = None):
     lib.gdn_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.gdn_prefill_workspace_bytes.restype = sz
     lib.gdn_prefill_chunked.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, P, P,
-                                        P, sz, P]
+                                        P, sz, P, P]
     lib.gdn_prefill_chunked.restype = ctypes.c_int
     lib.gdn_prefill_chunked_noalloc.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32,
-                                                P, P, P]
+                                                P, P, P, P]
     lib.gdn_prefill_chunked_noalloc.restype = ctypes.c_int
     lib.gdn_status_string.argtypes = [ctypes.c_int]
     lib.gdn_status_string.restype = ctypes.c_char_p
@@ -152,7 +157,8 @@ def _need(cond, msg):
 
 
 def make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, *, slot=None, n_slots=None,
-                     status=None, cache_slot_stride=None, tile_cols=0, row_warps=0):
+                     status=None, cache_slot_stride=None, tile_cols=0, row_warps=0,
+                     max_depth=0):
     """Build a gdn_verify_args from tensors.  q, k [B,N,Hk,dk]; v [B,N,Hv,dv];
     alpha, beta [B,N,Hv] fp32; state_cache [n_slots,Hv,dk,dv] fp32 (or any
     buffer with `cache_slot_stride`); snapshots [B,N,Hv,dk,dv] fp32 or None
@@ -177,7 +183,8 @@ def make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, *, slot=No
         beta=beta.data_ptr(), state_cache=state_cache.data_ptr(), slot=ptr(slot),
         snapshots=ptr(snapshots), o=ptr(o), status=ptr(status),
         cache_slot_stride=cache_slot_stride, n_slots=n_slots, B=B, N=N, Hk=Hk, Hv=Hv, dk=dk,
-        dv=dv, in_dtype=_dtype_code(k), tile_cols=tile_cols, row_warps=row_warps)
+        dv=dv, in_dtype=_dtype_code(k), tile_cols=tile_cols, row_warps=row_warps,
+        max_depth=max_depth)
 
 
 def gdn_verify_chain(q, k, v, alpha, beta, state_cache, snapshots, o, *, slot=None, n_slots=None,
@@ -212,14 +219,15 @@ def gdn_verify_chain_f16(q, k, v, alpha, beta, state_cache, snapshots_f16, o, *,
 
 def gdn_verify_tree(q, k, v, alpha, beta, state_cache, snapshots, o, parent, *, depth_out=None,
                     slot=None, n_slots=None, status=None, cache_slot_stride=None, tile_cols=0,
-                    row_warps=0, stream=None, prep=False):
-    """Tree verification; parent [B,N] int32 (see include/gdn.h).  prep=True:
-    raw projections and gate pre-activations (gdn_verify_tree_prep)."""
+                    row_warps=0, max_depth=0, stream=None, prep=False):
+    """Tree verification; parent [B,N] int32 (see include/gdn.h).  max_depth > 0
+    skips (and reports through `status`) any sequence whose tree is deeper.
+    prep=True: raw projections and gate pre-activations (gdn_verify_tree_prep)."""
     _need(parent.is_contiguous() and tuple(parent.shape) == tuple(q.shape[:2]),
           "parent must be a contiguous [B,N] int32 tensor")
     a = make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, slot=slot,
                          n_slots=n_slots, status=status, cache_slot_stride=cache_slot_stride,
-                         tile_cols=tile_cols, row_warps=row_warps)
+                         tile_cols=tile_cols, row_warps=row_warps, max_depth=max_depth)
     fn = load().gdn_verify_tree_prep if prep else load().gdn_verify_tree
     _check(fn(ctypes.byref(a), _ptr(parent), _ptr(depth_out), _stream(stream)),
            "gdn_verify_tree_prep" if prep else "gdn_verify_tree")
@@ -303,20 +311,23 @@ def gdn_prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk=64) -> int:
 
 
 def gdn_prefill_chunked(q, k, v, alpha, beta, state, o, workspace=None, *, chunk=64,
-                        stream=None):
+                        status=None, stream=None):
     """Chunked prefill of one sequence: q, k [T,Hk,dk]; v [T,Hv,dv]; alpha, beta [T,Hv];
     state [Hv,dk,dv] fp32 in/out; o [T,Hv,dv] fp32; workspace a uint8 device tensor of
-    gdn_prefill_workspace_bytes(...) bytes (or None when that is 0)."""
+    gdn_prefill_workspace_bytes(...) bytes (or None when that is 0); status an
+    optional int32 device word that receives GDN_ERR_TIMEOUT if a bounded wait
+    inside the kernel expired."""
     T, Hk, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().gdn_prefill_chunked(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha),
                                       _ptr(beta), T, Hk, Hv, dk, dv, chunk, _ptr(state), _ptr(o),
-                                      _ptr(workspace), wbytes, _stream(stream)),
+                                      _ptr(workspace), wbytes, _ptr(status), _stream(stream)),
            "gdn_prefill_chunked")
 
 
-def gdn_prefill_chunked_noalloc(q, k, v, alpha, beta, state, o, *, chunk=64, stream=None):
+def gdn_prefill_chunked_noalloc(q, k, v, alpha, beta, state, o, *, chunk=64, status=None,
+                                stream=None):
     """gdn_prefill_chunked on the library's built-in device scratch, for callers
     that cannot allocate device memory (no workspace argument).  Problems whose
     workspace would exceed PREFILL_NOALLOC_SCRATCH_BYTES raise GdnError with
@@ -326,5 +337,95 @@ def gdn_prefill_chunked_noalloc(q, k, v, alpha, beta, state, o, *, chunk=64, str
     Hv, dv = v.shape[1], v.shape[2]
     _check(load().gdn_prefill_chunked_noalloc(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q),
                                               _ptr(alpha), _ptr(beta), T, Hk, Hv, dk, dv, chunk,
-                                              _ptr(state), _ptr(o), _stream(stream)),
+                                              _ptr(state), _ptr(o), _ptr(status),
+                                              _stream(stream)),
            "gdn_prefill_chunked_noalloc")
+
+
+# ------------------------------------------------------- bound calls (serving)
+class BoundCall:
+    """One entry point with its arguments marshalled once.
+
+    A serving loop that issues the same call every step (the same buffers,
+    refilled in place) binds it once; each call then costs a single ctypes
+    call: no shape checks, no argument struct built, no stream lookup.  The
+    tensors given at binding time are kept alive by this object and must keep
+    their addresses and shapes; the stream is fixed at binding time.  A
+    non-zero status from the library raises GdnError, as the plain functions
+    do."""
+
+    __slots__ = ("_fn", "_name", "_args", "_keep")
+
+    def __init__(self, fn, name, args, keep):
+        self._fn, self._name, self._args, self._keep = fn, name, tuple(args), keep
+
+    def __call__(self):
+        code = self._fn(*self._args)
+        if code != GDN_OK:
+            raise GdnError(code, self._name)
+
+
+def bind_verify_chain(q, k, v, alpha, beta, state_cache, snapshots, o, *, snapshots_f16=None,
+                      stream=None, **kw):
+    """gdn_verify_chain (or, with snapshots_f16, gdn_verify_chain_f16) bound
+    to these buffers; keyword arguments as for gdn_verify_chain."""
+    a = make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, **kw)
+    s = _stream(stream)
+    if snapshots_f16 is not None:
+        return BoundCall(load().gdn_verify_chain_f16, "gdn_verify_chain_f16",
+                         (ctypes.byref(a), _ptr(snapshots_f16), s),
+                         (a, q, k, v, alpha, beta, state_cache, snapshots_f16, o))
+    return BoundCall(load().gdn_verify_chain, "gdn_verify_chain", (ctypes.byref(a), s),
+                     (a, q, k, v, alpha, beta, state_cache, snapshots, o))
+
+
+def bind_verify_tree(q, k, v, alpha, beta, state_cache, snapshots, o, parent, *, depth_out=None,
+                     stream=None, **kw):
+    """gdn_verify_tree bound to these buffers; keyword arguments as for
+    gdn_verify_tree."""
+    _need(parent.is_contiguous() and tuple(parent.shape) == tuple(k.shape[:2]),
+          "parent must be a contiguous [B,N] int32 tensor")
+    a = make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, **kw)
+    return BoundCall(load().gdn_verify_tree, "gdn_verify_tree",
+                     (ctypes.byref(a), _ptr(parent), _ptr(depth_out), _stream(stream)),
+                     (a, q, k, v, alpha, beta, state_cache, snapshots, o, parent, depth_out))
+
+
+def bind_commit_accepted(snapshots, accept_idx, state_cache, *, B, N, Hv, dk, dv, n_layers=1,
+                         snap_layer_stride=0, cache_slot_stride=None, cache_layer_stride=0,
+                         slot=None, n_slots=None, status=None, stream=None):
+    """gdn_commit_accepted (gdn_commit_accepted_f16 for float16 snapshots)
+    bound to these buffers."""
+    if cache_slot_stride is None:
+        cache_slot_stride = Hv * dk * dv
+    if n_slots is None:
+        n_slots = (state_cache.numel() - (n_layers - 1) * cache_layer_stride) // cache_slot_stride
+    fn, name = load().gdn_commit_accepted, "gdn_commit_accepted"
+    if snapshots.dtype != state_cache.dtype:
+        fn, name = load().gdn_commit_accepted_f16, "gdn_commit_accepted_f16"
+    args = (_ptr(snapshots), snap_layer_stride, _ptr(accept_idx), _ptr(state_cache),
+            cache_slot_stride, cache_layer_stride, _ptr(slot), n_slots, B, N, Hv, dk, dv,
+            n_layers, _ptr(status), _stream(stream))
+    return BoundCall(fn, name, args, (snapshots, accept_idx, state_cache, slot, status))
+
+
+def bind_replay_accepted(k, v, alpha, beta, state_cache, accept_idx, *, parent=None, stream=None,
+                         **kw):
+    """gdn_replay_accepted bound to these buffers."""
+    a = make_verify_args(None, k, v, alpha, beta, state_cache, None, None, **kw)
+    return BoundCall(load().gdn_replay_accepted, "gdn_replay_accepted",
+                     (ctypes.byref(a), _ptr(parent), _ptr(accept_idx), _stream(stream)),
+                     (a, k, v, alpha, beta, state_cache, accept_idx, parent))
+
+
+def bind_prefill_chunked(q, k, v, alpha, beta, state, o, workspace=None, *, chunk=64,
+                         status=None, stream=None):
+    """gdn_prefill_chunked bound to these buffers."""
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    args = (_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), _ptr(beta), T, Hk, Hv, dk,
+            dv, chunk, _ptr(state), _ptr(o), _ptr(workspace), wbytes, _ptr(status),
+            _stream(stream))
+    return BoundCall(load().gdn_prefill_chunked, "gdn_prefill_chunked", args,
+                     (q, k, v, alpha, beta, state, o, workspace, status))

@@ -1,11 +1,35 @@
 // The C ABI (include/gdn.h): argument checks, tile choice and launches.
 // Nothing here allocates, synchronises or keeps state between calls.
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
 
 namespace {
+
+// NVTX range around one entry point, pushed only when GDN_NVTX is set (to
+// anything but "0") at the first call; the header-only NVTX calls are no-ops
+// unless a profiler injects itself.
+bool nvtx_on() {
+  static const bool on = [] {
+    const char* e = getenv("GDN_NVTX");
+    return e != nullptr && e[0] != '\0' && !(e[0] == '0' && e[1] == '\0');
+  }();
+  return on;
+}
+
+struct Range {
+  const bool on;
+  explicit Range(const char* name) : on(nvtx_on()) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~Range() {
+    if (on) nvtxRangePop();
+  }
+};
+#define GDN_RANGE() Range gdn_range_(__func__)
 
 bool ok_ptr16(const void* p) { return p != nullptr && gdn::aligned16(p); }
 bool ok_ptr4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -55,6 +79,7 @@ int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   if (snap16 != nullptr && !gdn::aligned16(snap16)) return GDN_ERR_MISALIGNED;
   if (a->alpha == nullptr || a->beta == nullptr) return GDN_ERR_INVALID_ARG;
   if (tree && parent == nullptr) return GDN_ERR_INVALID_ARG;
+  if (tree && a->max_depth < 0) return GDN_ERR_INVALID_ARG;
   const void* need4[] = {a->alpha, a->beta, a->slot, a->status, parent, depth_out};
   for (const void* p : need4)
     if (!ok_ptr4(p)) return GDN_ERR_MISALIGNED;
@@ -125,39 +150,70 @@ int replay_common(const gdn_verify_args* a, const int32_t* parent, const int32_t
   return gdn::launch_replay(a, parent, accept, wc, nw, static_cast<cudaStream_t>(stream), prep);
 }
 
+// Host checks shared by the two prefill entry points.
+int prefill_checks(const void* q, const void* k, const void* v, int32_t in_dtype,
+                   const float* alpha, const float* beta, int32_t T, int32_t Hk, int32_t Hv,
+                   int32_t dk, int32_t dv, int32_t chunk, const float* state, const float* o,
+                   const int32_t* status) {
+  if (T < 0 || Hk < 1 || Hv < 1 || Hv % Hk != 0) return GDN_ERR_INVALID_ARG;
+  if (in_dtype != GDN_F32 && in_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  // the tensor-core form takes bf16 inputs at d_k = d_v = 128, chunk 64 only
+  if (dk != 128 || dv != 128 || chunk != 64 || in_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  if (Hv > 65535) return GDN_ERR_UNSUPPORTED;
+  if (state == nullptr) return GDN_ERR_INVALID_ARG;
+  if (!gdn::aligned16(state)) return GDN_ERR_MISALIGNED;
+  if (!ok_ptr4(status)) return GDN_ERR_MISALIGNED;
+  if (T == 0) return GDN_OK;
+  const void* need16[] = {q, k, v, o};
+  for (const void* p : need16) {
+    if (p == nullptr) return GDN_ERR_INVALID_ARG;
+    if (!gdn::aligned16(p)) return GDN_ERR_MISALIGNED;
+  }
+  if (alpha == nullptr || beta == nullptr) return GDN_ERR_INVALID_ARG;
+  if (!ok_ptr4(alpha) || !ok_ptr4(beta)) return GDN_ERR_MISALIGNED;
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
 int gdn_replay_accepted(const gdn_verify_args* args, const int32_t* parent,
                         const int32_t* accept_idx, void* stream) {
+  GDN_RANGE();
   return replay_common(args, parent, accept_idx, stream);
 }
 
 int gdn_verify_chain_prep(const gdn_verify_args* args, void* stream) {
+  GDN_RANGE();
   return verify_common(args, nullptr, nullptr, false, stream, nullptr, true);
 }
 
 int gdn_verify_tree_prep(const gdn_verify_args* args, const int32_t* parent, int32_t* depth_out,
                          void* stream) {
+  GDN_RANGE();
   return verify_common(args, parent, depth_out, true, stream, nullptr, true);
 }
 
 int gdn_replay_accepted_prep(const gdn_verify_args* args, const int32_t* parent,
                              const int32_t* accept_idx, void* stream) {
+  GDN_RANGE();
   return replay_common(args, parent, accept_idx, stream, true);
 }
 
 int gdn_verify_chain(const gdn_verify_args* args, void* stream) {
+  GDN_RANGE();
   return verify_common(args, nullptr, nullptr, false, stream);
 }
 
 int gdn_verify_tree(const gdn_verify_args* args, const int32_t* parent, int32_t* depth_out,
                     void* stream) {
+  GDN_RANGE();
   return verify_common(args, parent, depth_out, true, stream);
 }
 
 int gdn_verify_chain_f16(const gdn_verify_args* args, void* snapshots_f16, void* stream) {
+  GDN_RANGE();
   if (snapshots_f16 == nullptr) return GDN_ERR_INVALID_ARG;
   return verify_common(args, nullptr, nullptr, false, stream, snapshots_f16);
 }
@@ -167,6 +223,7 @@ int gdn_commit_accepted(const float* snapshots, int64_t snap_layer_stride,
                         int64_t cache_layer_stride, const int32_t* slot, int32_t n_slots,
                         int32_t B, int32_t N, int32_t Hv, int32_t dk, int32_t dv,
                         int32_t n_layers, int32_t* status, void* stream) {
+  GDN_RANGE();
   return commit_common(snapshots, false, snap_layer_stride, accept_idx, state_cache,
                        cache_slot_stride, cache_layer_stride, slot, n_slots, B, N, Hv, dk, dv,
                        n_layers, status, stream);
@@ -178,6 +235,7 @@ int gdn_commit_accepted_f16(const void* snapshots_f16, int64_t snap_layer_stride
                             const int32_t* slot, int32_t n_slots, int32_t B, int32_t N,
                             int32_t Hv, int32_t dk, int32_t dv, int32_t n_layers,
                             int32_t* status, void* stream) {
+  GDN_RANGE();
   return commit_common(snapshots_f16, true, snap_layer_stride, accept_idx, state_cache,
                        cache_slot_stride, cache_layer_stride, slot, n_slots, B, N, Hv, dk, dv,
                        n_layers, status, stream);
@@ -187,6 +245,7 @@ int gdn_conv_commit(const void* x, int32_t in_dtype, void* conv_state,
                     int64_t state_slot_stride, const int32_t* slot, int32_t n_slots,
                     const int32_t* parent, const int32_t* accept_idx, int32_t B, int32_t N,
                     int32_t C, int32_t W, int32_t* status, void* stream) {
+  GDN_RANGE();
   if (in_dtype != GDN_F32 && in_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
   if (B < 0 || N < 1 || C < 1 || W < 1 || n_slots < 1) return GDN_ERR_INVALID_ARG;
   if (W > 8 || B > 65535) return GDN_ERR_UNSUPPORTED;
@@ -205,6 +264,7 @@ int gdn_conv_commit(const void* x, int32_t in_dtype, void* conv_state,
 
 int gdn_commit_index(const int32_t* accept_idx, int32_t B, int32_t N, int32_t base_slot,
                      int32_t* slot, int32_t* status, void* stream) {
+  GDN_RANGE();
   if (B < 0 || N < 1 || base_slot < 0) return GDN_ERR_INVALID_ARG;
   if ((int64_t)base_slot + (int64_t)B * N > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
   if (B == 0) return GDN_OK;
@@ -223,48 +283,28 @@ size_t gdn_prefill_workspace_bytes(int32_t T, int32_t Hk, int32_t Hv, int32_t dk
 int gdn_prefill_chunked(const void* q, const void* k, const void* v, int32_t in_dtype,
                         const float* alpha, const float* beta, int32_t T, int32_t Hk, int32_t Hv,
                         int32_t dk, int32_t dv, int32_t chunk, float* state, float* o,
-                        void* workspace, size_t workspace_bytes, void* stream) {
-  if (T < 0 || Hk < 1 || Hv < 1 || Hv % Hk != 0) return GDN_ERR_INVALID_ARG;
-  if (in_dtype != GDN_F32 && in_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
-  if (dk != 128 || dv != 128 || chunk != 64) return GDN_ERR_UNSUPPORTED;
-  if (Hv > 65535) return GDN_ERR_UNSUPPORTED;
-  if (state == nullptr) return GDN_ERR_INVALID_ARG;
-  if (!gdn::aligned16(state)) return GDN_ERR_MISALIGNED;
-  if (T == 0) return GDN_OK;
-  const void* need16[] = {q, k, v, o};
-  for (const void* p : need16) {
-    if (p == nullptr) return GDN_ERR_INVALID_ARG;
-    if (!gdn::aligned16(p)) return GDN_ERR_MISALIGNED;
-  }
-  if (alpha == nullptr || beta == nullptr) return GDN_ERR_INVALID_ARG;
-  if (!ok_ptr4(alpha) || !ok_ptr4(beta)) return GDN_ERR_MISALIGNED;
+                        void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+  GDN_RANGE();
+  const int st = prefill_checks(q, k, v, in_dtype, alpha, beta, T, Hk, Hv, dk, dv, chunk, state,
+                                o, status);
+  if (st != GDN_OK || T == 0) return st;
   const size_t need = gdn::prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
   if (need > 0 && !gdn::aligned16(workspace)) return GDN_ERR_MISALIGNED;
-  return gdn::launch_prefill(q, k, v, in_dtype == GDN_BF16, alpha, beta, T, Hk, Hv, dk, dv, chunk,
-                             state, o, workspace, static_cast<cudaStream_t>(stream));
+  return gdn::launch_prefill(q, k, v, true, alpha, beta, T, Hk, Hv, dk, dv, chunk, state, o,
+                             workspace, status, static_cast<cudaStream_t>(stream));
 }
 
 int gdn_prefill_chunked_noalloc(const void* q, const void* k, const void* v, int32_t in_dtype,
                                 const float* alpha, const float* beta, int32_t T, int32_t Hk,
                                 int32_t Hv, int32_t dk, int32_t dv, int32_t chunk, float* state,
-                                float* o, void* stream) {
-  if (T < 0 || Hk < 1 || Hv < 1 || Hv % Hk != 0) return GDN_ERR_INVALID_ARG;
-  if (in_dtype != GDN_F32 && in_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
-  if (dk != 128 || dv != 128 || chunk != 64 || in_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
-  if (Hv > 65535) return GDN_ERR_UNSUPPORTED;
-  if (state == nullptr) return GDN_ERR_INVALID_ARG;
-  if (!gdn::aligned16(state)) return GDN_ERR_MISALIGNED;
-  if (T == 0) return GDN_OK;
-  const void* need16[] = {q, k, v, o};
-  for (const void* p : need16) {
-    if (p == nullptr) return GDN_ERR_INVALID_ARG;
-    if (!gdn::aligned16(p)) return GDN_ERR_MISALIGNED;
-  }
-  if (alpha == nullptr || beta == nullptr) return GDN_ERR_INVALID_ARG;
-  if (!ok_ptr4(alpha) || !ok_ptr4(beta)) return GDN_ERR_MISALIGNED;
+                                float* o, int32_t* status, void* stream) {
+  GDN_RANGE();
+  const int st = prefill_checks(q, k, v, in_dtype, alpha, beta, T, Hk, Hv, dk, dv, chunk, state,
+                                o, status);
+  if (st != GDN_OK || T == 0) return st;
   return gdn::launch_prefill_noalloc(q, k, v, true, alpha, beta, T, Hk, Hv, dk, dv, chunk, state,
-                                     o, static_cast<cudaStream_t>(stream));
+                                     o, status, static_cast<cudaStream_t>(stream));
 }
 
 const char* gdn_status_string(int status) {
@@ -279,6 +319,7 @@ const char* gdn_status_string(int status) {
     case GDN_ERR_SLOT_RANGE: return "GDN_ERR_SLOT_RANGE";
     case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
     case GDN_ERR_SCRATCH_LIMIT: return "GDN_ERR_SCRATCH_LIMIT";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
     default: return "GDN_ERR_UNKNOWN";
   }
 }

@@ -40,11 +40,12 @@ int launch_conv_commit(const void* x, bool bf16, void* state, int64_t slot_strid
 size_t prefill_workspace_bytes(int T, int Hk, int Hv, int dk, int dv, int chunk);
 int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const float* alpha,
                    const float* beta, int T, int Hk, int Hv, int dk, int dv, int chunk,
-                   float* state, float* o, void* workspace, cudaStream_t stream);
+                   float* state, float* o, void* workspace, int32_t* status, cudaStream_t stream);
 
 // gdn_prefill_chunked on the library's built-in scratch (no allocation).
 int launch_prefill_noalloc(const void* q, const void* k, const void* v, bool bf16,
                            const float* alpha, const float* beta, int T, int Hk, int Hv, int dk,
-                           int dv, int chunk, float* state, float* o, cudaStream_t stream);
+                           int dv, int chunk, float* state, float* o, int32_t* status,
+                           cudaStream_t stream);
 
 }  // namespace gdn

@@ -37,8 +37,6 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
-#include <mutex>
-
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
 #include "gdn_tc.cuh"
@@ -549,7 +547,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
 scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
             const __grid_constant__ CUtensorMap tm_v48, const __grid_constant__ CUtensorMap tm_v32,
             const __grid_constant__ CUtensorMap tm_o48, const __grid_constant__ CUtensorMap tm_o32,
-            float* __restrict__ state, const char* __restrict__ ws, int T, int Hk, int Hv) {
+            float* __restrict__ state, const char* __restrict__ ws, int T, int Hk, int Hv,
+            int32_t* __restrict__ status) {
   pdl_enter();
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -573,12 +572,13 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
   char* db = smem + SCAN_DB;
   float* otile = reinterpret_cast<float*>(smem + SCAN_O);
   // mbarriers: [0], [1] staging buffers; [2], [3], [4] completion of the
-  // chunk's first, second and third MMA group (one phase per chunk each)
+  // chunk's first, second and third MMA group (one phase per chunk each);
+  // [5] all MMAs issued, on the failure path only
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SCAN_BAR);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + SCAN_BAR + 40);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + SCAN_BAR + 48);
 
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
+    for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
     mbar_init_fence();
   }
   if (w == 0) {
@@ -746,13 +746,19 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
   }
 
   ok = tc_barrier(ok);
-  if (tid == kCopier) {
-    // a staged chunk or an MMA never completed: give the staging still in
-    // flight a last bounded chance to land; the output stores complete here
-    if (!ok && inflight >= 0)
+  if (!ok) {
+    // A wait expired.  Before the tensor memory is released, every MMA this
+    // CTA issued must have completed (one more commit tracks all of them) and
+    // the staging still in flight must have landed; each wait is bounded.
+    if (tid == kIssuer) {
+      tc::mma_commit(&bar[5]);
+      mbar_wait_bounded(&bar[5], 0, kWaitPolls);
+      report(status, GDN_ERR_TIMEOUT);
+    }
+    if (tid == kCopier && inflight >= 0)
       mbar_wait_bounded(&bar[inflight & 1], (inflight >> 1) & 1, kWaitPolls);
-    tc::bulk_wait_all();
   }
+  if (tid == kCopier) tc::bulk_wait_all();  // the output stores complete here
   if (!ok) {
 #pragma unroll
     for (int e = 0; e < NH; ++e) Hr[e] = __int_as_float(0x7fc00000);  // the slab failed
@@ -772,45 +778,27 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
 // so that callers who cannot allocate device memory still get the chunked
 // prefill.  Every GPU that loads the library holds it until the process exits.
 // Host code must not hand the symbol itself to a kernel (on the host it names
-// a stand-in, not device memory): its device address is looked up once per
-// device with cudaGetSymbolAddress and cached.
+// a stand-in, not device memory): its device address on the current device is
+// looked up with cudaGetSymbolAddress on every call.  The lookup is a host-side
+// query; repeating it means that a device reset or a new primary context,
+// after which the module is loaded again (possibly elsewhere), never receives
+// an address from before.
 static __device__ __align__(256) char g_prefill_scratch[GDN_PREFILL_NOALLOC_SCRATCH_BYTES];
-
-namespace {
-
-constexpr int kMaxDevices = 256;
-
-// Device address of g_prefill_scratch on the current device (set up on the
-// first call for that device).  Returns GDN_OK or GDN_ERR_CUDA.
-int scratch_on_current_device(void** ptr) {
-  static std::mutex mu;
-  static void* addr[kMaxDevices] = {};
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess || p == nullptr)
-      return GDN_ERR_CUDA;
-    addr[dev] = p;
-  }
-  *ptr = addr[dev];
-  return GDN_OK;
-}
-
-}  // namespace
 
 int launch_prefill_noalloc(const void* q, const void* k, const void* v, bool bf16,
                            const float* alpha, const float* beta, int T, int Hk, int Hv, int dk,
-                           int dv, int chunk, float* state, float* o, cudaStream_t stream) {
+                           int dv, int chunk, float* state, float* o, int32_t* status,
+                           cudaStream_t stream) {
   if (!bf16 || dk != DK || dv != DV || chunk != C) return GDN_ERR_UNSUPPORTED;
   const size_t need = prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk);
   if (need > (size_t)GDN_PREFILL_NOALLOC_SCRATCH_BYTES) return GDN_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
-  const int st = scratch_on_current_device(&scratch);
-  if (st != GDN_OK) return st;
+  if (cudaGetSymbolAddress(&scratch, g_prefill_scratch) != cudaSuccess || scratch == nullptr) {
+    (void)cudaGetLastError();
+    return GDN_ERR_CUDA;
+  }
   return launch_prefill(q, k, v, bf16, alpha, beta, T, Hk, Hv, dk, dv, chunk, state, o, scratch,
-                        stream);
+                        status, stream);
 }
 
 size_t prefill_workspace_bytes(int T, int Hk, int Hv, int dk, int dv, int chunk) {
@@ -858,7 +846,8 @@ int rows_tensor_map(CUtensorMap* m, const void* base, CUtensorMapDataType type, 
 
 int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const float* alpha,
                    const float* beta, int T, int Hk, int Hv, int dk, int dv, int chunk,
-                   float* state, float* o, void* workspace, cudaStream_t stream) {
+                   float* state, float* o, void* workspace, int32_t* status,
+                   cudaStream_t stream) {
   if (!bf16 || dk != DK || dv != DV || chunk != C) return GDN_ERR_UNSUPPORTED;
   const int n_chunks = (T + C - 1) / C;
   // K and Q in 64 x 64 tiles, 128-byte swizzle; V and O in 64-row tiles of
@@ -885,7 +874,7 @@ int launch_prefill(const void* q, const void* k, const void* v, bool bf16, const
   if (st != GDN_OK) return st;
   return launch_pdl(scan_kernel, dim3(3, Hv), dim3(SCAN_THREADS), SCAN_SMEM, stream, tm_k, tm_q,
                     tm_v48, tm_v32, tm_o48, tm_o32, state, static_cast<const char*>(workspace),
-                    T, Hk, Hv);
+                    T, Hk, Hv, status);
 }
 
 }  // namespace gdn

@@ -148,7 +148,8 @@ struct VerifyParams {
   int32_t* depth_out;
   int64_t cache_slot_stride;
   int n_slots, N, Hk, Hv, dv, bf16;
-  int hint;  // issue the pre-wait L2 hints
+  int hint;       // issue the pre-wait L2 hints
+  int max_depth;  // tree: deepest node allowed (root = 1), 0 = no cap
 };
 
 // Launches of up to this many blocks (4 per SM on 152 SMs, one wave) issue
@@ -609,12 +610,19 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
     }
   }
   // depths, then the order of the walk: by depth, then by index
+  bool shallow = true;
   for (int n = tid; n < N; n += NT) {
     int d = 1;
     for (int m = n; m > 0; m = spar[m]) ++d;
     sdep[n] = d;
+    shallow = shallow && (p.max_depth <= 0 || d <= p.max_depth);
   }
-  __syncthreads();
+  if (!block_all<TW>(shallow)) {  // deeper than the caller's cap: skipped, depths reported
+    if (lead && tid == 0) report(p.status, GDN_ERR_BAD_TREE);
+    if (lead && p.depth_out != nullptr)
+      for (int n = tid; n < N; n += NT) p.depth_out[(int64_t)b * N + n] = sdep[n];
+    return;
+  }
   for (int n = tid; n < N; n += NT) {
     const int dn = sdep[n];
     int pos = 0;
@@ -1060,6 +1068,7 @@ int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   p.bf16 = a->in_dtype == GDN_BF16;
   p.snap16 = static_cast<__half*>(snap16);
   p.hint = (int64_t)(p.dv / wc) * a->Hv * a->B <= kHintBlocks;
+  p.max_depth = parent != nullptr ? a->max_depth : 0;
   if (parent != nullptr)  // row warps do not apply: a tree block's warps take whole nodes
     return prep ? dispatch_tree<true>(p, a->B, a->dk, wc, stream)
                 : dispatch_tree<false>(p, a->B, a->dk, wc, stream);

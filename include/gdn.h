@@ -28,9 +28,16 @@
  *    q and k are used as given (callers L2-normalise them upstream).
  *  - Every pointer argument is DEVICE memory of the current CUDA device,
  *    allocated and owned by the caller, unless stated otherwise.  The library
- *    allocates nothing, keeps no global state and never synchronises: work
- *    is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
- *    stream) and the call returns once it is launched.
+ *    allocates nothing and never synchronises: work is enqueued on `stream`
+ *    (a cudaStream_t; NULL = the legacy default stream) and the call returns
+ *    once it is launched.  It keeps no mutable state between calls, with one
+ *    exception: the built-in scratch array of gdn_prefill_chunked_noalloc
+ *    (see there for how concurrent calls of that entry point race).
+ *  - Profiling ranges: with the environment variable GDN_NVTX set to a value
+ *    other than "0" when the library is loaded, every entry point pushes an
+ *    NVTX range named after itself for the duration of the host call (so a
+ *    timeline tool shows where each launch was issued); unset, the check
+ *    costs one branch per call.
  *  - Kernels are launched with programmatic dependent launch allowed: each
  *    kernel starts by waiting until the kernel before it on the stream has
  *    completed and its memory is visible, then lets the next kernel begin
@@ -56,7 +63,7 @@
 extern "C" {
 #endif
 
-#define GDN_VERSION 2
+#define GDN_VERSION 3
 
 typedef enum gdn_status {
   GDN_OK = 0,
@@ -68,7 +75,9 @@ typedef enum gdn_status {
   GDN_ERR_ACCEPT_RANGE = -6,  /* device: accept index outside [0, N) */
   GDN_ERR_SLOT_RANGE = -7,    /* device: slot outside [0, n_slots) */
   GDN_ERR_WORKSPACE = -8,     /* workspace missing or smaller than required */
-  GDN_ERR_SCRATCH_LIMIT = -9  /* problem too large for the built-in scratch of the _noalloc call */
+  GDN_ERR_SCRATCH_LIMIT = -9, /* problem too large for the built-in scratch of the _noalloc call */
+  GDN_ERR_TIMEOUT = -10       /* device: a bounded wait on an asynchronous copy or tensor-core
+                                 operation expired; that call's outputs are not valid */
 } gdn_status;
 
 typedef enum gdn_dtype {
@@ -105,6 +114,10 @@ typedef enum gdn_dtype {
  *                 tile.  GDN_ERR_UNSUPPORTED for any other combination.
  *                 A tree verify takes tile_cols only: its block's warps
  *                 take whole nodes of a depth level, never rows.
+ *   max_depth     tree verify only: 0 = no cap; otherwise a sequence whose
+ *                 tree has a node deeper than max_depth (the root has depth 1)
+ *                 is skipped and GDN_ERR_BAD_TREE is written to `status`.
+ *                 Ignored by the chain and replay calls.
  *
  * Supported sizes: dk in {16, 32, 64, 128}; dv a multiple of 16, <= 1024;
  * 1 <= N <= 64; Hv a multiple of Hk; B >= 0 (B = 0 launches nothing).
@@ -131,6 +144,7 @@ typedef struct gdn_verify_args {
   int32_t in_dtype;
   int32_t tile_cols;
   int32_t row_warps;
+  int32_t max_depth;
 } gdn_verify_args;
 
 /*
@@ -147,7 +161,9 @@ int gdn_verify_chain(const gdn_verify_args* args, void* stream);
  * 0 <= parent[b][n] < n otherwise (nodes in topological order).  Node n starts
  * from its parent's state.  depth_out [B][N] int32 (optional, may be NULL)
  * receives each node's depth, root = 1.  A sequence whose parent array breaks
- * the rule is skipped and GDN_ERR_BAD_TREE is written to args->status.
+ * the rule, or whose tree is deeper than args->max_depth (when not 0), is
+ * skipped and GDN_ERR_BAD_TREE is written to args->status (its depth_out row
+ * is still written when the parent array itself is valid).
  */
 int gdn_verify_tree(const gdn_verify_args* args, const int32_t* parent, int32_t* depth_out,
                     void* stream);
@@ -163,7 +179,9 @@ int gdn_verify_tree(const gdn_verify_args* args, const int32_t* parent, int32_t*
  * at + h*dk*dv.  For a chain with accept length L, accept_idx = L - 1.
  * The copy is bit-exact.  An accept index outside [0, N) or a slot outside
  * [0, n_slots) skips that sequence and is reported through `status`.
- * snapshots and state_cache must not overlap.
+ * snapshots and state_cache must not overlap, and the slot[] entries of one
+ * call must be distinct (two sequences committing into one slot race, and
+ * the slot then holds either state).
  */
 int gdn_commit_accepted(const float* snapshots, int64_t snap_layer_stride,
                         const int32_t* accept_idx, float* state_cache, int64_t cache_slot_stride,
@@ -230,7 +248,9 @@ int gdn_commit_accepted_f16(const void* snapshots_f16, int64_t snap_layer_stride
  * of accept_idx[b] from the root, parent [B][N] as in gdn_verify_tree): the
  * new history is the last W elements of [old history, x of the path nodes].
  * The copy is bit-exact.  1 <= W <= 8.  A bad accept index, slot or parent
- * array skips that sequence and is reported through `status`.
+ * array skips that sequence and is reported through `status`.  The slot[]
+ * entries of one call must be distinct: the history is rewritten in place,
+ * and two sequences sharing a slot race on it.
  */
 int gdn_conv_commit(const void* x, int32_t in_dtype, void* conv_state,
                     int64_t state_slot_stride, const int32_t* slot, int32_t n_slots,
@@ -282,19 +302,25 @@ int gdn_replay_accepted(const gdn_verify_args* args, const int32_t* parent,
  * Chunked prefill of one sequence of T tokens: the same recurrence, evaluated
  * chunk by chunk in the WY / UT-transform form on tensor cores.
  *
- *   q, k   [T][Hk][dk]  bf16 (in_dtype must be GDN_BF16);  v [T][Hv][dv] bf16
+ *   q, k   [T][Hk][dk]  bf16;  v [T][Hv][dv] bf16
  *   alpha, beta [T][Hv] fp32
  *   state  [Hv][dk][dv] fp32, in: the state before token 0, out: after token T-1
  *   o      [T][Hv][dv] fp32 output
  *   workspace  device scratch of at least gdn_prefill_workspace_bytes(...) bytes,
  *              owned by the caller, contents need not be initialised
+ *   status optional device int32 error word (first error wins; the caller
+ *          zeroes it): GDN_ERR_TIMEOUT if a bounded wait of the kernel on its
+ *          own asynchronous copies or tensor-core work expired.  The kernel
+ *          then stops early; the state of the affected heads is written as
+ *          NaN, and o is not valid.
  *
- * Supported: dk = dv = 128, chunk = 64, bf16 inputs, T >= 0 (any T; the last
- * chunk may be partial).  GDN_ERR_WORKSPACE if the workspace is NULL or too
- * small.  Two kernels run on `stream`: a parallel pass over (chunk, q/k head)
- * that fills the workspace, then the sequential pass over the chunks of each
- * value head; the workspace may be reused once the call's work has finished
- * on the stream.
+ * Supported: dk = dv = 128, chunk = 64, in_dtype = GDN_BF16, T >= 0 (any T;
+ * the last chunk may be partial); any other size or dtype returns
+ * GDN_ERR_UNSUPPORTED before anything is launched.  GDN_ERR_WORKSPACE if the
+ * workspace is NULL or too small.  Two kernels run on `stream`: a parallel
+ * pass over (chunk, q/k head) that fills the workspace, then the sequential
+ * pass over the chunks of each value head; the workspace may be reused once
+ * the call's work has finished on the stream.
  */
 size_t gdn_prefill_workspace_bytes(int32_t T, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
                                    int32_t chunk);
@@ -302,7 +328,7 @@ size_t gdn_prefill_workspace_bytes(int32_t T, int32_t Hk, int32_t Hv, int32_t dk
 int gdn_prefill_chunked(const void* q, const void* k, const void* v, int32_t in_dtype,
                         const float* alpha, const float* beta, int32_t T, int32_t Hk, int32_t Hv,
                         int32_t dk, int32_t dv, int32_t chunk, float* state, float* o,
-                        void* workspace, size_t workspace_bytes, void* stream);
+                        void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
  * gdn_prefill_chunked without a workspace argument, for callers that cannot
@@ -321,9 +347,12 @@ int gdn_prefill_chunked(const void* q, const void* k, const void* v, int32_t in_
  * GDN_ERR_SCRATCH_LIMIT without launching anything.  The library allocates
  * nothing here: no cudaMalloc, cudaFree or allocating library routine.
  *
- * The first call on a device looks up the device address of the scratch
- * array (cudaGetSymbolAddress, with that device current); make that first
- * call before any stream capture.  All calls share the one array, which keeps
+ * Every call looks up the device address of the scratch array on the current
+ * device (cudaGetSymbolAddress, a host-side query that is repeated each time
+ * so that a reset device or a new context is never handed a stale address).
+ * The first such lookup on a device loads the library's device code there;
+ * make that first call before any stream capture.  All calls share the one
+ * array, which keeps
  * the previous call's contents (nothing in it needs clearing: the first kernel
  * of a call writes every byte the second kernel reads).  Calls that overlap on
  * the GPU -- on different streams, or from different host threads -- race on
@@ -334,7 +363,7 @@ int gdn_prefill_chunked(const void* q, const void* k, const void* v, int32_t in_
 int gdn_prefill_chunked_noalloc(const void* q, const void* k, const void* v, int32_t in_dtype,
                                 const float* alpha, const float* beta, int32_t T, int32_t Hk,
                                 int32_t Hv, int32_t dk, int32_t dv, int32_t chunk, float* state,
-                                float* o, void* stream);
+                                float* o, int32_t* status, void* stream);
 
 /* Human-readable name of a gdn_status value (static string, never NULL). */
 const char* gdn_status_string(int status);

@@ -42,9 +42,10 @@ def bind(lib):
     for name in ("oracle_verify_f64", "oracle_verify_ld"):
         f = getattr(lib, name)
         f.restype = ctypes.c_int
-        f.argtypes = [P, P, P, P, P, P, i64, P, i32, P, i32, i32, i32, i32, i32, i32, P, P]
+        f.argtypes = [P, P, P, P, P, P, i64, P, i32, P, i32, i32, i32, i32, i32, i32, P, P,
+                      i32]
     lib.oracle_tree_depth.restype = ctypes.c_int
-    lib.oracle_tree_depth.argtypes = [P, i32, i32, P]
+    lib.oracle_tree_depth.argtypes = [P, i32, i32, P, i32]
     lib.oracle_commit_f64.restype = ctypes.c_int
     lib.oracle_commit_f64.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32,
                                       i32, i32]
@@ -80,9 +81,10 @@ def _c(a, dtype):
 
 
 def verify(q, k, v, alpha, beta, cache, slot, parent, *, B, N, Hk, Hv, dk, dv,
-           cache_slot_stride=None, n_slots=None, precision="f64"):
+           cache_slot_stride=None, n_slots=None, precision="f64", max_depth=0):
     """Run a verify block.  parent=None -> chain.  Returns (status, snap, o)
-    with snap [B][N][Hv][dk][dv] and o [B][N][Hv][dv] in the chosen precision."""
+    with snap [B][N][Hv][dk][dv] and o [B][N][Hv][dv] in the chosen precision.
+    max_depth > 0 rejects (skips) a tree with a node deeper than that."""
     lib = _load()
     R = np.float64 if precision == "f64" else np.longdouble
     fn = lib.oracle_verify_f64 if precision == "f64" else lib.oracle_verify_ld
@@ -97,7 +99,7 @@ def verify(q, k, v, alpha, beta, cache, slot, parent, *, B, N, Hk, Hv, dk, dv,
     slot_a = None if slot is None else _c(slot, np.int32)
     par_a = None if parent is None else _c(parent, np.int32)
     st = fn(*[_ptr(a) for a in arrs], _ptr(cache), cache_slot_stride, _ptr(slot_a), n_slots,
-            _ptr(par_a), B, N, Hk, Hv, dk, dv, _ptr(snap), _ptr(o))
+            _ptr(par_a), B, N, Hk, Hv, dk, dv, _ptr(snap), _ptr(o), max_depth)
     return st, snap, o
 
 
@@ -110,12 +112,12 @@ def verify_inputs(inp, tree=None, precision="f64"):
                   n_slots=inp["n_slots"], precision=precision)
 
 
-def tree_depth(parent):
+def tree_depth(parent, max_depth=0):
     lib = _load()
     parent = _c(parent, np.int32)
     B, N = parent.shape
     depth = np.zeros((B, N), dtype=np.int32)
-    st = lib.oracle_tree_depth(_ptr(parent), B, N, _ptr(depth))
+    st = lib.oracle_tree_depth(_ptr(parent), B, N, _ptr(depth), max_depth)
     return st, depth
 
 

@@ -63,7 +63,11 @@ void gdn_step(R* H, const R* k, const R* v, const R* q, R alpha, R beta, int dk,
 }
 
 // parent[0] must be -1 and 0 <= parent[n] < n for n >= 1.  depth(root) = 1.
-int tree_depth(const int32_t* parent, int N, int32_t* depth) {
+// A draft tree's depth is capped ("Qwen3.6 27B: From 20 t/s to 184 t/s",
+// DFlash section: a best-first tree grown under a budget; the DDTree workload
+// caps it at 16): with max_depth > 0, a tree holding a node deeper than the
+// cap is rejected after every depth has been filled in.
+int tree_depth(const int32_t* parent, int N, int32_t* depth, int max_depth = 0) {
   if (N <= 0) return ERR_INVALID_ARG;
   if (parent[0] != -1) return ERR_BAD_TREE;
   depth[0] = 1;
@@ -72,13 +76,17 @@ int tree_depth(const int32_t* parent, int N, int32_t* depth) {
     if (p < 0 || p >= n) return ERR_BAD_TREE;
     depth[n] = depth[p] + 1;
   }
+  if (max_depth > 0)
+    for (int n = 0; n < N; ++n)
+      if (depth[n] > max_depth) return ERR_BAD_TREE;
   return OK;
 }
 
 template <typename R>
 int verify(const R* q, const R* k, const R* v, const R* alpha, const R* beta, const R* cache,
            int64_t cache_slot_stride, const int32_t* slot, int32_t n_slots, const int32_t* parent,
-           int32_t B, int32_t N, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv, R* snap, R* o) {
+           int32_t B, int32_t N, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv, R* snap, R* o,
+           int32_t max_depth) {
   if (B < 0 || N <= 0 || Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || Hv % Hk != 0)
     return ERR_INVALID_ARG;
   const int G = Hv / Hk;               // value heads per q/k head (contiguous groups)
@@ -89,7 +97,7 @@ int verify(const R* q, const R* k, const R* v, const R* alpha, const R* beta, co
   for (int b = 0; b < B; ++b) {
     const int32_t* par = parent ? parent + (int64_t)b * N : nullptr;
     if (par) {
-      int st = tree_depth(par, N, depth.data());
+      int st = tree_depth(par, N, depth.data(), max_depth);
       if (st != OK) { status = st; continue; }
     }
     int sl = slot ? slot[b] : b;
@@ -265,31 +273,35 @@ int oracle_replay_f64(const double* k, const double* v, const double* alpha, con
 //   q, k [B][N][Hk][dk]; v [B][N][Hv][dv]; alpha, beta [B][N][Hv]
 //   cache: slot s, head h at cache + s*cache_slot_stride + h*dk*dv, [dk][dv]
 //   snap [B][N][Hv][dk][dv]; o [B][N][Hv][dv]
-// A sequence with an invalid tree or slot is skipped and its error returned.
+// A sequence with an invalid tree or slot is skipped and its error returned;
+// max_depth > 0 also rejects a tree deeper than that (root = 1).
 int oracle_verify_f64(const double* q, const double* k, const double* v, const double* alpha,
                       const double* beta, const double* cache, int64_t cache_slot_stride,
                       const int32_t* slot, int32_t n_slots, const int32_t* parent, int32_t B,
                       int32_t N, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv, double* snap,
-                      double* o) {
+                      double* o, int32_t max_depth) {
   return verify<double>(q, k, v, alpha, beta, cache, cache_slot_stride, slot, n_slots, parent, B,
-                        N, Hk, Hv, dk, dv, snap, o);
+                        N, Hk, Hv, dk, dv, snap, o, max_depth);
 }
 
 int oracle_verify_ld(const long double* q, const long double* k, const long double* v,
                      const long double* alpha, const long double* beta, const long double* cache,
                      int64_t cache_slot_stride, const int32_t* slot, int32_t n_slots,
                      const int32_t* parent, int32_t B, int32_t N, int32_t Hk, int32_t Hv,
-                     int32_t dk, int32_t dv, long double* snap, long double* o) {
+                     int32_t dk, int32_t dv, long double* snap, long double* o,
+                     int32_t max_depth) {
   return verify<long double>(q, k, v, alpha, beta, cache, cache_slot_stride, slot, n_slots,
-                             parent, B, N, Hk, Hv, dk, dv, snap, o);
+                             parent, B, N, Hk, Hv, dk, dv, snap, o, max_depth);
 }
 
 // depth[b][n] of each node, root depth 1; returns ERR_BAD_TREE for any
-// sequence whose parent array is not topologically ordered from a root at 0.
-int oracle_tree_depth(const int32_t* parent, int32_t B, int32_t N, int32_t* depth) {
+// sequence whose parent array is not topologically ordered from a root at 0,
+// or (max_depth > 0) that holds a node deeper than max_depth.
+int oracle_tree_depth(const int32_t* parent, int32_t B, int32_t N, int32_t* depth,
+                      int32_t max_depth) {
   int status = OK;
   for (int b = 0; b < B; ++b) {
-    int st = tree_depth(parent + (int64_t)b * N, N, depth + (int64_t)b * N);
+    int st = tree_depth(parent + (int64_t)b * N, N, depth + (int64_t)b * N, max_depth);
     if (st != OK) status = st;
   }
   return status;

@@ -309,6 +309,26 @@ def check_tree_depth_and_validation():
                                 dk=c["dk"], dv=c["dv"])
     assert st == oracle.ERR_BAD_TREE
     assert not np.any(snap[1]) and np.any(snap[0])
+    # the depth cap: a path of 6 nodes has depth 6 and a star depth 2 (counted
+    # by hand, root = 1); a cap at the depth keeps the tree, one below rejects it
+    path = np.array([[-1, 0, 1, 2, 3, 4]], np.int32)
+    star = np.array([[-1, 0, 0, 0, 0, 0]], np.int32)
+    for tree, deepest in ((path, 6), (star, 2)):
+        st, depth = oracle.tree_depth(tree, max_depth=deepest)
+        assert st == oracle.OK and int(depth.max()) == deepest
+        st, _ = oracle.tree_depth(tree, max_depth=deepest - 1)
+        assert st == oracle.ERR_BAD_TREE
+    c = _case(rng, B=2, N=6, tree=True)
+    c["parent"][0], c["parent"][1] = path[0], star[0]
+    common = dict(B=2, N=6, Hk=c["Hk"], Hv=c["Hv"], dk=c["dk"], dv=c["dv"])
+    args = (c["q"], c["k"], c["v"], c["alpha"], c["beta"], c["cache"], c["slot"], c["parent"])
+    st, snap_free, o_free = oracle.verify(*args, **common)
+    assert st == oracle.OK
+    st, snap_cap, o_cap = oracle.verify(*args, max_depth=6, **common)
+    assert st == oracle.OK and np.array_equal(snap_cap, snap_free) and np.array_equal(o_cap, o_free)
+    st, snap_cap, o_cap = oracle.verify(*args, max_depth=5, **common)
+    assert st == oracle.ERR_BAD_TREE
+    assert not np.any(snap_cap[0]) and np.array_equal(snap_cap[1], snap_free[1])
 
 
 def check_commit():

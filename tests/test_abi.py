@@ -43,23 +43,27 @@ def test_every_declared_symbol_is_exported(lib):
 def test_struct_layout_matches_c(tmp_path):
     src = tmp_path / "layout.c"
     src.write_text('#include "gdn.h"\n#include <stdio.h>\n#include <stddef.h>\n'
-                   'int main(void){printf("%zu %zu %zu %zu\\n", sizeof(gdn_verify_args),'
+                   'int main(void){printf("%zu %zu %zu %zu %zu\\n", sizeof(gdn_verify_args),'
                    ' offsetof(gdn_verify_args, cache_slot_stride),'
-                   ' offsetof(gdn_verify_args, n_slots), offsetof(gdn_verify_args, row_warps));'
+                   ' offsetof(gdn_verify_args, n_slots), offsetof(gdn_verify_args, row_warps),'
+                   ' offsetof(gdn_verify_args, max_depth));'
                    'return 0;}\n')
     exe = tmp_path / "layout"
     import subprocess
     subprocess.check_call(["gcc", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)])
-    size, off_stride, off_slots, off_rw = map(int, subprocess.check_output([str(exe)]).split())
+    size, off_stride, off_slots, off_rw, off_md = map(
+        int, subprocess.check_output([str(exe)]).split())
     A = gdn.VerifyArgs
     assert ctypes.sizeof(A) == size
     assert A.cache_slot_stride.offset == off_stride
     assert A.n_slots.offset == off_slots and A.row_warps.offset == off_rw
+    assert A.max_depth.offset == off_md
 
 
 def test_version_and_status_strings(lib):
-    assert lib.gdn_version() == 2
+    assert lib.gdn_version() == 3
     assert gdn.status_string(gdn.GDN_ERR_BAD_TREE) == "GDN_ERR_BAD_TREE"
+    assert gdn.status_string(gdn.GDN_ERR_TIMEOUT) == "GDN_ERR_TIMEOUT"
     assert gdn.status_string(12345) == "GDN_ERR_UNKNOWN"
 
 
@@ -101,6 +105,16 @@ def test_verify_host_checks(lib, change, want):
     a = _args(**change)
     assert lib.gdn_verify_chain(ctypes.byref(a), None) == want
     assert lib.gdn_verify_tree(ctypes.byref(a), ctypes.c_void_p(0x90000), None, None) == want
+
+
+def test_verify_tree_rejects_negative_depth_cap(lib):
+    """max_depth = 0 means no cap; a negative cap is an argument error (tree
+    call only: a chain ignores the field, so its call would launch)."""
+    a = _args(max_depth=-1)
+    assert lib.gdn_verify_tree(ctypes.byref(a), ctypes.c_void_p(0x90000), None, None) == \
+        gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_verify_tree_prep(ctypes.byref(a), ctypes.c_void_p(0x90000), None, None) == \
+        gdn.GDN_ERR_INVALID_ARG
 
 
 def test_verify_tree_needs_parent(lib):
@@ -248,30 +262,63 @@ def test_commit_host_checks(lib, change, want):
     assert _commit(lib, **change) == want
 
 
-def test_prefill_host_checks(lib):
-    f = lib.gdn_prefill_chunked
+@pytest.mark.parametrize("noalloc", [False, True])
+def test_prefill_host_checks(lib, noalloc):
     P = 0x100000
     ok = dict(q=P, k=P, v=P, dt=gdn.GDN_BF16, a=P, b=P, T=128, Hk=16, Hv=48, dk=128, dv=128,
-              C=64, s=P, o=P, w=P, wb=1 << 40)
+              C=64, s=P, o=P, w=P, wb=1 << 40, st=None)
 
     def call(**kw):
         x = dict(ok)
         x.update(kw)
-        return f(x["q"], x["k"], x["v"], x["dt"], x["a"], x["b"], x["T"], x["Hk"], x["Hv"],
-                 x["dk"], x["dv"], x["C"], x["s"], x["o"], x["w"], x["wb"], None)
+        head = (x["q"], x["k"], x["v"], x["dt"], x["a"], x["b"], x["T"], x["Hk"], x["Hv"],
+                x["dk"], x["dv"], x["C"], x["s"], x["o"])
+        if noalloc:
+            return lib.gdn_prefill_chunked_noalloc(*head, x["st"], None)
+        return lib.gdn_prefill_chunked(*head, x["w"], x["wb"], x["st"], None)
 
     assert call(T=-1) == gdn.GDN_ERR_INVALID_ARG
     assert call(Hv=47) == gdn.GDN_ERR_INVALID_ARG
+    assert call(dt=5) == gdn.GDN_ERR_INVALID_ARG
+    assert call(dt=gdn.GDN_F32) == gdn.GDN_ERR_UNSUPPORTED   # host-side, before any launch
     assert call(dk=64) == gdn.GDN_ERR_UNSUPPORTED
     assert call(C=32) == gdn.GDN_ERR_UNSUPPORTED
     assert call(s=0) == gdn.GDN_ERR_INVALID_ARG
     assert call(o=P + 4) == gdn.GDN_ERR_MISALIGNED
+    assert call(st=P + 2) == gdn.GDN_ERR_MISALIGNED
+    assert call(q=0) == gdn.GDN_ERR_INVALID_ARG
+    assert call(a=P + 1) == gdn.GDN_ERR_MISALIGNED
     assert call(T=0) == gdn.GDN_OK
-    need = lib.gdn_prefill_workspace_bytes(128, 16, 48, 128, 128, 64)
-    if need > 0:
-        assert call(w=0) == gdn.GDN_ERR_WORKSPACE
-        assert call(wb=need - 1) == gdn.GDN_ERR_WORKSPACE
+    if noalloc:
+        # 11 chunks x 48 value heads of workspace do not fit the built-in scratch
+        assert call(T=704) == gdn.GDN_ERR_SCRATCH_LIMIT
+    else:
+        need = lib.gdn_prefill_workspace_bytes(128, 16, 48, 128, 128, 64)
+        if need > 0:
+            assert call(w=0) == gdn.GDN_ERR_WORKSPACE
+            assert call(wb=need - 1) == gdn.GDN_ERR_WORKSPACE
     assert lib.gdn_prefill_workspace_bytes(-1, 16, 48, 128, 128, 64) == 0
+
+
+def test_nvtx_ranges_switch_on_without_changing_results(tmp_path):
+    """GDN_NVTX=1 wraps every entry point in an NVTX range; host-side checks
+    return the same codes with the ranges on (run in a fresh process, since
+    the switch is read once per process)."""
+    import subprocess
+    import sys
+
+    code = ("import ctypes, hybrid_gated_deltanet_delta_gb300 as g; lib = g.load(); "
+            "a = g.VerifyArgs(); "
+            "assert lib.gdn_verify_chain(ctypes.byref(a), None) == g.GDN_ERR_INVALID_ARG; "
+            "assert lib.gdn_verify_chain(None, None) == g.GDN_ERR_INVALID_ARG; "
+            "assert lib.gdn_commit_index(None, 1, 4, 0, None, None, None) == "
+            "g.GDN_ERR_INVALID_ARG; print('ok')")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for val in ("1", "0"):
+        env = dict(os.environ, GDN_NVTX=val, PYTHONPATH=root)
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True,
+                             text=True, cwd=root, timeout=120)
+        assert out.returncode == 0 and out.stdout.strip() == "ok", out.stderr
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -20,8 +20,10 @@ def run_prefill(gdn, inp):
     o, o_back = guarded((T, Hv, dv), fill=float("nan"))
     wbytes = gdn.gdn_prefill_workspace_bytes(T, Hk, Hv, dk, dv, 64)
     ws = t.empty(max(wbytes, 16), dtype=t.uint8, device="cuda")
-    gdn.gdn_prefill_chunked(q, k, v, alpha, beta, state, o, ws)
+    status = t.zeros(1, dtype=t.int32, device="cuda")
+    gdn.gdn_prefill_chunked(q, k, v, alpha, beta, state, o, ws, status=status)
     t.cuda.synchronize()
+    assert status.item() == 0, "a bounded wait inside the prefill expired"
     assert canaries_ok(s_back, state.numel()), "state buffer overrun"
     assert canaries_ok(o_back, o.numel()), "output buffer overrun"
     return state.cpu().numpy(), o.cpu().numpy()

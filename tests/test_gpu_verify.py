@@ -290,3 +290,44 @@ def test_tree_kernel_level_shapes(gpu_lib, shape):
     assert_close(out["snap"], snap, f"{shape} snapshots")
     st, depth = oracle.tree_depth(par)
     assert st == oracle.OK and np.array_equal(out["depth"], depth)
+
+
+def test_tree_depth_cap_skips_only_the_deep_tree(gpu_lib):
+    """max_depth: a star (depth 2), a path (depth 8) and a broom (a path of 4
+    then a fan: depth 5) under a cap of 5.  The path is skipped and reported
+    as GDN_ERR_BAD_TREE, its depths still written; the others match the
+    oracle run under the same cap.  At a cap of 8 nothing is skipped."""
+    t = torch()
+    B, N = 3, 8
+    inp = synthetic.make_verify_inputs(B=B, N=N, Hk=1, Hv=2, dk=128, dv=32, dtype="bf16",
+                                       alpha_kind="near_one", state_sigma=0.05, seed=77,
+                                       tree=True)
+    n = np.arange(N)
+    par = np.stack([np.where(n == 0, -1, 0), n - 1, np.where(n < 4, n - 1, 3)]).astype(np.int32)
+    inp = dict(inp, parent=par)
+    for cap, want in ((5, gpu_lib.GDN_ERR_BAD_TREE), (8, 0)):
+        snap, snap_back = guarded((B, N, 2, 128, 32))
+        o, o_back = guarded((B, N, 2, 32))
+        st = t.zeros(1, dtype=t.int32, device="cuda")
+        depth = t.full((B, N), -9, dtype=t.int32, device="cuda")
+        gpu_lib.gdn_verify_tree(dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha"]),
+                                dev(inp["beta"]), dev(inp["cache"]), snap, o, dev(par),
+                                depth_out=depth, slot=dev(inp["slot"]), n_slots=inp["n_slots"],
+                                status=st, max_depth=cap)
+        t.cuda.synchronize()
+        assert st.item() == want
+        assert canaries_ok(snap_back, snap.numel()) and canaries_ok(o_back, o.numel())
+        ost, ref_snap, ref_o = oracle.verify(
+            inp["q_f64"], inp["k_f64"], inp["v_f64"], inp["alpha"], inp["beta"], inp["cache"],
+            inp["slot"], par, B=B, N=N, Hk=1, Hv=2, dk=128, dv=32, n_slots=inp["n_slots"],
+            max_depth=cap)
+        assert ost == (oracle.ERR_BAD_TREE if want else oracle.OK)
+        _, ref_depth = oracle.tree_depth(par)
+        assert np.array_equal(depth.cpu().numpy(), ref_depth)
+        got_snap, got_o = snap.cpu().numpy(), o.cpu().numpy()
+        for b in range(B):
+            if want and b == 1:
+                assert not np.any(got_snap[b]) and not np.any(got_o[b]), "deep tree not skipped"
+                continue
+            assert_close(got_snap[b], ref_snap[b], f"cap {cap} sequence {b} snapshots")
+            assert_close(got_o[b], ref_o[b], f"cap {cap} sequence {b} o")

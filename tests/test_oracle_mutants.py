@@ -29,6 +29,8 @@ MUTANTS = {
     "commit_ignores_slot": ("double* to = cache + l * cache_layer_stride + sl * cache_slot_stride",
                             "double* to = cache + l * cache_layer_stride + b * cache_slot_stride"),
     "depth_off_by_one": ("depth[n] = depth[p] + 1;", "depth[n] = depth[p] + (p > 0);"),
+    "depth_cap_off_by_one": ("if (depth[n] > max_depth) return ERR_BAD_TREE;",
+                             "if (depth[n] >= max_depth) return ERR_BAD_TREE;"),
     "prefill_drops_decay": ("alpha[(int64_t)t * Hv + h],\n",
                             "1.0 + 0 * alpha[(int64_t)t * Hv + h],\n"),
     "replay_drops_root": ("for (int m = acc; m >= 0; m = par[m]) path.insert",
