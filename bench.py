@@ -74,7 +74,7 @@ KERNEL_BLOCK = 100
 
 METRIC = "GDN verify node-heads/s per layer at block 16 / tree 22; % of GB300 HBM roofline"
 HEADLINE = "chain16"
-NESTED = ("tree22", "batched8x16", "prefill8192")
+NESTED = ("tree22", "batched8x16", "prefill8192", "tree22_f16", "tree22_replay")
 
 
 def hold_device(torch, host_s_per_step, steps):
@@ -155,6 +155,14 @@ WORKLOADS = {
     "batched8x16_f16": dict(B=8, N=16, tree=False, layers=48, snap16=True,
                             desc="batched8x16 persisting binary16 snapshots, 48-layer "
                                  "widening commit"),
+    "tree22_f16": dict(B=1, N=22, tree=True, layers=1, snap16=True,
+                       desc="tree22 persisting binary16 snapshots (gdn_verify_tree_f16, the "
+                            "per-block solve that never reads a persisted state back) and "
+                            "committing by widening (gdn_commit_accepted_f16)"),
+    "tree22_replay": dict(B=1, N=22, tree=True, layers=1, replay=True,
+                          desc="tree22 committed by checkpoint and replay: the tree verified "
+                               "without snapshots, then the accepted node's ancestors re-run "
+                               "from the cached state into the cache"),
     "prefill8192": dict(T=8192, layers=1,
                         desc="1 sequence of 8192 tokens, 16 q/k heads, 48 value heads, "
                              "d_k=d_v=128, bf16 q/k/v, chunk 64, WY/UT form on tensor cores"),
@@ -480,7 +488,10 @@ class VerifyCase:
         """The binding's plain (checked) call."""
         d = self.dev
         args = (d["q"], d["k"], d["v"], d["alpha"], d["beta"], self.cache, self.snap, self.o)
-        if self.snap16:
+        if self.snap16 and self.parent is not None:
+            gdn.gdn_verify_tree_f16(*args, self.parent, slot=self.slot,
+                                    n_slots=self.inp["n_slots"])
+        elif self.snap16:
             gdn.gdn_verify_chain_f16(*args, slot=self.slot, n_slots=self.inp["n_slots"])
         elif self.parent is not None:
             gdn.gdn_verify_tree(*args, self.parent, slot=self.slot, n_slots=self.inp["n_slots"])
@@ -500,7 +511,11 @@ class VerifyCase:
         d = self.dev
         n_slots = self.inp["n_slots"]
         common = (d["q"], d["k"], d["v"], d["alpha"], d["beta"], self.cache)
-        if self.snap16:
+        if self.snap16 and self.parent is not None:
+            self.verify_c = gdn.bind_verify_tree(*common, None, self.o, self.parent,
+                                                 snapshots_f16=self.snap, slot=self.slot,
+                                                 n_slots=n_slots, stream=stream)
+        elif self.snap16:
             self.verify_c = gdn.bind_verify_chain(*common, None, self.o, snapshots_f16=self.snap,
                                                   slot=self.slot, n_slots=n_slots, stream=stream)
         elif self.parent is not None:
@@ -771,7 +786,8 @@ def measure_verify(ctx, wl_name):
     hbm, _, peak_kind = ctx.peaks
     kname = ("gdn_verify_tree" if tree else "gdn_verify_chain") + \
         (" (no snapshots)" if replay else " (binary16 snapshots)" if snap16 else
-         " (state and snapshots in the slot region)" if index else "")
+         " (state and snapshots in the slot region)" if index else "") + \
+        (", per-block solve" if tree and (replay or snap16) else "")
     out = {
         "metric": METRIC,
         "value": job_throughput(node_heads, K, total_ms, world),

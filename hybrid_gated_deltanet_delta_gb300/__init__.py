@@ -7,7 +7,8 @@ in the library's CUDA kernels; there is no CPU or PyTorch fallback, and the
 functions raise if the library is missing or a call fails.
 
 Entry points (same names as the C ABI):
-  gdn_verify_chain, gdn_verify_chain_f16, gdn_verify_tree, gdn_commit_accepted,
+  gdn_verify_chain, gdn_verify_chain_f16, gdn_verify_tree, gdn_verify_tree_f16,
+  gdn_commit_accepted,
   gdn_commit_accepted_f16, gdn_commit_index, gdn_conv_commit,
   gdn_replay_accepted,
   gdn_prefill_chunked, gdn_prefill_workspace_bytes, gdn_prefill_chunked_noalloc
@@ -90,6 +91,8 @@ def load(path: str | None = None):
     lib.gdn_replay_accepted_prep.restype = ctypes.c_int
     lib.gdn_verify_chain_f16.argtypes = [ctypes.POINTER(VerifyArgs), P, P]
     lib.gdn_verify_chain_f16.restype = ctypes.c_int
+    lib.gdn_verify_tree_f16.argtypes = [ctypes.POINTER(VerifyArgs), P, P, P, P]
+    lib.gdn_verify_tree_f16.restype = ctypes.c_int
     lib.gdn_commit_accepted_f16.argtypes = [P, i64, P, P, i64, i64, P, i32, i32, i32, i32, i32,
                                             i32, i32, P, P]
     lib.gdn_commit_accepted_f16.restype = ctypes.c_int
@@ -215,6 +218,26 @@ def gdn_verify_chain_f16(q, k, v, alpha, beta, state_cache, snapshots_f16, o, *,
                          tile_cols=tile_cols, row_warps=row_warps)
     _check(load().gdn_verify_chain_f16(ctypes.byref(a), _ptr(snapshots_f16), _stream(stream)),
            "gdn_verify_chain_f16")
+
+
+def gdn_verify_tree_f16(q, k, v, alpha, beta, state_cache, snapshots_f16, o, parent, *,
+                        depth_out=None, slot=None, n_slots=None, status=None,
+                        cache_slot_stride=None, tile_cols=0, row_warps=0, max_depth=0,
+                        stream=None):
+    """Tree verification persisting every node's state as float16 (RNE) in
+    snapshots_f16 [B,N,Hv,dk,dv]; outputs unchanged (see include/gdn.h)."""
+    import torch
+
+    _need(snapshots_f16.dtype == torch.float16 and snapshots_f16.is_contiguous(),
+          "snapshots_f16 must be a contiguous float16 tensor")
+    _need(parent.is_contiguous() and tuple(parent.shape) == tuple(k.shape[:2]),
+          "parent must be a contiguous [B,N] int32 tensor")
+    a = make_verify_args(q, k, v, alpha, beta, state_cache, None, o, slot=slot,
+                         n_slots=n_slots, status=status, cache_slot_stride=cache_slot_stride,
+                         tile_cols=tile_cols, row_warps=row_warps, max_depth=max_depth)
+    _check(load().gdn_verify_tree_f16(ctypes.byref(a), _ptr(parent), _ptr(depth_out),
+                                      _ptr(snapshots_f16), _stream(stream)),
+           "gdn_verify_tree_f16")
 
 
 def gdn_verify_tree(q, k, v, alpha, beta, state_cache, snapshots, o, parent, *, depth_out=None,
@@ -380,14 +403,20 @@ def bind_verify_chain(q, k, v, alpha, beta, state_cache, snapshots, o, *, snapsh
 
 
 def bind_verify_tree(q, k, v, alpha, beta, state_cache, snapshots, o, parent, *, depth_out=None,
-                     stream=None, **kw):
-    """gdn_verify_tree bound to these buffers; keyword arguments as for
-    gdn_verify_tree."""
+                     snapshots_f16=None, stream=None, **kw):
+    """gdn_verify_tree (or, with snapshots_f16, gdn_verify_tree_f16) bound to
+    these buffers; keyword arguments as for gdn_verify_tree."""
     _need(parent.is_contiguous() and tuple(parent.shape) == tuple(k.shape[:2]),
           "parent must be a contiguous [B,N] int32 tensor")
     a = make_verify_args(q, k, v, alpha, beta, state_cache, snapshots, o, **kw)
+    s = _stream(stream)
+    if snapshots_f16 is not None:
+        return BoundCall(load().gdn_verify_tree_f16, "gdn_verify_tree_f16",
+                         (ctypes.byref(a), _ptr(parent), _ptr(depth_out), _ptr(snapshots_f16), s),
+                         (a, q, k, v, alpha, beta, state_cache, snapshots_f16, o, parent,
+                          depth_out))
     return BoundCall(load().gdn_verify_tree, "gdn_verify_tree",
-                     (ctypes.byref(a), _ptr(parent), _ptr(depth_out), _stream(stream)),
+                     (ctypes.byref(a), _ptr(parent), _ptr(depth_out), s),
                      (a, q, k, v, alpha, beta, state_cache, snapshots, o, parent, depth_out))
 
 

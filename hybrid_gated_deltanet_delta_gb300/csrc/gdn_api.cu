@@ -39,17 +39,16 @@ bool ok_ptr4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0;
 constexpr int64_t kTwoWarpBlocks = 608;
 
 // Default slab shape for the verify and replay kernels: 16 columns per block,
-// and, for chains, two warps splitting the d_k rows when there are too few
-// blocks to give every SM sub-partition a warp of its own (one warp walking
-// the nodes alone is latency-bound); with many blocks, one warp per block.
-// A tree keeps one warp: its stash traffic and per-branch reductions gain
-// nothing from the split.  A replay takes the chain's shape, so that a chain
-// committed by replay repeats the verify arithmetic bit for bit.
-void auto_tile(int dk, int dv, int B, int Hv, bool tree, int* wc, int* nw) {
+// and two warps splitting the d_k rows when there are too few blocks to give
+// every SM sub-partition a warp of its own; with many blocks, one warp per
+// block.  The level-by-level tree walk keeps one warp layout per node (its
+// block's warps take whole nodes).  A replay takes the chain's shape, so that
+// a chain committed by replay repeats the verify arithmetic bit for bit.
+void auto_tile(int dk, int dv, int B, int Hv, bool level_walk, int* wc, int* nw) {
   *wc = 16;
   *nw = 1;
   const int64_t blocks = (int64_t)(dv / 16) * Hv * B;
-  if (!tree && (dk == 128 || dk == 64) && blocks <= kTwoWarpBlocks) *nw = 2;
+  if (!level_walk && (dk == 128 || dk == 64) && blocks <= kTwoWarpBlocks) *nw = 2;
 }
 
 int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, bool tree,
@@ -71,9 +70,8 @@ int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
     if (p == nullptr) return GDN_ERR_INVALID_ARG;
     if (!gdn::aligned16(p)) return GDN_ERR_MISALIGNED;
   }
-  // a chain may skip persistence (commit by replay); a tree re-reads persisted
-  // states when its stash pool runs out, so it needs them
-  if (a->snapshots == nullptr && tree) return GDN_ERR_INVALID_ARG;
+  // snapshots may be NULL: nothing is persisted and the accepted state is
+  // committed by replay
   if (snap16 == nullptr && a->snapshots != nullptr && !gdn::aligned16(a->snapshots))
     return GDN_ERR_MISALIGNED;
   if (snap16 != nullptr && !gdn::aligned16(snap16)) return GDN_ERR_MISALIGNED;
@@ -85,7 +83,8 @@ int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
     if (!ok_ptr4(p)) return GDN_ERR_MISALIGNED;
 
   int wc = 0, nw = 0;
-  auto_tile(a->dk, a->dv, a->B, a->Hv, tree, &wc, &nw);
+  const bool level_walk = tree && snap16 == nullptr && a->snapshots != nullptr;
+  auto_tile(a->dk, a->dv, a->B, a->Hv, level_walk, &wc, &nw);
   if (a->tile_cols != 0) wc = a->tile_cols;
   if (a->row_warps != 0) nw = a->row_warps;
   else if (!gdn::verify_tile_supported(a->dk, wc, nw)) nw = 1;  // automatic, for a forced width
@@ -216,6 +215,13 @@ int gdn_verify_chain_f16(const gdn_verify_args* args, void* snapshots_f16, void*
   GDN_RANGE();
   if (snapshots_f16 == nullptr) return GDN_ERR_INVALID_ARG;
   return verify_common(args, nullptr, nullptr, false, stream, snapshots_f16);
+}
+
+int gdn_verify_tree_f16(const gdn_verify_args* args, const int32_t* parent, int32_t* depth_out,
+                        void* snapshots_f16, void* stream) {
+  GDN_RANGE();
+  if (snapshots_f16 == nullptr) return GDN_ERR_INVALID_ARG;
+  return verify_common(args, parent, depth_out, true, stream, snapshots_f16);
 }
 
 int gdn_commit_accepted(const float* snapshots, int64_t snap_layer_stride,

@@ -1,0 +1,898 @@
+// Tree verification by one solve per block, then a stream of states: the
+// gated delta rule over a draft tree verified under its ancestor mask ("Qwen3.6
+// 27B: From 20 t/s to 184 t/s", DFlash section, steps 3-4), for the cases the
+// level-by-level tree walk in gdn_verify.cu cannot serve because it reads
+// parent states back from the persisted snapshots: binary16 snapshots ("We got
+// 207 tok/s with Qwen3.5-27B on an RTX 3090", list "Key wins": an f16
+// intermediate cache "at the same tree budget") and trees verified without
+// snapshots, committed by replay ("Photon 2.6", section "Handling recurrent
+// state").  This kernel never reads a persisted state back.
+//
+// Recurrence
+// ----------
+// The state of one value head is H = S^T (d_k x d_v, fp32, row-major).  With
+// src(n) the parent of node n (the cached state H0 for the root),
+//     delta_n = beta_n (v_n - alpha_n H_src(n)^T k_n),
+//     H_n = alpha_n H_src(n) + k_n delta_n^T,   o_n = H_n^T q_n,
+// which is S_n = alpha_n S_src(n) (I - beta_n k_n k_n^T) + beta_n v_n k_n^T,
+// o_n = S_n q_n with the product distributed.
+//
+// The block solved at once
+// ------------------------
+// Unrolling the recurrence along the path from H0 to node n, with r(n, m) the
+// product of alpha over the path nodes after m up to n (r(n, n) = 1; g_n =
+// r(n, -1), the product over the whole path),
+//     H_n = g_n H0 + sum_{m in path(n)} r(n, m) k_m delta_m^T.
+// Putting that into delta_n gives one lower-triangular system for all nodes
+// of the block,
+//     (I + A) Delta = X,   A[n][m] = beta_n r(n, m) (k_n . k_m)   (m a strict ancestor of n),
+//                          X[n]    = beta_n (v_n - g_n H0^T k_n),
+// and the outputs
+//     o_n = g_n H0^T q_n + sum_{m in path(n)} r(n, m) (q_n . k_m) delta_m.
+// The decay products are taken from the log decay along the path,
+// r(n, m) = e^(L_n - L_m) with L_n the sum of log alpha over path(n).  A block
+// is verified in three phases, none of which walks the nodes through a
+// reduction:
+//   1. K K^T and Q K^T on tensor cores (mma.sync; exact for bf16 inputs), r,
+//      A and P = r (Q K^T) under the ancestor mask, and the depth-first order
+//      of the tree; none of it needs the cached state, so it overlaps that
+//      state's load;
+//   2. K H0 and Q H0 on tensor cores (the fp32 state split into bf16 hi + lo),
+//      X, Delta by forward substitution (one column per lane, 16 rows at a
+//      time in registers) and the outputs O = diag(g) Q H0 + P Delta;
+//   3. the states, column slab by column slab in registers, in depth-first
+//      order: H_n = alpha_n H_parent + k_n delta_n^T when the parent's state
+//      is the one just formed, otherwise g_n H0 plus the path's terms; each
+//      state leaves as 16-byte vector stores (fp32 or binary16) while the next
+//      is formed.
+//
+// Work decomposition
+// ------------------
+// A thread block owns a slab of WC columns of one (sequence, value head):
+// grid = (dv / WC, Hv, B).  In phase 3, lane = cg + CG*rl of warp wi keeps R
+// consecutive rows (row0 = wi*DK/NW + rl*R) x 4 columns (cg) of the state as
+// float2 pairs.  Phases 1-2 use all warps of the block on small matrices in
+// shared memory.
+//
+// Variants (template flags): SNAP16 persists binary16 snapshots (rounded to
+// nearest even from the fp32 states); PREP takes raw q/k projections and gate
+// pre-activations (1/|q|, 1/|k| scale the products, alpha = 1/(1 + e^a),
+// beta = sigmoid(b)); SPLIT takes fp32 q/k/v, whose tensor-core operands are
+// split into bf16 hi + lo.
+#include <cuda_fp16.h>
+
+#include "gdn_common.cuh"
+#include "gdn_launch.h"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+namespace {
+
+template <int DK, int WC, int NW>
+struct Shape {
+  static constexpr int CG = WC / 4;        // 16-byte column groups per row of the slab
+  static constexpr int RL = 32 / CG;       // row lanes per warp
+  static constexpr int R = DK / (RL * NW); // rows per lane (NW warps split the rows)
+  static_assert(WC % 4 == 0 && 32 % CG == 0 && RL >= 2, "slab width");
+  static_assert(R >= 1 && R * RL * NW == DK, "row split");
+};
+
+__host__ __device__ constexpr int round16(int x) { return (x + 15) & ~15; }
+
+// Shared-memory plan in bytes (every array on a 16-byte boundary).  NP = N
+// rounded up to the 16 rows of a tensor-core tile.
+//   ks, qs   [NP][lds]  bf16  k and q rows (with SPLIT a lo plane follows)
+//   kf       [N][DK]    fp32  k rows (scaled by 1/|k| for PREP); with SPLIT
+//                             the fp32 k rows are staged here, and the fp32 q
+//                             rows over kk.. (dead until K K^T is formed)
+//   h0       [DK][ldh]  fp32  the cached state's slab
+//   v        [N][WC]    input the v slab
+//   a, b, g  [N]        fp32  alpha, beta, g_n = r(n, -1)
+//   L        [N]        fp32  log decay along the path, r(n, m) = e^(L_n - L_m)
+//   ord      [N]        int   the order phase 3 forms the states in (a tree:
+//                             depth first, so most nodes follow their parent)
+//   iq, ik   [NP]       fp32  1/|q_n|, 1/|k_n| (PREP; zero past N)
+//   par, dep [N]        int   parent (chain: n - 1), depth (root = 1)
+//   anc      [N]        u64   strict ancestors as a bit set
+//   kk, qk, rr [NP][ldm] fp32  K K^T -> A, Q K^T -> P, r(n, m)
+//   u, qh, d [NP][WC]   fp32  K H0 -> X, Q H0, Delta
+struct Plan {
+  int ks, qs, kf, h0, v, a, b, g, L, ord, iq, ik, par, dep, anc, kk, qk, rr, u, qh, d, total;
+  int NP, lds, ldh, ldm;
+};
+
+__host__ __device__ inline Plan make_plan(int N, int DK, int WC, bool split, bool has_q) {
+  Plan s{};
+  s.NP = (N + 15) & ~15;
+  s.lds = DK + 8;
+  s.ldh = WC + 4;
+  s.ldm = s.NP + 4;
+  const int esz = split ? 4 : 2;
+  const int planes = split ? 2 : 1;
+  int o = 0;
+  s.ks = o; o += round16(planes * s.NP * s.lds * 2);
+  s.qs = o; o += has_q ? round16(planes * s.NP * s.lds * 2) : 0;
+  s.kf = o; o += round16(N * DK * 4);
+  s.h0 = o; o += round16(DK * s.ldh * 4);
+  s.v = o; o += round16(N * WC * esz);
+  s.a = o; o += round16(N * 4);
+  s.b = o; o += round16(N * 4);
+  s.g = o; o += round16(N * 4);
+  s.L = o; o += round16(N * 4);
+  s.ord = o; o += round16(N * 4);
+  s.iq = o; o += round16(s.NP * 4);
+  s.ik = o; o += round16(s.NP * 4);
+  s.par = o; o += round16(N * 4);
+  s.dep = o; o += round16(N * 4);
+  s.anc = o; o += round16(N * 8);
+  const int mat = round16(s.NP * s.ldm * 4);
+  s.kk = o; o += mat;
+  s.qk = o; o += has_q ? mat : 0;
+  s.rr = o; o += mat;
+  const int slab = round16(s.NP * WC * 4);
+  s.u = o; o += slab;
+  s.qh = o; o += has_q ? slab : 0;
+  s.d = o; o += slab;
+  s.total = o;
+  if (split && has_q && s.total < s.kk + N * DK * 4) s.total = s.kk + round16(N * DK * 4);
+  return s;
+}
+
+struct VerifyParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* alpha;
+  const float* beta;
+  const float* cache;
+  const int32_t* slot;
+  float* snap;
+  __half* snap16;  // binary16 snapshots instead of snap
+  float* o;
+  int32_t* status;
+  const int32_t* parent;  // tree verify only
+  int32_t* depth_out;
+  int64_t cache_slot_stride;
+  int n_slots, N, Hk, Hv, dv, bf16;
+  int hint;       // issue the pre-wait L2 hints
+  int max_depth;  // tree: deepest node allowed (root = 1), 0 = no cap
+};
+
+struct ReplayParams {
+  const void* k;
+  const void* v;
+  const float* alpha;
+  const float* beta;
+  float* cache;
+  const int32_t* slot;
+  const int32_t* parent;
+  const int32_t* accept;
+  int32_t* status;
+  int64_t cache_slot_stride;
+  int n_slots, N, Hk, Hv, dv, bf16;
+};
+
+// Launches of up to this many blocks (4 per SM on 152 SMs, one wave) issue
+// the pre-wait L2 hints.  A larger launch runs in several waves behind a
+// stream of snapshot writes that evicts the hinted lines before they are
+// used.
+constexpr int kHintBlocks = 608;
+
+__device__ __forceinline__ void prefetch_l2(const void* a) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a));
+}
+
+// Before the programmatic wait (which orders this kernel after the previous
+// one on the stream): hint L2 with the lines the block is about to read, so
+// that their DRAM latency overlaps the previous kernel's tail.  The slot table
+// and the inputs may still be being written by that kernel: a stale or
+// out-of-range slot only wastes (or skips) the hint, a prefetch never changes
+// memory, and every load that feeds a result is issued after the wait.
+template <int DK>
+__device__ __forceinline__ void prefetch_block(const VerifyParams& p, int b, int h, int hk, int j0,
+                                               int WC, int t, int nt) {
+  const int N = p.N, dv = p.dv, esz = p.bf16 ? 2 : 4;
+  const int s0 = p.slot != nullptr ? __ldcg(p.slot + b) : b;
+  const int seg = (WC * 4 + 127) / 128;  // 128-byte lines per state row of the slab
+  if (s0 >= 0 && s0 < p.n_slots) {
+    const char* c0 = reinterpret_cast<const char*>(p.cache + (int64_t)s0 * p.cache_slot_stride +
+                                                   (int64_t)h * DK * dv + j0);
+    for (int i = t; i < DK * seg; i += nt)
+      prefetch_l2(c0 + (int64_t)(i / seg) * dv * 4 + (i % seg) * 128);
+  }
+  const int per = (DK * esz + 127) / 128;
+  const int qk_lines = N * per;
+  const int64_t node0 = (int64_t)b * N;
+  for (int i = t; i < 2 * qk_lines + N; i += nt) {
+    if (i < 2 * qk_lines) {
+      const int which = i / qk_lines, r = i - which * qk_lines;
+      const int n = r / per, part = r - n * per;
+      const char* base = static_cast<const char*>(which ? p.q : p.k);
+      prefetch_l2(base + ((node0 + n) * p.Hk + hk) * DK * esz + part * 128);
+    } else {
+      const int n = i - 2 * qk_lines;
+      prefetch_l2(static_cast<const char*>(p.v) + ((node0 + n) * p.Hv + h) * dv * esz +
+                  (int64_t)j0 * esz);
+    }
+  }
+}
+
+// Start copying rows rows[i] (i < n_rows; rows 0.. when rows is null) of
+// row_bytes bytes each (row r at src + r*src_stride) to dst + i*dst_stride
+// with 16-byte cp.async, thread t of nt.
+__device__ __forceinline__ void stage_rows(char* dst, int dst_stride, const char* src,
+                                           int64_t src_stride, const int* rows, int n_rows,
+                                           int row_bytes, int t, int nt) {
+  const int per_row = row_bytes / 16;
+  for (int idx = t; idx < n_rows * per_row; idx += nt) {
+    const int i = idx / per_row, c = idx - i * per_row;
+    const int r = rows != nullptr ? rows[i] : i;
+    cp_async16(dst + i * dst_stride + c * 16, src + r * src_stride + c * 16);
+  }
+}
+
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+
+__device__ __forceinline__ uint32_t lds32(const uint16_t* p) {
+  return *reinterpret_cast<const uint32_t*>(p);
+}
+
+// ---------------------------------------------------------- phases 1 and 2
+// Tile fragments for mma.sync m16n8k16 (bf16 operands, fp32 accumulate):
+//   frag_a:  rows r0..r0+15, columns k0..k0+15 of a bf16 matrix [row][ld]
+//   frag_bt: B[k][n] = M[n][k] for n0..n0+7 (a bf16 matrix stored [n][ld])
+//   frag_bs: B[k][n] = M[k][n] of an fp32 matrix [k][ld], split into hi + lo
+__device__ __forceinline__ void frag_a(const uint16_t* A, int ld, int r0, int k0, int g8, int t4,
+                                       uint32_t (&a)[4]) {
+  const uint16_t* p = A + (r0 + g8) * ld + k0 + 2 * t4;
+  a[0] = lds32(p);
+  a[1] = lds32(p + 8 * ld);
+  a[2] = lds32(p + 8);
+  a[3] = lds32(p + 8 * ld + 8);
+}
+
+__device__ __forceinline__ void frag_bt(const uint16_t* M, int ld, int n0, int k0, int g8, int t4,
+                                        uint32_t& b0, uint32_t& b1) {
+  const uint16_t* p = M + (n0 + g8) * ld + k0 + 2 * t4;
+  b0 = lds32(p);
+  b1 = lds32(p + 8);
+}
+
+__device__ __forceinline__ void frag_bs(const float* M, int ld, int k0, int n0, int g8, int t4,
+                                        uint32_t (&hi)[2], uint32_t (&lo)[2]) {
+  const float* p = M + (k0 + 2 * t4) * ld + n0 + g8;
+  tc::split_bf16x2(p[0], p[ld], hi[0], lo[0]);
+  tc::split_bf16x2(p[8 * ld], p[9 * ld], hi[1], lo[1]);
+}
+
+// One 16 x 8 tile of C = A B over DK, scaled by the row and column factors
+// (when given) and written into the fp32 matrix C [row][ldc].
+//   BT: B[k][n] = Bm[n][k] (bf16, exact); otherwise B is the fp32 state slab
+//   [k][ldb] split into hi + lo.  SPLIT: A (and a bf16 B) carry a lo plane
+//   `plane` elements after the hi plane.
+template <int DK, bool BT, bool SPLIT>
+__device__ __forceinline__ void tile_mma(const uint16_t* A, int lda, int plane, const void* Bm,
+                                         int ldb, int r0, int n0, float* C, int ldc,
+                                         const float* rs, const float* cs, int g8, int t4) {
+  // two accumulators (even and odd k-steps) halve the chain of dependent MMAs
+  float accs[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+  for (int k0 = 0; k0 < DK; k0 += 16) {
+    float (&acc)[4] = accs[(k0 >> 4) & 1];
+    uint32_t ah[4];
+    frag_a(A, lda, r0, k0, g8, t4, ah);
+    if constexpr (BT) {
+      const uint16_t* B = static_cast<const uint16_t*>(Bm);
+      uint32_t b0, b1;
+      frag_bt(B, ldb, n0, k0, g8, t4, b0, b1);
+      mma_bf16_16816(acc, ah, b0, b1);
+      if constexpr (SPLIT) {
+        uint32_t al[4], c0, c1;
+        frag_a(A + plane, lda, r0, k0, g8, t4, al);
+        frag_bt(B + plane, ldb, n0, k0, g8, t4, c0, c1);
+        mma_bf16_16816(acc, ah, c0, c1);
+        mma_bf16_16816(acc, al, b0, b1);
+      }
+    } else {
+      uint32_t bh[2], bl[2];
+      frag_bs(static_cast<const float*>(Bm), ldb, k0, n0, g8, t4, bh, bl);
+      mma_bf16_16816(acc, ah, bh[0], bh[1]);
+      mma_bf16_16816(acc, ah, bl[0], bl[1]);
+      if constexpr (SPLIT) {
+        uint32_t al[4];
+        frag_a(A + plane, lda, r0, k0, g8, t4, al);
+        mma_bf16_16816(acc, al, bh[0], bh[1]);
+      }
+    }
+  }
+  float acc[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) acc[e] = accs[0][e] + accs[1][e];
+  const int r = r0 + g8, c = n0 + 2 * t4;
+  float s0 = 1.f, s1 = 1.f, t0 = 1.f, t1 = 1.f;
+  if (rs != nullptr) {
+    s0 = rs[r];
+    s1 = rs[r + 8];
+  }
+  if (cs != nullptr) {
+    t0 = cs[c];
+    t1 = cs[c + 1];
+  }
+  *reinterpret_cast<float2*>(C + r * ldc + c) = make_float2(acc[0] * s0 * t0, acc[1] * s0 * t1);
+  *reinterpret_cast<float2*>(C + (r + 8) * ldc + c) =
+      make_float2(acc[2] * s1 * t0, acc[3] * s1 * t1);
+}
+
+// Phase 1 for N nodes whose k (and q) rows, gates and parents are staged:
+// the working forms of the inputs, the tree's depths and ancestor sets,
+// K K^T and Q K^T, the decay products r, A and P.  Returns 0, or 1 if the
+// parent array is malformed, 2 if the tree is deeper than max_depth (depths
+// filled in); every thread returns the same value.
+template <int DK, int NW, bool TREE, bool SPLIT, bool PREP, bool HAS_Q>
+__device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth) {
+  constexpr int NT = 32 * NW;
+  const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  uint16_t* ks = reinterpret_cast<uint16_t*>(smem + pl.ks);
+  uint16_t* qs = reinterpret_cast<uint16_t*>(smem + pl.qs);
+  float* kf = reinterpret_cast<float*>(smem + pl.kf);
+  // fp32 inputs (SPLIT): k staged in kf, q over the matrices
+  const float* rawk = kf;
+  const float* rawq = reinterpret_cast<const float*>(smem + pl.kk);
+  float* sa = reinterpret_cast<float*>(smem + pl.a);
+  float* sb = reinterpret_cast<float*>(smem + pl.b);
+  float* sg = reinterpret_cast<float*>(smem + pl.g);
+  float* siq = reinterpret_cast<float*>(smem + pl.iq);
+  float* sik = reinterpret_cast<float*>(smem + pl.ik);
+  const int* spar = reinterpret_cast<const int*>(smem + pl.par);
+  int* sdep = reinterpret_cast<int*>(smem + pl.dep);
+  uint64_t* sanc = reinterpret_cast<uint64_t*>(smem + pl.anc);
+  float* kk = reinterpret_cast<float*>(smem + pl.kk);
+  float* qk = reinterpret_cast<float*>(smem + pl.qk);
+  float* rr = reinterpret_cast<float*>(smem + pl.rr);
+  const int NP = pl.NP, lds = pl.lds, ldm = pl.ldm;
+  const int plane = NP * lds;
+
+  // ---- fp32 rows split into bf16 planes (SPLIT), norms and gate maps (PREP)
+  if constexpr (SPLIT) {
+    const int half = N * DK / 2;
+    for (int i = tid; i < (HAS_Q ? 2 : 1) * half; i += NT) {
+      const int which = i / half, e = 2 * (i - which * half);
+      const int n = e / DK, c = e - n * DK;
+      const float2 x = *reinterpret_cast<const float2*>((which ? rawq : rawk) + e);
+      uint32_t hi, lo;
+      tc::split_bf16x2(x.x, x.y, hi, lo);
+      uint16_t* dst = (which ? qs : ks) + n * lds + c;
+      *reinterpret_cast<uint32_t*>(dst) = hi;
+      *reinterpret_cast<uint32_t*>(dst + plane) = lo;
+    }
+  }
+  if constexpr (PREP) {
+    for (int r = tid; r < 2 * NP; r += NT) {
+      const int which = r / NP, n = r - which * NP;
+      float ss = 0.f;
+      if (n < N && (HAS_Q || which == 0)) {
+        if constexpr (SPLIT) {
+          const float* x = (which ? rawq : rawk) + n * DK;
+          for (int c = 0; c < DK; ++c) ss = fmaf(x[c], x[c], ss);
+        } else {
+          const uint16_t* x = (which ? qs : ks) + n * lds;
+          for (int c = 0; c < DK; c += 2) {
+            const uint32_t w = lds32(x + c);
+            const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+          }
+        }
+      }
+      (which ? siq : sik)[n] = ss > 0.f ? rsqrtf(ss) : 0.f;
+    }
+    for (int n = tid; n < N; n += NT) {
+      sa[n] = 1.f / (1.f + __expf(sa[n]));
+      sb[n] = 1.f / (1.f + __expf(-sb[n]));
+    }
+  }
+  __syncthreads();
+  // k rows in fp32 for phase 3 (normalised for PREP), 8 elements a step
+  for (int i = tid; i < N * DK / 8; i += NT) {
+    const int e = 8 * i, n = e / DK, c = e - n * DK;
+    float x[8];
+    if constexpr (SPLIT) {
+      const float4 u0 = *reinterpret_cast<const float4*>(rawk + e);
+      const float4 u1 = *reinterpret_cast<const float4*>(rawk + e + 4);
+      x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
+      x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+    } else {
+      const uint4 w = *reinterpret_cast<const uint4*>(ks + n * lds + c);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[2 * j] = __uint_as_float(ww[j] << 16);
+        x[2 * j + 1] = __uint_as_float(ww[j] & 0xffff0000u);
+      }
+    }
+    const float sc = PREP ? sik[n] : 1.f;
+    *reinterpret_cast<float4*>(kf + e) = make_float4(sc * x[0], sc * x[1], sc * x[2], sc * x[3]);
+    *reinterpret_cast<float4*>(kf + e + 4) = make_float4(sc * x[4], sc * x[5], sc * x[6], sc * x[7]);
+  }
+
+  // ---- depths, strict ancestors and the log decay L_n = sum over the path of
+  //      log alpha (alpha clamped below at 1e-30, where its log is finite)
+  float* sL = reinterpret_cast<float*>(smem + pl.L);
+  int* sord = reinterpret_cast<int*>(smem + pl.ord);
+  if constexpr (TREE) {
+    bool ok = true;
+    for (int n = tid; n < N; n += NT) {
+      const int pp = spar[n];
+      ok = ok && (n == 0 ? pp == -1 : (pp >= 0 && pp < n));
+    }
+    if (__syncthreads_and(ok) == 0) return 1;
+    bool shallow = true;
+    for (int n = tid; n < N; n += NT) {
+      int d = 1;
+      uint64_t anc = 0;
+      float l = logf(fmaxf(sa[n], 1e-30f));
+      for (int m = spar[n]; m >= 0; m = spar[m]) {
+        ++d;
+        anc |= 1ull << m;
+        l += logf(fmaxf(sa[m], 1e-30f));
+      }
+      sdep[n] = d;
+      sanc[n] = anc;
+      sL[n] = l;
+      shallow = shallow && (max_depth <= 0 || d <= max_depth);
+    }
+    if (__syncthreads_and(shallow) == 0) return 2;
+  } else {
+    for (int n = tid; n < N; n += NT) {
+      sdep[n] = n + 1;
+      sanc[n] = (1ull << n) - 1;
+      sord[n] = n;
+    }
+    if (wi == 0) {
+      // inclusive scan of log alpha over the chain, two nodes per lane
+      const int n0 = 2 * lane, n1 = n0 + 1;
+      const float l0 = n0 < N ? logf(fmaxf(sa[n0], 1e-30f)) : 0.f;
+      const float l1 = n1 < N ? logf(fmaxf(sa[n1], 1e-30f)) : 0.f;
+      float sum = l0 + l1;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, sum, off);
+        if (lane >= off) sum += y;
+      }
+      float excl = __shfl_up_sync(0xffffffffu, sum, 1);
+      if (lane == 0) excl = 0.f;
+      const float L0 = excl + l0;
+      if (n0 < N) sL[n0] = L0;
+      if (n1 < N) sL[n1] = L0 + l1;
+    }
+  }
+
+  // ---- K K^T and Q K^T, the tiles on and below the diagonal (PREP: scaled
+  //      by 1/|q_n| or 1/|k_n| and 1/|k_m|)
+  {
+    const int mt_n = NP / 16, nt_n = NP / 8, n_tiles = mt_n * nt_n;
+    for (int task = wi; task < (HAS_Q ? 2 : 1) * n_tiles; task += NW) {
+      const int which = task / n_tiles, tl = task - which * n_tiles;
+      const int mt = tl / nt_n, nt = tl - mt * nt_n;
+      if (nt * 8 > mt * 16 + 15) continue;
+      tile_mma<DK, true, SPLIT>(which ? qs : ks, lds, plane, ks, lds, mt * 16, nt * 8,
+                                which ? qk : kk, ldm, PREP ? (which ? siq : sik) : nullptr,
+                                PREP ? sik : nullptr, g8, t4);
+    }
+  }
+  __syncthreads();
+
+  // ---- r(n, m) = e^(L_n - L_m) for the strict ancestors m of n (1 on the
+  //      diagonal), A = beta r (K K^T) and P = r (Q K^T) under the ancestor
+  //      mask and zero elsewhere, g_n = e^(L_n); every entry on its own
+  for (int idx = tid; idx < NP * (NP + 1); idx += NT) {
+    const int n = idx / (NP + 1), m = idx - n * (NP + 1) - 1;  // m = -1 .. NP-1
+    if (m < 0) {
+      if (n < N) sg[n] = expf(sL[n]);
+      continue;
+    }
+    const bool anc = n < N && m < n && ((sanc[n] >> m) & 1ull) != 0;
+    const float r = anc ? expf(sL[n] - sL[m]) : (n == m && n < N ? 1.f : 0.f);
+    rr[n * ldm + m] = r;
+    kk[n * ldm + m] = anc ? sb[n] * r * kk[n * ldm + m] : 0.f;
+    if constexpr (HAS_Q) qk[n * ldm + m] = r != 0.f ? r * qk[n * ldm + m] : 0.f;
+  }
+  if constexpr (TREE) {
+    // depth-first order: a node after its parent and the parent's earlier
+    // subtrees (children in index order), from the subtree sizes
+    int* ssz = reinterpret_cast<int*>(smem + pl.u);  // free until phase 2
+    for (int n = tid; n < N; n += NT) {
+      int sz = 1;
+      for (int m = n + 1; m < N; ++m) sz += (int)((sanc[m] >> n) & 1ull);
+      ssz[n] = sz;
+    }
+    __syncthreads();
+    for (int n = tid; n < N; n += NT) {
+      int pre = 0;
+      for (int a = n; a > 0; a = spar[a]) {
+        const int pa = spar[a];
+        pre += 1;
+        for (int s2 = pa + 1; s2 < a; ++s2)
+          if (spar[s2] == pa) pre += ssz[s2];
+      }
+      sord[pre] = n;
+    }
+  }
+  __syncthreads();
+  return 0;
+}
+
+// Phase 2, once the state slab is in h0: K H0 and Q H0 on tensor cores,
+// X = diag(beta)(V - diag(g) K H0), Delta solving (I + A) Delta = X by forward
+// substitution, and (with HAS_Q) the outputs O = diag(g) Q H0 + P Delta, row
+// n to o_out + n*o_stride (WC columns).  The substitution and the outputs run
+// one column per lane of warp 0, 16 rows at a time in registers: the rows
+// of a block take the earlier blocks' terms as independent sums, then solve
+// among themselves.
+template <int DK, int WC, int NW, bool SPLIT, bool PREP, bool HAS_Q>
+__device__ void solve_finish(const Plan& pl, char* smem, int N, float* o_out, int64_t o_stride) {
+  constexpr int NT = 32 * NW;
+  const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const uint16_t* ks = reinterpret_cast<const uint16_t*>(smem + pl.ks);
+  const uint16_t* qs = reinterpret_cast<const uint16_t*>(smem + pl.qs);
+  const float* h0 = reinterpret_cast<const float*>(smem + pl.h0);
+  const float* sb = reinterpret_cast<const float*>(smem + pl.b);
+  const float* sg = reinterpret_cast<const float*>(smem + pl.g);
+  const float* siq = reinterpret_cast<const float*>(smem + pl.iq);
+  const float* sik = reinterpret_cast<const float*>(smem + pl.ik);
+  const float* kk = reinterpret_cast<const float*>(smem + pl.kk);
+  const float* qk = reinterpret_cast<const float*>(smem + pl.qk);
+  float* su = reinterpret_cast<float*>(smem + pl.u);
+  float* sqh = reinterpret_cast<float*>(smem + pl.qh);
+  float* sd = reinterpret_cast<float*>(smem + pl.d);
+  const int NP = pl.NP, lds = pl.lds, ldm = pl.ldm, ldh = pl.ldh;
+  const int plane = NP * lds;
+
+  {
+    const int mt_n = NP / 16, nt_n = WC / 8, n_tiles = mt_n * nt_n;
+    for (int task = wi; task < (HAS_Q ? 2 : 1) * n_tiles; task += NW) {
+      const int which = task / n_tiles, tl = task - which * n_tiles;
+      const int mt = tl / nt_n, nt = tl - mt * nt_n;
+      tile_mma<DK, false, SPLIT>(which ? qs : ks, lds, plane, h0, ldh, mt * 16, nt * 8,
+                                 which ? sqh : su, WC, PREP ? (which ? siq : sik) : nullptr,
+                                 nullptr, g8, t4);
+    }
+  }
+  __syncthreads();
+  // X in place of K H0 (the v slab is staged in the input dtype)
+  for (int idx = tid; idx < N * WC; idx += NT) {
+    const int n = idx / WC;
+    float vv;
+    if constexpr (SPLIT) vv = reinterpret_cast<const float*>(smem + pl.v)[idx];
+    else vv = bf16_to_f32(reinterpret_cast<const uint16_t*>(smem + pl.v)[idx]);
+    su[idx] = sb[n] * (vv - sg[n] * su[idx]);
+  }
+  __syncthreads();
+  if (wi == 0 && lane < WC) {
+    const int c = lane;
+    for (int n0 = 0; n0 < N; n0 += 16) {
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = n0 + i < N ? su[(n0 + i) * WC + c] : 0.f;
+      // the earlier blocks' terms
+      for (int m = 0; m < n0; ++m) {
+        const float dm = sd[m * WC + c];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = fmaf(-kk[(n0 + i) * ldm + m], dm, x[i]);
+      }
+      // the block's own rows, in order
+#pragma unroll
+      for (int i = 1; i < 16; ++i)
+#pragma unroll
+        for (int t = 0; t < i; ++t) x[i] = fmaf(-kk[(n0 + i) * ldm + n0 + t], x[t], x[i]);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sd[(n0 + i) * WC + c] = x[i];
+    }
+  }
+  if constexpr (HAS_Q) {
+    __syncthreads();
+    // O = diag(g) Q H0 + P Delta (P is zero above the diagonal), every output
+    // on its own
+    for (int idx = tid; idx < N * WC; idx += NT) {
+      const int n = idx / WC, c = idx - n * WC;
+      float e0 = sg[n] * sqh[idx], e1 = 0.f;
+      int m = 0;
+      for (; m + 1 <= n; m += 2) {
+        e0 = fmaf(qk[n * ldm + m], sd[m * WC + c], e0);
+        e1 = fmaf(qk[n * ldm + m + 1], sd[(m + 1) * WC + c], e1);
+      }
+      if (m <= n) e0 = fmaf(qk[n * ldm + m], sd[m * WC + c], e0);
+      o_out[n * o_stride + c] = e0 + e1;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- phase 3
+// x[0..R) = R consecutive fp32 values of a k row.
+template <int R>
+__device__ __forceinline__ void load_k(float (&x)[R], const float* row) {
+  if constexpr (R % 4 == 0) {
+#pragma unroll
+    for (int m = 0; m < R; m += 4) {
+      const float4 t = *reinterpret_cast<const float4*>(row + m);
+      x[m] = t.x; x[m + 1] = t.y; x[m + 2] = t.z; x[m + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int m = 0; m < R; ++m) x[m] = row[m];
+  }
+}
+
+// H <- alpha H + k delta^T on this lane's R x 4 block.
+template <int R>
+__device__ __forceinline__ void rank1_step(float2 (&H)[R][2], const float (&k)[R], float4 dl,
+                                           float al) {
+  const float2 d01 = make_float2(dl.x, dl.y), d23 = make_float2(dl.z, dl.w), al2 = f2(al);
+#pragma unroll
+  for (int m = 0; m < R; ++m) {
+    H[m][0] = __ffma2_rn(f2(k[m]), d01, __fmul2_rn(al2, H[m][0]));
+    H[m][1] = __ffma2_rn(f2(k[m]), d23, __fmul2_rn(al2, H[m][1]));
+  }
+}
+
+// H <- H + k (s delta)^T.
+template <int R>
+__device__ __forceinline__ void rank1_add(float2 (&H)[R][2], const float (&k)[R], float4 dl,
+                                          float s) {
+  const float2 d01 = make_float2(s * dl.x, s * dl.y), d23 = make_float2(s * dl.z, s * dl.w);
+#pragma unroll
+  for (int m = 0; m < R; ++m) {
+    H[m][0] = __ffma2_rn(f2(k[m]), d01, H[m][0]);
+    H[m][1] = __ffma2_rn(f2(k[m]), d23, H[m][1]);
+  }
+}
+
+template <int R>
+__device__ __forceinline__ void store_state(float* dst, int64_t dv, const float2 (&H)[R][2]) {
+#pragma unroll
+  for (int m = 0; m < R; ++m)
+    st_f4(dst + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
+}
+
+// binary16, round to nearest even: 8 bytes per lane and row
+template <int R>
+__device__ __forceinline__ void store_state16(__half* dst, int64_t dv, const float2 (&H)[R][2]) {
+#pragma unroll
+  for (int m = 0; m < R; ++m) {
+    const __half2 lo = __floats2half2_rn(H[m][0].x, H[m][0].y);
+    const __half2 hi = __floats2half2_rn(H[m][1].x, H[m][1].y);
+    *reinterpret_cast<uint2*>(dst + (int64_t)m * dv) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  }
+}
+
+// Zero the padding rows N .. NP-1 of the bf16 k (and q) tiles.
+__device__ __forceinline__ void zero_padding(const Plan& pl, char* smem, int N, bool split,
+                                             bool has_q, int t, int nt) {
+  uint16_t* ks = reinterpret_cast<uint16_t*>(smem + pl.ks);
+  uint16_t* qs = reinterpret_cast<uint16_t*>(smem + pl.qs);
+  const int per_plane = (pl.NP - N) * pl.lds;
+  const int planes = split ? 2 : 1;
+  for (int i = t; i < planes * per_plane; i += nt) {
+    const int pi = i / per_plane, e = i - pi * per_plane;
+    ks[pi * pl.NP * pl.lds + N * pl.lds + e] = 0;
+    if (has_q) qs[pi * pl.NP * pl.lds + N * pl.lds + e] = 0;
+  }
+}
+
+// ---------------------------------------------------------------- verify
+template <int DK, int WC, int NW, bool TREE, bool SNAP16, bool PREP, bool SPLIT>
+__global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
+  using S = Shape<DK, WC, NW>;
+  constexpr int R = S::R;
+  constexpr int NT = 32 * NW;
+  const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
+  const int j0 = blockIdx.x * WC, h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / (p.Hv / p.Hk);
+  if (p.hint) prefetch_block<DK>(p, b, h, hk, j0, WC, tid, NT);
+  pdl_enter();
+  extern __shared__ __align__(16) char smem[];
+  const int N = p.N, dv = p.dv;
+  const Plan pl = make_plan(N, DK, WC, SPLIT, true);
+  const bool lead = blockIdx.x == 0 && blockIdx.y == 0;  // per-sequence reporting
+  const int64_t node0 = (int64_t)b * N;
+  constexpr int esz = SPLIT ? 4 : 2;
+  int* spar = reinterpret_cast<int*>(smem + pl.par);
+  const int* sdep = reinterpret_cast<const int*>(smem + pl.dep);
+
+  // ---- stage k, q, v, gates and parents (cp.async group 0), then the
+  //      cached state's slab (group 1, waited for only in phase 2)
+  {
+    const char* kb = static_cast<const char*>(p.k) + ((node0 * p.Hk + hk) * DK) * esz;
+    const char* qb = static_cast<const char*>(p.q) + ((node0 * p.Hk + hk) * DK) * esz;
+    const char* vb = static_cast<const char*>(p.v) + ((node0 * p.Hv + h) * dv + j0) * esz;
+    const int64_t qk_stride = (int64_t)p.Hk * DK * esz;
+    if constexpr (SPLIT) {
+      stage_rows(smem + pl.kf, DK * 4, kb, qk_stride, nullptr, N, DK * 4, tid, NT);
+      stage_rows(smem + pl.kk, DK * 4, qb, qk_stride, nullptr, N, DK * 4, tid, NT);
+    } else {
+      stage_rows(smem + pl.ks, pl.lds * 2, kb, qk_stride, nullptr, N, DK * 2, tid, NT);
+      stage_rows(smem + pl.qs, pl.lds * 2, qb, qk_stride, nullptr, N, DK * 2, tid, NT);
+    }
+    stage_rows(smem + pl.v, WC * esz, vb, (int64_t)p.Hv * dv * esz, nullptr, N, WC * esz, tid,
+               NT);
+    for (int n = tid; n < N; n += NT) {
+      cp_async4(reinterpret_cast<float*>(smem + pl.a) + n, p.alpha + (node0 + n) * p.Hv + h);
+      cp_async4(reinterpret_cast<float*>(smem + pl.b) + n, p.beta + (node0 + n) * p.Hv + h);
+      if constexpr (TREE) cp_async4(spar + n, p.parent + node0 + n);
+      else spar[n] = n - 1;
+    }
+    zero_padding(pl, smem, N, SPLIT, true, tid, NT);
+    cp_async_commit();
+  }
+  const int sl = p.slot != nullptr ? __ldg(p.slot + b) : b;
+  const bool slot_ok = sl >= 0 && sl < p.n_slots;
+  if (slot_ok) {
+    const char* c0 = reinterpret_cast<const char*>(p.cache + (int64_t)sl * p.cache_slot_stride +
+                                                   (int64_t)h * DK * dv + j0);
+    stage_rows(smem + pl.h0, pl.ldh * 4, c0, (int64_t)dv * 4, nullptr, DK, WC * 4, tid, NT);
+  }
+  cp_async_commit();
+  if (!slot_ok) {
+    cp_async_wait<0>();
+    if (lead && tid == 0) report(p.status, GDN_ERR_SLOT_RANGE);
+    return;
+  }
+  cp_async_wait<1>();
+  __syncthreads();
+
+  const int bad =
+      solve_prepare<DK, NW, TREE, SPLIT, PREP, true>(pl, smem, N, TREE ? p.max_depth : 0);
+  if (bad != 0) {  // a malformed tree, or one deeper than the cap (depths reported)
+    cp_async_wait<0>();
+    if (lead && tid == 0) report(p.status, GDN_ERR_BAD_TREE);
+    if (TREE && bad == 2 && lead && p.depth_out != nullptr)
+      for (int n = tid; n < N; n += NT) p.depth_out[node0 + n] = sdep[n];
+    return;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  solve_finish<DK, WC, NW, SPLIT, PREP, true>(pl, smem, N, p.o + (node0 * p.Hv + h) * dv + j0,
+                                              (int64_t)p.Hv * dv);
+  if (TREE && lead && p.depth_out != nullptr)
+    for (int n = tid; n < N; n += NT) p.depth_out[node0 + n] = sdep[n];
+  __syncthreads();
+
+  // ---- phase 3: the states in registers, stored as they are formed
+  const int cg = lane % S::CG, rl = lane / S::CG;
+  const int row0 = wi * (DK / NW) + rl * R;
+  const float* h0 = reinterpret_cast<const float*>(smem + pl.h0);
+  const float* kf = reinterpret_cast<const float*>(smem + pl.kf);
+  const float* sd = reinterpret_cast<const float*>(smem + pl.d);
+  const float* sa = reinterpret_cast<const float*>(smem + pl.a);
+  const float* sg = reinterpret_cast<const float*>(smem + pl.g);
+  const float* rr = reinterpret_cast<const float*>(smem + pl.rr);
+  const uint64_t* sanc = reinterpret_cast<const uint64_t*>(smem + pl.anc);
+  float2 H[R][2];
+  float2 Hc[TREE ? R : 1][2];  // the cached state, kept for trees
+#pragma unroll
+  for (int m = 0; m < R; ++m) {
+    const float4 t = *reinterpret_cast<const float4*>(h0 + (row0 + m) * pl.ldh + cg * 4);
+    H[m][0] = make_float2(t.x, t.y);
+    H[m][1] = make_float2(t.z, t.w);
+    if constexpr (TREE) {
+      Hc[m][0] = H[m][0];
+      Hc[m][1] = H[m][1];
+    }
+  }
+  const int64_t node_stride = (int64_t)p.Hv * DK * dv;
+  const int64_t lane_off =
+      ((int64_t)b * N * p.Hv + h) * DK * dv + (int64_t)row0 * dv + j0 + cg * 4;
+  float* snap_l = p.snap == nullptr ? nullptr : p.snap + lane_off;
+  __half* snap16_l = SNAP16 ? p.snap16 + lane_off : nullptr;
+  const int* sord = reinterpret_cast<const int*>(smem + pl.ord);
+  int held = -1;  // the node whose state H holds (-1: the cached state)
+  for (int i = 0; i < N; ++i) {
+    const int n = TREE ? sord[i] : i;
+    float kr[R];
+    if (!TREE || spar[n] == held) {
+      load_k<R>(kr, kf + n * DK + row0);
+      rank1_step<R>(H, kr, *reinterpret_cast<const float4*>(sd + n * WC + cg * 4), sa[n]);
+    } else if constexpr (TREE) {
+      // H_n = g_n H0 + sum over the path of r(n, m) k_m delta_m^T, root first
+      const float2 gn = f2(sg[n]);
+#pragma unroll
+      for (int m = 0; m < R; ++m) {
+        H[m][0] = __fmul2_rn(gn, Hc[m][0]);
+        H[m][1] = __fmul2_rn(gn, Hc[m][1]);
+      }
+      uint64_t path = sanc[n] | (1ull << n);
+      while (path != 0) {
+        const int m = __ffsll((long long)path) - 1;
+        path &= path - 1;
+        load_k<R>(kr, kf + m * DK + row0);
+        rank1_add<R>(H, kr, *reinterpret_cast<const float4*>(sd + m * WC + cg * 4),
+                     rr[n * pl.ldm + m]);
+      }
+    }
+    held = n;
+    if constexpr (SNAP16) store_state16<R>(snap16_l + (int64_t)n * node_stride, dv, H);
+    else if (snap_l != nullptr) store_state<R>(snap_l + (int64_t)n * node_stride, dv, H);
+  }
+}
+
+template <typename Kern, typename Params>
+int launch_with_smem(Kern kern, const Params& p, dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream) {
+  if (smem > 227 * 1024) return GDN_ERR_UNSUPPORTED;
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return GDN_ERR_CUDA;
+  }
+  return launch_pdl(kern, grid, block, smem, stream, p);
+}
+
+template <int DK, int WC, int NW, bool TREE, bool SNAP16, bool PREP>
+int launch_verify_t(const VerifyParams& p, int B, cudaStream_t stream) {
+  const dim3 grid(p.dv / WC, p.Hv, B);
+  if (p.bf16)
+    return launch_with_smem(verify_kernel<DK, WC, NW, TREE, SNAP16, PREP, false>, p, grid,
+                            dim3(32 * NW), make_plan(p.N, DK, WC, false, true).total, stream);
+  return launch_with_smem(verify_kernel<DK, WC, NW, TREE, SNAP16, PREP, true>, p, grid,
+                          dim3(32 * NW), make_plan(p.N, DK, WC, true, true).total, stream);
+}
+
+#define GDN_TILES(X)  \
+  X(128, 16, 1)       \
+  X(128, 16, 2)       \
+  X(128, 8, 1)        \
+  X(64, 16, 1)        \
+  X(64, 16, 2)        \
+  X(64, 8, 1)         \
+  X(32, 16, 1)        \
+  X(32, 8, 1)         \
+  X(16, 16, 1)        \
+  X(16, 8, 1)
+
+template <bool TREE, bool SNAP16, bool PREP>
+int dispatch_verify(const VerifyParams& p, int B, int dk, int wc, int nw, cudaStream_t s) {
+#define GDN_CASE(DK_, WC_, NW_) \
+  if (dk == DK_ && wc == WC_ && nw == NW_) return launch_verify_t<DK_, WC_, NW_, TREE, SNAP16, PREP>(p, B, s);
+  GDN_TILES(GDN_CASE)
+#undef GDN_CASE
+  return GDN_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+int launch_verify_tree_solve(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out,
+                             int wc, int nw, cudaStream_t stream, void* snap16, bool prep) {
+  VerifyParams p{};
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.alpha = a->alpha;
+  p.beta = a->beta;
+  p.cache = a->state_cache;
+  p.slot = a->slot;
+  p.snap = snap16 != nullptr ? nullptr : a->snapshots;
+  p.o = a->o;
+  p.status = a->status;
+  p.parent = parent;
+  p.depth_out = depth_out;
+  p.cache_slot_stride = a->cache_slot_stride;
+  p.n_slots = a->n_slots;
+  p.N = a->N;
+  p.Hk = a->Hk;
+  p.Hv = a->Hv;
+  p.dv = a->dv;
+  p.bf16 = a->in_dtype == GDN_BF16;
+  p.snap16 = static_cast<__half*>(snap16);
+  p.hint = (int64_t)(p.dv / wc) * a->Hv * a->B <= kHintBlocks;
+  p.max_depth = parent != nullptr ? a->max_depth : 0;
+  const bool s16 = snap16 != nullptr;
+  const int B = a->B, dk = a->dk;
+  if (s16) return prep ? dispatch_verify<true, true, true>(p, B, dk, wc, nw, stream)
+                       : dispatch_verify<true, true, false>(p, B, dk, wc, nw, stream);
+  return prep ? dispatch_verify<true, false, true>(p, B, dk, wc, nw, stream)
+              : dispatch_verify<true, false, false>(p, B, dk, wc, nw, stream);
+}
+
+}  // namespace gdn

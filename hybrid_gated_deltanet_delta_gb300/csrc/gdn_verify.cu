@@ -37,7 +37,9 @@
 // loads.  Snapshots leave as 16-byte stores; a warp-wide store covers RL rows
 // x WC*4 contiguous bytes.
 //
-// Variants (template flags): SNAP16 persists binary16 snapshots (chains);
+// Variants (template flags): SNAP16 persists binary16 snapshots (chains; a
+// tree with binary16 snapshots, or with none, is verified by the per-block
+// solve in gdn_solve.cu, which never reads a persisted state back);
 // PREP takes raw q/k projections and gate pre-activations (the per-node
 // inverse norms scale the reduced sums and delta instead of every element);
 // a chain may persist nothing at all and commit by replay, for which
@@ -1069,6 +1071,10 @@ int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   p.snap16 = static_cast<__half*>(snap16);
   p.hint = (int64_t)(p.dv / wc) * a->Hv * a->B <= kHintBlocks;
   p.max_depth = parent != nullptr ? a->max_depth : 0;
+  // a tree whose snapshots are binary16 or not kept at all cannot re-read its
+  // parents from them: it is solved per block instead (gdn_solve.cu)
+  if (parent != nullptr && (snap16 != nullptr || a->snapshots == nullptr))
+    return launch_verify_tree_solve(a, parent, depth_out, wc, nw, stream, snap16, prep);
   if (parent != nullptr)  // row warps do not apply: a tree block's warps take whole nodes
     return prep ? dispatch_tree<true>(p, a->B, a->dk, wc, stream)
                 : dispatch_tree<false>(p, a->B, a->dk, wc, stream);

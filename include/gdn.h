@@ -100,7 +100,7 @@ typedef enum gdn_dtype {
  *   slot          [B] int32 cache slot per sequence; NULL means slot[b] = b
  *   n_slots       number of valid slots (slot[b] is checked against it)
  *   snapshots     [B][N][Hv][dk][dv] fp32 output: S_n of every node.  May be
- *                 NULL for a chain: nothing is persisted and the accepted
+ *                 NULL (chain or tree): nothing is persisted and the accepted
  *                 state is committed by replay (gdn_replay_accepted)
  *   o             [B][N][Hv][dv] fp32 output
  *   status        optional device int32 error word (see above)
@@ -112,8 +112,6 @@ typedef enum gdn_dtype {
  *                 in which the column sums are added, and a replay commit
  *                 repeats a chain verify bit for bit only with the same
  *                 tile.  GDN_ERR_UNSUPPORTED for any other combination.
- *                 A tree verify takes tile_cols only: its block's warps
- *                 take whole nodes of a depth level, never rows.
  *   max_depth     tree verify only: 0 = no cap; otherwise a sequence whose
  *                 tree has a node deeper than max_depth (the root has depth 1)
  *                 is skipped and GDN_ERR_BAD_TREE is written to `status`.
@@ -209,16 +207,19 @@ int gdn_replay_accepted_prep(const gdn_verify_args* args, const int32_t* parent,
                              const int32_t* accept_idx, void* stream);
 
 /*
- * Chain verification with 16-bit persisted states ("We got 207 tok/s with
+ * Verification with 16-bit persisted states ("We got 207 tok/s with
  * Qwen3.5-27B on an RTX 3090", list "Key wins": an f16 intermediate cache at
- * half the bandwidth).  The same as gdn_verify_chain, except that every
- * node's state is written to `snapshots_f16` [B][N][Hv][dk][dv] as IEEE
- * binary16, rounded to nearest even from the fp32 state the recurrence keeps
- * (args->snapshots is not used).  The recurrence itself and the outputs o
- * are unchanged; only the persisted copies are rounded.  Chains only (a tree
- * re-reads persisted parents, which would then continue from rounded states).
+ * half the bandwidth, "at the same tree budget").  The same as
+ * gdn_verify_chain / gdn_verify_tree, except that every node's state is
+ * written to `snapshots_f16` [B][N][Hv][dk][dv] as IEEE binary16, rounded to
+ * nearest even from the fp32 state the kernel forms (args->snapshots is not
+ * used).  The recurrence itself and the outputs o are unchanged: the kernel
+ * never reads a persisted state back, so no node continues from a rounded
+ * one; only the persisted copies are rounded.
  */
 int gdn_verify_chain_f16(const gdn_verify_args* args, void* snapshots_f16, void* stream);
+int gdn_verify_tree_f16(const gdn_verify_args* args, const int32_t* parent, int32_t* depth_out,
+                        void* snapshots_f16, void* stream);
 
 /*
  * gdn_commit_accepted for binary16 snapshots: the accepted node's state is

@@ -122,14 +122,13 @@ def test_verify_tree_needs_parent(lib):
     assert lib.gdn_verify_chain(None, None) == gdn.GDN_ERR_INVALID_ARG
 
 
-def test_verify_tree_needs_snapshots(lib):
-    """A chain may skip persistence (commit by replay); a tree may not.  Only
-    the tree call is made: the chain call would pass the checks and launch."""
-    a = _args(snapshots=0)
+def test_verify_without_snapshots_checks_q(lib):
+    """Chains and trees may skip persistence (commit by replay); the other
+    arguments are still checked (calls that fail before any launch)."""
+    a = _args(snapshots=0, q=0)
+    assert lib.gdn_verify_chain(ctypes.byref(a), None) == gdn.GDN_ERR_INVALID_ARG
     assert lib.gdn_verify_tree(ctypes.byref(a), ctypes.c_void_p(0x90000), None, None) == \
         gdn.GDN_ERR_INVALID_ARG
-    a = _args(snapshots=0x70004, q=0)
-    assert lib.gdn_verify_chain(ctypes.byref(a), None) == gdn.GDN_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("change, acc, want", [
@@ -185,6 +184,13 @@ def test_f16_entry_points_host_checks(lib):
     a = _args(q=0)
     assert lib.gdn_verify_chain_f16(ctypes.byref(a), ctypes.c_void_p(0x70000), None) == \
         gdn.GDN_ERR_INVALID_ARG
+    a = _args()
+    assert lib.gdn_verify_tree_f16(ctypes.byref(a), ctypes.c_void_p(0x90000), None, None,
+                                   None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_verify_tree_f16(ctypes.byref(a), ctypes.c_void_p(0x90000), None,
+                                   ctypes.c_void_p(0x70008), None) == gdn.GDN_ERR_MISALIGNED
+    assert lib.gdn_verify_tree_f16(ctypes.byref(a), None, None, ctypes.c_void_p(0x70000),
+                                   None) == gdn.GDN_ERR_INVALID_ARG
     f = lib.gdn_commit_accepted_f16
     assert f(None, 0, 0x20000, 0x30000, 48 * 128 * 128, 0, None, 1, 1, 16, 48, 128, 128, 1,
              None, None) == gdn.GDN_ERR_INVALID_ARG

@@ -183,3 +183,48 @@ def test_rounds_of_verify_and_replay_equal_sequential(gpu_lib):
     assert st == oracle.OK
     t.cuda.synchronize()
     assert_close(cache_t.cpu().numpy()[0], sT, "rounds of verify + replay")
+
+
+@pytest.mark.parametrize("tile", [(0, 0), (16, 1), (8, 1)])
+def test_tree_verify_without_snapshots_then_replay(gpu_lib, tile):
+    """A draft tree verified with snapshots=None (nothing persisted) gives the
+    oracle's outputs, and the replay commit of the accepted node (the
+    ancestors re-run from the cached state) gives the oracle's accepted
+    state: the whole round persists no per-node state."""
+    t = torch()
+    inp = _inputs(True, seed=7300)
+    o, o_back = guarded((inp["B"], inp["N"], inp["Hv"], inp["dv"]), fill=float("nan"))
+    st = t.zeros(1, dtype=t.int32, device="cuda")
+    cache_t = dev(inp["cache"])
+    gpu_lib.gdn_verify_tree(dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha"]),
+                            dev(inp["beta"]), cache_t, None, o, dev(inp["parent"]),
+                            slot=dev(inp["slot"]), n_slots=inp["n_slots"], status=st,
+                            tile_cols=tile[0], row_warps=tile[1])
+    t.cuda.synchronize()
+    assert st.item() == 0 and canaries_ok(o_back, o.numel())
+    ost, osnap, oo = oracle.verify_inputs(inp)
+    assert ost == oracle.OK
+    assert_close(o.cpu().numpy(), oo, "tree o without snapshots")
+    accept = inp["accept"]
+    rst, cache_t = _gpu_replay(gpu_lib, inp, accept, True, cache_t=cache_t)
+    assert rst == 0
+    ost, ocache = _oracle_replay(inp, accept, True)
+    assert ost == oracle.OK
+    got = cache_t.cpu().numpy()
+    for b in range(inp["B"]):
+        sl = inp["slot"][b]
+        assert_close(got[sl], ocache[sl], f"replayed state, sequence {b}")
+
+
+def test_tree22_without_snapshots_matches_persisting_outputs(gpu_lib):
+    """tree22: the snapshot-free verify gives the persisting verify's outputs
+    within the float bar (the two run different kernels)."""
+    t = torch()
+    inp = synthetic.tree22()
+    out = verify_on_gpu(gpu_lib, inp)
+    o = t.empty((1, 22, 48, 128), device="cuda")
+    gpu_lib.gdn_verify_tree(dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha"]),
+                            dev(inp["beta"]), dev(inp["cache"]), None, o, dev(inp["parent"]),
+                            slot=dev(inp["slot"]), n_slots=inp["n_slots"])
+    t.cuda.synchronize()
+    assert_close(o.cpu().numpy(), out["o"], "snapshot-free tree22 o vs persisting verify")

@@ -110,3 +110,112 @@ def test_rounds_with_f16_commits(gpu_lib):
         ocache = osnap[0, L - 1][None].astype(np.float16).astype(np.float64)
     t.cuda.synchronize()
     assert_close16(cache_t.cpu().numpy(), ocache, "state after 5 binary16 commits", ulps=2)
+
+
+def _run_tree16(gdn, inp, tile=0, row_warps=0, max_depth=0):
+    t = torch()
+    B, N, Hv, dk, dv = inp["B"], inp["N"], inp["Hv"], inp["dk"], inp["dv"]
+    snap16 = t.full((B, N, Hv, dk, dv), float("nan"), dtype=t.float16, device="cuda")
+    o = t.full((B, N, Hv, dv), float("nan"), device="cuda")
+    st = t.zeros(1, dtype=t.int32, device="cuda")
+    depth = t.zeros((B, N), dtype=t.int32, device="cuda")
+    gdn.gdn_verify_tree_f16(dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha"]),
+                            dev(inp["beta"]), dev(inp["cache"]), snap16, o, dev(inp["parent"]),
+                            depth_out=depth, slot=dev(inp["slot"]), n_slots=inp["n_slots"],
+                            status=st, tile_cols=tile, row_warps=row_warps, max_depth=max_depth)
+    t.cuda.synchronize()
+    return int(st.item()), snap16, o, depth
+
+
+@pytest.mark.parametrize("tile", [(0, 0), (16, 1), (8, 1)])
+def test_tree22_f16_snapshots(gpu_lib, tile):
+    """The DDTree block with binary16 snapshots: every node's persisted state
+    within the binary16 bar of the oracle (no node continues from a rounded
+    state: the kernel never reads a persisted state back), outputs within the
+    float bar, depths exact."""
+    inp = synthetic.tree22()
+    st, snap16, o, depth = _run_tree16(gpu_lib, inp, *tile)
+    assert st == 0
+    ost, osnap, oo = oracle.verify_inputs(inp)
+    assert ost == oracle.OK
+    assert_close(o.cpu().numpy(), oo, "tree22 o")
+    assert_close16(snap16.cpu().numpy(), osnap, "tree22 binary16 snapshots vs oracle")
+    assert np.array_equal(depth.cpu().numpy(), oracle.tree_depth(inp["parent"])[1])
+
+
+@pytest.mark.parametrize("shape", ["star", "path", "broom", "random"])
+def test_tree64_f16_snapshots(gpu_lib, shape):
+    """64-node trees of several shapes, three sequences, binary16 snapshots."""
+    B, N = 3, 64
+    inp = synthetic.make_verify_inputs(B=B, N=N, Hk=2, Hv=4, dk=128, dv=32, dtype="bf16",
+                                       alpha_kind="near_one", state_sigma=0.05,
+                                       seed=9300 + len(shape), tree=True, n_slots=B + 1,
+                                       depth_cap=64)
+    if shape != "random":
+        n = np.arange(N)
+        p = {"star": np.where(n == 0, -1, 0), "path": n - 1,
+             "broom": np.where(n < 24, n - 1, 23)}[shape].astype(np.int32)
+        p[0] = -1
+        inp = dict(inp, parent=np.tile(p, (B, 1)))
+    st, snap16, o, depth = _run_tree16(gpu_lib, inp)
+    assert st == 0
+    ost, osnap, oo = oracle.verify_inputs(inp)
+    assert ost == oracle.OK
+    assert_close(o.cpu().numpy(), oo, f"{shape} o")
+    assert_close16(snap16.cpu().numpy(), osnap, f"{shape} binary16 snapshots")
+    assert np.array_equal(depth.cpu().numpy(), oracle.tree_depth(inp["parent"])[1])
+
+
+def test_tree_f16_depth_cap_and_bad_tree(gpu_lib):
+    """The binary16 tree path reports a tree deeper than max_depth and a
+    malformed parent array as GDN_ERR_BAD_TREE and skips only that sequence."""
+    inp = synthetic.make_verify_inputs(B=3, N=8, Hk=1, Hv=2, dk=128, dv=32, dtype="bf16",
+                                       alpha_kind="near_one", state_sigma=0.05, seed=9400,
+                                       tree=True)
+    n = np.arange(8)
+    par = np.stack([np.where(n == 0, -1, 0), n - 1, np.where(n < 4, n - 1, 3)]).astype(np.int32)
+    inp = dict(inp, parent=par)
+    st, snap16, o, _ = _run_tree16(gpu_lib, inp, max_depth=5)
+    assert st == gpu_lib.GDN_ERR_BAD_TREE
+    s16 = snap16.cpu().numpy()
+    assert np.all(np.isnan(s16[1])), "the too-deep tree must be skipped"
+    ost, osnap, _ = oracle.verify_inputs(inp)
+    for b in (0, 2):
+        assert_close16(s16[b], osnap[b], f"sequence {b}")
+    bad = dict(inp, parent=par.copy())
+    bad["parent"][2, 5] = 6
+    st, snap16, _, _ = _run_tree16(gpu_lib, bad)
+    assert st == gpu_lib.GDN_ERR_BAD_TREE
+    assert np.all(np.isnan(snap16.cpu().numpy()[2]))
+
+
+def test_tree_rounds_with_f16_commits(gpu_lib):
+    """Tree blocks verified with binary16 snapshots and committed through them
+    (accepted node of each block), against an oracle that rounds its own
+    accepted state the same way."""
+    t = torch()
+    Hk, Hv, dk, dv, N = 2, 6, 128, 128, 22
+    cache_t, ocache = None, None
+    for r in range(4):
+        inp = synthetic.make_verify_inputs(B=1, N=N, Hk=Hk, Hv=Hv, dk=dk, dv=dv, dtype="bf16",
+                                           alpha_kind="near_one", state_sigma=0.05,
+                                           seed=9500 + r, n_slots=1, slot_perm=False, tree=True)
+        if cache_t is None:
+            cache_t = dev(inp["cache"])
+            ocache = inp["cache"].astype(np.float64)
+        snap16 = t.empty((1, N, Hv, dk, dv), dtype=t.float16, device="cuda")
+        o = t.empty((1, N, Hv, dv), device="cuda")
+        gpu_lib.gdn_verify_tree_f16(dev(inp["q"]), dev(inp["k"]), dev(inp["v"]),
+                                    dev(inp["alpha"]), dev(inp["beta"]), cache_t, snap16, o,
+                                    dev(inp["parent"]), slot=dev(inp["slot"]), n_slots=1)
+        acc = int(inp["accept"][0])
+        gpu_lib.gdn_commit_accepted_f16(snap16, dev(np.array([acc], np.int32)), cache_t, B=1,
+                                        N=N, Hv=Hv, dk=dk, dv=dv, slot=dev(inp["slot"]),
+                                        n_slots=1)
+        st, osnap, _ = oracle.verify(inp["q_f64"], inp["k_f64"], inp["v_f64"], inp["alpha"],
+                                     inp["beta"], ocache, inp["slot"], inp["parent"], B=1, N=N,
+                                     Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+        assert st == oracle.OK
+        ocache = osnap[0, acc][None].astype(np.float16).astype(np.float64)
+    t.cuda.synchronize()
+    assert_close16(cache_t.cpu().numpy(), ocache, "state after 4 binary16 tree commits", ulps=2)
