@@ -402,6 +402,13 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
   __half* snap16_h = SNAP16 ? p.snap16 + lane_off : nullptr;
   float* o_h = p.o + ((int64_t)b * N * p.Hv + h) * dv + j0 + cg * 4;
 
+  // The shuffle tree of node n reduces the look-ahead sums for u_{n+1} (from
+  // the state before node n's update) together with the output sums of node
+  // n-1, so that it does not wait for node n's update: the update, its
+  // output partials and the snapshot stores overlap the tree's latency, and
+  // o_{n-1} is stored one node late (o_{N-1} after the loop).
+  float po[4] = {0.f, 0.f, 0.f, 0.f};  // output partials of the previous node
+  float iq_prev = 1.f;
   for (int n = 0; n < N; ++n) {
     const bool has_next = n + 1 < N;
     float knx[R];  // k of node n+1
@@ -430,8 +437,14 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
       w23 = __ffma2_rn(H[m][1], f2(knx[m]), w23);
       kk = fmaf(kn[m], knx[m], kk);
     }
+    // (e) one shuffle tree for those 4 + 1 sums and the previous node's 4
+    float red[9] = {w01.x, w01.y, w23.x, w23.y, kk, po[0], po[1], po[2], po[3]};
+#pragma unroll
+    for (int off = S::CG; off < 32; off <<= 1)
+#pragma unroll
+      for (int i = 0; i < 9; ++i) red[i] += __shfl_xor_sync(FULL, red[i], off);
 
-    // (d) delta_n, update, output partial
+    // (d) delta_n, update, output partial (independent of the tree above)
     float d[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) d[c] = be * (vj[c] - al * u[c]);
@@ -445,20 +458,7 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
       o01 = __ffma2_rn(H[m][0], f2(qr[m]), o01);
       o23 = __ffma2_rn(H[m][1], f2(qr[m]), o23);
     }
-
-    // (e) one shuffle tree for the 4 + 1 + 4 column sums
-    float red[9] = {w01.x, w01.y, w23.x, w23.y, kk, o01.x, o01.y, o23.x, o23.y};
-#pragma unroll
-    for (int off = S::CG; off < 32; off <<= 1)
-#pragma unroll
-      for (int i = 0; i < 9; ++i) red[i] += __shfl_xor_sync(FULL, red[i], off);
-    warps_sum<NW, S::CG>(red, sx, xc, wi, cg, rl);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) u[c] = fmaf(al, red[c] * ikx, d[c] * (red[4] * (ik * ikx)));
-
     // (f) persist (a chain verified for a replay commit keeps no snapshots)
-    if (rl == 0 && wi == 0)
-      st_f4(o_h + (int64_t)n * p.Hv * dv, red[5] * iq, red[6] * iq, red[7] * iq, red[8] * iq);
     if constexpr (SNAP16) {
       // binary16, round to nearest even: 8 bytes per lane and row
       __half* dst = snap16_h + (int64_t)n * node_stride;
@@ -476,9 +476,27 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
       for (int m = 0; m < R; ++m)
         st_f4(dst + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
     }
+    // cross-warp sums, u_{n+1}, and the previous node's output
+    warps_sum<NW, S::CG>(red, sx, xc, wi, cg, rl);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) u[c] = fmaf(al, red[c] * ikx, d[c] * (red[4] * (ik * ikx)));
+    if (n > 0 && rl == 0 && wi == 0)
+      st_f4(o_h + (int64_t)(n - 1) * p.Hv * dv, red[5] * iq_prev, red[6] * iq_prev,
+            red[7] * iq_prev, red[8] * iq_prev);
+    po[0] = o01.x; po[1] = o01.y; po[2] = o23.x; po[3] = o23.y;
+    iq_prev = iq;
 #pragma unroll
     for (int m = 0; m < R; ++m) kn[m] = knx[m];
   }
+  // the last node's output
+#pragma unroll
+  for (int off = S::CG; off < 32; off <<= 1)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) po[c] += __shfl_xor_sync(FULL, po[c], off);
+  warps_sum<NW, S::CG>(po, sx, xc, wi, cg, rl);
+  if (rl == 0 && wi == 0)
+    st_f4(o_h + (int64_t)(N - 1) * p.Hv * dv, po[0] * iq_prev, po[1] * iq_prev, po[2] * iq_prev,
+          po[3] * iq_prev);
 }
 
 // ------------------------------------------------------------------ tree
