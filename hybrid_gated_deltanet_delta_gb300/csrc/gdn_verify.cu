@@ -32,7 +32,8 @@
 //     u_{n+1} = H_n^T k_{n+1} = alpha_n (H_{n-1}^T k_{n+1}) + delta_n (k_n . k_{n+1}),
 // and both sums on the right come from the registers BEFORE node n's update.
 // Tree (tree_kernel, below): the block's warps take the nodes of each depth
-// level in turn.
+// level in turn; a warp reduces its previous node's output sums in the same
+// shuffle tree as its next node's u.
 // q, k, v and the gates are staged with cp.async while the cached state
 // loads.  Snapshots leave as 16-byte stores; a warp-wide store covers RL rows
 // x WC*4 contiguous bytes.
@@ -671,6 +672,12 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
   float* snap_h = p.snap + ((int64_t)b * N * p.Hv + h) * DK * dv + (int64_t)row0 * dv + j0 + cg * 4;
   float* o_h = p.o + ((int64_t)b * N * p.Hv + h) * dv + j0 + cg * 4;
 
+  // A warp's pending output: the output sums of the last node it formed are
+  // reduced in the shuffle tree of its next node's u (or after the walk), so
+  // that each node takes one tree, not two.
+  float po[4] = {0.f, 0.f, 0.f, 0.f};
+  int pn = -1;
+  float piq = 1.f;
   for (int L = 1; L <= N && slev[L] < N; ++L) {
     for (int i = slev[L] + w; i < slev[L + 1]; i += TW) {
       const int n = sord[i], par = spar[n];
@@ -702,8 +709,8 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
       const float ik = PREP ? sinvk[n] : 1.f;
       const float iq = PREP ? sinvq[n] : 1.f;
 
-      // u_n = H_par^T k_n
-      float u[4];
+      // u_n = H_par^T k_n, reduced together with the pending output sums
+      float red[8];
       {
         float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -711,16 +718,20 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
           a01 = __ffma2_rn(H[m][0], f2(kn[m]), a01);
           a23 = __ffma2_rn(H[m][1], f2(kn[m]), a23);
         }
-        u[0] = a01.x; u[1] = a01.y; u[2] = a23.x; u[3] = a23.y;
+        red[0] = a01.x; red[1] = a01.y; red[2] = a23.x; red[3] = a23.y;
+        red[4] = po[0]; red[5] = po[1]; red[6] = po[2]; red[7] = po[3];
 #pragma unroll
         for (int off = S::CG; off < 32; off <<= 1)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) u[c] += __shfl_xor_sync(FULL, u[c], off);
+          for (int c = 0; c < 8; ++c) red[c] += __shfl_xor_sync(FULL, red[c], off);
       }
-      // delta_n, update, o_n
+      if (pn >= 0 && rl == 0)
+        st_f4(o_h + (int64_t)pn * p.Hv * dv, red[4] * piq, red[5] * piq, red[6] * piq,
+              red[7] * piq);
+      // delta_n, update, o_n partials
       float d[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) d[c] = be * (vj[c] - al * (u[c] * ik));
+      for (int c = 0; c < 4; ++c) d[c] = be * (vj[c] - al * (red[c] * ik));
       const float2 d01 = make_float2(d[0] * ik, d[1] * ik), d23 = make_float2(d[2] * ik, d[3] * ik);
       const float2 al2 = f2(al);
       float2 o01 = make_float2(0.f, 0.f), o23 = make_float2(0.f, 0.f);
@@ -743,15 +754,20 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
           *reinterpret_cast<float4*>(to + m * 128) =
               make_float4(H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
       }
-      float o[4] = {o01.x, o01.y, o23.x, o23.y};
-#pragma unroll
-      for (int off = S::CG; off < 32; off <<= 1)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) o[c] += __shfl_xor_sync(FULL, o[c], off);
-      if (rl == 0) st_f4(o_h + (int64_t)n * p.Hv * dv, o[0] * iq, o[1] * iq, o[2] * iq, o[3] * iq);
+      po[0] = o01.x; po[1] = o01.y; po[2] = o23.x; po[3] = o23.y;
+      pn = n;
+      piq = iq;
       held = n;
     }
     __syncthreads();  // this level's snapshots are visible to the next level
+  }
+  if (pn >= 0) {  // the last node this warp formed
+#pragma unroll
+    for (int off = S::CG; off < 32; off <<= 1)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) po[c] += __shfl_xor_sync(FULL, po[c], off);
+    if (rl == 0)
+      st_f4(o_h + (int64_t)pn * p.Hv * dv, po[0] * piq, po[1] * piq, po[2] * piq, po[3] * piq);
   }
 
   // node depths (root = 1), written once per sequence
