@@ -190,7 +190,9 @@ def roofline_entry(bound, kernel, work_per_launch, launch_ms, peak, peak_kind, t
             "peak_source": (f"{peak_kind} (MEASURED_PEAKS.json "
                             f"{'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})"
                             if peak_kind == "measured" else f"fallback {peak} {unit}"),
-            work_key: work_per_launch, "launch_ms": launch_ms, "traffic": traffic}
+            work_key: work_per_launch, "launch_ms": launch_ms, "traffic": traffic,
+            "traffic_over_algorithmic": (traffic / work_per_launch
+                                         if traffic is not None and bound == "hbm" else None)}
 
 
 # --------------------------------------------------------------------- clocks
