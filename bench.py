@@ -658,6 +658,39 @@ def measure_verify(ctx, wl_name):
                 cache_layer_stride=B * Hv * dk * dv, slot=ws.slot, n_slots=B, stream=stream)]
         ws.verify_c = [c.verify_c for c in ws.layers]
 
+    def bind_calls(ws, on_stream):
+        """The set's step (verifies, then commit) as bound calls on another stream."""
+        out = []
+        for c in ws.layers:
+            d = c.dev
+            common = (d["q"], d["k"], d["v"], d["alpha"], d["beta"], c.cache)
+            kw = dict(slot=c.slot, n_slots=c.inp["n_slots"], stream=on_stream)
+            if c.snap16 and c.parent is not None:
+                out.append(gdn.bind_verify_tree(*common, None, c.o, c.parent,
+                                                snapshots_f16=c.snap, **kw))
+            elif c.snap16:
+                out.append(gdn.bind_verify_chain(*common, None, c.o, snapshots_f16=c.snap, **kw))
+            elif c.parent is not None:
+                out.append(gdn.bind_verify_tree(*common, c.snap, c.o, c.parent, **kw))
+            else:
+                out.append(gdn.bind_verify_chain(*common, c.snap, c.o, **kw))
+        if index:
+            out.append(lambda: gdn.gdn_commit_index(ws.accept, ws.slot_idx, N=N,
+                                                    stream=on_stream))
+        elif replay:
+            for c in ws.layers:
+                d = c.dev
+                out.append(gdn.bind_replay_accepted(d["k"], d["v"], d["alpha"], d["beta"],
+                                                    c.cache, d["accept"], parent=c.parent,
+                                                    slot=c.slot, n_slots=c.inp["n_slots"],
+                                                    stream=on_stream))
+        else:
+            out.append(gdn.bind_commit_accepted(
+                ws.snap_all, ws.accept, ws.cache_all, B=B, N=N, Hv=Hv, dk=dk, dv=dv,
+                n_layers=len(ws.layers), snap_layer_stride=B * N * Hv * dk * dv,
+                cache_layer_stride=B * Hv * dk * dv, slot=ws.slot, n_slots=B, stream=on_stream))
+        return out
+
     def step_c(ws, ev=None):
         """One step through the bound calls; ev = (start, after verify, end)."""
         if ev is not None:
@@ -758,31 +791,62 @@ def measure_verify(ctx, wl_name):
     t1 = time.time()
     total_ms = max_over_ranks(total_ms, world)
 
-    # end to end through the bound calls: every step copies its inputs from
-    # pinned host memory and its outputs back; the whole run is enqueued
-    # asynchronously and timed on the host clock around it
+    # end to end through the package's calls: every step copies its inputs
+    # from pinned host memory, runs the bound verify and commit calls and
+    # copies its outputs back.  Each set's step (copies and launches) is
+    # captured once into a CUDA graph, as a serving loop would, and the
+    # graphs are replayed back to back; host clock around the run.
     for ws in sets:
         if ws.cache_init is not None:
             ws.cache_all.copy_(ws.cache_init)
     e2e_steps = max(K, 50 if batched else 400)
-    h2d = d2h = 0
-    for i in range(3):   # warm the copy paths
-        ws = sets[i % n_sets]
-        for c in ws.layers:
-            c.h2d()
-        step_c(ws)
-        for c in ws.layers:
-            c.d2h()
+    cap_stream, side = torch.cuda.Stream(), torch.cuda.Stream()
+    graphs = []
+    h2d = sum(c.host.numel() for c in sets[0].layers)
+    d2h = sum(c.o.numel() * 4 for c in sets[0].layers)
+    pipelined = n_sets >= 2
+    for j, ws in enumerate(sets):
+        calls = bind_calls(ws, cap_stream)
+        g = torch.cuda.CUDAGraph()
+        cap_stream.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap_stream, capture_error_mode="thread_local"):
+            if pipelined:
+                # this step's launches, and beside them the previous step's
+                # outputs out and the next step's inputs in
+                side.wait_stream(cap_stream)
+                with torch.cuda.stream(side):
+                    for c in sets[(j - 1) % n_sets].layers:
+                        c.d2h()
+                    for c in sets[(j + 1) % n_sets].layers:
+                        c.h2d()
+                for f in calls:
+                    f()
+                cap_stream.wait_stream(side)
+            else:
+                for c in ws.layers:
+                    c.h2d()
+                for f in calls:
+                    f()
+                for c in ws.layers:
+                    c.d2h()
+        graphs.append(g)
+    torch.cuda.synchronize()
+    for i in range(3):   # warm the graphs
+        graphs[i % n_sets].replay()
     torch.cuda.synchronize()
     barrier(world)
     ta = time.perf_counter()
+    if pipelined:
+        for c in sets[0].layers:   # the first step's inputs
+            c.h2d()
     for i in range(e2e_steps):
-        ws = sets[i % n_sets]
-        h2d = sum(c.h2d() for c in ws.layers)
-        step_c(ws)
-        d2h = sum(c.d2h() for c in ws.layers)
+        graphs[i % n_sets].replay()
+    if pipelined:
+        for c in sets[(e2e_steps - 1) % n_sets].layers:   # the last step's outputs
+            c.d2h()
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - ta, world)
+    del graphs
 
     node_heads = B * N * Hv * len(layers)
     hbm, _, peak_kind = ctx.peaks
@@ -821,9 +885,11 @@ def measure_verify(ctx, wl_name):
                                    "algorithmic_bytes_per_launch"),
         "e2e": {"value": world * node_heads * e2e_steps / e2e_s, "unit": "node-heads/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "how": "bound calls; per step the packed inputs copied from pinned host memory "
-                       "and the outputs o copied back, all enqueued on the stream, host clock "
-                       "around the run"},
+                "how": "per step the packed inputs copied from pinned host memory, the bound "
+                       "verify and commit calls, and the outputs o copied back; captured once "
+                       "per set into a CUDA graph (with several sets, a step's graph copies the "
+                       "previous step's outputs out and the next step's inputs in beside its "
+                       "own launches) and replayed back to back; host clock around the run"},
         "gpu_launches": launches_per_step * K,
         "clocks": ctx.sampler.summary(t0, t1),
     }
@@ -885,28 +951,65 @@ def measure_prefill(ctx, wl_name="prefill8192"):
     total_ms = max_over_ranks(sum(ms[:K]), world)
     call_stats = stats_ms(ms, "one event pair per call (prep + scan kernels), 256 MiB flush "
                               "before each call not timed")
-    # end to end: host inputs (pinned) -> device -> prefill -> host o and state,
-    # enqueued on the stream for every step, host clock around the run
+    # end to end: host inputs (pinned) -> device -> prefill -> host o and state
+    # for every step, each buffer set's step captured once into a CUDA graph
+    # and the graphs (two sets) replayed back to back; host clock around the
+    # run
     hq, hk, hv, ha, hb = (x.cpu().pin_memory() for x in (q, k, v, alpha, beta))
     hs0 = state0.cpu().pin_memory()
     ho = torch.empty(o.shape).pin_memory()
     hst = torch.empty(state.shape).pin_memory()
-    pairs = ((q, hq), (k, hk), (v, hv), (alpha, ha), (beta, hb), (state, hs0))
+    bufs = []
+    for j in range(2):
+        if j == 0:
+            dq, dk_, dv_, da, db, ds, do_, dws, dstat = q, k, v, alpha, beta, state, o, ws, status
+        else:
+            dq, dk_, dv_, da, db = (torch.empty_like(x) for x in (q, k, v, alpha, beta))
+            ds, do_ = torch.empty_like(state), torch.empty_like(o)
+            dws, dstat = torch.empty_like(ws), torch.zeros_like(status)
+        bufs.append(dict(
+            pairs=((dq, hq), (dk_, hk), (dv_, hv), (da, ha), (db, hb), (ds, hs0)), o=do_, state=ds,
+            ws=dws, status=dstat))
+    pairs = bufs[0]["pairs"]
 
-    def e2e_step():
-        for d, h in pairs:
+    cap_stream, side = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def h2d_set(bset):
+        for d, h in bset["pairs"]:
             d.copy_(h, non_blocking=True)
-        call()
-        ho.copy_(o, non_blocking=True)
-        hst.copy_(state, non_blocking=True)
 
+    def d2h_set(bset):
+        ho.copy_(bset["o"], non_blocking=True)
+        hst.copy_(bset["state"], non_blocking=True)
+
+    for j, bset in enumerate(bufs):
+        # this step's prefill, and beside it the other set's outputs out and
+        # next inputs in
+        dq, dk_, dv_, da, db, ds = (d for d, _ in bset["pairs"])
+        call_cap = gdn.bind_prefill_chunked(dq, dk_, dv_, da, db, ds, bset["o"], bset["ws"],
+                                            status=bset["status"], stream=cap_stream)
+        other = bufs[1 - j]
+        g = torch.cuda.CUDAGraph()
+        cap_stream.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap_stream, capture_error_mode="thread_local"):
+            side.wait_stream(cap_stream)
+            with torch.cuda.stream(side):
+                d2h_set(other)
+                h2d_set(other)
+            call_cap()
+            cap_stream.wait_stream(side)
+        bset["graph"] = g
+    torch.cuda.synchronize()
     e2e_steps = max(min(K, 40), 10)
-    e2e_step()
+    for i in range(2):
+        bufs[i]["graph"].replay()
     torch.cuda.synchronize()
     barrier(world)
     ta = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+    h2d_set(bufs[0])   # the first step's inputs
+    for i in range(e2e_steps):
+        bufs[i % 2]["graph"].replay()
+    d2h_set(bufs[(e2e_steps - 1) % 2])   # the last step's outputs
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - ta, world)
     h2d = sum(h.numel() * h.element_size() for _, h in pairs)
@@ -937,13 +1040,15 @@ def measure_prefill(ctx, wl_name="prefill8192"):
                                    "algorithmic_flops_per_launch"),
         "e2e": {"value": world * T * Hv * e2e_steps / e2e_s, "unit": "token-heads/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "how": "bound call; per step q, k, v, gates and the initial state copied from "
-                       "pinned host memory, o and the final state copied back, all enqueued "
-                       "on the stream, host clock around the run"},
+                "how": "per step q, k, v, gates and the initial state copied from pinned host "
+                       "memory, the bound prefill call, o and the final state copied back; "
+                       "two buffer sets, each step's graph copying the other set's outputs out "
+                       "and next inputs in beside its own prefill; graphs replayed back to "
+                       "back; host clock around the run"},
         "gpu_launches": 2 * K,   # prep + scan per call
         "clocks": ctx.sampler.summary(t0, t1),
     }
-    del ws, o, q, k, v
+    del ws, o, q, k, v, bufs
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return out
