@@ -11,6 +11,8 @@ A step is one pass of the hot path over one batch of synthetic input:
   batched8x16  8 sequences x 16-position chains over 48 layers:
                48 x gdn_verify_chain + one gdn_commit_accepted over the 48 layers
   prefill8192  one 8192-token sequence, chunk 64: gdn_prefill_chunked
+  batched8x22  8 sequences x 22-node draft trees over 48 layers:
+               48 x gdn_verify_tree + one gdn_commit_accepted over the 48 layers
   (and variants: *_replay, *_index, *_f16; see WORKLOADS)
 
 With no --workload the run prints ONE JSON line: the headline is chain16
@@ -18,7 +20,9 @@ With no --workload the run prints ONE JSON line: the headline is chain16
 its measurement plan name -- tree22 ("tree 22"), batched8x16 and
 prefill8192 -- are measured in the same run and nested under "workloads",
 each with its step time and percentiles, its own roofline and its end-to-end
-figure.  --workload NAME measures that one workload alone (for profiling).
+figure, together with the tree variants (binary16 snapshots, checkpoint and
+replay, the batched tree).  A workload committed by a copy also reports the
+commit kernel's own time and roofline.  --workload NAME measures that one workload alone (for profiling).
 
 Metric: node-heads/s (B x N x Hv per layer call, summed over the step; for
 the prefill, token-heads/s).  No step finds its data in L2 (129 MB): the
@@ -32,8 +36,9 @@ replica (independent sequences, no collective on the data path): weak scaling.
 
 The end-to-end figure goes through the package's public API (bound calls,
 one ctypes call per launch): every step copies its inputs from pinned host
-memory to the device and its outputs back, all enqueued on the stream, timed
-on the host clock around the whole run.
+memory to the device and its outputs back; each buffer set's step is
+captured once into a CUDA graph and the graphs are replayed back to back,
+timed on the host clock around the whole run.
 
 --impl reference times the CPU oracle (plain float64 C++, the reference for
 every parity test) on this host's cores, on a bounded sample of the same
@@ -74,7 +79,8 @@ KERNEL_BLOCK = 100
 
 METRIC = "GDN verify node-heads/s per layer at block 16 / tree 22; % of GB300 HBM roofline"
 HEADLINE = "chain16"
-NESTED = ("tree22", "batched8x16", "prefill8192", "tree22_f16", "tree22_replay")
+NESTED = ("tree22", "batched8x16", "prefill8192", "tree22_f16", "tree22_replay", "batched8x22",
+          "batched8x22_replay")
 
 
 def hold_device(torch, host_s_per_step, steps):
@@ -102,8 +108,10 @@ def verify_bytes(B, N, Hk, Hv, dk, dv, in_bytes=2, tree=False, persist=True, sna
     return state_in + snap + qk + v + gates + o + extra
 
 
-def commit_bytes(B, Hv, dk, dv, n_layers=1):
-    return 2 * B * Hv * dk * dv * 4 * n_layers
+def commit_bytes(B, Hv, dk, dv, n_layers=1, snap_bytes=4):
+    """Algorithmic HBM bytes of one copy commit: the accepted snapshot of every
+    (layer, sequence, head) read once and the cached state written once."""
+    return B * Hv * dk * dv * (snap_bytes + 4) * n_layers
 
 
 def prefill_bytes(T, Hk, Hv, dk, dv, in_bytes=2):
@@ -134,6 +142,14 @@ WORKLOADS = {
     "batched8x16": dict(B=8, N=16, tree=False, layers=48,
                         desc="8 sequences x 16-position chains, same heads, 48 GDN layers with "
                              "fresh inputs per layer; 48 verifies + one 48-layer commit"),
+    "batched8x22": dict(B=8, N=22, tree=True, layers=48,
+                        desc="8 sequences x 22-node DDTrees (the same trees in every layer), "
+                             "same heads, 48 GDN layers with fresh inputs per layer; 48 tree "
+                             "verifies + one 48-layer commit"),
+    "batched8x22_replay": dict(B=8, N=22, tree=True, layers=48, replay=True,
+                               desc="batched8x22 committed by checkpoint and replay: 48 tree "
+                                    "verifies without snapshots (per-block solve), 48 replays "
+                                    "of the accepted nodes' ancestor paths"),
     "chain16_replay": dict(B=1, N=16, tree=False, layers=1, replay=True,
                            desc="chain16 committed by checkpoint and replay: verify without "
                                 "snapshots, then the accepted prefix re-run from the cached "
@@ -279,6 +295,8 @@ def source_sha(files):
 KERNEL_SOURCES = {
     "verify": ["hybrid_gated_deltanet_delta_gb300/csrc/gdn_verify.cu",
                "hybrid_gated_deltanet_delta_gb300/csrc/gdn_common.cuh"],
+    "commit": ["hybrid_gated_deltanet_delta_gb300/csrc/gdn_commit.cu",
+               "hybrid_gated_deltanet_delta_gb300/csrc/gdn_common.cuh"],
     "prefill": ["hybrid_gated_deltanet_delta_gb300/csrc/gdn_prefill.cu",
                 "hybrid_gated_deltanet_delta_gb300/csrc/gdn_common.cuh",
                 "hybrid_gated_deltanet_delta_gb300/csrc/gdn_tc.cuh"],
@@ -342,6 +360,8 @@ class OracleSampler:
             self.inp = synthetic.chain16()
         elif wl_name.startswith("tree22"):
             self.inp = synthetic.tree22()
+        elif wl_name.startswith("batched8x22"):
+            self.inp = synthetic.batched8x22_layer(0)
         else:
             self.inp = synthetic.batched8x16_layer(0)
 
@@ -451,32 +471,33 @@ class VerifyCase:
     buffer so that the end-to-end leg moves them with a single copy from one
     pinned host buffer."""
 
-    NAMES = ("q", "k", "v", "alpha", "beta", "accept")
+    NAMES = ("q", "k", "v", "alpha", "beta", "accept")   # and a tree's parent array
 
     def __init__(self, inp, torch, pinned=False, persist=True, snap16=False):
         self.inp = inp
         self.snap16 = snap16
         self.B, self.N, self.Hv = inp["B"], inp["N"], inp["Hv"]
         dk, dv = inp["dk"], inp["dv"]
-        arrays = {n: np.ascontiguousarray(inp[n]) for n in self.NAMES}
+        names = self.NAMES + (("parent",) if inp["tree"] else ())
+        arrays = {n: np.ascontiguousarray(inp[n]) for n in names}
         offs, total = {}, 0
-        for n in self.NAMES:
+        for n in names:
             offs[n] = total
             total += (arrays[n].nbytes + 255) // 256 * 256
         host = np.zeros(total, np.uint8)
-        for n in self.NAMES:
+        for n in names:
             host[offs[n]:offs[n] + arrays[n].nbytes] = arrays[n].view(np.uint8).ravel()
         self.packed = torch.from_numpy(host).cuda()
         tdt = {np.dtype(np.uint16): torch.bfloat16, np.dtype(np.float32): torch.float32,
                np.dtype(np.int32): torch.int32}
         self.dev = {}
-        for n in self.NAMES:
+        for n in names:
             a = arrays[n]
             seg = self.packed[offs[n]:offs[n] + a.nbytes]
             self.dev[n] = seg.view(tdt[a.dtype]).view(*a.shape)
         self.cache = _dev(inp["cache"], torch)
         self.slot = _dev(inp["slot"], torch)
-        self.parent = _dev(inp["parent"], torch) if inp["tree"] else None
+        self.parent = self.dev["parent"] if inp["tree"] else None
         self.snap = (torch.empty((self.B, self.N, self.Hv, dk, dv), device="cuda",
                                  dtype=torch.float16 if snap16 else torch.float32)
                      if persist else None)
@@ -578,7 +599,7 @@ def measure_verify(ctx, wl_name):
     index = wl.get("index", False)
     snap16 = wl.get("snap16", False)
     tree = wl.get("tree", False)
-    batched = wl_name.startswith("batched8x16")
+    batched = wl_name.startswith("batched")
     L = args.layers if (args.layers and batched) else wl["layers"]
     vbytes = verify_bytes(B, N, Hk, Hv, dk, dv, tree=tree, persist=not replay,
                           snap_bytes=2 if snap16 else 4)
@@ -596,7 +617,8 @@ def measure_verify(ctx, wl_name):
         """Buffers of one copy of the workload and its step (verify, commit)."""
         ws = argparse.Namespace()
         if batched:
-            ws.layers = [VerifyCase(synthetic.batched8x16_layer(l), torch, pinned=True,
+            layer_inputs = synthetic.batched8x22_layer if tree else synthetic.batched8x16_layer
+            ws.layers = [VerifyCase(layer_inputs(l), torch, pinned=True,
                                     persist=not replay, snap16=snap16) for l in range(L)]
             # one cache for all layers: [layer][slot][Hv][dk][dv]; snapshots likewise
             ws.cache_all = torch.stack([c.cache for c in ws.layers])
@@ -740,6 +762,8 @@ def measure_verify(ctx, wl_name):
         torch.cuda.synchronize()
         step_list = [e[0].elapsed_time(e[2]) for e in evs]
         kernel_list = [e[0].elapsed_time(e[1]) / len(layers) for e in evs]
+        commit_stats = stats_ms([e[1].elapsed_time(e[2]) for e in evs],
+                                "commit phase of each timed step")
         total_ms = sum(step_list)
         step_stats = stats_ms(step_list, "one event pair per step (flush before each step "
                                          "not timed)")
@@ -786,6 +810,21 @@ def measure_verify(ctx, wl_name):
             per_launch.append(e[0].elapsed_time(e[1]) / (KERNEL_BLOCK * len(layers)))
         kernel_stats = stats_ms(per_launch, f"{STAT_BLOCKS} blocks of {KERNEL_BLOCK} "
                                             "back-to-back verify launches over the rotating "
+                                            "copies, one event pair per block")
+        # the commit on its own, likewise
+        per_commit = []
+        for r in range(STAT_BLOCKS):
+            hold_device(torch, host_s / 2, KERNEL_BLOCK)
+            e = ctx.events(2)
+            e[0].record(stream)
+            for i in range(KERNEL_BLOCK):
+                for f in sets[(r * KERNEL_BLOCK + i) % n_sets].commit_c:
+                    f()
+            e[1].record(stream)
+            torch.cuda.synchronize()
+            per_commit.append(e[0].elapsed_time(e[1]) / KERNEL_BLOCK)
+        commit_stats = stats_ms(per_commit, f"{STAT_BLOCKS} blocks of {KERNEL_BLOCK} "
+                                            "back-to-back commit calls over the rotating "
                                             "copies, one event pair per block")
     barrier(world)
     t1 = time.time()
@@ -893,6 +932,15 @@ def measure_verify(ctx, wl_name):
         "gpu_launches": launches_per_step * K,
         "clocks": ctx.sampler.summary(t0, t1),
     }
+    if not (index or replay):
+        # the copy commit's own kernel (replay and index commits are other work)
+        cbytes = commit_bytes(B, Hv, dk, dv, len(layers), snap_bytes=2 if snap16 else 4)
+        out["commit"] = {
+            "kernel_ms": commit_stats,
+            "roofline": roofline_entry("hbm", "gdn_commit_accepted" + ("_f16" if snap16 else ""),
+                                       cbytes, commit_stats["p50"], hbm, peak_kind,
+                                       profiled_traffic("commit", wl_name),
+                                       "algorithmic_bytes_per_launch")}
     del sets
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

@@ -21,7 +21,7 @@ int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
 // and snapshot-free trees (a->snapshots may be NULL), which never read a
 // persisted state back.
 int launch_verify_tree_solve(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out,
-                             int wc, int nw, cudaStream_t stream, void* snap16, bool prep);
+                             int wc, cudaStream_t stream, void* snap16, bool prep);
 
 // Replay of the accepted path from the cached state, written back in place.
 int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept, int wc,

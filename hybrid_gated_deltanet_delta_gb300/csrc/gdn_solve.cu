@@ -29,30 +29,34 @@
 //                          X[n]    = beta_n (v_n - g_n H0^T k_n),
 // and the outputs
 //     o_n = g_n H0^T q_n + sum_{m in path(n)} r(n, m) (q_n . k_m) delta_m.
-// The decay products are taken from the log decay along the path,
-// r(n, m) = e^(L_n - L_m) with L_n the sum of log alpha over path(n).  A block
-// is verified in three phases, none of which walks the nodes through a
-// reduction:
-//   1. K K^T and Q K^T on tensor cores (mma.sync; exact for bf16 inputs), r,
-//      A and P = r (Q K^T) under the ancestor mask, and the depth-first order
-//      of the tree; none of it needs the cached state, so it overlaps that
-//      state's load;
-//   2. K H0 and Q H0 on tensor cores (the fp32 state split into bf16 hi + lo),
-//      X, Delta by forward substitution (one column per lane, 16 rows at a
-//      time in registers) and the outputs O = diag(g) Q H0 + P Delta;
-//   3. the states, column slab by column slab in registers, in depth-first
-//      order: H_n = alpha_n H_parent + k_n delta_n^T when the parent's state
-//      is the one just formed, otherwise g_n H0 plus the path's terms; each
-//      state leaves as 16-byte vector stores (fp32 or binary16) while the next
-//      is formed.
+// With T = (I + A)^-1 and P[n][m] = r(n, m) (q_n . k_m) on the path,
+//     Delta = T X,   O = diag(g) Q H0 + (P T) X,
+// and T, P T depend on the block's inputs only, not on the cached state.  T
+// inherits the ancestor mask (T[n][m] = 0 unless m is on n's path), and a row
+// of T needs only the rows of the node's ancestors, so it is formed depth
+// level by depth level.  The decay products come from the log decay along
+// the path, r(n, m) = e^(L_n - L_m) with L_n the sum of log alpha over
+// path(n).  A block is verified in three phases:
+//   1. while the cached state's slab loads: K K^T and Q K^T on tensor cores
+//      (mma.sync; exact for bf16 inputs), r, A and P under the ancestor mask,
+//      T by depth levels, P T, and the depth-first order of the tree;
+//   2. once it has landed: K H0 and Q H0 on tensor cores (the fp32 state
+//      split into bf16 hi + lo) with X formed in the epilogue, then Delta and
+//      the outputs in one pass, every entry on its own (a sum over the node's
+//      path);
+//   3. only when states are persisted: the states, in registers, in
+//      depth-first order: H_n = alpha_n H_parent + k_n delta_n^T when the
+//      parent's state is the one just formed, otherwise g_n H0 plus the
+//      path's terms; each state leaves as 16-byte vector stores (fp32) or
+//      8-byte stores (binary16) while the next is formed.
 //
 // Work decomposition
 // ------------------
-// A thread block owns a slab of WC columns of one (sequence, value head):
-// grid = (dv / WC, Hv, B).  In phase 3, lane = cg + CG*rl of warp wi keeps R
-// consecutive rows (row0 = wi*DK/NW + rl*R) x 4 columns (cg) of the state as
-// float2 pairs.  Phases 1-2 use all warps of the block on small matrices in
-// shared memory.
+// A thread block of four warps owns a slab of WC columns of one (sequence,
+// value head): grid = (dv / WC, Hv, B).  Phases 1 and 2 spread over all
+// threads.  In phase 3, lane = cg + CG*rl of row warp wi keeps R consecutive
+// rows (row0 = wi*DK/NW + rl*R) x 4 columns (cg) of the state as float2
+// pairs.
 //
 // Variants (template flags): SNAP16 persists binary16 snapshots (rounded to
 // nearest even from the fp32 states); PREP takes raw q/k projections and gate
@@ -68,13 +72,18 @@
 namespace gdn {
 namespace {
 
-template <int DK, int WC, int NW>
+constexpr int kWarps = 4;
+constexpr int NT = 32 * kWarps;
+
+// Phase 3 lane layout: NW row warps (at most the block's four).
+template <int DK, int WC>
 struct Shape {
-  static constexpr int CG = WC / 4;        // 16-byte column groups per row of the slab
-  static constexpr int RL = 32 / CG;       // row lanes per warp
-  static constexpr int R = DK / (RL * NW); // rows per lane (NW warps split the rows)
+  static constexpr int CG = WC / 4;                     // 16-byte column groups per slab row
+  static constexpr int RL = 32 / CG;                    // row lanes per warp
+  static constexpr int NW = DK / RL < kWarps ? DK / RL : kWarps;
+  static constexpr int R = DK / (RL * NW);              // rows per lane
   static_assert(WC % 4 == 0 && 32 % CG == 0 && RL >= 2, "slab width");
-  static_assert(R >= 1 && R * RL * NW == DK, "row split");
+  static_assert(NW >= 1 && R >= 1 && R * RL * NW == DK, "row split");
 };
 
 __host__ __device__ constexpr int round16(int x) { return (x + 15) & ~15; }
@@ -82,28 +91,28 @@ __host__ __device__ constexpr int round16(int x) { return (x + 15) & ~15; }
 // Shared-memory plan in bytes (every array on a 16-byte boundary).  NP = N
 // rounded up to the 16 rows of a tensor-core tile.
 //   ks, qs   [NP][lds]  bf16  k and q rows (with SPLIT a lo plane follows)
-//   kf       [N][DK]    fp32  k rows (scaled by 1/|k| for PREP); with SPLIT
-//                             the fp32 k rows are staged here, and the fp32 q
-//                             rows over kk.. (dead until K K^T is formed)
+//   kf       [N][DK]    fp32  k rows for phase 3 (scaled by 1/|k| for PREP);
+//                             with SPLIT the fp32 k rows are staged here, and
+//                             the fp32 q rows over kk.. (dead until K K^T)
 //   h0       [DK][ldh]  fp32  the cached state's slab
 //   v        [N][WC]    input the v slab
-//   a, b, g  [N]        fp32  alpha, beta, g_n = r(n, -1)
-//   L        [N]        fp32  log decay along the path, r(n, m) = e^(L_n - L_m)
-//   ord      [N]        int   the order phase 3 forms the states in (a tree:
-//                             depth first, so most nodes follow their parent)
+//   a, b, la [N]        fp32  alpha, beta, log alpha
+//   g, L     [N]        fp32  g_n = e^(L_n), L_n = log decay along path(n)
 //   iq, ik   [NP]       fp32  1/|q_n|, 1/|k_n| (PREP; zero past N)
-//   par, dep [N]        int   parent (chain: n - 1), depth (root = 1)
+//   par, dep, ord [N]   int   parent, depth (root = 1), depth-first order
 //   anc      [N]        u64   strict ancestors as a bit set
-//   kk, qk, rr [NP][ldm] fp32  K K^T -> A, Q K^T -> P, r(n, m)
-//   u, qh, d [NP][WC]   fp32  K H0 -> X, Q H0, Delta
+//   kk       [NP][ldm]  fp32  K K^T -> A -> P T
+//   qk       [NP][ldm]  fp32  Q K^T -> P
+//   rr, tt   [NP][ldm]  fp32  r(n, m); T = (I + A)^-1
+//   x, qh, d [NP][WC]   fp32  X, Q H0, Delta
 struct Plan {
-  int ks, qs, kf, h0, v, a, b, g, L, ord, iq, ik, par, dep, anc, kk, qk, rr, u, qh, d, total;
-  int NP, lds, ldh, ldm;
+  int ks, qs, kf, h0, v, a, b, la, g, L, iq, ik, par, dep, ord, anc, kk, qk, rr, tt, x, qh, d;
+  int total, NP, lds, ldh, ldm;
 };
 
-__host__ __device__ inline Plan make_plan(int N, int DK, int WC, bool split, bool has_q) {
+__host__ __device__ inline Plan make_plan(int N, int DK, int WC, bool split) {
   Plan s{};
-  s.NP = (N + 15) & ~15;
+  s.NP = round16(N);
   s.lds = DK + 8;
   s.ldh = WC + 4;
   s.ldm = s.NP + 4;
@@ -111,30 +120,32 @@ __host__ __device__ inline Plan make_plan(int N, int DK, int WC, bool split, boo
   const int planes = split ? 2 : 1;
   int o = 0;
   s.ks = o; o += round16(planes * s.NP * s.lds * 2);
-  s.qs = o; o += has_q ? round16(planes * s.NP * s.lds * 2) : 0;
+  s.qs = o; o += round16(planes * s.NP * s.lds * 2);
   s.kf = o; o += round16(N * DK * 4);
   s.h0 = o; o += round16(DK * s.ldh * 4);
   s.v = o; o += round16(N * WC * esz);
   s.a = o; o += round16(N * 4);
   s.b = o; o += round16(N * 4);
+  s.la = o; o += round16(N * 4);
   s.g = o; o += round16(N * 4);
   s.L = o; o += round16(N * 4);
-  s.ord = o; o += round16(N * 4);
   s.iq = o; o += round16(s.NP * 4);
   s.ik = o; o += round16(s.NP * 4);
   s.par = o; o += round16(N * 4);
   s.dep = o; o += round16(N * 4);
+  s.ord = o; o += round16(N * 4);
   s.anc = o; o += round16(N * 8);
   const int mat = round16(s.NP * s.ldm * 4);
   s.kk = o; o += mat;
-  s.qk = o; o += has_q ? mat : 0;
+  s.qk = o; o += mat;
   s.rr = o; o += mat;
+  s.tt = o; o += mat;
   const int slab = round16(s.NP * WC * 4);
-  s.u = o; o += slab;
-  s.qh = o; o += has_q ? slab : 0;
+  s.x = o; o += slab;
+  s.qh = o; o += slab;
   s.d = o; o += slab;
   s.total = o;
-  if (split && has_q && s.total < s.kk + N * DK * 4) s.total = s.kk + round16(N * DK * 4);
+  if (split && s.total < s.kk + N * DK * 4) s.total = s.kk + round16(N * DK * 4);
   return s;
 }
 
@@ -150,32 +161,17 @@ struct VerifyParams {
   __half* snap16;  // binary16 snapshots instead of snap
   float* o;
   int32_t* status;
-  const int32_t* parent;  // tree verify only
+  const int32_t* parent;
   int32_t* depth_out;
   int64_t cache_slot_stride;
   int n_slots, N, Hk, Hv, dv, bf16;
   int hint;       // issue the pre-wait L2 hints
-  int max_depth;  // tree: deepest node allowed (root = 1), 0 = no cap
+  int max_depth;  // deepest node allowed (root = 1), 0 = no cap
 };
 
-struct ReplayParams {
-  const void* k;
-  const void* v;
-  const float* alpha;
-  const float* beta;
-  float* cache;
-  const int32_t* slot;
-  const int32_t* parent;
-  const int32_t* accept;
-  int32_t* status;
-  int64_t cache_slot_stride;
-  int n_slots, N, Hk, Hv, dv, bf16;
-};
-
-// Launches of up to this many blocks (4 per SM on 152 SMs, one wave) issue
-// the pre-wait L2 hints.  A larger launch runs in several waves behind a
-// stream of snapshot writes that evicts the hinted lines before they are
-// used.
+// Launches of up to this many blocks (four per SM on 152 SMs) issue the
+// pre-wait L2 hints.  A larger launch runs in several waves behind a stream
+// of snapshot writes that evicts the hinted lines before they are used.
 constexpr int kHintBlocks = 608;
 
 __device__ __forceinline__ void prefetch_l2(const void* a) {
@@ -190,20 +186,20 @@ __device__ __forceinline__ void prefetch_l2(const void* a) {
 // memory, and every load that feeds a result is issued after the wait.
 template <int DK>
 __device__ __forceinline__ void prefetch_block(const VerifyParams& p, int b, int h, int hk, int j0,
-                                               int WC, int t, int nt) {
+                                               int WC, int t) {
   const int N = p.N, dv = p.dv, esz = p.bf16 ? 2 : 4;
   const int s0 = p.slot != nullptr ? __ldcg(p.slot + b) : b;
   const int seg = (WC * 4 + 127) / 128;  // 128-byte lines per state row of the slab
   if (s0 >= 0 && s0 < p.n_slots) {
     const char* c0 = reinterpret_cast<const char*>(p.cache + (int64_t)s0 * p.cache_slot_stride +
                                                    (int64_t)h * DK * dv + j0);
-    for (int i = t; i < DK * seg; i += nt)
+    for (int i = t; i < DK * seg; i += NT)
       prefetch_l2(c0 + (int64_t)(i / seg) * dv * 4 + (i % seg) * 128);
   }
   const int per = (DK * esz + 127) / 128;
   const int qk_lines = N * per;
   const int64_t node0 = (int64_t)b * N;
-  for (int i = t; i < 2 * qk_lines + N; i += nt) {
+  for (int i = t; i < 2 * qk_lines + N; i += NT) {
     if (i < 2 * qk_lines) {
       const int which = i / qk_lines, r = i - which * qk_lines;
       const int n = r / per, part = r - n * per;
@@ -217,17 +213,14 @@ __device__ __forceinline__ void prefetch_block(const VerifyParams& p, int b, int
   }
 }
 
-// Start copying rows rows[i] (i < n_rows; rows 0.. when rows is null) of
-// row_bytes bytes each (row r at src + r*src_stride) to dst + i*dst_stride
-// with 16-byte cp.async, thread t of nt.
+// Start copying n_rows rows of row_bytes bytes each (row r at src +
+// r*src_stride) to dst + r*dst_stride with 16-byte cp.async, thread t.
 __device__ __forceinline__ void stage_rows(char* dst, int dst_stride, const char* src,
-                                           int64_t src_stride, const int* rows, int n_rows,
-                                           int row_bytes, int t, int nt) {
+                                           int64_t src_stride, int n_rows, int row_bytes, int t) {
   const int per_row = row_bytes / 16;
-  for (int idx = t; idx < n_rows * per_row; idx += nt) {
-    const int i = idx / per_row, c = idx - i * per_row;
-    const int r = rows != nullptr ? rows[i] : i;
-    cp_async16(dst + i * dst_stride + c * 16, src + r * src_stride + c * 16);
+  for (int idx = t; idx < n_rows * per_row; idx += NT) {
+    const int r = idx / per_row, c = idx - r * per_row;
+    cp_async16(dst + r * dst_stride + c * 16, src + r * src_stride + c * 16);
   }
 }
 
@@ -235,6 +228,13 @@ __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
 __device__ __forceinline__ uint32_t lds32(const uint16_t* p) {
   return *reinterpret_cast<const uint32_t*>(p);
+}
+
+// Next member of a bit set (lowest first), removed from it.
+__device__ __forceinline__ int pop_low(uint64_t& set) {
+  const int m = __ffsll(static_cast<long long>(set)) - 1;
+  set &= set - 1;
+  return m;
 }
 
 // ---------------------------------------------------------- phases 1 and 2
@@ -265,72 +265,58 @@ __device__ __forceinline__ void frag_bs(const float* M, int ld, int k0, int n0, 
   tc::split_bf16x2(p[8 * ld], p[9 * ld], hi[1], lo[1]);
 }
 
-// One 16 x 8 tile of C = A B over DK, scaled by the row and column factors
-// (when given) and written into the fp32 matrix C [row][ldc].
+// One 16 x 8 tile of A B over DK into acc: rows r0 + g8 (acc[0], acc[1]) and
+// r0 + g8 + 8 (acc[2], acc[3]), columns n0 + 2 t4, +1.
 //   BT: B[k][n] = Bm[n][k] (bf16, exact); otherwise B is the fp32 state slab
 //   [k][ldb] split into hi + lo.  SPLIT: A (and a bf16 B) carry a lo plane
 //   `plane` elements after the hi plane.
 template <int DK, bool BT, bool SPLIT>
 __device__ __forceinline__ void tile_mma(const uint16_t* A, int lda, int plane, const void* Bm,
-                                         int ldb, int r0, int n0, float* C, int ldc,
-                                         const float* rs, const float* cs, int g8, int t4) {
+                                         int ldb, int r0, int n0, int g8, int t4,
+                                         float (&acc)[4]) {
   // two accumulators (even and odd k-steps) halve the chain of dependent MMAs
   float accs[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
   for (int k0 = 0; k0 < DK; k0 += 16) {
-    float (&acc)[4] = accs[(k0 >> 4) & 1];
+    float (&c)[4] = accs[(k0 >> 4) & 1];
     uint32_t ah[4];
     frag_a(A, lda, r0, k0, g8, t4, ah);
     if constexpr (BT) {
       const uint16_t* B = static_cast<const uint16_t*>(Bm);
       uint32_t b0, b1;
       frag_bt(B, ldb, n0, k0, g8, t4, b0, b1);
-      mma_bf16_16816(acc, ah, b0, b1);
+      mma_bf16_16816(c, ah, b0, b1);
       if constexpr (SPLIT) {
         uint32_t al[4], c0, c1;
         frag_a(A + plane, lda, r0, k0, g8, t4, al);
         frag_bt(B + plane, ldb, n0, k0, g8, t4, c0, c1);
-        mma_bf16_16816(acc, ah, c0, c1);
-        mma_bf16_16816(acc, al, b0, b1);
+        mma_bf16_16816(c, ah, c0, c1);
+        mma_bf16_16816(c, al, b0, b1);
       }
     } else {
       uint32_t bh[2], bl[2];
       frag_bs(static_cast<const float*>(Bm), ldb, k0, n0, g8, t4, bh, bl);
-      mma_bf16_16816(acc, ah, bh[0], bh[1]);
-      mma_bf16_16816(acc, ah, bl[0], bl[1]);
+      mma_bf16_16816(c, ah, bh[0], bh[1]);
+      mma_bf16_16816(c, ah, bl[0], bl[1]);
       if constexpr (SPLIT) {
         uint32_t al[4];
         frag_a(A + plane, lda, r0, k0, g8, t4, al);
-        mma_bf16_16816(acc, al, bh[0], bh[1]);
+        mma_bf16_16816(c, al, bh[0], bh[1]);
       }
     }
   }
-  float acc[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) acc[e] = accs[0][e] + accs[1][e];
-  const int r = r0 + g8, c = n0 + 2 * t4;
-  float s0 = 1.f, s1 = 1.f, t0 = 1.f, t1 = 1.f;
-  if (rs != nullptr) {
-    s0 = rs[r];
-    s1 = rs[r + 8];
-  }
-  if (cs != nullptr) {
-    t0 = cs[c];
-    t1 = cs[c + 1];
-  }
-  *reinterpret_cast<float2*>(C + r * ldc + c) = make_float2(acc[0] * s0 * t0, acc[1] * s0 * t1);
-  *reinterpret_cast<float2*>(C + (r + 8) * ldc + c) =
-      make_float2(acc[2] * s1 * t0, acc[3] * s1 * t1);
 }
 
-// Phase 1 for N nodes whose k (and q) rows, gates and parents are staged:
-// the working forms of the inputs, the tree's depths and ancestor sets,
-// K K^T and Q K^T, the decay products r, A and P.  Returns 0, or 1 if the
-// parent array is malformed, 2 if the tree is deeper than max_depth (depths
-// filled in); every thread returns the same value.
-template <int DK, int NW, bool TREE, bool SPLIT, bool PREP, bool HAS_Q>
-__device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth) {
-  constexpr int NT = 32 * NW;
+// Phase 1 for N nodes whose k and q rows, gates and parents are staged: the
+// working forms of the inputs, the tree's depths, ancestor sets and log decay,
+// K K^T and Q K^T, r, A and P, then T = (I + A)^-1 by depth levels and P T;
+// with `order`, the k rows in fp32 and the depth-first order for phase 3.
+// Returns 0, or 1 if the parent array is malformed, 2 if the tree is deeper
+// than max_depth (depths filled in); every thread returns the same value.
+template <int DK, bool SPLIT, bool PREP>
+__device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth, bool order) {
   const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
   const int g8 = lane >> 2, t4 = lane & 3;
   uint16_t* ks = reinterpret_cast<uint16_t*>(smem + pl.ks);
@@ -341,22 +327,26 @@ __device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth) {
   const float* rawq = reinterpret_cast<const float*>(smem + pl.kk);
   float* sa = reinterpret_cast<float*>(smem + pl.a);
   float* sb = reinterpret_cast<float*>(smem + pl.b);
+  float* sla = reinterpret_cast<float*>(smem + pl.la);
   float* sg = reinterpret_cast<float*>(smem + pl.g);
+  float* sL = reinterpret_cast<float*>(smem + pl.L);
   float* siq = reinterpret_cast<float*>(smem + pl.iq);
   float* sik = reinterpret_cast<float*>(smem + pl.ik);
   const int* spar = reinterpret_cast<const int*>(smem + pl.par);
   int* sdep = reinterpret_cast<int*>(smem + pl.dep);
+  int* sord = reinterpret_cast<int*>(smem + pl.ord);
   uint64_t* sanc = reinterpret_cast<uint64_t*>(smem + pl.anc);
   float* kk = reinterpret_cast<float*>(smem + pl.kk);
   float* qk = reinterpret_cast<float*>(smem + pl.qk);
   float* rr = reinterpret_cast<float*>(smem + pl.rr);
+  float* tt = reinterpret_cast<float*>(smem + pl.tt);
   const int NP = pl.NP, lds = pl.lds, ldm = pl.ldm;
   const int plane = NP * lds;
 
   // ---- fp32 rows split into bf16 planes (SPLIT), norms and gate maps (PREP)
   if constexpr (SPLIT) {
     const int half = N * DK / 2;
-    for (int i = tid; i < (HAS_Q ? 2 : 1) * half; i += NT) {
+    for (int i = tid; i < 2 * half; i += NT) {
       const int which = i / half, e = 2 * (i - which * half);
       const int n = e / DK, c = e - n * DK;
       const float2 x = *reinterpret_cast<const float2*>((which ? rawq : rawk) + e);
@@ -371,7 +361,7 @@ __device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth) {
     for (int r = tid; r < 2 * NP; r += NT) {
       const int which = r / NP, n = r - which * NP;
       float ss = 0.f;
-      if (n < N && (HAS_Q || which == 0)) {
+      if (n < N) {
         if constexpr (SPLIT) {
           const float* x = (which ? rawq : rawk) + n * DK;
           for (int c = 0; c < DK; ++c) ss = fmaf(x[c], x[c], ss);
@@ -392,121 +382,113 @@ __device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth) {
     }
   }
   __syncthreads();
-  // k rows in fp32 for phase 3 (normalised for PREP), 8 elements a step
-  for (int i = tid; i < N * DK / 8; i += NT) {
-    const int e = 8 * i, n = e / DK, c = e - n * DK;
-    float x[8];
-    if constexpr (SPLIT) {
-      const float4 u0 = *reinterpret_cast<const float4*>(rawk + e);
-      const float4 u1 = *reinterpret_cast<const float4*>(rawk + e + 4);
-      x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
-      x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
-    } else {
-      const uint4 w = *reinterpret_cast<const uint4*>(ks + n * lds + c);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        x[2 * j] = __uint_as_float(ww[j] << 16);
-        x[2 * j + 1] = __uint_as_float(ww[j] & 0xffff0000u);
-      }
-    }
-    const float sc = PREP ? sik[n] : 1.f;
-    *reinterpret_cast<float4*>(kf + e) = make_float4(sc * x[0], sc * x[1], sc * x[2], sc * x[3]);
-    *reinterpret_cast<float4*>(kf + e + 4) = make_float4(sc * x[4], sc * x[5], sc * x[6], sc * x[7]);
+  // log alpha (clamped below at 1e-30, where its log is finite); a malformed
+  // parent array stops the block
+  bool ok = true;
+  for (int n = tid; n < N; n += NT) {
+    sla[n] = logf(fmaxf(sa[n], 1e-30f));
+    const int pp = spar[n];
+    ok = ok && (n == 0 ? pp == -1 : (pp >= 0 && pp < n));
   }
+  if (__syncthreads_and(ok) == 0) return 1;
 
-  // ---- depths, strict ancestors and the log decay L_n = sum over the path of
-  //      log alpha (alpha clamped below at 1e-30, where its log is finite)
-  float* sL = reinterpret_cast<float*>(smem + pl.L);
-  int* sord = reinterpret_cast<int*>(smem + pl.ord);
-  if constexpr (TREE) {
-    bool ok = true;
-    for (int n = tid; n < N; n += NT) {
-      const int pp = spar[n];
-      ok = ok && (n == 0 ? pp == -1 : (pp >= 0 && pp < n));
+  // ---- depths, strict ancestors, L_n and g_n (one node per thread, walking
+  //      up to the root); K K^T and Q K^T, the tiles on and below the
+  //      diagonal (PREP: scaled by 1/|q_n| or 1/|k_n| and 1/|k_m|)
+  bool shallow = true;
+  for (int n = tid; n < N; n += NT) {
+    int d = 1;
+    uint64_t anc = 0;
+    float l = sla[n];
+    for (int m = spar[n]; m >= 0; m = spar[m]) {
+      ++d;
+      anc |= 1ull << m;
+      l += sla[m];
     }
-    if (__syncthreads_and(ok) == 0) return 1;
-    bool shallow = true;
-    for (int n = tid; n < N; n += NT) {
-      int d = 1;
-      uint64_t anc = 0;
-      float l = logf(fmaxf(sa[n], 1e-30f));
-      for (int m = spar[n]; m >= 0; m = spar[m]) {
-        ++d;
-        anc |= 1ull << m;
-        l += logf(fmaxf(sa[m], 1e-30f));
-      }
-      sdep[n] = d;
-      sanc[n] = anc;
-      sL[n] = l;
-      shallow = shallow && (max_depth <= 0 || d <= max_depth);
-    }
-    if (__syncthreads_and(shallow) == 0) return 2;
-  } else {
-    for (int n = tid; n < N; n += NT) {
-      sdep[n] = n + 1;
-      sanc[n] = (1ull << n) - 1;
-      sord[n] = n;
-    }
-    if (wi == 0) {
-      // inclusive scan of log alpha over the chain, two nodes per lane
-      const int n0 = 2 * lane, n1 = n0 + 1;
-      const float l0 = n0 < N ? logf(fmaxf(sa[n0], 1e-30f)) : 0.f;
-      const float l1 = n1 < N ? logf(fmaxf(sa[n1], 1e-30f)) : 0.f;
-      float sum = l0 + l1;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, sum, off);
-        if (lane >= off) sum += y;
-      }
-      float excl = __shfl_up_sync(0xffffffffu, sum, 1);
-      if (lane == 0) excl = 0.f;
-      const float L0 = excl + l0;
-      if (n0 < N) sL[n0] = L0;
-      if (n1 < N) sL[n1] = L0 + l1;
-    }
+    sdep[n] = d;
+    sanc[n] = anc;
+    sL[n] = l;
+    sg[n] = expf(l);
+    shallow = shallow && (max_depth <= 0 || d <= max_depth);
   }
-
-  // ---- K K^T and Q K^T, the tiles on and below the diagonal (PREP: scaled
-  //      by 1/|q_n| or 1/|k_n| and 1/|k_m|)
   {
     const int mt_n = NP / 16, nt_n = NP / 8, n_tiles = mt_n * nt_n;
-    for (int task = wi; task < (HAS_Q ? 2 : 1) * n_tiles; task += NW) {
+    for (int task = wi; task < 2 * n_tiles; task += kWarps) {
       const int which = task / n_tiles, tl = task - which * n_tiles;
       const int mt = tl / nt_n, nt = tl - mt * nt_n;
       if (nt * 8 > mt * 16 + 15) continue;
-      tile_mma<DK, true, SPLIT>(which ? qs : ks, lds, plane, ks, lds, mt * 16, nt * 8,
-                                which ? qk : kk, ldm, PREP ? (which ? siq : sik) : nullptr,
-                                PREP ? sik : nullptr, g8, t4);
+      float acc[4];
+      tile_mma<DK, true, SPLIT>(which ? qs : ks, lds, plane, ks, lds, mt * 16, nt * 8, g8, t4,
+                                acc);
+      const int r = mt * 16 + g8, c = nt * 8 + 2 * t4;
+      float s0 = 1.f, s1 = 1.f, c0 = 1.f, c1 = 1.f;
+      if constexpr (PREP) {
+        const float* rs = which ? siq : sik;
+        s0 = rs[r];
+        s1 = rs[r + 8];
+        c0 = sik[c];
+        c1 = sik[c + 1];
+      }
+      float* C = which ? qk : kk;
+      *reinterpret_cast<float2*>(C + r * ldm + c) = make_float2(acc[0] * s0 * c0, acc[1] * s0 * c1);
+      *reinterpret_cast<float2*>(C + (r + 8) * ldm + c) =
+          make_float2(acc[2] * s1 * c0, acc[3] * s1 * c1);
     }
   }
-  __syncthreads();
+  if (__syncthreads_and(shallow) == 0) return 2;
 
-  // ---- r(n, m) = e^(L_n - L_m) for the strict ancestors m of n (1 on the
-  //      diagonal), A = beta r (K K^T) and P = r (Q K^T) under the ancestor
-  //      mask and zero elsewhere, g_n = e^(L_n); every entry on its own
-  for (int idx = tid; idx < NP * (NP + 1); idx += NT) {
-    const int n = idx / (NP + 1), m = idx - n * (NP + 1) - 1;  // m = -1 .. NP-1
-    if (m < 0) {
-      if (n < N) sg[n] = expf(sL[n]);
-      continue;
-    }
-    const bool anc = n < N && m < n && ((sanc[n] >> m) & 1ull) != 0;
-    const float r = anc ? expf(sL[n] - sL[m]) : (n == m && n < N ? 1.f : 0.f);
+  // ---- r(n, m) = e^(L_n - L_m) on n's path (1 at m = n), A = beta r (K K^T)
+  //      for the strict ancestors, P = r (Q K^T) on the path; entries off the
+  //      path are never read.  With `order`: the k rows in fp32 (normalised
+  //      for PREP) and every node's subtree size (into the d slab, free
+  //      until phase 2).
+  for (int idx = tid; idx < N * NP; idx += NT) {
+    const int n = idx / NP, m = idx - n * NP;
+    if (m > n || (m < n && ((sanc[n] >> m) & 1ull) == 0)) continue;
+    const float r = m == n ? 1.f : expf(sL[n] - sL[m]);
     rr[n * ldm + m] = r;
-    kk[n * ldm + m] = anc ? sb[n] * r * kk[n * ldm + m] : 0.f;
-    if constexpr (HAS_Q) qk[n * ldm + m] = r != 0.f ? r * qk[n * ldm + m] : 0.f;
+    if (m < n) kk[n * ldm + m] = sb[n] * r * kk[n * ldm + m];
+    qk[n * ldm + m] = r * qk[n * ldm + m];
   }
-  if constexpr (TREE) {
-    // depth-first order: a node after its parent and the parent's earlier
-    // subtrees (children in index order), from the subtree sizes
-    int* ssz = reinterpret_cast<int*>(smem + pl.u);  // free until phase 2
+  int* ssz = reinterpret_cast<int*>(smem + pl.d);
+  if (order) {
+    for (int i = tid; i < N * DK / 8; i += NT) {
+      const int e = 8 * i, n = e / DK, c = e - n * DK;
+      float x[8];
+      if constexpr (SPLIT) {
+        const float4 u0 = *reinterpret_cast<const float4*>(rawk + e);
+        const float4 u1 = *reinterpret_cast<const float4*>(rawk + e + 4);
+        x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
+        x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+      } else {
+        const uint4 w = *reinterpret_cast<const uint4*>(ks + n * lds + c);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          x[2 * j] = __uint_as_float(ww[j] << 16);
+          x[2 * j + 1] = __uint_as_float(ww[j] & 0xffff0000u);
+        }
+      }
+      const float sc = PREP ? sik[n] : 1.f;
+      *reinterpret_cast<float4*>(kf + e) = make_float4(sc * x[0], sc * x[1], sc * x[2], sc * x[3]);
+      *reinterpret_cast<float4*>(kf + e + 4) =
+          make_float4(sc * x[4], sc * x[5], sc * x[6], sc * x[7]);
+    }
     for (int n = tid; n < N; n += NT) {
       int sz = 1;
       for (int m = n + 1; m < N; ++m) sz += (int)((sanc[m] >> n) & 1ull);
       ssz[n] = sz;
     }
-    __syncthreads();
+  }
+  __syncthreads();
+
+  // ---- T = (I + A)^-1, depth level by depth level:
+  //      T[n][m] = [n = m] - sum over the strict ancestors s >= m of n of
+  //      A[n][s] T[s][m], zero unless m is on n's path.  The level's barrier
+  //      also tells whether any node was that deep.  With `order`, the
+  //      depth-first position of each node (after its parent and the earlier
+  //      siblings' subtrees, children in index order) meanwhile.
+  if (order) {
     for (int n = tid; n < N; n += NT) {
       int pre = 0;
       for (int a = n; a > 0; a = spar[a]) {
@@ -518,20 +500,49 @@ __device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth) {
       sord[pre] = n;
     }
   }
-  __syncthreads();
+  for (int d = 1;; ++d) {
+    bool any = false;
+    for (int idx = tid; idx < N * N; idx += NT) {
+      const int n = idx / N, m = idx - n * N;
+      if (sdep[n] != d) continue;
+      any = true;
+      const uint64_t anc = sanc[n];
+      if (m > n || (m < n && ((anc >> m) & 1ull) == 0)) continue;
+      float t = m == n ? 1.f : 0.f;
+      uint64_t s_set = anc & ~((1ull << m) - 1ull);  // strict ancestors s >= m
+      while (s_set != 0) {
+        const int s = pop_low(s_set);
+        t = fmaf(-kk[n * ldm + s], tt[s * ldm + m], t);
+      }
+      tt[n * ldm + m] = t;
+    }
+    if (__syncthreads_or(any) == 0) break;
+  }
+
+  // ---- P T over A (A is dead): (P T)[n][m] = sum over s on n's path with m
+  //      on s's path of P[n][s] T[s][m]
+  for (int idx = tid; idx < N * N; idx += NT) {
+    const int n = idx / N, m = idx - n * N;
+    const uint64_t path = sanc[n] | (1ull << n);
+    if (((path >> m) & 1ull) == 0) continue;
+    float acc = 0.f;
+    uint64_t s_set = path & ~((1ull << m) - 1ull);
+    while (s_set != 0) {
+      const int s = pop_low(s_set);
+      if (((sanc[s] | (1ull << s)) >> m) & 1ull) acc = fmaf(qk[n * ldm + s], tt[s * ldm + m], acc);
+    }
+    kk[n * ldm + m] = acc;
+  }
   return 0;
 }
 
-// Phase 2, once the state slab is in h0: K H0 and Q H0 on tensor cores,
-// X = diag(beta)(V - diag(g) K H0), Delta solving (I + A) Delta = X by forward
-// substitution, and (with HAS_Q) the outputs O = diag(g) Q H0 + P Delta, row
-// n to o_out + n*o_stride (WC columns).  The substitution and the outputs run
-// one column per lane of warp 0, 16 rows at a time in registers: the rows
-// of a block take the earlier blocks' terms as independent sums, then solve
-// among themselves.
-template <int DK, int WC, int NW, bool SPLIT, bool PREP, bool HAS_Q>
+// Phase 2, once the state slab is in h0 (and phase 1's results are visible):
+// K H0 and Q H0 on tensor cores, X = diag(beta)(V - diag(g) K H0) formed in
+// the epilogue, then every entry of Delta = T X and of the outputs
+// O = diag(g) Q H0 + (P T) X on its own, a sum over the node's path; row n of
+// O to o_out + n*o_stride (WC columns).
+template <int DK, int WC, bool SPLIT, bool PREP>
 __device__ void solve_finish(const Plan& pl, char* smem, int N, float* o_out, int64_t o_stride) {
-  constexpr int NT = 32 * NW;
   const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
   const int g8 = lane >> 2, t4 = lane & 3;
   const uint16_t* ks = reinterpret_cast<const uint16_t*>(smem + pl.ks);
@@ -541,9 +552,10 @@ __device__ void solve_finish(const Plan& pl, char* smem, int N, float* o_out, in
   const float* sg = reinterpret_cast<const float*>(smem + pl.g);
   const float* siq = reinterpret_cast<const float*>(smem + pl.iq);
   const float* sik = reinterpret_cast<const float*>(smem + pl.ik);
-  const float* kk = reinterpret_cast<const float*>(smem + pl.kk);
-  const float* qk = reinterpret_cast<const float*>(smem + pl.qk);
-  float* su = reinterpret_cast<float*>(smem + pl.u);
+  const uint64_t* sanc = reinterpret_cast<const uint64_t*>(smem + pl.anc);
+  const float* pt = reinterpret_cast<const float*>(smem + pl.kk);
+  const float* tt = reinterpret_cast<const float*>(smem + pl.tt);
+  float* sx = reinterpret_cast<float*>(smem + pl.x);
   float* sqh = reinterpret_cast<float*>(smem + pl.qh);
   float* sd = reinterpret_cast<float*>(smem + pl.d);
   const int NP = pl.NP, lds = pl.lds, ldm = pl.ldm, ldh = pl.ldh;
@@ -551,60 +563,63 @@ __device__ void solve_finish(const Plan& pl, char* smem, int N, float* o_out, in
 
   {
     const int mt_n = NP / 16, nt_n = WC / 8, n_tiles = mt_n * nt_n;
-    for (int task = wi; task < (HAS_Q ? 2 : 1) * n_tiles; task += NW) {
+    for (int task = wi; task < 2 * n_tiles; task += kWarps) {
       const int which = task / n_tiles, tl = task - which * n_tiles;
       const int mt = tl / nt_n, nt = tl - mt * nt_n;
-      tile_mma<DK, false, SPLIT>(which ? qs : ks, lds, plane, h0, ldh, mt * 16, nt * 8,
-                                 which ? sqh : su, WC, PREP ? (which ? siq : sik) : nullptr,
-                                 nullptr, g8, t4);
+      float acc[4];
+      tile_mma<DK, false, SPLIT>(which ? qs : ks, lds, plane, h0, ldh, mt * 16, nt * 8, g8, t4,
+                                 acc);
+      const int c = nt * 8 + 2 * t4;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = mt * 16 + g8 + 8 * hh;
+        if (r >= N) continue;
+        float e0 = acc[2 * hh], e1 = acc[2 * hh + 1];
+        if constexpr (PREP) {
+          const float sc = which ? siq[r] : sik[r];
+          e0 *= sc;
+          e1 *= sc;
+        }
+        if (which) {
+          *reinterpret_cast<float2*>(sqh + r * WC + c) = make_float2(e0, e1);
+        } else {
+          // X = beta (v - g K H0); the v slab is staged in the input dtype
+          float v0, v1;
+          if constexpr (SPLIT) {
+            const float2 vv = *reinterpret_cast<const float2*>(
+                reinterpret_cast<const float*>(smem + pl.v) + r * WC + c);
+            v0 = vv.x;
+            v1 = vv.y;
+          } else {
+            const uint32_t w =
+                lds32(reinterpret_cast<const uint16_t*>(smem + pl.v) + r * WC + c);
+            v0 = __uint_as_float(w << 16);
+            v1 = __uint_as_float(w & 0xffff0000u);
+          }
+          const float be = sb[r], gr = sg[r];
+          *reinterpret_cast<float2*>(sx + r * WC + c) =
+              make_float2(be * (v0 - gr * e0), be * (v1 - gr * e1));
+        }
+      }
     }
   }
   __syncthreads();
-  // X in place of K H0 (the v slab is staged in the input dtype)
-  for (int idx = tid; idx < N * WC; idx += NT) {
-    const int n = idx / WC;
-    float vv;
-    if constexpr (SPLIT) vv = reinterpret_cast<const float*>(smem + pl.v)[idx];
-    else vv = bf16_to_f32(reinterpret_cast<const uint16_t*>(smem + pl.v)[idx]);
-    su[idx] = sb[n] * (vv - sg[n] * su[idx]);
-  }
-  __syncthreads();
-  if (wi == 0 && lane < WC) {
-    const int c = lane;
-    for (int n0 = 0; n0 < N; n0 += 16) {
-      float x[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = n0 + i < N ? su[(n0 + i) * WC + c] : 0.f;
-      // the earlier blocks' terms
-      for (int m = 0; m < n0; ++m) {
-        const float dm = sd[m * WC + c];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = fmaf(-kk[(n0 + i) * ldm + m], dm, x[i]);
-      }
-      // the block's own rows, in order
-#pragma unroll
-      for (int i = 1; i < 16; ++i)
-#pragma unroll
-        for (int t = 0; t < i; ++t) x[i] = fmaf(-kk[(n0 + i) * ldm + n0 + t], x[t], x[i]);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) sd[(n0 + i) * WC + c] = x[i];
+  for (int idx = tid; idx < 2 * N * WC; idx += NT) {
+    const int which = idx >= N * WC;
+    const int e = idx - (which ? N * WC : 0);
+    const int n = e / WC, c = e - n * WC;
+    const float* M = which ? pt : tt;
+    float a0 = which ? sg[n] * sqh[e] : 0.f, a1 = 0.f;
+    uint64_t path = sanc[n] | (1ull << n);
+    while (path != 0) {
+      const int m = pop_low(path);
+      a0 = fmaf(M[n * ldm + m], sx[m * WC + c], a0);
+      if (path == 0) break;
+      const int m2 = pop_low(path);
+      a1 = fmaf(M[n * ldm + m2], sx[m2 * WC + c], a1);
     }
-  }
-  if constexpr (HAS_Q) {
-    __syncthreads();
-    // O = diag(g) Q H0 + P Delta (P is zero above the diagonal), every output
-    // on its own
-    for (int idx = tid; idx < N * WC; idx += NT) {
-      const int n = idx / WC, c = idx - n * WC;
-      float e0 = sg[n] * sqh[idx], e1 = 0.f;
-      int m = 0;
-      for (; m + 1 <= n; m += 2) {
-        e0 = fmaf(qk[n * ldm + m], sd[m * WC + c], e0);
-        e1 = fmaf(qk[n * ldm + m + 1], sd[(m + 1) * WC + c], e1);
-      }
-      if (m <= n) e0 = fmaf(qk[n * ldm + m], sd[m * WC + c], e0);
-      o_out[n * o_stride + c] = e0 + e1;
-    }
+    if (which) o_out[n * o_stride + c] = a0 + a1;
+    else sd[e] = a0 + a1;
   }
 }
 
@@ -667,35 +682,34 @@ __device__ __forceinline__ void store_state16(__half* dst, int64_t dv, const flo
   }
 }
 
-// Zero the padding rows N .. NP-1 of the bf16 k (and q) tiles.
-__device__ __forceinline__ void zero_padding(const Plan& pl, char* smem, int N, bool split,
-                                             bool has_q, int t, int nt) {
+// Zero the padding rows N .. NP-1 of the bf16 k and q tiles.
+__device__ __forceinline__ void zero_padding(const Plan& pl, char* smem, int N, bool split, int t) {
   uint16_t* ks = reinterpret_cast<uint16_t*>(smem + pl.ks);
   uint16_t* qs = reinterpret_cast<uint16_t*>(smem + pl.qs);
   const int per_plane = (pl.NP - N) * pl.lds;
   const int planes = split ? 2 : 1;
-  for (int i = t; i < planes * per_plane; i += nt) {
+  for (int i = t; i < planes * per_plane; i += NT) {
     const int pi = i / per_plane, e = i - pi * per_plane;
     ks[pi * pl.NP * pl.lds + N * pl.lds + e] = 0;
-    if (has_q) qs[pi * pl.NP * pl.lds + N * pl.lds + e] = 0;
+    qs[pi * pl.NP * pl.lds + N * pl.lds + e] = 0;
   }
 }
 
 // ---------------------------------------------------------------- verify
-template <int DK, int WC, int NW, bool TREE, bool SNAP16, bool PREP, bool SPLIT>
-__global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
-  using S = Shape<DK, WC, NW>;
+template <int DK, int WC, bool SNAP16, bool PREP, bool SPLIT>
+__global__ void __launch_bounds__(NT) tree_solve_kernel(const VerifyParams p) {
+  using S = Shape<DK, WC>;
   constexpr int R = S::R;
-  constexpr int NT = 32 * NW;
   const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
   const int j0 = blockIdx.x * WC, h = blockIdx.y, b = blockIdx.z;
   const int hk = h / (p.Hv / p.Hk);
-  if (p.hint) prefetch_block<DK>(p, b, h, hk, j0, WC, tid, NT);
+  if (p.hint) prefetch_block<DK>(p, b, h, hk, j0, WC, tid);
   pdl_enter();
   extern __shared__ __align__(16) char smem[];
   const int N = p.N, dv = p.dv;
-  const Plan pl = make_plan(N, DK, WC, SPLIT, true);
+  const Plan pl = make_plan(N, DK, WC, SPLIT);
   const bool lead = blockIdx.x == 0 && blockIdx.y == 0;  // per-sequence reporting
+  const bool persist = SNAP16 || p.snap != nullptr;
   const int64_t node0 = (int64_t)b * N;
   constexpr int esz = SPLIT ? 4 : 2;
   int* spar = reinterpret_cast<int*>(smem + pl.par);
@@ -709,21 +723,19 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
     const char* vb = static_cast<const char*>(p.v) + ((node0 * p.Hv + h) * dv + j0) * esz;
     const int64_t qk_stride = (int64_t)p.Hk * DK * esz;
     if constexpr (SPLIT) {
-      stage_rows(smem + pl.kf, DK * 4, kb, qk_stride, nullptr, N, DK * 4, tid, NT);
-      stage_rows(smem + pl.kk, DK * 4, qb, qk_stride, nullptr, N, DK * 4, tid, NT);
+      stage_rows(smem + pl.kf, DK * 4, kb, qk_stride, N, DK * 4, tid);
+      stage_rows(smem + pl.kk, DK * 4, qb, qk_stride, N, DK * 4, tid);
     } else {
-      stage_rows(smem + pl.ks, pl.lds * 2, kb, qk_stride, nullptr, N, DK * 2, tid, NT);
-      stage_rows(smem + pl.qs, pl.lds * 2, qb, qk_stride, nullptr, N, DK * 2, tid, NT);
+      stage_rows(smem + pl.ks, pl.lds * 2, kb, qk_stride, N, DK * 2, tid);
+      stage_rows(smem + pl.qs, pl.lds * 2, qb, qk_stride, N, DK * 2, tid);
     }
-    stage_rows(smem + pl.v, WC * esz, vb, (int64_t)p.Hv * dv * esz, nullptr, N, WC * esz, tid,
-               NT);
+    stage_rows(smem + pl.v, WC * esz, vb, (int64_t)p.Hv * dv * esz, N, WC * esz, tid);
     for (int n = tid; n < N; n += NT) {
       cp_async4(reinterpret_cast<float*>(smem + pl.a) + n, p.alpha + (node0 + n) * p.Hv + h);
       cp_async4(reinterpret_cast<float*>(smem + pl.b) + n, p.beta + (node0 + n) * p.Hv + h);
-      if constexpr (TREE) cp_async4(spar + n, p.parent + node0 + n);
-      else spar[n] = n - 1;
+      cp_async4(spar + n, p.parent + node0 + n);
     }
-    zero_padding(pl, smem, N, SPLIT, true, tid, NT);
+    zero_padding(pl, smem, N, SPLIT, tid);
     cp_async_commit();
   }
   const int sl = p.slot != nullptr ? __ldg(p.slot + b) : b;
@@ -731,7 +743,7 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
   if (slot_ok) {
     const char* c0 = reinterpret_cast<const char*>(p.cache + (int64_t)sl * p.cache_slot_stride +
                                                    (int64_t)h * DK * dv + j0);
-    stage_rows(smem + pl.h0, pl.ldh * 4, c0, (int64_t)dv * 4, nullptr, DK, WC * 4, tid, NT);
+    stage_rows(smem + pl.h0, pl.ldh * 4, c0, (int64_t)dv * 4, DK, WC * 4, tid);
   }
   cp_async_commit();
   if (!slot_ok) {
@@ -742,26 +754,27 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
   cp_async_wait<1>();
   __syncthreads();
 
-  const int bad =
-      solve_prepare<DK, NW, TREE, SPLIT, PREP, true>(pl, smem, N, TREE ? p.max_depth : 0);
+  const int bad = solve_prepare<DK, SPLIT, PREP>(pl, smem, N, p.max_depth, persist);
   if (bad != 0) {  // a malformed tree, or one deeper than the cap (depths reported)
     cp_async_wait<0>();
     if (lead && tid == 0) report(p.status, GDN_ERR_BAD_TREE);
-    if (TREE && bad == 2 && lead && p.depth_out != nullptr)
+    if (bad == 2 && lead && p.depth_out != nullptr)
       for (int n = tid; n < N; n += NT) p.depth_out[node0 + n] = sdep[n];
     return;
   }
   cp_async_wait<0>();
   __syncthreads();
-  solve_finish<DK, WC, NW, SPLIT, PREP, true>(pl, smem, N, p.o + (node0 * p.Hv + h) * dv + j0,
-                                              (int64_t)p.Hv * dv);
-  if (TREE && lead && p.depth_out != nullptr)
+  solve_finish<DK, WC, SPLIT, PREP>(pl, smem, N, p.o + (node0 * p.Hv + h) * dv + j0,
+                                    (int64_t)p.Hv * dv);
+  if (lead && p.depth_out != nullptr)
     for (int n = tid; n < N; n += NT) p.depth_out[node0 + n] = sdep[n];
+  if (!persist) return;  // verified for a replay commit: outputs only
   __syncthreads();
 
   // ---- phase 3: the states in registers, stored as they are formed
+  if (wi >= S::NW) return;
   const int cg = lane % S::CG, rl = lane / S::CG;
-  const int row0 = wi * (DK / NW) + rl * R;
+  const int row0 = wi * (DK / S::NW) + rl * R;
   const float* h0 = reinterpret_cast<const float*>(smem + pl.h0);
   const float* kf = reinterpret_cast<const float*>(smem + pl.kf);
   const float* sd = reinterpret_cast<const float*>(smem + pl.d);
@@ -769,32 +782,28 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
   const float* sg = reinterpret_cast<const float*>(smem + pl.g);
   const float* rr = reinterpret_cast<const float*>(smem + pl.rr);
   const uint64_t* sanc = reinterpret_cast<const uint64_t*>(smem + pl.anc);
+  const int* sord = reinterpret_cast<const int*>(smem + pl.ord);
   float2 H[R][2];
-  float2 Hc[TREE ? R : 1][2];  // the cached state, kept for trees
+  float2 Hc[R][2];  // the cached state
 #pragma unroll
   for (int m = 0; m < R; ++m) {
     const float4 t = *reinterpret_cast<const float4*>(h0 + (row0 + m) * pl.ldh + cg * 4);
-    H[m][0] = make_float2(t.x, t.y);
-    H[m][1] = make_float2(t.z, t.w);
-    if constexpr (TREE) {
-      Hc[m][0] = H[m][0];
-      Hc[m][1] = H[m][1];
-    }
+    H[m][0] = Hc[m][0] = make_float2(t.x, t.y);
+    H[m][1] = Hc[m][1] = make_float2(t.z, t.w);
   }
   const int64_t node_stride = (int64_t)p.Hv * DK * dv;
   const int64_t lane_off =
       ((int64_t)b * N * p.Hv + h) * DK * dv + (int64_t)row0 * dv + j0 + cg * 4;
-  float* snap_l = p.snap == nullptr ? nullptr : p.snap + lane_off;
+  float* snap_l = SNAP16 ? nullptr : p.snap + lane_off;
   __half* snap16_l = SNAP16 ? p.snap16 + lane_off : nullptr;
-  const int* sord = reinterpret_cast<const int*>(smem + pl.ord);
   int held = -1;  // the node whose state H holds (-1: the cached state)
   for (int i = 0; i < N; ++i) {
-    const int n = TREE ? sord[i] : i;
+    const int n = sord[i];
     float kr[R];
-    if (!TREE || spar[n] == held) {
+    if (spar[n] == held) {
       load_k<R>(kr, kf + n * DK + row0);
       rank1_step<R>(H, kr, *reinterpret_cast<const float4*>(sd + n * WC + cg * 4), sa[n]);
-    } else if constexpr (TREE) {
+    } else {
       // H_n = g_n H0 + sum over the path of r(n, m) k_m delta_m^T, root first
       const float2 gn = f2(sg[n]);
 #pragma unroll
@@ -804,8 +813,7 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
       }
       uint64_t path = sanc[n] | (1ull << n);
       while (path != 0) {
-        const int m = __ffsll((long long)path) - 1;
-        path &= path - 1;
+        const int m = pop_low(path);
         load_k<R>(kr, kf + m * DK + row0);
         rank1_add<R>(H, kr, *reinterpret_cast<const float4*>(sd + m * WC + cg * 4),
                      rr[n * pl.ldm + m]);
@@ -813,49 +821,38 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
     }
     held = n;
     if constexpr (SNAP16) store_state16<R>(snap16_l + (int64_t)n * node_stride, dv, H);
-    else if (snap_l != nullptr) store_state<R>(snap_l + (int64_t)n * node_stride, dv, H);
+    else store_state<R>(snap_l + (int64_t)n * node_stride, dv, H);
   }
 }
 
-template <typename Kern, typename Params>
-int launch_with_smem(Kern kern, const Params& p, dim3 grid, dim3 block, size_t smem,
-                     cudaStream_t stream) {
+template <int DK, int WC, bool SNAP16, bool PREP>
+int launch_solve_t(const VerifyParams& p, int B, cudaStream_t stream) {
+  const dim3 grid(p.dv / WC, p.Hv, B);
+  const bool split = !p.bf16;
+  const size_t smem = (size_t)make_plan(p.N, DK, WC, split).total;
   if (smem > 227 * 1024) return GDN_ERR_UNSUPPORTED;
+  auto kern = split ? tree_solve_kernel<DK, WC, SNAP16, PREP, true>
+                    : tree_solve_kernel<DK, WC, SNAP16, PREP, false>;
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return GDN_ERR_CUDA;
   }
-  return launch_pdl(kern, grid, block, smem, stream, p);
+  return launch_pdl(kern, grid, dim3(NT), smem, stream, p);
 }
 
-template <int DK, int WC, int NW, bool TREE, bool SNAP16, bool PREP>
-int launch_verify_t(const VerifyParams& p, int B, cudaStream_t stream) {
-  const dim3 grid(p.dv / WC, p.Hv, B);
-  if (p.bf16)
-    return launch_with_smem(verify_kernel<DK, WC, NW, TREE, SNAP16, PREP, false>, p, grid,
-                            dim3(32 * NW), make_plan(p.N, DK, WC, false, true).total, stream);
-  return launch_with_smem(verify_kernel<DK, WC, NW, TREE, SNAP16, PREP, true>, p, grid,
-                          dim3(32 * NW), make_plan(p.N, DK, WC, true, true).total, stream);
-}
-
-#define GDN_TILES(X)  \
-  X(128, 16, 1)       \
-  X(128, 16, 2)       \
-  X(128, 8, 1)        \
-  X(64, 16, 1)        \
-  X(64, 16, 2)        \
-  X(64, 8, 1)         \
-  X(32, 16, 1)        \
-  X(32, 8, 1)         \
-  X(16, 16, 1)        \
-  X(16, 8, 1)
-
-template <bool TREE, bool SNAP16, bool PREP>
-int dispatch_verify(const VerifyParams& p, int B, int dk, int wc, int nw, cudaStream_t s) {
-#define GDN_CASE(DK_, WC_, NW_) \
-  if (dk == DK_ && wc == WC_ && nw == NW_) return launch_verify_t<DK_, WC_, NW_, TREE, SNAP16, PREP>(p, B, s);
-  GDN_TILES(GDN_CASE)
+template <bool SNAP16, bool PREP>
+int dispatch_solve(const VerifyParams& p, int B, int dk, int wc, cudaStream_t s) {
+#define GDN_CASE(DK_, WC_) \
+  if (dk == DK_ && wc == WC_) return launch_solve_t<DK_, WC_, SNAP16, PREP>(p, B, s);
+  GDN_CASE(128, 16)
+  GDN_CASE(128, 8)
+  GDN_CASE(64, 16)
+  GDN_CASE(64, 8)
+  GDN_CASE(32, 16)
+  GDN_CASE(32, 8)
+  GDN_CASE(16, 16)
+  GDN_CASE(16, 8)
 #undef GDN_CASE
   return GDN_ERR_UNSUPPORTED;
 }
@@ -863,7 +860,7 @@ int dispatch_verify(const VerifyParams& p, int B, int dk, int wc, int nw, cudaSt
 }  // namespace
 
 int launch_verify_tree_solve(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out,
-                             int wc, int nw, cudaStream_t stream, void* snap16, bool prep) {
+                             int wc, cudaStream_t stream, void* snap16, bool prep) {
   VerifyParams p{};
   p.q = a->q;
   p.k = a->k;
@@ -886,13 +883,13 @@ int launch_verify_tree_solve(const gdn_verify_args* a, const int32_t* parent, in
   p.bf16 = a->in_dtype == GDN_BF16;
   p.snap16 = static_cast<__half*>(snap16);
   p.hint = (int64_t)(p.dv / wc) * a->Hv * a->B <= kHintBlocks;
-  p.max_depth = parent != nullptr ? a->max_depth : 0;
-  const bool s16 = snap16 != nullptr;
+  p.max_depth = a->max_depth;
   const int B = a->B, dk = a->dk;
-  if (s16) return prep ? dispatch_verify<true, true, true>(p, B, dk, wc, nw, stream)
-                       : dispatch_verify<true, true, false>(p, B, dk, wc, nw, stream);
-  return prep ? dispatch_verify<true, false, true>(p, B, dk, wc, nw, stream)
-              : dispatch_verify<true, false, false>(p, B, dk, wc, nw, stream);
+  if (snap16 != nullptr)
+    return prep ? dispatch_solve<true, true>(p, B, dk, wc, stream)
+                : dispatch_solve<true, false>(p, B, dk, wc, stream);
+  return prep ? dispatch_solve<false, true>(p, B, dk, wc, stream)
+              : dispatch_solve<false, false>(p, B, dk, wc, stream);
 }
 
 }  // namespace gdn

@@ -1108,7 +1108,7 @@ int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   // a tree whose snapshots are binary16 or not kept at all cannot re-read its
   // parents from them: it is solved per block instead (gdn_solve.cu)
   if (parent != nullptr && (snap16 != nullptr || a->snapshots == nullptr))
-    return launch_verify_tree_solve(a, parent, depth_out, wc, nw, stream, snap16, prep);
+    return launch_verify_tree_solve(a, parent, depth_out, wc, stream, snap16, prep);
   if (parent != nullptr)  // row warps do not apply: a tree block's warps take whole nodes
     return prep ? dispatch_tree<true>(p, a->B, a->dk, wc, stream)
                 : dispatch_tree<false>(p, a->B, a->dk, wc, stream);

@@ -30,7 +30,7 @@ SEED_BASE = 0x6D6E0000
 GOLDEN_RATIO_64 = 0x9E3779B97F4A7C15
 MASK64 = (1 << 64) - 1
 
-WORKLOADS = ("tiny_chain", "chain16", "tree22", "batched8x16", "prefill8192")
+WORKLOADS = ("tiny_chain", "chain16", "tree22", "batched8x16", "prefill8192", "batched8x22")
 
 
 def workload_seed(name: str) -> int:
@@ -194,6 +194,21 @@ def batched8x16_layer(layer: int):
     rng = np.random.default_rng(base)
     inp["slot"] = rng.permutation(8).astype(np.int32)
     inp["accept"] = (rng.integers(1, 17, size=8) - 1).astype(np.int32)
+    return inp
+
+
+def batched8x22_layer(layer: int):
+    """One of the 48 layers of a batch of 8 sequences, each verifying a
+    22-node draft tree.  The trees, slots and accepted nodes belong to the
+    batch (every layer verifies the same trees), so they are drawn once from
+    the workload's base seed; q, k, v, gates and states are per layer."""
+    base = workload_seed("batched8x22")
+    inp = make_verify_inputs(B=8, N=22, dtype="bf16", alpha_kind="near_one", state_sigma=0.05,
+                             tree=True, seed=layer_seed(base, layer), **HEADS)
+    rng = np.random.default_rng(base)
+    inp["slot"] = rng.permutation(8).astype(np.int32)
+    inp["parent"] = np.stack([random_tree(rng, 22) for _ in range(8)]).astype(np.int32)
+    inp["accept"] = rng.integers(0, 22, size=8).astype(np.int32)
     return inp
 
 
