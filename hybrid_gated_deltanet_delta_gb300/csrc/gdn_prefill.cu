@@ -476,30 +476,17 @@ constexpr long long kWaitPolls = 1ll << 22;
 // the three column slabs of a 128-wide state: 48 + 48 + 32 columns
 __device__ __forceinline__ int slab_width(int s) { return s == 2 ? 32 : 48; }
 
-// NH = 16 fp32 columns of TMEM lane (warp quarter base + lane) starting at
-// `taddr`.
-__device__ __forceinline__ void tmem_cols(uint32_t taddr, int nh, float (&x)[NH]) {
-  (void)nh;
-  uint32_t r0[8], r1[8];
-  tc::tmem_ld8(taddr, r0);
-  tc::tmem_ld8(taddr + 8, r1);
+// An accumulator of the [hi | lo] products: the NH = 16 fp32 columns of this
+// thread's TMEM lane at `taddr` plus the 16 at taddr + n, both loads in
+// flight together (one wait).
+__device__ __forceinline__ void tmem_cols_sum(uint32_t taddr, int n, float (&x)[NH]) {
+  uint32_t r0[16], r1[16];
+  tc::tmem_ld16(taddr, r0);
+  tc::tmem_ld16(taddr + n, r1);
   tc::tmem_wait_ld(r0);
-  tc::tmem_wait_ld(r1);
+  tc::tmem_ready(r1);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    x[e] = __uint_as_float(r0[e]);
-    x[8 + e] = __uint_as_float(r1[e]);
-  }
-}
-
-// An accumulator of the [hi | lo] products: columns c .. c+nh-1 (at `taddr`)
-// plus columns n+c .. n+c+nh-1.
-__device__ __forceinline__ void tmem_cols_sum(uint32_t taddr, int n, int nh, float (&x)[NH]) {
-  float y[NH];
-  tmem_cols(taddr, nh, x);
-  tmem_cols(taddr + n, nh, y);
-#pragma unroll
-  for (int e = 0; e < NH; ++e) x[e] += y[e];
+  for (int e = 0; e < NH; ++e) x[e] = __uint_as_float(r0[e]) + __uint_as_float(r1[e]);
 }
 
 // Row `row`, columns c0 .. c0+nh-1 of an fp32 matrix as bf16 hi (columns c0..)
@@ -664,7 +651,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     float qh[NH];
     {
       float x[NH];
-      if (active) tmem_cols_sum(t_mine, n, nh, x);
+      if (active) tmem_cols_sum(t_mine, n, x);
       if (chunk_warp) {
         // X = beta (V - g K H)
 #pragma unroll
@@ -698,7 +685,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     tc::fence_after_sync();
     {
       float x[NH];
-      if (active) tmem_cols_sum(t_mine + 128, n, nh, x);
+      if (active) tmem_cols_sum(t_mine + 128, n, x);
       if (chunk_warp) {
         // D' = (g_C / g) Delta
         const float rg = __expf(GC - G_r);
@@ -736,7 +723,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     tc::fence_after_sync();
     {
       float x[NH];
-      if (active) tmem_cols_sum(t_mine + 256, n, nh, x);
+      if (active) tmem_cols_sum(t_mine + 256, n, x);
 #pragma unroll
       for (int e = 0; e < NH; ++e) Hr[e] = fmaf(gC, Hr[e], x[e]);
       put_split(hb, 16384, r, c0, n, Hr, nh);

@@ -510,13 +510,15 @@ __global__ void __launch_bounds__(32 * NW) verify_kernel(const VerifyParams p) {
 // the parent's snapshot, which a warp of this block stored one level earlier
 // (the barrier between levels makes it visible; it is read through L2).  Each
 // node reduces u = H^T k before its update and o = H'^T q after it.
-// Tree state stash: the states of the first kTreeSlots nodes of a level stay
-// in shared memory for the next level (two level buffers), so most children
-// read their parent from shared memory instead of L2.
+// Tree state stash: the states of up to kTreeSlots nodes of a level that have
+// children stay in shared memory for the next level (two level buffers), so
+// their children read them from shared memory instead of L2.  The tree's
+// shape (depths, walk order, level starts, stash slots) is worked out by one
+// warp with shuffles while the block's inputs and the cached state load.
 constexpr int kTreeSlots = 3;
 
 struct TreePlan {
-  int q, k, v, a, b, par, dep, ord, lev, pos, inv, stash, total;
+  int q, k, v, a, b, par, dep, ord, lev, slot, inv, stash, total;
 };
 
 __host__ __device__ inline TreePlan tree_plan(int N, int DK, int WC, int esz) {
@@ -530,11 +532,80 @@ __host__ __device__ inline TreePlan tree_plan(int N, int DK, int WC, int esz) {
   s.dep = s.par + round16(N * 4);        // depth of each node (root = 1)
   s.ord = s.dep + round16(N * 4);        // nodes by depth, then index
   s.lev = s.ord + round16(N * 4);        // lev[L] = first position of depth L
-  s.pos = s.lev + round16((N + 2) * 4);  // position of each node within its level
-  s.inv = s.pos + round16(N * 4);        // 1/|q_n|, 1/|k_n| (input preparation)
+  s.slot = s.lev + round16((N + 2) * 4); // stash slot of each node, -1 = none
+  s.inv = s.slot + round16(N * 4);       // 1/|q_n|, 1/|k_n| (input preparation)
   s.stash = s.inv + 2 * round16(N * 4);  // [2 levels][kTreeSlots][DK * WC] fp32
   s.total = s.stash + 2 * kTreeSlots * DK * WC * 4;
   return s;
+}
+
+// The value of node m (0 <= m < 64) from the two per-lane registers that
+// hold nodes lane and lane + 32 (every lane of the warp must call).
+__device__ __forceinline__ int node_val(int v0, int v1, int m) {
+  const int a = __shfl_sync(FULL, v0, m & 31), b = __shfl_sync(FULL, v1, m & 31);
+  return m < 32 ? a : b;
+}
+
+// The shape of a tree of N <= 64 nodes, by one warp: lane l takes nodes l
+// and l + 32.  parent[] is read from global memory (after the programmatic
+// wait); writes par[], dep[] (root = 1), ord[] (the walk order: by depth,
+// then index), lev[L] (first position of depth L, L = 1 .. N + 1) and
+// slot[] (the stash slot: the rank of the node among the nodes of its depth
+// that have children, when below kTreeSlots; otherwise -1).  Returns 0, 1
+// for a malformed parent array, 2 for a tree deeper than max_depth (depths
+// written); the same value in every lane.
+__device__ int tree_shape(const int32_t* parent, int N, int max_depth, int* spar, int* sdep,
+                          int* sord, int* slev, int* sslot) {
+  const int lane = threadIdx.x & 31;
+  const int n0 = lane, n1 = lane + 32;
+  const int p0 = n0 < N ? __ldcg(parent + n0) : -2;
+  const int p1 = n1 < N ? __ldcg(parent + n1) : -2;
+  const bool ok0 = n0 >= N || (n0 == 0 ? p0 == -1 : (p0 >= 0 && p0 < n0));
+  const bool ok1 = n1 >= N || (p1 >= 0 && p1 < n1);
+  if (!__all_sync(FULL, ok0 && ok1)) return 1;
+  // depths by pointer jumping: d counts the nodes from n up to (not
+  // including) the ancestor a; six rounds cover 64 levels
+  int d0 = n0 < N ? 1 : 0, d1 = n1 < N ? 1 : 0, a0 = p0, a1 = p1;
+#pragma unroll
+  for (int r = 0; r < 6; ++r) {
+    const int x0 = node_val(d0, d1, a0 < 0 ? 0 : a0), y0 = node_val(a0, a1, a0 < 0 ? 0 : a0);
+    const int x1 = node_val(d0, d1, a1 < 0 ? 0 : a1), y1 = node_val(a0, a1, a1 < 0 ? 0 : a1);
+    if (a0 >= 0) { d0 += x0; a0 = y0; }
+    if (a1 >= 0) { d1 += x1; a1 = y1; }
+  }
+  if (n0 < N) { spar[n0] = p0; sdep[n0] = d0; }
+  if (n1 < N) { spar[n1] = p1; sdep[n1] = d1; }
+  const bool shallow = max_depth <= 0 || ((n0 >= N || d0 <= max_depth) && (n1 >= N || d1 <= max_depth));
+  if (!__all_sync(FULL, shallow)) return 2;
+  // walk positions, level starts (lane l: depths l + 1 and l + 33) and which
+  // nodes have children, in one pass over the nodes
+  int pos0 = 0, pos1 = 0, lv0 = 0, lv1 = 0;
+  bool ch0 = false, ch1 = false;
+  for (int m = 0; m < N; ++m) {
+    const int dm = node_val(d0, d1, m), pm = node_val(p0, p1, m);
+    pos0 += (dm < d0 || (dm == d0 && m < n0)) ? 1 : 0;
+    pos1 += (dm < d1 || (dm == d1 && m < n1)) ? 1 : 0;
+    lv0 += dm < lane + 1 ? 1 : 0;
+    lv1 += dm < lane + 33 ? 1 : 0;
+    ch0 = ch0 || pm == n0;
+    ch1 = ch1 || pm == n1;
+  }
+  if (n0 < N) sord[pos0] = n0;
+  if (n1 < N) sord[pos1] = n1;
+  if (lane + 1 <= N) slev[lane + 1] = lv0;
+  if (lane + 33 <= N) slev[lane + 33] = lv1;
+  if (lane == 0) slev[N + 1] = N;  // past the deepest level
+  // stash slots: rank among the nodes of the same depth that have children
+  int r0 = 0, r1 = 0;
+  const int c0 = ch0 ? 1 : 0, c1 = ch1 ? 1 : 0;
+  for (int m = 0; m < N; ++m) {
+    const int dm = node_val(d0, d1, m), cm = node_val(c0, c1, m);
+    r0 += (cm != 0 && dm == d0 && m < n0) ? 1 : 0;
+    r1 += (cm != 0 && dm == d1 && m < n1) ? 1 : 0;
+  }
+  if (n0 < N) sslot[n0] = ch0 && r0 < kTreeSlots ? r0 : -1;
+  if (n1 < N) sslot[n1] = ch1 && r1 < kTreeSlots ? r1 : -1;
+  return 0;
 }
 
 template <int DK, int WC, int TW, bool PREP>
@@ -563,7 +634,7 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
   int* sdep = reinterpret_cast<int*>(smem + pl.dep);
   int* sord = reinterpret_cast<int*>(smem + pl.ord);
   int* slev = reinterpret_cast<int*>(smem + pl.lev);
-  int* spos = reinterpret_cast<int*>(smem + pl.pos);
+  int* sslot = reinterpret_cast<int*>(smem + pl.slot);
   float* sinvq = reinterpret_cast<float*>(smem + pl.inv);
   float* sinvk = sinvq + round16(N * 4) / 4;
   float* stash = reinterpret_cast<float*>(smem + pl.stash);
@@ -577,7 +648,7 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
   const int row0 = rl * R;
   const int64_t node0 = (int64_t)b * N;
 
-  // ---- stage q, k, v, gates, parents
+  // ---- stage q, k, v, gates
   {
     const char* qb = static_cast<const char*>(p.q) + ((node0 * p.Hk + hk) * DK) * esz;
     const char* kb = static_cast<const char*>(p.k) + ((node0 * p.Hk + hk) * DK) * esz;
@@ -588,7 +659,6 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
     for (int n = tid; n < N; n += NT) {
       cp_async4(sa + n, p.alpha + (node0 + n) * p.Hv + h);
       cp_async4(sb + n, p.beta + (node0 + n) * p.Hv + h);
-      cp_async4(spar + n, p.parent + node0 + n);
     }
   }
   const int sl = p.slot != nullptr ? __ldg(p.slot + b) : b;
@@ -610,60 +680,29 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
     }
   }
   int held = w == 0 ? -1 : -2;  // node whose state this warp holds (-1: the cache)
+  // the tree's shape, by the last warp while the copies are in flight; its
+  // verdict (0 ok, 1 malformed parent array, 2 deeper than the caller's cap)
+  // in lev[0], which the walk does not use
+  if (w == TW - 1) {
+    const int shape = tree_shape(p.parent + node0, N, p.max_depth, spar, sdep, sord, slev, sslot);
+    if (lane == 0) slev[0] = shape;
+  }
   cp_async_wait_all();
   __syncthreads();
+  const int bad = slev[0];
 
+  if (bad != 0) {
+    if (lead && tid == 0) report(p.status, GDN_ERR_BAD_TREE);
+    if (bad == 2 && lead && p.depth_out != nullptr)  // skipped; depths reported
+      for (int n = tid; n < N; n += NT) p.depth_out[(int64_t)b * N + n] = sdep[n];
+    return;
+  }
   if constexpr (PREP) {
     prep_rows<DK>(sq, N, bf16, sinvq, tid, NT);
     prep_rows<DK>(sk, N, bf16, sinvk, tid, NT);
     prep_gates(sa, sb, N, tid, NT);
+    __syncthreads();
   }
-  // parent[0] == -1, 0 <= parent[n] < n; the block leaves otherwise
-  {
-    bool ok = true;
-    for (int n = tid; n < N; n += NT) {
-      const int pp = spar[n];
-      ok = ok && (n == 0 ? pp == -1 : (pp >= 0 && pp < n));
-    }
-    if (!block_all<TW>(ok)) {
-      if (lead && tid == 0) report(p.status, GDN_ERR_BAD_TREE);
-      return;
-    }
-  }
-  // depths, then the order of the walk: by depth, then by index
-  bool shallow = true;
-  for (int n = tid; n < N; n += NT) {
-    int d = 1;
-    for (int m = n; m > 0; m = spar[m]) ++d;
-    sdep[n] = d;
-    shallow = shallow && (p.max_depth <= 0 || d <= p.max_depth);
-  }
-  if (!block_all<TW>(shallow)) {  // deeper than the caller's cap: skipped, depths reported
-    if (lead && tid == 0) report(p.status, GDN_ERR_BAD_TREE);
-    if (lead && p.depth_out != nullptr)
-      for (int n = tid; n < N; n += NT) p.depth_out[(int64_t)b * N + n] = sdep[n];
-    return;
-  }
-  for (int n = tid; n < N; n += NT) {
-    const int dn = sdep[n];
-    int pos = 0;
-    for (int m = 0; m < N; ++m) {
-      const int dm = sdep[m];
-      pos += (dm < dn || (dm == dn && m < n)) ? 1 : 0;
-    }
-    sord[pos] = n;
-  }
-  for (int L = tid; L < N + 2; L += NT) {
-    int c = 0;
-    for (int m = 0; m < N; ++m) c += sdep[m] < L ? 1 : 0;
-    slev[L] = c;
-  }
-  __syncthreads();
-  for (int i = tid; i < N; i += NT) {
-    const int n = sord[i];
-    spos[n] = i - slev[sdep[n]];
-  }
-  __syncthreads();
   // a stash slot holds each lane's R x 4 block lane-major: row m of lane l at
   // float offset (m*32 + l)*4, so every slot access is bank-conflict free
   constexpr int kSlot = DK * WC;
@@ -682,9 +721,9 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
     for (int i = slev[L] + w; i < slev[L + 1]; i += TW) {
       const int n = sord[i], par = spar[n];
       if (par != held) {
-        const int ppos = par < 0 ? kTreeSlots : spos[par];
-        if (ppos < kTreeSlots) {
-          const float* rs = stash + (((L - 1) & 1) * kTreeSlots + ppos) * kSlot + lane * 4;
+        const int pslot = par < 0 ? -1 : sslot[par];
+        if (pslot >= 0) {
+          const float* rs = stash + (((L - 1) & 1) * kTreeSlots + pslot) * kSlot + lane * 4;
 #pragma unroll
           for (int m = 0; m < R; ++m) {
             const float4 t = *reinterpret_cast<const float4*>(rs + m * 128);
@@ -746,9 +785,9 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
 #pragma unroll
       for (int m = 0; m < R; ++m)
         st_f4(dst + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
-      const int mypos = i - slev[L];
-      if (mypos < kTreeSlots) {
-        float* to = stash + ((L & 1) * kTreeSlots + mypos) * kSlot + lane * 4;
+      const int myslot = sslot[n];
+      if (myslot >= 0) {
+        float* to = stash + ((L & 1) * kTreeSlots + myslot) * kSlot + lane * 4;
 #pragma unroll
         for (int m = 0; m < R; ++m)
           *reinterpret_cast<float4*>(to + m * 128) =
