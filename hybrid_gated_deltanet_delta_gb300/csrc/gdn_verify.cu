@@ -608,8 +608,9 @@ __device__ int tree_shape(const int32_t* parent, int N, int max_depth, int* spar
   return 0;
 }
 
-template <int DK, int WC, int TW, bool PREP>
-__global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
+// Three blocks per SM keep a single-wave launch of 384 slab blocks resident.
+template <int DK, int WC, int TW, bool PREP, bool SNAP16>
+__global__ void __launch_bounds__(32 * TW, 3) tree_kernel(const VerifyParams p) {
   using S = Shape<DK, WC, 1>;
   constexpr int R = S::R;
   constexpr int NT = 32 * TW;
@@ -708,7 +709,9 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
   constexpr int kSlot = DK * WC;
 
   const int64_t node_stride = (int64_t)p.Hv * DK * dv;
-  float* snap_h = p.snap + ((int64_t)b * N * p.Hv + h) * DK * dv + (int64_t)row0 * dv + j0 + cg * 4;
+  const int64_t lane_off = ((int64_t)b * N * p.Hv + h) * DK * dv + (int64_t)row0 * dv + j0 + cg * 4;
+  float* snap_h = SNAP16 ? nullptr : p.snap + lane_off;
+  __half* snap16_h = SNAP16 ? p.snap16 + lane_off : nullptr;
   float* o_h = p.o + ((int64_t)b * N * p.Hv + h) * dv + j0 + cg * 4;
 
   // A warp's pending output: the output sums of the last node it formed are
@@ -729,6 +732,15 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
             const float4 t = *reinterpret_cast<const float4*>(rs + m * 128);
             H[m][0] = make_float2(t.x, t.y);
             H[m][1] = make_float2(t.z, t.w);
+          }
+        } else if (SNAP16 && par >= 0) {
+          // binary16 snapshots: the parent continues from its rounded state
+          const __half* from = snap16_h + (int64_t)par * node_stride;
+#pragma unroll
+          for (int m = 0; m < R; ++m) {
+            const uint2 t = __ldcg(reinterpret_cast<const uint2*>(from + (int64_t)m * dv));
+            H[m][0] = __half22float2(*reinterpret_cast<const __half2*>(&t.x));
+            H[m][1] = __half22float2(*reinterpret_cast<const __half2*>(&t.y));
           }
         } else {
           const float* from = par < 0 ? cache_h : snap_h + (int64_t)par * node_stride;
@@ -781,10 +793,23 @@ __global__ void __launch_bounds__(32 * TW) tree_kernel(const VerifyParams p) {
         o01 = __ffma2_rn(H[m][0], f2(qr[m]), o01);
         o23 = __ffma2_rn(H[m][1], f2(qr[m]), o23);
       }
-      float* dst = snap_h + (int64_t)n * node_stride;
+      if constexpr (SNAP16) {
+        // binary16, round to nearest even: 8 bytes per lane and row
+        __half* dst = snap16_h + (int64_t)n * node_stride;
 #pragma unroll
-      for (int m = 0; m < R; ++m)
-        st_f4(dst + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
+        for (int m = 0; m < R; ++m) {
+          const __half2 lo = __floats2half2_rn(H[m][0].x, H[m][0].y);
+          const __half2 hi = __floats2half2_rn(H[m][1].x, H[m][1].y);
+          *reinterpret_cast<uint2*>(dst + (int64_t)m * dv) =
+              make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                         *reinterpret_cast<const uint32_t*>(&hi));
+        }
+      } else {
+        float* dst = snap_h + (int64_t)n * node_stride;
+#pragma unroll
+        for (int m = 0; m < R; ++m)
+          st_f4(dst + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
+      }
       const int myslot = sslot[n];
       if (myslot >= 0) {
         float* to = stash + ((L & 1) * kTreeSlots + myslot) * kSlot + lane * 4;
@@ -1062,12 +1087,12 @@ int launch(const VerifyParams& p, int B, cudaStream_t stream) {
 // a 22-node draft tree: 4 warps 20.7 us, 8 warps 33.5 us per launch).
 constexpr int kTreeWarps = 4;
 
-template <int DK, int WC, int TW, bool PREP>
+template <int DK, int WC, int TW, bool PREP, bool SNAP16>
 int launch_tree(const VerifyParams& p, int B, cudaStream_t stream) {
   const TreePlan pl = tree_plan(p.N, DK, WC, p.bf16 ? 2 : 4);
   const size_t smem = (size_t)pl.total;
   if (smem > 227 * 1024) return GDN_ERR_UNSUPPORTED;
-  auto kern = tree_kernel<DK, WC, TW, PREP>;
+  auto kern = tree_kernel<DK, WC, TW, PREP, SNAP16>;
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -1077,10 +1102,10 @@ int launch_tree(const VerifyParams& p, int B, cudaStream_t stream) {
   return launch_pdl(kern, grid, dim3(32 * TW), smem, stream, p);
 }
 
-template <bool PREP>
+template <bool PREP, bool SNAP16>
 int dispatch_tree(const VerifyParams& p, int B, int dk, int wc, cudaStream_t s) {
 #define GDN_CASE(DK_, WC_) \
-  if (dk == DK_ && wc == WC_) return launch_tree<DK_, WC_, kTreeWarps, PREP>(p, B, s);
+  if (dk == DK_ && wc == WC_) return launch_tree<DK_, WC_, kTreeWarps, PREP, SNAP16>(p, B, s);
   GDN_CASE(128, 16)
   GDN_CASE(128, 8)
   GDN_CASE(64, 16)
@@ -1144,13 +1169,16 @@ int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
   p.snap16 = static_cast<__half*>(snap16);
   p.hint = (int64_t)(p.dv / wc) * a->Hv * a->B <= kHintBlocks;
   p.max_depth = parent != nullptr ? a->max_depth : 0;
-  // a tree whose snapshots are binary16 or not kept at all cannot re-read its
-  // parents from them: it is solved per block instead (gdn_solve.cu)
-  if (parent != nullptr && (snap16 != nullptr || a->snapshots == nullptr))
+  // a tree that keeps no snapshots cannot re-read a parent's state from
+  // them: it is solved per block instead (gdn_solve.cu)
+  if (parent != nullptr && (a->snapshots == nullptr && snap16 == nullptr))
     return launch_verify_tree_solve(a, parent, depth_out, wc, stream, snap16, prep);
+  if (parent != nullptr && snap16 != nullptr)
+    return prep ? launch_verify_tree_solve(a, parent, depth_out, wc, stream, snap16, prep)
+                : dispatch_tree<false, true>(p, a->B, a->dk, wc, stream);
   if (parent != nullptr)  // row warps do not apply: a tree block's warps take whole nodes
-    return prep ? dispatch_tree<true>(p, a->B, a->dk, wc, stream)
-                : dispatch_tree<false>(p, a->B, a->dk, wc, stream);
+    return prep ? dispatch_tree<true, false>(p, a->B, a->dk, wc, stream)
+                : dispatch_tree<false, false>(p, a->B, a->dk, wc, stream);
   if (snap16 != nullptr) {
     if (prep) return GDN_ERR_UNSUPPORTED;
     return dispatch<true, false>(p, a->B, a->dk, wc, nw, stream);

@@ -213,9 +213,17 @@ int gdn_replay_accepted_prep(const gdn_verify_args* args, const int32_t* parent,
  * gdn_verify_chain / gdn_verify_tree, except that every node's state is
  * written to `snapshots_f16` [B][N][Hv][dk][dv] as IEEE binary16, rounded to
  * nearest even from the fp32 state the kernel forms (args->snapshots is not
- * used).  The recurrence itself and the outputs o are unchanged: the kernel
- * never reads a persisted state back, so no node continues from a rounded
- * one; only the persisted copies are rounded.
+ * used).
+ *   chain: the recurrence and the outputs o are unchanged; only the
+ *          persisted copies are rounded.
+ *   tree:  the tree is walked depth level by depth level (the warps of a
+ *          block take a level's nodes round robin, in index order).  A node
+ *          continues from its parent's exact fp32 state when the warp that
+ *          formed the parent takes the node next, or when the parent is one
+ *          of the first three nodes of its depth (in index order) that have
+ *          children (those stay in shared memory); otherwise it continues
+ *          from the parent's binary16 snapshot, as an f16 intermediate cache
+ *          does.  The root starts from the fp32 cache.
  */
 int gdn_verify_chain_f16(const gdn_verify_args* args, void* snapshots_f16, void* stream);
 int gdn_verify_tree_f16(const gdn_verify_args* args, const int32_t* parent, int32_t* depth_out,

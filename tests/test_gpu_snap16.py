@@ -1,4 +1,4 @@
-"""16-bit persisted states on the GPU (gdn_verify_chain_f16,
+"""16-bit persisted states on the GPU (gdn_verify_chain_f16, gdn_verify_tree_f16,
 gdn_commit_accepted_f16) against the fp32 path and the oracle, through the C
 ABI.  The bar for a binary16 snapshot is the float bar plus its own rounding:
 |gpu - oracle| <= 2e-3 * rms(oracle) + 2^-11 * |oracle| element by element
@@ -127,13 +127,76 @@ def _run_tree16(gdn, inp, tile=0, row_warps=0, max_depth=0):
     return int(st.item()), snap16, o, depth
 
 
+TREE_WARPS = 4      # warps of a tree block
+STASH_SLOTS = 3      # stashed states per depth level
+
+
+def rounded_edges(parent):
+    """For each node, whether the level-by-level tree walk continues it from
+    its parent's binary16 snapshot (True) rather than from the parent's exact
+    fp32 state.  The walk keeps a parent exact when the warp that formed it
+    takes the child next (its registers), or when the parent is one of the
+    first STASH_SLOTS nodes of its depth that have children (the shared-memory
+    stash); the root starts from the fp32 cache.  The warps of a block take
+    the nodes of each depth level round robin, in index order."""
+    N = len(parent)
+    depth = [0] * N
+    for n in range(N):
+        depth[n] = 1 if parent[n] < 0 else depth[parent[n]] + 1
+    has_child = [False] * N
+    for n in range(1, N):
+        has_child[parent[n]] = True
+    stashed = [False] * N
+    for n in range(N):
+        rank = sum(1 for m in range(n) if has_child[m] and depth[m] == depth[n])
+        stashed[n] = has_child[n] and rank < STASH_SLOTS
+    order = sorted(range(N), key=lambda n: (depth[n], n))
+    held = [-1] + [-2] * (TREE_WARPS - 1)     # warp 0 starts with the cached state
+    rounded = [False] * N
+    for d in range(1, max(depth) + 1):
+        level = [n for n in order if depth[n] == d]
+        for i, n in enumerate(level):
+            w = i % TREE_WARPS
+            p = parent[n]
+            rounded[n] = p >= 0 and held[w] != p and not stashed[p]
+            held[w] = n
+    return rounded
+
+
+def rounded_walk_reference(inp, b):
+    """The oracle stepped node by node over sequence b's tree, each node
+    continuing from its parent's oracle state, rounded to binary16 (nearest
+    even) exactly where rounded_edges() says the walk re-reads it.
+    Returns (snap [N][Hv][dk][dv], o [N][Hv][dv]) in float64."""
+    N, Hk, Hv, dk, dv = inp["N"], inp["Hk"], inp["Hv"], inp["dk"], inp["dv"]
+    parent = [int(x) for x in inp["parent"][b]]
+    rnd = rounded_edges(parent)
+    snaps = np.zeros((N, Hv, dk, dv))
+    outs = np.zeros((N, Hv, dv))
+    cache0 = inp["cache"][inp["slot"][b]].astype(np.float64)
+    for n in range(N):
+        p = parent[n]
+        src = cache0 if p < 0 else snaps[p]
+        if rnd[n]:
+            src = src.astype(np.float16).astype(np.float64)
+        sl = (slice(b, b + 1), slice(n, n + 1))
+        st, snap, o = oracle.verify(inp["q_f64"][sl], inp["k_f64"][sl], inp["v_f64"][sl],
+                                    inp["alpha"][sl], inp["beta"][sl], src[None],
+                                    np.zeros(1, np.int32), None, B=1, N=1, Hk=Hk, Hv=Hv, dk=dk,
+                                    dv=dv)
+        assert st == oracle.OK
+        snaps[n], outs[n] = snap[0, 0], o[0, 0]
+    return snaps, outs
+
+
 @pytest.mark.parametrize("tile", [(0, 0), (16, 1), (8, 1)])
 def test_tree22_f16_snapshots(gpu_lib, tile):
-    """The DDTree block with binary16 snapshots: every node's persisted state
-    within the binary16 bar of the oracle (no node continues from a rounded
-    state: the kernel never reads a persisted state back), outputs within the
-    float bar, depths exact."""
+    """The DDTree block with binary16 snapshots: every parent of the test tree
+    is kept exact (registers or the stash), so every persisted state is within
+    the binary16 bar of the plain oracle and the outputs within the float
+    bar; depths exact."""
     inp = synthetic.tree22()
+    assert not any(rounded_edges([int(x) for x in inp["parent"][0]]))
     st, snap16, o, depth = _run_tree16(gpu_lib, inp, *tile)
     assert st == 0
     ost, osnap, oo = oracle.verify_inputs(inp)
@@ -143,9 +206,29 @@ def test_tree22_f16_snapshots(gpu_lib, tile):
     assert np.array_equal(depth.cpu().numpy(), oracle.tree_depth(inp["parent"])[1])
 
 
+def test_rounded_walk_reference_is_the_oracle_on_exact_trees():
+    """Pin of the reference used below: with no rounded edge (a path, whose
+    every parent is stashed) stepping the oracle node by node equals the
+    oracle's own tree run."""
+    inp = synthetic.make_verify_inputs(B=1, N=12, Hk=1, Hv=2, dk=16, dv=16, dtype="bf16",
+                                       alpha_kind="near_one", state_sigma=0.05, seed=9250,
+                                       tree=True)
+    inp = dict(inp, parent=np.arange(-1, 11, dtype=np.int32)[None])
+    assert not any(rounded_edges(list(range(-1, 11))))
+    snaps, outs = rounded_walk_reference(inp, 0)
+    st, osnap, oo = oracle.verify_inputs(inp)
+    assert st == oracle.OK
+    assert np.allclose(snaps, osnap[0], rtol=1e-12, atol=1e-14)
+    assert np.allclose(outs, oo[0], rtol=1e-12, atol=1e-14)
+
+
 @pytest.mark.parametrize("shape", ["star", "path", "broom", "random"])
 def test_tree64_f16_snapshots(gpu_lib, shape):
-    """64-node trees of several shapes, three sequences, binary16 snapshots."""
+    """64-node trees of several shapes, three sequences, binary16 snapshots.
+    A node whose parent is neither in a warp's registers nor stashed continues
+    from the parent's binary16 snapshot, as an f16 intermediate cache does:
+    compared with the oracle stepped over the same tree with the same
+    roundings (snapshots at the binary16 bar, outputs at the float bar)."""
     B, N = 3, 64
     inp = synthetic.make_verify_inputs(B=B, N=N, Hk=2, Hv=4, dk=128, dv=32, dtype="bf16",
                                        alpha_kind="near_one", state_sigma=0.05,
@@ -159,10 +242,14 @@ def test_tree64_f16_snapshots(gpu_lib, shape):
         inp = dict(inp, parent=np.tile(p, (B, 1)))
     st, snap16, o, depth = _run_tree16(gpu_lib, inp)
     assert st == 0
-    ost, osnap, oo = oracle.verify_inputs(inp)
-    assert ost == oracle.OK
-    assert_close(o.cpu().numpy(), oo, f"{shape} o")
-    assert_close16(snap16.cpu().numpy(), osnap, f"{shape} binary16 snapshots")
+    s16, og = snap16.cpu().numpy(), o.cpu().numpy()
+    for b in range(B):
+        rsnap, ro = rounded_walk_reference(inp, b)
+        assert_close(og[b], ro, f"{shape} o, sequence {b}")
+        assert_close16(s16[b], rsnap, f"{shape} binary16 snapshots, sequence {b}")
+    if shape == "random":
+        assert any(any(rounded_edges([int(x) for x in inp["parent"][b]])) for b in range(B)), \
+            "the random trees must exercise the rounded re-read"
     assert np.array_equal(depth.cpu().numpy(), oracle.tree_depth(inp["parent"])[1])
 
 
