@@ -17,11 +17,10 @@ bool verify_tile_supported(int dk, int wc, int nw);
 int launch_verify(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, int wc,
                   int nw, cudaStream_t stream, void* snap16 = nullptr, bool prep = false);
 
-// Tree verify by one solve per block (gdn_solve.cu): the binary16-snapshot
-// and snapshot-free trees (a->snapshots may be NULL), which never read a
-// persisted state back.
+// Tree verify without snapshots by one solve per block (gdn_solve.cu): the
+// outputs (and depths) only, for a block committed by replay.
 int launch_verify_tree_solve(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out,
-                             int wc, cudaStream_t stream, void* snap16, bool prep);
+                             int wc, cudaStream_t stream, bool prep);
 
 // Replay of the accepted path from the cached state, written back in place.
 int launch_replay(const gdn_verify_args* a, const int32_t* parent, const int32_t* accept, int wc,

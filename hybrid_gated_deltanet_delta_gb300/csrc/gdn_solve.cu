@@ -1,12 +1,12 @@
-// Tree verification by one solve per block, then a stream of states: the
+// Tree verification without persisted states, by one solve per block: the
 // gated delta rule over a draft tree verified under its ancestor mask ("Qwen3.6
-// 27B: From 20 t/s to 184 t/s", DFlash section, steps 3-4), for the cases the
-// level-by-level tree walk in gdn_verify.cu cannot serve because it reads
-// parent states back from the persisted snapshots: binary16 snapshots ("We got
-// 207 tok/s with Qwen3.5-27B on an RTX 3090", list "Key wins": an f16
-// intermediate cache "at the same tree budget") and trees verified without
-// snapshots, committed by replay ("Photon 2.6", section "Handling recurrent
-// state").  This kernel never reads a persisted state back.
+// 27B: From 20 t/s to 184 t/s", DFlash section, steps 3-4) for a block that
+// keeps no snapshots and is committed by replay ("Photon 2.6", section
+// "Handling recurrent state").  The level-by-level tree walk in gdn_verify.cu
+// continues a node from its parent's snapshot when the parent is neither in a
+// warp's registers nor in its shared-memory stash; without snapshots there is
+// nothing to continue from, so this kernel forms every node's delta and output
+// from the cached state directly and writes only the outputs.
 //
 // Recurrence
 // ----------
@@ -36,35 +36,24 @@
 // of T needs only the rows of the node's ancestors, so it is formed depth
 // level by depth level.  The decay products come from the log decay along
 // the path, r(n, m) = e^(L_n - L_m) with L_n the sum of log alpha over
-// path(n).  A block is verified in three phases:
+// path(n).  A block is verified in two phases:
 //   1. while the cached state's slab loads: K K^T and Q K^T on tensor cores
 //      (mma.sync; exact for bf16 inputs), r, A and P under the ancestor mask,
-//      T by depth levels, P T, and the depth-first order of the tree;
+//      T by depth levels and P T;
 //   2. once it has landed: K H0 and Q H0 on tensor cores (the fp32 state
 //      split into bf16 hi + lo) with X formed in the epilogue, then Delta and
 //      the outputs in one pass, every entry on its own (a sum over the node's
-//      path);
-//   3. only when states are persisted: the states, in registers, in
-//      depth-first order: H_n = alpha_n H_parent + k_n delta_n^T when the
-//      parent's state is the one just formed, otherwise g_n H0 plus the
-//      path's terms; each state leaves as 16-byte vector stores (fp32) or
-//      8-byte stores (binary16) while the next is formed.
+//      path).
 //
 // Work decomposition
 // ------------------
 // A thread block of four warps owns a slab of WC columns of one (sequence,
-// value head): grid = (dv / WC, Hv, B).  Phases 1 and 2 spread over all
-// threads.  In phase 3, lane = cg + CG*rl of row warp wi keeps R consecutive
-// rows (row0 = wi*DK/NW + rl*R) x 4 columns (cg) of the state as float2
-// pairs.
+// value head): grid = (dv / WC, Hv, B); both phases spread over all threads.
 //
-// Variants (template flags): SNAP16 persists binary16 snapshots (rounded to
-// nearest even from the fp32 states); PREP takes raw q/k projections and gate
+// Variants (template flags): PREP takes raw q/k projections and gate
 // pre-activations (1/|q|, 1/|k| scale the products, alpha = 1/(1 + e^a),
 // beta = sigmoid(b)); SPLIT takes fp32 q/k/v, whose tensor-core operands are
 // split into bf16 hi + lo.
-#include <cuda_fp16.h>
-
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
 #include "gdn_tc.cuh"
@@ -75,38 +64,26 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int NT = 32 * kWarps;
 
-// Phase 3 lane layout: NW row warps (at most the block's four).
-template <int DK, int WC>
-struct Shape {
-  static constexpr int CG = WC / 4;                     // 16-byte column groups per slab row
-  static constexpr int RL = 32 / CG;                    // row lanes per warp
-  static constexpr int NW = DK / RL < kWarps ? DK / RL : kWarps;
-  static constexpr int R = DK / (RL * NW);              // rows per lane
-  static_assert(WC % 4 == 0 && 32 % CG == 0 && RL >= 2, "slab width");
-  static_assert(NW >= 1 && R >= 1 && R * RL * NW == DK, "row split");
-};
-
 __host__ __device__ constexpr int round16(int x) { return (x + 15) & ~15; }
 
 // Shared-memory plan in bytes (every array on a 16-byte boundary).  NP = N
 // rounded up to the 16 rows of a tensor-core tile.
 //   ks, qs   [NP][lds]  bf16  k and q rows (with SPLIT a lo plane follows)
-//   kf       [N][DK]    fp32  k rows for phase 3 (scaled by 1/|k| for PREP);
-//                             with SPLIT the fp32 k rows are staged here, and
-//                             the fp32 q rows over kk.. (dead until K K^T)
+//   kf       [N][DK]    fp32  SPLIT only: the fp32 k rows as staged (the fp32
+//                             q rows are staged over kk.., dead until K K^T)
 //   h0       [DK][ldh]  fp32  the cached state's slab
 //   v        [N][WC]    input the v slab
 //   a, b, la [N]        fp32  alpha, beta, log alpha
 //   g, L     [N]        fp32  g_n = e^(L_n), L_n = log decay along path(n)
 //   iq, ik   [NP]       fp32  1/|q_n|, 1/|k_n| (PREP; zero past N)
-//   par, dep, ord [N]   int   parent, depth (root = 1), depth-first order
+//   par, dep [N]        int   parent, depth (root = 1)
 //   anc      [N]        u64   strict ancestors as a bit set
 //   kk       [NP][ldm]  fp32  K K^T -> A -> P T
 //   qk       [NP][ldm]  fp32  Q K^T -> P
 //   rr, tt   [NP][ldm]  fp32  r(n, m); T = (I + A)^-1
 //   x, qh, d [NP][WC]   fp32  X, Q H0, Delta
 struct Plan {
-  int ks, qs, kf, h0, v, a, b, la, g, L, iq, ik, par, dep, ord, anc, kk, qk, rr, tt, x, qh, d;
+  int ks, qs, kf, h0, v, a, b, la, g, L, iq, ik, par, dep, anc, kk, qk, rr, tt, x, qh, d;
   int total, NP, lds, ldh, ldm;
 };
 
@@ -121,7 +98,7 @@ __host__ __device__ inline Plan make_plan(int N, int DK, int WC, bool split) {
   int o = 0;
   s.ks = o; o += round16(planes * s.NP * s.lds * 2);
   s.qs = o; o += round16(planes * s.NP * s.lds * 2);
-  s.kf = o; o += round16(N * DK * 4);
+  s.kf = o; o += split ? round16(N * DK * 4) : 0;
   s.h0 = o; o += round16(DK * s.ldh * 4);
   s.v = o; o += round16(N * WC * esz);
   s.a = o; o += round16(N * 4);
@@ -133,7 +110,6 @@ __host__ __device__ inline Plan make_plan(int N, int DK, int WC, bool split) {
   s.ik = o; o += round16(s.NP * 4);
   s.par = o; o += round16(N * 4);
   s.dep = o; o += round16(N * 4);
-  s.ord = o; o += round16(N * 4);
   s.anc = o; o += round16(N * 8);
   const int mat = round16(s.NP * s.ldm * 4);
   s.kk = o; o += mat;
@@ -157,8 +133,6 @@ struct VerifyParams {
   const float* beta;
   const float* cache;
   const int32_t* slot;
-  float* snap;
-  __half* snap16;  // binary16 snapshots instead of snap
   float* o;
   int32_t* status;
   const int32_t* parent;
@@ -223,8 +197,6 @@ __device__ __forceinline__ void stage_rows(char* dst, int dst_stride, const char
     cp_async16(dst + r * dst_stride + c * 16, src + r * src_stride + c * 16);
   }
 }
-
-__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
 __device__ __forceinline__ uint32_t lds32(const uint16_t* p) {
   return *reinterpret_cast<const uint32_t*>(p);
@@ -311,19 +283,17 @@ __device__ __forceinline__ void tile_mma(const uint16_t* A, int lda, int plane, 
 
 // Phase 1 for N nodes whose k and q rows, gates and parents are staged: the
 // working forms of the inputs, the tree's depths, ancestor sets and log decay,
-// K K^T and Q K^T, r, A and P, then T = (I + A)^-1 by depth levels and P T;
-// with `order`, the k rows in fp32 and the depth-first order for phase 3.
+// K K^T and Q K^T, r, A and P, then T = (I + A)^-1 by depth levels and P T.
 // Returns 0, or 1 if the parent array is malformed, 2 if the tree is deeper
 // than max_depth (depths filled in); every thread returns the same value.
 template <int DK, bool SPLIT, bool PREP>
-__device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth, bool order) {
+__device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth) {
   const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
   const int g8 = lane >> 2, t4 = lane & 3;
   uint16_t* ks = reinterpret_cast<uint16_t*>(smem + pl.ks);
   uint16_t* qs = reinterpret_cast<uint16_t*>(smem + pl.qs);
-  float* kf = reinterpret_cast<float*>(smem + pl.kf);
   // fp32 inputs (SPLIT): k staged in kf, q over the matrices
-  const float* rawk = kf;
+  const float* rawk = reinterpret_cast<const float*>(smem + pl.kf);
   const float* rawq = reinterpret_cast<const float*>(smem + pl.kk);
   float* sa = reinterpret_cast<float*>(smem + pl.a);
   float* sb = reinterpret_cast<float*>(smem + pl.b);
@@ -334,7 +304,6 @@ __device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth, b
   float* sik = reinterpret_cast<float*>(smem + pl.ik);
   const int* spar = reinterpret_cast<const int*>(smem + pl.par);
   int* sdep = reinterpret_cast<int*>(smem + pl.dep);
-  int* sord = reinterpret_cast<int*>(smem + pl.ord);
   uint64_t* sanc = reinterpret_cast<uint64_t*>(smem + pl.anc);
   float* kk = reinterpret_cast<float*>(smem + pl.kk);
   float* qk = reinterpret_cast<float*>(smem + pl.qk);
@@ -439,9 +408,7 @@ __device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth, b
 
   // ---- r(n, m) = e^(L_n - L_m) on n's path (1 at m = n), A = beta r (K K^T)
   //      for the strict ancestors, P = r (Q K^T) on the path; entries off the
-  //      path are never read.  With `order`: the k rows in fp32 (normalised
-  //      for PREP) and every node's subtree size (into the d slab, free
-  //      until phase 2).
+  //      path are never read.
   for (int idx = tid; idx < N * NP; idx += NT) {
     const int n = idx / NP, m = idx - n * NP;
     if (m > n || (m < n && ((sanc[n] >> m) & 1ull) == 0)) continue;
@@ -450,56 +417,12 @@ __device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth, b
     if (m < n) kk[n * ldm + m] = sb[n] * r * kk[n * ldm + m];
     qk[n * ldm + m] = r * qk[n * ldm + m];
   }
-  int* ssz = reinterpret_cast<int*>(smem + pl.d);
-  if (order) {
-    for (int i = tid; i < N * DK / 8; i += NT) {
-      const int e = 8 * i, n = e / DK, c = e - n * DK;
-      float x[8];
-      if constexpr (SPLIT) {
-        const float4 u0 = *reinterpret_cast<const float4*>(rawk + e);
-        const float4 u1 = *reinterpret_cast<const float4*>(rawk + e + 4);
-        x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
-        x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
-      } else {
-        const uint4 w = *reinterpret_cast<const uint4*>(ks + n * lds + c);
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          x[2 * j] = __uint_as_float(ww[j] << 16);
-          x[2 * j + 1] = __uint_as_float(ww[j] & 0xffff0000u);
-        }
-      }
-      const float sc = PREP ? sik[n] : 1.f;
-      *reinterpret_cast<float4*>(kf + e) = make_float4(sc * x[0], sc * x[1], sc * x[2], sc * x[3]);
-      *reinterpret_cast<float4*>(kf + e + 4) =
-          make_float4(sc * x[4], sc * x[5], sc * x[6], sc * x[7]);
-    }
-    for (int n = tid; n < N; n += NT) {
-      int sz = 1;
-      for (int m = n + 1; m < N; ++m) sz += (int)((sanc[m] >> n) & 1ull);
-      ssz[n] = sz;
-    }
-  }
   __syncthreads();
 
   // ---- T = (I + A)^-1, depth level by depth level:
   //      T[n][m] = [n = m] - sum over the strict ancestors s >= m of n of
   //      A[n][s] T[s][m], zero unless m is on n's path.  The level's barrier
-  //      also tells whether any node was that deep.  With `order`, the
-  //      depth-first position of each node (after its parent and the earlier
-  //      siblings' subtrees, children in index order) meanwhile.
-  if (order) {
-    for (int n = tid; n < N; n += NT) {
-      int pre = 0;
-      for (int a = n; a > 0; a = spar[a]) {
-        const int pa = spar[a];
-        pre += 1;
-        for (int s2 = pa + 1; s2 < a; ++s2)
-          if (spar[s2] == pa) pre += ssz[s2];
-      }
-      sord[pre] = n;
-    }
-  }
+  //      also tells whether any node was that deep.
   for (int d = 1;; ++d) {
     bool any = false;
     for (int idx = tid; idx < N * N; idx += NT) {
@@ -623,65 +546,6 @@ __device__ void solve_finish(const Plan& pl, char* smem, int N, float* o_out, in
   }
 }
 
-// ---------------------------------------------------------------- phase 3
-// x[0..R) = R consecutive fp32 values of a k row.
-template <int R>
-__device__ __forceinline__ void load_k(float (&x)[R], const float* row) {
-  if constexpr (R % 4 == 0) {
-#pragma unroll
-    for (int m = 0; m < R; m += 4) {
-      const float4 t = *reinterpret_cast<const float4*>(row + m);
-      x[m] = t.x; x[m + 1] = t.y; x[m + 2] = t.z; x[m + 3] = t.w;
-    }
-  } else {
-#pragma unroll
-    for (int m = 0; m < R; ++m) x[m] = row[m];
-  }
-}
-
-// H <- alpha H + k delta^T on this lane's R x 4 block.
-template <int R>
-__device__ __forceinline__ void rank1_step(float2 (&H)[R][2], const float (&k)[R], float4 dl,
-                                           float al) {
-  const float2 d01 = make_float2(dl.x, dl.y), d23 = make_float2(dl.z, dl.w), al2 = f2(al);
-#pragma unroll
-  for (int m = 0; m < R; ++m) {
-    H[m][0] = __ffma2_rn(f2(k[m]), d01, __fmul2_rn(al2, H[m][0]));
-    H[m][1] = __ffma2_rn(f2(k[m]), d23, __fmul2_rn(al2, H[m][1]));
-  }
-}
-
-// H <- H + k (s delta)^T.
-template <int R>
-__device__ __forceinline__ void rank1_add(float2 (&H)[R][2], const float (&k)[R], float4 dl,
-                                          float s) {
-  const float2 d01 = make_float2(s * dl.x, s * dl.y), d23 = make_float2(s * dl.z, s * dl.w);
-#pragma unroll
-  for (int m = 0; m < R; ++m) {
-    H[m][0] = __ffma2_rn(f2(k[m]), d01, H[m][0]);
-    H[m][1] = __ffma2_rn(f2(k[m]), d23, H[m][1]);
-  }
-}
-
-template <int R>
-__device__ __forceinline__ void store_state(float* dst, int64_t dv, const float2 (&H)[R][2]) {
-#pragma unroll
-  for (int m = 0; m < R; ++m)
-    st_f4(dst + (int64_t)m * dv, H[m][0].x, H[m][0].y, H[m][1].x, H[m][1].y);
-}
-
-// binary16, round to nearest even: 8 bytes per lane and row
-template <int R>
-__device__ __forceinline__ void store_state16(__half* dst, int64_t dv, const float2 (&H)[R][2]) {
-#pragma unroll
-  for (int m = 0; m < R; ++m) {
-    const __half2 lo = __floats2half2_rn(H[m][0].x, H[m][0].y);
-    const __half2 hi = __floats2half2_rn(H[m][1].x, H[m][1].y);
-    *reinterpret_cast<uint2*>(dst + (int64_t)m * dv) =
-        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
-  }
-}
-
 // Zero the padding rows N .. NP-1 of the bf16 k and q tiles.
 __device__ __forceinline__ void zero_padding(const Plan& pl, char* smem, int N, bool split, int t) {
   uint16_t* ks = reinterpret_cast<uint16_t*>(smem + pl.ks);
@@ -696,11 +560,9 @@ __device__ __forceinline__ void zero_padding(const Plan& pl, char* smem, int N, 
 }
 
 // ---------------------------------------------------------------- verify
-template <int DK, int WC, bool SNAP16, bool PREP, bool SPLIT>
+template <int DK, int WC, bool PREP, bool SPLIT>
 __global__ void __launch_bounds__(NT) tree_solve_kernel(const VerifyParams p) {
-  using S = Shape<DK, WC>;
-  constexpr int R = S::R;
-  const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
+  const int tid = threadIdx.x;
   const int j0 = blockIdx.x * WC, h = blockIdx.y, b = blockIdx.z;
   const int hk = h / (p.Hv / p.Hk);
   if (p.hint) prefetch_block<DK>(p, b, h, hk, j0, WC, tid);
@@ -709,7 +571,6 @@ __global__ void __launch_bounds__(NT) tree_solve_kernel(const VerifyParams p) {
   const int N = p.N, dv = p.dv;
   const Plan pl = make_plan(N, DK, WC, SPLIT);
   const bool lead = blockIdx.x == 0 && blockIdx.y == 0;  // per-sequence reporting
-  const bool persist = SNAP16 || p.snap != nullptr;
   const int64_t node0 = (int64_t)b * N;
   constexpr int esz = SPLIT ? 4 : 2;
   int* spar = reinterpret_cast<int*>(smem + pl.par);
@@ -754,7 +615,7 @@ __global__ void __launch_bounds__(NT) tree_solve_kernel(const VerifyParams p) {
   cp_async_wait<1>();
   __syncthreads();
 
-  const int bad = solve_prepare<DK, SPLIT, PREP>(pl, smem, N, p.max_depth, persist);
+  const int bad = solve_prepare<DK, SPLIT, PREP>(pl, smem, N, p.max_depth);
   if (bad != 0) {  // a malformed tree, or one deeper than the cap (depths reported)
     cp_async_wait<0>();
     if (lead && tid == 0) report(p.status, GDN_ERR_BAD_TREE);
@@ -768,71 +629,16 @@ __global__ void __launch_bounds__(NT) tree_solve_kernel(const VerifyParams p) {
                                     (int64_t)p.Hv * dv);
   if (lead && p.depth_out != nullptr)
     for (int n = tid; n < N; n += NT) p.depth_out[node0 + n] = sdep[n];
-  if (!persist) return;  // verified for a replay commit: outputs only
-  __syncthreads();
-
-  // ---- phase 3: the states in registers, stored as they are formed
-  if (wi >= S::NW) return;
-  const int cg = lane % S::CG, rl = lane / S::CG;
-  const int row0 = wi * (DK / S::NW) + rl * R;
-  const float* h0 = reinterpret_cast<const float*>(smem + pl.h0);
-  const float* kf = reinterpret_cast<const float*>(smem + pl.kf);
-  const float* sd = reinterpret_cast<const float*>(smem + pl.d);
-  const float* sa = reinterpret_cast<const float*>(smem + pl.a);
-  const float* sg = reinterpret_cast<const float*>(smem + pl.g);
-  const float* rr = reinterpret_cast<const float*>(smem + pl.rr);
-  const uint64_t* sanc = reinterpret_cast<const uint64_t*>(smem + pl.anc);
-  const int* sord = reinterpret_cast<const int*>(smem + pl.ord);
-  float2 H[R][2];
-  float2 Hc[R][2];  // the cached state
-#pragma unroll
-  for (int m = 0; m < R; ++m) {
-    const float4 t = *reinterpret_cast<const float4*>(h0 + (row0 + m) * pl.ldh + cg * 4);
-    H[m][0] = Hc[m][0] = make_float2(t.x, t.y);
-    H[m][1] = Hc[m][1] = make_float2(t.z, t.w);
-  }
-  const int64_t node_stride = (int64_t)p.Hv * DK * dv;
-  const int64_t lane_off =
-      ((int64_t)b * N * p.Hv + h) * DK * dv + (int64_t)row0 * dv + j0 + cg * 4;
-  float* snap_l = SNAP16 ? nullptr : p.snap + lane_off;
-  __half* snap16_l = SNAP16 ? p.snap16 + lane_off : nullptr;
-  int held = -1;  // the node whose state H holds (-1: the cached state)
-  for (int i = 0; i < N; ++i) {
-    const int n = sord[i];
-    float kr[R];
-    if (spar[n] == held) {
-      load_k<R>(kr, kf + n * DK + row0);
-      rank1_step<R>(H, kr, *reinterpret_cast<const float4*>(sd + n * WC + cg * 4), sa[n]);
-    } else {
-      // H_n = g_n H0 + sum over the path of r(n, m) k_m delta_m^T, root first
-      const float2 gn = f2(sg[n]);
-#pragma unroll
-      for (int m = 0; m < R; ++m) {
-        H[m][0] = __fmul2_rn(gn, Hc[m][0]);
-        H[m][1] = __fmul2_rn(gn, Hc[m][1]);
-      }
-      uint64_t path = sanc[n] | (1ull << n);
-      while (path != 0) {
-        const int m = pop_low(path);
-        load_k<R>(kr, kf + m * DK + row0);
-        rank1_add<R>(H, kr, *reinterpret_cast<const float4*>(sd + m * WC + cg * 4),
-                     rr[n * pl.ldm + m]);
-      }
-    }
-    held = n;
-    if constexpr (SNAP16) store_state16<R>(snap16_l + (int64_t)n * node_stride, dv, H);
-    else store_state<R>(snap_l + (int64_t)n * node_stride, dv, H);
-  }
 }
 
-template <int DK, int WC, bool SNAP16, bool PREP>
+template <int DK, int WC, bool PREP>
 int launch_solve_t(const VerifyParams& p, int B, cudaStream_t stream) {
   const dim3 grid(p.dv / WC, p.Hv, B);
   const bool split = !p.bf16;
   const size_t smem = (size_t)make_plan(p.N, DK, WC, split).total;
   if (smem > 227 * 1024) return GDN_ERR_UNSUPPORTED;
-  auto kern = split ? tree_solve_kernel<DK, WC, SNAP16, PREP, true>
-                    : tree_solve_kernel<DK, WC, SNAP16, PREP, false>;
+  auto kern = split ? tree_solve_kernel<DK, WC, PREP, true>
+                    : tree_solve_kernel<DK, WC, PREP, false>;
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -841,10 +647,10 @@ int launch_solve_t(const VerifyParams& p, int B, cudaStream_t stream) {
   return launch_pdl(kern, grid, dim3(NT), smem, stream, p);
 }
 
-template <bool SNAP16, bool PREP>
+template <bool PREP>
 int dispatch_solve(const VerifyParams& p, int B, int dk, int wc, cudaStream_t s) {
 #define GDN_CASE(DK_, WC_) \
-  if (dk == DK_ && wc == WC_) return launch_solve_t<DK_, WC_, SNAP16, PREP>(p, B, s);
+  if (dk == DK_ && wc == WC_) return launch_solve_t<DK_, WC_, PREP>(p, B, s);
   GDN_CASE(128, 16)
   GDN_CASE(128, 8)
   GDN_CASE(64, 16)
@@ -860,7 +666,7 @@ int dispatch_solve(const VerifyParams& p, int B, int dk, int wc, cudaStream_t s)
 }  // namespace
 
 int launch_verify_tree_solve(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out,
-                             int wc, cudaStream_t stream, void* snap16, bool prep) {
+                             int wc, cudaStream_t stream, bool prep) {
   VerifyParams p{};
   p.q = a->q;
   p.k = a->k;
@@ -869,7 +675,6 @@ int launch_verify_tree_solve(const gdn_verify_args* a, const int32_t* parent, in
   p.beta = a->beta;
   p.cache = a->state_cache;
   p.slot = a->slot;
-  p.snap = snap16 != nullptr ? nullptr : a->snapshots;
   p.o = a->o;
   p.status = a->status;
   p.parent = parent;
@@ -881,15 +686,10 @@ int launch_verify_tree_solve(const gdn_verify_args* a, const int32_t* parent, in
   p.Hv = a->Hv;
   p.dv = a->dv;
   p.bf16 = a->in_dtype == GDN_BF16;
-  p.snap16 = static_cast<__half*>(snap16);
   p.hint = (int64_t)(p.dv / wc) * a->Hv * a->B <= kHintBlocks;
   p.max_depth = a->max_depth;
-  const int B = a->B, dk = a->dk;
-  if (snap16 != nullptr)
-    return prep ? dispatch_solve<true, true>(p, B, dk, wc, stream)
-                : dispatch_solve<true, false>(p, B, dk, wc, stream);
-  return prep ? dispatch_solve<false, true>(p, B, dk, wc, stream)
-              : dispatch_solve<false, false>(p, B, dk, wc, stream);
+  return prep ? dispatch_solve<true>(p, a->B, a->dk, wc, stream)
+              : dispatch_solve<false>(p, a->B, a->dk, wc, stream);
 }
 
 }  // namespace gdn
