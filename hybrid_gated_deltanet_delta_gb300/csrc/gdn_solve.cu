@@ -77,13 +77,15 @@ __host__ __device__ constexpr int round16(int x) { return (x + 15) & ~15; }
 //   g, L     [N]        fp32  g_n = e^(L_n), L_n = log decay along path(n)
 //   iq, ik   [NP]       fp32  1/|q_n|, 1/|k_n| (PREP; zero past N)
 //   par, dep [N]        int   parent, depth (root = 1)
+//   ord      [N]        int   the nodes by depth, then index
+//   lev      [N + 2]    int   lev[L] = first position of depth L in ord
 //   anc      [N]        u64   strict ancestors as a bit set
 //   kk       [NP][ldm]  fp32  K K^T -> A -> P T
 //   qk       [NP][ldm]  fp32  Q K^T -> P
 //   rr, tt   [NP][ldm]  fp32  r(n, m); T = (I + A)^-1
 //   x, qh, d [NP][WC]   fp32  X, Q H0, Delta
 struct Plan {
-  int ks, qs, kf, h0, v, a, b, la, g, L, iq, ik, par, dep, anc, kk, qk, rr, tt, x, qh, d;
+  int ks, qs, kf, h0, v, a, b, la, g, L, iq, ik, par, dep, ord, lev, anc, kk, qk, rr, tt, x, qh, d;
   int total, NP, lds, ldh, ldm;
 };
 
@@ -110,6 +112,8 @@ __host__ __device__ inline Plan make_plan(int N, int DK, int WC, bool split) {
   s.ik = o; o += round16(s.NP * 4);
   s.par = o; o += round16(N * 4);
   s.dep = o; o += round16(N * 4);
+  s.ord = o; o += round16(N * 4);
+  s.lev = o; o += round16((N + 2) * 4);
   s.anc = o; o += round16(N * 8);
   const int mat = round16(s.NP * s.ldm * 4);
   s.kk = o; o += mat;
@@ -305,6 +309,8 @@ __device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth) {
   const int* spar = reinterpret_cast<const int*>(smem + pl.par);
   int* sdep = reinterpret_cast<int*>(smem + pl.dep);
   uint64_t* sanc = reinterpret_cast<uint64_t*>(smem + pl.anc);
+  int* sord = reinterpret_cast<int*>(smem + pl.ord);
+  int* slev = reinterpret_cast<int*>(smem + pl.lev);
   float* kk = reinterpret_cast<float*>(smem + pl.kk);
   float* qk = reinterpret_cast<float*>(smem + pl.qk);
   float* rr = reinterpret_cast<float*>(smem + pl.rr);
@@ -407,54 +413,79 @@ __device__ int solve_prepare(const Plan& pl, char* smem, int N, int max_depth) {
   if (__syncthreads_and(shallow) == 0) return 2;
 
   // ---- r(n, m) = e^(L_n - L_m) on n's path (1 at m = n), A = beta r (K K^T)
-  //      for the strict ancestors, P = r (Q K^T) on the path; entries off the
-  //      path are never read.
-  for (int idx = tid; idx < N * NP; idx += NT) {
-    const int n = idx / NP, m = idx - n * NP;
-    if (m > n || (m < n && ((sanc[n] >> m) & 1ull) == 0)) continue;
-    const float r = m == n ? 1.f : expf(sL[n] - sL[m]);
-    rr[n * ldm + m] = r;
-    if (m < n) kk[n * ldm + m] = sb[n] * r * kk[n * ldm + m];
-    qk[n * ldm + m] = r * qk[n * ldm + m];
+  //      for the strict ancestors, P = r (Q K^T) on the path (entries off the
+  //      path are never read): one warp per node, lanes over m (N <= 64).
+  //      Meanwhile the walk order (by depth, then index) and the level starts.
+  for (int n = wi; n < N; n += kWarps) {
+    const uint64_t path = sanc[n] | (1ull << n);
+    const float Ln = sL[n], bn = sb[n];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int m = lane + 32 * h;
+      if (m >= N || ((path >> m) & 1ull) == 0) continue;
+      const float r = m == n ? 1.f : expf(Ln - sL[m]);
+      rr[n * ldm + m] = r;
+      if (m < n) kk[n * ldm + m] = bn * r * kk[n * ldm + m];
+      qk[n * ldm + m] = r * qk[n * ldm + m];
+    }
+  }
+  for (int n = tid; n < N; n += NT) {
+    const int dn = sdep[n];
+    int pos = 0;
+    for (int m = 0; m < N; ++m) {
+      const int dm = sdep[m];
+      pos += (dm < dn || (dm == dn && m < n)) ? 1 : 0;
+    }
+    sord[pos] = n;
+  }
+  for (int L = tid; L < N + 2; L += NT) {
+    int c = 0;
+    for (int m = 0; m < N; ++m) c += sdep[m] < L ? 1 : 0;
+    slev[L] = c;
   }
   __syncthreads();
 
-  // ---- T = (I + A)^-1, depth level by depth level:
+  // ---- T = (I + A)^-1, depth level by depth level, one warp per node of the
+  //      level and lanes over m:
   //      T[n][m] = [n = m] - sum over the strict ancestors s >= m of n of
-  //      A[n][s] T[s][m], zero unless m is on n's path.  The level's barrier
-  //      also tells whether any node was that deep.
-  for (int d = 1;; ++d) {
-    bool any = false;
-    for (int idx = tid; idx < N * N; idx += NT) {
-      const int n = idx / N, m = idx - n * N;
-      if (sdep[n] != d) continue;
-      any = true;
+  //      A[n][s] T[s][m], zero unless m is on n's path (then m is on the path
+  //      of every such s, whose row an earlier level formed)
+  for (int L = 1; L <= N && slev[L] < N; ++L) {
+    for (int i = slev[L] + wi; i < slev[L + 1]; i += kWarps) {
+      const int n = sord[i];
       const uint64_t anc = sanc[n];
-      if (m > n || (m < n && ((anc >> m) & 1ull) == 0)) continue;
-      float t = m == n ? 1.f : 0.f;
-      uint64_t s_set = anc & ~((1ull << m) - 1ull);  // strict ancestors s >= m
-      while (s_set != 0) {
-        const int s = pop_low(s_set);
-        t = fmaf(-kk[n * ldm + s], tt[s * ldm + m], t);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int m = lane + 32 * h;
+        if (m > n || (m < n && ((anc >> m) & 1ull) == 0)) continue;
+        float t = m == n ? 1.f : 0.f;
+        uint64_t s_set = anc & ~((1ull << m) - 1ull);  // strict ancestors s >= m
+        while (s_set != 0) {
+          const int s2 = pop_low(s_set);
+          t = fmaf(-kk[n * ldm + s2], tt[s2 * ldm + m], t);
+        }
+        tt[n * ldm + m] = t;
       }
-      tt[n * ldm + m] = t;
     }
-    if (__syncthreads_or(any) == 0) break;
+    __syncthreads();
   }
 
-  // ---- P T over A (A is dead): (P T)[n][m] = sum over s on n's path with m
-  //      on s's path of P[n][s] T[s][m]
-  for (int idx = tid; idx < N * N; idx += NT) {
-    const int n = idx / N, m = idx - n * N;
+  // ---- P T over A (A is dead), one warp per node, lanes over m:
+  //      (P T)[n][m] = sum over the path nodes s >= m of P[n][s] T[s][m]
+  for (int n = wi; n < N; n += kWarps) {
     const uint64_t path = sanc[n] | (1ull << n);
-    if (((path >> m) & 1ull) == 0) continue;
-    float acc = 0.f;
-    uint64_t s_set = path & ~((1ull << m) - 1ull);
-    while (s_set != 0) {
-      const int s = pop_low(s_set);
-      if (((sanc[s] | (1ull << s)) >> m) & 1ull) acc = fmaf(qk[n * ldm + s], tt[s * ldm + m], acc);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int m = lane + 32 * h;
+      if (m >= N || ((path >> m) & 1ull) == 0) continue;
+      float acc = 0.f;
+      uint64_t s_set = path & ~((1ull << m) - 1ull);
+      while (s_set != 0) {
+        const int s2 = pop_low(s_set);
+        acc = fmaf(qk[n * ldm + s2], tt[s2 * ldm + m], acc);
+      }
+      kk[n * ldm + m] = acc;
     }
-    kk[n * ldm + m] = acc;
   }
   return 0;
 }
