@@ -38,13 +38,14 @@
 // loads.  Snapshots leave as 16-byte stores; a warp-wide store covers RL rows
 // x WC*4 contiguous bytes.
 //
-// Variants (template flags): SNAP16 persists binary16 snapshots (chains; a
-// tree with binary16 snapshots, or with none, is verified by the per-block
-// solve in gdn_solve.cu, which never reads a persisted state back);
-// PREP takes raw q/k projections and gate pre-activations (the per-node
-// inverse norms scale the reduced sums and delta instead of every element);
-// a chain may persist nothing at all and commit by replay, for which
-// replay_kernel below re-runs the accepted path from the cached state.
+// Variants (template flags): SNAP16 persists binary16 snapshots (RNE from
+// the fp32 state; in a tree, a parent that is neither in the warp's registers
+// nor stashed is continued from its binary16 snapshot); PREP takes raw q/k
+// projections and gate pre-activations (the per-node inverse norms scale the
+// reduced sums and delta instead of every element).  A chain may persist
+// nothing at all and commit by replay, for which replay_kernel below re-runs
+// the accepted path from the cached state; a tree that persists nothing is
+// verified by the per-block solve in gdn_solve.cu.
 #include <cuda_fp16.h>
 
 #include "gdn_common.cuh"
