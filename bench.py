@@ -1067,6 +1067,7 @@ def measure_prefill(ctx, wl_name="prefill8192"):
     flops = prefill_flops(T, Hk, Hv, dk, dv)
     launch_ms = call_stats["p50"]
     gbs = pbytes / (launch_ms / 1e3) / 1e9
+    ptraffic = profiled_traffic("prefill", wl_name)
     out = {
         "metric": METRIC,
         "value": world * T * Hv * K / (total_ms / 1e3),
@@ -1081,10 +1082,12 @@ def measure_prefill(ctx, wl_name="prefill8192"):
                              "on the launch stream",
                    "hbm_achieved_gbs": gbs, "hbm_frac_of_measured": gbs / hbm,
                    "algorithmic_bytes_per_call": pbytes,
+                   "dram_traffic_over_algorithmic_bytes": (ptraffic / pbytes
+                                                           if ptraffic is not None else None),
                    "workspace_bytes": wbytes},
         "kernel_ms": call_stats,
         "roofline": roofline_entry("tensor", "gdn_prefill_chunked (prep + scan)", flops,
-                                   launch_ms, bf16, kind, profiled_traffic("prefill", wl_name),
+                                   launch_ms, bf16, kind, ptraffic,
                                    "algorithmic_flops_per_launch"),
         "e2e": {"value": world * T * Hv * e2e_steps / e2e_s, "unit": "token-heads/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
