@@ -589,6 +589,74 @@ class Context:
         return [self.torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
 
+TREE_WARPS = 4      # warps of a tree verify block
+TREE_STASH_SLOTS = 3
+
+
+def tree_walk_stats(parent):
+    """Rounds and parent reads of the level-by-level tree walk for one tree:
+    the warps of a block take each depth level's nodes round robin (index
+    order); a node finds its parent in its warp's registers (the warp formed
+    it last), in the shared-memory stash (the first TREE_STASH_SLOTS nodes
+    of a level that have children), or reads it back through L2."""
+    N = len(parent)
+    depth = [0] * N
+    for n in range(N):
+        depth[n] = 1 if parent[n] < 0 else depth[parent[n]] + 1
+    has_child = [False] * N
+    for n in range(1, N):
+        has_child[parent[n]] = True
+    stashed = [has_child[n] and sum(1 for m in range(n) if has_child[m] and depth[m] == depth[n])
+               < TREE_STASH_SLOTS for n in range(N)]
+    held = [-1] + [-2] * (TREE_WARPS - 1)
+    rounds = l2 = 0
+    for d in range(1, max(depth) + 1):
+        level = [n for n in range(N) if depth[n] == d]
+        rounds += (len(level) + TREE_WARPS - 1) // TREE_WARPS
+        for i, n in enumerate(level):
+            w = i % TREE_WARPS
+            if parent[n] >= 0 and held[w] != parent[n] and not stashed[parent[n]]:
+                l2 += 1
+            held[w] = n
+    return {"depth": max(depth), "rounds": rounds, "parents_read_from_l2": l2}
+
+
+def tree_shape_sweep(ctx, n_trees=16, copies=4, launches=100):
+    """The tree22 verify on other seeded 22-node trees (same generator, same
+    head shapes): per-launch time back to back over rotating copies larger
+    than L2, with each tree's walk statistics."""
+    torch, gdn, stream = ctx.torch, ctx.gdn, ctx.stream
+    base = synthetic.workload_seed("tree22")
+    rows = []
+    for t in range(1, n_trees + 1):
+        inp = synthetic.tree22(seed=base + 0x1000 + t)
+        cases = [VerifyCase(inp, torch) for _ in range(copies)]
+        calls = [gdn.bind_verify_tree(c.dev["q"], c.dev["k"], c.dev["v"], c.dev["alpha"],
+                                      c.dev["beta"], c.cache, c.snap, c.o, c.parent,
+                                      slot=c.slot, n_slots=inp["n_slots"], stream=stream)
+                 for c in cases]
+        for i in range(20):
+            calls[i % copies]()
+        torch.cuda.synchronize()
+        hold_device(torch, 20e-6, launches)
+        e = ctx.events(2)
+        e[0].record(stream)
+        for i in range(launches):
+            calls[i % copies]()
+        e[1].record(stream)
+        torch.cuda.synchronize()
+        row = tree_walk_stats([int(x) for x in inp["parent"][0]])
+        row["verify_us"] = e[0].elapsed_time(e[1]) / launches * 1e3
+        rows.append(row)
+        del cases, calls
+    us = sorted(r["verify_us"] for r in rows)
+    return {"trees": n_trees, "verify_us_min": us[0], "verify_us_p50": us[len(us) // 2],
+            "verify_us_max": us[-1], "per_tree": rows,
+            "how": f"tree22's generator with {n_trees} other seeds; per tree {launches} "
+                   f"back-to-back verify launches over {copies} rotating copies, one event "
+                   "pair; rounds and parent reads through L2 of the level walk"}
+
+
 def measure_verify(ctx, wl_name):
     torch, gdn, args, stream, flush = ctx.torch, ctx.gdn, ctx.args, ctx.stream, ctx.flush
     world = ctx.world
@@ -932,6 +1000,8 @@ def measure_verify(ctx, wl_name):
         "gpu_launches": launches_per_step * K,
         "clocks": ctx.sampler.summary(t0, t1),
     }
+    if wl_name == "tree22" and world == 1:
+        out["shape_sweep"] = tree_shape_sweep(ctx)
     if not (index or replay):
         # the copy commit's own kernel (replay and index commits are other work)
         cbytes = commit_bytes(B, Hv, dk, dv, len(layers), snap_bytes=2 if snap16 else 4)

@@ -89,3 +89,25 @@ def test_reference_arm_prints_one_line():
     assert d["impl"] == "reference" and d["unit"] == "node-heads/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_tree_walk_stats():
+    """Rounds and L2 parent reads of the level walk reported by the tree22
+    shape sweep: the test tree takes 8 rounds with every parent on chip; a
+    star takes 1 + ceil(21 / 4) rounds; a level with four parents that have
+    children puts the fourth one's children on L2 unless a warp still holds
+    it."""
+    import bench
+    import synthetic
+
+    st = bench.tree_walk_stats([int(x) for x in synthetic.tree22()["parent"][0]])
+    assert st == {"depth": 6, "rounds": 8, "parents_read_from_l2": 0}
+    star = [-1] + [0] * 21
+    assert bench.tree_walk_stats(star) == {"depth": 2, "rounds": 7, "parents_read_from_l2": 0}
+    # level 2 holds nodes 1..5, each with one child (nodes 6..10); nodes 1-3
+    # are stashed, 4 and 5 are not.  Round robin: level 2 puts nodes 1..5 on
+    # warps 0, 1, 2, 3, 0 and level 3 nodes 6..10 on the same warps, so node 9
+    # finds its parent 4 in warp 3's registers, but warp 0 has formed node 6
+    # since node 5: node 10 reads node 5 back through L2
+    wide = [-1, 0, 0, 0, 0, 0, 1, 2, 3, 4, 5]
+    assert bench.tree_walk_stats(wide) == {"depth": 3, "rounds": 5, "parents_read_from_l2": 1}
