@@ -161,7 +161,11 @@ int gdn_verify_chain(const gdn_verify_args* args, void* stream);
  * receives each node's depth, root = 1.  A sequence whose parent array breaks
  * the rule, or whose tree is deeper than args->max_depth (when not 0), is
  * skipped and GDN_ERR_BAD_TREE is written to args->status (its depth_out row
- * is still written when the parent array itself is valid).
+ * is still written when the parent array itself is valid).  With
+ * args->snapshots == NULL (a block committed by gdn_replay_accepted) the
+ * block is verified by one lower-triangular solve per slab instead of the
+ * node-by-node walk, and only o (and depth_out) is written; the outputs agree
+ * with the walk's up to floating-point rounding.
  */
 int gdn_verify_tree(const gdn_verify_args* args, const int32_t* parent, int32_t* depth_out,
                     void* stream);
