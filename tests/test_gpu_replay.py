@@ -185,6 +185,56 @@ def test_rounds_of_verify_and_replay_equal_sequential(gpu_lib):
     assert_close(cache_t.cpu().numpy()[0], sT, "rounds of verify + replay")
 
 
+def test_rounds_of_tree_verify_and_replay_equal_sequential(gpu_lib):
+    """DDTree blocks verified without snapshots (the per-block solve), each
+    committed by replaying the accepted node's ancestor path from the cache:
+    every round's outputs match the oracle's verify of that block from the
+    oracle's own running state, and after five rounds the cached state equals
+    one token-by-token run over the accepted paths."""
+    t = torch()
+    Hk, Hv, dk, dv, N = 2, 6, 128, 64, 22
+    start = None
+    cache_t = None
+    ocache = None
+    acc_tok = {key: [] for key in ("q_f64", "k_f64", "v_f64", "alpha", "beta")}
+    for r in range(5):
+        inp = synthetic.make_verify_inputs(B=1, N=N, Hk=Hk, Hv=Hv, dk=dk, dv=dv, dtype="bf16",
+                                           alpha_kind="near_one", state_sigma=0.05,
+                                           seed=7600 + r, n_slots=1, slot_perm=False, tree=True)
+        if cache_t is None:
+            cache_t = dev(inp["cache"])
+            start = inp["cache"][0].astype(np.float64)
+            ocache = inp["cache"].astype(np.float64)
+        o, o_back = guarded((1, N, Hv, dv), fill=float("nan"))
+        st_t = t.zeros(1, dtype=t.int32, device="cuda")
+        gpu_lib.gdn_verify_tree(dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha"]),
+                                dev(inp["beta"]), cache_t, None, o, dev(inp["parent"]),
+                                slot=dev(inp["slot"]), n_slots=1, status=st_t)
+        t.cuda.synchronize()
+        assert st_t.item() == 0 and canaries_ok(o_back, o.numel())
+        ost, osnap, oo = oracle.verify(inp["q_f64"], inp["k_f64"], inp["v_f64"], inp["alpha"],
+                                       inp["beta"], ocache, inp["slot"], inp["parent"], B=1, N=N,
+                                       Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+        assert ost == oracle.OK
+        assert_close(o.cpu().numpy(), oo, f"round {r} outputs")
+        acc = int(inp["accept"][0])
+        st, cache_t = _gpu_replay(gpu_lib, inp, np.array([acc], np.int32), True, cache_t=cache_t)
+        assert st == 0
+        ocache = osnap[0, acc][None]
+        path, nd = [], acc
+        while nd >= 0:
+            path.append(nd)
+            nd = int(inp["parent"][0, nd])
+        path.reverse()
+        for key in acc_tok:
+            acc_tok[key].append(inp[key][0, path])
+    cat = [np.concatenate(acc_tok[key]) for key in ("q_f64", "k_f64", "v_f64", "alpha", "beta")]
+    st, sT, _ = oracle.prefill_step(*cat, start, T=cat[0].shape[0], Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+    assert st == oracle.OK
+    t.cuda.synchronize()
+    assert_close(cache_t.cpu().numpy()[0], sT, "rounds of tree verify + replay")
+
+
 @pytest.mark.parametrize("tile", [(0, 0), (16, 1), (8, 1)])
 def test_tree_verify_without_snapshots_then_replay(gpu_lib, tile):
     """A draft tree verified with snapshots=None (nothing persisted) gives the
