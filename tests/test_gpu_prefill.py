@@ -125,3 +125,52 @@ def test_prefill_rejects_short_workspace(gpu_lib):
                                     dev(inp["alpha"]), dev(inp["beta"]), dev(inp["state"]),
                                     t.empty((100, 3, 128), device="cuda"), ws)
     assert e.value.code == gpu_lib.GDN_ERR_WORKSPACE
+
+
+def _slice(inp, a, b):
+    """Tokens a .. b-1 of a prefill input (the state is the caller's)."""
+    out = dict(inp, T=b - a)
+    for key in ("q", "k", "v", "q_f64", "k_f64", "v_f64", "alpha", "beta"):
+        out[key] = np.ascontiguousarray(inp[key][a:b])
+    return out
+
+
+def test_prefill_split_across_calls(gpu_lib):
+    """A sequence prefilled in three calls of ragged lengths (the state passed
+    from call to call through the in/out state buffer) gives the outputs and
+    final state of one step-by-step run over the whole sequence."""
+    inp = synthetic.make_prefill_inputs(T=333, Hk=2, Hv=6, dk=128, dv=128, dtype="bf16",
+                                        alpha_kind="near_one", state_sigma=0.05, seed=4500)
+    Hr, Or = oracle_prefill(inp)
+    state = inp["state"]
+    outs = []
+    for a, b in ((0, 100), (100, 164), (164, 333)):
+        part = dict(_slice(inp, a, b), state=state)
+        state, o = run_prefill(gpu_lib, part)
+        outs.append(o)
+    assert_close(np.concatenate(outs), Or, "split prefill o")
+    assert_close(state, Hr, "split prefill state")
+
+
+def test_prefill_then_chain_verify(gpu_lib):
+    """The serving path: a prompt prefilled, then a 16-position block verified
+    from the prefill's final state, equals one step-by-step run over the prompt
+    and the block (the block's outputs and its last snapshot)."""
+    t = torch()
+    Hk, Hv, dk, dv, T, N = 2, 6, 128, 128, 130, 16
+    inp = synthetic.make_prefill_inputs(T=T + N, Hk=Hk, Hv=Hv, dk=dk, dv=dv, dtype="bf16",
+                                        alpha_kind="near_one", state_sigma=0.05, seed=4600)
+    Hr, Or = oracle_prefill(inp)
+    state, _ = run_prefill(gpu_lib, _slice(inp, 0, T))
+    blk = _slice(inp, T, T + N)
+    cache = dev(state[None].astype(np.float32))
+    snap = t.empty((1, N, Hv, dk, dv), device="cuda")
+    o = t.empty((1, N, Hv, dv), device="cuda")
+    st = t.zeros(1, dtype=t.int32, device="cuda")
+    gpu_lib.gdn_verify_chain(dev(blk["q"][None]), dev(blk["k"][None]), dev(blk["v"][None]),
+                             dev(blk["alpha"][None]), dev(blk["beta"][None]), cache, snap, o,
+                             n_slots=1, status=st)
+    t.cuda.synchronize()
+    assert st.item() == 0
+    assert_close(o.cpu().numpy()[0], Or[T:], "verify after prefill: o")
+    assert_close(snap.cpu().numpy()[0, N - 1], Hr, "verify after prefill: last state")
