@@ -34,23 +34,17 @@ struct Range {
 bool ok_ptr16(const void* p) { return p != nullptr && gdn::aligned16(p); }
 bool ok_ptr4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-// Block count up to which the tree solve's slab is split over two row warps
-// (4 blocks per SM on 152 SMs).
-constexpr int64_t kTwoWarpBlocks = 608;
-
-// Default slab shape for the verify and replay kernels: 16 columns per block.
-// A chain keeps one warp per block: its node loop overlaps each node's update
-// with the shuffle tree of the look-ahead sums, which a cross-warp exchange
-// would interrupt (measured on the 16-node chain: one warp 13.1 us, two row
-// warps 13.4 us per launch).  The per-block tree solve takes two row warps
-// when there are too few blocks to give every SM sub-partition a warp of its
-// own.  A replay takes the chain's shape, so that a chain committed by replay
-// repeats the verify arithmetic bit for bit.
-void auto_tile(int dk, int dv, int B, int Hv, bool tree_solve, int* wc, int* nw) {
+// Default slab shape for the verify and replay kernels: 16 columns per block
+// and one warp per block for a chain: its node loop overlaps each node's
+// update with the shuffle tree of the look-ahead sums, which a cross-warp
+// exchange would interrupt (measured on the 16-node chain: one warp 13.1 us,
+// two row warps 13.4 us per launch).  Tree blocks take whole nodes per warp,
+// so the row-warp count applies to chains and replays only.  A replay takes
+// the chain's shape, so that a chain committed by replay repeats the verify
+// arithmetic bit for bit.
+void auto_tile(int* wc, int* nw) {
   *wc = 16;
   *nw = 1;
-  const int64_t blocks = (int64_t)(dv / 16) * Hv * B;
-  if (tree_solve && (dk == 128 || dk == 64) && blocks <= kTwoWarpBlocks) *nw = 2;
 }
 
 int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* depth_out, bool tree,
@@ -85,8 +79,7 @@ int verify_common(const gdn_verify_args* a, const int32_t* parent, int32_t* dept
     if (!ok_ptr4(p)) return GDN_ERR_MISALIGNED;
 
   int wc = 0, nw = 0;
-  const bool tree_solve = tree && (snap16 != nullptr || a->snapshots == nullptr);
-  auto_tile(a->dk, a->dv, a->B, a->Hv, tree_solve, &wc, &nw);
+  auto_tile(&wc, &nw);
   if (a->tile_cols != 0) wc = a->tile_cols;
   if (a->row_warps != 0) nw = a->row_warps;
   else if (!gdn::verify_tile_supported(a->dk, wc, nw)) nw = 1;  // automatic, for a forced width
@@ -143,7 +136,7 @@ int replay_common(const gdn_verify_args* a, const int32_t* parent, const int32_t
   for (const void* p : need4)
     if (!ok_ptr4(p)) return GDN_ERR_MISALIGNED;
   int wc = 0, nw = 0;
-  auto_tile(a->dk, a->dv, a->B, a->Hv, false, &wc, &nw);
+  auto_tile(&wc, &nw);
   if (a->tile_cols != 0) wc = a->tile_cols;
   if (a->row_warps != 0) nw = a->row_warps;
   else if (!gdn::verify_tile_supported(a->dk, wc, nw)) nw = 1;  // automatic, for a forced width
