@@ -1244,7 +1244,7 @@ def run_reference(args, wl_name, world, rank):
         return None
     smp = OracleSampler(wl_name)
     cores, model = host_cpu()
-    n_heads = 1
+    n_heads = 1 if smp.prefill else 3   # as the cpu_baseline leg samples
     with cf.ThreadPoolExecutor(max_workers=cores) as ex:
         def one_step(i):
             return sum(f.result() for f in [ex.submit(smp.run, (i * cores + j) * n_heads, n_heads)
