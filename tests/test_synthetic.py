@@ -57,3 +57,25 @@ def test_prefill_shapes():
     inp = synthetic.prefill8192(T=100)
     assert inp["q"].shape == (100, 16, 128) and inp["v"].shape == (100, 48, 128)
     assert inp["state"].shape == (48, 128, 128)
+
+
+def test_batched8x22_layers_share_trees_not_inputs():
+    """The batched tree workload: eight 22-node trees drawn once for the batch
+    (the same in every layer, depth within the cap, parents before children),
+    one slot permutation and accepted node per sequence, fresh per-layer
+    q/k/v, gates and states."""
+    l0, l1 = synthetic.batched8x22_layer(0), synthetic.batched8x22_layer(5)
+    for key in ("parent", "slot", "accept"):
+        assert np.array_equal(l0[key], l1[key]), key
+    assert not np.array_equal(l0["k"], l1["k"]) and not np.array_equal(l0["cache"], l1["cache"])
+    par = l0["parent"]
+    assert par.shape == (8, 22) and np.all(par[:, 0] == -1)
+    n = np.arange(1, 22)
+    assert np.all((par[:, 1:] >= 0) & (par[:, 1:] < n))
+    assert sorted(l0["slot"].tolist()) == list(range(8))
+    assert np.all((l0["accept"] >= 0) & (l0["accept"] < 22))
+    for b in range(8):
+        depth = [0] * 22
+        for i in range(22):
+            depth[i] = 1 if par[b, i] < 0 else depth[par[b, i]] + 1
+        assert max(depth) <= 16
