@@ -331,3 +331,48 @@ def test_tree_depth_cap_skips_only_the_deep_tree(gpu_lib):
                 continue
             assert_close(got_snap[b], ref_snap[b], f"cap {cap} sequence {b} snapshots")
             assert_close(got_o[b], ref_o[b], f"cap {cap} sequence {b} o")
+
+
+def test_tree_shape_follows_parents_rewritten_between_launches(gpu_lib):
+    """One parent buffer rewritten on the launch stream before each of eight
+    back-to-back tree verifies, as a drafter that reuses its buffer would (the
+    tree kernel reads the parent array before its programmatic wait to work
+    the shape out early and reads it again after the wait): every launch
+    follows the array as its predecessors on the stream left it, against the
+    oracle, depths exact.  Launches of 48 blocks, so the early analysis runs."""
+    t = torch()
+    B, N, Hk, Hv, dk, dv = 2, 22, 2, 6, 128, 64
+    inp = synthetic.make_verify_inputs(B=B, N=N, Hk=Hk, Hv=Hv, dk=dk, dv=dv, dtype="bf16",
+                                       alpha_kind="near_one", state_sigma=0.05, seed=31337,
+                                       tree=True)
+    rng = np.random.default_rng(31338)
+    n = np.arange(N)
+    trees = [inp["parent"],
+             np.stack([synthetic.random_tree(rng, N) for _ in range(B)]),
+             np.stack([np.where(n == 0, -1, 0)] * B),          # a star
+             np.stack([n - 1] * B)]                              # a path
+    trees = [np.ascontiguousarray(p, dtype=np.int32) for p in trees]
+    q, k, v = dev(inp["q"]), dev(inp["k"]), dev(inp["v"])
+    alpha, beta, cache, slot = dev(inp["alpha"]), dev(inp["beta"]), dev(inp["cache"]), dev(inp["slot"])
+    srcs = [dev(p) for p in trees]
+    parent = t.empty_like(srcs[0])
+    st = t.zeros(1, dtype=t.int32, device="cuda")
+    runs = []
+    for i in (0, 1, 2, 3, 1, 0, 3, 2):
+        parent.copy_(srcs[i])
+        snap = t.empty((B, N, Hv, dk, dv), device="cuda")
+        o = t.empty((B, N, Hv, dv), device="cuda")
+        depth = t.empty((B, N), dtype=t.int32, device="cuda")
+        gpu_lib.gdn_verify_tree(q, k, v, alpha, beta, cache, snap, o, parent, depth_out=depth,
+                                slot=slot, n_slots=inp["n_slots"], status=st)
+        runs.append((i, snap, o, depth))
+    t.cuda.synchronize()
+    assert st.item() == 0
+    refs = {}
+    for i, snap, o, depth in runs:
+        if i not in refs:
+            refs[i] = _oracle(dict(inp, parent=trees[i])), oracle.tree_depth(trees[i])[1]
+        (ref_snap, ref_o), ref_depth = refs[i]
+        assert np.array_equal(depth.cpu().numpy(), ref_depth), f"tree {i}: depths"
+        assert_close(o.cpu().numpy(), ref_o, f"tree {i} o")
+        assert_close(snap.cpu().numpy(), ref_snap, f"tree {i} snapshots")
